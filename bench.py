@@ -1,0 +1,371 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-expert FFN layer on GB300.
+
+Default workload: GPT-OSS-20B-shaped decode with every expert resident --
+24 stacked MoE layers (hidden 2880, expert intermediate 2880, 32 experts,
+top-4), one token per step, 768 distinct MXFP4 experts (10.2 GB) in the GPU
+slot pool.  One step = one token through all 24 layers: routing (top-k,
+softmax, histogram, permutation), the slot lookup, gate/up + SwiGLU, down,
+and the weighted combine.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores on a bounded sample of the same workload instead.
+
+Multi-GPU: the layer does not shard in this form (one token's four experts);
+``--gpus N`` under torchrun runs N independent replicas and reports the sum.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_synth as S  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 roofline"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in [("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")]:
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------
+# oracle leg (CPU baseline / reference arm)
+# --------------------------------------------------------------------------
+
+def _oracle_token_sample(wl, step, layers, weights_cache, threads):
+    """Time the oracle on `layers` of one decode step; returns seconds."""
+    import oracle
+
+    t0 = time.perf_counter()
+    for l in layers:
+        lg = S.logits(wl, l, step)
+        ids, w = oracle.route(lg, wl.top_k)
+        oracle.hist_perm(ids, wl.experts)
+        x = S.activations_bf16_bits(wl, l, step)
+        oracle.layer(x, ids, w, weights_cache[l], prefill=False, threads=threads)
+    return time.perf_counter() - t0
+
+
+def oracle_leg(wl, steps, layers_per_sample, threads):
+    layers = list(range(0, wl.layers, max(1, wl.layers // layers_per_sample)))[:layers_per_sample]
+    cache = {l: S.stack_experts(S.layer_weights(wl, l)) for l in layers}
+    times = [_oracle_token_sample(wl, s, layers, cache, threads) for s in range(steps)]
+    per_token = statistics.median(times) * wl.layers / len(layers)
+    return 1.0 / per_token, layers, times
+
+
+# --------------------------------------------------------------------------
+# GPU leg
+# --------------------------------------------------------------------------
+
+def gpu_leg(args, wl, rank, world):
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L, E, k, H, I = wl.layers, wl.experts, wl.top_k, wl.hidden, wl.inter
+    eb = M.moe_expert_bytes(H, I)
+
+    # pinned host store of all experts (packed once), pool preloaded: resident
+    host = torch.empty(L * E * eb, dtype=torch.uint8).pin_memory()
+    for l in range(L):
+        for e, w in enumerate(S.layer_weights(wl, l)):
+            M.moe_pack_expert(w, H, I, host.data_ptr() + (l * E + e) * eb)
+    slots = torch.empty(L * E * eb, dtype=torch.uint8, device=dev)
+    pool = M.Pool(L, E, E, H, I, host_experts=host, dev_slots=slots, preload=True)
+    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
+
+    G = args.warmup + args.steps
+    step_ids = [(rank * 131 + g) % wl.steps for g in range(G)]
+    lg_h = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, s) for l in range(L)]) for s in step_ids]))
+    x_h = torch.from_numpy(np.stack([np.stack([S.activations_bf16_bits(wl, l, s) for l in range(L)])
+                                     for s in step_ids]).view(np.int16)).view(torch.bfloat16)
+    lg_d = lg_h.to(dev)
+    x_d = x_h.to(dev)
+    out_d = torch.empty((G, L, 1, H), dtype=torch.float32, device=dev)
+    plan = M.RoutePlan.allocate(1, E, k, device=dev)
+    ws = torch.empty(M.moe_ffn_workspace_bytes(1, k, H, I, M.MOE_PATH_DECODE), dtype=torch.uint8, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    ext = dict(enable_timing=True)
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext["external"] = True
+    except TypeError:
+        pass
+    ev = [[(torch.cuda.Event(**ext), torch.cuda.Event(**ext), torch.cuda.Event(**ext)) for _ in range(L)]
+          for _ in range(G)]
+
+    def step(g):
+        for l in range(L):
+            e0, e1, e2 = ev[g][l]
+            e0.record(stream)
+            M.moe_route_plan(lg_d[g, l], k, plan, stream=stream, with_counts_host=False)
+            e1.record(stream)
+            M.moe_expert_ffn(pool, l, x_d[g, l], plan, slot_of, out_d[g, l], ws, path=M.MOE_PATH_DECODE,
+                             stream=stream)
+            e2.record(stream)
+
+    # one CUDA graph per step (each step has its own inputs and events)
+    graphs = []
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        step(0)  # eager once before capture
+    stream.synchronize()
+    for g in range(G):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(g)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+
+    for g in range(args.warmup):
+        graphs[g].replay()
+    torch.cuda.synchronize()
+
+    import torch.distributed as dist
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    clocks = Clocks(torch.cuda.current_device())
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for g in range(args.warmup, G):
+            graphs[g].replay()
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    ffn_ms = [ev[g][l][1].elapsed_time(ev[g][l][2]) for g in range(args.warmup, G) for l in range(L)]
+    route_ms = [ev[g][l][0].elapsed_time(ev[g][l][1]) for g in range(args.warmup, G) for l in range(L)]
+
+    # e2e through the public API, host buffers, copies inside the timed region
+    lg_pin = lg_h.pin_memory()
+    x_pin = x_h.pin_memory()
+    out_pin = torch.empty((G, L, 1, H), dtype=torch.float32).pin_memory()
+    lg_stage = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
+    x_stage = torch.empty((L, 1, H), dtype=torch.bfloat16, device=dev)
+    out_stage = torch.empty((L, 1, H), dtype=torch.float32, device=dev)
+
+    def e2e_step(g):
+        lg_stage.copy_(lg_pin[g], non_blocking=True)
+        x_stage.copy_(x_pin[g], non_blocking=True)
+        for l in range(L):
+            M.moe_route_plan(lg_stage[l], k, plan, stream=stream, with_counts_host=False)
+            M.moe_expert_ffn(pool, l, x_stage[l], plan, slot_of, out_stage[l], ws, path=M.MOE_PATH_DECODE,
+                             stream=stream)
+        out_pin[g].copy_(out_stage, non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for g in range(args.warmup):
+            e2e_step(g)
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for g in range(args.warmup, G):
+            e2e_step(g)
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = a.elapsed_time(b)
+    # the graphed and eager runs produced the same outputs
+    same = bool(torch.equal(out_pin[args.warmup:].to(dev), out_d[args.warmup:]))
+
+    res = dict(elapsed_ms=elapsed_ms, ffn_ms=ffn_ms, route_ms=route_ms, clocks=clk, e2e_ms=e2e_ms,
+               h2d=(lg_pin[0].numel() * 4 + x_pin[0].numel() * 2), d2h=out_pin[0].numel() * 4,
+               e2e_matches_graph=same, expert_bytes=eb)
+    pool.close()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-layers", type=int, default=4, help="layers per oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers (smaller case for profiler captures)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = _dist()
+    wl = S.WORKLOADS[1]
+    if args.layers:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, layers=min(args.layers, wl.layers))
+    hbm_peak, _, peak_kind = _peaks()
+    workload = {"workload": wl.name, "layers": wl.layers, "hidden": wl.hidden, "inter": wl.inter,
+                "experts": wl.experts, "top_k": wl.top_k, "tokens_per_step": 1,
+                "resident_experts": wl.layers * wl.experts,
+                "l2": "inputs larger than L2: each step reads 96 distinct experts (1.27 GB) of a 10.2 GB set",
+                "parallelism": f"replicas{world}"}
+    threads = os.cpu_count() or 1
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+
+        oracle.build()
+        tps, layers, times = oracle_leg(wl, args.warmup + args.steps, args.cpu_layers, threads)
+        timed = times[args.warmup:]
+        per_token = statistics.median(timed) * wl.layers / len(layers)
+        v = 1.0 / per_token
+        sample = f"{len(layers)} of {wl.layers} layers per step (layers {layers}), scaled to {wl.layers} layers"
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_token * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic", "config": workload,
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from routed_expert_ffn_histogram_gb300 import build as B
+
+    B.build()
+    res = gpu_leg(args, wl, rank, world)
+    ms = res["elapsed_ms"] / args.steps
+    e2e_ms = res["e2e_ms"] / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return
+    value = world * 1e3 / ms
+    layer_bytes = wl.top_k * 3 * (wl.hidden * wl.inter // 2 + wl.hidden * wl.inter // 32)
+    ffn_avg_s = statistics.mean(res["ffn_ms"]) / 1e3
+    achieved = layer_bytes / ffn_avg_s / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload,
+            "formats": "weights MXFP4 (E2M1 + E8M0 per 32), activations bf16, fp32 accumulation",
+            "roofline": {"kernel": "decode expert FFN (gate/up+SwiGLU, down+combine) per layer",
+                         "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": layer_bytes,
+                         "avg_launch_us": ffn_avg_s * 1e6},
+            "kernels_us": {"route_plan": statistics.mean(res["route_ms"]) * 1e3,
+                           "expert_ffn": ffn_avg_s * 1e6},
+            "e2e": {"value": world * 1e3 / e2e_ms, "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"], "matches_graph_outputs": res["e2e_matches_graph"]},
+            "gpu_launches": args.steps * wl.layers * 3,
+            "clocks": res["clocks"]}
+    if not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        tps, layers, times = oracle_leg(wl, 1, args.cpu_layers, threads)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"1 decode step, {len(layers)} of {wl.layers} layers "
+                                          f"({layers}), scaled to {wl.layers} layers"}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

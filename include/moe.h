@@ -1,0 +1,289 @@
+/*
+ * moe.h -- C ABI of the routed-expert FFN layer over a fixed GPU expert-slot
+ * pool, for NVIDIA GB300 (sm_103a).
+ *
+ * One routed mixture-of-experts FFN layer: router logits -> top-k and a
+ * softmax over the selected experts -> tokens grouped by expert -> each
+ * selected expert looked up in a (layer, expert) -> slot map, misses copied
+ * from pinned host memory into evicted slots -> per expert gate and up
+ * projections, SwiGLU, down projection on MXFP4 weights used in their native
+ * format -> outputs summed with the routing weights.
+ *
+ * Sources of the operations (page title, section):
+ *   [R1] tinyserve README, "Performance": GPT-OSS-20B, 24 layers x 32
+ *        experts, top_k=4.
+ *   [R2] tinyserve README, "How it works" item 1: expert weights are raw
+ *        quantised bytes in pinned CPU memory, not dequantised at load.
+ *   [R3] tinyserve README, "How it works" item 2: fused dequant+matmul in the
+ *        native quantised format; an expert is gate, up and down.
+ *   [R4] tinyserve README, "How it works" item 3: expert cache keyed by
+ *        (layer, expert_id) with a GPU slot map; "Configuration":
+ *        cache_policy lru.
+ *   [R5] tinyserve README, "How it works" item 6: batched prefill groups
+ *        tokens by expert and loads each unique expert once.
+ *   [P1] llama.cpp discussion "fixed GPU expert working set with Native CPU
+ *        miss execution", main post: a fixed subset of packed experts is
+ *        materialised in a GPU pool; selected IDs are split into resident
+ *        hits and misses; outputs are merged with the routing weights.
+ *   [X1] "Expert Offloading" topic page, replay-semantics study: cache
+ *        events are fused per (layer, step), not replayed per access.
+ *   [MX] OCP Microscaling Formats (MX) v1.0: E2M1 elements with block-32
+ *        E8M0 scales (MXFP4), E4M3 elements (MXFP8).
+ *
+ * Conventions for every call:
+ *   - Return value: MOE_OK or a negative MOE_ERR_* status; nothing aborts.
+ *     Arguments are validated before anything is launched; on
+ *     MOE_ERR_INVALID nothing was enqueued.  On MOE_ERR_CUDA,
+ *     moe_last_cuda_error() gives the CUDA runtime error code.
+ *   - All buffers are owned by the caller.  "device" pointers must be
+ *     device-accessible memory of the current CUDA device; "host" pointers
+ *     are ordinary host memory; "pinned" pointers are page-locked host
+ *     memory (cudaHostAlloc / cudaHostRegister).  The library keeps host
+ *     metadata only and allocates no device memory.
+ *   - moe_stream_t is a cudaStream_t passed as an opaque pointer (NULL is
+ *     the legacy default stream).  Work is enqueued asynchronously; no call
+ *     synchronises the device except the bounded host wait in
+ *     moe_pool_stage.
+ *   - Tensors are dense row-major.  T tokens, E experts, k top_k,
+ *     H hidden size, I expert intermediate size, A = T*k assignments,
+ *     assignment a = t*k + j is the j-th ranked expert of token t.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID (-1)     /* bad argument; nothing enqueued          */
+#define MOE_ERR_CUDA (-2)        /* a CUDA runtime call failed              */
+#define MOE_ERR_CAPACITY (-3)    /* unique routed experts exceed the slots  */
+#define MOE_ERR_TIMEOUT (-4)     /* a bounded host wait ran out             */
+#define MOE_ERR_STATE (-5)       /* object in the wrong state for the call  */
+#define MOE_ERR_UNSUPPORTED (-6) /* shape or device the kernels do not handle */
+
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 32
+
+/* moe_expert_ffn path selection */
+#define MOE_PATH_AUTO 0          /* decode when A <= MOE_DECODE_MAX_ASSIGN   */
+#define MOE_PATH_DECODE 1        /* bf16 activations, CUDA-core GEMV         */
+#define MOE_PATH_PREFILL 2       /* MXFP8 activations, tcgen05 grouped GEMM  */
+#define MOE_DECODE_MAX_ASSIGN 64
+
+typedef void* moe_stream_t;
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Text of a status code (static string, never NULL). */
+MOE_API const char* moe_status_str(int status);
+
+/* CUDA runtime error code of the last MOE_ERR_CUDA on this thread (0 if
+ * none). */
+MOE_API int moe_last_cuda_error(void);
+
+/* Number of CUDA devices the library sees (0 without a GPU); never fails. */
+MOE_API int moe_device_count(void);
+
+/* ------------------------------------------------------------------------ */
+/* Weights [R2][R3][MX]                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes one expert occupies in the GPU-native packed layout (the unit of a
+ * pool slot and of one miss copy).  hidden and inter must be positive
+ * multiples of 64.  Errors: MOE_ERR_INVALID. */
+MOE_API int moe_expert_bytes(int hidden, int inter, size_t* out_bytes);
+
+/* Convert one expert from the canonical MXFP4 layout into the GPU-native
+ * layout, on the host, once, outside any timed region.
+ *   gate_codes, up_codes   host [inter][hidden/2]  E2M1 pairs, element 2i in
+ *                          the low nibble of byte i
+ *   gate_scales, up_scales host [inter][hidden/32] E8M0 bytes, one per block
+ *                          of 32 along hidden
+ *   down_codes             host [hidden][inter/2]
+ *   down_scales            host [hidden][inter/32]
+ *   dst                    host, moe_expert_bytes() bytes, written fully
+ * The native layout keeps each row's codes followed by its scales (padded to
+ * 16 bytes) and interleaves gate and up rows in chunks of 64 so one tile of
+ * the fused gate/up product holds matching gate and up rows.
+ * Errors: MOE_ERR_INVALID. */
+MOE_API int moe_pack_expert(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                    const uint8_t* up_codes, const uint8_t* up_scales,
+                    const uint8_t* down_codes, const uint8_t* down_scales,
+                    int hidden, int inter, void* dst);
+
+/* ------------------------------------------------------------------------ */
+/* Routing and grouping [R1][R5][P1]                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Scratch bytes moe_route_plan needs for T tokens, E experts, top-k. */
+MOE_API int moe_route_workspace_bytes(int T, int E, int k, size_t* out_bytes);
+
+/* Top-k + softmax + per-expert histogram + stable permutation, one call.
+ *   logits      device fp32 [T][E]
+ *   ids         device int32 [T][k]  out: selected experts, larger logit
+ *               first, equal logits by lower id (NaN ranks last)
+ *   w           device fp32 [T][k]   out: softmax over the k selected logits
+ *               (evaluated in fp64, rounded to fp32)
+ *   counts      device int32 [E]     out: assignments per expert
+ *   offsets     device int32 [E+1]   out: exclusive prefix sum of counts
+ *   perm        device int32 [A]     out: assignment indices grouped by
+ *               expert (ascending), ascending a inside a group
+ *   inv         device int32 [A]     out: inv[perm[p]] = p
+ *   counts_host pinned int32 [E] or NULL: when given, counts are copied
+ *               there asynchronously on the same stream
+ *   workspace   device, >= moe_route_workspace_bytes(), 16-byte aligned
+ * Limits: 1 <= E <= MOE_MAX_EXPERTS, 1 <= k <= min(E, MOE_MAX_TOPK),
+ * T >= 0 (T = 0 writes zero counts).  Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+MOE_API int moe_route_plan(const float* logits, int T, int E, int k,
+                   int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                   int32_t* perm, int32_t* inv, int32_t* counts_host,
+                   void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Expert-slot pool [R2][R4][P1][X1]                                         */
+/* ------------------------------------------------------------------------ */
+
+typedef struct moe_pool moe_pool_t;
+
+typedef struct {
+    int layers;            /* L >= 1                                         */
+    int experts;           /* E, 1..MOE_MAX_EXPERTS                          */
+    int slots_per_layer;   /* S, 1..E                                        */
+    int hidden, inter;     /* H, I (multiples of 64)                         */
+    void* host_experts;    /* pinned [L][E][expert_bytes] packed experts;
+                              NULL only in dry-run mode                      */
+    void* dev_slots;       /* device [L][S][expert_bytes]; NULL only in
+                              dry-run mode                                   */
+    int preload;           /* 1: at create, slot s of every layer is filled
+                              with expert s (s < S), copied synchronously    */
+    int dry_run;           /* 1: policy only -- no CUDA call is ever made;
+                              stage updates the map and counters and reports
+                              the copies it would issue                      */
+} moe_pool_desc;
+
+typedef struct {
+    uint64_t hits;         /* unique routed experts found resident           */
+    uint64_t misses;       /* unique routed experts copied in                */
+    uint64_t evictions;    /* resident experts displaced by a miss           */
+    uint64_t h2d_bytes;    /* bytes copied host -> device by stage           */
+    uint64_t errors;       /* stage calls that failed and were rolled back   */
+    uint64_t events;       /* stage calls served                             */
+} moe_counters;
+
+/* Create a pool.  Stores a copy of *desc; the buffers stay caller-owned and
+ * must outlive the pool.  With preload, the initial copies are issued on
+ * the legacy stream and waited for before returning.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+MOE_API int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out_pool);
+
+/* One fused cache event for (layer, this step) [X1]:
+ *   1. waits (polling, at most timeout_ms; <= 0 means 10 s) until all work
+ *      enqueued so far on `compute` is done, so counts_host is valid;
+ *   2. U = {e : counts_host[e] > 0}.  Every resident e in U is a hit and is
+ *      touched; every absent e in U, ascending, takes the lowest free slot,
+ *      else evicts the least recently used resident expert not in U;
+ *   3. issues one cudaMemcpyAsync (pinned host -> slot) per miss on `copy`,
+ *      records an event there and makes `compute` wait on it;
+ *   4. copies the layer's slot map (int32 [E], -1 = absent) to slot_of_dev
+ *      on `compute` (skipped when slot_of_dev is NULL).
+ *   counts_host  pinned int32 [E] (typically from moe_route_plan)
+ *   slot_of_dev  device int32 [E] or NULL
+ * If |U| > S nothing changes and MOE_ERR_CAPACITY is returned.  If a copy
+ * fails to enqueue, the event is rolled back (map, stamps and counters as
+ * before the call, errors += 1) and MOE_ERR_CUDA is returned.  The wait
+ * returns MOE_ERR_TIMEOUT without changing any state.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT, MOE_ERR_CUDA. */
+MOE_API int moe_pool_stage(moe_pool_t* pool, int layer, const int32_t* counts_host,
+                   int32_t* slot_of_dev, moe_stream_t compute, moe_stream_t copy,
+                   int timeout_ms);
+
+/* Counters of one layer, or summed over all layers with layer = -1. */
+MOE_API int moe_pool_counters(const moe_pool_t* pool, int layer, moe_counters* out);
+
+/* The layer's expert -> slot map, host int32 [E] (-1 = absent). */
+MOE_API int moe_pool_slot_map(const moe_pool_t* pool, int layer, int32_t* slot_of_host);
+
+/* Copies issued by the last successful stage call of a layer, in issue
+ * order: load_expert/load_slot host int32 [S]; *n_loads <= S. */
+MOE_API int moe_pool_last_loads(const moe_pool_t* pool, int layer, int32_t* load_expert,
+                        int32_t* load_slot, int* n_loads);
+
+/* Checkpoint / resume of the pool's host state (slot maps, recency stamps,
+ * counters) -- not the slot contents.  moe_pool_state_bytes gives the size;
+ * save writes it to a host buffer; load restores it into a pool created with
+ * the same desc (MOE_ERR_STATE otherwise).  After a load the caller must
+ * refill the device slots (e.g. by re-creating with preload or copying). */
+MOE_API int moe_pool_state_bytes(const moe_pool_t* pool, size_t* out_bytes);
+MOE_API int moe_pool_save(const moe_pool_t* pool, void* buf, size_t bytes);
+MOE_API int moe_pool_load(moe_pool_t* pool, const void* buf, size_t bytes);
+
+/* Host-side fault injection for tests: the next n miss copies of stage
+ * report failure before being enqueued (no GPU work is affected). */
+MOE_API int moe_pool_inject_copy_failures(moe_pool_t* pool, int n);
+
+MOE_API void moe_pool_destroy(moe_pool_t* pool);
+
+/* ------------------------------------------------------------------------ */
+/* Expert FFN and combine [R3][R5][P1][MX]                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Scratch bytes moe_expert_ffn needs (path as passed to moe_expert_ffn). */
+MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int path,
+                            size_t* out_bytes);
+
+/* The routed experts of one layer, combined:
+ *   out[t] = sum_j w[t][j] * down_e(bf16(silu(gate_e x_t) * up_e x_t)),
+ *   e = ids[t][j], j ascending, fp32.
+ *   pool      the pool whose dev_slots hold the layer's experts
+ *   x_bf16    device bf16 [T][H]
+ *   ids, w    device, from moe_route_plan
+ *   offsets, perm, inv  device, from moe_route_plan (prefill path only;
+ *             may be NULL for the decode path)
+ *   slot_of   device int32 [E]: slot of each expert in this layer; every
+ *             routed expert must be resident (moe_pool_stage ensures it)
+ *   path      MOE_PATH_DECODE: bf16 activations times fp32-dequantised
+ *             MXFP4 on CUDA cores, fp32 accumulation, SwiGLU output rounded
+ *             to bf16.  MOE_PATH_PREFILL: activations and the SwiGLU output
+ *             quantised to MXFP8 (E4M3, block-32 E8M0 scale
+ *             2^(floor(log2 amax) - 8), RNE, satfinite) and multiplied on
+ *             tcgen05 block-scaled tensor cores, fp32 accumulation.
+ *             MOE_PATH_AUTO: decode when T*k <= MOE_DECODE_MAX_ASSIGN.
+ *   workspace device, >= moe_ffn_workspace_bytes(), 256-byte aligned
+ *   out       device fp32 [T][H], fully overwritten
+ * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16, int T, int k,
+                   const int32_t* ids, const float* w, const int32_t* offsets,
+                   const int32_t* perm, const int32_t* inv, const int32_t* slot_of,
+                   int path, void* workspace, size_t ws_bytes, float* out,
+                   moe_stream_t stream);
+
+/* Weighted combine of per-assignment expert outputs held in grouped order:
+ *   out[t][h] = sum_j w[t][j] * y_perm[inv[t*k+j]][h], j ascending, fp32.
+ *   y_perm device fp32 [A][H]; w device fp32 [T][k]; inv device int32 [A];
+ *   out device fp32 [T][H].  Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+MOE_API int moe_combine(const float* y_perm, const float* w, const int32_t* inv,
+                int T, int k, int H, float* out, moe_stream_t stream);
+
+/* MXFP8 quantisation of bf16 rows, optionally gathered by a permutation:
+ * output row p quantises x[perm[p] / k] (or x[p] when perm is NULL).
+ *   x_bf16 device [*][K]; q device uint8 [rows][K] E4M3 codes;
+ *   scales device uint8 [rows][scale_stride] E8M0 bytes (the first K/32 of
+ *   each row are written); K a multiple of 32; scale_stride >= K/32.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+MOE_API int moe_quant_mxfp8(const void* x_bf16, int K, const int32_t* perm, int k, int rows,
+                    uint8_t* q, uint8_t* scales, int scale_stride, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

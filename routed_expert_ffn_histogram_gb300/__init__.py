@@ -1,0 +1,196 @@
+"""Routed-expert FFN over a fixed GPU expert-slot pool, for GB300 (sm_103a).
+
+Python face of the C library declared in ``include/moe.h``.  The functions
+keep the C names and only marshal arguments (torch tensors -> pointers,
+torch streams -> ``cudaStream_t``); every computation runs in the library's
+CUDA kernels.  PyTorch provides device memory, pinned host memory and
+streams.
+
+Typical use for one layer and one step::
+
+    plan = RoutePlan.allocate(T, E, k, device)
+    moe_route_plan(logits, k, plan)                      # top-k, histogram, perm
+    pool.stage(layer, plan.counts_host, slot_of)         # LRU + miss copies
+    moe_expert_ffn(pool, layer, x, plan, slot_of, out)   # experts + combine
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+from . import _lib
+from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_INVALID, MOE_ERR_STATE,
+                   MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_OK,
+                   MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MoeCounters, MoeError, MoePoolDesc, check,
+                   lib, ptr, status_str, stream_handle)
+
+__all__ = [
+    "moe_expert_bytes", "moe_pack_expert", "moe_route_workspace_bytes", "moe_route_plan", "moe_ffn_workspace_bytes",
+    "moe_expert_ffn", "moe_combine", "moe_quant_mxfp8", "Pool", "RoutePlan", "MoeError", "lib", "status_str",
+    "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL",
+]
+
+
+def moe_expert_bytes(hidden: int, inter: int) -> int:
+    out = C.c_size_t(0)
+    check("moe_expert_bytes", lib().moe_expert_bytes(hidden, inter, C.byref(out)))
+    return out.value
+
+
+def moe_pack_expert(w: dict, hidden: int, inter: int, dst) -> None:
+    """Canonical MXFP4 arrays (host numpy, see ``include/moe.h``) -> native
+    layout written at host address/array ``dst``."""
+    import numpy as np
+
+    a = {k: np.ascontiguousarray(v, np.uint8) for k, v in w.items()}
+    check("moe_pack_expert", lib().moe_pack_expert(
+        ptr(a["gate_codes"]), ptr(a["gate_scales"]), ptr(a["up_codes"]), ptr(a["up_scales"]),
+        ptr(a["down_codes"]), ptr(a["down_scales"]), hidden, inter, ptr(dst)))
+
+
+def moe_route_workspace_bytes(T: int, E: int, k: int) -> int:
+    out = C.c_size_t(0)
+    check("moe_route_workspace_bytes", lib().moe_route_workspace_bytes(T, E, k, C.byref(out)))
+    return out.value
+
+
+@dataclass
+class RoutePlan:
+    """Device buffers written by moe_route_plan (plus optional pinned counts)."""
+
+    T: int
+    E: int
+    k: int
+    ids: object
+    w: object
+    counts: object
+    offsets: object
+    perm: object
+    inv: object
+    workspace: object
+    counts_host: object = None
+
+    @staticmethod
+    def allocate(T: int, E: int, k: int, device="cuda", counts_host: bool = False) -> "RoutePlan":
+        import torch
+
+        i32 = dict(dtype=torch.int32, device=device)
+        ws = max(moe_route_workspace_bytes(T, E, k), 16)
+        return RoutePlan(T, E, k,
+                         ids=torch.empty((T, k), **i32), w=torch.empty((T, k), dtype=torch.float32, device=device),
+                         counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+                         perm=torch.empty(max(T * k, 1), **i32), inv=torch.empty(max(T * k, 1), **i32),
+                         workspace=torch.empty(ws, dtype=torch.uint8, device=device),
+                         counts_host=torch.empty(E, dtype=torch.int32).pin_memory() if counts_host else None)
+
+
+def moe_route_plan(logits, k: int, plan: RoutePlan, stream=None, with_counts_host: bool = True) -> None:
+    """Top-k + softmax + histogram + stable permutation (moe_route_plan)."""
+    T, E = logits.shape
+    ch = plan.counts_host if with_counts_host else None
+    check("moe_route_plan", lib().moe_route_plan(
+        ptr(logits), T, E, k, ptr(plan.ids), ptr(plan.w), ptr(plan.counts), ptr(plan.offsets), ptr(plan.perm),
+        ptr(plan.inv), ptr(ch), ptr(plan.workspace), plan.workspace.numel(), stream_handle(stream)))
+
+
+def moe_ffn_workspace_bytes(T: int, k: int, hidden: int, inter: int, path: int = MOE_PATH_AUTO) -> int:
+    out = C.c_size_t(0)
+    check("moe_ffn_workspace_bytes", lib().moe_ffn_workspace_bytes(T, k, hidden, inter, path, C.byref(out)))
+    return out.value
+
+
+def moe_expert_ffn(pool: "Pool", layer: int, x_bf16, plan: RoutePlan, slot_of, out, workspace,
+                   path: int = MOE_PATH_AUTO, stream=None) -> None:
+    """Routed experts of one layer with the weighted combine (moe_expert_ffn)."""
+    T = x_bf16.shape[0]
+    check("moe_expert_ffn", lib().moe_expert_ffn(
+        pool.handle, layer, ptr(x_bf16), T, plan.k, ptr(plan.ids), ptr(plan.w), ptr(plan.offsets),
+        ptr(plan.perm), ptr(plan.inv), ptr(slot_of), path, ptr(workspace),
+        workspace.numel() * workspace.element_size() if workspace is not None else 0, ptr(out),
+        stream_handle(stream)))
+
+
+def moe_combine(y_perm, w, inv, out, stream=None) -> None:
+    T, k = w.shape
+    H = out.shape[1]
+    check("moe_combine", lib().moe_combine(ptr(y_perm), ptr(w), ptr(inv), T, k, H, ptr(out),
+                                           stream_handle(stream)))
+
+
+def moe_quant_mxfp8(x_bf16, q, scales, perm=None, k: int = 1, stream=None) -> None:
+    rows, K = q.shape
+    check("moe_quant_mxfp8", lib().moe_quant_mxfp8(ptr(x_bf16), K, ptr(perm), k, rows, ptr(q), ptr(scales),
+                                                   scales.shape[1], stream_handle(stream)))
+
+
+class Pool:
+    """An expert-slot pool (moe_pool_*).  Buffers stay owned by the caller
+    (kept referenced here so they outlive the pool)."""
+
+    def __init__(self, layers, experts, slots, hidden, inter, host_experts=None, dev_slots=None,
+                 preload=False, dry_run=False):
+        self.layers, self.experts, self.slots, self.hidden, self.inter = layers, experts, slots, hidden, inter
+        self._keep = (host_experts, dev_slots)
+        d = MoePoolDesc(layers, experts, slots, hidden, inter, ptr(host_experts), ptr(dev_slots),
+                        int(bool(preload)), int(bool(dry_run)))
+        h = C.c_void_p()
+        check("moe_pool_create", lib().moe_pool_create(C.byref(d), C.byref(h)))
+        self.handle = h.value
+
+    def stage(self, layer, counts_host, slot_of_dev=None, compute=None, copy=None, timeout_ms=10000) -> int:
+        """One fused cache event; returns the status (raises on errors other
+        than capacity and timeout, which are returned)."""
+        comp = stream_handle(compute) if (compute is not None or slot_of_dev is not None) else None
+        cop = stream_handle(copy) if copy is not None else comp
+        rc = lib().moe_pool_stage(self.handle, layer, ptr(counts_host), ptr(slot_of_dev), comp, cop, timeout_ms)
+        if rc in (MOE_OK, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT):
+            return rc
+        check("moe_pool_stage", rc)
+        return rc
+
+    def counters(self, layer=-1) -> dict:
+        c = MoeCounters()
+        check("moe_pool_counters", lib().moe_pool_counters(self.handle, layer, C.byref(c)))
+        return c.as_dict()
+
+    def slot_map(self, layer):
+        import numpy as np
+
+        m = np.zeros(self.experts, np.int32)
+        check("moe_pool_slot_map", lib().moe_pool_slot_map(self.handle, layer, m.ctypes.data))
+        return m
+
+    def last_loads(self, layer):
+        import numpy as np
+
+        le = np.zeros(self.slots, np.int32)
+        ls = np.zeros(self.slots, np.int32)
+        n = C.c_int(0)
+        check("moe_pool_last_loads", lib().moe_pool_last_loads(self.handle, layer, le.ctypes.data,
+                                                                ls.ctypes.data, C.byref(n)))
+        return list(zip(le[: n.value].tolist(), ls[: n.value].tolist()))
+
+    def save(self) -> bytes:
+        n = C.c_size_t(0)
+        check("moe_pool_state_bytes", lib().moe_pool_state_bytes(self.handle, C.byref(n)))
+        buf = C.create_string_buffer(n.value)
+        check("moe_pool_save", lib().moe_pool_save(self.handle, buf, n.value))
+        return buf.raw
+
+    def load(self, state: bytes) -> int:
+        buf = C.create_string_buffer(state, len(state))
+        return lib().moe_pool_load(self.handle, buf, len(state))
+
+    def inject_copy_failures(self, n: int) -> None:
+        check("moe_pool_inject_copy_failures", lib().moe_pool_inject_copy_failures(self.handle, n))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().moe_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

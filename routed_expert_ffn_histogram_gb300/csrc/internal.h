@@ -1,0 +1,93 @@
+// Host-side definitions shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Remember a CUDA error for moe_last_cuda_error() and map it to a status.
+int cuda_fail(cudaError_t e);
+
+#define MOE_CUDA_TRY(expr)                                  \
+    do {                                                    \
+        cudaError_t _e = (expr);                            \
+        if (_e != cudaSuccess) return ::moe::cuda_fail(_e); \
+    } while (0)
+
+inline size_t pad16(size_t x) { return (x + 15) & ~size_t(15); }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// GPU-native packed expert.  Every row stores its K/2 code bytes followed by
+// its K/32 E8M0 scale bytes, padded to a multiple of 16 bytes.  The gate/up
+// matrix has 2I rows interleaved in chunks of 64: chunk c holds gate rows
+// 64c..64c+63 then up rows 64c..64c+63.  The down matrix (H rows) follows.
+struct Layout {
+    int H = 0, I = 0;
+    size_t rs_gu = 0;        // bytes per gate/up row (K = H)
+    size_t rs_d = 0;         // bytes per down row (K = I)
+    size_t d_off = 0;        // byte offset of the down matrix
+    size_t expert_bytes = 0; // whole expert, a multiple of 1024
+
+    static bool make(int hidden, int inter, Layout* L) {
+        if (hidden <= 0 || inter <= 0 || hidden % 64 || inter % 64) return false;
+        L->H = hidden;
+        L->I = inter;
+        L->rs_gu = size_t(hidden) / 2 + pad16(size_t(hidden) / 32);
+        L->rs_d = size_t(inter) / 2 + pad16(size_t(inter) / 32);
+        L->d_off = 2 * size_t(inter) * L->rs_gu;
+        L->expert_bytes = round_up(L->d_off + size_t(hidden) * L->rs_d, 1024);
+        return true;
+    }
+    // Row of the gate/up matrix that holds gate row r (up row: + 64).
+    __host__ __device__ static inline size_t gate_row(int r) { return size_t(r / 64) * 128 + size_t(r % 64); }
+};
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;
+};
+// Properties of the current device (cached per device).
+int current_device_info(DeviceInfo* out);
+
+// ---- kernel launchers (route.cu, decode.cu, prefill.cu) -------------------
+
+int launch_route_plan(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                      int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                      int32_t* tile_hist, int n_tiles, cudaStream_t s);
+int route_tiles(int T, int k);
+
+struct FfnArgs {
+    const uint8_t* slots;      // base of this layer's slots
+    size_t expert_bytes;
+    int S, E;
+    const Layout* L;
+    const uint16_t* x;         // bf16 [T][H]
+    int T, k;
+    const int32_t* ids;
+    const float* w;
+    const int32_t* offsets;
+    const int32_t* perm;
+    const int32_t* inv;
+    const int32_t* slot_of;
+    float* out;
+};
+
+size_t decode_workspace_bytes(int T, int k, int H, int I);
+int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+
+size_t prefill_workspace_bytes(int T, int k, int H, int I);
+int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+
+int launch_combine(const float* y_perm, const float* w, const int32_t* inv, int T, int k, int H,
+                   float* out, cudaStream_t s);
+int launch_quant_mxfp8(const uint16_t* x, int K, const int32_t* perm, int k, int rows, uint8_t* q,
+                       uint8_t* scales, int scale_stride, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,148 @@
+// Prefill-side elementwise kernels: MXFP8 quantisation of activations
+// (gathered into grouped order) and the weighted combine of grouped expert
+// outputs.
+//
+// MXFP8 rule (OCP Microscaling Formats v1.0, section 6.3): per block of 32
+// along the reduction dimension, shared exponent = floor(log2(amax)) - 8
+// (8 = largest E4M3 exponent), stored as an E8M0 byte clamped to [0, 254]
+// (0 for an all-zero block); elements are E4M3 with round-to-nearest-even
+// and saturation of finite overflow to +-448.
+//
+// Combine: llama.cpp discussion "fixed GPU expert working set with Native
+// CPU miss execution", main post -- routed experts' outputs are merged with
+// the routing weights; here in ascending rank j, fp32, without fused
+// multiply-add so the sum is the plain w*y + acc sequence.
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ uint32_t e8m0_of_amax(float amax) {
+    const uint32_t bits = __float_as_uint(amax);
+    const int ef = int((bits >> 23) & 0xffu);
+    if (amax == 0.0f || ef == 0) return 0u;  // zero or subnormal amax clamps to 0
+    return uint32_t(min(max(ef - 8, 0), 254));
+}
+
+// 2^(127 - sb) as fp32 (sb in [0, 254]).
+__device__ __forceinline__ float inv_scale(uint32_t sb) {
+    const int ef = 254 - int(sb);
+    return ef > 0 ? __uint_as_float(uint32_t(ef) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One lane quantises one 32-element block: 64 bytes in, 32 codes + 1 scale out.
+__global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint16_t* __restrict__ x, int K,
+                                                          const int32_t* __restrict__ perm, int k, int rows,
+                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales,
+                                                          int scale_stride) {
+    const int nb = K / 32;
+    const long total = (long)rows * nb;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+        const int row = int(i / nb), b = int(i - (long)row * nb);
+        const int src = perm ? perm[row] / k : row;
+        const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)src * K + (size_t)b * 32);
+        uint4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = __ldg(p + c);
+        float f[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[c * 8 + 2 * j] = __uint_as_float(u[j] << 16);
+                f[c * 8 + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+            }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        const uint32_t sb = e8m0_of_amax(amax);
+        const float m = inv_scale(sb);
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t a = cvt_e4m3x2(f[4 * j] * m, f[4 * j + 1] * m);
+            const uint32_t c = cvt_e4m3x2(f[4 * j + 2] * m, f[4 * j + 3] * m);
+            w[j] = a | (c << 16);
+        }
+        uint4* o = reinterpret_cast<uint4*>(q + (size_t)row * K + (size_t)b * 32);
+        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        scales[(size_t)row * scale_stride + b] = uint8_t(sb);
+    }
+}
+
+// out[t][h] = sum_j w[t][j] * y[inv[t*k+j]][h]; one thread per 4 outputs.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
+                                                      const int32_t* __restrict__ inv, int T, int k, int H,
+                                                      float* __restrict__ out) {
+    const int h4 = H / 4;
+    const long total = (long)T * h4;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+        const int t = int(i / h4), c = int(i - (long)t * h4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float wj = w[(size_t)t * k + j];
+            const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)inv[(size_t)t * k + j] * H) + c);
+            acc.x = __fadd_rn(acc.x, __fmul_rn(wj, v.x));
+            acc.y = __fadd_rn(acc.y, __fmul_rn(wj, v.y));
+            acc.z = __fadd_rn(acc.z, __fmul_rn(wj, v.z));
+            acc.w = __fadd_rn(acc.w, __fmul_rn(wj, v.w));
+        }
+        reinterpret_cast<float4*>(out + (size_t)t * H)[c] = acc;
+    }
+}
+
+__global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __restrict__ y,
+                                                             const float* __restrict__ w,
+                                                             const int32_t* __restrict__ inv, int T, int k,
+                                                             int H, float* __restrict__ out) {
+    const long total = (long)T * H;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+        const int t = int(i / H), c = int(i - (long)t * H);
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j)
+            acc = __fadd_rn(acc, __fmul_rn(w[(size_t)t * k + j], y[(size_t)inv[(size_t)t * k + j] * H + c]));
+        out[(size_t)t * H + c] = acc;
+    }
+}
+
+int grid_for(long work, int threads) {
+    DeviceInfo di;
+    if (current_device_info(&di) != MOE_OK) return 1;
+    long g = (work + threads - 1) / threads;
+    const long cap = long(di.sms) * 8;
+    return int(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+}  // namespace
+
+int launch_quant_mxfp8(const uint16_t* x, int K, const int32_t* perm, int k, int rows, uint8_t* q,
+                       uint8_t* scales, int scale_stride, cudaStream_t s) {
+    const long work = (long)rows * (K / 32);
+    quant_mxfp8_kernel<<<grid_for(work, 256), 256, 0, s>>>(x, K, perm, k, rows, q, scales, scale_stride);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int launch_combine(const float* y, const float* w, const int32_t* inv, int T, int k, int H, float* out,
+                   cudaStream_t s) {
+    const bool vec = (H % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+    if (vec) {
+        combine_kernel<<<grid_for((long)T * (H / 4), 256), 256, 0, s>>>(y, w, inv, T, k, H, out);
+    } else {
+        combine_scalar_kernel<<<grid_for((long)T * H, 256), 256, 0, s>>>(y, w, inv, T, k, H, out);
+    }
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,252 @@
+// Routing and grouping: top-k + softmax over the selected experts, a
+// shared-memory atomic histogram per tile of tokens, an exclusive prefix sum
+// over experts and a stable permutation of the assignments by expert.
+//
+// Source: tinyserve README, "Performance" (top_k=4 routing of GPT-OSS-20B)
+// and "How it works" item 6 (batched prefill groups tokens by expert so each
+// unique expert is loaded once); llama.cpp discussion "fixed GPU expert
+// working set with Native CPU miss execution", main post (selected expert IDs
+// are split per step before the experts run).
+//
+// Layout: one warp per token for the top-k (each lane holds E/32 logits,
+// k rounds of a warp-wide arg-best); tiles of 256 tokens per CTA.  With one
+// tile the whole plan is a single launch; otherwise a second launch turns
+// the per-tile histograms into global offsets and scatters the permutation.
+// Ranks inside a warp come from __match_any_sync + __popc, so the order is
+// fixed by the assignment index, never by the order atomics land in.
+#include <cfloat>
+#include <cmath>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTileTokens = 256;
+constexpr int kMaxPerLane = MOE_MAX_EXPERTS / 32;
+
+__device__ __forceinline__ bool ranks_before(float la, int a, float lb, int b) {
+    const bool na = isnan(la), nb = isnan(lb);
+    if (na != nb) return nb;
+    if (!na && la != lb) return la > lb;
+    return a < b;
+}
+
+struct Smem {
+    int hist[MOE_MAX_EXPERTS];
+    int base[MOE_MAX_EXPERTS];
+    int scan_tmp[kWarps];
+    int warp_cnt[kWarps][MOE_MAX_EXPERTS];
+};
+
+// Top-k + softmax for the tokens of this CTA's tile; accumulates the tile
+// histogram into sm.hist (which must be zeroed by the caller).
+__device__ void topk_tile(const float* __restrict__ logits, int T, int E, int k,
+                          int32_t* __restrict__ ids, float* __restrict__ w, int t0, Smem& sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t1 = min(T, t0 + kTileTokens);
+    for (int t = t0 + warp; t < t1; t += kWarps) {
+        const float* row = logits + (size_t)t * E;
+        float v[kMaxPerLane];
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = (e < E) ? __ldg(row + e) : 0.0f;
+        }
+        uint32_t taken = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i)
+            if (lane + 32 * i >= E) taken |= 1u << i;
+
+        float sel_v = 0.0f;
+        int sel_id = -1;
+        for (int j = 0; j < k; ++j) {
+            float bv = 0.0f;
+            int bid = -1;
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane; ++i) {
+                if (taken & (1u << i)) continue;
+                const int e = lane + 32 * i;
+                if (bid < 0 || ranks_before(v[i], e, bv, bid)) { bv = v[i]; bid = e; }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
+                if (oid >= 0 && (bid < 0 || ranks_before(ov, oid, bv, bid))) { bv = ov; bid = oid; }
+            }
+            // every lane now holds the same winner
+            if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+            if (lane == j) { sel_v = bv; sel_id = bid; }
+            if (lane == 0) atomicAdd(&sm.hist[bid], 1);
+        }
+        // softmax over the k selected logits in fp64, summed in rank order
+        const double m = (double)__shfl_sync(0xffffffffu, sel_v, 0);
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const float vj = __shfl_sync(0xffffffffu, sel_v, j);
+            sum += exp((double)vj - m);
+        }
+        if (lane < k) {
+            const double d = exp((double)sel_v - m);
+            ids[(size_t)t * k + lane] = sel_id;
+            w[(size_t)t * k + lane] = (float)(d / sum);
+        }
+    }
+}
+
+// Exclusive scan of tot[e] over e < E (E <= kThreads) into out[e]; returns
+// the total to every thread.
+__device__ int block_exclusive_scan(int v, int* out, Smem& sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += n;
+    }
+    if (lane == 31) sm.scan_tmp[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int i = 0; i < kWarps; ++i) {
+        const int s = sm.scan_tmp[i];
+        if (i < warp) wbase += s;
+        total += s;
+    }
+    out[threadIdx.x] = wbase + incl - v;
+    __syncthreads();
+    return total;
+}
+
+// Offsets + stable scatter of the assignments [a0, a1) of one tile, given
+// this tile's first position per expert in sm.base.
+__device__ void scatter_tile(const int32_t* __restrict__ ids, int a0, int a1, int E,
+                             int32_t* __restrict__ perm, int32_t* __restrict__ inv, Smem& sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kWarps * MOE_MAX_EXPERTS; i += kThreads) (&sm.warp_cnt[0][0])[i] = 0;
+    __syncthreads();
+    const int n = a1 - a0;
+    const int seg = ((n + kWarps - 1) / kWarps + 31) / 32 * 32;
+    const int ws = a0 + warp * seg, we = min(a1, ws + seg);
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int c = ws; c < we; c += 32) {
+        const int a = c + lane;
+        const int e = (a < we) ? ids[a] : -1;
+        const uint32_t mask = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (mask & lt) == 0) sm.warp_cnt[warp][e] += __popc(mask);
+    }
+    __syncthreads();
+    if (threadIdx.x < E) {
+        int run = sm.base[threadIdx.x];
+        for (int i = 0; i < kWarps; ++i) {
+            const int c = sm.warp_cnt[i][threadIdx.x];
+            sm.warp_cnt[i][threadIdx.x] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int c = ws; c < we; c += 32) {
+        const int a = c + lane;
+        const int e = (a < we) ? ids[a] : -1;
+        const uint32_t mask = __match_any_sync(0xffffffffu, e);
+        int pos = 0;
+        if (e >= 0) pos = sm.warp_cnt[warp][e] + __popc(mask & lt);
+        __syncwarp();
+        if (e >= 0) {
+            perm[pos] = a;
+            inv[a] = pos;
+            if ((mask & lt) == 0) sm.warp_cnt[warp][e] += __popc(mask);
+        }
+        __syncwarp();
+    }
+}
+
+// Whole plan in one CTA (T <= one tile).
+__global__ void __launch_bounds__(kThreads) route_single_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+    float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    __shared__ Smem sm;
+    if (threadIdx.x < MOE_MAX_EXPERTS) sm.hist[threadIdx.x] = 0;
+    __syncthreads();
+    topk_tile(logits, T, E, k, ids, w, 0, sm);
+    __syncthreads();
+    const int tot = (threadIdx.x < E) ? sm.hist[threadIdx.x] : 0;
+    const int total = block_exclusive_scan(tot, sm.base, sm);
+    if (threadIdx.x < E) {
+        counts[threadIdx.x] = tot;
+        offsets[threadIdx.x] = sm.base[threadIdx.x];
+    }
+    if (threadIdx.x == 0) offsets[E] = total;
+    __syncthreads();
+    scatter_tile(ids, 0, T * k, E, perm, inv, sm);
+}
+
+// Multi-tile, pass 1: top-k + per-tile histogram.
+__global__ void __launch_bounds__(kThreads) route_topk_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+    float* __restrict__ w, int32_t* __restrict__ tile_hist) {
+    __shared__ Smem sm;
+    if (threadIdx.x < MOE_MAX_EXPERTS) sm.hist[threadIdx.x] = 0;
+    __syncthreads();
+    topk_tile(logits, T, E, k, ids, w, blockIdx.x * kTileTokens, sm);
+    __syncthreads();
+    if (threadIdx.x < E) tile_hist[(size_t)blockIdx.x * E + threadIdx.x] = sm.hist[threadIdx.x];
+}
+
+// Multi-tile, pass 2: global offsets from all tile histograms, then the
+// stable scatter of this tile.
+__global__ void __launch_bounds__(kThreads) route_scatter_kernel(
+    const int32_t* __restrict__ ids, int T, int E, int k, const int32_t* __restrict__ tile_hist,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv) {
+    __shared__ Smem sm;
+    const int tile = blockIdx.x, n_tiles = gridDim.x;
+    int tot = 0, pre = 0;
+    if (threadIdx.x < E) {
+        for (int i = 0; i < n_tiles; ++i) {
+            const int c = tile_hist[(size_t)i * E + threadIdx.x];
+            tot += c;
+            if (i < tile) pre += c;
+        }
+    }
+    const int total = block_exclusive_scan(tot, sm.base, sm);
+    if (threadIdx.x < E) {
+        if (tile == 0) {
+            counts[threadIdx.x] = tot;
+            offsets[threadIdx.x] = sm.base[threadIdx.x];
+        }
+        sm.base[threadIdx.x] += pre;
+    }
+    if (tile == 0 && threadIdx.x == 0) offsets[E] = total;
+    __syncthreads();
+    const int a0 = tile * kTileTokens * k;
+    const int a1 = min(T, (tile + 1) * kTileTokens) * k;
+    scatter_tile(ids, a0, a1, E, perm, inv, sm);
+}
+
+}  // namespace
+
+int route_tiles(int T, int k) {
+    (void)k;
+    return T <= kTileTokens ? 1 : (T + kTileTokens - 1) / kTileTokens;
+}
+
+int launch_route_plan(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                      int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                      int32_t* tile_hist, int n_tiles, cudaStream_t s) {
+    if (n_tiles <= 1) {
+        route_single_kernel<<<1, kThreads, 0, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, inv);
+        MOE_CUDA_TRY(cudaGetLastError());
+        return MOE_OK;
+    }
+    route_topk_kernel<<<n_tiles, kThreads, 0, s>>>(logits, T, E, k, ids, w, tile_hist);
+    MOE_CUDA_TRY(cudaGetLastError());
+    route_scatter_kernel<<<n_tiles, kThreads, 0, s>>>(ids, T, E, k, tile_hist, counts, offsets, perm, inv);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+}  // namespace moe

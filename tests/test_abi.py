@@ -1,0 +1,170 @@
+"""CPU tests of the C ABI: the library loads, exports every symbol the
+header declares, validates arguments, and its host-side logic (native
+packing, the pool's LRU policy in dry-run mode, checkpoint/resume, fault
+injection) matches the oracle."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import moe_synth as S
+import oracle
+import routed_expert_ffn_histogram_gb300 as M
+from routed_expert_ffn_histogram_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol():
+    names = _declared()
+    assert len(names) >= 20
+    L = M.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SIGNATURES), set(names) ^ set(_lib.SIGNATURES)
+
+
+def test_status_strings_and_no_device_count():
+    for s in [0, -1, -2, -3, -4, -5, -6]:
+        assert M.status_str(s)
+    assert M.lib().moe_device_count() >= 0
+
+
+def test_expert_bytes():
+    for H, I in [(2880, 2880), (2048, 768), (256, 512)]:
+        eb = M.moe_expert_bytes(H, I)
+        canon = 3 * (H * I // 2 + H * I // 32)
+        assert eb % 1024 == 0 and canon <= eb <= canon * 1.05
+    with pytest.raises(M.MoeError):
+        M.moe_expert_bytes(100, 64)
+
+
+def test_pack_native_layout():
+    """Gate/up rows interleave in chunks of 64; every row is codes then scales."""
+    wl = S.WORKLOADS[0]
+    H, I = wl.hidden, wl.inter
+    w = S.expert_weights(wl, 0, 1)
+    eb = M.moe_expert_bytes(H, I)
+    buf = np.zeros(eb, np.uint8)
+    M.moe_pack_expert(w, H, I, buf)
+    rs_gu = H // 2 + ((H // 32 + 15) // 16) * 16
+    rs_d = I // 2 + ((I // 32 + 15) // 16) * 16
+    for r in [0, 1, 63, 64, 200, I - 1]:
+        g = (r // 64) * 128 + r % 64
+        row = buf[g * rs_gu:(g + 1) * rs_gu]
+        assert np.array_equal(row[:H // 2], w["gate_codes"][r])
+        assert np.array_equal(row[H // 2:H // 2 + H // 32], w["gate_scales"][r])
+        assert not row[H // 2 + H // 32:].any()
+        row = buf[(g + 64) * rs_gu:(g + 65) * rs_gu]
+        assert np.array_equal(row[:H // 2], w["up_codes"][r])
+        assert np.array_equal(row[H // 2:H // 2 + H // 32], w["up_scales"][r])
+    d_off = 2 * I * rs_gu
+    for r in [0, 7, H - 1]:
+        row = buf[d_off + r * rs_d:d_off + (r + 1) * rs_d]
+        assert np.array_equal(row[:I // 2], w["down_codes"][r])
+        assert np.array_equal(row[I // 2:I // 2 + I // 32], w["down_scales"][r])
+
+
+def test_invalid_arguments_rejected_before_launch():
+    L = M.lib()
+    sz = C.c_size_t()
+    assert L.moe_route_workspace_bytes(10, 300, 2, C.byref(sz)) == M.MOE_ERR_INVALID
+    assert L.moe_route_workspace_bytes(10, 8, 9, C.byref(sz)) == M.MOE_ERR_INVALID
+    assert L.moe_route_plan(None, 4, 8, 2, None, None, None, None, None, None, None, None, 0, None) == \
+        M.MOE_ERR_INVALID
+    assert L.moe_combine(None, None, None, 2, 0, 8, None, None) == M.MOE_ERR_INVALID
+    assert L.moe_quant_mxfp8(None, 33, None, 1, 1, None, None, 2, None) == M.MOE_ERR_INVALID
+    assert L.moe_ffn_workspace_bytes(4, 2, 250, 512, 0, C.byref(sz)) == M.MOE_ERR_INVALID
+    assert L.moe_expert_ffn(None, 0, None, 1, 1, None, None, None, None, None, None, 0, None, 0, None, None) == \
+        M.MOE_ERR_INVALID
+    d = _lib.MoePoolDesc(1, 8, 9, 256, 512, None, None, 0, 1)
+    h = C.c_void_p()
+    assert L.moe_pool_create(C.byref(d), C.byref(h)) == M.MOE_ERR_INVALID  # S > E
+    d = _lib.MoePoolDesc(1, 8, 4, 256, 512, None, None, 0, 0)
+    assert L.moe_pool_create(C.byref(d), C.byref(h)) == M.MOE_ERR_INVALID  # buffers required
+
+
+def _stream_counts(wl, layer, step):
+    ids, _ = oracle.route(S.logits(wl, layer, step), wl.top_k)
+    return np.bincount(ids.reshape(-1), minlength=wl.experts).astype(np.int32)
+
+
+def test_dry_run_pool_matches_oracle_lru():
+    """The library's pool policy equals the oracle's LRU event by event
+    (slot maps, load lists and counters bit-exact) on the skewed GPT-OSS
+    offload routing, 24 layers x 40 steps."""
+    wl = S.WORKLOADS[2]
+    pool = M.Pool(wl.layers, wl.experts, wl.slots, wl.hidden, wl.inter, dry_run=True)
+    ref = [oracle.LRUPool(wl.slots, wl.experts) for _ in range(wl.layers)]
+    for step in range(40):
+        for l in range(wl.layers):
+            c = _stream_counts(wl, l, step)
+            loads = ref[l].step(c)
+            assert pool.stage(l, c) == M.MOE_OK
+            assert pool.last_loads(l) == loads
+            assert np.array_equal(pool.slot_map(l), ref[l].slot_map())
+    for l in range(wl.layers):
+        got = pool.counters(l)
+        exp = ref[l].counters()
+        assert (got["hits"], got["misses"], got["evictions"]) == (exp["hits"], exp["misses"], exp["evictions"])
+        assert got["h2d_bytes"] == exp["misses"] * M.moe_expert_bytes(wl.hidden, wl.inter)
+
+
+def test_dry_run_capacity_and_preload():
+    pool = M.Pool(1, 8, 2, 256, 512, dry_run=True, preload=True)
+    assert np.array_equal(pool.slot_map(0), [0, 1, -1, -1, -1, -1, -1, -1])
+    assert pool.stage(0, np.array([1, 1, 1, 0, 0, 0, 0, 0], np.int32)) == M.MOE_ERR_CAPACITY
+    assert np.array_equal(pool.slot_map(0), [0, 1, -1, -1, -1, -1, -1, -1])
+    assert pool.stage(0, np.array([0, 3, 0, 0, 0, 0, 0, 2], np.int32)) == M.MOE_OK
+    assert pool.last_loads(0) == [(7, 0)]  # preloaded stamps tie -> lowest slot evicted
+
+
+def test_checkpoint_resume_roundtrip():
+    wl = S.WORKLOADS[2]
+    a = M.Pool(wl.layers, wl.experts, wl.slots, wl.hidden, wl.inter, dry_run=True)
+    for step in range(10):
+        for l in range(wl.layers):
+            a.stage(l, _stream_counts(wl, l, step))
+    state = a.save()
+    b = M.Pool(wl.layers, wl.experts, wl.slots, wl.hidden, wl.inter, dry_run=True)
+    assert b.load(state) == M.MOE_OK
+    for step in range(10, 20):
+        for l in range(wl.layers):
+            c = _stream_counts(wl, l, step)
+            a.stage(l, c)
+            b.stage(l, c)
+            assert a.last_loads(l) == b.last_loads(l)
+    assert a.counters() == b.counters()
+    other = M.Pool(wl.layers, wl.experts, 4, wl.hidden, wl.inter, dry_run=True)
+    assert other.load(state) == M.MOE_ERR_STATE
+    bad = bytearray(state)
+    bad[24:28] = (99).to_bytes(4, "little", signed=True)  # corrupt a slot entry
+    assert b.load(bytes(bad)) == M.MOE_ERR_STATE
+
+
+def test_injected_copy_failure_rolls_back():
+    """A failed copy leaves the event unapplied; the retry is a clean event."""
+    pool = M.Pool(1, 8, 2, 256, 512, dry_run=True)
+    ref = oracle.LRUPool(2, 8)
+    c1 = np.array([1, 0, 0, 1, 0, 0, 0, 0], np.int32)
+    assert pool.stage(0, c1) == M.MOE_OK
+    ref.step(c1)
+    before = (pool.slot_map(0).copy(), pool.counters(0))
+    pool.inject_copy_failures(1)
+    c2 = np.array([0, 0, 1, 1, 0, 0, 0, 0], np.int32)
+    with pytest.raises(M.MoeError) as ei:
+        pool.stage(0, c2)
+    assert ei.value.status == M.MOE_ERR_CUDA
+    assert np.array_equal(pool.slot_map(0), before[0])
+    after = pool.counters(0)
+    assert after["errors"] == 1 and after["misses"] == before[1]["misses"] and after["hits"] == before[1]["hits"]
+    assert pool.stage(0, c2) == M.MOE_OK
+    assert pool.last_loads(0) == ref.step(c2)
+    assert np.array_equal(pool.slot_map(0), ref.slot_map())

@@ -1,0 +1,79 @@
+"""GPU parity of the offloaded decode (GPT-OSS shape, 8 of 32 slots per
+layer, LRU, skewed routing): slot maps, load lists and hit/miss/eviction
+counters bit-exact against the oracle's LRU for every (layer, step) event;
+layer outputs computed from the staged slots match the oracle."""
+import numpy as np
+import pytest
+
+import moe_synth as S
+import oracle
+from helpers import make_pool, rel_l2
+from test_gpu_decode import DECODE_REL_L2, _oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+
+def test_offload_decode_lru_and_outputs():
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    pool, host, dev = make_pool(M, wl, preload=False)
+    ref = [oracle.LRUPool(wl.slots, wl.experts) for _ in range(wl.layers)]
+    compute = torch.cuda.Stream()
+    copy = torch.cuda.Stream()
+    T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
+    plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    ws = torch.empty(M.moe_ffn_workspace_bytes(T, k, H, I, M.MOE_PATH_DECODE), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    samples = {(0, 0), (3, 11), (7, 23)}
+    with torch.cuda.stream(compute):
+        for step in range(8):
+            for layer in range(wl.layers):
+                lg = torch.from_numpy(S.logits(wl, layer, step)).cuda()
+                x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step).view(np.int16)).cuda().view(
+                    torch.bfloat16)
+                M.moe_route_plan(lg, k, plan, stream=compute)
+                assert pool.stage(layer, plan.counts_host, slot_of, compute=compute, copy=copy) == M.MOE_OK
+                counts = plan.counts_host.numpy().copy()
+                assert pool.last_loads(layer) == ref[layer].step(counts)
+                assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
+                M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE, stream=compute)
+                if (step, layer) in samples:
+                    compute.synchronize()
+                    got = out.cpu().numpy()
+                    r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                    assert rel_l2(got, r) <= DECODE_REL_L2
+    compute.synchronize()
+    eb = M.moe_expert_bytes(H, I)
+    for layer in range(wl.layers):
+        c = pool.counters(layer)
+        e = ref[layer].counters()
+        assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+        assert c["h2d_bytes"] == e["misses"] * eb
+
+
+def test_injected_copy_failure_on_device_pool():
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[0]
+    pool, host, dev = make_pool(M, wl, slots=2, preload=False)
+    counts = torch.zeros(8, dtype=torch.int32).pin_memory()
+    slot_of = torch.full((8,), -7, dtype=torch.int32, device="cuda")
+    counts[3] = 1
+    pool.inject_copy_failures(1)
+    with pytest.raises(M.MoeError):
+        pool.stage(0, counts, slot_of)
+    torch.cuda.synchronize()
+    assert pool.slot_map(0).tolist() == [-1] * 8
+    assert pool.counters(0)["errors"] == 1
+    assert pool.stage(0, counts, slot_of) == M.MOE_OK
+    torch.cuda.synchronize()
+    assert slot_of.cpu().tolist() == [-1, -1, -1, 0, -1, -1, -1, -1]
+    # slot 0 now holds expert 3's bytes
+    eb = M.moe_expert_bytes(wl.hidden, wl.inter)
+    assert torch.equal(dev[:eb].cpu(), host[3 * eb:4 * eb])
