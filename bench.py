@@ -268,6 +268,76 @@ def gpu_leg(args, wl, rank, world):
     return res
 
 
+def prefill_leg(args, wl):
+    """One prefill layer call per step: routing + grouped tcgen05 expert FFN +
+    combine, graph-captured, inputs resident in HBM."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    E, k, H, I, T = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.tokens
+    eb = M.moe_expert_bytes(H, I)
+    host = torch.empty(E * eb, dtype=torch.uint8).pin_memory()
+    for e, w in enumerate(S.layer_weights(wl, 0)):
+        M.moe_pack_expert(w, H, I, host.data_ptr() + e * eb)
+    slots = torch.empty(E * eb, dtype=torch.uint8, device=dev)
+    pool = M.Pool(1, E, E, H, I, host_experts=host, dev_slots=slots, preload=True)
+    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
+    G = 2  # two distinct input batches, alternated
+    lg = [torch.from_numpy(S.logits(wl, 0, g)).to(dev) for g in range(G)]
+    xb = [torch.from_numpy(S.activations_bf16_bits(wl, 0, g).view(np.int16)).to(dev).view(torch.bfloat16)
+          for g in range(G)]
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    plans = [M.RoutePlan.allocate(T, E, k, device=dev) for _ in range(G)]
+    ws = torch.empty(M.moe_ffn_workspace_bytes(T, k, H, I, M.MOE_PATH_PREFILL), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    ext = dict(enable_timing=True)
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext["external"] = True
+    except TypeError:
+        pass
+    ev = [(torch.cuda.Event(**ext), torch.cuda.Event(**ext), torch.cuda.Event(**ext)) for _ in range(G)]
+
+    def step(g):
+        e0, e1, e2 = ev[g]
+        flush.fill_(g)  # larger than L2: every step starts from a cold L2
+        e0.record(stream)
+        M.moe_route_plan(lg[g], k, plans[g], stream=stream, with_counts_host=False)
+        e1.record(stream)
+        M.moe_expert_ffn(pool, 0, xb[g], plans[g], slot_of, out, ws, path=M.MOE_PATH_PREFILL, stream=stream)
+        e2.record(stream)
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    graphs = []
+    for g in range(G):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(g)
+        graphs.append(gr)
+    for i in range(args.warmup):
+        graphs[i % G].replay()
+    torch.cuda.synchronize()
+    route_ms, ffn_ms = [], []
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    total = 0.0
+    for i in range(args.steps):
+        graphs[i % G].replay()
+        torch.cuda.synchronize()
+        e0, e1, e2 = ev[i % G]
+        route_ms.append(e0.elapsed_time(e1))
+        ffn_ms.append(e1.elapsed_time(e2))
+        total += e0.elapsed_time(e2)
+    clk = clocks.stop()
+    pool.close()
+    return dict(step_ms=total / args.steps, route_ms=route_ms, ffn_ms=ffn_ms, clocks=clk)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -276,12 +346,43 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=4, help="layers per oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=1, choices=[1, 3, 4],
+                    help="1: GPT-OSS decode (default); 3, 4: prefill layers (extra measurement)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (smaller case for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = _dist()
-    wl = S.WORKLOADS[1]
+    wl = S.WORKLOADS[args.workload]
+    if args.workload in (3, 4):
+        import torch
+
+        torch.cuda.set_device(0)
+        from routed_expert_ffn_histogram_gb300 import build as B
+
+        B.build()
+        res = prefill_leg(args, wl)
+        flops = 6.0 * wl.hidden * wl.inter * wl.tokens * wl.top_k
+        ffn_s = statistics.median(res["ffn_ms"]) / 1e3
+        _, bf16_peak, peak_kind = _peaks()
+        tc_peak = bf16_peak * 2.0  # kind::mxf8f6f4 issues at the FP8 rate: 2x the measured bf16 rate
+        achieved = flops / ffn_s / 1e12
+        line = {"metric": METRIC, "value": wl.tokens / (res["step_ms"] / 1e3), "unit": "tokens/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["step_ms"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxf8f6f4->f32",
+                "data": "synthetic",
+                "config": {"workload": wl.name, "hidden": wl.hidden, "inter": wl.inter, "experts": wl.experts,
+                           "top_k": wl.top_k, "tokens": wl.tokens, "l2": "256 MB flush before every step"},
+                "roofline": {"kernel": "prefill expert FFN (MXFP8 quant, gate/up GEMM, down GEMM, combine)",
+                             "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                             "frac": achieved / tc_peak, "peak_kind": peak_kind + " bf16 x 2 (FP8-class rate)",
+                             "traffic": None, "algorithmic_flops_per_launch": flops,
+                             "avg_launch_us": ffn_s * 1e6},
+                "kernels_us": {"route_plan": statistics.median(res["route_ms"]) * 1e3,
+                               "expert_ffn": ffn_s * 1e6},
+                "clocks": res["clocks"]}
+        print(json.dumps(line))
+        return
     if args.layers:
         import dataclasses
 

@@ -316,7 +316,7 @@ int launch_down_nit(const DecodeParams& p, int T, cudaStream_t s) {
 
 size_t decode_workspace_bytes(int T, int k, int H, int I) {
     (void)H;
-    return round_up(size_t(T) * k * I * 2, 256);
+    return 256 + round_up(size_t(T) * k * I * 2, 256);
 }
 
 int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
@@ -324,6 +324,12 @@ int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t 
     if (ws_bytes < decode_workspace_bytes(a.T, a.k, L.H, L.I)) return MOE_ERR_INVALID;
     if (L.H > 4096 || L.I > 4096 * 4) return MOE_ERR_UNSUPPORTED;
     if (a.T == 0) return MOE_OK;
+    // one cooperative kernel per layer when the activations and h fit in
+    // shared memory; otherwise a gate/up launch and a down launch
+    if (decode_fused_smem(a.T, a.k, L.H, L.I) != 0) {
+        const int rc = launch_decode_fused(a, ws, s);
+        if (rc != MOE_ERR_UNSUPPORTED) return rc;
+    }
     DecodeParams p;
     p.slots = a.slots;
     p.expert_bytes = a.expert_bytes;
@@ -339,7 +345,7 @@ int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t 
     p.ids = a.ids;
     p.w = a.w;
     p.slot_of = a.slot_of;
-    p.h = reinterpret_cast<uint16_t*>(ws);
+    p.h = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + 256);
     p.out = a.out;
     const int nit_gu = (L.H / 32 + 31) / 32;
     int rc;

@@ -23,7 +23,7 @@ inline size_t pad16(size_t x) { return (x + 15) & ~size_t(15); }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // GPU-native packed expert.  Every row stores its K/2 code bytes followed by
-// its K/32 E8M0 scale bytes, padded to a multiple of 16 bytes.  The gate/up
+// its K/32 E8M0 scale bytes, zero-padded to a multiple of 32 bytes.  The gate/up
 // matrix has 2I rows interleaved in chunks of 64: chunk c holds gate rows
 // 64c..64c+63 then up rows 64c..64c+63.  The down matrix (H rows) follows.
 struct Layout {
@@ -37,8 +37,9 @@ struct Layout {
         if (hidden <= 0 || inter <= 0 || hidden % 64 || inter % 64) return false;
         L->H = hidden;
         L->I = inter;
-        L->rs_gu = size_t(hidden) / 2 + pad16(size_t(hidden) / 32);
-        L->rs_d = size_t(inter) / 2 + pad16(size_t(inter) / 32);
+        // rows are multiples of 32 bytes: a TMA rule for the unpacked-FP4 tile type
+        L->rs_gu = round_up(size_t(hidden) / 2 + pad16(size_t(hidden) / 32), 32);
+        L->rs_d = round_up(size_t(inter) / 2 + pad16(size_t(inter) / 32), 32);
         L->d_off = 2 * size_t(inter) * L->rs_gu;
         L->expert_bytes = round_up(L->d_off + size_t(hidden) * L->rs_d, 1024);
         return true;
@@ -80,6 +81,8 @@ struct FfnArgs {
 };
 
 size_t decode_workspace_bytes(int T, int k, int H, int I);
+size_t decode_fused_smem(int T, int k, int H, int I);
+int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s);
 int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 
 size_t prefill_workspace_bytes(int T, int k, int H, int I);

@@ -1,16 +1,549 @@
-// Prefill path of the expert FFN (tcgen05 block-scaled grouped GEMM).
+// Prefill path of the expert FFN: tcgen05 block-scaled grouped GEMM over the
+// per-expert token groups, fed by TMA, accumulating in tensor memory.
+//
+// Source: tinyserve README, "How it works" item 6 -- batched prefill groups
+// tokens by expert and loads each unique expert once; item 2 -- the expert
+// runs directly on its quantised bytes (gate, up, down).  llama.cpp
+// discussion "fixed GPU expert working set with Native CPU miss execution",
+// prefill update -- grouped matrix products over a per-layer unique-expert
+// pack.  Formats: OCP MX v1.0 (E4M3 activations and E2M1 weights, E8M0
+// scale per 32 along K).
+//
+// Per layer call:
+//   1. quant: x (bf16) -> MXFP8, rows gathered in grouped (perm) order;
+//   2. gate/up GEMM: per expert e, rows [offsets[e], offsets[e+1]) of the
+//      grouped activations times the expert's interleaved gate/up matrix;
+//      epilogue h = bf16(silu(g) * u) -> MXFP8 (scale per 32 along I);
+//   3. down GEMM: grouped h times the expert's down matrix -> y (fp32, in
+//      grouped order);
+//   4. combine: out[t] = sum_j w[t][j] * y[inv[t*k+j]] in ascending j.
+//
+// GEMM kernel (persistent, one CTA per SM, 6 warps):
+//   warp 0     TMA producer: 128x128-byte A tile (E4M3) and 128x128-element
+//              B tile (E2M1, unpacked by TMA into the 16-byte-aligned layout
+//              the f8f6f4 MMA reads) per stage, 128-byte swizzle;
+//   warp 1     MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale 1X,
+//              M=128 N=128 K=32, four per stage; scale factors in TMEM;
+//   warps 2-5  epilogue: write the tile's scale factors into TMEM, then read
+//              the fp32 accumulator (tcgen05.ld) and finish the tile.
+// Tiles (expert, 128-row block, 128-column block) are enumerated on the
+// device from the offsets; columns vary fastest so the CTAs working at the
+// same time share an expert's activation rows and weight rows through L2.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
+namespace {
 
-size_t prefill_workspace_bytes(int T, int k, int H, int I) {
-    (void)T; (void)k; (void)H; (void)I;
-    return 0;
+constexpr int kBM = 128;           // rows (tokens) per tile
+constexpr int kBN = 128;           // weight rows per tile
+constexpr int kBK = 128;           // K elements per pipeline stage
+constexpr int kStages = 6;
+constexpr int kThreads = 192;
+constexpr uint32_t kStageBytesA = kBM * kBK;   // E4M3: one byte per element
+constexpr uint32_t kStageBytesB = kBN * kBK;   // E2M1 unpacked: 16 bytes per 16 elements in smem
+constexpr uint32_t kTxBytesB = kBN * kBK / 2;  // ...of which TMA writes the 8 packed bytes per 16
+constexpr uint32_t kTmemCols = 512;
+// Tensor-memory columns: fp32 accumulator [0, 128); scale factors of A and B
+// at 128 and 256, four columns per K stage of 128 (row m of a 128-row
+// operand keeps its stage's four E8M0 bytes in lane m, column base + m/32;
+// byte j belongs to the stage's j-th block of 32 and is picked by the MMA's
+// scale-factor id).
+constexpr uint32_t kColAcc = 0, kColSfa = 128, kColSfb = 256;
+constexpr int kMaxKStages = 32;    // K <= 4096
+constexpr int kMaxExperts = MOE_MAX_EXPERTS;
+
+struct GemmParams {
+    const int32_t* offsets;     // [E+1] grouped row ranges
+    const int32_t* slot_of;     // [E]
+    int E, A, S;
+    int K, KB;                  // reduction length and its 32-blocks
+    int N;                      // weight rows (2I for gate/up, H for down)
+    const uint8_t* a_scales;    // [A][a_sf_stride] E8M0 of the activations
+    int a_sf_stride;
+    const uint8_t* b_base;      // this layer's slots + offset of the weight matrix
+    size_t expert_bytes;
+    size_t b_rs;                // bytes per weight row
+    int b_code_bytes;           // K/2: scales start here in each row
+    int b_sf_bytes;             // pad16(K/32)
+    int mode;                   // 0: gate/up -> SwiGLU -> MXFP8 h; 1: down -> fp32 y
+    int I;                      // mode 0: width of h
+    uint8_t* hq;                // mode 0: [A][I]
+    uint8_t* hs;                // mode 0: [A][hs_stride]
+    int hs_stride;
+    float* y;                   // mode 1: [A][N]
+    uint32_t* err;              // error bits (device word)
+};
+
+struct __align__(1024) Smem {
+    uint8_t a[kStages][kStageBytesA];
+    uint8_t b[kStages][kStageBytesB];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t sf_full;
+    uint64_t acc_full;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int32_t mt_prefix[kMaxExperts + 1];
+    uint32_t n_tiles;
+};
+
+struct Tile {
+    int e, m0, rows, nt;
+};
+
+__device__ __forceinline__ Tile decode_tile(const Smem& sm, const GemmParams& p, int t, int NT) {
+    Tile tl;
+    const int mt = t / NT;
+    tl.nt = t - mt * NT;
+    int lo = 0, hi = p.E;  // largest e with mt_prefix[e] <= mt
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.mt_prefix[mid] <= mt) lo = mid; else hi = mid;
+    }
+    // skip experts with no tiles (equal prefix values)
+    while (lo + 1 < p.E && sm.mt_prefix[lo + 1] <= mt) ++lo;
+    tl.e = lo;
+    const int off = p.offsets[lo];
+    tl.m0 = off + (mt - sm.mt_prefix[lo]) * kBM;
+    tl.rows = min(kBM, p.offsets[lo + 1] - tl.m0);
+    return tl;
 }
 
+__device__ __forceinline__ float e8m0_inv_scale_f(uint32_t sb) {
+    const int ef = 254 - int(sb);
+    return ef > 0 ? __uint_as_float(uint32_t(ef) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t e8m0_from_amax(float amax) {
+    const uint32_t bits = __float_as_uint(amax);
+    const int ef = int((bits >> 23) & 0xffu);
+    if (amax == 0.0f || ef == 0) return 0u;
+    return uint32_t(min(max(ef - 8, 0), 254));
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                       const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile uint32_t* err = p.err;
+
+    // ---- set-up: tile prefix over experts, barriers, tensor memory ----
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < p.E; base += 32) {
+            const int e = base + lane;
+            int v = 0;
+            if (e < p.E) {
+                const int n = p.offsets[e + 1] - p.offsets[e];
+                v = (n + kBM - 1) / kBM;
+            }
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += u;
+            }
+            if (e < p.E) sm.mt_prefix[e] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            sm.mt_prefix[p.E] = carry;
+            const int NT = (p.N + kBN - 1) / kBN;
+            sm.n_tiles = uint32_t(carry) * uint32_t(NT);
+            for (int s = 0; s < kStages; ++s) {
+                tc::mbar_init(&sm.full[s], 1);
+                tc::mbar_init(&sm.empty[s], 1);
+            }
+            tc::mbar_init(&sm.sf_full, 128);
+            tc::mbar_init(&sm.acc_full, 1);
+            tc::mbar_init(&sm.mma_done, 1);
+            tc::fence_barrier_init();
+            tc::tma_prefetch_desc(&map_a);
+            tc::tma_prefetch_desc(&map_b);
+        }
+    } else if (warp == 1) {
+        tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const int NT = (p.N + kBN - 1) / kBN;
+    const int n_tiles = int(sm.n_tiles);
+    const int n_kstages = (p.K + kBK - 1) / kBK;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x) {
+                const Tile tl = decode_tile(sm, p, t, NT);
+                const int slot = p.slot_of[tl.e];
+                if (slot < 0 || slot >= p.S) {
+                    atomicOr(const_cast<uint32_t*>(err), 4u);
+                    break;
+                }
+                for (int ks = 0; ks < n_kstages; ++ks) {
+                    if (!tc::mbar_wait(&sm.empty[stage], phase ^ 1u, err, 1u)) break;
+                    tc::mbar_arrive_expect_tx(&sm.full[stage], kStageBytesA + kTxBytesB);
+                    tc::tma_load_2d(sm.a[stage], &map_a, &sm.full[stage], ks * kBK, tl.m0);
+                    tc::tma_load_3d(sm.b[stage], &map_b, &sm.full[stage], ks * kBK, tl.nt * kBN, slot);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, tphase = 0;
+            for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x) {
+                if (!tc::mbar_wait(&sm.sf_full, tphase, err, 2u)) break;
+                tphase ^= 1u;
+                tc::tc_fence_after();
+                for (int ks = 0; ks < n_kstages; ++ks) {
+                    if (!tc::mbar_wait(&sm.full[stage], phase, err, 2u)) break;
+                    tc::tc_fence_after();
+                    const uint32_t a0 = tc::smem_u32(sm.a[stage]);
+                    const uint32_t b0 = tc::smem_u32(sm.b[stage]);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk) {
+                        const int kb = ks * (kBK / 32) + kk;
+                        if (kb < p.KB) {
+                            const uint32_t idesc = tc::idesc_mxf8f6f4(0, 5, kBM, kBN, kk, kk);
+                            tc::mma_mxf8f6f4(tmem + kColAcc, tc::smem_desc_sw128(a0 + kk * 32),
+                                             tc::smem_desc_sw128(b0 + kk * 32), idesc, tmem + kColSfa + 4 * ks,
+                                             tmem + kColSfb + 4 * ks, (ks | kk) != 0);
+                        }
+                    }
+                    tc::mma_commit(&sm.empty[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                tc::mma_commit(&sm.acc_full);
+            }
+            // all MMAs issued by this CTA have finished before TMEM is freed
+            tc::mma_commit(&sm.mma_done);
+            tc::mbar_wait(&sm.mma_done, 0, err, 16u);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5 = TMEM lane quarters 2,3,0,1) ----------------
+        const int q = warp & 3;
+        const int r = q * 32 + lane;                // tile row == TMEM lane
+        const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+        uint32_t aphase = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+            if (*err) break;
+            const Tile tl = decode_tile(sm, p, t, NT);
+            const int slot = p.slot_of[tl.e];
+            if (slot < 0 || slot >= p.S) break;
+            // scale factors of the tile's activation rows and weight rows -> TMEM:
+            // this thread fills lane r, columns base + 4s + c with the four
+            // bytes of stage s of rows 32c + lane (c = 0..3)
+            {
+                const int nst = (p.KB + 3) / 4;           // K stages (4 bytes each)
+                const int nvec = (p.b_sf_bytes + 15) / 16; // 16-byte chunks per scale row
+                const uint4* as[4];
+                const uint4* bs[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int arow = min(tl.m0 + 32 * c + lane, p.A - 1);
+                    const int brow = min(tl.nt * kBN + 32 * c + lane, p.N - 1);
+                    as[c] = reinterpret_cast<const uint4*>(p.a_scales + (size_t)arow * p.a_sf_stride);
+                    bs[c] = reinterpret_cast<const uint4*>(p.b_base + (size_t)slot * p.expert_bytes +
+                                                           (size_t)brow * p.b_rs + p.b_code_bytes);
+                }
+                for (int v = 0; v < nvec; ++v) {
+                    uint4 xa[4], xb[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        xa[c] = __ldg(as[c] + v);
+                        xb[c] = __ldg(bs[c] + v);
+                    }
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int st = 4 * v + w;
+                        if (st >= nst) break;
+                        const uint32_t* a32[4] = {&xa[0].x, &xa[1].x, &xa[2].x, &xa[3].x};
+                        const uint32_t* b32[4] = {&xb[0].x, &xb[1].x, &xb[2].x, &xb[3].x};
+                        tc::tmem_st_x4(lane_base + kColSfa + 4 * st, a32[0][w], a32[1][w], a32[2][w], a32[3][w]);
+                        tc::tmem_st_x4(lane_base + kColSfb + 4 * st, b32[0][w], b32[1][w], b32[2][w], b32[3][w]);
+                    }
+                }
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sm.sf_full);
+            }
+            if (!tc::mbar_wait(&sm.acc_full, aphase, err, 8u)) break;
+            aphase ^= 1u;
+            tc::tc_fence_after();
+            const bool valid = r < tl.rows;
+            const int m = tl.m0 + r;
+            if (p.mode == 0) {
+                // columns 0..63: gate rows of chunk nt; 64..127: the matching up rows
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t g0[16], g1[16], u0[16], u1[16];
+                    tc::tmem_ld_x16(lane_base + kColAcc + half * 32, g0);
+                    tc::tmem_ld_x16(lane_base + kColAcc + half * 32 + 16, g1);
+                    tc::tmem_ld_x16(lane_base + kColAcc + 64 + half * 32, u0);
+                    tc::tmem_ld_x16(lane_base + kColAcc + 64 + half * 32 + 16, u1);
+                    tc::tmem_ld_wait();
+                    float hv[32];
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float g = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
+                        const float u = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
+                        const float s = g / (1.0f + expf(-g));
+                        const float hb = __bfloat162float(__float2bfloat16_rn(s * u));
+                        hv[j] = hb;
+                        amax = fmaxf(amax, fabsf(hb));
+                    }
+                    if (valid) {
+                        const uint32_t sb = e8m0_from_amax(amax);
+                        const float mul = e8m0_inv_scale_f(sb);
+                        uint32_t wv[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            wv[j] = cvt_e4m3x2(hv[4 * j] * mul, hv[4 * j + 1] * mul) |
+                                    (cvt_e4m3x2(hv[4 * j + 2] * mul, hv[4 * j + 3] * mul) << 16);
+                        const int col = tl.nt * 64 + half * 32;
+                        uint4* dst = reinterpret_cast<uint4*>(p.hq + (size_t)m * p.I + col);
+                        if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0 || m >= p.A || col + 32 > p.I) {
+                            atomicOr(const_cast<uint32_t*>(err), 32u);
+                        } else {
+                            dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                            dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                            p.hs[(size_t)m * p.hs_stride + col / 32] = uint8_t(sb);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < kBN / 16; ++c) {
+                    uint32_t v[16];
+                    tc::tmem_ld_x16(lane_base + kColAcc + c * 16, v);
+                    tc::tmem_ld_wait();
+                    const int n = tl.nt * kBN + c * 16;
+                    if (valid && n < p.N) {
+                        float4* dst = reinterpret_cast<float4*>(p.y + (size_t)m * p.N + n);
+                        if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0 || m >= p.A) {
+                            atomicOr(const_cast<uint32_t*>(err), 32u);
+                            continue;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    }
+                }
+            }
+            tc::tc_fence_before();
+        }
+    }
+
+    // ---- teardown: every role has left its loop ----
+    __syncthreads();
+    if (*err && threadIdx.x == 0) {
+        // after a failure, give tile copies already issued time to land
+        // before the CTA's shared memory is released
+        for (int i = 0; i < 2000; ++i) __nanosleep(100);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- host side -------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiledFn* out) {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    static cudaError_t status = cudaSuccess;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (status == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!fn) return status != cudaSuccess ? cuda_fail(status) : MOE_ERR_UNSUPPORTED;
+    *out = fn;
+    return MOE_OK;
+}
+
+// Activation rows: [rows][K] bytes (E4M3), tile 128 x 128.
+int make_map_act(CUtensorMap* m, const void* base, int K, int rows) {
+    EncodeTiledFn enc;
+    int rc = get_encoder(&enc);
+    if (rc != MOE_OK) return rc;
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(K)};
+    const cuuint32_t box[2] = {uint32_t(kBK), uint32_t(kBM)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+// Weight rows of every slot of a layer: [S][rows][row_bytes] with K E2M1
+// codes at the start of each row, unpacked by TMA into 16-byte-aligned
+// groups of 16.  The inner extent is K rounded up to 128 (a TMA rule for
+// this type); the extra codes come from the row's own scale bytes and are
+// never multiplied (the MMA loop stops at K).
+int make_map_weights(CUtensorMap* m, const void* base, int K, int rows, int slots, size_t row_bytes,
+                     size_t expert_bytes) {
+    EncodeTiledFn enc;
+    int rc = get_encoder(&enc);
+    if (rc != MOE_OK) return rc;
+    const size_t k128 = round_up(size_t(K), 128);
+    if (k128 / 2 > row_bytes || (reinterpret_cast<uintptr_t>(base) & 31)) return MOE_ERR_UNSUPPORTED;
+    const cuuint64_t dims[3] = {cuuint64_t(k128), cuuint64_t(rows), cuuint64_t(slots)};
+    const cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(expert_bytes)};
+    const cuuint32_t box[3] = {uint32_t(kBK), uint32_t(kBN), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+size_t smem_bytes() { return sizeof(Smem) + 1024; }
+
+int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int max_tiles, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != MOE_OK) return rc;
+    if (di.cc_major < 10) return MOE_ERR_UNSUPPORTED;
+    if (smem_bytes() > di.smem_optin) return MOE_ERR_UNSUPPORTED;
+    if (!attr_set[di.device]) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem_bytes()));
+        attr_set[di.device] = true;
+    }
+    const int grid = max(1, min(di.sms, max_tiles));
+    grouped_gemm_tc_kernel<<<grid, kThreads, smem_bytes(), s>>>(ma, mb, p);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+struct PrefillWs {
+    size_t xq, xs, hq, hs, y, err, total;
+    int xs_stride, hs_stride;
+};
+
+PrefillWs prefill_ws(int T, int k, int H, int I) {
+    PrefillWs w;
+    const size_t A = size_t(T) * k;
+    w.xs_stride = int(pad16(size_t(H) / 32));
+    w.hs_stride = int(pad16(size_t(I) / 32));
+    size_t o = 0;
+    w.err = o; o += 256;
+    w.xq = o; o = round_up(o + A * H, 256);
+    w.xs = o; o = round_up(o + A * w.xs_stride, 256);
+    w.hq = o; o = round_up(o + A * I, 256);
+    w.hs = o; o = round_up(o + A * w.hs_stride, 256);
+    w.y = o; o = round_up(o + A * H * 4, 256);
+    w.total = o;
+    return w;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int T, int k, int H, int I) { return prefill_ws(T, k, H, I).total; }
+
 int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
-    (void)a; (void)ws; (void)ws_bytes; (void)s;
-    return MOE_ERR_UNSUPPORTED;
+    const Layout& L = *a.L;
+    const PrefillWs w = prefill_ws(a.T, a.k, L.H, L.I);
+    if (ws_bytes < w.total) return MOE_ERR_INVALID;
+    if (L.H > 4096 || L.I > 4096 || a.E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+    static_assert(kColSfb + 4 * kMaxKStages <= kTmemCols, "tensor-memory columns");
+    if (a.T == 0) return MOE_OK;
+    const int A = a.T * a.k;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint8_t* xq = base + w.xq;
+    uint8_t* xs = base + w.xs;
+    uint8_t* hq = base + w.hq;
+    uint8_t* hs = base + w.hs;
+    float* y = reinterpret_cast<float*>(base + w.y);
+    uint32_t* err = reinterpret_cast<uint32_t*>(base + w.err);
+
+    MOE_CUDA_TRY(cudaMemsetAsync(err, 0, 4, s));
+    MOE_CUDA_TRY(cudaMemsetAsync(xs, 0, size_t(A) * w.xs_stride, s));
+    MOE_CUDA_TRY(cudaMemsetAsync(hs, 0, size_t(A) * w.hs_stride, s));
+    int rc = launch_quant_mxfp8(a.x, L.H, a.perm, a.k, A, xq, xs, w.xs_stride, s);
+    if (rc != MOE_OK) return rc;
+
+    CUtensorMap map_x, map_gu, map_h, map_d;
+    rc = make_map_act(&map_x, xq, L.H, A);
+    if (rc == MOE_OK) rc = make_map_weights(&map_gu, a.slots, L.H, 2 * L.I, a.S, L.rs_gu, a.expert_bytes);
+    if (rc == MOE_OK) rc = make_map_act(&map_h, hq, L.I, A);
+    if (rc == MOE_OK) rc = make_map_weights(&map_d, a.slots + L.d_off, L.I, L.H, a.S, L.rs_d, a.expert_bytes);
+    if (rc != MOE_OK) return rc;
+
+    const int max_mtiles = A / kBM + a.E;
+    GemmParams g{};
+    g.offsets = a.offsets;
+    g.slot_of = a.slot_of;
+    g.E = a.E;
+    g.A = A;
+    g.S = a.S;
+    g.expert_bytes = a.expert_bytes;
+    g.err = err;
+    // gate/up: K = H, N = 2I, epilogue SwiGLU -> MXFP8 h
+    g.K = L.H;
+    g.KB = L.H / 32;
+    g.N = 2 * L.I;
+    g.a_scales = xs;
+    g.a_sf_stride = w.xs_stride;
+    g.b_base = a.slots;
+    g.b_rs = L.rs_gu;
+    g.b_code_bytes = L.H / 2;
+    g.b_sf_bytes = int(pad16(size_t(L.H) / 32));
+    g.mode = 0;
+    g.I = L.I;
+    g.hq = hq;
+    g.hs = hs;
+    g.hs_stride = w.hs_stride;
+    rc = launch_gemm(map_x, map_gu, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
+    if (rc != MOE_OK) return rc;
+    // down: K = I, N = H, epilogue fp32 y in grouped order
+    g.K = L.I;
+    g.KB = L.I / 32;
+    g.N = L.H;
+    g.a_scales = hs;
+    g.a_sf_stride = w.hs_stride;
+    g.b_base = a.slots + L.d_off;
+    g.b_rs = L.rs_d;
+    g.b_code_bytes = L.I / 2;
+    g.b_sf_bytes = int(pad16(size_t(L.I) / 32));
+    g.mode = 1;
+    g.y = y;
+    rc = launch_gemm(map_h, map_d, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
+    if (rc != MOE_OK) return rc;
+    return launch_combine(y, a.w, a.inv, a.T, a.k, L.H, a.out, s);
 }
 
 }  // namespace moe

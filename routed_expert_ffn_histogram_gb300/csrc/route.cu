@@ -82,15 +82,13 @@ __device__ void topk_tile(const float* __restrict__ logits, int T, int E, int k,
             if (lane == j) { sel_v = bv; sel_id = bid; }
             if (lane == 0) atomicAdd(&sm.hist[bid], 1);
         }
-        // softmax over the k selected logits in fp64, summed in rank order
+        // softmax over the k selected logits in fp64: lane j < k evaluates its
+        // own exponential, the sum is folded in rank order, lane j divides
         const double m = (double)__shfl_sync(0xffffffffu, sel_v, 0);
+        const double d = (lane < k) ? exp((double)sel_v - m) : 0.0;
         double sum = 0.0;
-        for (int j = 0; j < k; ++j) {
-            const float vj = __shfl_sync(0xffffffffu, sel_v, j);
-            sum += exp((double)vj - m);
-        }
+        for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, d, j);
         if (lane < k) {
-            const double d = exp((double)sel_v - m);
             ids[(size_t)t * k + lane] = sel_id;
             w[(size_t)t * k + lane] = (float)(d / sum);
         }

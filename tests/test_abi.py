@@ -41,7 +41,7 @@ def test_expert_bytes():
     for H, I in [(2880, 2880), (2048, 768), (256, 512)]:
         eb = M.moe_expert_bytes(H, I)
         canon = 3 * (H * I // 2 + H * I // 32)
-        assert eb % 1024 == 0 and canon <= eb <= canon * 1.05
+        assert eb % 1024 == 0 and canon <= eb <= canon * (1.01 if H >= 2048 else 1.15)
     with pytest.raises(M.MoeError):
         M.moe_expert_bytes(100, 64)
 
@@ -54,8 +54,8 @@ def test_pack_native_layout():
     eb = M.moe_expert_bytes(H, I)
     buf = np.zeros(eb, np.uint8)
     M.moe_pack_expert(w, H, I, buf)
-    rs_gu = H // 2 + ((H // 32 + 15) // 16) * 16
-    rs_d = I // 2 + ((I // 32 + 15) // 16) * 16
+    rs_gu = -(-(H // 2 + ((H // 32 + 15) // 16) * 16) // 32) * 32
+    rs_d = -(-(I // 2 + ((I // 32 + 15) // 16) * 16) // 32) * 32
     for r in [0, 1, 63, 64, 200, I - 1]:
         g = (r // 64) * 128 + r % 64
         row = buf[g * rs_gu:(g + 1) * rs_gu]

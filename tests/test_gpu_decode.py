@@ -60,7 +60,7 @@ def test_decode_tiny():
     ref, it = _oracle_layer(wl, 0, 0, prefill=False)
     assert rel_l2(out, ref) <= DECODE_REL_L2
     assert rel_l2(out, ref) <= 1e-4  # only summation order and rare bf16(h) flips differ
-    h = ws[: wl.tokens * wl.top_k * wl.inter * 2].cpu().numpy().view(np.uint16).reshape(-1, wl.inter)
+    h = ws[256:256 + wl.tokens * wl.top_k * wl.inter * 2].cpu().numpy().view(np.uint16).reshape(-1, wl.inter)
     d = np.abs(h.astype(np.int32) - it["h"].astype(np.int32))
     assert d.max() <= 1 and (d == 0).mean() > 0.999
 
