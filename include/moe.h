@@ -148,6 +148,27 @@ MOE_API int moe_route_plan(const float* logits, int T, int E, int k,
                    int32_t* perm, int32_t* inv, int32_t* counts_host,
                    void* workspace, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route_plan without a workspace argument.  The pages have no
+ * counterpart: this entry exists for callers that cannot allocate device
+ * memory where they route -- code running while a CUDA graph is captured,
+ * engines whose device memory is owned by their own fixed-budget allocator,
+ * decode loops that must not call into the driver's allocator.  The
+ * per-tile histograms use a 64 KB array that the library keeps in device
+ * memory (every GPU that loads the library holds it until exit); nothing is
+ * allocated per call, and no cudaMalloc/cudaFree is ever made.
+ *   Arguments, outputs and results are those of moe_route_plan.
+ *   Limit: T <= 16384 tokens (64 tiles of 256); larger T returns
+ *   MOE_ERR_INVALID before anything is enqueued.
+ *   The first call on a device resolves the array's device address for that
+ *   device (with it current); make that first call before any stream
+ *   capture.  The array needs no clearing (each call overwrites what it
+ *   reads), but all calls share it: calls that can overlap on the GPU race.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+MOE_API int moe_route_plan_noalloc(const float* logits, int T, int E, int k,
+                                   int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                   int32_t* perm, int32_t* inv, int32_t* counts_host,
+                                   moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Expert-slot pool [R2][R4][P1][X1]                                         */
 /* ------------------------------------------------------------------------ */

@@ -25,7 +25,8 @@ from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ER
                    lib, ptr, status_str, stream_handle)
 
 __all__ = [
-    "moe_expert_bytes", "moe_pack_expert", "moe_route_workspace_bytes", "moe_route_plan", "moe_ffn_workspace_bytes",
+    "moe_expert_bytes", "moe_pack_expert", "moe_route_workspace_bytes", "moe_route_plan", "moe_route_plan_noalloc",
+    "moe_ffn_workspace_bytes",
     "moe_expert_ffn", "moe_combine", "moe_quant_mxfp8", "Pool", "RoutePlan", "MoeError", "lib", "status_str",
     "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL",
 ]
@@ -91,6 +92,17 @@ def moe_route_plan(logits, k: int, plan: RoutePlan, stream=None, with_counts_hos
     check("moe_route_plan", lib().moe_route_plan(
         ptr(logits), T, E, k, ptr(plan.ids), ptr(plan.w), ptr(plan.counts), ptr(plan.offsets), ptr(plan.perm),
         ptr(plan.inv), ptr(ch), ptr(plan.workspace), plan.workspace.numel(), stream_handle(stream)))
+
+
+def moe_route_plan_noalloc(logits, k: int, plan: RoutePlan, stream=None, with_counts_host: bool = True) -> None:
+    """moe_route_plan for callers that cannot allocate device memory: the
+    library's own device array replaces the workspace (T <= 16384; calls
+    that overlap on the GPU race on it).  ``plan.workspace`` is not used."""
+    T, E = logits.shape
+    ch = plan.counts_host if with_counts_host else None
+    check("moe_route_plan_noalloc", lib().moe_route_plan_noalloc(
+        ptr(logits), T, E, k, ptr(plan.ids), ptr(plan.w), ptr(plan.counts), ptr(plan.offsets), ptr(plan.perm),
+        ptr(plan.inv), ptr(ch), stream_handle(stream)))
 
 
 def moe_ffn_workspace_bytes(T: int, k: int, hidden: int, inter: int, path: int = MOE_PATH_AUTO) -> int:

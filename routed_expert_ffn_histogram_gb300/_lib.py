@@ -55,6 +55,7 @@ SIGNATURES = {
     "moe_pack_expert": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp]),
     "moe_route_workspace_bytes": (_i32, [_i32, _i32, _i32, _szp]),
     "moe_route_plan": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_route_plan_noalloc": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_pool_create": (_i32, [C.POINTER(MoePoolDesc), C.POINTER(C.c_void_p)]),
     "moe_pool_stage": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _i32]),
     "moe_pool_counters": (_i32, [_vp, _i32, C.POINTER(MoeCounters)]),

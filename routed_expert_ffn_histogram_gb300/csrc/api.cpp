@@ -129,6 +129,20 @@ extern "C" int moe_route_plan(const float* logits, int T, int E, int k, int32_t*
     return MOE_OK;
 }
 
+extern "C" int moe_route_plan_noalloc(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                                      int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                      int32_t* counts_host, moe_stream_t stream) {
+    if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || k > MOE_MAX_TOPK) return MOE_ERR_INVALID;
+    if (!counts || !offsets || (T > 0 && (!logits || !ids || !w || !perm || !inv))) return MOE_ERR_INVALID;
+    if (T > moe::route_noalloc_max_tokens()) return MOE_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = moe::route_plan_noalloc(logits, T, E, k, ids, w, counts, offsets, perm, inv, s);
+    if (rc != MOE_OK) return rc;
+    if (counts_host)
+        MOE_CUDA_TRY(cudaMemcpyAsync(counts_host, counts, sizeof(int32_t) * E, cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+}
+
 static int resolve_path(int path, int T, int k) {
     if (path == MOE_PATH_AUTO) return size_t(T) * k <= MOE_DECODE_MAX_ASSIGN ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
     return path;

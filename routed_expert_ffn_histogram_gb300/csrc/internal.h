@@ -63,6 +63,9 @@ int launch_route_plan(const float* logits, int T, int E, int k, int32_t* ids, fl
                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                       int32_t* tile_hist, int n_tiles, cudaStream_t s);
 int route_tiles(int T, int k);
+int route_plan_noalloc(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s);
+int route_noalloc_max_tokens();
 
 struct FfnArgs {
     const uint8_t* slots;      // base of this layer's slots

@@ -16,6 +16,7 @@
 // fixed by the assignment index, never by the order atomics land in.
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 
@@ -246,5 +247,57 @@ int launch_route_plan(const float* logits, int T, int E, int k, int32_t* ids, fl
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Routing without caller-provided scratch (moe_route_plan_noalloc).
+//
+// Some callers cannot allocate device memory where they route: code running
+// while a CUDA graph is being captured (an allocation there would either be
+// refused or baked into the graph), engines whose device memory is carved
+// up in advance by their own allocator under a fixed budget, and real-time
+// decode loops that must never call into the driver's allocator, which can
+// block or synchronise.  For them the per-tile histograms live in this
+// file-scope device array instead of a workspace.  It holds
+// kNoallocMaxTiles * MOE_MAX_EXPERTS int32 (64 KB), enough for up to
+// kNoallocMaxTiles * 256 = 16384 tokens; every GPU that loads the library
+// keeps it until the process exits.  Its contents need no clearing: each
+// call overwrites every entry it reads.  All calls share it, so calls that
+// can overlap on the GPU (different streams, or different host threads
+// without ordering) race on it.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kNoallocMaxTiles = 64;
+__device__ __align__(256) int32_t g_route_noalloc_scratch[kNoallocMaxTiles * MOE_MAX_EXPERTS];
+
+// Device address of the scratch array on the current device, resolved once
+// per device (with that device current) on the first call made there.
+int noalloc_scratch(int32_t** out) {
+    static std::mutex mu;
+    static int32_t* addr[64] = {};
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_route_noalloc_scratch));
+        addr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = addr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+int route_plan_noalloc(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s) {
+    const int tiles = route_tiles(T, k);
+    if (tiles > kNoallocMaxTiles) return MOE_ERR_INVALID;
+    int32_t* scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != MOE_OK) return rc;
+    return launch_route_plan(logits, T, E, k, ids, w, counts, offsets, perm, inv, scratch, tiles, s);
+}
+
+int route_noalloc_max_tokens() { return kNoallocMaxTiles * kTileTokens; }
 
 }  // namespace moe
