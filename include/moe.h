@@ -278,7 +278,11 @@ MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int pat
  *             2^(floor(log2 amax) - 8), RNE, satfinite) and multiplied on
  *             tcgen05 block-scaled tensor cores, fp32 accumulation.
  *             MOE_PATH_AUTO: decode when T*k <= MOE_DECODE_MAX_ASSIGN.
- *   workspace device, >= moe_ffn_workspace_bytes(), 256-byte aligned
+ *   workspace device, >= moe_ffn_workspace_bytes(), 256-byte aligned.
+ *             Its first 256 bytes hold a grid-barrier word that must be zero
+ *             when the workspace is first used (allocate it zeroed); the
+ *             library leaves it zero after every call.  One workspace must
+ *             not be used by two calls that can run at the same time.
  *   out       device fp32 [T][H], fully overwritten
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16, int T, int k,
@@ -286,6 +290,25 @@ MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16
                    const int32_t* perm, const int32_t* inv, const int32_t* slot_of,
                    int path, void* workspace, size_t ws_bytes, float* out,
                    moe_stream_t stream);
+
+/* One decode step of one layer in a single launch: moe_route_plan followed
+ * by moe_expert_ffn on the decode path, fused [R1][R3][P1].  For small
+ * batches on a pool whose routed experts are resident (no staging between
+ * routing and the experts).  Every CTA ranks the logits itself; the routing
+ * outputs (ids, w, counts, offsets, perm, inv, as moe_route_plan defines
+ * them) are written too.  Results equal moe_route_plan + moe_expert_ffn
+ * (MOE_PATH_DECODE) on the same inputs.
+ *   logits   device fp32 [T][E]; x_bf16 device bf16 [T][H]
+ *   slot_of  device int32 [E]: every routed expert must be resident
+ *   workspace as moe_expert_ffn, MOE_PATH_DECODE (first 256 bytes zeroed
+ *            before first use)
+ * Limits: T*k <= 32.  Errors: MOE_ERR_INVALID, MOE_ERR_STATE,
+ * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API int moe_decode_layer(const moe_pool_t* pool, int layer, const float* logits,
+                             const void* x_bf16, int T, int k, int32_t* ids, float* w,
+                             int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                             const int32_t* slot_of, void* workspace, size_t ws_bytes,
+                             float* out, moe_stream_t stream);
 
 /* Weighted combine of per-assignment expert outputs held in grouped order:
  *   out[t][h] = sum_j w[t][j] * y_perm[inv[t*k+j]][h], j ascending, fp32.

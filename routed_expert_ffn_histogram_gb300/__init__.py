@@ -26,8 +26,8 @@ from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ER
 
 __all__ = [
     "moe_expert_bytes", "moe_pack_expert", "moe_route_workspace_bytes", "moe_route_plan", "moe_route_plan_noalloc",
-    "moe_ffn_workspace_bytes",
-    "moe_expert_ffn", "moe_combine", "moe_quant_mxfp8", "Pool", "RoutePlan", "MoeError", "lib", "status_str",
+    "moe_ffn_workspace_bytes", "alloc_ffn_workspace",
+    "moe_expert_ffn", "moe_decode_layer", "moe_combine", "moe_quant_mxfp8", "Pool", "RoutePlan", "MoeError", "lib", "status_str",
     "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL",
 ]
 
@@ -111,6 +111,15 @@ def moe_ffn_workspace_bytes(T: int, k: int, hidden: int, inter: int, path: int =
     return out.value
 
 
+def alloc_ffn_workspace(T: int, k: int, hidden: int, inter: int, path: int = MOE_PATH_AUTO, device="cuda"):
+    """A zeroed device workspace for moe_expert_ffn (its first bytes hold a
+    grid-barrier word that must start at zero)."""
+    import torch
+
+    n = max(moe_ffn_workspace_bytes(T, k, hidden, inter, path), 256)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def moe_expert_ffn(pool: "Pool", layer: int, x_bf16, plan: RoutePlan, slot_of, out, workspace,
                    path: int = MOE_PATH_AUTO, stream=None) -> None:
     """Routed experts of one layer with the weighted combine (moe_expert_ffn)."""
@@ -120,6 +129,17 @@ def moe_expert_ffn(pool: "Pool", layer: int, x_bf16, plan: RoutePlan, slot_of, o
         ptr(plan.perm), ptr(plan.inv), ptr(slot_of), path, ptr(workspace),
         workspace.numel() * workspace.element_size() if workspace is not None else 0, ptr(out),
         stream_handle(stream)))
+
+
+def moe_decode_layer(pool: "Pool", layer: int, logits, x_bf16, plan: RoutePlan, slot_of, out, workspace,
+                     stream=None) -> None:
+    """Routing + routed experts of one decode step in one launch
+    (moe_decode_layer); fills ``plan`` like moe_route_plan."""
+    T = x_bf16.shape[0]
+    check("moe_decode_layer", lib().moe_decode_layer(
+        pool.handle, layer, ptr(logits), ptr(x_bf16), T, plan.k, ptr(plan.ids), ptr(plan.w), ptr(plan.counts),
+        ptr(plan.offsets), ptr(plan.perm), ptr(plan.inv), ptr(slot_of), ptr(workspace),
+        workspace.numel() * workspace.element_size(), ptr(out), stream_handle(stream)))
 
 
 def moe_combine(y_perm, w, inv, out, stream=None) -> None:

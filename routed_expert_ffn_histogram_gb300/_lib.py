@@ -69,6 +69,8 @@ SIGNATURES = {
     "moe_ffn_workspace_bytes": (_i32, [_i32, _i32, _i32, _i32, _i32, _szp]),
     "moe_expert_ffn": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp,
                               _vp]),
+    "moe_decode_layer": (_i32, [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                _vp]),
     "moe_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "moe_quant_mxfp8": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _vp]),
 }

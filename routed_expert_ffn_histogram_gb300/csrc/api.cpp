@@ -199,6 +199,48 @@ extern "C" int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_b
     return moe::launch_prefill_ffn(a, workspace, ws_bytes, s);
 }
 
+extern "C" int moe_decode_layer(const moe_pool_t* pool, int layer, const float* logits, const void* x_bf16, int T,
+                                int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                int32_t* inv, const int32_t* slot_of, void* workspace, size_t ws_bytes, float* out,
+                                moe_stream_t stream) {
+    if (!pool) return MOE_ERR_INVALID;
+    const moe_pool_desc& d = *moe::pool_desc(pool);
+    const Layout& L = *moe::pool_layout(pool);
+    if (d.dry_run || !d.dev_slots) return MOE_ERR_STATE;
+    if (layer < 0 || layer >= d.layers || T < 1 || k < 1 || k > d.experts || k > MOE_MAX_TOPK || T * k > 32)
+        return MOE_ERR_INVALID;
+    if (!logits || !x_bf16 || !ids || !w || !counts || !offsets || !perm || !inv || !slot_of || !out)
+        return MOE_ERR_INVALID;
+    size_t need = 0;
+    moe_ffn_workspace_bytes(T, k, d.hidden, d.inter, MOE_PATH_DECODE, &need);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256) || !aligned(x_bf16, 16)) return MOE_ERR_INVALID;
+    moe::FfnArgs a;
+    a.slots = static_cast<const uint8_t*>(d.dev_slots) + size_t(layer) * d.slots_per_layer * L.expert_bytes;
+    a.expert_bytes = L.expert_bytes;
+    a.S = d.slots_per_layer;
+    a.E = d.experts;
+    a.L = &L;
+    a.x = static_cast<const uint16_t*>(x_bf16);
+    a.T = T;
+    a.k = k;
+    a.ids = ids;
+    a.w = w;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.inv = inv;
+    a.slot_of = slot_of;
+    a.out = out;
+    moe::RouteOut ro;
+    ro.logits = logits;
+    ro.ids = ids;
+    ro.w = w;
+    ro.counts = counts;
+    ro.offsets = offsets;
+    ro.perm = perm;
+    ro.inv = inv;
+    return moe::launch_decode_layer(a, ro, workspace, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int moe_combine(const float* y_perm, const float* w, const int32_t* inv, int T, int k, int H,
                            float* out, moe_stream_t stream) {
     if (T < 0 || k < 1 || k > MOE_MAX_TOPK || H < 1) return MOE_ERR_INVALID;

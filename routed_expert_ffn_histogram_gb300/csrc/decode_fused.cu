@@ -12,31 +12,42 @@
 // (every product exact in fp32), fp32 sums, SwiGLU in fp32 rounded to bf16,
 // down product on bf16(h), combine sum_j w_j * y_j in ascending j.
 //
-// Shape: one CTA per SM (or as many as fit), 16 warps each, all co-resident
-// (cooperative launch).
-//   phase 1  every warp takes (token, expert, row) items: the gate row and
-//            the up row (64 rows apart in the packed layout), one 16-byte
-//            load = one MX block per lane, x staged once per CTA in shared
-//            memory as fp32 (XOR-swizzled 16-byte chunks, conflict-free),
-//            products accumulated with packed fp32x2 FMAs; lane 0 writes
-//            bf16(silu(g) * u).  Meanwhile each CTA asks L2 to prefetch its
-//            share of the routed experts' down matrices, so HBM stays busy
-//            across the phase boundary and phase 2 reads from L2.
+// Shape: one CTA per SM, 24 warps each, all co-resident (cooperative
+// launch).  Each CTA owns a contiguous range of (assignment, row) items of
+// the gate/up product and a contiguous range of output rows of the down
+// product, and first asks L2 to prefetch exactly those weight bytes
+// (cp.async.bulk.prefetch), gate/up first: HBM then streams the layer's
+// experts at full rate whatever the warps are doing, and the warps' loads
+// meet the data in L2.
+//   phase 1  a warp takes one item at a time: the gate row and the up row
+//            (64 rows apart in the packed layout), one 16-byte load = one MX
+//            block per lane; x is staged once per CTA in shared memory as
+//            f16 scaled per 32-block by a power of two (exact for every
+//            value within 2^-31 of the block maximum) in XOR-swizzled
+//            16-byte chunks; E2M1 pairs become f16x2 by hardware conversion
+//            and multiply-add into fp32 (products exact); lane 0 writes
+//            bf16(silu(g) * u).
 //   barrier  bounded grid barrier (arrival counter zeroed before launch).
-//   phase 2  h of a token staged per CTA (bf16, swizzled); every warp takes
-//            output rows, reads that row of all k experts, and folds
+//   phase 2  h of a token staged per CTA the same way; a warp takes an
+//            output row, reads that row of all k experts, and folds
 //            w_j * y_j in rank order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "internal.h"
+#include "route_warp.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 768;
+constexpr int kGroup = 16;             // row pairs per ring slot (one bulk copy each for gate and up)
+constexpr int kThreads = 32 * (kGroup + 1);  // warp 0: copy producer; warps 1..16: one row pair each
+constexpr int kMaxSlots = 16;
+constexpr int kMaxRows2 = 64;          // output rows per CTA in phase 2
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kBarrierLimit = 1u << 23;  // polls (~1 s) before the grid barrier gives up
 
@@ -81,20 +92,21 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t word, uint32_t (&h)[4]) {
 __device__ __forceinline__ int hswz(int b, int q) { return b * 4 + (q ^ ((b >> 1) & 3)); }
 
 // Dot of one MX block (16 code bytes = 32 elements) with staged block b.
+// Eight independent accumulation chains keep the FMA latency hidden.
 __device__ __forceinline__ float block_dot_f16(const uint4 c, const uint4* __restrict__ xs, int b) {
     const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    float a0 = 0.f, a1 = 0.f;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint4 xv = xs[hswz(b, q)];
         uint32_t wv[4];
         e2m1x8_f16(cw[q], wv);
-        fma2_f16_f32(a0, a1, wv[0], xv.x);
-        fma2_f16_f32(a0, a1, wv[1], xv.y);
-        fma2_f16_f32(a0, a1, wv[2], xv.z);
-        fma2_f16_f32(a0, a1, wv[3], xv.w);
+        fma2_f16_f32(a[0], a[1], wv[0], xv.x);
+        fma2_f16_f32(a[2], a[3], wv[1], xv.y);
+        fma2_f16_f32(a[4], a[5], wv[2], xv.z);
+        fma2_f16_f32(a[6], a[7], wv[3], xv.w);
     }
-    return a0 + a1;
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
 // Two rows (gate, up) against the same staged block b.
@@ -102,24 +114,24 @@ __device__ __forceinline__ void block_dot2_f16(const uint4 cg, const uint4 cu, c
                                                int b, float& dg, float& du) {
     const uint32_t wg[4] = {cg.x, cg.y, cg.z, cg.w};
     const uint32_t wu[4] = {cu.x, cu.y, cu.z, cu.w};
-    float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
+    float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint4 xv = xs[hswz(b, q)];
         uint32_t fg[4], fu[4];
         e2m1x8_f16(wg[q], fg);
         e2m1x8_f16(wu[q], fu);
-        fma2_f16_f32(g0, g1, fg[0], xv.x);
-        fma2_f16_f32(u0, u1, fu[0], xv.x);
-        fma2_f16_f32(g0, g1, fg[1], xv.y);
-        fma2_f16_f32(u0, u1, fu[1], xv.y);
-        fma2_f16_f32(g0, g1, fg[2], xv.z);
-        fma2_f16_f32(u0, u1, fu[2], xv.z);
-        fma2_f16_f32(g0, g1, fg[3], xv.w);
-        fma2_f16_f32(u0, u1, fu[3], xv.w);
+        fma2_f16_f32(g[0], g[1], fg[0], xv.x);
+        fma2_f16_f32(u[0], u[1], fu[0], xv.x);
+        fma2_f16_f32(g[2], g[3], fg[1], xv.y);
+        fma2_f16_f32(u[2], u[3], fu[1], xv.y);
+        fma2_f16_f32(g[0], g[1], fg[2], xv.z);
+        fma2_f16_f32(u[0], u[1], fu[2], xv.z);
+        fma2_f16_f32(g[2], g[3], fg[3], xv.w);
+        fma2_f16_f32(u[2], u[3], fu[3], xv.w);
     }
-    dg = g0 + g1;
-    du = u0 + u1;
+    dg = (g[0] + g[1]) + (g[2] + g[3]);
+    du = (u[0] + u[1]) + (u[2] + u[3]);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -178,8 +190,19 @@ struct FusedParams {
     const int32_t* slot_of;
     uint16_t* h;       // bf16 [T*k][I]
     float* out;        // fp32 [T][H]
-    unsigned* bar;     // [0] arrivals (zeroed before launch), [1] error bits
+    unsigned* bar;     // [0] arrivals (zero when idle), [1] generation, [2] error bits
+    // fused routing (logits != nullptr): the kernel selects the experts itself
+    // and CTA 0 writes the routing outputs below
+    const float* logits;
+    int32_t* r_ids;
+    float* r_w;
+    int32_t* r_counts;
+    int32_t* r_offsets;
+    int32_t* r_perm;
+    int32_t* r_inv;
 };
+
+constexpr int kMaxAssign = MOE_DECODE_MAX_ASSIGN;
 
 __device__ __forceinline__ const uint8_t* expert_of(const FusedParams& p, int a) {
     const int e = p.ids[a];
@@ -189,22 +212,46 @@ __device__ __forceinline__ const uint8_t* expert_of(const FusedParams& p, int a)
     return p.slots + (size_t)s * p.expert_bytes;
 }
 
-__device__ bool grid_barrier(unsigned* bar, unsigned target, int* ok_smem) {
+// Per-CTA table of the routed assignments, filled once so the work loops
+// never wait on dependent loads of ids / slot_of / w.
+struct AssignTable {
+    int slot_of[MOE_MAX_EXPERTS];
+    const uint8_t* base[kMaxAssign];
+    float w[kMaxAssign];
+    float sel_v[kMaxAssign];
+    int id[kMaxAssign];
+};
+
+// Sense-reversing grid barrier in the workspace's first bytes: bar[0]
+// counts arrivals and is reset to zero by the last arriver, which then
+// advances the generation bar[1] that the others wait on; bar[2] collects
+// error bits.  bar[0] must be zero when the workspace is first used; the
+// kernel leaves it zero.  A wait that runs out (about one second) sets an
+// error bit instead of spinning on.
+__device__ bool grid_barrier(unsigned* bar, unsigned G, int* ok_smem) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        atomicAdd(bar, 1u);
+        unsigned gen;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(bar + 1) : "memory");
+        const unsigned arrived = atomicAdd(bar, 1u);
         int ok = 1;
-        for (uint32_t i = 0;; ++i) {
-            unsigned v;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
-            if (v >= target) break;
-            if (i >= kBarrierLimit) {
-                atomicOr(bar + 1, 1u);
-                ok = 0;
-                break;
+        if (arrived == G - 1) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(bar + 1), "r"(gen + 1) : "memory");
+        } else {
+            for (uint32_t i = 0;; ++i) {
+                unsigned v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar + 1) : "memory");
+                if (v != gen) break;
+                if (i >= kBarrierLimit) {
+                    atomicOr(bar + 2, 1u);
+                    ok = 0;
+                    break;
+                }
+                if (i > 256) __nanosleep(32);
             }
-            __nanosleep(64);
         }
         __threadfence();
         *ok_smem = ok;
@@ -213,170 +260,309 @@ __device__ bool grid_barrier(unsigned* bar, unsigned target, int* ok_smem) {
     return *ok_smem != 0;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+    if (bytes >= 16)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(uint32_t(bytes & ~size_t(15)))
+                     : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            tc::smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+
 template <int NG, int ND>
-__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p) {
-    extern __shared__ uint4 sm4[];
+__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p, int slots, int ring_off) {
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int ok_smem;
+    __shared__ AssignTable tab;
+    __shared__ __align__(8) uint64_t full[kMaxSlots];
+    __shared__ __align__(8) uint64_t empty[kMaxSlots];
+    __shared__ __align__(8) uint64_t down_full;
+    __shared__ float ypart[kMaxRows2][kMaxAssign];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x;
     const int A = p.T * p.k;
-
-    // L2 prefetch of this CTA's share of the routed down matrices
-    if (threadIdx.x == 0) {
-        const size_t dbytes = (size_t)p.H * p.rs_d;
-        const size_t total = (size_t)A * dbytes;
-        size_t lo = (total * blockIdx.x / G) & ~size_t(15), hi = (total * (blockIdx.x + 1) / G) & ~size_t(15);
-        if (blockIdx.x + 1 == (unsigned)G) hi = total;
-        while (lo < hi) {
-            const int a = int(lo / dbytes);
-            const size_t in = lo - (size_t)a * dbytes;
-            const size_t n = min(min(hi - lo, dbytes - in), size_t(1) << 16);
-            const uint8_t* base = expert_of(p, a);
-            if (base != nullptr && n >= 16)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + p.d_off + in),
-                             "r"(uint32_t(n & ~size_t(15)))
-                             : "memory");
-            lo += n;
+    volatile uint32_t* err = p.bar + 2;
+    if (p.logits != nullptr) {
+        // routing in every CTA: warp 0 ranks each token's logits while the
+        // other warps fetch the slot map
+        if (warp == 0) {
+            for (int t = 0; t < p.T; ++t) {
+                float sv;
+                int sid;
+                const float* row = p.logits + (size_t)t * p.E;
+                if (p.E <= 32) topk_warp<1>(row, p.E, p.k, sv, sid);
+                else if (p.E <= 64) topk_warp<2>(row, p.E, p.k, sv, sid);
+                else if (p.E <= 128) topk_warp<4>(row, p.E, p.k, sv, sid);
+                else topk_warp<8>(row, p.E, p.k, sv, sid);
+                if (lane < p.k) {
+                    tab.id[t * p.k + lane] = sid;
+                    tab.sel_v[t * p.k + lane] = sv;
+                }
+            }
+        } else {
+            for (int e = threadIdx.x - 32; e < p.E; e += kThreads - 32) tab.slot_of[e] = p.slot_of[e];
+        }
+        __syncthreads();
+        for (int a = threadIdx.x; a < A; a += kThreads) {
+            const int e = tab.id[a];
+            const int sl = (e >= 0 && e < p.E) ? tab.slot_of[e] : -1;
+            tab.base[a] = (sl >= 0 && sl < p.S) ? p.slots + (size_t)sl * p.expert_bytes : nullptr;
+        }
+    } else {
+        for (int a = threadIdx.x; a < A; a += kThreads) {
+            tab.base[a] = expert_of(p, a);
+            tab.w[a] = p.w[a];
         }
     }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < slots; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], kGroup);
+        }
+        tc::mbar_init(&down_full, 1);
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
 
-    // ---- phase 1: gate/up + SwiGLU ----
+    // This CTA's work: a contiguous range of groups of kGroup (assignment,
+    // row) gate/up items -- kGroup consecutive gate rows, and the matching up
+    // rows, are contiguous in the packed layout -- and a contiguous range of
+    // output rows for the down product.
+    const int groups = A * p.I / kGroup;
+    const int perg = (groups + G - 1) / G;
+    const int g0 = min(groups, (int)blockIdx.x * perg), g1 = min(groups, g0 + perg);
+    const int per2 = (p.H + G - 1) / G;
+    const int r0 = min(p.H, (int)blockIdx.x * per2), r1 = min(p.H, r0 + per2);
     const int nbx = p.H / 32;
-    {
-        uint4* xs = sm4;
-        int* xe = reinterpret_cast<int*>(sm4 + (size_t)p.T * nbx * 4);
-        for (int c = threadIdx.x; c < p.T * nbx; c += kThreads) {
+    const size_t row_bytes = p.rs_gu;
+    const size_t slot_bytes = 2 * kGroup * row_bytes;
+    uint8_t* ring = smem + ring_off;
+
+    if (warp == 0) {
+        // ---- producer: the down rows this CTA needs go to L2 first; then
+        //      gate/up rows stream through the ring, kGroup pairs per slot ----
+        if (lane == 0) {
+            if (r1 > r0)
+                for (int a = 0; a < A; ++a) {
+                    const uint8_t* eb = tab.base[a];
+                    if (eb != nullptr) prefetch_l2(eb + p.d_off + (size_t)r0 * p.rs_d, size_t(r1 - r0) * p.rs_d);
+                }
+            for (int n = 0; g0 + n < g1; ++n) {
+                const int slot = n % slots;
+                const uint32_t phase = uint32_t(n / slots) & 1u;
+                if (!tc::mbar_wait(&empty[slot], phase ^ 1u, err, 4u)) break;
+                const int it = (g0 + n) * kGroup;
+                const int a = it / p.I, r = it - a * p.I;
+                const uint8_t* eb = tab.base[a];
+                if (eb != nullptr) {
+                    const uint8_t* g = eb + Layout::gate_row(r) * p.rs_gu;
+                    tc::mbar_arrive_expect_tx(&full[slot], uint32_t(slot_bytes));
+                    bulk_copy_g2s(ring + (size_t)slot * slot_bytes, g, uint32_t(kGroup * row_bytes), &full[slot]);
+                    bulk_copy_g2s(ring + (size_t)slot * slot_bytes + kGroup * row_bytes, g + 64 * p.rs_gu,
+                                  uint32_t(kGroup * row_bytes), &full[slot]);
+                } else {
+                    tc::mbar_arrive(&full[slot]);
+                }
+            }
+            // once every slot is released, this CTA's down rows of all
+            // assignments are copied into the ring: they land while the grid
+            // barrier is in progress, and phase 2 reads shared memory only.
+            const int issued = g1 - g0;
+            bool free_all = true;
+            for (int n = issued; n < issued + slots && free_all; ++n)
+                free_all = tc::mbar_wait(&empty[n % slots], (uint32_t(n / slots) & 1u) ^ 1u, err, 4u);
+            const size_t dbytes = size_t(r1 - r0) * p.rs_d;
+            if (free_all && r1 > r0) {
+                tc::mbar_arrive_expect_tx(&down_full, uint32_t(dbytes * A));
+                for (int a = 0; a < A; ++a) {
+                    const uint8_t* eb = tab.base[a];
+                    const uint8_t* src = eb != nullptr ? eb + p.d_off + (size_t)r0 * p.rs_d : nullptr;
+                    if (src != nullptr) bulk_copy_g2s(ring + (size_t)a * dbytes, src, uint32_t(dbytes), &down_full);
+                    else asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(&down_full)),
+                                      "r"(uint32_t(dbytes)) : "memory");
+                }
+            } else {
+                tc::mbar_arrive(&down_full);
+            }
+        }
+    } else {
+        // ---- consumers: warp w computes row pair w - 1 of every slot ----
+        uint4* xs = reinterpret_cast<uint4*>(smem);
+        int* xe = reinterpret_cast<int*>(smem + (size_t)p.T * nbx * 64);
+        for (int c = threadIdx.x - 32; c < p.T * nbx; c += kThreads - 32) {
             const int t = c / nbx, b = c - t * nbx;
             stage_block_f16(p.x + (size_t)t * p.H, xs + (size_t)t * nbx * 4, b, xe + t * nbx);
         }
-        __syncthreads();
-        const int items = A * p.I;
-        for (int item = blockIdx.x * kWarps + warp; item < items; item += G * kWarps) {
-            const int a = item / p.I, r = item - a * p.I;
-            const int t = a / p.k;
-            const uint8_t* eb = expert_of(p, a);
-            if (eb == nullptr) {
+        asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+        if (p.logits != nullptr && warp == 1) {
+            // softmax weights (needed only by phase 2), computed while the first
+            // copies are in flight; CTA 0 also writes the routing outputs
+            int my_id = MOE_MAX_EXPERTS;
+            for (int t = 0; t < p.T; ++t) {
+                const int a0 = t * p.k;
+                const float sv = lane < p.k ? tab.sel_v[a0 + lane] : 0.0f;
+                const float wv = softmax_lane(sv, p.k);
+                if (lane < p.k) tab.w[a0 + lane] = wv;
+            }
+            __syncwarp();
+            if (blockIdx.x == 0) {
+                if (lane < A) {
+                    my_id = tab.id[lane];
+                    p.r_ids[lane] = my_id;
+                    p.r_w[lane] = tab.w[lane];
+                }
+                plan_warp(my_id, A, p.E, p.r_counts, p.r_offsets, p.r_perm, p.r_inv);
+            }
+        }
+        const int j = warp - 1;
+        for (int n = 0; g0 + n < g1; ++n) {
+            const int slot = n % slots;
+            const uint32_t phase = uint32_t(n / slots) & 1u;
+            const bool got = tc::mbar_wait(&full[slot], phase, err, 8u);
+            const int it = (g0 + n) * kGroup + j;
+            const int a = it / p.I, r = it - a * p.I;
+            const uint8_t* eb = tab.base[a];
+            if (!got || eb == nullptr) {
                 if (lane == 0) p.h[(size_t)a * p.I + r] = 0x7fc0;
-                continue;
-            }
-            const uint8_t* g = eb + Layout::gate_row(r) * p.rs_gu;
-            const uint8_t* u = g + 64 * p.rs_gu;
-            uint4 cg[NG], cu[NG];
-            int sg[NG], su[NG];
+            } else {
+                const uint8_t* g = ring + (size_t)slot * slot_bytes + (size_t)j * row_bytes;
+                const uint8_t* u = g + kGroup * row_bytes;
+                const int t = a / p.k;
+                const uint4* xt = xs + (size_t)t * nbx * 4;
+                const int* et = xe + t * nbx;
+                float ag = 0.0f, au = 0.0f;
 #pragma unroll
-            for (int i = 0; i < NG; ++i) {
-                const int b = lane + 32 * i;
-                if (b < nbx) {
-                    cg[i] = ld_stream(g + 16 * b);
-                    cu[i] = ld_stream(u + 16 * b);
-                    sg[i] = __ldg(g + p.H / 2 + b);
-                    su[i] = __ldg(u + p.H / 2 + b);
+                for (int i = 0; i < NG; ++i) {
+                    const int b = lane + 32 * i;
+                    if (b < nbx) {
+                        const uint4 cg = *reinterpret_cast<const uint4*>(g + 16 * b);
+                        const uint4 cu = *reinterpret_cast<const uint4*>(u + 16 * b);
+                        const int e = et[b];
+                        float dg, du;
+                        block_dot2_f16(cg, cu, xt, b, dg, du);
+                        ag = fmaf(dg, pow2_biased(int(g[p.H / 2 + b]) + e), ag);
+                        au = fmaf(du, pow2_biased(int(u[p.H / 2 + b]) + e), au);
+                    }
+                }
+                ag = warp_sum(ag);
+                au = warp_sum(au);
+                if (lane == 0) {
+                    const float silu = ag / (1.0f + expf(-ag));
+                    const __nv_bfloat16 hv = __float2bfloat16_rn(silu * au);
+                    p.h[(size_t)a * p.I + r] = *reinterpret_cast<const uint16_t*>(&hv);
                 }
             }
-            const uint4* xt = xs + (size_t)t * nbx * 4;
-            const int* et = xe + t * nbx;
-            float ag = 0.0f, au = 0.0f;
-#pragma unroll
-            for (int i = 0; i < NG; ++i) {
-                const int b = lane + 32 * i;
-                if (b < nbx) {
-                    float dg, du;
-                    block_dot2_f16(cg[i], cu[i], xt, b, dg, du);
-                    const int e = et[b];
-                    ag = fmaf(dg, pow2_biased(sg[i] + e), ag);
-                    au = fmaf(du, pow2_biased(su[i] + e), au);
-                }
-            }
-            ag = warp_sum(ag);
-            au = warp_sum(au);
-            if (lane == 0) {
-                const float silu = ag / (1.0f + expf(-ag));
-                const __nv_bfloat16 hv = __float2bfloat16_rn(silu * au);
-                p.h[(size_t)a * p.I + r] = *reinterpret_cast<const uint16_t*>(&hv);
-            }
+            __syncwarp();
+            if (lane == 0 && got) tc::mbar_arrive(&empty[slot]);
         }
     }
 
-    const bool ok = grid_barrier(p.bar, (unsigned)G, &ok_smem);
+    const bool ok0 = grid_barrier(p.bar, (unsigned)G, &ok_smem);
+    const bool ok = ok0 && tc::mbar_wait(&down_full, 0, err, 16u);
 
-    // ---- phase 2: down + weighted combine ----
-    uint4* hs = sm4;
+    // ---- phase 2: down + weighted combine (rows prefetched into L2) ----
+    // Items are (row, expert) pairs; y of each lands in shared memory and
+    // one pass per row folds w_j * y_j in rank order.
+    constexpr int kWarpsAll = kThreads / 32;
+    uint4* hs = reinterpret_cast<uint4*>(smem);
     const int nbh = p.I / 32;
-    int* he = reinterpret_cast<int*>(sm4 + (size_t)p.k * nbh * 4);
+    int* he = reinterpret_cast<int*>(smem + (size_t)p.k * nbh * 64);
+    const int nrows = r1 - r0;
     for (int t = 0; t < p.T; ++t) {
         __syncthreads();
         for (int c = threadIdx.x; c < p.k * nbh; c += kThreads) {
-            const int j = c / nbh, b = c - j * nbh;
-            stage_block_f16(p.h + ((size_t)t * p.k + j) * p.I, hs + (size_t)j * nbh * 4, b, he + j * nbh);
+            const int jj = c / nbh, b = c - jj * nbh;
+            stage_block_f16(p.h + ((size_t)t * p.k + jj) * p.I, hs + (size_t)jj * nbh * 4, b, he + jj * nbh);
         }
         __syncthreads();
-        for (int r = blockIdx.x * kWarps + warp; r < p.H; r += G * kWarps) {
-            float out = 0.0f;
-            bool bad = !ok;
-            for (int j0 = 0; j0 < p.k && !bad; j0 += 2) {
-                uint4 c[2][ND];
-                int sc[2][ND];
-                const uint8_t* rows[2];
+        const int items2 = nrows * p.k;
+        for (int q0 = warp * 2; q0 < items2; q0 += kWarpsAll * 2) {
+            uint4 c[2][ND];
+            int sc[2][ND];
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int j = j0 + jj;
-                    rows[jj] = nullptr;
-                    if (j < p.k) {
-                        const uint8_t* eb = expert_of(p, t * p.k + j);
-                        if (eb == nullptr) bad = true;
-                        else rows[jj] = eb + p.d_off + (size_t)r * p.rs_d;
-                    }
-                    if (rows[jj] != nullptr) {
+            for (int u2 = 0; u2 < 2; ++u2) {
+                const int q = q0 + u2;
+                if (q >= items2) break;
+                const int rr = q / p.k, jj = q % p.k;
+                if (tab.base[t * p.k + jj] == nullptr || !ok) continue;
+                const uint8_t* row = ring + (size_t)(t * p.k + jj) * nrows * p.rs_d + (size_t)rr * p.rs_d;
 #pragma unroll
-                        for (int i = 0; i < ND; ++i) {
-                            const int b = lane + 32 * i;
-                            if (b < nbh) {
-                                c[jj][i] = __ldg(reinterpret_cast<const uint4*>(rows[jj] + 16 * b));
-                                sc[jj][i] = __ldg(rows[jj] + p.I / 2 + b);
-                            }
-                        }
+                for (int i = 0; i < ND; ++i) {
+                    const int b = lane + 32 * i;
+                    if (b < nbh) {
+                        c[u2][i] = *reinterpret_cast<const uint4*>(row + 16 * b);
+                        sc[u2][i] = row[p.I / 2 + b];
                     }
                 }
+            }
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    if (rows[jj] == nullptr) continue;
-                    const int j = j0 + jj;
-                    const uint4* hj = hs + (size_t)j * nbh * 4;
-                    const int* ej = he + j * nbh;
+            for (int u2 = 0; u2 < 2; ++u2) {
+                const int q = q0 + u2;
+                if (q >= items2) break;
+                const int jj = q % p.k;
+                float y = __int_as_float(0x7fc00000);
+                if (tab.base[t * p.k + jj] != nullptr && ok) {
+                    const uint4* hj = hs + (size_t)jj * nbh * 4;
+                    const int* ej = he + jj * nbh;
                     float acc = 0.0f;
 #pragma unroll
                     for (int i = 0; i < ND; ++i) {
                         const int b = lane + 32 * i;
-                        if (b < nbh) {
-                            acc = fmaf(block_dot_f16(c[jj][i], hj, b), pow2_biased(sc[jj][i] + ej[b]), acc);
-                        }
+                        if (b < nbh)
+                            acc = fmaf(block_dot_f16(c[u2][i], hj, b), pow2_biased(sc[u2][i] + ej[b]), acc);
                     }
-                    const float y = warp_sum(acc);
-                    out = __fadd_rn(out, __fmul_rn(p.w[t * p.k + j], y));
+                    y = warp_sum(acc);
                 }
+                if (lane == 0) ypart[q / p.k][jj] = y;
             }
-            if (lane == 0) p.out[(size_t)t * p.H + r] = bad ? __int_as_float(0x7fc00000) : out;
+        }
+        __syncthreads();
+        for (int q = threadIdx.x; q < nrows; q += kThreads) {
+            float out = 0.0f;
+            for (int jj = 0; jj < p.k; ++jj) out = __fadd_rn(out, __fmul_rn(tab.w[t * p.k + jj], ypart[q][jj]));
+            p.out[(size_t)t * p.H + r0 + q] = out;
         }
     }
 }
 
 }  // namespace
 
-// Shared memory the fused kernel needs, or 0 if the shape does not fit it.
-size_t decode_fused_smem(int T, int k, int H, int I) {
+// Shared memory of the fused kernel: the activation staging (phase 1) or
+// the h staging (phase 2), then the copy ring of gate/up row pairs.
+static size_t staging_bytes(int T, int k, int H, int I) {
     const size_t x = size_t(T) * H * 2 + size_t(T) * (H / 32) * 4;
     const size_t h = size_t(k) * I * 2 + size_t(k) * (I / 32) * 4;
-    const size_t s = x > h ? x : h;
-    return s <= 96 * 1024 ? s : 0;
+    return round_up(x > h ? x : h, 128);
 }
 
-int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s) {
+size_t decode_fused_smem(int T, int k, int H, int I) {
+    Layout L;
+    if (!Layout::make(H, I, &L) || T * k > kMaxAssign || I % kGroup) return 0;
+    if (k * ((H + 151) / 152) > kMaxRows2 * kMaxAssign) return 0;
+    const size_t st = staging_bytes(T, k, H, I);
+    const size_t ring_min = 2 * 2 * kGroup * L.rs_gu;
+    return st + ring_min <= 200 * 1024 ? st + ring_min : 0;
+}
+
+int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const RouteOut* ro) {
     const Layout& L = *a.L;
     DeviceInfo di;
     int rc = current_device_info(&di);
     if (rc != MOE_OK) return rc;
-    const size_t smem = decode_fused_smem(a.T, a.k, L.H, L.I);
-    if (smem == 0) return MOE_ERR_UNSUPPORTED;
+    if (decode_fused_smem(a.T, a.k, L.H, L.I) == 0) return MOE_ERR_UNSUPPORTED;
+    const size_t st = staging_bytes(a.T, a.k, L.H, L.I);
+    const size_t slot_bytes = 2 * kGroup * L.rs_gu;
+    const size_t budget = 200 * 1024;
+    if ((L.H + di.sms - 1) / di.sms > kMaxRows2) return MOE_ERR_UNSUPPORTED;
+    const int slots = int(std::min<size_t>(kMaxSlots, (budget - st) / slot_bytes));
+    const size_t down_bytes = size_t(a.T) * a.k * ((L.H + di.sms - 1) / di.sms) * L.rs_d;
+    if (slots < 2 || down_bytes > size_t(slots) * slot_bytes) return MOE_ERR_UNSUPPORTED;
+    const size_t smem = st + size_t(slots) * slot_bytes;
     FusedParams p;
     p.slots = a.slots;
     p.expert_bytes = a.expert_bytes;
@@ -396,28 +582,31 @@ int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s) {
     p.bar = static_cast<unsigned*>(ws);
     p.h = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + 256);
     p.out = a.out;
+    p.logits = ro ? ro->logits : nullptr;
+    p.r_ids = ro ? ro->ids : nullptr;
+    p.r_w = ro ? ro->w : nullptr;
+    p.r_counts = ro ? ro->counts : nullptr;
+    p.r_offsets = ro ? ro->offsets : nullptr;
+    p.r_perm = ro ? ro->perm : nullptr;
+    p.r_inv = ro ? ro->inv : nullptr;
+    if (ro && (a.T * a.k > 32 || a.E > MOE_MAX_EXPERTS)) return MOE_ERR_UNSUPPORTED;
     const int ng = (L.H / 32 + 31) / 32, nd = (L.I / 32 + 31) / 32;
-    void (*kern)(FusedParams) = nullptr;
+    void (*kern)(FusedParams, int, int) = nullptr;
 #define MOE_PICK(G_, D_) \
     if (ng == G_ && nd == D_) kern = decode_fused_kernel<G_, D_>;
     MOE_PICK(1, 1) MOE_PICK(1, 2) MOE_PICK(2, 1) MOE_PICK(2, 2) MOE_PICK(3, 3) MOE_PICK(3, 1)
     MOE_PICK(1, 3) MOE_PICK(4, 4) MOE_PICK(2, 4) MOE_PICK(4, 2) MOE_PICK(3, 2) MOE_PICK(2, 3)
 #undef MOE_PICK
     if (kern == nullptr) return MOE_ERR_UNSUPPORTED;
-    static int occ_cache[64][16] = {};
-    const int slot = (ng - 1) * 4 + (nd - 1);
+    static bool attr_set[16][64] = {};  // per kernel variant and device
+    const int variant = (ng - 1) * 4 + (nd - 1);
     if (di.device >= 64) return MOE_ERR_UNSUPPORTED;
-    if (occ_cache[di.device][slot] == 0) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024));
-        int occ = 0;
-        MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, 96 * 1024));
-        occ_cache[di.device][slot] = occ > 0 ? occ : -1;
+    if (!attr_set[variant][di.device]) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(budget)));
+        attr_set[variant][di.device] = true;
     }
-    const int occ = occ_cache[di.device][slot];
-    if (occ < 0) return MOE_ERR_UNSUPPORTED;
-    MOE_CUDA_TRY(cudaMemsetAsync(p.bar, 0, 8, s));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(di.sms * occ);
+    cfg.gridDim = dim3(di.sms);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -426,8 +615,14 @@ int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p));
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p, slots, int(st)));
     return MOE_OK;
+}
+
+int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s) { return launch_decode_fused_impl(a, ws, s, nullptr); }
+
+int launch_decode_layer(const FfnArgs& a, const RouteOut& ro, void* ws, cudaStream_t s) {
+    return launch_decode_fused_impl(a, ws, s, &ro);
 }
 
 }  // namespace moe

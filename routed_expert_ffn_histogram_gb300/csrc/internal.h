@@ -83,7 +83,14 @@ struct FfnArgs {
     float* out;
 };
 
+struct RouteOut {
+    const float* logits;
+    int32_t *ids, *counts, *offsets, *perm, *inv;
+    float* w;
+};
+
 size_t decode_workspace_bytes(int T, int k, int H, int I);
+int launch_decode_layer(const FfnArgs& a, const RouteOut& ro, void* ws, cudaStream_t s);
 size_t decode_fused_smem(int T, int k, int H, int I);
 int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s);
 int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);

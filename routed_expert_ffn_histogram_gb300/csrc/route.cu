@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "route_warp.cuh"
 
 namespace moe {
 namespace {
@@ -28,13 +29,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTileTokens = 256;
 constexpr int kMaxPerLane = MOE_MAX_EXPERTS / 32;
 
-__device__ __forceinline__ bool ranks_before(float la, int a, float lb, int b) {
-    const bool na = isnan(la), nb = isnan(lb);
-    if (na != nb) return nb;
-    if (!na && la != lb) return la > lb;
-    return a < b;
-}
-
 struct Smem {
     int hist[MOE_MAX_EXPERTS];
     int base[MOE_MAX_EXPERTS];
@@ -42,56 +36,22 @@ struct Smem {
     int warp_cnt[kWarps][MOE_MAX_EXPERTS];
 };
 
-// Top-k + softmax for the tokens of this CTA's tile; accumulates the tile
-// histogram into sm.hist (which must be zeroed by the caller).
-__device__ void topk_tile(const float* __restrict__ logits, int T, int E, int k,
-                          int32_t* __restrict__ ids, float* __restrict__ w, int t0, Smem& sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t1 = min(T, t0 + kTileTokens);
-    for (int t = t0 + warp; t < t1; t += kWarps) {
-        const float* row = logits + (size_t)t * E;
-        float v[kMaxPerLane];
-#pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = (e < E) ? __ldg(row + e) : 0.0f;
-        }
-        uint32_t taken = 0;
-#pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i)
-            if (lane + 32 * i >= E) taken |= 1u << i;
-
-        float sel_v = 0.0f;
-        int sel_id = -1;
-        for (int j = 0; j < k; ++j) {
-            float bv = 0.0f;
-            int bid = -1;
-#pragma unroll
-            for (int i = 0; i < kMaxPerLane; ++i) {
-                if (taken & (1u << i)) continue;
-                const int e = lane + 32 * i;
-                if (bid < 0 || ranks_before(v[i], e, bv, bid)) { bv = v[i]; bid = e; }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
-                if (oid >= 0 && (bid < 0 || ranks_before(ov, oid, bv, bid))) { bv = ov; bid = oid; }
-            }
-            // every lane now holds the same winner
-            if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-            if (lane == j) { sel_v = bv; sel_id = bid; }
-            if (lane == 0) atomicAdd(&sm.hist[bid], 1);
-        }
-        // softmax over the k selected logits in fp64: lane j < k evaluates its
-        // own exponential, the sum is folded in rank order, lane j divides
-        const double m = (double)__shfl_sync(0xffffffffu, sel_v, 0);
-        const double d = (lane < k) ? exp((double)sel_v - m) : 0.0;
-        double sum = 0.0;
-        for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, d, j);
+// Top-k + softmax for the tokens [t0, t0 + ntok) of this CTA, one warp per
+// token at a time; accumulates the histogram into hist (zeroed by the caller).
+template <int EPL>
+__device__ void topk_tokens(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+                            float* __restrict__ w, int t0, int ntok, int* hist) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int t1 = min(T, t0 + ntok);
+    for (int t = t0 + warp; t < t1; t += nwarps) {
+        float sel_v;
+        int sel_id;
+        topk_warp<EPL>(logits + (size_t)t * E, E, k, sel_v, sel_id);
+        const float wv = softmax_lane(sel_v, k);
         if (lane < k) {
             ids[(size_t)t * k + lane] = sel_id;
-            w[(size_t)t * k + lane] = (float)(d / sum);
+            w[(size_t)t * k + lane] = wv;
+            if (hist) atomicAdd(&hist[sel_id], 1);
         }
     }
 }
@@ -163,6 +123,7 @@ __device__ void scatter_tile(const int32_t* __restrict__ ids, int a0, int a1, in
 }
 
 // Whole plan in one CTA (T <= one tile).
+template <int EPL>
 __global__ void __launch_bounds__(kThreads) route_single_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -170,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) route_single_kernel(
     __shared__ Smem sm;
     if (threadIdx.x < MOE_MAX_EXPERTS) sm.hist[threadIdx.x] = 0;
     __syncthreads();
-    topk_tile(logits, T, E, k, ids, w, 0, sm);
+    topk_tokens<EPL>(logits, T, E, k, ids, w, 0, kTileTokens, sm.hist);
     __syncthreads();
     const int tot = (threadIdx.x < E) ? sm.hist[threadIdx.x] : 0;
     const int total = block_exclusive_scan(tot, sm.base, sm);
@@ -183,16 +144,46 @@ __global__ void __launch_bounds__(kThreads) route_single_kernel(
     scatter_tile(ids, 0, T * k, E, perm, inv, sm);
 }
 
-// Multi-tile, pass 1: top-k + per-tile histogram.
-__global__ void __launch_bounds__(kThreads) route_topk_kernel(
+// Multi-tile, pass 1: top-k + per-tile histogram (32 warps per tile).
+constexpr int kTopkThreads = 1024;
+template <int EPL>
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ tile_hist) {
-    __shared__ Smem sm;
-    if (threadIdx.x < MOE_MAX_EXPERTS) sm.hist[threadIdx.x] = 0;
+    __shared__ int hist[MOE_MAX_EXPERTS];
+    if (threadIdx.x < MOE_MAX_EXPERTS) hist[threadIdx.x] = 0;
     __syncthreads();
-    topk_tile(logits, T, E, k, ids, w, blockIdx.x * kTileTokens, sm);
+    topk_tokens<EPL>(logits, T, E, k, ids, w, blockIdx.x * kTileTokens, kTileTokens, hist);
     __syncthreads();
-    if (threadIdx.x < E) tile_hist[(size_t)blockIdx.x * E + threadIdx.x] = sm.hist[threadIdx.x];
+    if (threadIdx.x < E) tile_hist[(size_t)blockIdx.x * E + threadIdx.x] = hist[threadIdx.x];
+}
+
+// Whole plan in one warp when T * k <= 32 (the decode shapes): no shared
+// memory and no block barriers.  Lane a owns assignment a = t*k + j; its
+// grouped position is (# assignments with a smaller expert id) + (# earlier
+// assignments with the same id).
+template <int EPL>
+__global__ void __launch_bounds__(32) route_tiny_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+    float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    const int lane = threadIdx.x;
+    const int A = T * k;
+    int my_id = MOE_MAX_EXPERTS;  // sorts after every real id
+    for (int t = 0; t < T; ++t) {
+        float sel_v;
+        int sel_id;
+        topk_warp<EPL>(logits + (size_t)t * E, E, k, sel_v, sel_id);
+        const float wv = softmax_lane(sel_v, k);
+        if (lane < k) {
+            ids[(size_t)t * k + lane] = sel_id;
+            w[(size_t)t * k + lane] = wv;
+        }
+        const int src = lane - t * k;
+        const int got = __shfl_sync(0xffffffffu, sel_id, src & 31);
+        if (src >= 0 && src < k) my_id = got;
+    }
+    plan_warp(my_id, A, E, counts, offsets, perm, inv);
 }
 
 // Multi-tile, pass 2: global offsets from all tile histograms, then the
@@ -233,19 +224,30 @@ int route_tiles(int T, int k) {
     return T <= kTileTokens ? 1 : (T + kTileTokens - 1) / kTileTokens;
 }
 
+template <int EPL>
+int launch_route_epl(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
+                     int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* tile_hist, int n_tiles,
+                     cudaStream_t s) {
+    if (T * k <= 32) {
+        route_tiny_kernel<EPL><<<1, 32, 0, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, inv);
+    } else if (n_tiles <= 1) {
+        route_single_kernel<EPL><<<1, kThreads, 0, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, inv);
+    } else {
+        route_topk_kernel<EPL><<<n_tiles, kTopkThreads, 0, s>>>(logits, T, E, k, ids, w, tile_hist);
+        MOE_CUDA_TRY(cudaGetLastError());
+        route_scatter_kernel<<<n_tiles, kThreads, 0, s>>>(ids, T, E, k, tile_hist, counts, offsets, perm, inv);
+    }
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
 int launch_route_plan(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                       int32_t* tile_hist, int n_tiles, cudaStream_t s) {
-    if (n_tiles <= 1) {
-        route_single_kernel<<<1, kThreads, 0, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, inv);
-        MOE_CUDA_TRY(cudaGetLastError());
-        return MOE_OK;
-    }
-    route_topk_kernel<<<n_tiles, kThreads, 0, s>>>(logits, T, E, k, ids, w, tile_hist);
-    MOE_CUDA_TRY(cudaGetLastError());
-    route_scatter_kernel<<<n_tiles, kThreads, 0, s>>>(ids, T, E, k, tile_hist, counts, offsets, perm, inv);
-    MOE_CUDA_TRY(cudaGetLastError());
-    return MOE_OK;
+    if (E <= 32) return launch_route_epl<1>(logits, T, E, k, ids, w, counts, offsets, perm, inv, tile_hist, n_tiles, s);
+    if (E <= 64) return launch_route_epl<2>(logits, T, E, k, ids, w, counts, offsets, perm, inv, tile_hist, n_tiles, s);
+    if (E <= 128) return launch_route_epl<4>(logits, T, E, k, ids, w, counts, offsets, perm, inv, tile_hist, n_tiles, s);
+    return launch_route_epl<8>(logits, T, E, k, ids, w, counts, offsets, perm, inv, tile_hist, n_tiles, s);
 }
 
 // ---------------------------------------------------------------------------

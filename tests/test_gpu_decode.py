@@ -25,8 +25,7 @@ def _gpu_layer(M, pool, layer, logits, xbits, k, path, slot_of=None, ret_ws=Fals
     M.moe_route_plan(lg, k, plan, with_counts_host=False)
     if slot_of is None:
         slot_of = torch.from_numpy(pool_slot_map(pool, layer)).cuda()
-    ws = torch.empty(max(M.moe_ffn_workspace_bytes(T, k, pool.hidden, pool.inter, path), 256),
-                     dtype=torch.uint8, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, pool.hidden, pool.inter, path)
     out = torch.empty((T, H), dtype=torch.float32, device="cuda")
     M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=path)
     torch.cuda.synchronize()
@@ -122,3 +121,46 @@ def test_decode_not_resident_gives_nan_not_fault():
     lg[0, 1] = 4.0
     out = _gpu_layer(M, pool, 0, lg, S.activations_bf16_bits(wl, 0)[:1], 2, M.MOE_PATH_DECODE, slot_of=slot_of)
     assert np.all(np.isnan(out))
+
+
+@pytest.mark.parametrize("wid,T", [(0, 16), (1, 1), (4, 2)])
+def test_decode_layer_fused_equals_two_calls(wid, T):
+    """moe_decode_layer (routing inside the decode kernel) writes the same
+    routing outputs as moe_route_plan and the same layer output as
+    moe_route_plan + moe_expert_ffn on the decode path; and matches the
+    oracle."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[wid]
+    if wid == 4:
+        wl = S.Workload(4, "qwen_decode_probe", 1, 2048, 768, 128, 8, T, 1, 128, 0.8, 4)
+    pool, host, dev = make_pool(M, wl, layers=1)
+    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    lg_np = S.logits(wl, 0, 0, T)
+    x_np = S.activations_bf16_bits(wl, 0, 0, T)
+    lg = torch.from_numpy(lg_np).cuda()
+    x = torch.from_numpy(x_np.view(np.int16)).cuda().view(torch.bfloat16)
+    slot_of = torch.arange(E, dtype=torch.int32, device="cuda")
+    a, b = M.RoutePlan.allocate(T, E, k), M.RoutePlan.allocate(T, E, k)
+    out_a = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    out_b = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws_a = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    ws_b = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    for _ in range(2):  # twice: the workspace barrier must stay consistent
+        M.moe_decode_layer(pool, 0, lg, x, a, slot_of, out_a, ws_a)
+        M.moe_route_plan(lg, k, b, with_counts_host=False)
+        M.moe_expert_ffn(pool, 0, x, b, slot_of, out_b, ws_b, path=M.MOE_PATH_DECODE)
+        torch.cuda.synchronize()
+        n = T * k
+        for key in ("ids", "w", "counts", "offsets"):
+            assert torch.equal(getattr(a, key), getattr(b, key)), key
+        assert torch.equal(a.perm[:n], b.perm[:n]) and torch.equal(a.inv[:n], b.inv[:n])
+        assert torch.equal(out_a, out_b)
+    ids, w = oracle.route(lg_np, k)
+    uniq = sorted(set(ids.reshape(-1).tolist()))
+    ws = S.stack_experts(S.layer_weights(wl, 0, uniq))
+    remap = {e: i for i, e in enumerate(uniq)}
+    ref = oracle.layer(x_np, np.vectorize(remap.get)(ids).astype(np.int32), w, ws, prefill=False, threads=16)
+    assert rel_l2(out_a.cpu().numpy(), ref) <= DECODE_REL_L2

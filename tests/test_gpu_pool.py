@@ -26,7 +26,7 @@ def test_offload_decode_lru_and_outputs():
     T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
     plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
     slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
-    ws = torch.empty(M.moe_ffn_workspace_bytes(T, k, H, I, M.MOE_PATH_DECODE), dtype=torch.uint8, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
     out = torch.empty((T, H), dtype=torch.float32, device="cuda")
     samples = {(0, 0), (3, 11), (7, 23)}
     with torch.cuda.stream(compute):

@@ -34,8 +34,7 @@ def _run_prefill(M, pool, wl, layer=0, step=0, tokens=None, logits=None):
     plan = M.RoutePlan.allocate(T, E, wl.top_k)
     M.moe_route_plan(torch.from_numpy(lg).cuda(), wl.top_k, plan, with_counts_host=False)
     slot_of = torch.from_numpy(pool.slot_map(layer).astype(np.int32)).cuda()
-    ws = torch.empty(M.moe_ffn_workspace_bytes(T, wl.top_k, wl.hidden, wl.inter, M.MOE_PATH_PREFILL),
-                     dtype=torch.uint8, device="cuda")
+    ws = M.alloc_ffn_workspace(T, wl.top_k, wl.hidden, wl.inter, M.MOE_PATH_PREFILL)
     out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
     xt = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     M.moe_expert_ffn(pool, layer, xt, plan, slot_of, out, ws, path=M.MOE_PATH_PREFILL)
