@@ -1,7 +1,7 @@
 // Warp-level routing pieces shared by the routing kernels and the fused
 // decode kernel: top-k of one token's logits (larger logit first, equal
 // logits by lower id, NaN last) and the softmax over the k selected logits
-// (fp64, summed in rank order, rounded to fp32).
+// (float-float, about 48 bits, summed in rank order, rounded to fp32).
 #pragma once
 
 #include <cmath>
@@ -53,15 +53,86 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, 
     }
 }
 
-// Softmax over the k selected logits in fp64: lane j < k evaluates its own
-// exponential, the sum is folded in rank order, lane j divides.
+// ---- float-float ("double-single") arithmetic --------------------------
+// A value is an unevaluated sum hi + lo of two floats (about 48 bits).  The
+// error-free transforms are Knuth's two-sum and the fma-based two-product;
+// exp uses Cody-Waite reduction by ln 2 (split in three floats so n * c1 and
+// n * c2 are exact), a further reduction by 8, a degree-10 Taylor series and
+// three squarings.  GB300's fp64 rate is a small fraction of its fp32 rate,
+// so this is much faster than double while matching a double evaluation
+// after rounding to fp32 except in rare near-ties.
+struct FF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float v = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, v)), __fsub_rn(b, v))};
+}
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ FF ff_two_prod(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ FF ff_add(FF x, FF y) {
+    const FF s = ff_two_sum(x.hi, y.hi);
+    return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+__device__ __forceinline__ FF ff_mul(FF x, FF y) {
+    const FF p = ff_two_prod(x.hi, y.hi);
+    return ff_fast_two_sum(p.hi, __fadd_rn(p.lo, __fadd_rn(__fmul_rn(x.hi, y.lo), __fmul_rn(x.lo, y.hi))));
+}
+
+// e^d for d <= 0 given as a float-float.
+__device__ __forceinline__ FF ff_exp_nonpos(FF d) {
+    if (d.hi < -110.0f) return {0.0f, 0.0f};
+    // ln 2 = c1 + c2 + c3 (c1 has 16 significant bits)
+    const float c1 = 0.693145751953125f, c2 = 1.428606765330187e-06f, c3 = 5.497923148104107e-14f;
+    const float n = rintf(d.hi * 1.4426950216293335f);
+    FF r = ff_add(d, FF{-n * c1, 0.0f});
+    r = ff_add(r, ff_two_prod(-n, c2));
+    r = ff_add(r, FF{-n * c3, 0.0f});
+    r.hi *= 0.125f;
+    r.lo *= 0.125f;
+    // 1/i! as float-float pairs, i = 0..10
+    const float ch[11] = {1.0f, 1.0f, 0.5f, 0.1666666716337204f, 0.0416666679084301f, 0.008333333767950535f,
+                          0.0013888889225199819f, 0.00019841270113829523f, 2.4801587642286904e-05f,
+                          2.7557318844628753e-06f, 2.755731998149713e-07f};
+    const float cl[11] = {0.0f, 0.0f, 0.0f, -4.967053879312289e-09f, -1.2417634698280722e-09f, -4.34617203337595e-10f,
+                          -3.3631094437103215e-11f, -2.725596874933456e-12f, -3.40699609366682e-13f,
+                          3.793571224297229e-14f, -7.575112209051195e-15f};
+    FF p{ch[10], cl[10]};
+#pragma unroll
+    for (int i = 9; i >= 0; --i) p = ff_add(ff_mul(p, r), FF{ch[i], cl[i]});
+    p = ff_mul(p, p);
+    p = ff_mul(p, p);
+    p = ff_mul(p, p);
+    const int ni = int(n);
+    return {ldexpf(p.hi, ni), ldexpf(p.lo, ni)};
+}
+
+// Softmax over the k selected logits: lane j < k evaluates its own
+// exponential of (l_j - l_0) in float-float, the sum is folded in rank
+// order, lane j divides; the result is rounded once to fp32.
 __device__ __forceinline__ float softmax_lane(float sel_v, int k) {
     const int lane = threadIdx.x & 31;
-    const double m = (double)__shfl_sync(0xffffffffu, sel_v, 0);
-    const double d = (lane < k) ? exp((double)sel_v - m) : 0.0;
-    double sum = 0.0;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, d, j);
-    return (float)(d / sum);
+    const float m = __shfl_sync(0xffffffffu, sel_v, 0);
+    FF e{0.0f, 0.0f};
+    if (lane < k) e = ff_exp_nonpos(ff_two_sum(sel_v, -m));
+    FF s{0.0f, 0.0f};
+    for (int j = 0; j < k; ++j) {
+        const FF ej{__shfl_sync(0xffffffffu, e.hi, j), __shfl_sync(0xffffffffu, e.lo, j)};
+        s = ff_add(s, ej);
+    }
+    const float q1 = __fdiv_rn(e.hi, s.hi);
+    FF qs = ff_two_prod(s.hi, q1);
+    qs.lo = __fmaf_rn(s.lo, q1, qs.lo);
+    const FF r = ff_add(e, FF{-qs.hi, -qs.lo});
+    return __fadd_rn(q1, __fdiv_rn(r.hi, s.hi));
 }
 
 // Grouping of A <= 32 assignments by one warp: lane a holds the expert id
