@@ -112,8 +112,9 @@ MOE_API int moe_expert_bytes(int hidden, int inter, size_t* out_bytes);
  *   down_scales            host [hidden][inter/32]
  *   dst                    host, moe_expert_bytes() bytes, written fully
  * The native layout keeps each row's codes followed by its scales (rows
- * padded to 32 bytes) and interleaves gate and up rows in chunks of 64 so one tile of
- * the fused gate/up product holds matching gate and up rows.
+ * padded to 32 bytes) and interleaves gate and up rows in chunks of 32 (gate rows
+ * 32c..32c+31, then up rows 32c..32c+31) so one tile of the fused gate/up
+ * product holds matching gate and up rows.
  * Errors: MOE_ERR_INVALID. */
 MOE_API int moe_pack_expert(const uint8_t* gate_codes, const uint8_t* gate_scales,
                     const uint8_t* up_codes, const uint8_t* up_scales,

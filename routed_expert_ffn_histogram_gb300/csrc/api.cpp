@@ -87,7 +87,7 @@ extern "C" int moe_pack_expert(const uint8_t* gc, const uint8_t* gs, const uint8
     const size_t ic = size_t(inter) / 2, isc = size_t(inter) / 32;
     for (int r = 0; r < inter; ++r) {
         uint8_t* grow = o + Layout::gate_row(r) * L.rs_gu;
-        uint8_t* urow = grow + 64 * L.rs_gu;
+        uint8_t* urow = grow + Layout::kChunk * L.rs_gu;
         std::memcpy(grow, gc + size_t(r) * hc, hc);
         std::memcpy(grow + hc, gs + size_t(r) * hsc, hsc);
         std::memcpy(urow, uc + size_t(r) * hc, hc);

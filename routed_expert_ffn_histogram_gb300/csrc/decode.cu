@@ -13,7 +13,7 @@
 //
 // Kernels (both HBM-bound: every weight byte is read once per call):
 //   gateup: one warp per (assignment, row) item reads the gate row and the up
-//           row (they sit 64 rows apart in the native layout), one 16-byte
+//           row (they sit 32 rows apart in the native layout), one 16-byte
 //           load = 32 codes = exactly one MX block per lane; x is staged in
 //           shared memory (bf16, 16-byte chunks XOR-swizzled so a warp's
 //           LDS.128 is conflict-free);
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) decode_gateup_kernel(DecodeParams p)
             continue;
         }
         const uint8_t* g = base + Layout::gate_row(r) * p.rs_gu;
-        const uint8_t* u = g + 64 * p.rs_gu;
+        const uint8_t* u = g + Layout::kChunk * p.rs_gu;
         uint4 cg[NIT], cu[NIT];
         uint32_t sg[NIT], su[NIT];
 #pragma unroll

@@ -20,7 +20,7 @@
 // experts at full rate whatever the warps are doing, and the warps' loads
 // meet the data in L2.
 //   phase 1  a warp takes one item at a time: the gate row and the up row
-//            (64 rows apart in the packed layout), one 16-byte load = one MX
+//            (32 rows apart in the packed layout), one 16-byte load = one MX
 //            block per lane; x is staged once per CTA in shared memory as
 //            f16 scaled per 32-block by a power of two (exact for every
 //            value within 2^-31 of the block maximum) in XOR-swizzled
@@ -46,6 +46,7 @@ namespace {
 
 constexpr int kGroup = 16;             // row pairs per ring slot (one bulk copy each for gate and up)
 constexpr int kThreads = 32 * (kGroup + 1);  // warp 0: copy producer; warps 1..16: one row pair each
+static_assert(Layout::kChunk % kGroup == 0, "a group of gate rows stays inside one interleave chunk");
 constexpr int kMaxSlots = 16;
 constexpr int kMaxRows2 = 64;          // output rows per CTA in phase 2
 constexpr int kWarps = kThreads / 32;
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                     const uint8_t* g = eb + Layout::gate_row(r) * p.rs_gu;
                     tc::mbar_arrive_expect_tx(&full[slot], uint32_t(slot_bytes));
                     bulk_copy_g2s(ring + (size_t)slot * slot_bytes, g, uint32_t(kGroup * row_bytes), &full[slot]);
-                    bulk_copy_g2s(ring + (size_t)slot * slot_bytes + kGroup * row_bytes, g + 64 * p.rs_gu,
+                    bulk_copy_g2s(ring + (size_t)slot * slot_bytes + kGroup * row_bytes, g + Layout::kChunk * p.rs_gu,
                                   uint32_t(kGroup * row_bytes), &full[slot]);
                 } else {
                     tc::mbar_arrive(&full[slot]);

@@ -24,8 +24,9 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // GPU-native packed expert.  Every row stores its K/2 code bytes followed by
 // its K/32 E8M0 scale bytes, zero-padded to a multiple of 32 bytes.  The gate/up
-// matrix has 2I rows interleaved in chunks of 64: chunk c holds gate rows
-// 64c..64c+63 then up rows 64c..64c+63.  The down matrix (H rows) follows.
+// matrix has 2I rows interleaved in chunks of 32: chunk c holds gate rows
+// 32c..32c+31 then up rows 32c..32c+31, so a 32-wide block of h = SwiGLU(g, u)
+// comes from one 64-row pair of chunks.  The down matrix (H rows) follows.
 struct Layout {
     int H = 0, I = 0;
     size_t rs_gu = 0;        // bytes per gate/up row (K = H)
@@ -44,8 +45,11 @@ struct Layout {
         L->expert_bytes = round_up(L->d_off + size_t(hidden) * L->rs_d, 1024);
         return true;
     }
-    // Row of the gate/up matrix that holds gate row r (up row: + 64).
-    __host__ __device__ static inline size_t gate_row(int r) { return size_t(r / 64) * 128 + size_t(r % 64); }
+    static constexpr int kChunk = 32;
+    // Row of the gate/up matrix that holds gate row r (its up row: + kChunk).
+    __host__ __device__ static inline size_t gate_row(int r) {
+        return size_t(r / kChunk) * (2 * kChunk) + size_t(r % kChunk);
+    }
 };
 
 struct DeviceInfo {

@@ -18,15 +18,23 @@
 //      grouped order);
 //   4. combine: out[t] = sum_j w[t][j] * y[inv[t*k+j]] in ascending j.
 //
-// GEMM kernel (persistent, one CTA per SM, 6 warps):
-//   warp 0     TMA producer: 128x128-byte A tile (E4M3) and 128x128-element
+// GEMM kernel (persistent, one CTA per SM, 10 warps):
+//   warp 0     TMA producer: 128x128-byte A tile (E4M3) and 192x128-element
 //              B tile (E2M1, unpacked by TMA into the 16-byte-aligned layout
 //              the f8f6f4 MMA reads) per stage, 128-byte swizzle;
 //   warp 1     MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale 1X,
-//              M=128 N=128 K=32, four per stage; scale factors in TMEM;
-//   warps 2-5  epilogue: write the tile's scale factors into TMEM, then read
-//              the fp32 accumulator (tcgen05.ld) and finish the tile.
-// Tiles (expert, 128-row block, 128-column block) are enumerated on the
+//              M=128 N=192 K=32, four per stage, into one of two tensor-
+//              memory accumulators (tile i uses buffer i % 2);
+//   warps 2-5  epilogue: read the fp32 accumulator of tile i (tcgen05.ld)
+//              and finish it while the MMAs of tile i+1 run;
+//   warps 6-9  scale-factor feeders: per stage, the E8M0 bytes of the
+//              tile's 128 activation rows and 128 weight rows go into a
+//              tensor-memory ring slot tied to the shared-memory stage.
+// N = 192 is three 64-row chunk pairs of the interleaved gate/up matrix, and
+// the widest tile whose two accumulators leave tensor memory for the
+// scale-factor ring; a wider MMA also reads less shared memory per product
+// than N = 128.
+// Tiles (expert, 128-row block, 192-column block) are enumerated on the
 // device from the offsets; columns vary fastest so the CTAs working at the
 // same time share an expert's activation rows and weight rows through L2.
 #include <cuda.h>
@@ -41,22 +49,29 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;           // rows (tokens) per tile
-constexpr int kBN = 128;           // weight rows per tile
+constexpr int kBN = 192;           // weight rows per tile
 constexpr int kBK = 128;           // K elements per pipeline stage
-constexpr int kStages = 6;
-constexpr int kThreads = 192;
+constexpr int kStages = 5;
+constexpr int kThreads = 320;
 constexpr uint32_t kStageBytesA = kBM * kBK;   // E4M3: one byte per element
 constexpr uint32_t kStageBytesB = kBN * kBK;   // E2M1 unpacked: 16 bytes per 16 elements in smem
 constexpr uint32_t kTxBytesB = kBN * kBK / 2;  // ...of which TMA writes the 8 packed bytes per 16
 constexpr uint32_t kTmemCols = 512;
-// Tensor-memory columns: fp32 accumulator [0, 128); scale factors of A and B
-// at 128 and 256, four columns per K stage of 128 (row m of a 128-row
-// operand keeps its stage's four E8M0 bytes in lane m, column base + m/32;
-// byte j belongs to the stage's j-th block of 32 and is picked by the MMA's
-// scale-factor id).
-constexpr uint32_t kColAcc = 0, kColSfa = 128, kColSfb = 256;
-constexpr int kMaxKStages = 32;    // K <= 4096
+// Tensor-memory columns: fp32 accumulators at 0 and 256 (kBN columns each);
+// the scale-factor ring uses the gaps [kBN, 256) and [256 + kBN, 512), 16
+// columns per shared-memory stage: A at +0 (4 columns), B at +8 (kBN / 32
+// columns).  Row m of an operand keeps its stage's four E8M0 bytes in lane
+// m % 32 (the same in each lane quarter), column base + m / 32; byte j of
+// that word belongs to the stage's j-th block of 32 and is picked by the
+// MMA's scale-factor id.
+constexpr uint32_t kAccStride = 256;
+constexpr int kSfSlotsLow = (kAccStride - kBN) / 16;
+__host__ __device__ constexpr uint32_t sf_col(int s) {
+    return s < kSfSlotsLow ? kBN + 16 * s : kAccStride + kBN + 16 * (s - kSfSlotsLow);
+}
 constexpr int kMaxExperts = MOE_MAX_EXPERTS;
+static_assert(kBN % 64 == 0 && kBN / 32 <= 8, "tile width: whole chunk pairs, B scales in 8 columns");
+static_assert(sf_col(kStages - 1) + 16 <= kTmemCols && 2 * kSfSlotsLow >= kStages, "tensor-memory columns");
 
 struct GemmParams {
     const int32_t* offsets;     // [E+1] grouped row ranges
@@ -83,10 +98,11 @@ struct GemmParams {
 struct __align__(1024) Smem {
     uint8_t a[kStages][kStageBytesA];
     uint8_t b[kStages][kStageBytesB];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t sf_full;
-    uint64_t acc_full;
+    uint64_t full[kStages];      // TMA bytes landed
+    uint64_t sf_full[kStages];   // scale factors of the stage written to tensor memory
+    uint64_t empty[kStages];     // MMAs of the stage finished (smem and scale slot free)
+    uint64_t acc_full[2];        // accumulator holds a finished tile
+    uint64_t acc_empty[2];       // epilogue has read the accumulator
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t mt_prefix[kMaxExperts + 1];
@@ -113,6 +129,10 @@ __device__ __forceinline__ Tile decode_tile(const Smem& sm, const GemmParams& p,
     tl.m0 = off + (mt - sm.mt_prefix[lo]) * kBM;
     tl.rows = min(kBM, p.offsets[lo + 1] - tl.m0);
     return tl;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
 __device__ __forceinline__ float e8m0_inv_scale_f(uint32_t sb) {
@@ -166,10 +186,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
             sm.n_tiles = uint32_t(carry) * uint32_t(NT);
             for (int s = 0; s < kStages; ++s) {
                 tc::mbar_init(&sm.full[s], 1);
+                tc::mbar_init(&sm.sf_full[s], 128);
                 tc::mbar_init(&sm.empty[s], 1);
             }
-            tc::mbar_init(&sm.sf_full, 128);
-            tc::mbar_init(&sm.acc_full, 1);
+            for (int b = 0; b < 2; ++b) {
+                tc::mbar_init(&sm.acc_full[b], 1);
+                tc::mbar_init(&sm.acc_empty[b], 128);
+            }
             tc::mbar_init(&sm.mma_done, 1);
             tc::fence_barrier_init();
             tc::tma_prefetch_desc(&map_a);
@@ -211,97 +234,71 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0, tphase = 0;
-            for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x) {
-                if (!tc::mbar_wait(&sm.sf_full, tphase, err, 2u)) break;
-                tphase ^= 1u;
+            uint32_t phase = 0;
+            int i = 0;
+            for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x, ++i) {
+                const int buf = i & 1;
+                // the epilogue has drained this buffer (tile i - 2)
+                if (!tc::mbar_wait(&sm.acc_empty[buf], ((i >> 1) & 1) ^ 1u, err, 2u)) break;
                 tc::tc_fence_after();
+                const uint32_t d = tmem + buf * kAccStride;
+                bool ok = true;
                 for (int ks = 0; ks < n_kstages; ++ks) {
-                    if (!tc::mbar_wait(&sm.full[stage], phase, err, 2u)) break;
+                    if (!tc::mbar_wait(&sm.full[stage], phase, err, 2u) ||
+                        !tc::mbar_wait(&sm.sf_full[stage], phase, err, 2u)) {
+                        ok = false;
+                        break;
+                    }
                     tc::tc_fence_after();
                     const uint32_t a0 = tc::smem_u32(sm.a[stage]);
                     const uint32_t b0 = tc::smem_u32(sm.b[stage]);
+                    const uint32_t sfa = tmem + sf_col(stage);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk) {
                         const int kb = ks * (kBK / 32) + kk;
                         if (kb < p.KB) {
                             const uint32_t idesc = tc::idesc_mxf8f6f4(0, 5, kBM, kBN, kk, kk);
-                            tc::mma_mxf8f6f4(tmem + kColAcc, tc::smem_desc_sw128(a0 + kk * 32),
-                                             tc::smem_desc_sw128(b0 + kk * 32), idesc, tmem + kColSfa + 4 * ks,
-                                             tmem + kColSfb + 4 * ks, (ks | kk) != 0);
+                            tc::mma_mxf8f6f4(d, tc::smem_desc_sw128(a0 + kk * 32), tc::smem_desc_sw128(b0 + kk * 32),
+                                             idesc, sfa, sfa + 8, (ks | kk) != 0);
                         }
                     }
                     tc::mma_commit(&sm.empty[stage]);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
-                tc::mma_commit(&sm.acc_full);
+                if (!ok) break;
+                tc::mma_commit(&sm.acc_full[buf]);
             }
             // all MMAs issued by this CTA have finished before TMEM is freed
             tc::mma_commit(&sm.mma_done);
             tc::mbar_wait(&sm.mma_done, 0, err, 16u);
         }
-    } else {
+    } else if (warp < 6) {
         // ---------------- epilogue (warps 2..5 = TMEM lane quarters 2,3,0,1) ----------------
         const int q = warp & 3;
         const int r = q * 32 + lane;                // tile row == TMEM lane
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
-        uint32_t aphase = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        int i = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
             if (*err) break;
             const Tile tl = decode_tile(sm, p, t, NT);
-            const int slot = p.slot_of[tl.e];
-            if (slot < 0 || slot >= p.S) break;
-            // scale factors of the tile's activation rows and weight rows -> TMEM:
-            // this thread fills lane r, columns base + 4s + c with the four
-            // bytes of stage s of rows 32c + lane (c = 0..3)
-            {
-                const int nst = (p.KB + 3) / 4;           // K stages (4 bytes each)
-                const int nvec = (p.b_sf_bytes + 15) / 16; // 16-byte chunks per scale row
-                const uint4* as[4];
-                const uint4* bs[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int arow = min(tl.m0 + 32 * c + lane, p.A - 1);
-                    const int brow = min(tl.nt * kBN + 32 * c + lane, p.N - 1);
-                    as[c] = reinterpret_cast<const uint4*>(p.a_scales + (size_t)arow * p.a_sf_stride);
-                    bs[c] = reinterpret_cast<const uint4*>(p.b_base + (size_t)slot * p.expert_bytes +
-                                                           (size_t)brow * p.b_rs + p.b_code_bytes);
-                }
-                for (int v = 0; v < nvec; ++v) {
-                    uint4 xa[4], xb[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        xa[c] = __ldg(as[c] + v);
-                        xb[c] = __ldg(bs[c] + v);
-                    }
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int st = 4 * v + w;
-                        if (st >= nst) break;
-                        const uint32_t* a32[4] = {&xa[0].x, &xa[1].x, &xa[2].x, &xa[3].x};
-                        const uint32_t* b32[4] = {&xb[0].x, &xb[1].x, &xb[2].x, &xb[3].x};
-                        tc::tmem_st_x4(lane_base + kColSfa + 4 * st, a32[0][w], a32[1][w], a32[2][w], a32[3][w]);
-                        tc::tmem_st_x4(lane_base + kColSfb + 4 * st, b32[0][w], b32[1][w], b32[2][w], b32[3][w]);
-                    }
-                }
-                tc::tmem_st_wait();
-                tc::tc_fence_before();
-                tc::mbar_arrive(&sm.sf_full);
-            }
-            if (!tc::mbar_wait(&sm.acc_full, aphase, err, 8u)) break;
-            aphase ^= 1u;
+            const int buf = i & 1;
+            if (!tc::mbar_wait(&sm.acc_full[buf], (i >> 1) & 1, err, 8u)) break;
             tc::tc_fence_after();
+            const uint32_t acc = lane_base + buf * kAccStride;
             const bool valid = r < tl.rows;
             const int m = tl.m0 + r;
             if (p.mode == 0) {
-                // columns 0..63: gate rows of chunk nt; 64..127: the matching up rows
+                // columns 64j..64j+31: gate rows of chunk c = 3 nt + j (h columns
+                // 32c..32c+31); 64j+32..64j+63: the matching up rows
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < kBN / 64; ++half) {
+                    const int chunk = tl.nt * (kBN / 64) + half;
+                    if (chunk * 32 >= p.I) break;   // ragged last tile (warp-uniform)
                     uint32_t g0[16], g1[16], u0[16], u1[16];
-                    tc::tmem_ld_x16(lane_base + kColAcc + half * 32, g0);
-                    tc::tmem_ld_x16(lane_base + kColAcc + half * 32 + 16, g1);
-                    tc::tmem_ld_x16(lane_base + kColAcc + 64 + half * 32, u0);
-                    tc::tmem_ld_x16(lane_base + kColAcc + 64 + half * 32 + 16, u1);
+                    tc::tmem_ld_x16(acc + half * 64, g0);
+                    tc::tmem_ld_x16(acc + half * 64 + 16, g1);
+                    tc::tmem_ld_x16(acc + half * 64 + 32, u0);
+                    tc::tmem_ld_x16(acc + half * 64 + 48, u1);
                     tc::tmem_ld_wait();
                     float hv[32];
                     float amax = 0.0f;
@@ -322,7 +319,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                         for (int j = 0; j < 8; ++j)
                             wv[j] = cvt_e4m3x2(hv[4 * j] * mul, hv[4 * j + 1] * mul) |
                                     (cvt_e4m3x2(hv[4 * j + 2] * mul, hv[4 * j + 3] * mul) << 16);
-                        const int col = tl.nt * 64 + half * 32;
+                        const int col = chunk * 32;
                         uint4* dst = reinterpret_cast<uint4*>(p.hq + (size_t)m * p.I + col);
                         if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0 || m >= p.A || col + 32 > p.I) {
                             atomicOr(const_cast<uint32_t*>(err), 32u);
@@ -337,7 +334,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
 #pragma unroll 1
                 for (int c = 0; c < kBN / 16; ++c) {
                     uint32_t v[16];
-                    tc::tmem_ld_x16(lane_base + kColAcc + c * 16, v);
+                    tc::tmem_ld_x16(acc + c * 16, v);
                     tc::tmem_ld_wait();
                     const int n = tl.nt * kBN + c * 16;
                     if (valid && n < p.N) {
@@ -354,6 +351,75 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                 }
             }
             tc::tc_fence_before();
+            tc::mbar_arrive(&sm.acc_empty[buf]);
+        }
+    } else {
+        // ---------------- scale-factor feeders (warps 6..9 = lane quarters 2,3,0,1) ----------------
+        // Thread (quarter q, lane l) writes lane 32q + l of the ring slot:
+        // column c of the A part gets the stage's four scale bytes of
+        // activation row 32c + l (c < 4), column c of the B part those of
+        // weight row 32c + l (c < kBN / 32).  Each row's bytes are read 16 at
+        // a time (four stages), one group of four stages ahead.
+        constexpr int kRb = kBN / 32;
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x) {
+            const Tile tl = decode_tile(sm, p, t, NT);
+            const int slot = p.slot_of[tl.e];
+            if (slot < 0 || slot >= p.S) break;
+            const uint4* as[4];
+            const uint4* bs[kRb];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int arow = min(tl.m0 + 32 * c + lane, p.A - 1);
+                as[c] = reinterpret_cast<const uint4*>(p.a_scales + (size_t)arow * p.a_sf_stride);
+            }
+#pragma unroll
+            for (int c = 0; c < kRb; ++c) {
+                const int brow = min(tl.nt * kBN + 32 * c + lane, p.N - 1);
+                bs[c] = reinterpret_cast<const uint4*>(p.b_base + (size_t)slot * p.expert_bytes +
+                                                       (size_t)brow * p.b_rs + p.b_code_bytes);
+            }
+            uint4 xa[4], xb[kRb];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) xa[c] = __ldg(as[c]);
+#pragma unroll
+            for (int c = 0; c < kRb; ++c) xb[c] = __ldg(bs[c]);
+            bool ok = true;
+            for (int ks0 = 0; ks0 < n_kstages && ok; ks0 += 4) {
+                const bool more = ks0 + 4 < n_kstages;
+                uint4 na[4], nb[kRb];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) na[c] = more ? __ldg(as[c] + ks0 / 4 + 1) : xa[c];
+#pragma unroll
+                for (int c = 0; c < kRb; ++c) nb[c] = more ? __ldg(bs[c] + ks0 / 4 + 1) : xb[c];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    if (ks0 + w >= n_kstages) break;
+                    if (!tc::mbar_wait(&sm.empty[stage], phase ^ 1u, err, 64u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t col = lane_base + sf_col(stage);
+                    tc::tmem_st_x4(col, word_of(xa[0], w), word_of(xa[1], w), word_of(xa[2], w), word_of(xa[3], w));
+                    uint32_t bw[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) bw[c] = c < kRb ? word_of(xb[c < kRb ? c : 0], w) : 0u;
+                    tc::tmem_st_x8(col + 8, bw);
+                    tc::tmem_st_wait();
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&sm.sf_full[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) xa[c] = na[c];
+#pragma unroll
+                for (int c = 0; c < kRb; ++c) xb[c] = nb[c];
+            }
+            if (!ok) break;
         }
     }
 
@@ -479,7 +545,6 @@ int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
     const PrefillWs w = prefill_ws(a.T, a.k, L.H, L.I);
     if (ws_bytes < w.total) return MOE_ERR_INVALID;
     if (L.H > 4096 || L.I > 4096 || a.E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
-    static_assert(kColSfb + 4 * kMaxKStages <= kTmemCols, "tensor-memory columns");
     if (a.T == 0) return MOE_OK;
     const int A = a.T * a.k;
     uint8_t* base = static_cast<uint8_t*>(ws);

@@ -47,7 +47,7 @@ def test_expert_bytes():
 
 
 def test_pack_native_layout():
-    """Gate/up rows interleave in chunks of 64; every row is codes then scales."""
+    """Gate/up rows interleave in chunks of 32; every row is codes then scales."""
     wl = S.WORKLOADS[0]
     H, I = wl.hidden, wl.inter
     w = S.expert_weights(wl, 0, 1)
@@ -56,13 +56,13 @@ def test_pack_native_layout():
     M.moe_pack_expert(w, H, I, buf)
     rs_gu = -(-(H // 2 + ((H // 32 + 15) // 16) * 16) // 32) * 32
     rs_d = -(-(I // 2 + ((I // 32 + 15) // 16) * 16) // 32) * 32
-    for r in [0, 1, 63, 64, 200, I - 1]:
-        g = (r // 64) * 128 + r % 64
+    for r in [0, 1, 31, 32, 63, 64, 200, I - 1]:
+        g = (r // 32) * 64 + r % 32
         row = buf[g * rs_gu:(g + 1) * rs_gu]
         assert np.array_equal(row[:H // 2], w["gate_codes"][r])
         assert np.array_equal(row[H // 2:H // 2 + H // 32], w["gate_scales"][r])
         assert not row[H // 2 + H // 32:].any()
-        row = buf[(g + 64) * rs_gu:(g + 65) * rs_gu]
+        row = buf[(g + 32) * rs_gu:(g + 33) * rs_gu]
         assert np.array_equal(row[:H // 2], w["up_codes"][r])
         assert np.array_equal(row[H // 2:H // 2 + H // 32], w["up_scales"][r])
     d_off = 2 * I * rs_gu
