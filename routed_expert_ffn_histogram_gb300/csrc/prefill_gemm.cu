@@ -18,23 +18,24 @@
 //      grouped order);
 //   4. combine: out[t] = sum_j w[t][j] * y[inv[t*k+j]] in ascending j.
 //
-// GEMM kernel (persistent, one CTA per SM, 10 warps):
-//   warp 0     TMA producer: 128x128-byte A tile (E4M3) and 192x128-element
+// GEMM kernel (persistent, one CTA per SM, 16 warps in four warpgroups):
+//   warp 0     TMA producer: 128x128-byte A tile (E4M3) and 256x128-element
 //              B tile (E2M1, unpacked by TMA into the 16-byte-aligned layout
 //              the f8f6f4 MMA reads) per stage, 128-byte swizzle;
 //   warp 1     MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale 1X,
-//              M=128 N=192 K=32, four per stage, into one of two tensor-
-//              memory accumulators (tile i uses buffer i % 2);
-//   warps 2-5  epilogue: read the fp32 accumulator of tile i (tcgen05.ld)
-//              and finish it while the MMAs of tile i+1 run;
-//   warps 6-9  scale-factor feeders: per stage, the E8M0 bytes of the
-//              tile's 128 activation rows and 128 weight rows go into a
-//              tensor-memory ring slot tied to the shared-memory stage.
-// N = 192 is three 64-row chunk pairs of the interleaved gate/up matrix, and
-// the widest tile whose two accumulators leave tensor memory for the
-// scale-factor ring; a wider MMA also reads less shared memory per product
-// than N = 128.
-// Tiles (expert, 128-row block, 192-column block) are enumerated on the
+//              M=128 N=256 K=32, four per stage, into a tensor-memory
+//              accumulator;
+//   warps 4-7  scale-factor feeders: per stage, the E8M0 bytes of the
+//              tile's 128 activation rows and 256 weight rows go into a
+//              tensor-memory ring slot tied to the shared-memory stage;
+//   warps 8-15 epilogue: copy the finished accumulator into registers
+//              (a half row per thread), hand it back to the MMA for the
+//              next tile, and finish the tile from registers.
+// Each stage costs the MMA a roughly fixed overhead for fetching fresh
+// scale factors, so the widest tile the hardware takes (N = 256) gives the
+// most products per stage; its accumulator then fills half of tensor
+// memory, and the quick register copy stands in for a second accumulator.
+// Tiles (expert, 128-row block, 256-column block) are enumerated on the
 // device from the offsets; columns vary fastest so the CTAs working at the
 // same time share an expert's activation rows and weight rows through L2.
 #include <cuda.h>
@@ -49,29 +50,33 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;           // rows (tokens) per tile
-constexpr int kBN = 192;           // weight rows per tile
+constexpr int kBN = 256;           // weight rows per tile
 constexpr int kBK = 128;           // K elements per pipeline stage
-constexpr int kStages = 5;
-constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr int kThreads = 512;      // four warpgroups
 constexpr uint32_t kStageBytesA = kBM * kBK;   // E4M3: one byte per element
 constexpr uint32_t kStageBytesB = kBN * kBK;   // E2M1 unpacked: 16 bytes per 16 elements in smem
 constexpr uint32_t kTxBytesB = kBN * kBK / 2;  // ...of which TMA writes the 8 packed bytes per 16
 constexpr uint32_t kTmemCols = 512;
-// Tensor-memory columns: fp32 accumulators at 0 and 256 (kBN columns each);
-// the scale-factor ring uses the gaps [kBN, 256) and [256 + kBN, 512), 16
-// columns per shared-memory stage: A at +0 (4 columns), B at +8 (kBN / 32
-// columns).  Row m of an operand keeps its stage's four E8M0 bytes in lane
-// m % 32 (the same in each lane quarter), column base + m / 32; byte j of
-// that word belongs to the stage's j-th block of 32 and is picked by the
-// MMA's scale-factor id.
-constexpr uint32_t kAccStride = 256;
-constexpr int kSfSlotsLow = (kAccStride - kBN) / 16;
-__host__ __device__ constexpr uint32_t sf_col(int s) {
-    return s < kSfSlotsLow ? kBN + 16 * s : kAccStride + kBN + 16 * (s - kSfSlotsLow);
-}
+// Tensor-memory columns: the fp32 accumulator at [0, kBN); the scale-factor
+// ring after it, 16 columns per shared-memory stage: A at +0 (4 columns), B
+// at +8 (kBN / 32 columns).  Row m of an operand keeps its stage's four E8M0
+// bytes in lane m % 32 of every lane quarter, column base + m / 32 (each
+// quarter of the tensor core reads its own copy); byte j of that word
+// belongs to the stage's j-th block of 32 and is picked by the MMA's
+// scale-factor id.
+constexpr uint32_t kColSf = kBN;
+__host__ __device__ constexpr uint32_t sf_col(int s) { return kColSf + 16 * s; }
 constexpr int kMaxExperts = MOE_MAX_EXPERTS;
 static_assert(kBN % 64 == 0 && kBN / 32 <= 8, "tile width: whole chunk pairs, B scales in 8 columns");
-static_assert(sf_col(kStages - 1) + 16 <= kTmemCols && 2 * kSfSlotsLow >= kStages, "tensor-memory columns");
+static_assert(sf_col(kStages) <= kTmemCols, "tensor-memory columns");
+// Register split between the warpgroups (setmaxnreg): launched with
+// kLaunchRegs per thread, warpgroup 0 (TMA, MMA) gives registers up to the
+// scale-factor feeders (warpgroup 1) and the epilogue (warpgroups 2, 3),
+// which holds a thread's half row of the accumulator in registers.
+constexpr int kLaunchRegs = 65536 / kThreads;
+constexpr int kRegsCtl = 48, kRegsSf = 144, kRegsEpi = 160;
+static_assert(kRegsCtl + kRegsSf + 2 * kRegsEpi == 4 * kLaunchRegs, "register split sums to the launch's share");
 
 struct GemmParams {
     const int32_t* offsets;     // [E+1] grouped row ranges
@@ -101,16 +106,18 @@ struct __align__(1024) Smem {
     uint64_t full[kStages];      // TMA bytes landed
     uint64_t sf_full[kStages];   // scale factors of the stage written to tensor memory
     uint64_t empty[kStages];     // MMAs of the stage finished (smem and scale slot free)
-    uint64_t acc_full[2];        // accumulator holds a finished tile
-    uint64_t acc_empty[2];       // epilogue has read the accumulator
+    uint64_t acc_full;           // accumulator holds a finished tile
+    uint64_t acc_empty;          // epilogue has read the accumulator into registers
     uint64_t mma_done;
     uint32_t tmem_base;
-    int32_t mt_prefix[kMaxExperts + 1];
+    int32_t mt_prefix[kMaxExperts + 1];  // first 128-row tile of each expert
+    int32_t offs[kMaxExperts + 1];       // copy of the group offsets
+    int32_t slot[kMaxExperts];           // copy of the slot map
     uint32_t n_tiles;
 };
 
 struct Tile {
-    int e, m0, rows, nt;
+    int e, m0, rows, nt, slot;
 };
 
 __device__ __forceinline__ Tile decode_tile(const Smem& sm, const GemmParams& p, int t, int NT) {
@@ -125,14 +132,54 @@ __device__ __forceinline__ Tile decode_tile(const Smem& sm, const GemmParams& p,
     // skip experts with no tiles (equal prefix values)
     while (lo + 1 < p.E && sm.mt_prefix[lo + 1] <= mt) ++lo;
     tl.e = lo;
-    const int off = p.offsets[lo];
-    tl.m0 = off + (mt - sm.mt_prefix[lo]) * kBM;
-    tl.rows = min(kBM, p.offsets[lo + 1] - tl.m0);
+    tl.m0 = sm.offs[lo] + (mt - sm.mt_prefix[lo]) * kBM;
+    tl.rows = min(kBM, sm.offs[lo + 1] - tl.m0);
+    tl.slot = sm.slot[lo];
     return tl;
+}
+
+constexpr int kRb = kBN / 32;  // 32-row groups of a B tile
+
+// Scale bytes of group g (stages 4g..4g+3) of a tile's rows for feeder lane
+// `lane`: A rows m0 + 32c + lane, B rows nt * kBN + 32c + lane (clamped to
+// the last row; the clamped rows' factors only meet padding).
+__device__ __forceinline__ void sf_load_group(const GemmParams& p, const Tile& tl, int lane, int g, uint4 (&xa)[4],
+                                              uint4 (&xb)[kRb]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int arow = min(tl.m0 + 32 * c + lane, p.A - 1);
+        xa[c] = __ldg(reinterpret_cast<const uint4*>(p.a_scales + (size_t)arow * p.a_sf_stride) + g);
+    }
+    const uint8_t* bb = p.b_base + (size_t)tl.slot * p.expert_bytes + p.b_code_bytes;
+#pragma unroll
+    for (int c = 0; c < kRb; ++c) {
+        const int brow = min(tl.nt * kBN + 32 * c + lane, p.N - 1);
+        xb[c] = __ldg(reinterpret_cast<const uint4*>(bb + (size_t)brow * p.b_rs) + g);
+    }
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
     return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// 32 lanes x 16 columns into v[0..15] (v indexes a register array after unrolling).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
 }
 
 __device__ __forceinline__ float e8m0_inv_scale_f(uint32_t sb) {
@@ -159,17 +206,23 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = warp >> 2;
     volatile uint32_t* err = p.err;
 
     // ---- set-up: tile prefix over experts, barriers, tensor memory ----
+    // The offsets and the slot map are copied to shared memory once, so a
+    // tile start costs no global-memory round trip in any role.
     if (warp == 0) {
         int carry = 0;
         for (int base = 0; base < p.E; base += 32) {
             const int e = base + lane;
             int v = 0;
             if (e < p.E) {
-                const int n = p.offsets[e + 1] - p.offsets[e];
-                v = (n + kBM - 1) / kBM;
+                const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
+                sm.offs[e] = o0;
+                if (e == p.E - 1) sm.offs[p.E] = o1;
+                sm.slot[e] = p.slot_of[e];
+                v = (o1 - o0 + kBM - 1) / kBM;
             }
             int incl = v;
 #pragma unroll
@@ -189,10 +242,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                 tc::mbar_init(&sm.sf_full[s], 128);
                 tc::mbar_init(&sm.empty[s], 1);
             }
-            for (int b = 0; b < 2; ++b) {
-                tc::mbar_init(&sm.acc_full[b], 1);
-                tc::mbar_init(&sm.acc_empty[b], 128);
-            }
+            tc::mbar_init(&sm.acc_full, 1);
+            tc::mbar_init(&sm.acc_empty, 256);
             tc::mbar_init(&sm.mma_done, 1);
             tc::fence_barrier_init();
             tc::tma_prefetch_desc(&map_a);
@@ -209,14 +260,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
     const int n_tiles = int(sm.n_tiles);
     const int n_kstages = (p.K + kBK - 1) / kBK;
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
+    if (wg == 0) {
+        setmaxnreg_dec<kRegsCtl>();
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer ----------------
             int stage = 0;
             uint32_t phase = 0;
             for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x) {
                 const Tile tl = decode_tile(sm, p, t, NT);
-                const int slot = p.slot_of[tl.e];
+                const int slot = tl.slot;
                 if (slot < 0 || slot >= p.S) {
                     atomicOr(const_cast<uint32_t*>(err), 4u);
                     break;
@@ -229,19 +281,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer ----------------
             int stage = 0;
             uint32_t phase = 0;
             int i = 0;
             for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x, ++i) {
-                const int buf = i & 1;
-                // the epilogue has drained this buffer (tile i - 2)
-                if (!tc::mbar_wait(&sm.acc_empty[buf], ((i >> 1) & 1) ^ 1u, err, 2u)) break;
+                // the epilogue has read tile i - 1 out of the accumulator
+                if (!tc::mbar_wait(&sm.acc_empty, (i & 1) ^ 1u, err, 2u)) break;
                 tc::tc_fence_after();
-                const uint32_t d = tmem + buf * kAccStride;
                 bool ok = true;
                 for (int ks = 0; ks < n_kstages; ++ks) {
                     if (!tc::mbar_wait(&sm.full[stage], phase, err, 2u) ||
@@ -258,54 +306,127 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                         const int kb = ks * (kBK / 32) + kk;
                         if (kb < p.KB) {
                             const uint32_t idesc = tc::idesc_mxf8f6f4(0, 5, kBM, kBN, kk, kk);
-                            tc::mma_mxf8f6f4(d, tc::smem_desc_sw128(a0 + kk * 32), tc::smem_desc_sw128(b0 + kk * 32),
-                                             idesc, sfa, sfa + 8, (ks | kk) != 0);
+                            tc::mma_mxf8f6f4(tmem, tc::smem_desc_sw128(a0 + kk * 32),
+                                             tc::smem_desc_sw128(b0 + kk * 32), idesc, sfa, sfa + 8,
+                                             (ks | kk) != 0);
                         }
                     }
                     tc::mma_commit(&sm.empty[stage]);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc::mma_commit(&sm.acc_full[buf]);
+                tc::mma_commit(&sm.acc_full);
             }
             // all MMAs issued by this CTA have finished before TMEM is freed
             tc::mma_commit(&sm.mma_done);
             tc::mbar_wait(&sm.mma_done, 0, err, 16u);
         }
-    } else if (warp < 6) {
-        // ---------------- epilogue (warps 2..5 = TMEM lane quarters 2,3,0,1) ----------------
+    } else if (wg == 1) {
+        setmaxnreg_inc<kRegsSf>();
+        // ---------------- scale-factor feeders (warps 4..7 = lane quarters 0..3) ----------------
+        // Thread (quarter q, lane l) writes lane 32q + l of the ring slot:
+        // column c of the A part gets the stage's four scale bytes of
+        // activation row 32c + l (c < 4), column c of the B part those of
+        // weight row 32c + l (c < kBN / 32).  Each row's bytes are read 16 at
+        // a time (a group of four stages), one group ahead -- across tile
+        // boundaries too, so a new tile's first stages never wait for loads.
         const int q = warp & 3;
-        const int r = q * 32 + lane;                // tile row == TMEM lane
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+        const int ngroups = (n_kstages + 3) / 4;
+        int stage = 0;
+        uint32_t phase = 0;
+        int t = blockIdx.x;
+        Tile tl{};
+        uint4 xa[4], xb[kRb];
+        bool have = false;
+        if (t < n_tiles) {
+            tl = decode_tile(sm, p, t, NT);
+            if (tl.slot >= 0 && tl.slot < p.S) {
+                sf_load_group(p, tl, lane, 0, xa, xb);
+                have = true;
+            }
+        }
+        while (have && !*err) {
+            const int tn = t + gridDim.x;
+            Tile nx{};
+            bool next_ok = false, ok = true;
+            for (int g = 0; g < ngroups && ok; ++g) {
+                uint4 na[4], nb[kRb];
+                if (g + 1 < ngroups) {
+                    sf_load_group(p, tl, lane, g + 1, na, nb);
+                } else if (tn < n_tiles) {
+                    nx = decode_tile(sm, p, tn, NT);
+                    next_ok = nx.slot >= 0 && nx.slot < p.S;
+                    if (next_ok) sf_load_group(p, nx, lane, 0, na, nb);
+                }
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    if (4 * g + w >= n_kstages) break;
+                    if (!tc::mbar_wait(&sm.empty[stage], phase ^ 1u, err, 64u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t col = lane_base + sf_col(stage);
+                    tc::tmem_st_x4(col, word_of(xa[0], w), word_of(xa[1], w), word_of(xa[2], w), word_of(xa[3], w));
+                    uint32_t bw[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) bw[c] = c < kRb ? word_of(xb[c < kRb ? c : 0], w) : 0u;
+                    tc::tmem_st_x8(col + 8, bw);
+                    tc::tmem_st_wait();
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&sm.sf_full[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (g + 1 < ngroups || next_ok) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) xa[c] = na[c];
+#pragma unroll
+                    for (int c = 0; c < kRb; ++c) xb[c] = nb[c];
+                }
+            }
+            if (!ok || !next_ok) break;
+            t = tn;
+            tl = nx;
+        }
+    } else {
+        setmaxnreg_inc<kRegsEpi>();
+        // ---------------- epilogue (warps 8..15) ----------------
+        // Warp w serves lane quarter w % 4 (tile rows) and half (w - 8) / 4
+        // of the tile's columns.  It copies its 32 rows x kBN/2 columns of
+        // the accumulator into registers, releases the accumulator to the
+        // next tile's MMAs, and finishes the tile from registers.
+        constexpr int kHalf = kBN / 2;
+        const int q = warp & 3, hh = wg - 2;
+        const int r = q * 32 + lane;                // tile row == TMEM lane
+        const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16) + uint32_t(hh * kHalf);
         int i = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
             if (*err) break;
             const Tile tl = decode_tile(sm, p, t, NT);
-            const int buf = i & 1;
-            if (!tc::mbar_wait(&sm.acc_full[buf], (i >> 1) & 1, err, 8u)) break;
+            if (!tc::mbar_wait(&sm.acc_full, i & 1, err, 8u)) break;
             tc::tc_fence_after();
-            const uint32_t acc = lane_base + buf * kAccStride;
+            uint32_t v[kHalf];
+#pragma unroll
+            for (int c = 0; c < kHalf / 16; ++c) tmem_ld16(lane_base + 16 * c, &v[16 * c]);
+            tc::tmem_ld_wait();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sm.acc_empty);
             const bool valid = r < tl.rows;
             const int m = tl.m0 + r;
             if (p.mode == 0) {
-                // columns 64j..64j+31: gate rows of chunk c = 3 nt + j (h columns
-                // 32c..32c+31); 64j+32..64j+63: the matching up rows
-#pragma unroll 1
-                for (int half = 0; half < kBN / 64; ++half) {
-                    const int chunk = tl.nt * (kBN / 64) + half;
+                // columns 64j..64j+31 of the tile: gate rows of chunk c = (kBN/64) nt + j
+                // (h columns 32c..32c+31); 64j+32..64j+63: the matching up rows
+#pragma unroll
+                for (int jj = 0; jj < kHalf / 64; ++jj) {
+                    const int chunk = tl.nt * (kBN / 64) + hh * (kHalf / 64) + jj;
                     if (chunk * 32 >= p.I) break;   // ragged last tile (warp-uniform)
-                    uint32_t g0[16], g1[16], u0[16], u1[16];
-                    tc::tmem_ld_x16(acc + half * 64, g0);
-                    tc::tmem_ld_x16(acc + half * 64 + 16, g1);
-                    tc::tmem_ld_x16(acc + half * 64 + 32, u0);
-                    tc::tmem_ld_x16(acc + half * 64 + 48, u1);
-                    tc::tmem_ld_wait();
                     float hv[32];
                     float amax = 0.0f;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float g = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
-                        const float u = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
+                        const float g = __uint_as_float(v[64 * jj + j]);
+                        const float u = __uint_as_float(v[64 * jj + 32 + j]);
                         const float s = g / (1.0f + expf(-g));
                         const float hb = __bfloat162float(__float2bfloat16_rn(s * u));
                         hv[j] = hb;
@@ -330,96 +451,25 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                         }
                     }
                 }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < kBN / 16; ++c) {
-                    uint32_t v[16];
-                    tc::tmem_ld_x16(acc + c * 16, v);
-                    tc::tmem_ld_wait();
-                    const int n = tl.nt * kBN + c * 16;
-                    if (valid && n < p.N) {
+            } else if (valid) {
+#pragma unroll
+                for (int c = 0; c < kHalf / 16; ++c) {
+                    const int n = tl.nt * kBN + hh * kHalf + c * 16;
+                    if (n < p.N) {
                         float4* dst = reinterpret_cast<float4*>(p.y + (size_t)m * p.N + n);
                         if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0 || m >= p.A) {
                             atomicOr(const_cast<uint32_t*>(err), 32u);
-                            continue;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                dst[j] = make_float4(__uint_as_float(v[16 * c + 4 * j]),
+                                                     __uint_as_float(v[16 * c + 4 * j + 1]),
+                                                     __uint_as_float(v[16 * c + 4 * j + 2]),
+                                                     __uint_as_float(v[16 * c + 4 * j + 3]));
                         }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                     }
                 }
             }
-            tc::tc_fence_before();
-            tc::mbar_arrive(&sm.acc_empty[buf]);
-        }
-    } else {
-        // ---------------- scale-factor feeders (warps 6..9 = lane quarters 2,3,0,1) ----------------
-        // Thread (quarter q, lane l) writes lane 32q + l of the ring slot:
-        // column c of the A part gets the stage's four scale bytes of
-        // activation row 32c + l (c < 4), column c of the B part those of
-        // weight row 32c + l (c < kBN / 32).  Each row's bytes are read 16 at
-        // a time (four stages), one group of four stages ahead.
-        constexpr int kRb = kBN / 32;
-        const int q = warp & 3;
-        const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x) {
-            const Tile tl = decode_tile(sm, p, t, NT);
-            const int slot = p.slot_of[tl.e];
-            if (slot < 0 || slot >= p.S) break;
-            const uint4* as[4];
-            const uint4* bs[kRb];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int arow = min(tl.m0 + 32 * c + lane, p.A - 1);
-                as[c] = reinterpret_cast<const uint4*>(p.a_scales + (size_t)arow * p.a_sf_stride);
-            }
-#pragma unroll
-            for (int c = 0; c < kRb; ++c) {
-                const int brow = min(tl.nt * kBN + 32 * c + lane, p.N - 1);
-                bs[c] = reinterpret_cast<const uint4*>(p.b_base + (size_t)slot * p.expert_bytes +
-                                                       (size_t)brow * p.b_rs + p.b_code_bytes);
-            }
-            uint4 xa[4], xb[kRb];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) xa[c] = __ldg(as[c]);
-#pragma unroll
-            for (int c = 0; c < kRb; ++c) xb[c] = __ldg(bs[c]);
-            bool ok = true;
-            for (int ks0 = 0; ks0 < n_kstages && ok; ks0 += 4) {
-                const bool more = ks0 + 4 < n_kstages;
-                uint4 na[4], nb[kRb];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) na[c] = more ? __ldg(as[c] + ks0 / 4 + 1) : xa[c];
-#pragma unroll
-                for (int c = 0; c < kRb; ++c) nb[c] = more ? __ldg(bs[c] + ks0 / 4 + 1) : xb[c];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    if (ks0 + w >= n_kstages) break;
-                    if (!tc::mbar_wait(&sm.empty[stage], phase ^ 1u, err, 64u)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    const uint32_t col = lane_base + sf_col(stage);
-                    tc::tmem_st_x4(col, word_of(xa[0], w), word_of(xa[1], w), word_of(xa[2], w), word_of(xa[3], w));
-                    uint32_t bw[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) bw[c] = c < kRb ? word_of(xb[c < kRb ? c : 0], w) : 0u;
-                    tc::tmem_st_x8(col + 8, bw);
-                    tc::tmem_st_wait();
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(&sm.sf_full[stage]);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) xa[c] = na[c];
-#pragma unroll
-                for (int c = 0; c < kRb; ++c) xb[c] = nb[c];
-            }
-            if (!ok) break;
         }
     }
 
@@ -504,7 +554,13 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& 
     if (rc != MOE_OK) return rc;
     if (di.cc_major < 10) return MOE_ERR_UNSUPPORTED;
     if (smem_bytes() > di.smem_optin) return MOE_ERR_UNSUPPORTED;
+    if (di.device >= 64) return MOE_ERR_UNSUPPORTED;
     if (!attr_set[di.device]) {
+        // The warpgroups' register split must add up to exactly what the
+        // launch grants each thread, or a setmaxnreg.inc would wait forever.
+        cudaFuncAttributes fa{};
+        MOE_CUDA_TRY(cudaFuncGetAttributes(&fa, grouped_gemm_tc_kernel));
+        if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return MOE_ERR_UNSUPPORTED;
         MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem_bytes()));
         attr_set[di.device] = true;
