@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "internal.h"
@@ -68,6 +69,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSf = kBN;
 __host__ __device__ constexpr uint32_t sf_col(int s) { return kColSf + 16 * s; }
 constexpr int kMaxExperts = MOE_MAX_EXPERTS;
+constexpr int kYPad = 20;          // padded row of the epilogue's y staging tile (words)
 static_assert(kBN % 64 == 0 && kBN / 32 <= 8, "tile width: whole chunk pairs, B scales in 8 columns");
 static_assert(sf_col(kStages) <= kTmemCols, "tensor-memory columns");
 // Register split between the warpgroups (setmaxnreg): launched with
@@ -114,7 +116,13 @@ struct __align__(1024) Smem {
     int32_t offs[kMaxExperts + 1];       // copy of the group offsets
     int32_t slot[kMaxExperts];           // copy of the slot map
     uint32_t n_tiles;
+    // per epilogue warp: 32 rows x 16 fp32 of y, rows padded to 20 words so
+    // both the row-wise writes and the column-wise reads are conflict-free
+    __align__(16) float ystage[8][32 * kYPad];
 };
+static_assert(offsetof(Smem, ystage) % 16 == 0 && (32 * kYPad * 4) % 16 == 0, "16-byte staging rows");
+static_assert(offsetof(Smem, b) % 1024 == 0 && kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0,
+              "128-byte-swizzled operand tiles start on 1024-byte boundaries");
 
 struct Tile {
     int e, m0, rows, nt, slot;
@@ -451,23 +459,37 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                         }
                     }
                 }
-            } else if (valid) {
+            } else {
+                // y rows leave through a per-warp shared tile so that a store
+                // instruction writes 64 contiguous bytes in each of 8 rows
+                // instead of 16 bytes in each of 32 rows.
+                float* st = sm.ystage[warp - 8];
+                const int rr0 = lane >> 2, qq = lane & 3;
 #pragma unroll
                 for (int c = 0; c < kHalf / 16; ++c) {
-                    const int n = tl.nt * kBN + hh * kHalf + c * 16;
-                    if (n < p.N) {
-                        float4* dst = reinterpret_cast<float4*>(p.y + (size_t)m * p.N + n);
-                        if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0 || m >= p.A) {
-                            atomicOr(const_cast<uint32_t*>(err), 32u);
-                        } else {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                dst[j] = make_float4(__uint_as_float(v[16 * c + 4 * j]),
-                                                     __uint_as_float(v[16 * c + 4 * j + 1]),
-                                                     __uint_as_float(v[16 * c + 4 * j + 2]),
-                                                     __uint_as_float(v[16 * c + 4 * j + 3]));
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<float4*>(st + lane * kYPad + 4 * j) =
+                            make_float4(__uint_as_float(v[16 * c + 4 * j]), __uint_as_float(v[16 * c + 4 * j + 1]),
+                                        __uint_as_float(v[16 * c + 4 * j + 2]),
+                                        __uint_as_float(v[16 * c + 4 * j + 3]));
+                    __syncwarp();
+                    const int n = tl.nt * kBN + hh * kHalf + c * 16 + 4 * qq;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int rr = rr0 + 8 * j;              // row within this warp's 32
+                        const int row = q * 32 + rr;             // row within the tile
+                        const float4 val = *reinterpret_cast<const float4*>(st + rr * kYPad + 4 * qq);
+                        if (row < tl.rows && n < p.N) {
+                            const int mm = tl.m0 + row;
+                            float4* dst = reinterpret_cast<float4*>(p.y + (size_t)mm * p.N + n);
+                            if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0 || mm >= p.A)
+                                atomicOr(const_cast<uint32_t*>(err), 32u);
+                            else
+                                *dst = val;
                         }
                     }
+                    __syncwarp();
                 }
             }
         }
