@@ -162,8 +162,10 @@ MOE_API int moe_route_plan(const float* logits, int T, int E, int k,
  *   MOE_ERR_INVALID before anything is enqueued.
  *   The first call on a device resolves the array's device address for that
  *   device (with it current); make that first call before any stream
- *   capture.  The array needs no clearing (each call overwrites what it
- *   reads), but all calls share it: calls that can overlap on the GPU race.
+ *   capture.  Each call clears the part of the array it uses with an
+ *   asynchronous memset on `stream` (no allocation) before counting into
+ *   it; all calls share the array, so calls that can overlap on the GPU
+ *   race.
  * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
 MOE_API int moe_route_plan_noalloc(const float* logits, int T, int E, int k,
                                    int32_t* ids, float* w, int32_t* counts, int32_t* offsets,

@@ -36,46 +36,104 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// One lane quantises one 32-element block: 64 bytes in, 32 codes + 1 scale out.
+// One lane quantises one 32-element block (64 bytes of bf16 in, 32 codes +
+// 1 scale out); a warp handles a run of 32 consecutive blocks of one row.
+__device__ __forceinline__ void quant_block(const uint16_t* __restrict__ xrow, int b, bool act, uint32_t (&w)[8],
+                                            uint32_t& sb) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = 0;
+    sb = 0;
+    if (!act) return;
+    const uint4* p = reinterpret_cast<const uint4*>(xrow + (size_t)b * 32);
+    uint4 v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = __ldg(p + c);
+    float f[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[c * 8 + 2 * j] = __uint_as_float(u[j] << 16);
+            f[c * 8 + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+        }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    sb = e8m0_of_amax(amax);
+    const float m = inv_scale(sb);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t a = cvt_e4m3x2(f[4 * j] * m, f[4 * j + 1] * m);
+        const uint32_t c = cvt_e4m3x2(f[4 * j + 2] * m, f[4 * j + 3] * m);
+        w[j] = a | (c << 16);
+    }
+}
+
+// Stores a warp's run of quantised blocks (lane l holds block b0 + l) to
+// row `out` (already offset to block b0): the warp exchanges halves with
+// shuffles so that each store instruction writes 512 contiguous bytes
+// (blocks 16i..16i+15 of the run) rather than 16 bytes in each of 32 blocks.
+__device__ __forceinline__ void store_run(uint8_t* out, const uint32_t (&w)[8], int nvalid, int lane) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int srcl = 16 * i + (lane >> 1);
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = __shfl_sync(0xffffffffu, w[j], srcl);
+            const uint32_t hi = __shfl_sync(0xffffffffu, w[4 + j], srcl);
+            o[j] = (lane & 1) ? hi : lo;
+        }
+        if (srcl < nvalid)
+            *reinterpret_cast<uint4*>(out + 512 * i + 16 * lane) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// Gather form: output row r is the quantised x row perm[r] / k (or r when
+// perm is null).  Warp w handles blocks 32c..32c+31 of output row r,
+// (r, c) = divmod(w, warps_per_row).
 __global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint16_t* __restrict__ x, int K,
                                                           const int32_t* __restrict__ perm, int k, int rows,
                                                           uint8_t* __restrict__ q, uint8_t* __restrict__ scales,
-                                                          int scale_stride) {
+                                                          int scale_stride, int warps_per_row) {
     const int nb = K / 32;
-    const long total = (long)rows * nb;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const int row = int(i / nb), b = int(i - (long)row * nb);
-        const int src = perm ? perm[row] / k : row;
-        const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)src * K + (size_t)b * 32);
-        uint4 v[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = __ldg(p + c);
-        float f[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[c * 8 + 2 * j] = __uint_as_float(u[j] << 16);
-                f[c * 8 + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
-            }
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
-        const uint32_t sb = e8m0_of_amax(amax);
-        const float m = inv_scale(sb);
-        uint32_t w[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t a = cvt_e4m3x2(f[4 * j] * m, f[4 * j + 1] * m);
-            const uint32_t c = cvt_e4m3x2(f[4 * j + 2] * m, f[4 * j + 3] * m);
-            w[j] = a | (c << 16);
-        }
-        uint4* o = reinterpret_cast<uint4*>(q + (size_t)row * K + (size_t)b * 32);
-        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        scales[(size_t)row * scale_stride + b] = uint8_t(sb);
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int row = gw / warps_per_row;               // warp-uniform
+    const int b0 = (gw - row * warps_per_row) * 32;
+    if (row >= rows) return;                           // whole warp
+    const int nvalid = min(32, nb - b0);
+    const int src = perm ? perm[row] / k : row;
+    uint32_t w[8], sb;
+    quant_block(x + (size_t)src * K, b0 + lane, lane < nvalid, w, sb);
+    if (lane < nvalid) scales[(size_t)row * scale_stride + b0 + lane] = uint8_t(sb);
+    store_run(q + (size_t)row * K + (size_t)b0 * 32, w, nvalid, lane);
+}
+
+// Scatter form for the grouped prefill operand: token t's row is read and
+// quantised once, then written to the grouped rows inv[t*k + j], j < k.
+// (Quantisation does not depend on the expert, and reading each token once
+// keeps x from being re-read from DRAM k times in grouped order.)
+__global__ void __launch_bounds__(256) quant_mxfp8_scatter_kernel(const uint16_t* __restrict__ x, int K,
+                                                                  const int32_t* __restrict__ inv, int k, int T,
+                                                                  uint8_t* __restrict__ q,
+                                                                  uint8_t* __restrict__ scales, int scale_stride,
+                                                                  int warps_per_row) {
+    const int nb = K / 32;
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int t = gw / warps_per_row;                 // warp-uniform
+    const int b0 = (gw - t * warps_per_row) * 32;
+    if (t >= T) return;                                // whole warp
+    const int nvalid = min(32, nb - b0);
+    uint32_t w[8], sb;
+    quant_block(x + (size_t)t * K, b0 + lane, lane < nvalid, w, sb);
+    for (int j = 0; j < k; ++j) {
+        const int row = inv[(size_t)t * k + j];
+        if (lane < nvalid) scales[(size_t)row * scale_stride + b0 + lane] = uint8_t(sb);
+        store_run(q + (size_t)row * K + (size_t)b0 * 32, w, nvalid, lane);
     }
 }
 
@@ -126,8 +184,27 @@ int grid_for(long work, int threads) {
 
 int launch_quant_mxfp8(const uint16_t* x, int K, const int32_t* perm, int k, int rows, uint8_t* q,
                        uint8_t* scales, int scale_stride, cudaStream_t s) {
-    const long work = (long)rows * (K / 32);
-    quant_mxfp8_kernel<<<grid_for(work, 256), 256, 0, s>>>(x, K, perm, k, rows, q, scales, scale_stride);
+    // one warp per 32 blocks of a row: the gather (perm, then x) is a
+    // dependent load chain, so memory parallelism comes from many warps
+    const int warps_per_row = (K / 32 + 31) / 32;
+    const long warps = (long)rows * warps_per_row;
+    const long grid = (warps + 7) / 8;
+    if (grid > 0x7fffffffL || warps > 0x7fffffffL) return MOE_ERR_UNSUPPORTED;
+    if (grid == 0) return MOE_OK;
+    quant_mxfp8_kernel<<<(unsigned)grid, 256, 0, s>>>(x, K, perm, k, rows, q, scales, scale_stride, warps_per_row);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int launch_quant_mxfp8_scatter(const uint16_t* x, int K, const int32_t* inv, int k, int T, uint8_t* q,
+                               uint8_t* scales, int scale_stride, cudaStream_t s) {
+    const int warps_per_row = (K / 32 + 31) / 32;
+    const long warps = (long)T * warps_per_row;
+    const long grid = (warps + 7) / 8;
+    if (grid > 0x7fffffffL || warps > 0x7fffffffL) return MOE_ERR_UNSUPPORTED;
+    if (grid == 0) return MOE_OK;
+    quant_mxfp8_scatter_kernel<<<(unsigned)grid, 256, 0, s>>>(x, K, inv, k, T, q, scales, scale_stride,
+                                                              warps_per_row);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }

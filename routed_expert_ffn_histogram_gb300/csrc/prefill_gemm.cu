@@ -636,7 +636,7 @@ int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
     MOE_CUDA_TRY(cudaMemsetAsync(err, 0, 4, s));
     MOE_CUDA_TRY(cudaMemsetAsync(xs, 0, size_t(A) * w.xs_stride, s));
     MOE_CUDA_TRY(cudaMemsetAsync(hs, 0, size_t(A) * w.hs_stride, s));
-    int rc = launch_quant_mxfp8(a.x, L.H, a.perm, a.k, A, xq, xs, w.xs_stride, s);
+    int rc = launch_quant_mxfp8_scatter(a.x, L.H, a.inv, a.k, a.T, xq, xs, w.xs_stride, s);
     if (rc != MOE_OK) return rc;
 
     CUtensorMap map_x, map_gu, map_h, map_d;

@@ -144,18 +144,27 @@ __global__ void __launch_bounds__(kThreads) route_single_kernel(
     scatter_tile(ids, 0, T * k, E, perm, inv, sm);
 }
 
-// Multi-tile, pass 1: top-k + per-tile histogram (32 warps per tile).
-constexpr int kTopkThreads = 1024;
+// Multi-tile, pass 1: top-k + softmax, one warp per token and kTopkWarps
+// tokens per CTA, so every SM has tokens in flight (the per-token work is a
+// latency chain of shuffles); each token adds its k experts to the
+// histogram of its kTileTokens tile in tile_hist (zeroed before launch).
+constexpr int kTopkWarps = 8;
 template <int EPL>
-__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
+__global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ tile_hist) {
-    __shared__ int hist[MOE_MAX_EXPERTS];
-    if (threadIdx.x < MOE_MAX_EXPERTS) hist[threadIdx.x] = 0;
-    __syncthreads();
-    topk_tokens<EPL>(logits, T, E, k, ids, w, blockIdx.x * kTileTokens, kTileTokens, hist);
-    __syncthreads();
-    if (threadIdx.x < E) tile_hist[(size_t)blockIdx.x * E + threadIdx.x] = hist[threadIdx.x];
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    if (t >= T) return;  // whole warp
+    float sel_v;
+    int sel_id;
+    topk_warp<EPL>(logits + (size_t)t * E, E, k, sel_v, sel_id);
+    const float wv = softmax_lane(sel_v, k);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = sel_id;
+        w[(size_t)t * k + lane] = wv;
+        atomicAdd(&tile_hist[(size_t)(t / kTileTokens) * E + sel_id], 1);
+    }
 }
 
 // Whole plan in one warp when T * k <= 32 (the decode shapes): no shared
@@ -233,7 +242,9 @@ int launch_route_epl(const float* logits, int T, int E, int k, int32_t* ids, flo
     } else if (n_tiles <= 1) {
         route_single_kernel<EPL><<<1, kThreads, 0, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, inv);
     } else {
-        route_topk_kernel<EPL><<<n_tiles, kTopkThreads, 0, s>>>(logits, T, E, k, ids, w, tile_hist);
+        MOE_CUDA_TRY(cudaMemsetAsync(tile_hist, 0, sizeof(int32_t) * size_t(n_tiles) * E, s));
+        route_topk_kernel<EPL><<<(T + kTopkWarps - 1) / kTopkWarps, 32 * kTopkWarps, 0, s>>>(logits, T, E, k, ids,
+                                                                                             w, tile_hist);
         MOE_CUDA_TRY(cudaGetLastError());
         route_scatter_kernel<<<n_tiles, kThreads, 0, s>>>(ids, T, E, k, tile_hist, counts, offsets, perm, inv);
     }
@@ -262,8 +273,9 @@ int launch_route_plan(const float* logits, int T, int E, int k, int32_t* ids, fl
 // file-scope device array instead of a workspace.  It holds
 // kNoallocMaxTiles * MOE_MAX_EXPERTS int32 (64 KB), enough for up to
 // kNoallocMaxTiles * 256 = 16384 tokens; every GPU that loads the library
-// keeps it until the process exits.  Its contents need no clearing: each
-// call overwrites every entry it reads.  All calls share it, so calls that
+// keeps it until the process exits.  Each call clears the entries it uses
+// (an asynchronous memset on the caller's stream, not an allocation) before
+// counting into them.  All calls share it, so calls that
 // can overlap on the GPU (different streams, or different host threads
 // without ordering) race on it.
 // ---------------------------------------------------------------------------
