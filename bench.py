@@ -36,6 +36,17 @@ import moe_synth as S  # noqa: E402
 METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 roofline"
 
 
+# DRAM bytes per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from one ncu capture of the kernel as it is built
+# now; an entry goes back to None whenever that kernel changes.
+NCU_TRAFFIC = {
+    # one decode layer (2-layer decode capture; traffic per launch does not
+    # depend on the number of layers)
+    "decode_fused_kernel": 53_179_392 + 7_936,
+    # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
+    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_188_928 + 31_353_600) + (178_283_008 + 100_085_760),
+}
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -364,7 +375,9 @@ def main():
                 "roofline": {"kernel": "prefill expert FFN (MXFP8 quant, gate/up GEMM, down GEMM, combine)",
                              "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                              "frac": achieved / tc_peak, "peak_kind": peak_kind + " bf16 x 2 (FP8-class rate)",
-                             "traffic": None, "algorithmic_flops_per_launch": flops,
+                             "traffic": NCU_TRAFFIC.get("grouped_gemm_tc_kernel/" + wl.name),
+                             "traffic_scope": "DRAM bytes of the two GEMM launches of one layer",
+                             "algorithmic_flops_per_launch": flops,
                              "avg_launch_us": ffn_s * 1e6},
                 "kernels_us": {"route_plan": statistics.median(res["route_ms"]) * 1e3,
                                "expert_ffn": ffn_s * 1e6},
@@ -437,7 +450,8 @@ def main():
             "roofline": {"kernel": "decode_fused_kernel: one launch per layer (routing, gate/up+SwiGLU, "
                                    "down+combine)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "peak_kind": peak_kind, "traffic": None,
+                         "frac": achieved / hbm_peak, "peak_kind": peak_kind,
+                         "traffic": NCU_TRAFFIC["decode_fused_kernel"],
                          "algorithmic_bytes_per_launch": layer_bytes,
                          "avg_launch_us": ffn_avg_s * 1e6},
             "kernels_us": {"decode_layer": ffn_avg_s * 1e6},
