@@ -257,8 +257,11 @@ def gpu_leg(args, wl, rank, world):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = a.elapsed_time(b)
-    # the graphed and eager runs produced the same outputs
-    same = bool(torch.equal(out_pin[args.warmup:].to(dev), out_d[args.warmup:]))
+    # the graphed and eager runs produced the same outputs, up to the fp32
+    # rounding order of the cross-CTA atomic sums
+    ref_o = out_d[args.warmup:].double()
+    rel = float((out_pin[args.warmup:].to(dev).double() - ref_o).norm() / ref_o.norm().clamp_min(1e-30))
+    same = rel <= 1e-6
 
     res = dict(elapsed_ms=elapsed_ms, ffn_ms=ffn_ms, route_ms=route_ms, clocks=clk, e2e_ms=e2e_ms,
                h2d=(lg_pin[0].numel() * 4 + x_pin[0].numel() * 2), d2h=out_pin[0].numel() * 4,

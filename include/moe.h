@@ -114,7 +114,11 @@ MOE_API int moe_expert_bytes(int hidden, int inter, size_t* out_bytes);
  * The native layout keeps each row's codes followed by its scales (rows
  * padded to 32 bytes) and interleaves gate and up rows in chunks of 32 (gate rows
  * 32c..32c+31, then up rows 32c..32c+31) so one tile of the fused gate/up
- * product holds matching gate and up rows.
+ * product holds matching gate and up rows.  After the row-major down
+ * matrix it also keeps a column-blocked copy of down for the decode path:
+ * for each block of 16 columns, every row's 8 code bytes of those columns,
+ * then every row's scale byte of the 32-block they lie in (so one decode
+ * work item, 16 elements of h, reads its down weights contiguously).
  * Errors: MOE_ERR_INVALID. */
 MOE_API int moe_pack_expert(const uint8_t* gate_codes, const uint8_t* gate_scales,
                     const uint8_t* up_codes, const uint8_t* up_scales,
@@ -282,10 +286,11 @@ MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int pat
  *             tcgen05 block-scaled tensor cores, fp32 accumulation.
  *             MOE_PATH_AUTO: decode when T*k <= MOE_DECODE_MAX_ASSIGN.
  *   workspace device, >= moe_ffn_workspace_bytes(), 256-byte aligned.
- *             Its first 256 bytes hold a grid-barrier word that must be zero
- *             when the workspace is first used (allocate it zeroed); the
- *             library leaves it zero after every call.  One workspace must
- *             not be used by two calls that can run at the same time.
+ *             On the decode path it holds a completion counter and an fp32
+ *             [T][H] accumulator that must be zero when the workspace is
+ *             first used (allocate it zero-filled); the library leaves them
+ *             zero after every call.  One workspace must not be used by two
+ *             calls that can run at the same time.
  *   out       device fp32 [T][H], fully overwritten
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16, int T, int k,
@@ -300,11 +305,12 @@ MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16
  * routing and the experts).  Every CTA ranks the logits itself; the routing
  * outputs (ids, w, counts, offsets, perm, inv, as moe_route_plan defines
  * them) are written too.  Results equal moe_route_plan + moe_expert_ffn
- * (MOE_PATH_DECODE) on the same inputs.
+ * (MOE_PATH_DECODE) on the same inputs, up to fp32 rounding order: the
+ * down sums and the combine are folded across CTAs with fp32 atomics.
  *   logits   device fp32 [T][E]; x_bf16 device bf16 [T][H]
  *   slot_of  device int32 [E]: every routed expert must be resident
- *   workspace as moe_expert_ffn, MOE_PATH_DECODE (first 256 bytes zeroed
- *            before first use)
+ *   workspace as moe_expert_ffn, MOE_PATH_DECODE (zero-filled before first
+ *            use)
  * Limits: T*k <= 32.  Errors: MOE_ERR_INVALID, MOE_ERR_STATE,
  * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 MOE_API int moe_decode_layer(const moe_pool_t* pool, int layer, const float* logits,

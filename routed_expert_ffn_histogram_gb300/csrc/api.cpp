@@ -98,6 +98,16 @@ extern "C" int moe_pack_expert(const uint8_t* gc, const uint8_t* gs, const uint8
         std::memcpy(drow, dc + size_t(r) * ic, ic);
         std::memcpy(drow + ic, ds + size_t(r) * isc, isc);
     }
+    // column-blocked copy: block c holds, for every row n, the 8 code bytes
+    // of elements 16c..16c+15 and then, for every row, its scale of block c/2
+    constexpr int dc_cols = Layout::kDtCols;
+    for (int c = 0; c < inter / dc_cols; ++c) {
+        uint8_t* blk = o + L.dt_off + size_t(c) * L.dt_stride;
+        for (int r = 0; r < hidden; ++r) {
+            std::memcpy(blk + size_t(r) * (dc_cols / 2), dc + size_t(r) * ic + size_t(c) * (dc_cols / 2), dc_cols / 2);
+            blk[size_t(hidden) * (dc_cols / 2) + r] = ds[size_t(r) * isc + size_t(c) * dc_cols / 32];
+        }
+    }
     return MOE_OK;
 }
 

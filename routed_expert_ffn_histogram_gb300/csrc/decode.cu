@@ -314,9 +314,13 @@ int launch_down_nit(const DecodeParams& p, int T, cudaStream_t s) {
 
 }  // namespace
 
+// Decode workspace: [0, 256) control words (zero between calls), then h as
+// bf16 [T*k][I] (two-kernel path), then the fp32 [T][H] accumulator of the
+// fused kernel (zero between calls).
+size_t decode_acc_offset(int T, int k, int I) { return 256 + round_up(size_t(T) * k * I * 2, 256); }
+
 size_t decode_workspace_bytes(int T, int k, int H, int I) {
-    (void)H;
-    return 256 + round_up(size_t(T) * k * I * 2, 256);
+    return decode_acc_offset(T, k, I) + round_up(size_t(T) * H * 4, 256);
 }
 
 int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {

@@ -1,5 +1,6 @@
 // Decode path, fused: the whole expert FFN of one layer (gate/up + SwiGLU,
-// down + weighted combine) in one persistent cooperative kernel.
+// down + weighted combine) in one kernel, with the routing of the token(s)
+// folded in for moe_decode_layer.
 //
 // Source: tinyserve README, "How it works" item 2 -- gate, up and down run
 // directly on the quantised bytes, with no intermediate BF16 weights;
@@ -10,27 +11,30 @@
 //
 // Arithmetic is the decode path's: bf16 activation x fp32-dequantised fp4
 // (every product exact in fp32), fp32 sums, SwiGLU in fp32 rounded to bf16,
-// down product on bf16(h), combine sum_j w_j * y_j in ascending j.
+// down product on bf16(h), combine of w_j * y_j in fp32.  The down sums
+// and the combine are split over CTAs and folded with fp32 atomics, so
+// their rounding order (not their value beyond fp32 rounding) varies
+// between runs.
 //
-// Shape: one CTA per SM, 24 warps each, all co-resident (cooperative
-// launch).  Each CTA owns a contiguous range of (assignment, row) items of
-// the gate/up product and a contiguous range of output rows of the down
-// product, and first asks L2 to prefetch exactly those weight bytes
-// (cp.async.bulk.prefetch), gate/up first: HBM then streams the layer's
-// experts at full rate whatever the warps are doing, and the warps' loads
-// meet the data in L2.
-//   phase 1  a warp takes one item at a time: the gate row and the up row
-//            (32 rows apart in the packed layout), one 16-byte load = one MX
+// Shape: one CTA per SM, 17 warps.  The work is cut into items of 16
+// consecutive rows of h for one assignment: the 16 gate rows and 16 up rows
+// (contiguous in the packed layout, two bulk copies) and the matching
+// 16-column block of the column-blocked down copy (one bulk copy), streamed
+// by warp 0 through a shared-memory ring.
+//   gate/up  warp j takes row pair j of the item: one 16-byte load = one MX
 //            block per lane; x is staged once per CTA in shared memory as
 //            f16 scaled per 32-block by a power of two (exact for every
 //            value within 2^-31 of the block maximum) in XOR-swizzled
 //            16-byte chunks; E2M1 pairs become f16x2 by hardware conversion
-//            and multiply-add into fp32 (products exact); lane 0 writes
-//            bf16(silu(g) * u).
-//   barrier  bounded grid barrier (arrival counter zeroed before launch).
-//   phase 2  h of a token staged per CTA the same way; a warp takes an
-//            output row, reads that row of all k experts, and folds
-//            w_j * y_j in rank order.
+//            and multiply-add into fp32 (products exact); h = bf16(silu(g)*u).
+//   down     the 16 h values (f16 under one power-of-2 scale) times the
+//            block's codes, every consumer thread owning fixed output rows;
+//            partial sums stay in registers across an assignment's items.
+//   combine  w_a * y added to an fp32 accumulator in the workspace; the last
+//            CTA to finish (a ticket counter, no waiting) copies it to the
+//            output and clears it for the next call.
+// No CTA waits for another: there is no grid barrier and no cooperative
+// launch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -48,17 +52,6 @@ constexpr int kGroup = 16;             // row pairs per ring slot (one bulk copy
 constexpr int kThreads = 32 * (kGroup + 1);  // warp 0: copy producer; warps 1..16: one row pair each
 static_assert(Layout::kChunk % kGroup == 0, "a group of gate rows stays inside one interleave chunk");
 constexpr int kMaxSlots = 16;
-constexpr int kMaxRows2 = 64;          // output rows per CTA in phase 2
-constexpr int kWarps = kThreads / 32;
-constexpr uint32_t kBarrierLimit = 1u << 23;  // polls (~1 s) before the grid barrier gives up
-
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // 2^(e - 127) for an integer biased exponent e (any range), as fp32.
 __device__ __forceinline__ float pow2_biased(int e) {
@@ -91,24 +84,6 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t word, uint32_t (&h)[4]) {
 // Staged activation block b (32 f16 = 4 chunks of 16 bytes), chunk q;
 // XOR-swizzled so the 8 lanes of an LDS.128 phase hit distinct banks.
 __device__ __forceinline__ int hswz(int b, int q) { return b * 4 + (q ^ ((b >> 1) & 3)); }
-
-// Dot of one MX block (16 code bytes = 32 elements) with staged block b.
-// Eight independent accumulation chains keep the FMA latency hidden.
-__device__ __forceinline__ float block_dot_f16(const uint4 c, const uint4* __restrict__ xs, int b) {
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 xv = xs[hswz(b, q)];
-        uint32_t wv[4];
-        e2m1x8_f16(cw[q], wv);
-        fma2_f16_f32(a[0], a[1], wv[0], xv.x);
-        fma2_f16_f32(a[2], a[3], wv[1], xv.y);
-        fma2_f16_f32(a[4], a[5], wv[2], xv.z);
-        fma2_f16_f32(a[6], a[7], wv[3], xv.w);
-    }
-    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-}
 
 // Two rows (gate, up) against the same staged block b.
 __device__ __forceinline__ void block_dot2_f16(const uint4 cg, const uint4 cu, const uint4* __restrict__ xs,
@@ -184,14 +159,15 @@ struct FusedParams {
     const uint8_t* slots;
     size_t expert_bytes;
     int S, E, H, I, k, T;
-    size_t rs_gu, rs_d, d_off;
+    size_t rs_gu, dt_off, dt_stride;
     const uint16_t* x;
     const int32_t* ids;
     const float* w;
     const int32_t* slot_of;
-    uint16_t* h;       // bf16 [T*k][I]
+    uint16_t* h;       // bf16 [T*k][I]: the SwiGLU output, kept for inspection
+    float* acc;        // fp32 [T][H] accumulator, all zero between calls
     float* out;        // fp32 [T][H]
-    unsigned* bar;     // [0] arrivals (zero when idle), [1] generation, [2] error bits
+    unsigned* ctl;     // [0] CTAs finished (zero between calls), [2] error bits
     // fused routing (logits != nullptr): the kernel selects the experts itself
     // and CTA 0 writes the routing outputs below
     const float* logits;
@@ -204,6 +180,7 @@ struct FusedParams {
 };
 
 constexpr int kMaxAssign = MOE_DECODE_MAX_ASSIGN;
+constexpr int kConsumers = kThreads - 32;   // threads of warps 1..kGroup
 
 __device__ __forceinline__ const uint8_t* expert_of(const FusedParams& p, int a) {
     const int e = p.ids[a];
@@ -223,50 +200,6 @@ struct AssignTable {
     int id[kMaxAssign];
 };
 
-// Sense-reversing grid barrier in the workspace's first bytes: bar[0]
-// counts arrivals and is reset to zero by the last arriver, which then
-// advances the generation bar[1] that the others wait on; bar[2] collects
-// error bits.  bar[0] must be zero when the workspace is first used; the
-// kernel leaves it zero.  A wait that runs out (about one second) sets an
-// error bit instead of spinning on.
-__device__ bool grid_barrier(unsigned* bar, unsigned G, int* ok_smem) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        unsigned gen;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(bar + 1) : "memory");
-        const unsigned arrived = atomicAdd(bar, 1u);
-        int ok = 1;
-        if (arrived == G - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(bar + 1), "r"(gen + 1) : "memory");
-        } else {
-            for (uint32_t i = 0;; ++i) {
-                unsigned v;
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar + 1) : "memory");
-                if (v != gen) break;
-                if (i >= kBarrierLimit) {
-                    atomicOr(bar + 2, 1u);
-                    ok = 0;
-                    break;
-                }
-                if (i > 256) __nanosleep(32);
-            }
-        }
-        __threadfence();
-        *ok_smem = ok;
-    }
-    __syncthreads();
-    return *ok_smem != 0;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
-    if (bytes >= 16)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(uint32_t(bytes & ~size_t(15)))
-                     : "memory");
-}
-
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -275,19 +208,30 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
-template <int NG, int ND>
+__device__ __forceinline__ void named_bar_consumers() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+}
+
+// Work item (a, c): gate/up rows 16c..16c+15 of assignment a, and block c of
+// the column-blocked down copy.  Warp j (1..16) computes h[16c + j - 1]; then
+// the 512 consumer threads apply the 16 h values to the block: thread q owns
+// output rows n = q + 512 m and accumulates y[n] += sum_i W[n][16c+i] h[16c+i]
+// in registers while the items of one assignment follow each other.  When the
+// assignment changes (and at the end) the thread adds w_a * y[n] into the fp32
+// accumulator of its token; the last CTA to finish copies the accumulator to
+// `out` and clears it.  No CTA ever waits for another one.
+template <int NG, int NN>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p, int slots, int ring_off) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int ok_smem;
     __shared__ AssignTable tab;
     __shared__ __align__(8) uint64_t full[kMaxSlots];
     __shared__ __align__(8) uint64_t empty[kMaxSlots];
-    __shared__ __align__(8) uint64_t down_full;
-    __shared__ float ypart[kMaxRows2][kMaxAssign];
+    __shared__ float hval[2][kGroup];
+    __shared__ int last_cta;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x;
     const int A = p.T * p.k;
-    volatile uint32_t* err = p.bar + 2;
+    volatile uint32_t* err = p.ctl + 2;
     if (p.logits != nullptr) {
         // routing in every CTA: warp 0 ranks each token's logits while the
         // other warps fetch the slot map
@@ -325,34 +269,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
             tc::mbar_init(&full[i], 1);
             tc::mbar_init(&empty[i], kGroup);
         }
-        tc::mbar_init(&down_full, 1);
         tc::fence_barrier_init();
     }
     __syncthreads();
 
-    // This CTA's work: a contiguous range of groups of kGroup (assignment,
-    // row) gate/up items -- kGroup consecutive gate rows, and the matching up
-    // rows, are contiguous in the packed layout -- and a contiguous range of
-    // output rows for the down product.
-    const int groups = A * p.I / kGroup;
-    const int perg = (groups + G - 1) / G;
-    const int g0 = min(groups, (int)blockIdx.x * perg), g1 = min(groups, g0 + perg);
-    const int per2 = (p.H + G - 1) / G;
-    const int r0 = min(p.H, (int)blockIdx.x * per2), r1 = min(p.H, r0 + per2);
+    // This CTA's items: a contiguous range of the A * I / 16 items in
+    // (assignment, column block) order.
+    const int items = A * p.I / kGroup;
+    const int per = (items + G - 1) / G;
+    const int g0 = min(items, (int)blockIdx.x * per), g1 = min(items, g0 + per);
     const int nbx = p.H / 32;
     const size_t row_bytes = p.rs_gu;
-    const size_t slot_bytes = 2 * kGroup * row_bytes;
+    const uint32_t gu_bytes = uint32_t(2 * kGroup * row_bytes);       // gate rows, then up rows
+    const uint32_t dt_bytes = uint32_t(p.H) * (kGroup / 2 + 1);          // codes, then scales
+    const size_t slot_bytes = (size_t(gu_bytes) + dt_bytes + 127) / 128 * 128;
     uint8_t* ring = smem + ring_off;
 
     if (warp == 0) {
-        // ---- producer: the down rows this CTA needs go to L2 first; then
-        //      gate/up rows stream through the ring, kGroup pairs per slot ----
+        // ---- producer: the rows and the down block of each item, one ring slot per item ----
         if (lane == 0) {
-            if (r1 > r0)
-                for (int a = 0; a < A; ++a) {
-                    const uint8_t* eb = tab.base[a];
-                    if (eb != nullptr) prefetch_l2(eb + p.d_off + (size_t)r0 * p.rs_d, size_t(r1 - r0) * p.rs_d);
-                }
             for (int n = 0; g0 + n < g1; ++n) {
                 const int slot = n % slots;
                 const uint32_t phase = uint32_t(n / slots) & 1u;
@@ -361,48 +296,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 const int a = it / p.I, r = it - a * p.I;
                 const uint8_t* eb = tab.base[a];
                 if (eb != nullptr) {
+                    uint8_t* dst = ring + (size_t)slot * slot_bytes;
                     const uint8_t* g = eb + Layout::gate_row(r) * p.rs_gu;
-                    tc::mbar_arrive_expect_tx(&full[slot], uint32_t(slot_bytes));
-                    bulk_copy_g2s(ring + (size_t)slot * slot_bytes, g, uint32_t(kGroup * row_bytes), &full[slot]);
-                    bulk_copy_g2s(ring + (size_t)slot * slot_bytes + kGroup * row_bytes, g + Layout::kChunk * p.rs_gu,
-                                  uint32_t(kGroup * row_bytes), &full[slot]);
+                    tc::mbar_arrive_expect_tx(&full[slot], gu_bytes + dt_bytes);
+                    bulk_copy_g2s(dst, g, uint32_t(kGroup * row_bytes), &full[slot]);
+                    bulk_copy_g2s(dst + kGroup * row_bytes, g + Layout::kChunk * p.rs_gu, uint32_t(kGroup * row_bytes),
+                                  &full[slot]);
+                    bulk_copy_g2s(dst + gu_bytes, eb + p.dt_off + (size_t)(r / kGroup) * p.dt_stride, dt_bytes,
+                                  &full[slot]);
                 } else {
                     tc::mbar_arrive(&full[slot]);
                 }
             }
-            // once every slot is released, this CTA's down rows of all
-            // assignments are copied into the ring: they land while the grid
-            // barrier is in progress, and phase 2 reads shared memory only.
-            const int issued = g1 - g0;
-            bool free_all = true;
-            for (int n = issued; n < issued + slots && free_all; ++n)
-                free_all = tc::mbar_wait(&empty[n % slots], (uint32_t(n / slots) & 1u) ^ 1u, err, 4u);
-            const size_t dbytes = size_t(r1 - r0) * p.rs_d;
-            if (free_all && r1 > r0) {
-                tc::mbar_arrive_expect_tx(&down_full, uint32_t(dbytes * A));
-                for (int a = 0; a < A; ++a) {
-                    const uint8_t* eb = tab.base[a];
-                    const uint8_t* src = eb != nullptr ? eb + p.d_off + (size_t)r0 * p.rs_d : nullptr;
-                    if (src != nullptr) bulk_copy_g2s(ring + (size_t)a * dbytes, src, uint32_t(dbytes), &down_full);
-                    else asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(&down_full)),
-                                      "r"(uint32_t(dbytes)) : "memory");
-                }
-            } else {
-                tc::mbar_arrive(&down_full);
-            }
         }
     } else {
-        // ---- consumers: warp w computes row pair w - 1 of every slot ----
+        // ---- consumers (warps 1..16) ----
         uint4* xs = reinterpret_cast<uint4*>(smem);
         int* xe = reinterpret_cast<int*>(smem + (size_t)p.T * nbx * 64);
-        for (int c = threadIdx.x - 32; c < p.T * nbx; c += kThreads - 32) {
+        for (int c = threadIdx.x - 32; c < p.T * nbx; c += kConsumers) {
             const int t = c / nbx, b = c - t * nbx;
             stage_block_f16(p.x + (size_t)t * p.H, xs + (size_t)t * nbx * 4, b, xe + t * nbx);
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+        named_bar_consumers();
         if (p.logits != nullptr && warp == 1) {
-            // softmax weights (needed only by phase 2), computed while the first
-            // copies are in flight; CTA 0 also writes the routing outputs
+            // softmax weights, computed while the first copies are in flight;
+            // CTA 0 also writes the routing outputs
             int my_id = MOE_MAX_EXPERTS;
             for (int t = 0; t < p.T; ++t) {
                 const int a0 = t * p.k;
@@ -420,18 +338,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 plan_warp(my_id, A, p.E, p.r_counts, p.r_offsets, p.r_perm, p.r_inv);
             }
         }
+        named_bar_consumers();  // tab.w visible to every consumer
         const int j = warp - 1;
+        const int ct = threadIdx.x - 32;
+        float y[NN];
+#pragma unroll
+        for (int m = 0; m < NN; ++m) y[m] = 0.0f;
+        int cur_a = -1;
+        auto flush = [&](int a) {
+            if (a < 0) return;
+            const float wa = tab.w[a];
+            float* dst = p.acc + (size_t)(a / p.k) * p.H;
+#pragma unroll
+            for (int m = 0; m < NN; ++m) {
+                const int n = ct + kConsumers * m;
+                if (n < p.H) atomicAdd(dst + n, wa * y[m]);
+                y[m] = 0.0f;
+            }
+        };
         for (int n = 0; g0 + n < g1; ++n) {
             const int slot = n % slots;
             const uint32_t phase = uint32_t(n / slots) & 1u;
             const bool got = tc::mbar_wait(&full[slot], phase, err, 8u);
-            const int it = (g0 + n) * kGroup + j;
-            const int a = it / p.I, r = it - a * p.I;
+            const int a = (g0 + n) * kGroup / p.I;
+            if (a != cur_a) {
+                flush(cur_a);
+                cur_a = a;
+            }
             const uint8_t* eb = tab.base[a];
-            if (!got || eb == nullptr) {
-                if (lane == 0) p.h[(size_t)a * p.I + r] = 0x7fc0;
-            } else {
-                const uint8_t* g = ring + (size_t)slot * slot_bytes + (size_t)j * row_bytes;
+            const bool have = got && eb != nullptr;
+            const uint8_t* sl = ring + (size_t)slot * slot_bytes;
+            // (1) h for row r0 + j
+            float hj = __int_as_float(0x7fc00000);
+            if (have) {
+                const uint8_t* g = sl + (size_t)j * row_bytes;
                 const uint8_t* u = g + kGroup * row_bytes;
                 const int t = a / p.k;
                 const uint4* xt = xs + (size_t)t * nbx * 4;
@@ -452,102 +392,104 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 }
                 ag = warp_sum(ag);
                 au = warp_sum(au);
-                if (lane == 0) {
-                    const float silu = ag / (1.0f + expf(-ag));
-                    const __nv_bfloat16 hv = __float2bfloat16_rn(silu * au);
-                    p.h[(size_t)a * p.I + r] = *reinterpret_cast<const uint16_t*>(&hv);
+                const float silu = ag / (1.0f + expf(-ag));
+                hj = __bfloat162float(__float2bfloat16_rn(silu * au));
+            }
+            if (lane == 0) {
+                hval[n & 1][j] = hj;
+                const __nv_bfloat16 hb = __float2bfloat16_rn(hj);
+                p.h[(size_t)(g0 + n) * kGroup + j] = *reinterpret_cast<const uint16_t*>(&hb);
+            }
+            named_bar_consumers();
+            // (2) y[n] += W[n][r0..r0+15] . h[r0..r0+15]
+            if (have) {
+                // the 16 h values as f16 pairs under one power-of-2 scale (bf16 -> f16 is exact)
+                float hv[kGroup];
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kGroup; ++i) {
+                    hv[i] = hval[n & 1][i];
+                    amax = fmaxf(amax, fabsf(hv[i]));
                 }
+                const int ef = int((__float_as_uint(amax) >> 23) & 0xffu);
+                const int e = (amax == 0.f) ? 0 : (ef == 0 ? -126 - 14 : ef - 127 - 14);
+                const float mul = ldexpf(1.0f, -e);
+                uint32_t h2[kGroup / 2];
+#pragma unroll
+                for (int i = 0; i < kGroup / 2; ++i) {
+                    const __half2 hh = __floats2half2_rn(hv[2 * i] * mul, hv[2 * i + 1] * mul);
+                    h2[i] = *reinterpret_cast<const uint32_t*>(&hh);
+                }
+                const uint8_t* codes = sl + gu_bytes;
+                const uint8_t* scales = codes + (size_t)p.H * (kGroup / 2);
+#pragma unroll
+                for (int m = 0; m < NN; ++m) {
+                    const int nn = ct + kConsumers * m;
+                    if (nn < p.H) {
+                        const uint2 cw = *reinterpret_cast<const uint2*>(codes + (size_t)nn * (kGroup / 2));
+                        uint32_t w0[4], w1[4];
+                        e2m1x8_f16(cw.x, w0);
+                        e2m1x8_f16(cw.y, w1);
+                        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+                        fma2_f16_f32(s0, s1, w0[0], h2[0]);
+                        fma2_f16_f32(s2, s3, w0[1], h2[1]);
+                        fma2_f16_f32(s0, s1, w0[2], h2[2]);
+                        fma2_f16_f32(s2, s3, w0[3], h2[3]);
+                        fma2_f16_f32(s0, s1, w1[0], h2[4]);
+                        fma2_f16_f32(s2, s3, w1[1], h2[5]);
+                        fma2_f16_f32(s0, s1, w1[2], h2[6]);
+                        fma2_f16_f32(s2, s3, w1[3], h2[7]);
+                        y[m] = fmaf((s0 + s1) + (s2 + s3), pow2_biased(int(scales[nn]) + e), y[m]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < NN; ++m) y[m] = __int_as_float(0x7fc00000);
             }
             __syncwarp();
             if (lane == 0 && got) tc::mbar_arrive(&empty[slot]);
         }
+        flush(cur_a);
     }
 
-    const bool ok0 = grid_barrier(p.bar, (unsigned)G, &ok_smem);
-    const bool ok = ok0 && tc::mbar_wait(&down_full, 0, err, 16u);
-
-    // ---- phase 2: down + weighted combine (rows prefetched into L2) ----
-    // Items are (row, expert) pairs; y of each lands in shared memory and
-    // one pass per row folds w_j * y_j in rank order.
-    constexpr int kWarpsAll = kThreads / 32;
-    uint4* hs = reinterpret_cast<uint4*>(smem);
-    const int nbh = p.I / 32;
-    int* he = reinterpret_cast<int*>(smem + (size_t)p.k * nbh * 64);
-    const int nrows = r1 - r0;
-    for (int t = 0; t < p.T; ++t) {
-        __syncthreads();
-        for (int c = threadIdx.x; c < p.k * nbh; c += kThreads) {
-            const int jj = c / nbh, b = c - jj * nbh;
-            stage_block_f16(p.h + ((size_t)t * p.k + jj) * p.I, hs + (size_t)jj * nbh * 4, b, he + jj * nbh);
+    // ---- completion: the last CTA to finish moves the sums to `out` ----
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned done = atomicAdd(p.ctl, 1u);
+        last_cta = (done == unsigned(G) - 1u);
+    }
+    __syncthreads();
+    if (last_cta) {
+        __threadfence();
+        const int n_out = p.T * p.H;
+        for (int i = threadIdx.x; i < n_out; i += kThreads) {
+            p.out[i] = __ldcg(p.acc + i);
+            p.acc[i] = 0.0f;
         }
-        __syncthreads();
-        const int items2 = nrows * p.k;
-        for (int q0 = warp * 2; q0 < items2; q0 += kWarpsAll * 2) {
-            uint4 c[2][ND];
-            int sc[2][ND];
-#pragma unroll
-            for (int u2 = 0; u2 < 2; ++u2) {
-                const int q = q0 + u2;
-                if (q >= items2) break;
-                const int rr = q / p.k, jj = q % p.k;
-                if (tab.base[t * p.k + jj] == nullptr || !ok) continue;
-                const uint8_t* row = ring + (size_t)(t * p.k + jj) * nrows * p.rs_d + (size_t)rr * p.rs_d;
-#pragma unroll
-                for (int i = 0; i < ND; ++i) {
-                    const int b = lane + 32 * i;
-                    if (b < nbh) {
-                        c[u2][i] = *reinterpret_cast<const uint4*>(row + 16 * b);
-                        sc[u2][i] = row[p.I / 2 + b];
-                    }
-                }
-            }
-#pragma unroll
-            for (int u2 = 0; u2 < 2; ++u2) {
-                const int q = q0 + u2;
-                if (q >= items2) break;
-                const int jj = q % p.k;
-                float y = __int_as_float(0x7fc00000);
-                if (tab.base[t * p.k + jj] != nullptr && ok) {
-                    const uint4* hj = hs + (size_t)jj * nbh * 4;
-                    const int* ej = he + jj * nbh;
-                    float acc = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < ND; ++i) {
-                        const int b = lane + 32 * i;
-                        if (b < nbh)
-                            acc = fmaf(block_dot_f16(c[u2][i], hj, b), pow2_biased(sc[u2][i] + ej[b]), acc);
-                    }
-                    y = warp_sum(acc);
-                }
-                if (lane == 0) ypart[q / p.k][jj] = y;
-            }
-        }
-        __syncthreads();
-        for (int q = threadIdx.x; q < nrows; q += kThreads) {
-            float out = 0.0f;
-            for (int jj = 0; jj < p.k; ++jj) out = __fadd_rn(out, __fmul_rn(tab.w[t * p.k + jj], ypart[q][jj]));
-            p.out[(size_t)t * p.H + r0 + q] = out;
-        }
+        if (threadIdx.x == 0) p.ctl[0] = 0u;
     }
 }
 
 }  // namespace
 
-// Shared memory of the fused kernel: the activation staging (phase 1) or
-// the h staging (phase 2), then the copy ring of gate/up row pairs.
-static size_t staging_bytes(int T, int k, int H, int I) {
-    const size_t x = size_t(T) * H * 2 + size_t(T) * (H / 32) * 4;
-    const size_t h = size_t(k) * I * 2 + size_t(k) * (I / 32) * 4;
-    return round_up(x > h ? x : h, 128);
+// Shared memory of the fused kernel: the activation staging, then the ring
+// of work items (16 gate rows, 16 up rows, one column block of down).
+static size_t staging_bytes(int T, int H) {
+    return round_up(size_t(T) * H * 2 + size_t(T) * (H / 32) * 4, 128);
 }
+
+static size_t item_bytes(const Layout& L) {
+    return round_up(2 * size_t(kGroup) * L.rs_gu + size_t(L.H) * (kGroup / 2 + 1), 128);
+}
+
+constexpr size_t kFusedSmemBudget = 216 * 1024;
 
 size_t decode_fused_smem(int T, int k, int H, int I) {
     Layout L;
-    if (!Layout::make(H, I, &L) || T * k > kMaxAssign || I % kGroup) return 0;
-    if (k * ((H + 151) / 152) > kMaxRows2 * kMaxAssign) return 0;
-    const size_t st = staging_bytes(T, k, H, I);
-    const size_t ring_min = 2 * 2 * kGroup * L.rs_gu;
-    return st + ring_min <= 200 * 1024 ? st + ring_min : 0;
+    if (!Layout::make(H, I, &L) || T * k > kMaxAssign || I % kGroup || Layout::kDtCols != kGroup) return 0;
+    const size_t need = staging_bytes(T, H) + 2 * item_bytes(L);
+    return need <= kFusedSmemBudget ? need : 0;
 }
 
 int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const RouteOut* ro) {
@@ -556,14 +498,11 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     int rc = current_device_info(&di);
     if (rc != MOE_OK) return rc;
     if (decode_fused_smem(a.T, a.k, L.H, L.I) == 0) return MOE_ERR_UNSUPPORTED;
-    const size_t st = staging_bytes(a.T, a.k, L.H, L.I);
-    const size_t slot_bytes = 2 * kGroup * L.rs_gu;
-    const size_t budget = 200 * 1024;
-    if ((L.H + di.sms - 1) / di.sms > kMaxRows2) return MOE_ERR_UNSUPPORTED;
-    const int slots = int(std::min<size_t>(kMaxSlots, (budget - st) / slot_bytes));
-    const size_t down_bytes = size_t(a.T) * a.k * ((L.H + di.sms - 1) / di.sms) * L.rs_d;
-    if (slots < 2 || down_bytes > size_t(slots) * slot_bytes) return MOE_ERR_UNSUPPORTED;
-    const size_t smem = st + size_t(slots) * slot_bytes;
+    const size_t st = staging_bytes(a.T, L.H);
+    const size_t ib = item_bytes(L);
+    const int slots = int(std::min<size_t>(kMaxSlots, (kFusedSmemBudget - st) / ib));
+    if (slots < 2) return MOE_ERR_UNSUPPORTED;
+    const size_t smem = st + size_t(slots) * ib;
     FusedParams p;
     p.slots = a.slots;
     p.expert_bytes = a.expert_bytes;
@@ -574,14 +513,15 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     p.k = a.k;
     p.T = a.T;
     p.rs_gu = L.rs_gu;
-    p.rs_d = L.rs_d;
-    p.d_off = L.d_off;
+    p.dt_off = L.dt_off;
+    p.dt_stride = L.dt_stride;
     p.x = a.x;
     p.ids = a.ids;
     p.w = a.w;
     p.slot_of = a.slot_of;
-    p.bar = static_cast<unsigned*>(ws);
+    p.ctl = static_cast<unsigned*>(ws);
     p.h = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + 256);
+    p.acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_acc_offset(a.T, a.k, L.I));
     p.out = a.out;
     p.logits = ro ? ro->logits : nullptr;
     p.r_ids = ro ? ro->ids : nullptr;
@@ -591,32 +531,23 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     p.r_perm = ro ? ro->perm : nullptr;
     p.r_inv = ro ? ro->inv : nullptr;
     if (ro && (a.T * a.k > 32 || a.E > MOE_MAX_EXPERTS)) return MOE_ERR_UNSUPPORTED;
-    const int ng = (L.H / 32 + 31) / 32, nd = (L.I / 32 + 31) / 32;
+    const int ng = (L.H / 32 + 31) / 32, nn = (L.H + kConsumers - 1) / kConsumers;
     void (*kern)(FusedParams, int, int) = nullptr;
-#define MOE_PICK(G_, D_) \
-    if (ng == G_ && nd == D_) kern = decode_fused_kernel<G_, D_>;
-    MOE_PICK(1, 1) MOE_PICK(1, 2) MOE_PICK(2, 1) MOE_PICK(2, 2) MOE_PICK(3, 3) MOE_PICK(3, 1)
-    MOE_PICK(1, 3) MOE_PICK(4, 4) MOE_PICK(2, 4) MOE_PICK(4, 2) MOE_PICK(3, 2) MOE_PICK(2, 3)
+#define MOE_PICK(G_, N_) \
+    if (ng == G_ && nn == N_) kern = decode_fused_kernel<G_, N_>;
+    MOE_PICK(1, 1) MOE_PICK(1, 2) MOE_PICK(2, 4) MOE_PICK(2, 3) MOE_PICK(3, 6) MOE_PICK(3, 5)
+    MOE_PICK(4, 8) MOE_PICK(4, 7) MOE_PICK(2, 2) MOE_PICK(3, 4)
 #undef MOE_PICK
     if (kern == nullptr) return MOE_ERR_UNSUPPORTED;
     static bool attr_set[16][64] = {};  // per kernel variant and device
-    const int variant = (ng - 1) * 4 + (nd - 1);
+    const int variant = (ng - 1) * 4 + std::min(3, nn / 2);
     if (di.device >= 64) return MOE_ERR_UNSUPPORTED;
     if (!attr_set[variant][di.device]) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(budget)));
+        MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFusedSmemBudget)));
         attr_set[variant][di.device] = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(di.sms);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p, slots, int(st)));
+    kern<<<di.sms, kThreads, smem, s>>>(p, slots, int(st));
+    MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
 

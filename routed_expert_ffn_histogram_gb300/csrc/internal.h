@@ -26,12 +26,17 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // its K/32 E8M0 scale bytes, zero-padded to a multiple of 32 bytes.  The gate/up
 // matrix has 2I rows interleaved in chunks of 32: chunk c holds gate rows
 // 32c..32c+31 then up rows 32c..32c+31, so a 32-wide block of h = SwiGLU(g, u)
-// comes from one 64-row pair of chunks.  The down matrix (H rows) follows.
+// comes from one 64-row pair of chunks.  The down matrix (H rows) follows,
+// then a column-blocked copy of it for decode: for each block of 16 columns
+// (16 consecutive elements of h), the H rows' 8 code bytes of that block,
+// then the H rows' E8M0 scale bytes of the 32-block it lies in.
 struct Layout {
     int H = 0, I = 0;
     size_t rs_gu = 0;        // bytes per gate/up row (K = H)
     size_t rs_d = 0;         // bytes per down row (K = I)
     size_t d_off = 0;        // byte offset of the down matrix
+    size_t dt_off = 0;       // byte offset of the column-blocked down copy
+    size_t dt_stride = 0;    // bytes per 16-column block of it (H*8 codes + H scales, padded)
     size_t expert_bytes = 0; // whole expert, a multiple of 1024
 
     static bool make(int hidden, int inter, Layout* L) {
@@ -42,10 +47,13 @@ struct Layout {
         L->rs_gu = round_up(size_t(hidden) / 2 + pad16(size_t(hidden) / 32), 32);
         L->rs_d = round_up(size_t(inter) / 2 + pad16(size_t(inter) / 32), 32);
         L->d_off = 2 * size_t(inter) * L->rs_gu;
-        L->expert_bytes = round_up(L->d_off + size_t(hidden) * L->rs_d, 1024);
+        L->dt_off = round_up(L->d_off + size_t(hidden) * L->rs_d, 128);
+        L->dt_stride = round_up(size_t(hidden) * (kDtCols / 2 + 1), 128);
+        L->expert_bytes = round_up(L->dt_off + size_t(inter / kDtCols) * L->dt_stride, 1024);
         return true;
     }
     static constexpr int kChunk = 32;
+    static constexpr int kDtCols = 16;   // columns per block of the column-blocked down copy
     // Row of the gate/up matrix that holds gate row r (its up row: + kChunk).
     __host__ __device__ static inline size_t gate_row(int r) {
         return size_t(r / kChunk) * (2 * kChunk) + size_t(r % kChunk);
@@ -94,6 +102,7 @@ struct RouteOut {
 };
 
 size_t decode_workspace_bytes(int T, int k, int H, int I);
+size_t decode_acc_offset(int T, int k, int I);
 int launch_decode_layer(const FfnArgs& a, const RouteOut& ro, void* ws, cudaStream_t s);
 size_t decode_fused_smem(int T, int k, int H, int I);
 int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s);

@@ -41,7 +41,10 @@ def test_expert_bytes():
     for H, I in [(2880, 2880), (2048, 768), (256, 512)]:
         eb = M.moe_expert_bytes(H, I)
         canon = 3 * (H * I // 2 + H * I // 32)
-        assert eb % 1024 == 0 and canon <= eb <= canon * (1.01 if H >= 2048 else 1.15)
+        # row-major matrices (rows padded to 32 bytes) plus the column-blocked
+        # copy of down: 16 columns x H rows, 8 code bytes + 1 scale byte per row
+        dt = (I // 16) * (-(-(H * 9) // 128) * 128)
+        assert eb % 1024 == 0 and canon + dt <= eb <= (canon + dt) * (1.01 if H >= 2048 else 1.15)
     with pytest.raises(M.MoeError):
         M.moe_expert_bytes(100, 64)
 
@@ -70,6 +73,16 @@ def test_pack_native_layout():
         row = buf[d_off + r * rs_d:d_off + (r + 1) * rs_d]
         assert np.array_equal(row[:I // 2], w["down_codes"][r])
         assert np.array_equal(row[I // 2:I // 2 + I // 32], w["down_scales"][r])
+    # column-blocked copy of down: block c = elements 16c..16c+15 of every row
+    # (8 code bytes per row, rows in order), then every row's scale of block c//2
+    dt_off = -(-(d_off + H * rs_d) // 128) * 128
+    dt_stride = -(-(H * 9) // 128) * 128
+    for c in [0, 1, 2, I // 16 - 1]:
+        blk = buf[dt_off + c * dt_stride:dt_off + (c + 1) * dt_stride]
+        codes = blk[:H * 8].reshape(H, 8)
+        assert np.array_equal(codes, w["down_codes"][:, 8 * c:8 * c + 8])
+        assert np.array_equal(blk[H * 8:H * 9], w["down_scales"][:, c // 2])
+        assert not blk[H * 9:].any()
 
 
 def test_invalid_arguments_rejected_before_launch():

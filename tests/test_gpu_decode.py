@@ -126,9 +126,10 @@ def test_decode_not_resident_gives_nan_not_fault():
 @pytest.mark.parametrize("wid,T", [(0, 16), (1, 1), (4, 2)])
 def test_decode_layer_fused_equals_two_calls(wid, T):
     """moe_decode_layer (routing inside the decode kernel) writes the same
-    routing outputs as moe_route_plan and the same layer output as
-    moe_route_plan + moe_expert_ffn on the decode path; and matches the
-    oracle."""
+    routing outputs as moe_route_plan (bit-exact) and the layer output of
+    moe_route_plan + moe_expert_ffn on the decode path up to fp32 rounding
+    order (the down sums are folded across CTAs with atomics); and matches
+    the oracle."""
     import torch
 
     import routed_expert_ffn_histogram_gb300 as M
@@ -148,7 +149,7 @@ def test_decode_layer_fused_equals_two_calls(wid, T):
     out_b = torch.empty((T, H), dtype=torch.float32, device="cuda")
     ws_a = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
     ws_b = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
-    for _ in range(2):  # twice: the workspace barrier must stay consistent
+    for _ in range(2):  # twice: the workspace counter and accumulator must be left clean
         M.moe_decode_layer(pool, 0, lg, x, a, slot_of, out_a, ws_a)
         M.moe_route_plan(lg, k, b, with_counts_host=False)
         M.moe_expert_ffn(pool, 0, x, b, slot_of, out_b, ws_b, path=M.MOE_PATH_DECODE)
@@ -157,7 +158,7 @@ def test_decode_layer_fused_equals_two_calls(wid, T):
         for key in ("ids", "w", "counts", "offsets"):
             assert torch.equal(getattr(a, key), getattr(b, key)), key
         assert torch.equal(a.perm[:n], b.perm[:n]) and torch.equal(a.inv[:n], b.inv[:n])
-        assert torch.equal(out_a, out_b)
+        assert rel_l2(out_a.cpu().numpy(), out_b.cpu().numpy()) <= 1e-6
     ids, w = oracle.route(lg_np, k)
     uniq = sorted(set(ids.reshape(-1).tolist()))
     ws = S.stack_experts(S.layer_weights(wl, 0, uniq))
