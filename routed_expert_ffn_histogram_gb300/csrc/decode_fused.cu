@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 const int slot = n % slots;
                 const uint32_t phase = uint32_t(n / slots) & 1u;
                 if (!tc::mbar_wait(&empty[slot], phase ^ 1u, err, 4u)) break;
+                // the second item waits until the first has landed, so every
+                // CTA's first item is not queued behind the others' second
+                if (n == 1 && !tc::mbar_wait(&full[0], 0u, err, 4u)) break;
                 const int it = (g0 + n) * kGroup;
                 const int a = it / p.I, r = it - a * p.I;
                 const uint8_t* eb = tab.base[a];
