@@ -270,6 +270,110 @@ def gpu_leg(args, wl, rank, world):
     return res
 
 
+def offload_leg(args, wl):
+    """The GPT-OSS-shaped decode with a small GPU pool (8 of 32 slots per
+    layer, LRU, skewed routing) and every expert in pinned host memory: per
+    layer, routing on the GPU, the routed experts' counts to the host, the
+    slot lookup and the copies of missed experts from pinned host memory on
+    a copy stream, then the decode FFN.  Timed end to end: each step's
+    logits and activations come from pinned host memory and its outputs go
+    back there."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L = wl.layers if args.layers is None else min(args.layers, wl.layers)
+    E, k, H, I, Sl = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.slots
+    eb = M.moe_expert_bytes(H, I)
+    wsrc = S.WORKLOADS[wl.weight_wid]
+    host = torch.empty(L * E * eb, dtype=torch.uint8).pin_memory()
+    for l in range(L):
+        for e, w in enumerate(S.layer_weights(wsrc, l)):
+            M.moe_pack_expert(w, H, I, host.data_ptr() + (l * E + e) * eb)
+    slots = torch.empty(L * Sl * eb, dtype=torch.uint8, device=dev)
+    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False)
+
+    # pinned-host -> device copy rate on this box (the bound of this workload)
+    probe = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    probe_d.copy_(probe, non_blocking=True)
+    torch.cuda.synchronize()
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(3):
+        probe_d.copy_(probe, non_blocking=True)
+    b0.record()
+    torch.cuda.synchronize()
+    link_peak = 3 * (1 << 30) / (a0.elapsed_time(b0) / 1e3) / 1e9
+    del probe, probe_d
+
+    G = args.warmup + args.steps
+    lg_pin = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, g % wl.steps) for l in range(L)])
+                                        for g in range(G)])).pin_memory()
+    x_pin = torch.from_numpy(np.stack([np.stack([S.activations_bf16_bits(wl, l, g % wl.steps) for l in range(L)])
+                                       for g in range(G)]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_pin = torch.empty((G, L, 1, H), dtype=torch.float32).pin_memory()
+    lg_d = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
+    x_d = torch.empty((L, 1, H), dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty((L, 1, H), dtype=torch.float32, device=dev)
+    plan = M.RoutePlan.allocate(1, E, k, counts_host=True, device=dev)
+    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
+    ws = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
+    compute = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev)
+
+    def step(g):
+        lg_d.copy_(lg_pin[g], non_blocking=True)
+        x_d.copy_(x_pin[g], non_blocking=True)
+        for l in range(L):
+            M.moe_route_plan(lg_d[l], k, plan, stream=compute)
+            rc = pool.stage(l, plan.counts_host, slot_of, compute=compute, copy=copy)
+            if rc != M.MOE_OK:
+                raise RuntimeError(f"stage failed: {rc}")
+            M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE, stream=compute)
+        out_pin[g].copy_(out_d, non_blocking=True)
+
+    with torch.cuda.stream(compute):
+        for g in range(args.warmup):
+            step(g)
+        compute.synchronize()
+        c0 = pool.counters()
+        clk = Clocks(torch.cuda.current_device())
+        clk.start()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(compute)
+        for g in range(args.warmup, G):
+            step(g)
+        b.record(compute)
+        compute.synchronize()
+        clocks = clk.stop()
+    c1 = pool.counters()
+    ms = a.elapsed_time(b) / args.steps
+    h2d = c1["h2d_bytes"] - c0["h2d_bytes"]
+    link = h2d / (ms * args.steps / 1e3) / 1e9
+    line = {"metric": METRIC, "value": 1e3 / ms, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "layers": L, "hidden": H, "inter": I, "experts": E, "top_k": k,
+                       "slots_per_layer": Sl, "routing_bias": wl.bias_c, "tokens_per_step": 1,
+                       "timing": "end to end: inputs from and outputs to pinned host memory every step"},
+            "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host",
+                         "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
+                         "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
+                         "traffic": None, "bytes_per_miss": eb},
+            "offload": {"hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
+                        "evictions": c1["evictions"] - c0["evictions"], "h2d_bytes": h2d,
+                        "misses_per_step": (c1["misses"] - c0["misses"]) / args.steps},
+            "e2e": {"value": 1e3 / ms, "unit": "tokens/s",
+                    "h2d_bytes_per_step": (lg_pin[0].numel() * 4 + x_pin[0].numel() * 2) + h2d / args.steps,
+                    "d2h_bytes_per_step": out_pin[0].numel() * 4},
+            "gpu_launches": args.steps * L * 2,
+            "clocks": clocks}
+    print(json.dumps(line))
+
+
 def prefill_leg(args, wl):
     """One prefill layer call per step: routing + grouped tcgen05 expert FFN +
     combine, graph-captured, inputs resident in HBM."""
@@ -348,14 +452,24 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=4, help="layers per oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", type=int, default=1, choices=[1, 3, 4],
-                    help="1: GPT-OSS decode (default); 3, 4: prefill layers (extra measurement)")
+    ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3, 4],
+                    help="1: GPT-OSS decode (default); 2: the same with an 8-slot offload pool; "
+                         "3, 4: prefill layers (extra measurements)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (smaller case for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = _dist()
     wl = S.WORKLOADS[args.workload]
+    if args.workload == 2:
+        import torch
+
+        torch.cuda.set_device(0)
+        from routed_expert_ffn_histogram_gb300 import build as B
+
+        B.build()
+        offload_leg(args, wl)
+        return
     if args.workload in (3, 4):
         import torch
 

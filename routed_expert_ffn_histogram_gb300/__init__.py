@@ -112,8 +112,9 @@ def moe_ffn_workspace_bytes(T: int, k: int, hidden: int, inter: int, path: int =
 
 
 def alloc_ffn_workspace(T: int, k: int, hidden: int, inter: int, path: int = MOE_PATH_AUTO, device="cuda"):
-    """A zeroed device workspace for moe_expert_ffn (its first bytes hold a
-    grid-barrier word that must start at zero)."""
+    """A zeroed device workspace for moe_expert_ffn / moe_decode_layer (the
+    decode path keeps a completion counter and an fp32 accumulator in it
+    that must start at zero; the library leaves them zero)."""
     import torch
 
     n = max(moe_ffn_workspace_bytes(T, k, hidden, inter, path), 256)
