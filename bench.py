@@ -292,7 +292,7 @@ def offload_leg(args, wl):
         for e, w in enumerate(S.layer_weights(wsrc, l)):
             M.moe_pack_expert(w, H, I, host.data_ptr() + (l * E + e) * eb)
     slots = torch.empty(L * Sl * eb, dtype=torch.uint8, device=dev)
-    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False)
+    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy)
 
     # pinned-host -> device copy rate on this machine (the bound of this workload)
     probe = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
@@ -363,7 +363,7 @@ def offload_leg(args, wl):
                          "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
                          "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
                          "traffic": None, "bytes_per_miss": eb},
-            "offload": {"hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
+            "offload": {"policy": args.policy, "hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
                         "evictions": c1["evictions"] - c0["evictions"], "h2d_bytes": h2d,
                         "misses_per_step": (c1["misses"] - c0["misses"]) / args.steps},
             "e2e": {"value": 1e3 / ms, "unit": "tokens/s",
@@ -371,7 +371,39 @@ def offload_leg(args, wl):
                     "d2h_bytes_per_step": out_pin[0].numel() * 4},
             "gpu_launches": args.steps * L * 2,
             "clocks": clocks}
+    if args.policy_sweep:
+        line["policy_sweep"] = policy_sweep(wl, L, dev)
     print(json.dumps(line))
+
+
+def policy_sweep(wl, L, dev):
+    """Every (step, layer) routing event of the offload workload, routed on
+    the GPU once, replayed through a policy-only pool (no copies) for each
+    eviction policy: hits and misses over the whole stream, cold start."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    E, k = wl.experts, wl.top_k
+    plan = M.RoutePlan.allocate(1, E, k, counts_host=True, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    events = []
+    with torch.cuda.stream(stream):
+        for step in range(wl.steps):
+            lg = torch.from_numpy(np.stack([S.logits(wl, l, step) for l in range(L)])).to(dev)
+            for l in range(L):
+                M.moe_route_plan(lg[l], k, plan, stream=stream)
+                stream.synchronize()
+                events.append((l, plan.counts_host.numpy().copy()))
+    out = {}
+    for name in M.POLICIES:
+        pool = M.Pool(L, E, wl.slots, wl.hidden, wl.inter, dry_run=True, policy=name)
+        for l, c in events:
+            pool.stage(l, c)
+        c = pool.counters()
+        out[name] = {"hits": c["hits"], "misses": c["misses"], "hit_rate": c["hits"] / max(1, c["hits"] + c["misses"]),
+                     "misses_per_token": c["misses"] / wl.steps}
+    return {"events": len(events), "steps": wl.steps, "layers": L, "policies": out}
 
 
 def prefill_leg(args, wl):
@@ -455,6 +487,10 @@ def main():
     ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3, 4],
                     help="1: GPT-OSS decode (default); 2: the same with an 8-slot offload pool; "
                          "3, 4: prefill layers (extra measurements)")
+    ap.add_argument("--policy", default="lru", choices=["lru", "fifo", "lfu", "lfru", "slru"],
+                    help="eviction policy of the offload pool (--workload 2)")
+    ap.add_argument("--policy-sweep", action="store_true",
+                    help="with --workload 2: also replay the whole routing stream under every policy")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (smaller case for profiler captures)")
     args = ap.parse_args()

@@ -182,6 +182,25 @@ MOE_API int moe_route_plan_noalloc(const float* logits, int T, int E, int k,
 
 typedef struct moe_pool moe_pool_t;
 
+/* Eviction policies of the slot pool (tinyserve README, "Configuration":
+ * cache_policy lru, lfru, slru, lfu, fifo; "How it works" item 3:
+ * frequency-recency eviction).  The pages name them without defining them;
+ * the readings implemented (per fused event; a miss evicts a resident
+ * expert that is not routed in the same event):
+ *   LRU   victim: least recently routed.
+ *   FIFO  victim: loaded earliest (routing does not refresh).
+ *   LFU   victim: fewest events routed since loaded, ties by lower id.
+ *   LFRU  victim: fewest events routed since loaded, ties by least recent.
+ *   SLRU  segmented LRU: a routed probationary expert becomes protected
+ *         (at most S/2, at least 1; the least recent protected one drops back
+ *         to probation); victim: least recent probationary, else least
+ *         recent protected. */
+#define MOE_POLICY_LRU  0
+#define MOE_POLICY_FIFO 1
+#define MOE_POLICY_LFU  2
+#define MOE_POLICY_LFRU 3
+#define MOE_POLICY_SLRU 4
+
 typedef struct {
     int layers;            /* L >= 1                                         */
     int experts;           /* E, 1..MOE_MAX_EXPERTS                          */
@@ -196,6 +215,8 @@ typedef struct {
     int dry_run;           /* 1: policy only -- no CUDA call is ever made;
                               stage updates the map and counters and reports
                               the copies it would issue                      */
+    int policy;            /* MOE_POLICY_*: which resident expert a miss
+                              evicts (0 = LRU)                               */
 } moe_pool_desc;
 
 typedef struct {

@@ -15,6 +15,9 @@ Parity status per function (what pins it, see ``tests/test_oracle_*.py``):
   * route (top-k + softmax) ........... pinned (brute-force sort, closed forms)
   * hist_perm ......................... pinned (numpy stable argsort, invariants)
   * lru_step .......................... pinned (independent list simulator, hand cases)
+  * PolicyPool (lru/fifo/lfu/lfru/slru)  pinned (hand-worked event streams per policy,
+                                        LRU mode against lru_step, exhaustive
+                                        offline-optimal lower bound on tiny streams)
   * expert_gateup / expert_down ....... pinned (integer-exact case, float64 numpy bound)
   * layer (decode, prefill) ........... pinned piecewise; the end-to-end float
                                         value has no printed worked example
@@ -202,6 +205,127 @@ class LRUPool:
 
     def counters(self) -> dict:
         return dict(hits=self.hits.value, misses=self.misses.value, evictions=self.evictions.value)
+
+
+POLICIES = ("lru", "fifo", "lfu", "lfru", "slru")
+
+
+class PolicyPool:
+    """One layer's slot pool under any of the named cache policies, written
+    out plainly in Python (events are small: E <= 256 experts).
+
+    The policies are named in the tinyserve README ("Configuration":
+    cache_policy lru, lfru, slru, lfu, fifo; "How it works" item 3:
+    frequency-recency eviction); the pages do not define them, so the
+    plainest readings are taken.  One fused event per (layer, step), as the
+    replay-semantics study on the Expert Offloading topic page prescribes:
+    U = experts with a nonzero count.  First every resident member of U, in
+    ascending id, is "routed again"; then every absent member, in ascending
+    id, takes the lowest-numbered free slot, or else the slot of a resident
+    expert outside U chosen by the policy:
+      lru   the one routed longest ago (loading counts as routing)
+      fifo  the one loaded longest ago (being routed again does not count)
+      lfu   the one routed in the fewest events since it was loaded, then
+            the lowest expert id
+      lfru  the one routed in the fewest events since it was loaded, then
+            the one routed longest ago
+      slru  experts are probationary when loaded; routed again, a
+            probationary expert becomes protected; when more than
+            max(1, S // 2) are protected, the protected one routed longest
+            ago becomes probationary again (and counts as just routed);
+            the victim is the probationary one routed longest ago, else the
+            protected one routed longest ago
+    """
+
+    def __init__(self, slots: int, experts: int, policy: str = "lru", preload: bool = False):
+        assert policy in POLICIES
+        self.S, self.E, self.policy = slots, experts, policy
+        self.slot_of = {}          # expert -> slot
+        self.last_routed = {}      # expert -> time of last routing (or load)
+        self.loaded_at = {}        # expert -> time of load
+        self.uses = {}             # expert -> events routed since load (load = 1)
+        self.protected = set()     # slru
+        self.time = 0
+        self.hits = self.misses = self.evictions = 0
+        if preload:
+            for e in range(min(slots, experts)):
+                self._load(e, e)
+
+    def _tick(self):
+        self.time += 1
+        return self.time
+
+    def _load(self, e, slot):
+        self.slot_of[e] = slot
+        t = self._tick()
+        self.last_routed[e] = t
+        self.loaded_at[e] = t
+        self.uses[e] = 1
+        self.protected.discard(e)
+
+    def _route_again(self, e):
+        if self.policy == "fifo":
+            return
+        if self.policy == "lfu":
+            self.uses[e] += 1
+            return
+        if self.policy == "lfru":
+            self.uses[e] += 1
+        self.last_routed[e] = self._tick()
+        if self.policy == "slru" and e not in self.protected:
+            self.protected.add(e)
+            if len(self.protected) > max(1, self.S // 2):
+                oldest = min(self.protected, key=lambda x: self.last_routed[x])
+                self.protected.discard(oldest)
+                self.last_routed[oldest] = self._tick()
+
+    def _victim(self, routed):
+        cand = [e for e in self.slot_of if e not in routed]
+        if self.policy == "fifo":
+            return min(cand, key=lambda e: self.loaded_at[e])
+        if self.policy == "lfu":
+            return min(cand, key=lambda e: (self.uses[e], e))
+        if self.policy == "lfru":
+            return min(cand, key=lambda e: (self.uses[e], self.last_routed[e]))
+        if self.policy == "slru":
+            return min(cand, key=lambda e: (e in self.protected, self.last_routed[e]))
+        return min(cand, key=lambda e: self.last_routed[e])
+
+    def step(self, counts):
+        """Apply one event; returns the list of (expert, slot) loads."""
+        routed = [e for e in range(self.E) if counts[e] > 0]
+        if len(routed) > self.S:
+            raise OverflowError("unique routed experts exceed the slots")
+        for e in routed:
+            if e in self.slot_of:
+                self.hits += 1
+                self._route_again(e)
+        loads = []
+        for e in routed:
+            if e in self.slot_of:
+                continue
+            used = set(self.slot_of.values())
+            free = [s for s in range(self.S) if s not in used]
+            if free:
+                slot = free[0]
+            else:
+                v = self._victim(set(routed))
+                slot = self.slot_of.pop(v)
+                self.protected.discard(v)
+                self.evictions += 1
+            self._load(e, slot)
+            self.misses += 1
+            loads.append((e, slot))
+        return loads
+
+    def slot_map(self) -> np.ndarray:
+        m = np.full(self.E, -1, np.int32)
+        for e, s in self.slot_of.items():
+            m[e] = s
+        return m
+
+    def counters(self) -> dict:
+        return dict(hits=self.hits, misses=self.misses, evictions=self.evictions)
 
 
 # ---- expert FFN --------------------------------------------------------------

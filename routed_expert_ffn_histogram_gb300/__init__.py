@@ -21,7 +21,9 @@ from dataclasses import dataclass
 from . import _lib
 from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_INVALID, MOE_ERR_STATE,
                    MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_OK,
-                   MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MoeCounters, MoeError, MoePoolDesc, check,
+                   MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_POLICY_FIFO, MOE_POLICY_LFRU,
+                   MOE_POLICY_LFU, MOE_POLICY_LRU, MOE_POLICY_SLRU, POLICIES, MoeCounters, MoeError, MoePoolDesc,
+                   check,
                    lib, ptr, status_str, stream_handle)
 
 __all__ = [
@@ -161,11 +163,13 @@ class Pool:
     (kept referenced here so they outlive the pool)."""
 
     def __init__(self, layers, experts, slots, hidden, inter, host_experts=None, dev_slots=None,
-                 preload=False, dry_run=False):
+                 preload=False, dry_run=False, policy=0):
         self.layers, self.experts, self.slots, self.hidden, self.inter = layers, experts, slots, hidden, inter
         self._keep = (host_experts, dev_slots)
+        if isinstance(policy, str):
+            policy = POLICIES[policy]
         d = MoePoolDesc(layers, experts, slots, hidden, inter, ptr(host_experts), ptr(dev_slots),
-                        int(bool(preload)), int(bool(dry_run)))
+                        int(bool(preload)), int(bool(dry_run)), int(policy))
         h = C.c_void_p()
         check("moe_pool_create", lib().moe_pool_create(C.byref(d), C.byref(h)))
         self.handle = h.value

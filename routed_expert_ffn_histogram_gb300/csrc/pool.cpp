@@ -1,4 +1,4 @@
-// Expert-slot pool: per-layer (expert -> slot) map with LRU eviction and
+// Expert-slot pool: per-layer (expert -> slot) map with policy-driven eviction and
 // host-to-device staging of missed experts on a copy stream.
 //
 // Sources: tinyserve README, "How it works" item 1 (expert weights kept as
@@ -11,10 +11,20 @@
 // fused cache event per (layer, step) instead of per-access replay).
 //
 // Event of one (layer, step): U = routed experts with a nonzero count,
-// ascending.  Resident members of U are hits and are touched first (fresh
-// recency stamps in ascending id); then each absent member, ascending, takes
-// the lowest free slot or evicts the resident expert with the oldest stamp.
-// Members of U were all stamped during the event, so they are never evicted.
+// ascending.  Resident members of U are hits and are touched first, in
+// ascending id; then each absent member, ascending, takes the lowest free
+// slot or evicts a resident expert that is not in U, chosen by the pool's
+// policy (tinyserve README, "Configuration": cache_policy lru, lfru, slru,
+// lfu, fifo; "How it works" item 3: frequency-recency eviction):
+//   lru   touch: fresh stamp.             victim: oldest stamp.
+//   fifo  touch: nothing (stamp = load).  victim: oldest load.
+//   lfu   touch: count + 1.               victim: fewest uses, then lowest id.
+//   lfru  touch: count + 1, fresh stamp.  victim: fewest uses, then oldest stamp.
+//   slru  touch: fresh stamp; a probationary expert moves to the protected
+//         segment (capacity S / 2, at least 1), whose least recent member,
+//         if it overflows, goes back to probation with a fresh stamp.
+//         victim: oldest probationary, else oldest protected.
+// A loaded expert gets a fresh stamp, count 1, probation.
 #include <chrono>
 #include <cstring>
 #include <new>
@@ -29,7 +39,9 @@ struct moe_pool {
     size_t eb = 0;
     std::vector<int32_t> slot_expert;   // [L][S], -1 = free
     std::vector<int32_t> expert_slot;   // [L][E], -1 = absent
-    std::vector<int64_t> stamp;         // [L][S]
+    std::vector<int64_t> stamp;         // [L][S] last touch (fifo: load)
+    std::vector<int64_t> uses;          // [L][S] touches since load (lfu, lfru)
+    std::vector<int8_t> seg;            // [L][S] slru: 0 probation, 1 protected
     std::vector<int64_t> clock;         // [L]
     std::vector<moe_counters> ctr;      // [L]
     std::vector<int32_t> last_e, last_s;  // [L][S]
@@ -46,6 +58,65 @@ constexpr uint32_t kStateMagic = 0x4d4f4550u;  // "MOEP"
 struct Planned {
     int32_t e, slot, victim;
 };
+
+// Per-layer policy state, planned on copies and committed on success.
+struct LayerState {
+    std::vector<int32_t> se, es;  // slot -> expert, expert -> slot
+    std::vector<int64_t> st, uses;
+    std::vector<int8_t> seg;
+    int64_t clk = 0;
+};
+
+void touch(LayerState& ls, int s, int policy, int S) {
+    switch (policy) {
+        case MOE_POLICY_FIFO: break;
+        case MOE_POLICY_LFU: ++ls.uses[s]; break;
+        case MOE_POLICY_LFRU: ++ls.uses[s]; ls.st[s] = ++ls.clk; break;
+        case MOE_POLICY_SLRU: {
+            ls.st[s] = ++ls.clk;
+            if (ls.seg[s] == 0) {
+                ls.seg[s] = 1;
+                const int cap = S / 2 > 0 ? S / 2 : 1;
+                int n = 0, oldest = -1;
+                for (int i = 0; i < S; ++i)
+                    if (ls.se[i] >= 0 && ls.seg[i] == 1) {
+                        ++n;
+                        if (oldest < 0 || ls.st[i] < ls.st[oldest]) oldest = i;
+                    }
+                if (n > cap) {
+                    ls.seg[oldest] = 0;
+                    ls.st[oldest] = ++ls.clk;
+                }
+            }
+            break;
+        }
+        default: ls.st[s] = ++ls.clk; break;  // lru
+    }
+}
+
+// Slot to evict for a miss: a resident expert with counts[e] == 0 (not
+// routed in this event).
+int victim_slot(const LayerState& ls, int policy, int S, const int32_t* counts) {
+    int best = -1;
+    auto better = [&](int i, int b) -> bool {
+        switch (policy) {
+            case MOE_POLICY_LFU:
+                return ls.uses[i] != ls.uses[b] ? ls.uses[i] < ls.uses[b] : ls.se[i] < ls.se[b];
+            case MOE_POLICY_LFRU:
+                return ls.uses[i] != ls.uses[b] ? ls.uses[i] < ls.uses[b] : ls.st[i] < ls.st[b];
+            case MOE_POLICY_SLRU:
+                return ls.seg[i] != ls.seg[b] ? ls.seg[i] < ls.seg[b] : ls.st[i] < ls.st[b];
+            default:
+                return ls.st[i] < ls.st[b];  // lru, fifo
+        }
+    };
+    for (int i = 0; i < S; ++i) {
+        const int e = ls.se[i];
+        if (e < 0 || counts[e] > 0) continue;
+        if (best < 0 || better(i, best)) best = i;
+    }
+    return best;
+}
 
 int wait_stream(moe_pool_t* p, cudaStream_t s, int timeout_ms) {
     MOE_CUDA_TRY(cudaEventRecord(p->ev_compute, s));
@@ -71,6 +142,7 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
         d.slots_per_layer > d.experts || !moe::Layout::make(d.hidden, d.inter, &L))
         return MOE_ERR_INVALID;
     if (!d.dry_run && (!d.host_experts || !d.dev_slots)) return MOE_ERR_INVALID;
+    if (d.policy < MOE_POLICY_LRU || d.policy > MOE_POLICY_SLRU) return MOE_ERR_INVALID;
     moe_pool_t* p = new (std::nothrow) moe_pool;
     if (!p) return MOE_ERR_INVALID;
     p->d = d;
@@ -80,6 +152,8 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
     p->slot_expert.assign(nl * S, -1);
     p->expert_slot.assign(nl * E, -1);
     p->stamp.assign(nl * S, 0);
+    p->uses.assign(nl * S, 0);
+    p->seg.assign(nl * S, 0);
     p->clock.assign(nl, 0);
     p->ctr.assign(nl, moe_counters{});
     p->last_e.assign(nl * S, -1);
@@ -100,6 +174,7 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
             for (size_t s = 0; s < S; ++s) {
                 p->slot_expert[l * S + s] = int32_t(s);
                 p->expert_slot[l * E + s] = int32_t(s);
+                p->uses[l * S + s] = 1;
                 if (!d.dry_run) {
                     const uint8_t* src = static_cast<const uint8_t*>(d.host_experts) + (l * E + s) * p->eb;
                     uint8_t* dst = static_cast<uint8_t*>(d.dev_slots) + (l * S + s) * p->eb;
@@ -127,8 +202,11 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
     int32_t* se = &p->slot_expert[size_t(layer) * S];
     int32_t* es = &p->expert_slot[size_t(layer) * E];
     int64_t* st = &p->stamp[size_t(layer) * S];
+    int64_t* us = &p->uses[size_t(layer) * S];
+    int8_t* sg = &p->seg[size_t(layer) * S];
     int64_t& clk = p->clock[layer];
     moe_counters& c = p->ctr[layer];
+    const int policy = p->d.policy;
 
     int uniq = 0;
     for (int e = 0; e < E; ++e) {
@@ -137,32 +215,38 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
     }
     if (uniq > S) return MOE_ERR_CAPACITY;
 
-    // Plan the event on scratch copies; commit load by load as copies enqueue.
-    std::vector<int32_t> se2(se, se + S), es2(es, es + E);
-    std::vector<int64_t> st2(st, st + S);
-    int64_t clk2 = clk;
+    // Plan the event on copies of the layer's state; commit on success.
+    LayerState ls;
+    ls.se.assign(se, se + S);
+    ls.es.assign(es, es + E);
+    ls.st.assign(st, st + S);
+    ls.uses.assign(us, us + S);
+    ls.seg.assign(sg, sg + S);
+    ls.clk = clk;
     uint64_t hits = 0;
     for (int e = 0; e < E; ++e)
-        if (counts_host[e] > 0 && es2[e] >= 0) {
-            st2[es2[e]] = ++clk2;
+        if (counts_host[e] > 0 && ls.es[e] >= 0) {
+            touch(ls, ls.es[e], policy, S);
             ++hits;
         }
     std::vector<Planned> plan;
     for (int e = 0; e < E; ++e) {
-        if (counts_host[e] <= 0 || es2[e] >= 0) continue;
+        if (counts_host[e] <= 0 || ls.es[e] >= 0) continue;
         int s = -1;
         for (int i = 0; i < S; ++i)
-            if (se2[i] < 0) { s = i; break; }
+            if (ls.se[i] < 0) { s = i; break; }
         int victim = -1;
         if (s < 0) {
-            for (int i = 0; i < S; ++i)
-                if (s < 0 || st2[i] < st2[s]) s = i;
-            victim = se2[s];
-            es2[victim] = -1;
+            s = victim_slot(ls, policy, S, counts_host);
+            if (s < 0) return MOE_ERR_CAPACITY;  // cannot happen when uniq <= S
+            victim = ls.se[s];
+            ls.es[victim] = -1;
         }
-        se2[s] = e;
-        es2[e] = s;
-        st2[s] = ++clk2;
+        ls.se[s] = e;
+        ls.es[e] = s;
+        ls.st[s] = ++ls.clk;
+        ls.uses[s] = 1;
+        ls.seg[s] = 0;
         plan.push_back({e, s, victim});
     }
 
@@ -199,16 +283,20 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
             se[q.slot] = q.e;
             es[q.e] = q.slot;
             st[q.slot] = ++clk;
+            us[q.slot] = 1;
+            sg[q.slot] = 0;
             ++c.misses;
             c.h2d_bytes += p->eb;
         }
         ++c.errors;
         p->last_n[layer] = 0;
     } else {
-        std::memcpy(se, se2.data(), sizeof(int32_t) * S);
-        std::memcpy(es, es2.data(), sizeof(int32_t) * E);
-        std::memcpy(st, st2.data(), sizeof(int64_t) * S);
-        clk = clk2;
+        std::memcpy(se, ls.se.data(), sizeof(int32_t) * S);
+        std::memcpy(es, ls.es.data(), sizeof(int32_t) * E);
+        std::memcpy(st, ls.st.data(), sizeof(int64_t) * S);
+        std::memcpy(us, ls.uses.data(), sizeof(int64_t) * S);
+        std::memcpy(sg, ls.seg.data(), sizeof(int8_t) * S);
+        clk = ls.clk;
         c.hits += hits;
         c.misses += plan.size();
         for (const Planned& q : plan) c.evictions += q.victim >= 0;
@@ -274,11 +362,12 @@ extern "C" int moe_pool_last_loads(const moe_pool_t* p, int layer, int32_t* le, 
 namespace {
 struct StateHeader {
     uint32_t magic;
-    int32_t layers, experts, slots, hidden, inter;
+    int32_t layers, experts, slots, hidden, inter, policy;
 };
 size_t state_bytes(const moe_pool_t* p) {
     return sizeof(StateHeader) + p->slot_expert.size() * 4 + p->expert_slot.size() * 4 +
-           p->stamp.size() * 8 + p->clock.size() * 8 + p->ctr.size() * sizeof(moe_counters);
+           p->stamp.size() * 8 + p->uses.size() * 8 + p->seg.size() + p->clock.size() * 8 +
+           p->ctr.size() * sizeof(moe_counters);
 }
 }  // namespace
 
@@ -291,13 +380,16 @@ extern "C" int moe_pool_state_bytes(const moe_pool_t* p, size_t* out) {
 extern "C" int moe_pool_save(const moe_pool_t* p, void* buf, size_t bytes) {
     if (!p || !buf || bytes < state_bytes(p)) return MOE_ERR_INVALID;
     uint8_t* o = static_cast<uint8_t*>(buf);
-    StateHeader h{kStateMagic, p->d.layers, p->d.experts, p->d.slots_per_layer, p->d.hidden, p->d.inter};
+    StateHeader h{kStateMagic, p->d.layers, p->d.experts, p->d.slots_per_layer, p->d.hidden, p->d.inter,
+                  p->d.policy};
     std::memcpy(o, &h, sizeof h);
     o += sizeof h;
     auto put = [&o](const void* src, size_t n) { std::memcpy(o, src, n); o += n; };
     put(p->slot_expert.data(), p->slot_expert.size() * 4);
     put(p->expert_slot.data(), p->expert_slot.size() * 4);
     put(p->stamp.data(), p->stamp.size() * 8);
+    put(p->uses.data(), p->uses.size() * 8);
+    put(p->seg.data(), p->seg.size());
     put(p->clock.data(), p->clock.size() * 8);
     put(p->ctr.data(), p->ctr.size() * sizeof(moe_counters));
     return MOE_OK;
@@ -309,7 +401,8 @@ extern "C" int moe_pool_load(moe_pool_t* p, const void* buf, size_t bytes) {
     StateHeader h;
     std::memcpy(&h, i, sizeof h);
     if (h.magic != kStateMagic || h.layers != p->d.layers || h.experts != p->d.experts ||
-        h.slots != p->d.slots_per_layer || h.hidden != p->d.hidden || h.inter != p->d.inter)
+        h.slots != p->d.slots_per_layer || h.hidden != p->d.hidden || h.inter != p->d.inter ||
+        h.policy != p->d.policy)
         return MOE_ERR_STATE;
     i += sizeof h;
     // validate before committing: every map entry in range and consistent
@@ -331,6 +424,8 @@ extern "C" int moe_pool_load(moe_pool_t* p, const void* buf, size_t bytes) {
     get(p->slot_expert.data(), p->slot_expert.size() * 4);
     get(p->expert_slot.data(), p->expert_slot.size() * 4);
     get(p->stamp.data(), p->stamp.size() * 8);
+    get(p->uses.data(), p->uses.size() * 8);
+    get(p->seg.data(), p->seg.size());
     get(p->clock.data(), p->clock.size() * 8);
     get(p->ctr.data(), p->ctr.size() * sizeof(moe_counters));
     return MOE_OK;

@@ -1,0 +1,129 @@
+"""Pins of the oracle's cache-policy simulator (oracle.PolicyPool) against
+things other than itself: hand-worked event streams whose victim each
+policy's reading fixes, chosen so that the policies disagree; the LRU mode
+against the separately pinned C LRU step; and, on tiny streams, the fewest
+misses any eviction choices could give (exhaustive search), which no policy
+can beat.  Policies: tinyserve README, "Configuration" (cache_policy lru,
+lfru, slru, lfu, fifo) and "How it works" item 3; events: Expert Offloading
+topic page, replay-semantics study (one fused event per (layer, step))."""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _ev(E, *experts):
+    c = np.zeros(E, np.int32)
+    for e in experts:
+        c[e] += 1
+    return c
+
+
+def _run(policy, S, E, events):
+    p = oracle.PolicyPool(S, E, policy)
+    return p, [p.step(_ev(E, *ev)) for ev in events]
+
+
+def test_fifo_ignores_rerouting_lru_does_not():
+    # 0 loaded first, 1 second, 0 routed again, then 2 needs a slot
+    events = [(0,), (1,), (0,), (2,)]
+    _, fifo = _run("fifo", 2, 4, events)
+    _, lru = _run("lru", 2, 4, events)
+    assert fifo[-1] == [(2, 0)]      # evicts 0, the earliest load
+    assert lru[-1] == [(2, 1)]       # evicts 1, routed longest ago
+
+
+def test_lfu_and_lfru_prefer_frequency():
+    # 0 routed twice, 1 once: both evict 1 even though 0 is older
+    for pol in ("lfu", "lfru"):
+        _, loads = _run(pol, 2, 4, [(0,), (0,), (1,), (2,)])
+        assert loads[-1] == [(2, 1)], pol
+
+
+def test_lfu_ties_by_id_lfru_ties_by_recency():
+    # all routed once; load order 1, 0, 2 -> slots 0, 1, 2
+    events = [(1,), (0,), (2,), (3,)]
+    _, lfu = _run("lfu", 3, 5, events)
+    _, lfru = _run("lfru", 3, 5, events)
+    assert lfu[-1] == [(3, 1)]       # lowest id (0) sits in slot 1
+    assert lfru[-1] == [(3, 0)]      # routed longest ago (1) sits in slot 0
+
+
+def test_slru_protects_rerouted_experts():
+    # S = 2: protected capacity 1.  0 is routed twice (protected), then the
+    # scan 1, 2: SLRU evicts the probationary 1, LRU the older 0
+    events = [(0,), (0,), (1,), (2,)]
+    _, slru = _run("slru", 2, 4, events)
+    _, lru = _run("lru", 2, 4, events)
+    assert slru[-1] == [(2, 1)]
+    assert lru[-1] == [(2, 0)]
+
+
+def test_slru_demotes_the_least_recent_protected():
+    # S = 4: capacity 2.  0, 1, 2, 3 loaded; 0, 1, 2 routed again in turn:
+    # protecting 2 demotes 0 (routed longest ago), which counts as just
+    # routed, so the next victim is 3
+    p, _ = _run("slru", 4, 6, [(0,), (1,), (2,), (3,), (0,), (1,), (2,)])
+    assert p.protected == {1, 2}
+    assert p.step(_ev(6, 4)) == [(4, 3)]
+
+
+def test_victims_are_never_routed_in_the_same_event():
+    for pol in oracle.POLICIES:
+        p, _ = _run(pol, 2, 4, [(0,), (1,)])
+        loads = p.step(_ev(4, 0, 2))      # 0 is a hit; 2 must evict 1
+        assert loads == [(2, 1)], pol
+        with pytest.raises(OverflowError):
+            p.step(_ev(4, 0, 1, 3))
+
+
+def test_lru_mode_matches_the_c_lru_step():
+    rng = np.random.default_rng(7)
+    for S, E in [(2, 6), (4, 8), (8, 32)]:
+        a, b = oracle.PolicyPool(S, E, "lru"), oracle.LRUPool(S, E)
+        for _ in range(300):
+            k = int(rng.integers(1, min(S, 4) + 1))
+            ev = _ev(E, *rng.choice(E, size=k, replace=False))
+            assert a.step(ev) == b.step(ev)
+            assert np.array_equal(a.slot_map(), b.slot_map())
+        assert a.counters() == b.counters()
+
+
+def _fewest_misses(S, events):
+    """Fewest misses over every choice of victims (exhaustive search)."""
+    best = [10 ** 9]
+
+    def go(i, resident, misses):
+        if misses >= best[0]:
+            return
+        if i == len(events):
+            best[0] = misses
+            return
+        U = set(events[i])
+        need = sorted(U - resident)
+        keep = resident & U
+        others = sorted(resident - U)
+        free = S - len(resident)
+        n_evict = max(0, len(need) - free)
+        for out in itertools.combinations(others, n_evict):
+            go(i + 1, (resident - set(out)) | U, misses + len(need))
+
+    go(0, frozenset(), 0)
+    return best[0]
+
+
+def test_no_policy_beats_the_offline_optimum_and_bookkeeping_holds():
+    rng = np.random.default_rng(11)
+    for _ in range(40):
+        S, E = 2, 5
+        events = [tuple(sorted(rng.choice(E, size=int(rng.integers(1, 3)), replace=False))) for _ in range(10)]
+        opt = _fewest_misses(S, events)
+        for pol in oracle.POLICIES:
+            p, loads = _run(pol, S, E, events)
+            c = p.counters()
+            assert c["misses"] >= opt, (pol, events)
+            assert c["hits"] + c["misses"] == sum(len(ev) for ev in events)
+            assert c["misses"] >= len(set().union(*map(set, events)))
+            assert sum(len(l) for l in loads) == c["misses"]

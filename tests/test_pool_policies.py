@@ -1,0 +1,56 @@
+"""The library's slot pool (moe_pool_stage, dry-run mode: policy only, no
+CUDA call) under each eviction policy, event by event against the oracle's
+policy simulator: load lists, slot maps and hit/miss/eviction counters
+bit-exact, on uniform and skewed routing streams, plus a checkpoint taken
+mid-stream and restored into a fresh pool."""
+import numpy as np
+import pytest
+
+import oracle
+import routed_expert_ffn_histogram_gb300 as M
+
+
+def _stream(rng, E, k, steps, bias):
+    rank = rng.permutation(E) + 1
+    for _ in range(steps):
+        lg = rng.standard_normal(E) - bias * np.log(rank)
+        top = np.argsort(-lg, kind="stable")[:k]
+        c = np.zeros(E, np.int32)
+        c[top] = 1
+        yield c
+
+
+@pytest.mark.parametrize("policy", oracle.POLICIES)
+@pytest.mark.parametrize("S,E,k,bias", [(8, 32, 4, 1.2), (4, 16, 2, 0.0), (6, 64, 4, 0.8)])
+def test_dry_run_pool_matches_oracle_policy(policy, S, E, k, bias):
+    rng = np.random.default_rng(S * 1000 + E)
+    layers = 2
+    pool = M.Pool(layers, E, S, 256, 512, dry_run=True, policy=policy)
+    ref = [oracle.PolicyPool(S, E, policy) for _ in range(layers)]
+    for step, c in enumerate(_stream(rng, E, k, 400, bias)):
+        layer = step % layers
+        assert pool.stage(layer, c) == M.MOE_OK
+        assert pool.last_loads(layer) == ref[layer].step(c)
+        assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
+    for layer in range(layers):
+        got, exp = pool.counters(layer), ref[layer].counters()
+        assert (got["hits"], got["misses"], got["evictions"]) == (exp["hits"], exp["misses"], exp["evictions"])
+
+
+@pytest.mark.parametrize("policy", oracle.POLICIES)
+def test_policy_state_survives_checkpoint(policy):
+    rng = np.random.default_rng(5)
+    S, E, k = 4, 16, 2
+    events = list(_stream(rng, E, k, 120, 0.5))
+    a = M.Pool(1, E, S, 256, 512, dry_run=True, policy=policy)
+    for c in events[:60]:
+        a.stage(0, c)
+    state = a.save()
+    b = M.Pool(1, E, S, 256, 512, dry_run=True, policy=policy)
+    assert b.load(state) == M.MOE_OK
+    for c in events[60:]:
+        a.stage(0, c)
+        b.stage(0, c)
+        assert a.last_loads(0) == b.last_loads(0)
+    other = M.Pool(1, E, S, 256, 512, dry_run=True, policy=(M.MOE_POLICY_LRU if policy != "lru" else "fifo"))
+    assert other.load(state) == M.MOE_ERR_STATE
