@@ -292,7 +292,8 @@ def offload_leg(args, wl):
         for e, w in enumerate(S.layer_weights(wsrc, l)):
             M.moe_pack_expert(w, H, I, host.data_ptr() + (l * E + e) * eb)
     slots = torch.empty(L * Sl * eb, dtype=torch.uint8, device=dev)
-    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy)
+    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy,
+                  stage_parts=args.stage_parts)
 
     # pinned-host -> device copy rate on this machine (the bound of this workload)
     probe = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
@@ -362,8 +363,9 @@ def offload_leg(args, wl):
             "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host",
                          "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
                          "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
-                         "traffic": None, "bytes_per_miss": eb},
-            "offload": {"policy": args.policy, "hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
+                         "traffic": None, "bytes_per_miss": (c1["h2d_bytes"] - c0["h2d_bytes"]) //
+                                                           max(1, c1["misses"] - c0["misses"])},
+            "offload": {"policy": args.policy, "stage_parts": args.stage_parts, "hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
                         "evictions": c1["evictions"] - c0["evictions"], "h2d_bytes": h2d,
                         "misses_per_step": (c1["misses"] - c0["misses"]) / args.steps},
             "e2e": {"value": 1e3 / ms, "unit": "tokens/s",
@@ -489,6 +491,8 @@ def main():
                          "3, 4: prefill layers (extra measurements)")
     ap.add_argument("--policy", default="lru", choices=["lru", "fifo", "lfu", "lfru", "slru"],
                     help="eviction policy of the offload pool (--workload 2)")
+    ap.add_argument("--stage-parts", default="whole", choices=["whole", "decode"],
+                    help="--workload 2: copy whole experts, or only what the decode kernel reads")
     ap.add_argument("--policy-sweep", action="store_true",
                     help="with --workload 2: also replay the whole routing stream under every policy")
     ap.add_argument("--layers", type=int, default=None,

@@ -201,6 +201,10 @@ typedef struct moe_pool moe_pool_t;
 #define MOE_POLICY_LFRU 3
 #define MOE_POLICY_SLRU 4
 
+/* Which parts of a packed expert the pool copies in (moe_pool_desc). */
+#define MOE_STAGE_WHOLE  0
+#define MOE_STAGE_DECODE 1
+
 typedef struct {
     int layers;            /* L >= 1                                         */
     int experts;           /* E, 1..MOE_MAX_EXPERTS                          */
@@ -217,6 +221,13 @@ typedef struct {
                               the copies it would issue                      */
     int policy;            /* MOE_POLICY_*: which resident expert a miss
                               evicts (0 = LRU)                               */
+    int stage_parts;       /* MOE_STAGE_WHOLE (0): a miss copies the whole
+                              packed expert.  MOE_STAGE_DECODE: only what
+                              the fused decode kernel reads (gate/up rows and
+                              the column-blocked down copy, about 3/4 of the
+                              bytes); moe_expert_ffn then refuses the prefill
+                              path and decode shapes the fused kernel cannot
+                              take (MOE_ERR_UNSUPPORTED)                     */
 } moe_pool_desc;
 
 typedef struct {

@@ -22,7 +22,8 @@ from . import _lib
 from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_INVALID, MOE_ERR_STATE,
                    MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_OK,
                    MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_POLICY_FIFO, MOE_POLICY_LFRU,
-                   MOE_POLICY_LFU, MOE_POLICY_LRU, MOE_POLICY_SLRU, POLICIES, MoeCounters, MoeError, MoePoolDesc,
+                   MOE_POLICY_LFU, MOE_POLICY_LRU, MOE_POLICY_SLRU, MOE_STAGE_DECODE,
+                   MOE_STAGE_WHOLE, POLICIES, MoeCounters, MoeError, MoePoolDesc,
                    check,
                    lib, ptr, status_str, stream_handle)
 
@@ -163,13 +164,14 @@ class Pool:
     (kept referenced here so they outlive the pool)."""
 
     def __init__(self, layers, experts, slots, hidden, inter, host_experts=None, dev_slots=None,
-                 preload=False, dry_run=False, policy=0):
+                 preload=False, dry_run=False, policy=0, stage_parts=0):
         self.layers, self.experts, self.slots, self.hidden, self.inter = layers, experts, slots, hidden, inter
         self._keep = (host_experts, dev_slots)
         if isinstance(policy, str):
             policy = POLICIES[policy]
         d = MoePoolDesc(layers, experts, slots, hidden, inter, ptr(host_experts), ptr(dev_slots),
-                        int(bool(preload)), int(bool(dry_run)), int(policy))
+                        int(bool(preload)), int(bool(dry_run)), int(policy),
+                        {"whole": 0, "decode": 1}.get(stage_parts, stage_parts))
         h = C.c_void_p()
         check("moe_pool_create", lib().moe_pool_create(C.byref(d), C.byref(h)))
         self.handle = h.value

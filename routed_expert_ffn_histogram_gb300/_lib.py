@@ -29,6 +29,7 @@ MOE_PATH_PREFILL = 2
 MOE_DECODE_MAX_ASSIGN = 64
 MOE_POLICY_LRU, MOE_POLICY_FIFO, MOE_POLICY_LFU, MOE_POLICY_LFRU, MOE_POLICY_SLRU = 0, 1, 2, 3, 4
 POLICIES = {"lru": 0, "fifo": 1, "lfu": 2, "lfru": 3, "slru": 4}
+MOE_STAGE_WHOLE, MOE_STAGE_DECODE = 0, 1
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _i32, _sz = C.c_void_p, C.c_int, C.c_size_t
@@ -38,7 +39,8 @@ _szp = C.POINTER(C.c_size_t)
 class MoePoolDesc(C.Structure):
     _fields_ = [("layers", C.c_int), ("experts", C.c_int), ("slots_per_layer", C.c_int),
                 ("hidden", C.c_int), ("inter", C.c_int), ("host_experts", C.c_void_p),
-                ("dev_slots", C.c_void_p), ("preload", C.c_int), ("dry_run", C.c_int), ("policy", C.c_int)]
+                ("dev_slots", C.c_void_p), ("preload", C.c_int), ("dry_run", C.c_int), ("policy", C.c_int),
+                ("stage_parts", C.c_int)]
 
 
 class MoeCounters(C.Structure):

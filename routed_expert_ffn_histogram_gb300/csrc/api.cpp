@@ -204,8 +204,10 @@ extern "C" int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_b
     a.inv = inv;
     a.slot_of = slot_of;
     a.out = out;
+    a.decode_parts_only = d.stage_parts == MOE_STAGE_DECODE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (path == MOE_PATH_DECODE) return moe::launch_decode_ffn(a, workspace, ws_bytes, s);
+    if (a.decode_parts_only) return MOE_ERR_UNSUPPORTED;
     return moe::launch_prefill_ffn(a, workspace, ws_bytes, s);
 }
 

@@ -328,12 +328,14 @@ int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t 
     if (ws_bytes < decode_workspace_bytes(a.T, a.k, L.H, L.I)) return MOE_ERR_INVALID;
     if (L.H > 4096 || L.I > 4096 * 4) return MOE_ERR_UNSUPPORTED;
     if (a.T == 0) return MOE_OK;
-    // one cooperative kernel per layer when the activations and h fit in
-    // shared memory; otherwise a gate/up launch and a down launch
+    // one kernel per layer when the activations and a work-item ring fit
+    // in shared memory; otherwise a gate/up launch and a down launch (which
+    // read the row-major down matrix, absent from decode-only staged pools)
     if (decode_fused_smem(a.T, a.k, L.H, L.I) != 0) {
         const int rc = launch_decode_fused(a, ws, s);
         if (rc != MOE_ERR_UNSUPPORTED) return rc;
     }
+    if (a.decode_parts_only) return MOE_ERR_UNSUPPORTED;
     DecodeParams p;
     p.slots = a.slots;
     p.expert_bytes = a.expert_bytes;

@@ -82,6 +82,7 @@ int route_noalloc_max_tokens();
 struct FfnArgs {
     const uint8_t* slots;      // base of this layer's slots
     size_t expert_bytes;
+    bool decode_parts_only = false;  // the pool staged only what the fused decode kernel reads
     int S, E;
     const Layout* L;
     const uint16_t* x;         // bf16 [T][H]

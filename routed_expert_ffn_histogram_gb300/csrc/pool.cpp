@@ -44,6 +44,7 @@ struct moe_pool {
     std::vector<int8_t> seg;            // [L][S] slru: 0 probation, 1 protected
     std::vector<int64_t> clock;         // [L]
     std::vector<moe_counters> ctr;      // [L]
+    size_t bytes_per_load = 0;          // bytes one miss copies
     std::vector<int32_t> last_e, last_s;  // [L][S]
     std::vector<int> last_n;            // [L]
     int32_t* map_pinned = nullptr;      // [L][E] staging for slot-map uploads
@@ -118,6 +119,23 @@ int victim_slot(const LayerState& ls, int policy, int S, const int32_t* counts) 
     return best;
 }
 
+// Copy expert e of `layer` from the host store into slot `slot`: the whole
+// packed expert, or (MOE_STAGE_DECODE) the gate/up rows and the
+// column-blocked down copy, skipping the row-major down matrix.
+cudaError_t copy_expert(const moe_pool_t* p, int layer, int e, int slot, cudaMemcpyKind kind, cudaStream_t s,
+                        bool sync) {
+    const size_t E = size_t(p->d.experts), S = size_t(p->d.slots_per_layer);
+    const uint8_t* src = static_cast<const uint8_t*>(p->d.host_experts) + (size_t(layer) * E + e) * p->eb;
+    uint8_t* dst = static_cast<uint8_t*>(p->d.dev_slots) + (size_t(layer) * S + slot) * p->eb;
+    auto cp = [&](size_t off, size_t n) {
+        return sync ? cudaMemcpy(dst + off, src + off, n, kind) : cudaMemcpyAsync(dst + off, src + off, n, kind, s);
+    };
+    if (p->d.stage_parts != MOE_STAGE_DECODE) return cp(0, p->eb);
+    cudaError_t r = cp(0, p->L.d_off);
+    if (r == cudaSuccess) r = cp(p->L.dt_off, p->eb - p->L.dt_off);
+    return r;
+}
+
 int wait_stream(moe_pool_t* p, cudaStream_t s, int timeout_ms) {
     MOE_CUDA_TRY(cudaEventRecord(p->ev_compute, s));
     const auto t0 = std::chrono::steady_clock::now();
@@ -143,11 +161,13 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
         return MOE_ERR_INVALID;
     if (!d.dry_run && (!d.host_experts || !d.dev_slots)) return MOE_ERR_INVALID;
     if (d.policy < MOE_POLICY_LRU || d.policy > MOE_POLICY_SLRU) return MOE_ERR_INVALID;
+    if (d.stage_parts != MOE_STAGE_WHOLE && d.stage_parts != MOE_STAGE_DECODE) return MOE_ERR_INVALID;
     moe_pool_t* p = new (std::nothrow) moe_pool;
     if (!p) return MOE_ERR_INVALID;
     p->d = d;
     p->L = L;
     p->eb = L.expert_bytes;
+    p->bytes_per_load = d.stage_parts == MOE_STAGE_DECODE ? L.d_off + (L.expert_bytes - L.dt_off) : L.expert_bytes;
     const size_t nl = size_t(d.layers), S = size_t(d.slots_per_layer), E = size_t(d.experts);
     p->slot_expert.assign(nl * S, -1);
     p->expert_slot.assign(nl * E, -1);
@@ -176,9 +196,7 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
                 p->expert_slot[l * E + s] = int32_t(s);
                 p->uses[l * S + s] = 1;
                 if (!d.dry_run) {
-                    const uint8_t* src = static_cast<const uint8_t*>(d.host_experts) + (l * E + s) * p->eb;
-                    uint8_t* dst = static_cast<uint8_t*>(d.dev_slots) + (l * S + s) * p->eb;
-                    cudaError_t e = cudaMemcpy(dst, src, p->eb, cudaMemcpyHostToDevice);
+                    cudaError_t e = copy_expert(p, int(l), int(s), int(s), cudaMemcpyHostToDevice, nullptr, true);
                     if (e != cudaSuccess) {
                         moe_pool_destroy(p);
                         return moe::cuda_fail(e);
@@ -259,10 +277,7 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
             break;
         }
         if (!p->d.dry_run) {
-            const uint8_t* src = static_cast<const uint8_t*>(p->d.host_experts) +
-                                 (size_t(layer) * E + q.e) * p->eb;
-            uint8_t* dst = static_cast<uint8_t*>(p->d.dev_slots) + (size_t(layer) * S + q.slot) * p->eb;
-            cudaError_t e = cudaMemcpyAsync(dst, src, p->eb, cudaMemcpyHostToDevice, ps);
+            cudaError_t e = copy_expert(p, layer, q.e, q.slot, cudaMemcpyHostToDevice, ps, false);
             if (e != cudaSuccess) {
                 fail = moe::cuda_fail(e);
                 break;
@@ -286,7 +301,7 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
             us[q.slot] = 1;
             sg[q.slot] = 0;
             ++c.misses;
-            c.h2d_bytes += p->eb;
+            c.h2d_bytes += p->bytes_per_load;
         }
         ++c.errors;
         p->last_n[layer] = 0;
@@ -300,7 +315,7 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
         c.hits += hits;
         c.misses += plan.size();
         for (const Planned& q : plan) c.evictions += q.victim >= 0;
-        c.h2d_bytes += plan.size() * p->eb;
+        c.h2d_bytes += plan.size() * p->bytes_per_load;
         ++c.events;
         p->last_n[layer] = int(plan.size());
         for (size_t i = 0; i < plan.size(); ++i) {

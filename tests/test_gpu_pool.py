@@ -77,3 +77,43 @@ def test_injected_copy_failure_on_device_pool():
     # slot 0 now holds expert 3's bytes
     eb = M.moe_expert_bytes(wl.hidden, wl.inter)
     assert torch.equal(dev[:eb].cpu(), host[3 * eb:4 * eb])
+
+
+def test_offload_decode_only_staging():
+    """A pool that stages only what the fused decode kernel reads gives the
+    same layer outputs as the oracle, copies fewer bytes than whole experts,
+    and refuses the prefill path (which needs the skipped matrix)."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    L = 3
+    pool, host, dev = make_pool(M, wl, layers=L, preload=False)
+    pool.close()
+    pool = M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev,
+                  policy="lfru", stage_parts="decode")
+    T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
+    plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(compute):
+        for step in range(4):
+            for layer in range(L):
+                lg = torch.from_numpy(S.logits(wl, layer, step)).cuda()
+                x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step).view(np.int16)).cuda().view(
+                    torch.bfloat16)
+                M.moe_route_plan(lg, k, plan, stream=compute)
+                assert pool.stage(layer, plan.counts_host, slot_of, compute=compute, copy=copy) == M.MOE_OK
+                M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE, stream=compute)
+                compute.synchronize()
+                r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                assert rel_l2(out.cpu().numpy(), r) <= DECODE_REL_L2
+        c = pool.counters()
+        assert 0 < c["h2d_bytes"] < c["misses"] * M.moe_expert_bytes(H, I)
+        pws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_PREFILL)
+        with pytest.raises(M.MoeError):
+            M.moe_expert_ffn(pool, 0, x, plan, slot_of, out, pws, path=M.MOE_PATH_PREFILL, stream=compute)
+    pool.close()

@@ -54,3 +54,26 @@ def test_policy_state_survives_checkpoint(policy):
         assert a.last_loads(0) == b.last_loads(0)
     other = M.Pool(1, E, S, 256, 512, dry_run=True, policy=(M.MOE_POLICY_LRU if policy != "lru" else "fifo"))
     assert other.load(state) == M.MOE_ERR_STATE
+
+
+def test_decode_only_staging_accounting():
+    """A pool staging only the decode path's parts copies gate/up rows and
+    the column-blocked down copy: fewer bytes per miss, same events."""
+    E, S, H, I = 8, 4, 256, 512
+    whole = M.Pool(1, E, S, H, I, dry_run=True)
+    part = M.Pool(1, E, S, H, I, dry_run=True, stage_parts="decode")
+    rng = np.random.default_rng(3)
+    for c in _stream(rng, E, 2, 50, 0.0):
+        whole.stage(0, c)
+        part.stage(0, c)
+        assert whole.last_loads(0) == part.last_loads(0)
+    cw, cp = whole.counters(0), part.counters(0)
+    eb = M.moe_expert_bytes(H, I)
+    rs_gu = -(-(H // 2 + ((H // 32 + 15) // 16) * 16) // 32) * 32
+    rs_d = -(-(I // 2 + ((I // 32 + 15) // 16) * 16) // 32) * 32
+    d_off = 2 * I * rs_gu
+    dt_off = -(-(d_off + H * rs_d) // 128) * 128
+    assert cw["h2d_bytes"] == cw["misses"] * eb
+    assert cp["h2d_bytes"] == cp["misses"] * (d_off + eb - dt_off)
+    with pytest.raises(M.MoeError):
+        M.Pool(1, E, S, H, I, dry_run=True, stage_parts=2)
