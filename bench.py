@@ -111,6 +111,26 @@ class Clocks:
                 "power_w_max": max(r["power"] for r in rows)}
 
 
+def replica_steps(rank: int, count: int, steps: int):
+    """Decode steps (inputs) run by one replica: replicas are independent
+    (the method is single-GPU; N GPUs run N decodes), so each rank takes
+    its own sequence of the workload's steps."""
+    return [(rank * 131 + g) % steps for g in range(count)]
+
+
+def reduce_max_over_ranks(values, world: int, device="cpu"):
+    """Largest of each value over all ranks (the job's time is the slowest
+    rank's); identity on one process."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -167,7 +187,7 @@ def gpu_leg(args, wl, rank, world):
     slot_of = torch.arange(E, dtype=torch.int32, device=dev)
 
     G = args.warmup + args.steps
-    step_ids = [(rank * 131 + g) % wl.steps for g in range(G)]
+    step_ids = replica_steps(rank, G, wl.steps)
     lg_h = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, s) for l in range(L)]) for s in step_ids]))
     x_h = torch.from_numpy(np.stack([np.stack([S.activations_bf16_bits(wl, l, s) for l in range(L)])
                                      for s in step_ids]).view(np.int16)).view(torch.bfloat16)
@@ -588,12 +608,7 @@ def main():
     res = gpu_leg(args, wl, rank, world)
     ms = res["elapsed_ms"] / args.steps
     e2e_ms = res["e2e_ms"] / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = reduce_max_over_ranks([ms, e2e_ms], world, device="cuda")
     if rank != 0:
         return
     value = world * 1e3 / ms
