@@ -136,8 +136,9 @@ MOE_API int moe_route_workspace_bytes(int T, int E, int k, size_t* out_bytes);
  *   logits      device fp32 [T][E]
  *   ids         device int32 [T][k]  out: selected experts, larger logit
  *               first, equal logits by lower id (NaN ranks last)
- *   w           device fp32 [T][k]   out: softmax over the k selected logits
- *               (evaluated in fp64, rounded to fp32)
+ *   w           device fp32 [T][k]   out: softmax over the k selected logits,
+ *               evaluated in float-float (about 48 bits) and rounded once
+ *               to fp32: within 2 ulp of the fp64 value
  *   counts      device int32 [E]     out: assignments per expert
  *   offsets     device int32 [E+1]   out: exclusive prefix sum of counts
  *   perm        device int32 [A]     out: assignment indices grouped by
