@@ -303,7 +303,10 @@ MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int pat
 
 /* The routed experts of one layer, combined:
  *   out[t] = sum_j w[t][j] * down_e(bf16(silu(gate_e x_t) * up_e x_t)),
- *   e = ids[t][j], j ascending, fp32.
+ *   e = ids[t][j], summed in fp32.  Both paths fold the k terms (and the
+ *   decode path also the partial down sums) into out with fp32 atomics, so
+ *   the order of those additions, and with it the last bits of out, varies
+ *   between runs.
  *   pool      the pool whose dev_slots hold the layer's experts
  *   x_bf16    device bf16 [T][H]
  *   ids, w    device, from moe_route_plan

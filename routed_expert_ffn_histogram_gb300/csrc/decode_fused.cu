@@ -490,7 +490,7 @@ constexpr size_t kFusedSmemBudget = 216 * 1024;
 
 size_t decode_fused_smem(int T, int k, int H, int I) {
     Layout L;
-    if (!Layout::make(H, I, &L) || T * k > kMaxAssign || I % kGroup || Layout::kDtCols != kGroup) return 0;
+    if (!Layout::make(H, I, &L) || T * k > kMaxAssign || I % kGroup || Layout::kDtCols != kGroup || H > 4096) return 0;
     const size_t need = staging_bytes(T, H) + 2 * item_bytes(L);
     return need <= kFusedSmemBudget ? need : 0;
 }
@@ -535,19 +535,29 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     p.r_inv = ro ? ro->inv : nullptr;
     if (ro && (a.T * a.k > 32 || a.E > MOE_MAX_EXPERTS)) return MOE_ERR_UNSUPPORTED;
     const int ng = (L.H / 32 + 31) / 32, nn = (L.H + kConsumers - 1) / kConsumers;
-    void (*kern)(FusedParams, int, int) = nullptr;
-#define MOE_PICK(G_, N_) \
-    if (ng == G_ && nn == N_) kern = decode_fused_kernel<G_, N_>;
-    MOE_PICK(1, 1) MOE_PICK(1, 2) MOE_PICK(2, 4) MOE_PICK(2, 3) MOE_PICK(3, 6) MOE_PICK(3, 5)
-    MOE_PICK(4, 8) MOE_PICK(4, 7) MOE_PICK(2, 2) MOE_PICK(3, 4)
-#undef MOE_PICK
-    if (kern == nullptr) return MOE_ERR_UNSUPPORTED;
-    static bool attr_set[16][64] = {};  // per kernel variant and device
-    const int variant = (ng - 1) * 4 + std::min(3, nn / 2);
-    if (di.device >= 64) return MOE_ERR_UNSUPPORTED;
-    if (!attr_set[variant][di.device]) {
+    using Kern = void (*)(FusedParams, int, int);
+    struct Variant {
+        int ng, nn;
+        Kern kern;
+    };
+    // ng = ceil(H / 1024) groups of 32 scale blocks per row, nn = ceil(H / 512)
+    // outputs per consumer thread; H <= 4096 gives exactly these pairs.
+    static const Variant variants[] = {
+        {1, 1, decode_fused_kernel<1, 1>}, {1, 2, decode_fused_kernel<1, 2>}, {2, 3, decode_fused_kernel<2, 3>},
+        {2, 4, decode_fused_kernel<2, 4>}, {3, 5, decode_fused_kernel<3, 5>}, {3, 6, decode_fused_kernel<3, 6>},
+        {4, 7, decode_fused_kernel<4, 7>}, {4, 8, decode_fused_kernel<4, 8>},
+    };
+    constexpr int kVariants = int(sizeof(variants) / sizeof(variants[0]));
+    static DeviceOnce attr_set[kVariants];
+    int vi = -1;
+    for (int i = 0; i < kVariants; ++i)
+        if (variants[i].ng == ng && variants[i].nn == nn) vi = i;
+    if (vi < 0) return MOE_ERR_UNSUPPORTED;
+    const Kern kern = variants[vi].kern;
+    if (di.device < 0 || di.device >= 64) return MOE_ERR_UNSUPPORTED;
+    if (!attr_set[vi].done(di.device)) {
         MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFusedSmemBudget)));
-        attr_set[variant][di.device] = true;
+        attr_set[vi].mark(di.device);
     }
     kern<<<di.sms, kThreads, smem, s>>>(p, slots, int(st));
     MOE_CUDA_TRY(cudaGetLastError());

@@ -1,6 +1,7 @@
 // Host-side definitions shared by the library's translation units.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -68,6 +69,16 @@ struct DeviceInfo {
 };
 // Properties of the current device (cached per device).
 int current_device_info(DeviceInfo* out);
+
+// One bit per device (ordinal < 64), set once a kernel's launch attributes
+// are in place on that device.  Atomic, so host threads may launch
+// concurrently; two threads that both find the bit clear both set the same
+// attribute, which is harmless.
+struct DeviceOnce {
+    std::atomic<uint64_t> bits{0};
+    bool done(int dev) const { return (bits.load(std::memory_order_acquire) >> dev) & 1u; }
+    void mark(int dev) { bits.fetch_or(uint64_t(1) << dev, std::memory_order_release); }
+};
 
 // ---- kernel launchers (route.cu, decode.cu, prefill.cu) -------------------
 

@@ -93,12 +93,15 @@ struct GemmParams {
     size_t b_rs;                // bytes per weight row
     int b_code_bytes;           // K/2: scales start here in each row
     int b_sf_bytes;             // pad16(K/32)
-    int mode;                   // 0: gate/up -> SwiGLU -> MXFP8 h; 1: down -> fp32 y
+    int mode;                   // 0: gate/up -> SwiGLU -> MXFP8 h; 1: down -> weighted combine into out
     int I;                      // mode 0: width of h
     uint8_t* hq;                // mode 0: [A][I]
     uint8_t* hs;                // mode 0: [A][hs_stride]
     int hs_stride;
-    float* y;                   // mode 1: [A][N]
+    const int32_t* perm;        // mode 1: [A] grouped row -> assignment t * k + j
+    const float* w;             // mode 1: [A] routing weight of each assignment
+    int k;                      // mode 1: assignments per token
+    float* out;                 // mode 1: [A / k][N], zero before the launch; w * y added atomically
     uint32_t* err;              // error bits (device word)
 };
 
@@ -412,6 +415,24 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
             if (*err) break;
             const Tile tl = decode_tile(sm, p, t, NT);
+            // mode 1: the token and routing weight of the four tile rows this
+            // thread stores, fetched before the accumulator is ready
+            int tok[4] = {-1, -1, -1, -1};
+            float wgt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (p.mode != 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int row = q * 32 + (lane >> 2) + 8 * j;
+                    const int mm = tl.m0 + row;
+                    if (row < tl.rows && mm < p.A) {
+                        const int a = __ldg(p.perm + mm);
+                        if (a >= 0 && a < p.A) {
+                            tok[j] = a / p.k;
+                            wgt[j] = __ldg(p.w + a);
+                        }
+                    }
+                }
+            }
             if (!tc::mbar_wait(&sm.acc_full, i & 1, err, 8u)) break;
             tc::tc_fence_after();
             uint32_t v[kHalf];
@@ -460,9 +481,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                     }
                 }
             } else {
-                // y rows leave through a per-warp shared tile so that a store
-                // instruction writes 64 contiguous bytes in each of 8 rows
-                // instead of 16 bytes in each of 32 rows.
+                // y rows leave through a per-warp shared tile so that one
+                // vector atomic instruction covers 64 contiguous bytes in each
+                // of 8 output rows instead of 16 bytes in each of 32 rows; the
+                // k assignments of a token land in out[token] in whatever
+                // order their tiles finish (fp32 atomics).
                 float* st = sm.ystage[warp - 8];
                 const int rr0 = lane >> 2, qq = lane & 3;
 #pragma unroll
@@ -478,15 +501,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int rr = rr0 + 8 * j;              // row within this warp's 32
-                        const int row = q * 32 + rr;             // row within the tile
                         const float4 val = *reinterpret_cast<const float4*>(st + rr * kYPad + 4 * qq);
-                        if (row < tl.rows && n < p.N) {
-                            const int mm = tl.m0 + row;
-                            float4* dst = reinterpret_cast<float4*>(p.y + (size_t)mm * p.N + n);
-                            if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0 || mm >= p.A)
+                        if (tok[j] >= 0 && n < p.N) {
+                            float4* dst = reinterpret_cast<float4*>(p.out + (size_t)tok[j] * p.N + n);
+                            if ((reinterpret_cast<uintptr_t>(dst) & 15) != 0)
                                 atomicOr(const_cast<uint32_t*>(err), 32u);
                             else
-                                *dst = val;
+                                atomicAdd(dst, make_float4(wgt[j] * val.x, wgt[j] * val.y, wgt[j] * val.z,
+                                                           wgt[j] * val.w));
                         }
                     }
                     __syncwarp();
@@ -570,14 +592,14 @@ int make_map_weights(CUtensorMap* m, const void* base, int K, int rows, int slot
 size_t smem_bytes() { return sizeof(Smem) + 1024; }
 
 int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int max_tiles, cudaStream_t s) {
-    static bool attr_set[64] = {};
+    static DeviceOnce attr_set;
     DeviceInfo di;
     int rc = current_device_info(&di);
     if (rc != MOE_OK) return rc;
     if (di.cc_major < 10) return MOE_ERR_UNSUPPORTED;
     if (smem_bytes() > di.smem_optin) return MOE_ERR_UNSUPPORTED;
-    if (di.device >= 64) return MOE_ERR_UNSUPPORTED;
-    if (!attr_set[di.device]) {
+    if (di.device < 0 || di.device >= 64) return MOE_ERR_UNSUPPORTED;
+    if (!attr_set.done(di.device)) {
         // The warpgroups' register split must add up to exactly what the
         // launch grants each thread, or a setmaxnreg.inc would wait forever.
         cudaFuncAttributes fa{};
@@ -585,7 +607,7 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& 
         if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return MOE_ERR_UNSUPPORTED;
         MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem_bytes()));
-        attr_set[di.device] = true;
+        attr_set.mark(di.device);
     }
     const int grid = max(1, min(di.sms, max_tiles));
     grouped_gemm_tc_kernel<<<grid, kThreads, smem_bytes(), s>>>(ma, mb, p);
@@ -594,7 +616,7 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& 
 }
 
 struct PrefillWs {
-    size_t xq, xs, hq, hs, y, err, total;
+    size_t xq, xs, hq, hs, err, total;
     int xs_stride, hs_stride;
 };
 
@@ -609,7 +631,6 @@ PrefillWs prefill_ws(int T, int k, int H, int I) {
     w.xs = o; o = round_up(o + A * w.xs_stride, 256);
     w.hq = o; o = round_up(o + A * I, 256);
     w.hs = o; o = round_up(o + A * w.hs_stride, 256);
-    w.y = o; o = round_up(o + A * H * 4, 256);
     w.total = o;
     return w;
 }
@@ -630,12 +651,12 @@ int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
     uint8_t* xs = base + w.xs;
     uint8_t* hq = base + w.hq;
     uint8_t* hs = base + w.hs;
-    float* y = reinterpret_cast<float*>(base + w.y);
     uint32_t* err = reinterpret_cast<uint32_t*>(base + w.err);
 
     MOE_CUDA_TRY(cudaMemsetAsync(err, 0, 4, s));
     MOE_CUDA_TRY(cudaMemsetAsync(xs, 0, size_t(A) * w.xs_stride, s));
     MOE_CUDA_TRY(cudaMemsetAsync(hs, 0, size_t(A) * w.hs_stride, s));
+    MOE_CUDA_TRY(cudaMemsetAsync(a.out, 0, size_t(a.T) * L.H * sizeof(float), s));
     int rc = launch_quant_mxfp8_scatter(a.x, L.H, a.inv, a.k, a.T, xq, xs, w.xs_stride, s);
     if (rc != MOE_OK) return rc;
 
@@ -672,7 +693,7 @@ int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
     g.hs_stride = w.hs_stride;
     rc = launch_gemm(map_x, map_gu, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
     if (rc != MOE_OK) return rc;
-    // down: K = I, N = H, epilogue fp32 y in grouped order
+    // down: K = I, N = H, epilogue w * y added into out[token]
     g.K = L.I;
     g.KB = L.I / 32;
     g.N = L.H;
@@ -683,10 +704,11 @@ int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
     g.b_code_bytes = L.I / 2;
     g.b_sf_bytes = int(pad16(size_t(L.I) / 32));
     g.mode = 1;
-    g.y = y;
-    rc = launch_gemm(map_h, map_d, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
-    if (rc != MOE_OK) return rc;
-    return launch_combine(y, a.w, a.inv, a.T, a.k, L.H, a.out, s);
+    g.perm = a.perm;
+    g.w = a.w;
+    g.k = a.k;
+    g.out = a.out;
+    return launch_gemm(map_h, map_d, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
 }
 
 }  // namespace moe
