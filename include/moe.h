@@ -327,7 +327,7 @@ MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int pat
  *             first used (allocate it zero-filled); the library leaves them
  *             zero after every call.  One workspace must not be used by two
  *             calls that can run at the same time.
- *   out       device fp32 [T][H], fully overwritten
+ *   out       device fp32 [T][H], 16-byte aligned, fully overwritten
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16, int T, int k,
                    const int32_t* ids, const float* w, const int32_t* offsets,
@@ -347,6 +347,7 @@ MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16
  *   slot_of  device int32 [E]: every routed expert must be resident
  *   workspace as moe_expert_ffn, MOE_PATH_DECODE (zero-filled before first
  *            use)
+ *   out      device fp32 [T][H], 16-byte aligned, fully overwritten
  * Limits: T*k <= 32.  Errors: MOE_ERR_INVALID, MOE_ERR_STATE,
  * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 MOE_API int moe_decode_layer(const moe_pool_t* pool, int layer, const float* logits,

@@ -225,7 +225,8 @@ extern "C" int moe_decode_layer(const moe_pool_t* pool, int layer, const float* 
         return MOE_ERR_INVALID;
     size_t need = 0;
     moe_ffn_workspace_bytes(T, k, d.hidden, d.inter, MOE_PATH_DECODE, &need);
-    if (!workspace || ws_bytes < need || !aligned(workspace, 256) || !aligned(x_bf16, 16)) return MOE_ERR_INVALID;
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256) || !aligned(x_bf16, 16) || !aligned(out, 16))
+        return MOE_ERR_INVALID;
     moe::FfnArgs a;
     a.slots = static_cast<const uint8_t*>(d.dev_slots) + size_t(layer) * d.slots_per_layer * L.expert_bytes;
     a.expert_bytes = L.expert_bytes;

@@ -348,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
 #pragma unroll
         for (int m = 0; m < NN; ++m) y[m] = 0.0f;
         int cur_a = -1;
+        // Lanes 4i..4i+3 of a warp own four consecutive rows (H is a
+        // multiple of 32, so a quad is all inside or all outside [0, H));
+        // lane 4i adds the quad with one float4 atomic.
         auto flush = [&](int a) {
             if (a < 0) return;
             const float wa = tab.w[a];
@@ -355,7 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
 #pragma unroll
             for (int m = 0; m < NN; ++m) {
                 const int n = ct + kConsumers * m;
-                if (n < p.H) atomicAdd(dst + n, wa * y[m]);
+                const float v = wa * y[m];
+                const float v1 = __shfl_down_sync(0xffffffffu, v, 1);
+                const float v2 = __shfl_down_sync(0xffffffffu, v, 2);
+                const float v3 = __shfl_down_sync(0xffffffffu, v, 3);
+                if ((lane & 3) == 0 && n < p.H) atomicAdd(reinterpret_cast<float4*>(dst + n), make_float4(v, v1, v2, v3));
                 y[m] = 0.0f;
             }
         };
@@ -465,10 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
     __syncthreads();
     if (last_cta) {
         __threadfence();
-        const int n_out = p.T * p.H;
-        for (int i = threadIdx.x; i < n_out; i += kThreads) {
-            p.out[i] = __ldcg(p.acc + i);
-            p.acc[i] = 0.0f;
+        const int n4 = p.T * p.H / 4;
+        float4* acc4 = reinterpret_cast<float4*>(p.acc);
+        float4* out4 = reinterpret_cast<float4*>(p.out);
+        for (int i = threadIdx.x; i < n4; i += kThreads) {
+            out4[i] = __ldcg(acc4 + i);
+            acc4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
         if (threadIdx.x == 0) p.ctl[0] = 0u;
     }
