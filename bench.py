@@ -290,6 +290,114 @@ def gpu_leg(args, wl, rank, world):
     return res
 
 
+def _pinned_link_peak(dev):
+    """Pinned-host -> device copy rate on this machine, GB/s (the bound of the
+    staging workloads): three 1 GiB cudaMemcpyAsync copies, CUDA events."""
+    import torch
+
+    probe = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    probe_d.copy_(probe, non_blocking=True)
+    torch.cuda.synchronize()
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(3):
+        probe_d.copy_(probe, non_blocking=True)
+    b0.record()
+    torch.cuda.synchronize()
+    return 3 * (1 << 30) / (a0.elapsed_time(b0) / 1e3) / 1e9
+
+
+def staged_prefill_leg(args, wl):
+    """Prefill of one layer through a pool of ``--prefill-slots`` slots (fewer
+    than the routed experts), every expert in pinned host memory: per step,
+    routing on the GPU, then moe_prefill_staged (windows of unique experts
+    staged on a copy stream while the previous window's grouped GEMMs run).
+    Timed end to end on the host clock and by CUDA events on the compute
+    stream: x and logits come from pinned host memory, out goes back there."""
+    import time
+
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    E, k, H, I, T, Sl = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.tokens, args.prefill_slots
+    window = args.window or Sl // 2
+    eb = M.moe_expert_bytes(H, I)
+    host = torch.empty(E * eb, dtype=torch.uint8).pin_memory()
+    for e, w in enumerate(S.layer_weights(wl, 0)):
+        M.moe_pack_expert(w, H, I, host.data_ptr() + e * eb)
+    slots = torch.empty(Sl * eb, dtype=torch.uint8, device=dev)
+    pool = M.Pool(1, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy)
+    link_peak = _pinned_link_peak(dev)
+    G = 2  # two distinct input batches, alternated
+    lg_pin = [torch.from_numpy(S.logits(wl, 0, g)).pin_memory() for g in range(G)]
+    x_pin = [torch.from_numpy(S.activations_bf16_bits(wl, 0, g).view(np.int16)).view(torch.bfloat16).pin_memory()
+             for g in range(G)]
+    out_pin = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    lg_d = torch.empty((T, E), dtype=torch.float32, device=dev)
+    x_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty((T, H), dtype=torch.float32, device=dev)
+    plan = M.RoutePlan.allocate(T, E, k, counts_host=True, device=dev)
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_PREFILL, device=dev)
+    compute = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev)
+
+    def step(g):
+        lg_d.copy_(lg_pin[g % G], non_blocking=True)
+        x_d.copy_(x_pin[g % G], non_blocking=True)
+        M.moe_route_plan(lg_d, k, plan, stream=compute)
+        pool.prefill_staged(0, plan.counts_host, window, k, x_bf16=x_d, plan=plan, out=out_d, workspace=ws,
+                            compute=compute, copy=copy)
+        out_pin.copy_(out_d, non_blocking=True)
+
+    with torch.cuda.stream(compute):
+        for g in range(args.warmup):
+            step(g)
+        compute.synchronize()
+        c0 = pool.counters()
+        clk = Clocks(torch.cuda.current_device())
+        clk.start()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record(compute)
+        for g in range(args.steps):
+            step(g)
+        b.record(compute)
+        compute.synchronize()
+        wall = (time.perf_counter() - t0) / args.steps * 1e3
+        clocks = clk.stop()
+    c1 = pool.counters()
+    ms = a.elapsed_time(b) / args.steps
+    h2d = c1["h2d_bytes"] - c0["h2d_bytes"]
+    link = h2d / (ms * args.steps / 1e3) / 1e9
+    misses = c1["misses"] - c0["misses"]
+    uniq = int((plan.counts_host.numpy() > 0).sum())
+    line = {"metric": METRIC, "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "mxf8f6f4->f32", "data": "synthetic",
+            "config": {"workload": wl.name + f"_staged_s{Sl}_w{window}", "hidden": H, "inter": I, "experts": E,
+                       "top_k": k, "tokens": T, "slots_per_layer": Sl, "window": window, "policy": args.policy,
+                       "timing": "end to end: x and logits from pinned host memory, out back to it, every step"},
+            "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host, "
+                                   "overlapping the previous window's grouped GEMMs",
+                         "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
+                         "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
+                         "traffic": None, "bytes_per_miss": h2d // max(1, misses)},
+            "staging": {"unique_experts_per_step": uniq, "misses_per_step": misses / args.steps,
+                        "hits": c1["hits"] - c0["hits"], "events_per_step": (c1["events"] - c0["events"]) / args.steps,
+                        "h2d_bytes_per_step": h2d / args.steps, "host_ms_per_step": wall},
+            # per step: routing (top-k and scatter passes), quantisation, two GEMMs per window
+            "gpu_launches": args.steps * (2 + 1 + 2 * ((uniq + window - 1) // window)),
+            "e2e": {"value": T / (ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": lg_pin[0].numel() * 4 + x_pin[0].numel() * 2 + h2d / args.steps,
+                    "d2h_bytes_per_step": out_pin.numel() * 4},
+            "clocks": clocks}
+    print(json.dumps(line))
+
+
 def offload_leg(args, wl):
     """The GPT-OSS-shaped decode with a small GPU pool (8 of 32 slots per
     layer, LRU, skewed routing) and every expert in pinned host memory: per
@@ -315,19 +423,7 @@ def offload_leg(args, wl):
     pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy,
                   stage_parts=args.stage_parts)
 
-    # pinned-host -> device copy rate on this machine (the bound of this workload)
-    probe = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
-    probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    probe_d.copy_(probe, non_blocking=True)
-    torch.cuda.synchronize()
-    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record()
-    for _ in range(3):
-        probe_d.copy_(probe, non_blocking=True)
-    b0.record()
-    torch.cuda.synchronize()
-    link_peak = 3 * (1 << 30) / (a0.elapsed_time(b0) / 1e3) / 1e9
-    del probe, probe_d
+    link_peak = _pinned_link_peak(dev)
 
     G = args.warmup + args.steps
     lg_pin = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, g % wl.steps) for l in range(L)])
@@ -514,6 +610,10 @@ def main():
                     help="eviction policy of the offload pool (--workload 2)")
     ap.add_argument("--stage-parts", default="whole", choices=["whole", "decode"],
                     help="--workload 2: copy whole experts, or only what the decode kernel reads")
+    ap.add_argument("--prefill-slots", type=int, default=None,
+                    help="workloads 3/4: run the layer through a pool of this many slots (moe_prefill_staged)")
+    ap.add_argument("--window", type=int, default=None,
+                    help="with --prefill-slots: unique experts per staging window (default slots // 2)")
     ap.add_argument("--policy-sweep", action="store_true",
                     help="with --workload 2: also replay the whole routing stream under every policy")
     ap.add_argument("--layers", type=int, default=None,
@@ -538,6 +638,9 @@ def main():
         from routed_expert_ffn_histogram_gb300 import build as B
 
         B.build()
+        if args.prefill_slots:
+            staged_prefill_leg(args, wl)
+            return
         res = prefill_leg(args, wl)
         flops = 6.0 * wl.hidden * wl.inter * wl.tokens * wl.top_k
         ffn_s = statistics.median(res["ffn_ms"]) / 1e3

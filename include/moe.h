@@ -237,7 +237,8 @@ typedef struct {
     uint64_t evictions;    /* resident experts displaced by a miss           */
     uint64_t h2d_bytes;    /* bytes copied host -> device by stage           */
     uint64_t errors;       /* stage calls that failed and were rolled back   */
-    uint64_t events;       /* stage calls served                             */
+    uint64_t events;       /* staging events served (one per moe_pool_stage  */
+                           /* call, one per window of moe_prefill_staged)    */
 } moe_counters;
 
 /* Create a pool.  Stores a copy of *desc; the buffers stay caller-owned and
@@ -251,7 +252,8 @@ MOE_API int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out_pool);
  *      enqueued so far on `compute` is done, so counts_host is valid;
  *   2. U = {e : counts_host[e] > 0}.  Every resident e in U is a hit and is
  *      touched; every absent e in U, ascending, takes the lowest free slot,
- *      else evicts the least recently used resident expert not in U;
+ *      else evicts the resident expert not in U that the pool's policy
+ *      names (the least recently used one under MOE_POLICY_LRU);
  *   3. issues one cudaMemcpyAsync (pinned host -> slot) per miss on `copy`,
  *      records an event there and makes `compute` wait on it;
  *   4. copies the layer's slot map (int32 [E], -1 = absent) to slot_of_dev
@@ -266,6 +268,41 @@ MOE_API int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out_pool);
 MOE_API int moe_pool_stage(moe_pool_t* pool, int layer, const int32_t* counts_host,
                    int32_t* slot_of_dev, moe_stream_t compute, moe_stream_t copy,
                    int timeout_ms);
+
+/* Prefill of one layer through a pool whose slots may be fewer than the
+ * layer's routed experts: per-layer unique-expert staging in windows, each
+ * unique expert loaded at most once per call [R3][P2].
+ *   1. waits (as moe_pool_stage, at most timeout_ms) until all work enqueued
+ *      so far on `compute` is done, so counts_host is final;
+ *   2. on `compute`: zeroes out and quantises every token's x once into its
+ *      k grouped rows (as moe_expert_ffn, MOE_PATH_PREFILL);
+ *   3. cuts U = {e : counts_host[e] > 0}, ascending, into windows of at most
+ *      `window` experts.  Window i is one staging event (as moe_pool_stage,
+ *      step 2, over the window's experts) whose victims are never the
+ *      previous window's experts; its miss copies go on `copy` after the
+ *      GEMMs of window i - 2 (which may have read the evicted slots) and
+ *      overlap the GEMMs of window i - 1; `compute` then waits for them and
+ *      runs the window's grouped gate/up and down GEMMs, the down GEMM
+ *      adding w * y into out.  No host wait after step 1.
+ *   x_bf16, ids, w, offsets, perm, inv, workspace, out: as moe_expert_ffn
+ *            on the prefill path (workspace >= moe_ffn_workspace_bytes(...,
+ *            MOE_PATH_PREFILL)); out is complete once `compute` reaches the
+ *            end of the call's work
+ *   counts_host  pinned int32 [E] from the same moe_route_plan call (sum
+ *            T * k)
+ *   window   1 <= window <= S / 2 (a window and its predecessor are
+ *            resident together)
+ * A dry-run pool performs steps 1 and 3's bookkeeping only (no device
+ * pointers are read).  Pools staging decode parts only (MOE_STAGE_DECODE)
+ * lack the row-major down matrix: MOE_ERR_UNSUPPORTED.  If a window's
+ * staging fails, MOE_ERR_CUDA is returned as moe_pool_stage does, earlier
+ * windows' work stays enqueued and out is incomplete.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_TIMEOUT, MOE_ERR_CUDA. */
+MOE_API int moe_prefill_staged(moe_pool_t* pool, int layer, const void* x_bf16, int T, int k,
+                               const int32_t* ids, const float* w, const int32_t* offsets,
+                               const int32_t* perm, const int32_t* inv, const int32_t* counts_host,
+                               int window, void* workspace, size_t ws_bytes, float* out,
+                               moe_stream_t compute, moe_stream_t copy, int timeout_ms);
 
 /* Counters of one layer, or summed over all layers with layer = -1. */
 MOE_API int moe_pool_counters(const moe_pool_t* pool, int layer, moe_counters* out);

@@ -18,6 +18,10 @@ Parity status per function (what pins it, see ``tests/test_oracle_*.py``):
   * PolicyPool (lru/fifo/lfu/lfru/slru)  pinned (hand-worked event streams per policy,
                                         LRU mode against lru_step, exhaustive
                                         offline-optimal lower bound on tiny streams)
+  * PolicyPool.staged_prefill ......... pinned (hand-worked windows, a case where
+                                        keeping the window in flight changes the
+                                        LFU victim, load-once and residency
+                                        invariants)
   * expert_gateup / expert_down ....... pinned (integer-exact case, float64 numpy bound)
   * layer (decode, prefill) ........... pinned piecewise; the end-to-end float
                                         value has no printed worked example
@@ -291,8 +295,9 @@ class PolicyPool:
             return min(cand, key=lambda e: (e in self.protected, self.last_routed[e]))
         return min(cand, key=lambda e: self.last_routed[e])
 
-    def step(self, counts):
-        """Apply one event; returns the list of (expert, slot) loads."""
+    def step(self, counts, keep=()):
+        """Apply one event; returns the list of (expert, slot) loads.  Experts
+        in ``keep`` (still read by work in flight) are never victims."""
         routed = [e for e in range(self.E) if counts[e] > 0]
         if len(routed) > self.S:
             raise OverflowError("unique routed experts exceed the slots")
@@ -309,7 +314,7 @@ class PolicyPool:
             if free:
                 slot = free[0]
             else:
-                v = self._victim(set(routed))
+                v = self._victim(set(routed) | set(keep))
                 slot = self.slot_of.pop(v)
                 self.protected.discard(v)
                 self.evictions += 1
@@ -317,6 +322,23 @@ class PolicyPool:
             self.misses += 1
             loads.append((e, slot))
         return loads
+
+    def staged_prefill(self, counts, window):
+        """The staging events of one prefill call through a pool smaller than
+        the routed set: the routed experts, ascending, cut into windows of at
+        most ``window``; each window is one event, and the previous window's
+        experts (whose GEMMs may still run) are never its victims.  Returns
+        [(window experts, loads)].  Every routed expert sits in exactly one
+        window, so none is loaded twice in a call (the pages' "each unique
+        expert loaded once" for prefill)."""
+        routed = [e for e in range(self.E) if counts[e] > 0]
+        out, prev = [], []
+        for i in range(0, len(routed), window):
+            win = routed[i:i + window]
+            cw = [counts[e] if e in win else 0 for e in range(self.E)]
+            out.append((win, self.step(cw, keep=prev)))
+            prev = win
+        return out
 
     def slot_map(self) -> np.ndarray:
         m = np.full(self.E, -1, np.int32)

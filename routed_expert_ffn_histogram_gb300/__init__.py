@@ -166,6 +166,7 @@ class Pool:
     def __init__(self, layers, experts, slots, hidden, inter, host_experts=None, dev_slots=None,
                  preload=False, dry_run=False, policy=0, stage_parts=0):
         self.layers, self.experts, self.slots, self.hidden, self.inter = layers, experts, slots, hidden, inter
+        self.dry_run = bool(dry_run)
         self._keep = (host_experts, dev_slots)
         if isinstance(policy, str):
             policy = POLICIES[policy]
@@ -186,6 +187,23 @@ class Pool:
             return rc
         check("moe_pool_stage", rc)
         return rc
+
+    def prefill_staged(self, layer, counts_host, window, k, x_bf16=None, plan: RoutePlan = None, out=None,
+                       workspace=None, compute=None, copy=None, timeout_ms=10000, T=None) -> None:
+        """Prefill of one layer through this pool in windows of at most
+        ``window`` unique experts (moe_prefill_staged).  ``counts_host`` is
+        the routing's pinned per-expert counts.  On a dry-run pool only the
+        staging bookkeeping runs: pass T and leave the tensors out."""
+        if T is None:
+            T = x_bf16.shape[0]
+        comp = None if self.dry_run else stream_handle(compute)
+        cop = None if self.dry_run else (stream_handle(copy) if copy is not None else comp)
+        p = plan
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        check("moe_prefill_staged", lib().moe_prefill_staged(
+            self.handle, layer, ptr(x_bf16), T, k, ptr(p.ids) if p else None, ptr(p.w) if p else None,
+            ptr(p.offsets) if p else None, ptr(p.perm) if p else None, ptr(p.inv) if p else None,
+            ptr(counts_host), window, ptr(workspace), ws_bytes, ptr(out), comp, cop, timeout_ms))
 
     def counters(self, layer=-1) -> dict:
         c = MoeCounters()

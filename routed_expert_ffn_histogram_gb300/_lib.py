@@ -62,6 +62,8 @@ SIGNATURES = {
     "moe_route_plan_noalloc": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_pool_create": (_i32, [C.POINTER(MoePoolDesc), C.POINTER(C.c_void_p)]),
     "moe_pool_stage": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _i32]),
+    "moe_prefill_staged": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp,
+                                  _vp, _vp, _i32]),
     "moe_pool_counters": (_i32, [_vp, _i32, C.POINTER(MoeCounters)]),
     "moe_pool_slot_map": (_i32, [_vp, _i32, _vp]),
     "moe_pool_last_loads": (_i32, [_vp, _i32, _vp, _vp, C.POINTER(C.c_int)]),

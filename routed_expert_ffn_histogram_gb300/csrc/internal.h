@@ -122,6 +122,12 @@ int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t 
 
 size_t prefill_workspace_bytes(int T, int k, int H, int I);
 int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+// The prefill path in two parts: zeroing + activation quantisation once,
+// then the grouped GEMMs of the expert groups [e0, e1) (slots from the host
+// table slot_tab when it is given, else from the device map a.slot_of).
+int launch_prefill_prepare(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+int launch_prefill_experts(const FfnArgs& a, void* ws, int e0, int e1, const int32_t* slot_tab, int max_mtiles,
+                           cudaStream_t s);
 
 int launch_combine(const float* y_perm, const float* w, const int32_t* inv, int T, int k, int H,
                    float* out, cudaStream_t s);

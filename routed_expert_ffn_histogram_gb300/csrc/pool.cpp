@@ -25,7 +25,9 @@
 //         if it overflows, goes back to probation with a fresh stamp.
 //         victim: oldest probationary, else oldest protected.
 // A loaded expert gets a fresh stamp, count 1, probation.
+#include <algorithm>
 #include <chrono>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <thread>
@@ -49,6 +51,7 @@ struct moe_pool {
     std::vector<int> last_n;            // [L]
     int32_t* map_pinned = nullptr;      // [L][E] staging for slot-map uploads
     cudaEvent_t ev_compute = nullptr, ev_copy = nullptr;
+    cudaEvent_t ev_win[2] = {nullptr, nullptr};  // staged prefill: window GEMMs finished
     int inject_fail = 0;
 };
 
@@ -96,8 +99,9 @@ void touch(LayerState& ls, int s, int policy, int S) {
 }
 
 // Slot to evict for a miss: a resident expert with counts[e] == 0 (not
-// routed in this event).
-int victim_slot(const LayerState& ls, int policy, int S, const int32_t* counts) {
+// routed in this event) and, when keep is given, keep[e] == 0 (not read by
+// work still in flight).
+int victim_slot(const LayerState& ls, int policy, int S, const int32_t* counts, const uint8_t* keep) {
     int best = -1;
     auto better = [&](int i, int b) -> bool {
         switch (policy) {
@@ -113,7 +117,7 @@ int victim_slot(const LayerState& ls, int policy, int S, const int32_t* counts) 
     };
     for (int i = 0; i < S; ++i) {
         const int e = ls.se[i];
-        if (e < 0 || counts[e] > 0) continue;
+        if (e < 0 || counts[e] > 0 || (keep && keep[e])) continue;
         if (best < 0 || better(i, best)) best = i;
     }
     return best;
@@ -184,6 +188,7 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
                                       cudaHostAllocDefault);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_compute, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_copy, cudaEventDisableTiming);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&p->ev_win[i], cudaEventDisableTiming);
         if (e != cudaSuccess) {
             moe_pool_destroy(p);
             return moe::cuda_fail(e);
@@ -208,15 +213,17 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
     return MOE_OK;
 }
 
-extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_host, int32_t* slot_of_dev,
-                              moe_stream_t compute, moe_stream_t copy, int timeout_ms) {
-    if (!p || !counts_host || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+namespace {
+
+// One staging event of `layer` over U = {e : counts[e] > 0}: plan hits,
+// misses and victims on a copy of the layer's state (victims never in U,
+// nor in `keep`), enqueue the miss copies on `ps`, and commit.  If a copy
+// cannot be enqueued, only the copies already enqueued are applied.
+// *copied tells whether any copy was enqueued.
+int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* keep, cudaStream_t ps,
+                bool* copied) {
     const int S = p->d.slots_per_layer, E = p->d.experts;
-    cudaStream_t cs = static_cast<cudaStream_t>(compute), ps = static_cast<cudaStream_t>(copy);
-    if (!p->d.dry_run) {
-        const int rc = wait_stream(p, cs, timeout_ms);
-        if (rc != MOE_OK) return rc;
-    }
+    *copied = false;
     int32_t* se = &p->slot_expert[size_t(layer) * S];
     int32_t* es = &p->expert_slot[size_t(layer) * E];
     int64_t* st = &p->stamp[size_t(layer) * S];
@@ -228,8 +235,8 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
 
     int uniq = 0;
     for (int e = 0; e < E; ++e) {
-        if (counts_host[e] < 0) return MOE_ERR_INVALID;
-        uniq += counts_host[e] > 0;
+        if (counts[e] < 0) return MOE_ERR_INVALID;
+        uniq += counts[e] > 0;
     }
     if (uniq > S) return MOE_ERR_CAPACITY;
 
@@ -243,20 +250,20 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
     ls.clk = clk;
     uint64_t hits = 0;
     for (int e = 0; e < E; ++e)
-        if (counts_host[e] > 0 && ls.es[e] >= 0) {
+        if (counts[e] > 0 && ls.es[e] >= 0) {
             touch(ls, ls.es[e], policy, S);
             ++hits;
         }
     std::vector<Planned> plan;
     for (int e = 0; e < E; ++e) {
-        if (counts_host[e] <= 0 || ls.es[e] >= 0) continue;
+        if (counts[e] <= 0 || ls.es[e] >= 0) continue;
         int s = -1;
         for (int i = 0; i < S; ++i)
             if (ls.se[i] < 0) { s = i; break; }
         int victim = -1;
         if (s < 0) {
-            s = victim_slot(ls, policy, S, counts_host);
-            if (s < 0) return MOE_ERR_CAPACITY;  // cannot happen when uniq <= S
+            s = victim_slot(ls, policy, S, counts, keep);
+            if (s < 0) return MOE_ERR_CAPACITY;  // U and keep together fill the slots
             victim = ls.se[s];
             ls.es[victim] = -1;
         }
@@ -285,6 +292,7 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
         }
         ++done;
     }
+    *copied = done > 0 && !p->d.dry_run;
 
     if (fail != MOE_OK) {
         // Keep only the loads that were enqueued (their slots now hold the new
@@ -323,19 +331,135 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
             p->last_s[size_t(layer) * S + i] = plan[i].slot;
         }
     }
+    return fail;
+}
 
+}  // namespace
+
+extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_host, int32_t* slot_of_dev,
+                              moe_stream_t compute, moe_stream_t copy, int timeout_ms) {
+    if (!p || !counts_host || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    const int E = p->d.experts;
+    cudaStream_t cs = static_cast<cudaStream_t>(compute), ps = static_cast<cudaStream_t>(copy);
     if (!p->d.dry_run) {
-        if (done > 0 && ps != cs) {
+        const int rc = wait_stream(p, cs, timeout_ms);
+        if (rc != MOE_OK) return rc;
+    }
+    bool copied = false;
+    const int fail = stage_event(p, layer, counts_host, nullptr, ps, &copied);
+    if (fail == MOE_ERR_INVALID || fail == MOE_ERR_CAPACITY) return fail;
+    if (!p->d.dry_run) {
+        if (copied && ps != cs) {
             MOE_CUDA_TRY(cudaEventRecord(p->ev_copy, ps));
             MOE_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_copy, 0));
         }
         if (slot_of_dev) {
+            const int32_t* es = &p->expert_slot[size_t(layer) * E];
             int32_t* stage = p->map_pinned + size_t(layer) * E;
             std::memcpy(stage, es, sizeof(int32_t) * E);
             MOE_CUDA_TRY(cudaMemcpyAsync(slot_of_dev, stage, sizeof(int32_t) * E, cudaMemcpyHostToDevice, cs));
         }
     }
     return fail;
+}
+
+extern "C" int moe_prefill_staged(moe_pool_t* p, int layer, const void* x_bf16, int T, int k, const int32_t* ids,
+                                  const float* w, const int32_t* offsets, const int32_t* perm, const int32_t* inv,
+                                  const int32_t* counts_host, int window, void* workspace, size_t ws_bytes,
+                                  float* out, moe_stream_t compute, moe_stream_t copy, int timeout_ms) {
+    if (!p || !counts_host || layer < 0 || layer >= p->d.layers || T < 0 || k < 1 || k > p->d.experts ||
+        k > MOE_MAX_TOPK)
+        return MOE_ERR_INVALID;
+    const int S = p->d.slots_per_layer, E = p->d.experts;
+    if (window < 1 || 2 * window > S) return MOE_ERR_INVALID;
+    if (p->d.stage_parts == MOE_STAGE_DECODE) return MOE_ERR_UNSUPPORTED;  // no row-major down matrix
+    const bool dry = p->d.dry_run;
+    if (!dry && T > 0) {
+        if (!x_bf16 || !ids || !w || !offsets || !perm || !inv || !out || !workspace) return MOE_ERR_INVALID;
+        if (reinterpret_cast<uintptr_t>(x_bf16) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+            reinterpret_cast<uintptr_t>(workspace) % 256)
+            return MOE_ERR_INVALID;
+        if (ws_bytes < moe::prefill_workspace_bytes(T, k, p->d.hidden, p->d.inter)) return MOE_ERR_INVALID;
+    }
+    if (T == 0) return MOE_OK;
+    cudaStream_t cs = static_cast<cudaStream_t>(compute), ps = static_cast<cudaStream_t>(copy);
+    if (!dry) {
+        // routing finished (counts_host is final) and no earlier work still
+        // reads a slot this call may overwrite
+        const int rc = wait_stream(p, cs, timeout_ms);
+        if (rc != MOE_OK) return rc;
+    }
+    int64_t total = 0;
+    for (int e = 0; e < E; ++e) {
+        if (counts_host[e] < 0) return MOE_ERR_INVALID;
+        total += counts_host[e];
+    }
+    if (total != int64_t(T) * k) return MOE_ERR_INVALID;
+
+    // windows: the unique routed experts, ascending, `window` at a time
+    std::vector<int> uniq;
+    for (int e = 0; e < E; ++e)
+        if (counts_host[e] > 0) uniq.push_back(e);
+    const int nu = int(uniq.size()), n_win = (nu + window - 1) / window;
+
+    moe::FfnArgs a;
+    a.slots = static_cast<const uint8_t*>(p->d.dev_slots) + size_t(layer) * S * p->eb;
+    a.expert_bytes = p->eb;
+    a.S = S;
+    a.E = E;
+    a.L = &p->L;
+    a.x = static_cast<const uint16_t*>(x_bf16);
+    a.T = T;
+    a.k = k;
+    a.ids = ids;
+    a.w = w;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.inv = inv;
+    a.slot_of = nullptr;
+    a.out = out;
+    if (!dry) {
+        const int rc = moe::launch_prefill_prepare(a, workspace, ws_bytes, cs);
+        if (rc != MOE_OK) return rc;
+    }
+    const int32_t* es = &p->expert_slot[size_t(layer) * E];
+    std::vector<int32_t> cw(E);
+    std::vector<uint8_t> keep(E);
+    std::vector<int32_t> tab;
+    int prev_lo = 0, prev_hi = 0;
+    for (int wi = 0; wi < n_win; ++wi) {
+        const int lo = wi * window, hi = std::min(nu, lo + window);
+        std::fill(cw.begin(), cw.end(), 0);
+        std::fill(keep.begin(), keep.end(), uint8_t(0));
+        for (int i = lo; i < hi; ++i) cw[uniq[i]] = counts_host[uniq[i]];
+        // the previous window's GEMMs may still be running: its slots stay
+        for (int i = prev_lo; i < prev_hi; ++i) keep[uniq[i]] = 1;
+        // victims can only be slots last read by window wi - 2 or earlier
+        if (!dry && wi >= 2 && ps != cs) MOE_CUDA_TRY(cudaStreamWaitEvent(ps, p->ev_win[wi & 1], 0));
+        bool copied = false;
+        const int rc = stage_event(p, layer, cw.data(), keep.data(), ps, &copied);
+        if (rc != MOE_OK) return rc;
+        if (!dry) {
+            if (copied && ps != cs) {
+                MOE_CUDA_TRY(cudaEventRecord(p->ev_copy, ps));
+                MOE_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_copy, 0));
+            }
+            const int e0 = uniq[lo], e1 = uniq[hi - 1] + 1;
+            tab.assign(size_t(e1 - e0), -1);
+            int rows = 0;
+            for (int e = e0; e < e1; ++e)
+                if (cw[e] > 0) {
+                    tab[e - e0] = es[e];
+                    rows += cw[e];
+                }
+            const int r2 = moe::launch_prefill_experts(a, workspace, e0, e1, tab.data(), rows / 128 + (hi - lo) + 1, cs);
+            if (r2 != MOE_OK) return r2;
+            MOE_CUDA_TRY(cudaEventRecord(p->ev_win[wi & 1], cs));
+        }
+        prev_lo = lo;
+        prev_hi = hi;
+    }
+    return MOE_OK;
 }
 
 extern "C" int moe_pool_counters(const moe_pool_t* p, int layer, moe_counters* out) {
@@ -456,6 +580,8 @@ extern "C" void moe_pool_destroy(moe_pool_t* p) {
     if (!p) return;
     if (p->ev_compute) cudaEventDestroy(p->ev_compute);
     if (p->ev_copy) cudaEventDestroy(p->ev_copy);
+    for (cudaEvent_t ev : p->ev_win)
+        if (ev) cudaEventDestroy(ev);
     if (p->map_pinned) cudaFreeHost(p->map_pinned);
     delete p;
 }

@@ -80,9 +80,12 @@ constexpr int kLaunchRegs = 65536 / kThreads;
 constexpr int kRegsCtl = 48, kRegsSf = 144, kRegsEpi = 160;
 static_assert(kRegsCtl + kRegsSf + 2 * kRegsEpi == 4 * kLaunchRegs, "register split sums to the launch's share");
 
+constexpr int kMaxSlotTab = MOE_MAX_EXPERTS;  // experts of one launch when slots come by value
+
 struct GemmParams {
     const int32_t* offsets;     // [E+1] grouped row ranges
-    const int32_t* slot_of;     // [E]
+    const int32_t* slot_of;     // [E] device slot map, or nullptr: slot_tab
+    int32_t slot_tab[kMaxSlotTab];  // slot of each of the E experts (E <= kMaxSlotTab)
     int E, A, S;
     int K, KB;                  // reduction length and its 32-blocks
     int N;                      // weight rows (2I for gate/up, H for down)
@@ -232,7 +235,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                 const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
                 sm.offs[e] = o0;
                 if (e == p.E - 1) sm.offs[p.E] = o1;
-                sm.slot[e] = p.slot_of[e];
+                sm.slot[e] = p.slot_of ? p.slot_of[e] : p.slot_tab[e];
                 v = (o1 - o0 + kBM - 1) / kBM;
             }
             int incl = v;
@@ -639,12 +642,34 @@ PrefillWs prefill_ws(int T, int k, int H, int I) {
 
 size_t prefill_workspace_bytes(int T, int k, int H, int I) { return prefill_ws(T, k, H, I).total; }
 
-int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+// Zero the error word, scale buffers and out; quantise every token's x once
+// into its k grouped rows.
+int launch_prefill_prepare(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
     const Layout& L = *a.L;
     const PrefillWs w = prefill_ws(a.T, a.k, L.H, L.I);
     if (ws_bytes < w.total) return MOE_ERR_INVALID;
     if (L.H > 4096 || L.I > 4096 || a.E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
     if (a.T == 0) return MOE_OK;
+    const int A = a.T * a.k;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    MOE_CUDA_TRY(cudaMemsetAsync(base + w.err, 0, 4, s));
+    MOE_CUDA_TRY(cudaMemsetAsync(base + w.xs, 0, size_t(A) * w.xs_stride, s));
+    MOE_CUDA_TRY(cudaMemsetAsync(base + w.hs, 0, size_t(A) * w.hs_stride, s));
+    MOE_CUDA_TRY(cudaMemsetAsync(a.out, 0, size_t(a.T) * L.H * sizeof(float), s));
+    return launch_quant_mxfp8_scatter(a.x, L.H, a.inv, a.k, a.T, base + w.xq, base + w.xs, w.xs_stride, s);
+}
+
+// Gate/up and down GEMMs over the groups of experts [e0, e1); the down
+// epilogue adds w * y into out.  Slots come from slot_tab (host, e1 - e0
+// entries) when given, else from the device map a.slot_of.  max_mtiles
+// bounds the 128-row tiles of those groups (it only sizes the grid).
+int launch_prefill_experts(const FfnArgs& a, void* ws, int e0, int e1, const int32_t* slot_tab, int max_mtiles,
+                           cudaStream_t s) {
+    const Layout& L = *a.L;
+    const PrefillWs w = prefill_ws(a.T, a.k, L.H, L.I);
+    if (e0 < 0 || e1 > a.E || e0 > e1) return MOE_ERR_INVALID;
+    if (slot_tab && e1 - e0 > kMaxSlotTab) return MOE_ERR_UNSUPPORTED;
+    if (a.T == 0 || e0 == e1 || max_mtiles <= 0) return MOE_OK;
     const int A = a.T * a.k;
     uint8_t* base = static_cast<uint8_t*>(ws);
     uint8_t* xq = base + w.xq;
@@ -653,25 +678,22 @@ int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
     uint8_t* hs = base + w.hs;
     uint32_t* err = reinterpret_cast<uint32_t*>(base + w.err);
 
-    MOE_CUDA_TRY(cudaMemsetAsync(err, 0, 4, s));
-    MOE_CUDA_TRY(cudaMemsetAsync(xs, 0, size_t(A) * w.xs_stride, s));
-    MOE_CUDA_TRY(cudaMemsetAsync(hs, 0, size_t(A) * w.hs_stride, s));
-    MOE_CUDA_TRY(cudaMemsetAsync(a.out, 0, size_t(a.T) * L.H * sizeof(float), s));
-    int rc = launch_quant_mxfp8_scatter(a.x, L.H, a.inv, a.k, a.T, xq, xs, w.xs_stride, s);
-    if (rc != MOE_OK) return rc;
-
     CUtensorMap map_x, map_gu, map_h, map_d;
-    rc = make_map_act(&map_x, xq, L.H, A);
+    int rc = make_map_act(&map_x, xq, L.H, A);
     if (rc == MOE_OK) rc = make_map_weights(&map_gu, a.slots, L.H, 2 * L.I, a.S, L.rs_gu, a.expert_bytes);
     if (rc == MOE_OK) rc = make_map_act(&map_h, hq, L.I, A);
     if (rc == MOE_OK) rc = make_map_weights(&map_d, a.slots + L.d_off, L.I, L.H, a.S, L.rs_d, a.expert_bytes);
     if (rc != MOE_OK) return rc;
 
-    const int max_mtiles = A / kBM + a.E;
     GemmParams g{};
-    g.offsets = a.offsets;
-    g.slot_of = a.slot_of;
-    g.E = a.E;
+    g.offsets = a.offsets + e0;
+    g.E = e1 - e0;
+    if (slot_tab) {
+        g.slot_of = nullptr;
+        for (int e = 0; e < g.E; ++e) g.slot_tab[e] = slot_tab[e];
+    } else {
+        g.slot_of = a.slot_of + e0;
+    }
     g.A = A;
     g.S = a.S;
     g.expert_bytes = a.expert_bytes;
@@ -709,6 +731,12 @@ int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
     g.k = a.k;
     g.out = a.out;
     return launch_gemm(map_h, map_d, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
+}
+
+int launch_prefill_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+    int rc = launch_prefill_prepare(a, ws, ws_bytes, s);
+    if (rc != MOE_OK || a.T == 0) return rc;
+    return launch_prefill_experts(a, ws, 0, a.E, nullptr, a.T * a.k / kBM + a.E, s);
 }
 
 }  // namespace moe

@@ -116,3 +116,57 @@ def test_prefill_matches_decode_path_closely():
     out_p, lg, x, _, _ = _run_prefill(M, pool, wl)
     out_d = _gpu_layer(M, pool, 0, lg, x, wl.top_k, M.MOE_PATH_DECODE)
     assert rel_l2(out_p, out_d) < 0.1
+
+
+@pytest.mark.parametrize("wid,slots,window,T", [(0, 4, 2, 16), (0, 6, 1, 16), (3, 8, 4, 64)])
+def test_prefill_staged_small_pool(wid, slots, window, T):
+    """Prefill through a pool with fewer slots than routed experts
+    (moe_prefill_staged, windows staged on a copy stream): out within the
+    prefill tolerance of the oracle and within fp32 atomic-order rounding of
+    the resident-pool path; slot map and hit/miss/eviction counters
+    bit-exact against the oracle's window events; every routed expert loaded
+    at most once per call."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+    from helpers import build_host_store
+
+    wl = S.WORKLOADS[wid]
+    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    host, eb = build_host_store(M, wl, 1)
+    dev = torch.empty(slots * eb, dtype=torch.uint8, device="cuda")
+    pool = M.Pool(1, E, slots, H, I, host_experts=host, dev_slots=dev, policy="lru")
+    lg = S.logits(wl, 0, 0, T)
+    x = S.activations_bf16_bits(wl, 0, 0, T)
+    xt = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_PREFILL)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    ref_pool = oracle.PolicyPool(slots, E, "lru")
+    ref, _ = _oracle_tokens(wl, lg, x, np.arange(T))
+    for call in range(2):
+        with torch.cuda.stream(compute):
+            M.moe_route_plan(torch.from_numpy(lg).cuda(), k, plan, stream=compute)
+            pool.prefill_staged(0, plan.counts_host, window, k, x_bf16=xt, plan=plan, out=out, workspace=ws,
+                                compute=compute, copy=copy)
+        compute.synchronize()
+        counts = plan.counts_host.numpy().copy()
+        before = ref_pool.misses
+        ref_pool.staged_prefill(counts, window)
+        assert ref_pool.misses - before <= int((counts > 0).sum())
+        _check_prefill(out.cpu().numpy(), ref)
+        assert np.array_equal(pool.slot_map(0), ref_pool.slot_map())
+        c, r = pool.counters(0), ref_pool.counters()
+        assert (c["hits"], c["misses"], c["evictions"]) == (r["hits"], r["misses"], r["evictions"])
+        assert c["h2d_bytes"] == c["misses"] * eb
+    # the same routing on a fully resident pool
+    dev_all = torch.empty(E * eb, dtype=torch.uint8, device="cuda")
+    resident = M.Pool(1, E, E, H, I, host_experts=host, dev_slots=dev_all, preload=True)
+    out2 = torch.empty_like(out)
+    M.moe_expert_ffn(resident, 0, xt, plan, torch.arange(E, dtype=torch.int32, device="cuda"), out2, ws,
+                     path=M.MOE_PATH_PREFILL)
+    torch.cuda.synchronize()
+    assert rel_l2(out.cpu().numpy(), out2.cpu().numpy()) <= 1e-6
+    pool.close()
+    resident.close()

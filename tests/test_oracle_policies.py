@@ -127,3 +127,58 @@ def test_no_policy_beats_the_offline_optimum_and_bookkeeping_holds():
             assert c["hits"] + c["misses"] == sum(len(ev) for ev in events)
             assert c["misses"] >= len(set().union(*map(set, events)))
             assert sum(len(l) for l in loads) == c["misses"]
+
+
+def test_staged_prefill_hand_worked_lru():
+    """Six routed experts, four slots, windows of two, cold LRU pool: the
+    first two windows fill the free slots; the third evicts the first
+    window's experts (the oldest) and never the second window's."""
+    p = oracle.PolicyPool(4, 6, "lru")
+    got = p.staged_prefill(np.ones(6, np.int32), 2)
+    assert [w for w, _ in got] == [[0, 1], [2, 3], [4, 5]]
+    assert [loads for _, loads in got] == [[(0, 0), (1, 1)], [(2, 2), (3, 3)], [(4, 0), (5, 1)]]
+    assert p.counters() == dict(hits=0, misses=6, evictions=2)
+
+
+def test_staged_prefill_keeps_the_window_in_flight():
+    """LFU would evict the just-loaded (once-used) experts of the previous
+    window; the staged event must take the frequently used ones instead."""
+    p = oracle.PolicyPool(4, 6, "lfu")
+    for _ in range(3):
+        p.step(_ev(6, 2, 3))          # 2 -> slot 0, 3 -> slot 1, three uses each
+    got = p.staged_prefill(_ev(6, 0, 1, 4, 5), 2)
+    assert got == [([0, 1], [(0, 2), (1, 3)]), ([4, 5], [(4, 0), (5, 1)])]
+    # a plain event in the same state takes the once-used experts 0 and 1
+    q = oracle.PolicyPool(4, 6, "lfu")
+    for _ in range(3):
+        q.step(_ev(6, 2, 3))
+    q.step(_ev(6, 0, 1))
+    assert q.step(_ev(6, 4, 5)) == [(4, 2), (5, 3)]
+
+
+@pytest.mark.parametrize("policy", oracle.POLICIES)
+def test_staged_prefill_invariants(policy):
+    rng = np.random.default_rng(11)
+    S, E = 6, 20
+    p = oracle.PolicyPool(S, E, policy)
+    for call in range(60):
+        window = (1, 2, 3)[call % 3]
+        counts = np.bincount(rng.choice(E, size=int(rng.integers(1, 40))), minlength=E).astype(np.int32)
+        routed = [e for e in range(E) if counts[e] > 0]
+        before = p.misses
+        where = {e: int(s) for e, s in enumerate(p.slot_map()) if s >= 0}   # expert -> slot, replayed
+        held = set()          # slots of the previous window's experts
+        seen = []
+        for win, loads in p.staged_prefill(counts, window):
+            assert 1 <= len(win) <= window and all(counts[e] > 0 for e in win)
+            assert all(e in win for e, _ in loads)
+            for e, s in loads:
+                assert s not in held                  # the window in flight keeps its slots
+                where = {x: t for x, t in where.items() if t != s}
+                where[e] = s
+            assert all(e in where for e in win)       # the whole window is resident
+            held = {where[e] for e in win}
+            seen += win
+        assert seen == routed                         # every routed expert in exactly one window
+        assert p.misses - before <= len(routed)       # each routed expert loaded at most once
+        assert where == {e: int(s) for e, s in enumerate(p.slot_map()) if s >= 0}

@@ -77,3 +77,59 @@ def test_decode_only_staging_accounting():
     assert cp["h2d_bytes"] == cp["misses"] * (d_off + eb - dt_off)
     with pytest.raises(M.MoeError):
         M.Pool(1, E, S, H, I, dry_run=True, stage_parts=2)
+
+
+def _prefill_counts(rng, E, k, T, bias):
+    rank = rng.permutation(E) + 1
+    c = np.zeros(E, np.int32)
+    for _ in range(T):
+        lg = rng.standard_normal(E) - bias * np.log(rank)
+        c[np.argsort(-lg, kind="stable")[:k]] += 1
+    return c
+
+
+@pytest.mark.parametrize("policy", oracle.POLICIES)
+@pytest.mark.parametrize("S,E,window", [(4, 16, 2), (6, 16, 3), (8, 32, 4), (8, 32, 1)])
+def test_dry_run_staged_prefill_matches_oracle(policy, S, E, window):
+    """moe_prefill_staged's staging (dry run) against the oracle's window
+    events: slot maps after every call and counters bit-exact, one event per
+    window, interleaved with ordinary decode-style events."""
+    rng = np.random.default_rng(S * 100 + E + window)
+    layers, k = 2, 2
+    pool = M.Pool(layers, E, S, 256, 512, dry_run=True, policy=policy)
+    ref = [oracle.PolicyPool(S, E, policy) for _ in range(layers)]
+    windows = 0
+    for call in range(40):
+        layer = call % layers
+        if call % 5 == 4:
+            c = _prefill_counts(rng, E, k, 1, 1.0)    # a decode step in between
+            assert pool.stage(layer, c) == M.MOE_OK
+            ref[layer].step(c)
+        else:
+            T = int(rng.integers(1, 30))
+            c = _prefill_counts(rng, E, k, T, 0.8)
+            pool.prefill_staged(layer, c, window, k, T=T)
+            windows += len(ref[layer].staged_prefill(c, window))
+        assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
+    for layer in range(layers):
+        got, exp = pool.counters(layer), ref[layer].counters()
+        assert (got["hits"], got["misses"], got["evictions"]) == (exp["hits"], exp["misses"], exp["evictions"])
+    assert pool.counters()["events"] == windows + 8
+
+
+def test_staged_prefill_arguments():
+    pool = M.Pool(1, 16, 6, 256, 512, dry_run=True)
+    c = np.zeros(16, np.int32)
+    c[[1, 5, 9]] = [2, 1, 1]
+    with pytest.raises(M.MoeError) as e:
+        pool.prefill_staged(0, c, 4, 2, T=2)          # window > S / 2
+    assert e.value.status == M.MOE_ERR_INVALID
+    with pytest.raises(M.MoeError) as e:
+        pool.prefill_staged(0, c, 3, 2, T=3)          # counts do not sum to T * k
+    assert e.value.status == M.MOE_ERR_INVALID
+    pool.prefill_staged(0, c, 3, 2, T=2)
+    assert pool.counters(0)["misses"] == 3
+    dec = M.Pool(1, 16, 6, 256, 512, dry_run=True, stage_parts="decode")
+    with pytest.raises(M.MoeError) as e:
+        dec.prefill_staged(0, c, 3, 2, T=2)
+    assert e.value.status == M.MOE_ERR_UNSUPPORTED
