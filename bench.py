@@ -448,6 +448,9 @@ def offload_leg(args, wl):
             rc = pool.stage(l, plan.counts_host, slot_of, compute=compute, copy=copy)
             if rc != M.MOE_OK:
                 raise RuntimeError(f"stage failed: {rc}")
+            if args.prefetch:
+                # the next layer's likely experts, copied while this layer computes
+                pool.prefetch((l + 1) % L, args.prefetch, compute=compute, copy=copy)
             M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE, stream=compute)
         out_pin[g].copy_(out_d, non_blocking=True)
 
@@ -479,9 +482,13 @@ def offload_leg(args, wl):
             "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host",
                          "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
                          "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
-                         "traffic": None, "bytes_per_miss": (c1["h2d_bytes"] - c0["h2d_bytes"]) //
-                                                           max(1, c1["misses"] - c0["misses"])},
-            "offload": {"policy": args.policy, "stage_parts": args.stage_parts, "hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
+                         "traffic": None, "bytes_per_load": (c1["h2d_bytes"] - c0["h2d_bytes"]) //
+                                                           max(1, c1["misses"] - c0["misses"] + c1["prefetches"] -
+                                                               c0["prefetches"])},
+            "offload": {"policy": args.policy, "stage_parts": args.stage_parts, "prefetch": args.prefetch,
+                        "prefetches": c1["prefetches"] - c0["prefetches"],
+                        "prefetch_hits": c1["prefetch_hits"] - c0["prefetch_hits"],
+                        "hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
                         "evictions": c1["evictions"] - c0["evictions"], "h2d_bytes": h2d,
                         "misses_per_step": (c1["misses"] - c0["misses"]) / args.steps},
             "e2e": {"value": 1e3 / ms, "unit": "tokens/s",
@@ -610,6 +617,8 @@ def main():
                     help="eviction policy of the offload pool (--workload 2)")
     ap.add_argument("--stage-parts", default="whole", choices=["whole", "decode"],
                     help="--workload 2: copy whole experts, or only what the decode kernel reads")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="workload 2: after each layer's staging, prefetch up to this many experts of the next layer")
     ap.add_argument("--prefill-slots", type=int, default=None,
                     help="workloads 3/4: run the layer through a pool of this many slots (moe_prefill_staged)")
     ap.add_argument("--window", type=int, default=None,

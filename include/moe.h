@@ -239,6 +239,8 @@ typedef struct {
     uint64_t errors;       /* stage calls that failed and were rolled back   */
     uint64_t events;       /* staging events served (one per moe_pool_stage  */
                            /* call, one per window of moe_prefill_staged)    */
+    uint64_t prefetches;   /* experts copied in by moe_pool_prefetch         */
+    uint64_t prefetch_hits;/* of those, routed before being evicted          */
 } moe_counters;
 
 /* Create a pool.  Stores a copy of *desc; the buffers stay caller-owned and
@@ -303,6 +305,27 @@ MOE_API int moe_prefill_staged(moe_pool_t* pool, int layer, const void* x_bf16, 
                                const int32_t* perm, const int32_t* inv, const int32_t* counts_host,
                                int window, void* workspace, size_t ws_bytes, float* out,
                                moe_stream_t compute, moe_stream_t copy, int timeout_ms);
+
+/* Speculative staging of `layer` ahead of its routing (next-layer
+ * prefetch) [X3]: the layer's non-resident experts that were routed in at
+ * least one earlier event, most often routed first (ties: lower id), are
+ * copied in one by one, at most max_loads of them, each into the lowest
+ * free slot, else into the slot of the resident expert the pool's policy
+ * names as victim (never one loaded by this call), but only while that
+ * victim was routed in fewer events than the candidate; the first
+ * candidate that finds no such slot ends the call.  A prefetched expert is
+ * loaded as a miss would be (policy state, h2d_bytes, evictions), counts in
+ * `prefetches`, and counts in `prefetch_hits` when an event routes it
+ * before it is evicted.  The copies go on `copy` after all work enqueued so
+ * far on `compute` (which may still read the evicted slots); nothing waits
+ * for them here: the layer's next moe_pool_stage, moe_prefill_staged or
+ * moe_pool_prefetch makes its streams wait first.  No host wait.
+ *   loaded   host int, out: experts copied (may be NULL)
+ * A dry-run pool updates its state only.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA (state as after the copies that
+ * were enqueued). */
+MOE_API int moe_pool_prefetch(moe_pool_t* pool, int layer, int max_loads, moe_stream_t compute,
+                              moe_stream_t copy, int* loaded);
 
 /* Counters of one layer, or summed over all layers with layer = -1. */
 MOE_API int moe_pool_counters(const moe_pool_t* pool, int layer, moe_counters* out);

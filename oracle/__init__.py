@@ -249,8 +249,11 @@ class PolicyPool:
         self.loaded_at = {}        # expert -> time of load
         self.uses = {}             # expert -> events routed since load (load = 1)
         self.protected = set()     # slru
+        self.freq = [0] * experts  # events that routed the expert (prefetch ranking)
+        self.fresh = set()         # loaded by a prefetch, not routed since
         self.time = 0
         self.hits = self.misses = self.evictions = 0
+        self.prefetches = self.prefetch_hits = 0
         if preload:
             for e in range(min(slots, experts)):
                 self._load(e, e)
@@ -304,6 +307,9 @@ class PolicyPool:
         for e in routed:
             if e in self.slot_of:
                 self.hits += 1
+                if e in self.fresh:
+                    self.prefetch_hits += 1
+                    self.fresh.discard(e)
                 self._route_again(e)
         loads = []
         for e in routed:
@@ -317,9 +323,49 @@ class PolicyPool:
                 v = self._victim(set(routed) | set(keep))
                 slot = self.slot_of.pop(v)
                 self.protected.discard(v)
+                self.fresh.discard(v)
                 self.evictions += 1
             self._load(e, slot)
             self.misses += 1
+            loads.append((e, slot))
+        for e in routed:
+            self.freq[e] += 1
+        return loads
+
+    def prefetch(self, max_loads):
+        """Speculative loads ahead of the layer's routing (next-layer
+        prefetch; FATE is the pages' example of the idea, driven there by
+        the next layer's gate, which this path does not have).  Reading:
+        the non-resident experts routed in at least one earlier event, most
+        often routed first (ties: lower id), are loaded one by one, at most
+        ``max_loads``: into the lowest free slot, else into the policy's
+        victim (never one loaded by this call) if that victim was routed in
+        fewer events than the candidate; the first candidate without such a
+        slot ends the call.  Returns the (expert, slot) loads."""
+        cand = sorted((e for e in range(self.E) if e not in self.slot_of and self.freq[e] > 0),
+                      key=lambda e: (-self.freq[e], e))
+        loads, mine = [], set()
+        for e in cand:
+            if len(loads) >= max_loads:
+                break
+            used = set(self.slot_of.values())
+            free = [s for s in range(self.S) if s not in used]
+            if free:
+                slot = free[0]
+            else:
+                if len(mine) >= len(self.slot_of):
+                    break
+                v = self._victim(mine)
+                if self.freq[v] >= self.freq[e]:
+                    break
+                slot = self.slot_of.pop(v)
+                self.protected.discard(v)
+                self.fresh.discard(v)
+                self.evictions += 1
+            self._load(e, slot)
+            self.fresh.add(e)
+            mine.add(e)
+            self.prefetches += 1
             loads.append((e, slot))
         return loads
 
@@ -348,6 +394,9 @@ class PolicyPool:
 
     def counters(self) -> dict:
         return dict(hits=self.hits, misses=self.misses, evictions=self.evictions)
+
+    def prefetch_counters(self) -> dict:
+        return dict(prefetches=self.prefetches, prefetch_hits=self.prefetch_hits)
 
 
 # ---- expert FFN --------------------------------------------------------------

@@ -205,6 +205,15 @@ class Pool:
             ptr(p.offsets) if p else None, ptr(p.perm) if p else None, ptr(p.inv) if p else None,
             ptr(counts_host), window, ptr(workspace), ws_bytes, ptr(out), comp, cop, timeout_ms))
 
+    def prefetch(self, layer, max_loads, compute=None, copy=None) -> int:
+        """Speculative staging of ``layer`` ahead of its routing
+        (moe_pool_prefetch); returns the number of experts copied in."""
+        comp = None if self.dry_run else stream_handle(compute)
+        cop = None if self.dry_run else (stream_handle(copy) if copy is not None else comp)
+        n = C.c_int(0)
+        check("moe_pool_prefetch", lib().moe_pool_prefetch(self.handle, layer, max_loads, comp, cop, C.byref(n)))
+        return n.value
+
     def counters(self, layer=-1) -> dict:
         c = MoeCounters()
         check("moe_pool_counters", lib().moe_pool_counters(self.handle, layer, C.byref(c)))

@@ -45,7 +45,8 @@ class MoePoolDesc(C.Structure):
 
 class MoeCounters(C.Structure):
     _fields_ = [("hits", C.c_uint64), ("misses", C.c_uint64), ("evictions", C.c_uint64),
-                ("h2d_bytes", C.c_uint64), ("errors", C.c_uint64), ("events", C.c_uint64)]
+                ("h2d_bytes", C.c_uint64), ("errors", C.c_uint64), ("events", C.c_uint64),
+                ("prefetches", C.c_uint64), ("prefetch_hits", C.c_uint64)]
 
     def as_dict(self):
         return {f: int(getattr(self, f)) for f, _ in self._fields_}
@@ -64,6 +65,7 @@ SIGNATURES = {
     "moe_pool_stage": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _i32]),
     "moe_prefill_staged": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp,
                                   _vp, _vp, _i32]),
+    "moe_pool_prefetch": (_i32, [_vp, _i32, _i32, _vp, _vp, C.POINTER(C.c_int)]),
     "moe_pool_counters": (_i32, [_vp, _i32, C.POINTER(MoeCounters)]),
     "moe_pool_slot_map": (_i32, [_vp, _i32, _vp]),
     "moe_pool_last_loads": (_i32, [_vp, _i32, _vp, _vp, C.POINTER(C.c_int)]),

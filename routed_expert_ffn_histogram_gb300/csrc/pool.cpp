@@ -45,6 +45,9 @@ struct moe_pool {
     std::vector<int64_t> uses;          // [L][S] touches since load (lfu, lfru)
     std::vector<int8_t> seg;            // [L][S] slru: 0 probation, 1 protected
     std::vector<int64_t> clock;         // [L]
+    std::vector<int64_t> freq;          // [L][E] events that routed the expert (prefetch ranking)
+    std::vector<uint8_t> fresh;         // [L][E] loaded by a prefetch, not routed since
+    std::vector<uint8_t> pending;       // [L] prefetch copies not yet ordered before later work
     std::vector<moe_counters> ctr;      // [L]
     size_t bytes_per_load = 0;          // bytes one miss copies
     std::vector<int32_t> last_e, last_s;  // [L][S]
@@ -52,12 +55,13 @@ struct moe_pool {
     int32_t* map_pinned = nullptr;      // [L][E] staging for slot-map uploads
     cudaEvent_t ev_compute = nullptr, ev_copy = nullptr;
     cudaEvent_t ev_win[2] = {nullptr, nullptr};  // staged prefill: window GEMMs finished
+    std::vector<cudaEvent_t> ev_pf;     // [L] the layer's last prefetch copies finished
     int inject_fail = 0;
 };
 
 namespace {
 
-constexpr uint32_t kStateMagic = 0x4d4f4550u;  // "MOEP"
+constexpr uint32_t kStateMagic = 0x4d4f4551u;  // "MOEQ": with routing frequencies and prefetch flags
 
 struct Planned {
     int32_t e, slot, victim;
@@ -179,6 +183,9 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
     p->uses.assign(nl * S, 0);
     p->seg.assign(nl * S, 0);
     p->clock.assign(nl, 0);
+    p->freq.assign(nl * E, 0);
+    p->fresh.assign(nl * E, 0);
+    p->pending.assign(nl, 0);
     p->ctr.assign(nl, moe_counters{});
     p->last_e.assign(nl * S, -1);
     p->last_s.assign(nl * S, -1);
@@ -189,6 +196,8 @@ extern "C" int moe_pool_create(const moe_pool_desc* desc, moe_pool_t** out) {
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_compute, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_copy, cudaEventDisableTiming);
         for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&p->ev_win[i], cudaEventDisableTiming);
+        p->ev_pf.assign(nl, nullptr);
+        for (size_t l = 0; l < nl && e == cudaSuccess; ++l) e = cudaEventCreateWithFlags(&p->ev_pf[l], cudaEventDisableTiming);
         if (e != cudaSuccess) {
             moe_pool_destroy(p);
             return moe::cuda_fail(e);
@@ -249,10 +258,12 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
     ls.seg.assign(sg, sg + S);
     ls.clk = clk;
     uint64_t hits = 0;
+    std::vector<int> hit_e;
     for (int e = 0; e < E; ++e)
         if (counts[e] > 0 && ls.es[e] >= 0) {
             touch(ls, ls.es[e], policy, S);
             ++hits;
+            hit_e.push_back(e);
         }
     std::vector<Planned> plan;
     for (int e = 0; e < E; ++e) {
@@ -294,13 +305,17 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
     }
     *copied = done > 0 && !p->d.dry_run;
 
+    int64_t* fq = &p->freq[size_t(layer) * E];
+    uint8_t* fr = &p->fresh[size_t(layer) * E];
     if (fail != MOE_OK) {
         // Keep only the loads that were enqueued (their slots now hold the new
         // experts); everything else of the event is not applied.
         for (size_t i = 0; i < done; ++i) {
             const Planned& q = plan[i];
+            fr[q.e] = 0;
             if (q.victim >= 0) {
                 es[q.victim] = -1;
+                fr[q.victim] = 0;
                 ++c.evictions;
             }
             se[q.slot] = q.e;
@@ -323,6 +338,16 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
         c.hits += hits;
         c.misses += plan.size();
         for (const Planned& q : plan) c.evictions += q.victim >= 0;
+        for (int e : hit_e)
+            if (fr[e]) {
+                ++c.prefetch_hits;
+                fr[e] = 0;
+            }
+        for (const Planned& q : plan) {
+            fr[q.e] = 0;
+            if (q.victim >= 0) fr[q.victim] = 0;
+        }
+        for (int e = 0; e < E; ++e) fq[e] += counts[e] > 0;
         c.h2d_bytes += plan.size() * p->bytes_per_load;
         ++c.events;
         p->last_n[layer] = int(plan.size());
@@ -334,6 +359,17 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
     return fail;
 }
 
+// A prefetch of `layer` may still be copying into its slots: order the
+// copy stream (before it overwrites any slot) and the compute stream
+// (before it reads a prefetched expert) after those copies.
+int order_after_prefetch(moe_pool_t* p, int layer, cudaStream_t cs, cudaStream_t ps, bool both) {
+    if (p->d.dry_run || !p->pending[layer]) return MOE_OK;
+    MOE_CUDA_TRY(cudaStreamWaitEvent(ps, p->ev_pf[layer], 0));
+    if (both && cs != ps) MOE_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_pf[layer], 0));
+    p->pending[layer] = 0;
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_host, int32_t* slot_of_dev,
@@ -342,7 +378,8 @@ extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_ho
     const int E = p->d.experts;
     cudaStream_t cs = static_cast<cudaStream_t>(compute), ps = static_cast<cudaStream_t>(copy);
     if (!p->d.dry_run) {
-        const int rc = wait_stream(p, cs, timeout_ms);
+        int rc = wait_stream(p, cs, timeout_ms);
+        if (rc == MOE_OK) rc = order_after_prefetch(p, layer, cs, ps, true);
         if (rc != MOE_OK) return rc;
     }
     bool copied = false;
@@ -386,7 +423,8 @@ extern "C" int moe_prefill_staged(moe_pool_t* p, int layer, const void* x_bf16, 
     if (!dry) {
         // routing finished (counts_host is final) and no earlier work still
         // reads a slot this call may overwrite
-        const int rc = wait_stream(p, cs, timeout_ms);
+        int rc = wait_stream(p, cs, timeout_ms);
+        if (rc == MOE_OK) rc = order_after_prefetch(p, layer, cs, ps, true);
         if (rc != MOE_OK) return rc;
     }
     int64_t total = 0;
@@ -462,6 +500,94 @@ extern "C" int moe_prefill_staged(moe_pool_t* p, int layer, const void* x_bf16, 
     return MOE_OK;
 }
 
+extern "C" int moe_pool_prefetch(moe_pool_t* p, int layer, int max_loads, moe_stream_t compute, moe_stream_t copy,
+                                 int* loaded) {
+    if (loaded) *loaded = 0;
+    if (!p || layer < 0 || layer >= p->d.layers || max_loads < 0) return MOE_ERR_INVALID;
+    const int S = p->d.slots_per_layer, E = p->d.experts;
+    const bool dry = p->d.dry_run;
+    cudaStream_t cs = static_cast<cudaStream_t>(compute), ps = static_cast<cudaStream_t>(copy);
+    if (!dry) {
+        int rc = order_after_prefetch(p, layer, cs, ps, false);
+        if (rc != MOE_OK) return rc;
+        // the slots may still be read by work enqueued so far on `compute`
+        if (ps != cs) {
+            MOE_CUDA_TRY(cudaEventRecord(p->ev_compute, cs));
+            MOE_CUDA_TRY(cudaStreamWaitEvent(ps, p->ev_compute, 0));
+        }
+    }
+    int32_t* se = &p->slot_expert[size_t(layer) * S];
+    int32_t* es = &p->expert_slot[size_t(layer) * E];
+    int64_t* fq = &p->freq[size_t(layer) * E];
+    uint8_t* fr = &p->fresh[size_t(layer) * E];
+    moe_counters& c = p->ctr[layer];
+    std::vector<int> cand;
+    for (int e = 0; e < E; ++e)
+        if (es[e] < 0 && fq[e] > 0) cand.push_back(e);
+    std::stable_sort(cand.begin(), cand.end(), [&](int a, int b) { return fq[a] > fq[b]; });
+    const std::vector<int32_t> none(size_t(E), 0);
+    std::vector<uint8_t> mine(size_t(E), 0);  // loaded by this call: never victims
+    int n = 0;
+    for (int e : cand) {
+        if (n >= max_loads) break;
+        // plan on a copy of the layer's state, commit after the copy is enqueued
+        LayerState ls;
+        ls.se.assign(se, se + S);
+        ls.es.assign(es, es + E);
+        ls.st.assign(&p->stamp[size_t(layer) * S], &p->stamp[size_t(layer) * S] + S);
+        ls.uses.assign(&p->uses[size_t(layer) * S], &p->uses[size_t(layer) * S] + S);
+        ls.seg.assign(&p->seg[size_t(layer) * S], &p->seg[size_t(layer) * S] + S);
+        ls.clk = p->clock[layer];
+        int s = -1;
+        for (int i = 0; i < S; ++i)
+            if (ls.se[i] < 0) { s = i; break; }
+        int victim = -1;
+        if (s < 0) {
+            s = victim_slot(ls, p->d.policy, S, none.data(), mine.data());
+            if (s < 0) break;
+            victim = ls.se[s];
+            if (fq[victim] >= fq[e]) break;  // only displace experts routed less often
+        }
+        if (p->inject_fail > 0) {
+            --p->inject_fail;
+            ++c.errors;
+            return moe::cuda_fail(cudaErrorUnknown);
+        }
+        if (!dry) {
+            const cudaError_t r = copy_expert(p, layer, e, s, cudaMemcpyHostToDevice, ps, false);
+            if (r != cudaSuccess) {
+                ++c.errors;
+                if (n > 0) {
+                    MOE_CUDA_TRY(cudaEventRecord(p->ev_pf[layer], ps));
+                    p->pending[layer] = 1;
+                }
+                return moe::cuda_fail(r);
+            }
+        }
+        if (victim >= 0) {
+            es[victim] = -1;
+            fr[victim] = 0;
+            ++c.evictions;
+        }
+        se[s] = e;
+        es[e] = s;
+        p->stamp[size_t(layer) * S + s] = ++p->clock[layer];
+        p->uses[size_t(layer) * S + s] = 1;
+        p->seg[size_t(layer) * S + s] = 0;
+        fr[e] = 1;
+        mine[e] = 1;
+        ++c.prefetches;
+        c.h2d_bytes += p->bytes_per_load;
+        ++n;
+    }
+    if (!dry && n > 0) {
+        MOE_CUDA_TRY(cudaEventRecord(p->ev_pf[layer], ps));
+        p->pending[layer] = 1;
+    }
+    if (loaded) *loaded = n;
+    return MOE_OK;
+}
+
 extern "C" int moe_pool_counters(const moe_pool_t* p, int layer, moe_counters* out) {
     if (!p || !out || layer < -1 || layer >= p->d.layers) return MOE_ERR_INVALID;
     if (layer >= 0) {
@@ -476,6 +602,8 @@ extern "C" int moe_pool_counters(const moe_pool_t* p, int layer, moe_counters* o
         s.h2d_bytes += c.h2d_bytes;
         s.errors += c.errors;
         s.events += c.events;
+        s.prefetches += c.prefetches;
+        s.prefetch_hits += c.prefetch_hits;
     }
     *out = s;
     return MOE_OK;
@@ -506,7 +634,7 @@ struct StateHeader {
 size_t state_bytes(const moe_pool_t* p) {
     return sizeof(StateHeader) + p->slot_expert.size() * 4 + p->expert_slot.size() * 4 +
            p->stamp.size() * 8 + p->uses.size() * 8 + p->seg.size() + p->clock.size() * 8 +
-           p->ctr.size() * sizeof(moe_counters);
+           p->ctr.size() * sizeof(moe_counters) + p->freq.size() * 8 + p->fresh.size();
 }
 }  // namespace
 
@@ -531,6 +659,8 @@ extern "C" int moe_pool_save(const moe_pool_t* p, void* buf, size_t bytes) {
     put(p->seg.data(), p->seg.size());
     put(p->clock.data(), p->clock.size() * 8);
     put(p->ctr.data(), p->ctr.size() * sizeof(moe_counters));
+    put(p->freq.data(), p->freq.size() * 8);
+    put(p->fresh.data(), p->fresh.size());
     return MOE_OK;
 }
 
@@ -567,6 +697,8 @@ extern "C" int moe_pool_load(moe_pool_t* p, const void* buf, size_t bytes) {
     get(p->seg.data(), p->seg.size());
     get(p->clock.data(), p->clock.size() * 8);
     get(p->ctr.data(), p->ctr.size() * sizeof(moe_counters));
+    get(p->freq.data(), p->freq.size() * 8);
+    get(p->fresh.data(), p->fresh.size());
     return MOE_OK;
 }
 
@@ -581,6 +713,8 @@ extern "C" void moe_pool_destroy(moe_pool_t* p) {
     if (p->ev_compute) cudaEventDestroy(p->ev_compute);
     if (p->ev_copy) cudaEventDestroy(p->ev_copy);
     for (cudaEvent_t ev : p->ev_win)
+        if (ev) cudaEventDestroy(ev);
+    for (cudaEvent_t ev : p->ev_pf)
         if (ev) cudaEventDestroy(ev);
     if (p->map_pinned) cudaFreeHost(p->map_pinned);
     delete p;

@@ -117,3 +117,56 @@ def test_offload_decode_only_staging():
         with pytest.raises(M.MoeError):
             M.moe_expert_ffn(pool, 0, x, plan, slot_of, out, pws, path=M.MOE_PATH_PREFILL, stream=compute)
     pool.close()
+
+
+def test_offload_decode_with_prefetch():
+    """Next-layer prefetch (moe_pool_prefetch) between each layer's staging
+    and its FFN, on the copy stream: slot maps and all counters (including
+    prefetches and prefetch hits) bit-exact against the oracle's policy
+    simulation, and layer outputs that read prefetched experts match the
+    oracle (the copies are ordered before their first reader)."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    L = 3
+    pool, host, dev = make_pool(M, wl, layers=L, preload=False)
+    pool.close()
+    pool = M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev, policy="lru")
+    ref = [oracle.PolicyPool(wl.slots, wl.experts, "lru") for _ in range(L)]
+    T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
+    plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    checked = 0
+    with torch.cuda.stream(compute):
+        for step in range(14):
+            for layer in range(L):
+                lg = torch.from_numpy(S.logits(wl, layer, step)).cuda()
+                x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step).view(np.int16)).cuda().view(
+                    torch.bfloat16)
+                M.moe_route_plan(lg, k, plan, stream=compute)
+                assert pool.stage(layer, plan.counts_host, slot_of, compute=compute, copy=copy) == M.MOE_OK
+                counts = plan.counts_host.numpy().copy()
+                hits_before = ref[layer].prefetch_hits
+                ref[layer].step(counts)
+                nxt = (layer + 1) % L
+                assert pool.prefetch(nxt, 2, compute=compute, copy=copy) == len(ref[nxt].prefetch(2))
+                assert np.array_equal(pool.slot_map(nxt), ref[nxt].slot_map())
+                M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE, stream=compute)
+                if ref[layer].prefetch_hits > hits_before or step in (0, 13):
+                    compute.synchronize()
+                    r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                    assert rel_l2(out.cpu().numpy(), r) <= DECODE_REL_L2
+                    checked += 1
+    compute.synchronize()
+    for layer in range(L):
+        c, e, pc = pool.counters(layer), ref[layer].counters(), ref[layer].prefetch_counters()
+        assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+        assert (c["prefetches"], c["prefetch_hits"]) == (pc["prefetches"], pc["prefetch_hits"])
+    tot = pool.counters()
+    assert tot["prefetch_hits"] > 0 and checked > 6
+    pool.close()

@@ -182,3 +182,42 @@ def test_staged_prefill_invariants(policy):
         assert seen == routed                         # every routed expert in exactly one window
         assert p.misses - before <= len(routed)       # each routed expert loaded at most once
         assert where == {e: int(s) for e, s in enumerate(p.slot_map()) if s >= 0}
+
+
+def test_prefetch_hand_worked_lru():
+    """Two slots, LRU.  After routing 0, 1, 0, 2 the pool holds {0, 2};
+    prefetching the next candidate (1, routed once) would have to evict 0
+    (routed twice): declined.  After 1 is routed again it holds {1, 2};
+    prefetch then loads 0 (routed twice) over 2 (once), and routing 0 next
+    counts as a prefetch hit."""
+    p = oracle.PolicyPool(2, 5, "lru")
+    for ev in [(0,), (1,), (0,), (2,)]:
+        p.step(_ev(5, *ev))
+    assert p.slot_map().tolist() == [0, -1, 1, -1, -1]
+    assert p.prefetch(1) == []
+    p.step(_ev(5, 1))                     # evicts 0 (routed longest ago)
+    assert p.slot_map().tolist() == [-1, 0, 1, -1, -1]
+    assert p.prefetch(2) == [(0, 1)]      # over 2; experts 3, 4 never routed
+    p.step(_ev(5, 0))
+    assert p.prefetch_counters() == dict(prefetches=1, prefetch_hits=1)
+    assert p.counters() == dict(hits=2, misses=4, evictions=3)
+
+
+@pytest.mark.parametrize("policy", oracle.POLICIES)
+def test_prefetch_invariants(policy):
+    rng = np.random.default_rng(3)
+    S, E = 4, 12
+    p = oracle.PolicyPool(S, E, policy)
+    for _ in range(300):
+        c = np.zeros(E, np.int32)
+        c[rng.choice(E, 2, replace=False, p=np.linspace(2, 1, E) / np.linspace(2, 1, E).sum())] = 1
+        p.step(c)
+        before = dict(p.slot_of)
+        freq = list(p.freq)
+        loads = p.prefetch(int(rng.integers(0, 3)))
+        occupant = {s: e for e, s in before.items()}
+        for e, s in loads:
+            assert e not in before and freq[e] > 0
+            v = occupant.get(s)
+            assert v is None or freq[v] < freq[e]   # never displaces an expert routed as often or more
+        assert p.prefetch_hits <= p.prefetches

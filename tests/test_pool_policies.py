@@ -133,3 +133,33 @@ def test_staged_prefill_arguments():
     with pytest.raises(M.MoeError) as e:
         dec.prefill_staged(0, c, 3, 2, T=2)
     assert e.value.status == M.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("policy", oracle.POLICIES)
+@pytest.mark.parametrize("S,E,k", [(4, 16, 2), (8, 32, 4)])
+def test_dry_run_prefetch_matches_oracle(policy, S, E, k):
+    """moe_pool_prefetch (dry run) between routing events of the next layer,
+    against the oracle: slot maps and all counters bit-exact; a checkpoint
+    taken mid-stream carries the routing frequencies and prefetch flags."""
+    rng = np.random.default_rng(S + E)
+    layers = 3
+    pool = M.Pool(layers, E, S, 256, 512, dry_run=True, policy=policy)
+    ref = [oracle.PolicyPool(S, E, policy) for _ in range(layers)]
+    events = list(_stream(rng, E, k, 300, 1.0))
+    for step, c in enumerate(events):
+        layer = step % layers
+        if step == 150:
+            state = pool.save()
+            pool = M.Pool(layers, E, S, 256, 512, dry_run=True, policy=policy)
+            assert pool.load(state) == M.MOE_OK
+        assert pool.stage(layer, c) == M.MOE_OK
+        ref[layer].step(c)
+        nxt, n = (layer + 1) % layers, int(rng.integers(0, 3))
+        assert pool.prefetch(nxt, n) == len(ref[nxt].prefetch(n))
+        assert np.array_equal(pool.slot_map(nxt), ref[nxt].slot_map())
+    for layer in range(layers):
+        got, exp = pool.counters(layer), ref[layer].counters()
+        assert (got["hits"], got["misses"], got["evictions"]) == (exp["hits"], exp["misses"], exp["evictions"])
+        pc = ref[layer].prefetch_counters()
+        assert (got["prefetches"], got["prefetch_hits"]) == (pc["prefetches"], pc["prefetch_hits"])
+    assert pool.counters()["prefetches"] > 0
