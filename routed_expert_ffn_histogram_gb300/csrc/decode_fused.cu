@@ -53,10 +53,10 @@ constexpr int kThreads = 32 * (kGroup + 1);  // warp 0: copy producer; warps 1..
 static_assert(Layout::kChunk % kGroup == 0, "a group of gate rows stays inside one interleave chunk");
 constexpr int kMaxSlots = 16;
 
-// 2^(e - 127) for an integer biased exponent e (any range), as fp32.
-__device__ __forceinline__ float pow2_biased(int e) {
-    if (e >= 1 && e <= 254) return __int_as_float(e << 23);
-    return ldexpf(1.0f, e - 127);
+// Value of an E8M0 scale byte: 2^(b - 127), byte 255 NaN (OCP MX v1.0).
+__device__ __forceinline__ float e8m0_value_f(int b) {
+    if (b == 255) return __int_as_float(0x7fc00000);
+    return b >= 1 ? __int_as_float(b << 23) : __int_as_float(0x00400000);  // b = 0: 2^-127 (subnormal)
 }
 
 // acc0 += w.lo * x.lo, acc1 += w.hi * x.hi: f16 x f16 products formed
@@ -120,9 +120,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 // two 2^-e (e from the block's largest magnitude, so every value fits f16):
 // x * 2^-e is exact in f16 for all values within 2^-31 of the block maximum
 // (smaller ones round by less than 2^-24 of the block's dot product).
+// The block's factor 2^e is kept as fp32 (e in [-140, 113]: exact).
 // One thread per block.
 __device__ __forceinline__ void stage_block_f16(const uint16_t* __restrict__ src, uint4* dst, int b,
-                                                int* exps) {
+                                                float* factors) {
     const uint4* s4 = reinterpret_cast<const uint4*>(src) + b * 4;
     uint4 v[4];
     float amax = 0.f;
@@ -152,7 +153,7 @@ __device__ __forceinline__ void stage_block_f16(const uint16_t* __restrict__ src
         }
         dst[hswz(b, q)] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    exps[b] = e;
+    factors[b] = ldexpf(1.0f, e);
 }
 
 struct FusedParams {
@@ -208,6 +209,9 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
+// E8M0 byte -> fp32 value, one entry per byte, filled by each CTA at start:
+// a block's scale is then one shared-memory load and one multiply by the
+// power of two that staged its activations.
 __device__ __forceinline__ void named_bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
 }
@@ -226,12 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
     __shared__ AssignTable tab;
     __shared__ __align__(8) uint64_t full[kMaxSlots];
     __shared__ __align__(8) uint64_t empty[kMaxSlots];
-    __shared__ float hval[2][kGroup];
+    __shared__ __align__(16) float hval[2][kGroup];
+    __shared__ float e8m0_lut[256];
     __shared__ int last_cta;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x;
     const int A = p.T * p.k;
     volatile uint32_t* err = p.ctl + 2;
+    for (int i = threadIdx.x; i < 256; i += kThreads) e8m0_lut[i] = e8m0_value_f(i);
     if (p.logits != nullptr) {
         // routing in every CTA: warp 0 ranks each token's logits while the
         // other warps fetch the slot map
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
     } else {
         // ---- consumers (warps 1..16) ----
         uint4* xs = reinterpret_cast<uint4*>(smem);
-        int* xe = reinterpret_cast<int*>(smem + (size_t)p.T * nbx * 64);
+        float* xe = reinterpret_cast<float*>(smem + (size_t)p.T * nbx * 64);
         for (int c = threadIdx.x - 32; c < p.T * nbx; c += kConsumers) {
             const int t = c / nbx, b = c - t * nbx;
             stage_block_f16(p.x + (size_t)t * p.H, xs + (size_t)t * nbx * 4, b, xe + t * nbx);
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 const uint8_t* u = g + kGroup * row_bytes;
                 const int t = a / p.k;
                 const uint4* xt = xs + (size_t)t * nbx * 4;
-                const int* et = xe + t * nbx;
+                const float* et = xe + t * nbx;
                 float ag = 0.0f, au = 0.0f;
 #pragma unroll
                 for (int i = 0; i < NG; ++i) {
@@ -393,11 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                     if (b < nbx) {
                         const uint4 cg = *reinterpret_cast<const uint4*>(g + 16 * b);
                         const uint4 cu = *reinterpret_cast<const uint4*>(u + 16 * b);
-                        const int e = et[b];
+                        const float xf = et[b];
                         float dg, du;
                         block_dot2_f16(cg, cu, xt, b, dg, du);
-                        ag = fmaf(dg, pow2_biased(int(g[p.H / 2 + b]) + e), ag);
-                        au = fmaf(du, pow2_biased(int(u[p.H / 2 + b]) + e), au);
+                        ag = fmaf(dg, e8m0_lut[g[p.H / 2 + b]] * xf, ag);
+                        au = fmaf(du, e8m0_lut[u[p.H / 2 + b]] * xf, au);
                     }
                 }
                 ag = warp_sum(ag);
@@ -417,13 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 float hv[kGroup];
                 float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < kGroup; ++i) {
-                    hv[i] = hval[n & 1][i];
-                    amax = fmaxf(amax, fabsf(hv[i]));
+                for (int i = 0; i < kGroup / 4; ++i) {
+                    const float4 v4 = reinterpret_cast<const float4*>(hval[n & 1])[i];
+                    hv[4 * i] = v4.x;
+                    hv[4 * i + 1] = v4.y;
+                    hv[4 * i + 2] = v4.z;
+                    hv[4 * i + 3] = v4.w;
                 }
+#pragma unroll
+                for (int i = 0; i < kGroup; ++i) amax = fmaxf(amax, fabsf(hv[i]));
                 const int ef = int((__float_as_uint(amax) >> 23) & 0xffu);
                 const int e = (amax == 0.f) ? 0 : (ef == 0 ? -126 - 14 : ef - 127 - 14);
                 const float mul = ldexpf(1.0f, -e);
+                const float hf = ldexpf(1.0f, e);
                 uint32_t h2[kGroup / 2];
 #pragma unroll
                 for (int i = 0; i < kGroup / 2; ++i) {
@@ -449,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                         fma2_f16_f32(s2, s3, w1[1], h2[5]);
                         fma2_f16_f32(s0, s1, w1[2], h2[6]);
                         fma2_f16_f32(s2, s3, w1[3], h2[7]);
-                        y[m] = fmaf((s0 + s1) + (s2 + s3), pow2_biased(int(scales[nn]) + e), y[m]);
+                        y[m] = fmaf((s0 + s1) + (s2 + s3), e8m0_lut[scales[nn]] * hf, y[m]);
                     }
                 }
             } else {
