@@ -74,6 +74,9 @@ extern "C" {
 #define MOE_PATH_DECODE 1        /* bf16 activations, CUDA-core GEMV         */
 #define MOE_PATH_PREFILL 2       /* MXFP8 activations, tcgen05 grouped GEMM  */
 #define MOE_DECODE_MAX_ASSIGN 64
+/* OR-ed into moe_expert_ffn's path: out is added to (out += the layer's
+ * output, as a residual stream takes it) instead of overwritten. */
+#define MOE_FFN_ACCUMULATE 0x100
 
 typedef void* moe_stream_t;
 
@@ -381,13 +384,17 @@ MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int pat
  *             2^(floor(log2 amax) - 8), RNE, satfinite) and multiplied on
  *             tcgen05 block-scaled tensor cores, fp32 accumulation.
  *             MOE_PATH_AUTO: decode when T*k <= MOE_DECODE_MAX_ASSIGN.
+ *             With MOE_FFN_ACCUMULATE or-ed in, out += the result; the
+ *             decode path then needs no completion pass and prefill no
+ *             zeroing of out.
  *   workspace device, >= moe_ffn_workspace_bytes(), 256-byte aligned.
  *             On the decode path it holds a completion counter and an fp32
  *             [T][H] accumulator that must be zero when the workspace is
  *             first used (allocate it zero-filled); the library leaves them
  *             zero after every call.  One workspace must not be used by two
  *             calls that can run at the same time.
- *   out       device fp32 [T][H], 16-byte aligned, fully overwritten
+ *   out       device fp32 [T][H], 16-byte aligned, fully overwritten (added
+ *             to with MOE_FFN_ACCUMULATE)
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 MOE_API int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_bf16, int T, int k,
                    const int32_t* ids, const float* w, const int32_t* offsets,
@@ -415,6 +422,15 @@ MOE_API int moe_decode_layer(const moe_pool_t* pool, int layer, const float* log
                              int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                              const int32_t* slot_of, void* workspace, size_t ws_bytes,
                              float* out, moe_stream_t stream);
+
+/* moe_decode_layer with out += the layer's output (a residual stream)
+ * instead of out = ...: the CTAs add their partial sums into out directly,
+ * so the launch has no completion pass.  Same arguments and errors. */
+MOE_API int moe_decode_layer_acc(const moe_pool_t* pool, int layer, const float* logits,
+                                 const void* x_bf16, int T, int k, int32_t* ids, float* w,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                 const int32_t* slot_of, void* workspace, size_t ws_bytes,
+                                 float* out, moe_stream_t stream);
 
 /* Weighted combine of per-assignment expert outputs held in grouped order:
  *   out[t][h] = sum_j w[t][j] * y_perm[inv[t*k+j]][h], j ascending, fp32.

@@ -19,7 +19,7 @@ import ctypes as C
 from dataclasses import dataclass
 
 from . import _lib
-from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_INVALID, MOE_ERR_STATE,
+from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_FFN_ACCUMULATE, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_INVALID, MOE_ERR_STATE,
                    MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_OK,
                    MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_POLICY_FIFO, MOE_POLICY_LFRU,
                    MOE_POLICY_LFU, MOE_POLICY_LRU, MOE_POLICY_SLRU, MOE_STAGE_DECODE,
@@ -125,9 +125,13 @@ def alloc_ffn_workspace(T: int, k: int, hidden: int, inter: int, path: int = MOE
 
 
 def moe_expert_ffn(pool: "Pool", layer: int, x_bf16, plan: RoutePlan, slot_of, out, workspace,
-                   path: int = MOE_PATH_AUTO, stream=None) -> None:
-    """Routed experts of one layer with the weighted combine (moe_expert_ffn)."""
+                   path: int = MOE_PATH_AUTO, stream=None, accumulate: bool = False) -> None:
+    """Routed experts of one layer with the weighted combine (moe_expert_ffn);
+    ``accumulate`` adds into ``out`` (a residual stream) instead of
+    overwriting it."""
     T = x_bf16.shape[0]
+    if accumulate:
+        path |= MOE_FFN_ACCUMULATE
     check("moe_expert_ffn", lib().moe_expert_ffn(
         pool.handle, layer, ptr(x_bf16), T, plan.k, ptr(plan.ids), ptr(plan.w), ptr(plan.offsets),
         ptr(plan.perm), ptr(plan.inv), ptr(slot_of), path, ptr(workspace),
@@ -136,11 +140,13 @@ def moe_expert_ffn(pool: "Pool", layer: int, x_bf16, plan: RoutePlan, slot_of, o
 
 
 def moe_decode_layer(pool: "Pool", layer: int, logits, x_bf16, plan: RoutePlan, slot_of, out, workspace,
-                     stream=None) -> None:
+                     stream=None, accumulate: bool = False) -> None:
     """Routing + routed experts of one decode step in one launch
-    (moe_decode_layer); fills ``plan`` like moe_route_plan."""
+    (moe_decode_layer); fills ``plan`` like moe_route_plan.  ``accumulate``
+    adds into ``out`` (moe_decode_layer_acc) instead of overwriting it."""
     T = x_bf16.shape[0]
-    check("moe_decode_layer", lib().moe_decode_layer(
+    fn = lib().moe_decode_layer_acc if accumulate else lib().moe_decode_layer
+    check("moe_decode_layer", fn(
         pool.handle, layer, ptr(logits), ptr(x_bf16), T, plan.k, ptr(plan.ids), ptr(plan.w), ptr(plan.counts),
         ptr(plan.offsets), ptr(plan.perm), ptr(plan.inv), ptr(slot_of), ptr(workspace),
         workspace.numel() * workspace.element_size(), ptr(out), stream_handle(stream)))

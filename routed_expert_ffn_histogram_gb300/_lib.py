@@ -27,6 +27,7 @@ MOE_PATH_AUTO = 0
 MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
 MOE_DECODE_MAX_ASSIGN = 64
+MOE_FFN_ACCUMULATE = 0x100
 MOE_POLICY_LRU, MOE_POLICY_FIFO, MOE_POLICY_LFU, MOE_POLICY_LFRU, MOE_POLICY_SLRU = 0, 1, 2, 3, 4
 POLICIES = {"lru": 0, "fifo": 1, "lfu": 2, "lfru": 3, "slru": 4}
 MOE_STAGE_WHOLE, MOE_STAGE_DECODE = 0, 1
@@ -79,6 +80,8 @@ SIGNATURES = {
                               _vp]),
     "moe_decode_layer": (_i32, [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
                                 _vp]),
+    "moe_decode_layer_acc": (_i32, [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                    _vp, _vp]),
     "moe_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "moe_quant_mxfp8": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _vp]),
 }

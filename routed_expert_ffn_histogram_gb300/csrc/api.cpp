@@ -154,6 +154,8 @@ extern "C" int moe_route_plan_noalloc(const float* logits, int T, int E, int k, 
 }
 
 static int resolve_path(int path, int T, int k) {
+    if (path & ~(MOE_FFN_ACCUMULATE | 3)) return -1;
+    path &= ~MOE_FFN_ACCUMULATE;
     if (path == MOE_PATH_AUTO) return size_t(T) * k <= MOE_DECODE_MAX_ASSIGN ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
     return path;
 }
@@ -178,6 +180,7 @@ extern "C" int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_b
     if (d.dry_run || !d.dev_slots) return MOE_ERR_STATE;
     if (layer < 0 || layer >= d.layers || T < 0 || k < 1 || k > d.experts || k > MOE_MAX_TOPK)
         return MOE_ERR_INVALID;
+    const bool accumulate = (path & MOE_FFN_ACCUMULATE) != 0;
     path = resolve_path(path, T, k);
     if (path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL) return MOE_ERR_INVALID;
     size_t need = 0;
@@ -204,6 +207,7 @@ extern "C" int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_b
     a.inv = inv;
     a.slot_of = slot_of;
     a.out = out;
+    a.accumulate = accumulate;
     a.decode_parts_only = d.stage_parts == MOE_STAGE_DECODE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (path == MOE_PATH_DECODE) return moe::launch_decode_ffn(a, workspace, ws_bytes, s);
@@ -211,10 +215,10 @@ extern "C" int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_b
     return moe::launch_prefill_ffn(a, workspace, ws_bytes, s);
 }
 
-extern "C" int moe_decode_layer(const moe_pool_t* pool, int layer, const float* logits, const void* x_bf16, int T,
-                                int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
-                                int32_t* inv, const int32_t* slot_of, void* workspace, size_t ws_bytes, float* out,
-                                moe_stream_t stream) {
+static int decode_layer(const moe_pool_t* pool, int layer, const float* logits, const void* x_bf16, int T, int k,
+                        int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                        const int32_t* slot_of, void* workspace, size_t ws_bytes, float* out, moe_stream_t stream,
+                        bool accumulate) {
     if (!pool) return MOE_ERR_INVALID;
     const moe_pool_desc& d = *moe::pool_desc(pool);
     const Layout& L = *moe::pool_layout(pool);
@@ -243,6 +247,7 @@ extern "C" int moe_decode_layer(const moe_pool_t* pool, int layer, const float* 
     a.inv = inv;
     a.slot_of = slot_of;
     a.out = out;
+    a.accumulate = accumulate;
     moe::RouteOut ro;
     ro.logits = logits;
     ro.ids = ids;
@@ -252,6 +257,22 @@ extern "C" int moe_decode_layer(const moe_pool_t* pool, int layer, const float* 
     ro.perm = perm;
     ro.inv = inv;
     return moe::launch_decode_layer(a, ro, workspace, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_decode_layer(const moe_pool_t* pool, int layer, const float* logits, const void* x_bf16, int T,
+                                int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                int32_t* inv, const int32_t* slot_of, void* workspace, size_t ws_bytes, float* out,
+                                moe_stream_t stream) {
+    return decode_layer(pool, layer, logits, x_bf16, T, k, ids, w, counts, offsets, perm, inv, slot_of, workspace,
+                        ws_bytes, out, stream, false);
+}
+
+extern "C" int moe_decode_layer_acc(const moe_pool_t* pool, int layer, const float* logits, const void* x_bf16,
+                                    int T, int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                    int32_t* perm, int32_t* inv, const int32_t* slot_of, void* workspace,
+                                    size_t ws_bytes, float* out, moe_stream_t stream) {
+    return decode_layer(pool, layer, logits, x_bf16, T, k, ids, w, counts, offsets, perm, inv, slot_of, workspace,
+                        ws_bytes, out, stream, true);
 }
 
 extern "C" int moe_combine(const float* y_perm, const float* w, const int32_t* inv, int T, int k, int H,

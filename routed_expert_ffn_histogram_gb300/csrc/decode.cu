@@ -112,6 +112,7 @@ struct DecodeParams {
     const int32_t* slot_of;
     uint16_t* h;      // bf16 [T*k][I]
     float* out;       // fp32 [T][H]
+    int accumulate;   // out += result
 };
 
 __device__ __forceinline__ const uint8_t* expert_base(const DecodeParams& p, int a) {
@@ -247,7 +248,11 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(DecodeParams p) {
                 out = __fadd_rn(out, __fmul_rn(p.w[t * p.k + j], y));
             }
         }
-        if (lane == 0) p.out[(size_t)t * p.H + r] = bad ? __int_as_float(0x7fc00000) : out;
+        if (lane == 0) {
+            float* o = p.out + (size_t)t * p.H + r;
+            const float v = bad ? __int_as_float(0x7fc00000) : out;
+            *o = p.accumulate ? __fadd_rn(*o, v) : v;
+        }
     }
 }
 
@@ -353,6 +358,7 @@ int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t 
     p.slot_of = a.slot_of;
     p.h = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + 256);
     p.out = a.out;
+    p.accumulate = a.accumulate ? 1 : 0;
     const int nit_gu = (L.H / 32 + 31) / 32;
     int rc;
     switch (nit_gu) {

@@ -169,6 +169,7 @@ struct FusedParams {
     float* acc;        // fp32 [T][H] accumulator, all zero between calls
     float* out;        // fp32 [T][H]
     unsigned* ctl;     // [0] CTAs finished (zero between calls), [2] error bits
+    int accumulate;    // out += result: partial sums go to out, no completion pass
     // fused routing (logits != nullptr): the kernel selects the experts itself
     // and CTA 0 writes the routing outputs below
     const float* logits;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
         auto flush = [&](int a) {
             if (a < 0) return;
             const float wa = tab.w[a];
-            float* dst = p.acc + (size_t)(a / p.k) * p.H;
+            float* dst = (p.accumulate ? p.out : p.acc) + (size_t)(a / p.k) * p.H;
 #pragma unroll
             for (int m = 0; m < NN; ++m) {
                 const int n = ct + kConsumers * m;
@@ -475,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
     }
 
     // ---- completion: the last CTA to finish moves the sums to `out` ----
+    if (p.accumulate) return;  // the partial sums went to out directly
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -547,6 +549,7 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     p.h = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + 256);
     p.acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_acc_offset(a.T, a.k, L.I));
     p.out = a.out;
+    p.accumulate = a.accumulate ? 1 : 0;
     p.logits = ro ? ro->logits : nullptr;
     p.r_ids = ro ? ro->ids : nullptr;
     p.r_w = ro ? ro->w : nullptr;

@@ -105,6 +105,7 @@ struct FfnArgs {
     const int32_t* inv;
     const int32_t* slot_of;
     float* out;
+    bool accumulate = false;   // out += result instead of out = result
 };
 
 struct RouteOut {

@@ -655,7 +655,7 @@ int launch_prefill_prepare(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStre
     MOE_CUDA_TRY(cudaMemsetAsync(base + w.err, 0, 4, s));
     MOE_CUDA_TRY(cudaMemsetAsync(base + w.xs, 0, size_t(A) * w.xs_stride, s));
     MOE_CUDA_TRY(cudaMemsetAsync(base + w.hs, 0, size_t(A) * w.hs_stride, s));
-    MOE_CUDA_TRY(cudaMemsetAsync(a.out, 0, size_t(a.T) * L.H * sizeof(float), s));
+    if (!a.accumulate) MOE_CUDA_TRY(cudaMemsetAsync(a.out, 0, size_t(a.T) * L.H * sizeof(float), s));
     return launch_quant_mxfp8_scatter(a.x, L.H, a.inv, a.k, a.T, base + w.xq, base + w.xs, w.xs_stride, s);
 }
 

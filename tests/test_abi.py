@@ -95,6 +95,12 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.moe_combine(None, None, None, 2, 0, 8, None, None) == M.MOE_ERR_INVALID
     assert L.moe_quant_mxfp8(None, 33, None, 1, 1, None, None, 2, None) == M.MOE_ERR_INVALID
     assert L.moe_ffn_workspace_bytes(4, 2, 250, 512, 0, C.byref(sz)) == M.MOE_ERR_INVALID
+    # the accumulate flag is the only bit allowed beside the path; it does not change the size
+    assert L.moe_ffn_workspace_bytes(4, 2, 256, 512, 0x200, C.byref(sz)) == M.MOE_ERR_INVALID
+    assert L.moe_ffn_workspace_bytes(4, 2, 256, 512, M.MOE_PATH_DECODE, C.byref(sz)) == M.MOE_OK
+    plain = sz.value
+    assert L.moe_ffn_workspace_bytes(4, 2, 256, 512, M.MOE_PATH_DECODE | M.MOE_FFN_ACCUMULATE, C.byref(sz)) == M.MOE_OK
+    assert sz.value == plain
     assert L.moe_expert_ffn(None, 0, None, 1, 1, None, None, None, None, None, None, 0, None, 0, None, None) == \
         M.MOE_ERR_INVALID
     d = _lib.MoePoolDesc(1, 8, 9, 256, 512, None, None, 0, 1)

@@ -165,3 +165,65 @@ def test_decode_layer_fused_equals_two_calls(wid, T):
     remap = {e: i for i, e in enumerate(uniq)}
     ref = oracle.layer(x_np, np.vectorize(remap.get)(ids).astype(np.int32), w, ws, prefill=False, threads=16)
     assert rel_l2(out_a.cpu().numpy(), ref) <= DECODE_REL_L2
+
+
+def _oracle_T(wl, lg, xbits, prefill):
+    ids, w = oracle.route(lg, wl.top_k)
+    uniq = sorted(set(ids.reshape(-1).tolist()))
+    ws = S.stack_experts(S.layer_weights(wl, 0, uniq))
+    remap = {e: i for i, e in enumerate(uniq)}
+    ids_r = np.vectorize(remap.get)(ids).astype(np.int32)
+    return oracle.layer(xbits, ids_r, w, ws, prefill=prefill, threads=16, want_intermediates=True)[0]
+
+
+@pytest.mark.parametrize("case", ["fused", "two_kernel", "layer_acc", "prefill"])
+def test_accumulate_into_residual(case):
+    """MOE_FFN_ACCUMULATE / moe_decode_layer_acc: out holds a residual r
+    before the call and r + the layer afterwards -- the fused decode kernel
+    (partial sums straight into out, no completion pass), the two-kernel
+    decode path (16 GPT-OSS-shaped tokens exceed the fused kernel's shared
+    memory), the one-launch decode layer, and prefill (no zeroing of out).
+    The layer part is checked against the oracle and against the overwrite
+    mode on the same inputs."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[1 if case == "two_kernel" else 0]
+    T = 16
+    pool, host, dev = make_pool(M, wl, layers=1)
+    lg = S.logits(wl, 0, 0, T)
+    xb = S.activations_bf16_bits(wl, 0, 0, T)
+    ref = _oracle_T(wl, lg, xb, prefill=(case == "prefill"))
+    rng = np.random.default_rng(9)
+    r = (rng.standard_normal(ref.shape) * np.sqrt(np.mean(ref ** 2))).astype(np.float32)
+    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    lgt = torch.from_numpy(lg).cuda()
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    slot_of = torch.from_numpy(pool_slot_map(pool, 0)).cuda()
+    path = M.MOE_PATH_PREFILL if case == "prefill" else M.MOE_PATH_DECODE
+    plan = M.RoutePlan.allocate(T, E, k)
+    ws = M.alloc_ffn_workspace(T, k, H, I, path)
+    acc = torch.from_numpy(r).cuda()
+    ovr = torch.empty_like(acc)
+    if case == "layer_acc":
+        M.moe_decode_layer(pool, 0, lgt, x, plan, slot_of, acc, ws, accumulate=True)
+        M.moe_decode_layer(pool, 0, lgt, x, plan, slot_of, ovr, ws)
+    else:
+        M.moe_route_plan(lgt, k, plan, with_counts_host=False)
+        M.moe_expert_ffn(pool, 0, x, plan, slot_of, acc, ws, path=path, accumulate=True)
+        M.moe_expert_ffn(pool, 0, x, plan, slot_of, ovr, ws, path=path)
+    torch.cuda.synchronize()
+    got = acc.cpu().numpy().astype(np.float64) - r
+    tol = 2e-3 if case == "prefill" else DECODE_REL_L2
+    assert rel_l2(got, ref) <= tol
+    assert rel_l2(got, ovr.cpu().numpy()) <= 1e-6
+    if case != "prefill":
+        # the workspace invariant of the overwrite mode still holds afterwards
+        acc2 = torch.from_numpy(r).cuda()
+        if case == "layer_acc":
+            M.moe_decode_layer(pool, 0, lgt, x, plan, slot_of, acc2, ws, accumulate=True)
+        else:
+            M.moe_expert_ffn(pool, 0, x, plan, slot_of, acc2, ws, path=path, accumulate=True)
+        torch.cuda.synchronize()
+        assert rel_l2(acc2.cpu().numpy().astype(np.float64) - r, ref) <= tol
