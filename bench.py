@@ -193,7 +193,10 @@ def gpu_leg(args, wl, rank, world):
                                      for s in step_ids]).view(np.int16)).view(torch.bfloat16)
     lg_d = lg_h.to(dev)
     x_d = x_h.to(dev)
-    out_d = torch.empty((G, L, 1, H), dtype=torch.float32, device=dev)
+    residual = args.output == "residual"
+    # overwrite: one output per (step, layer); residual: every layer of a
+    # step adds into that step's residual-stream row (moe_decode_layer_acc)
+    out_d = torch.zeros((G, 1 if residual else L, 1, H), dtype=torch.float32, device=dev)
     plan = M.RoutePlan.allocate(1, E, k, device=dev)
     ws = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
 
@@ -203,7 +206,8 @@ def gpu_leg(args, wl, rank, world):
         # one launch per layer: routing (top-k, softmax, histogram,
         # permutation), slot lookup, gate/up + SwiGLU, down + combine
         for l in range(L):
-            M.moe_decode_layer(pool, l, lg_d[g, l], x_d[g, l], plan, slot_of, out_d[g, l], ws, stream=stream)
+            M.moe_decode_layer(pool, l, lg_d[g, l], x_d[g, l], plan, slot_of, out_d[g, 0 if residual else l], ws,
+                               stream=stream, accumulate=residual)
 
     # one CUDA graph per step (each step has its own inputs)
     graphs = []
@@ -211,6 +215,7 @@ def gpu_leg(args, wl, rank, world):
     with torch.cuda.stream(stream):
         step(0)  # eager once before capture
     stream.synchronize()
+    out_d.zero_()  # every graph below runs once: a residual row starts at zero
     for g in range(G):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
@@ -251,16 +256,21 @@ def gpu_leg(args, wl, rank, world):
     # e2e through the public API, host buffers, copies inside the timed region
     lg_pin = lg_h.pin_memory()
     x_pin = x_h.pin_memory()
-    out_pin = torch.empty((G, L, 1, H), dtype=torch.float32).pin_memory()
+    n_out = 1 if residual else L
+    out_pin = torch.empty((G, n_out, 1, H), dtype=torch.float32).pin_memory()
+    res_in = torch.zeros((n_out, 1, H), dtype=torch.float32).pin_memory()  # the residual row as it arrives
     lg_stage = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
     x_stage = torch.empty((L, 1, H), dtype=torch.bfloat16, device=dev)
-    out_stage = torch.empty((L, 1, H), dtype=torch.float32, device=dev)
+    out_stage = torch.empty((n_out, 1, H), dtype=torch.float32, device=dev)
 
     def e2e_step(g):
         lg_stage.copy_(lg_pin[g], non_blocking=True)
         x_stage.copy_(x_pin[g], non_blocking=True)
+        if residual:
+            out_stage.copy_(res_in, non_blocking=True)
         for l in range(L):
-            M.moe_decode_layer(pool, l, lg_stage[l], x_stage[l], plan, slot_of, out_stage[l], ws, stream=stream)
+            M.moe_decode_layer(pool, l, lg_stage[l], x_stage[l], plan, slot_of, out_stage[0 if residual else l], ws,
+                               stream=stream, accumulate=residual)
         out_pin[g].copy_(out_stage, non_blocking=True)
         stream.synchronize()
 
@@ -284,7 +294,8 @@ def gpu_leg(args, wl, rank, world):
     same = rel <= 1e-6
 
     res = dict(elapsed_ms=elapsed_ms, ffn_ms=ffn_ms, route_ms=route_ms, clocks=clk, e2e_ms=e2e_ms,
-               h2d=(lg_pin[0].numel() * 4 + x_pin[0].numel() * 2), d2h=out_pin[0].numel() * 4,
+               h2d=(lg_pin[0].numel() * 4 + x_pin[0].numel() * 2 + (res_in.numel() * 4 if residual else 0)),
+               d2h=out_pin[0].numel() * 4,
                e2e_matches_graph=same, expert_bytes=eb)
     pool.close()
     return res
@@ -617,6 +628,9 @@ def main():
                     help="eviction policy of the offload pool (--workload 2)")
     ap.add_argument("--stage-parts", default="whole", choices=["whole", "decode"],
                     help="--workload 2: copy whole experts, or only what the decode kernel reads")
+    ap.add_argument("--output", default="residual", choices=["residual", "overwrite"],
+                    help="decode: each layer adds into the step's residual row (moe_decode_layer_acc) or "
+                         "overwrites its own output (moe_decode_layer)")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="workload 2: after each layer's staging, prefetch up to this many experts of the next layer")
     ap.add_argument("--prefill-slots", type=int, default=None,
@@ -683,6 +697,8 @@ def main():
                 "experts": wl.experts, "top_k": wl.top_k, "tokens_per_step": 1,
                 "resident_experts": wl.layers * wl.experts,
                 "l2": "inputs larger than L2: each step reads 96 distinct experts (1.27 GB) of a 10.2 GB set",
+                "output": ("each layer adds into the step's residual row (moe_decode_layer_acc)"
+                           if args.output == "residual" else "each layer overwrites its own output (moe_decode_layer)"),
                 "parallelism": f"replicas{world}"}
     threads = os.cpu_count() or 1
     if args.impl == "reference":
