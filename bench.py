@@ -582,7 +582,8 @@ def prefill_leg(args, wl):
         e0.record(stream)
         M.moe_route_plan(lg[g], k, plans[g], stream=stream, with_counts_host=False)
         e1.record(stream)
-        M.moe_expert_ffn(pool, 0, xb[g], plans[g], slot_of, out, ws, path=M.MOE_PATH_PREFILL, stream=stream)
+        M.moe_expert_ffn(pool, 0, xb[g], plans[g], slot_of, out, ws, path=M.MOE_PATH_PREFILL, stream=stream,
+                         accumulate=args.output == "residual")
         e2.record(stream)
 
     with torch.cuda.stream(stream):
@@ -675,7 +676,9 @@ def main():
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxf8f6f4->f32",
                 "data": "synthetic",
                 "config": {"workload": wl.name, "hidden": wl.hidden, "inter": wl.inter, "experts": wl.experts,
-                           "top_k": wl.top_k, "tokens": wl.tokens, "l2": "256 MB flush before every step"},
+                           "top_k": wl.top_k, "tokens": wl.tokens, "l2": "256 MB flush before every step",
+                           "output": ("added into a residual stream (MOE_FFN_ACCUMULATE)" if args.output == "residual"
+                                      else "overwritten (out zeroed, then the combine adds into it)")},
                 "roofline": {"kernel": "prefill expert FFN (MXFP8 quant, gate/up GEMM, down GEMM with the combine in its epilogue)",
                              "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                              "frac": achieved / tc_peak, "peak_kind": peak_kind + " bf16 x 2 (FP8-class rate)",
