@@ -25,6 +25,23 @@
 //         if it overflows, goes back to probation with a fresh stamp.
 //         victim: oldest probationary, else oldest protected.
 // A loaded expert gets a fresh stamp, count 1, probation.
+//
+// Prefill through a pool smaller than the routed set (moe_prefill_staged):
+// tinyserve README, "How it works" item 6 (batched prefill groups tokens by
+// expert and loads each unique expert once).  The unique experts are cut
+// into windows of at most S/2; each window is one event as above whose
+// victims also exclude the previous window (its GEMMs may still read it);
+// copies wait on the device for the GEMMs of the window before that.
+//
+// Next-layer prefetch (moe_pool_prefetch): tinyserve README, "How it works"
+// item 4 (FATE: current-layer activations predict the next layer's experts,
+// H2D overlapped with compute).  This path has no router weights, so the
+// layer's own routing history ranks the candidates: the most often routed
+// non-resident experts, each displacing only an expert routed less often.
+// The Expert Offloading topic page (WiSP abstract) reports that speculative
+// transfers compete with demand transfers when the link is the bottleneck;
+// the same holds on GB300 for single-token decode (an expert copy outlasts
+// a layer's FFN), so the call is a building block, off by default.
 #include <algorithm>
 #include <chrono>
 #include <cstdint>
