@@ -238,7 +238,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
     const int G = gridDim.x;
     const int A = p.T * p.k;
     volatile uint32_t* err = p.ctl + 2;
+    // Prologue that touches no global memory, then the programmatic launch
+    // hand-off: the next kernel in the stream may launch now (its CTAs take
+    // SMs as ours exit and run their own prologue), and nothing below reads
+    // an input or writes an output before the previous kernel has finished.
     for (int i = threadIdx.x; i < 256; i += kThreads) e8m0_lut[i] = e8m0_value_f(i);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < slots; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], kGroup);
+        }
+        tc::fence_barrier_init();
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (p.logits != nullptr) {
         // routing in every CTA: warp 0 ranks each token's logits while the
         // other warps fetch the slot map
@@ -270,13 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
             tab.base[a] = expert_of(p, a);
             tab.w[a] = p.w[a];
         }
-    }
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < slots; ++i) {
-            tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], kGroup);
-        }
-        tc::fence_barrier_init();
     }
     __syncthreads();
 
@@ -583,7 +589,20 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
         MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFusedSmemBudget)));
         attr_set[vi].mark(di.device);
     }
-    kern<<<di.sms, kThreads, smem, s>>>(p, slots, int(st));
+    // programmatic stream serialisation: the kernel may launch while the
+    // previous kernel in the stream finishes; it waits for it (griddepcontrol)
+    // before touching global memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(di.sms));
+    cfg.blockDim = dim3(unsigned(kThreads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p, slots, int(st)));
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
