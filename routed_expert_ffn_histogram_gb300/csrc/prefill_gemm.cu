@@ -223,6 +223,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
     const int wg = warp >> 2;
     volatile uint32_t* err = p.err;
 
+    // Programmatic launch hand-off: the next kernel may launch now (its CTAs
+    // take SMs as ours exit); this grid reads and writes nothing in global
+    // memory before the previous kernel in the stream has finished.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // ---- set-up: tile prefix over experts, barriers, tensor memory ----
     // The offsets and the slot map are copied to shared memory once, so a
     // tile start costs no global-memory round trip in any role.
@@ -613,7 +619,19 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& 
         attr_set.mark(di.device);
     }
     const int grid = max(1, min(di.sms, max_tiles));
-    grouped_gemm_tc_kernel<<<grid, kThreads, smem_bytes(), s>>>(ma, mb, p);
+    // programmatic stream serialisation (the kernel waits for its
+    // predecessor with griddepcontrol before touching global memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(unsigned(kThreads));
+    cfg.dynamicSmemBytes = smem_bytes();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel, ma, mb, p));
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
