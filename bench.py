@@ -42,9 +42,9 @@ METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 roo
 NCU_TRAFFIC = {
     # one decode layer (2-layer decode capture; traffic per launch does not
     # depend on the number of layers)
-    "decode_fused_kernel": None,
+    "decode_fused_kernel": 54_183_424 + 110_848,
     # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
-    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": None,
+    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_090_880 + 30_390_016) + (232_850_176 + 29_782_016),
 }
 
 def _peaks():
