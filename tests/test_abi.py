@@ -103,6 +103,9 @@ def test_invalid_arguments_rejected_before_launch():
     assert sz.value == plain
     assert L.moe_expert_ffn(None, 0, None, 1, 1, None, None, None, None, None, None, 0, None, 0, None, None) == \
         M.MOE_ERR_INVALID
+    assert L.moe_decode_layer_acc(None, 0, None, None, 1, 1, None, None, None, None, None, None, None, None, 0,
+                                  None, None) == M.MOE_ERR_INVALID
+    assert L.moe_pool_prefetch(None, 0, 1, None, None, None) == M.MOE_ERR_INVALID
     d = _lib.MoePoolDesc(1, 8, 9, 256, 512, None, None, 0, 1)
     h = C.c_void_p()
     assert L.moe_pool_create(C.byref(d), C.byref(h)) == M.MOE_ERR_INVALID  # S > E

@@ -163,3 +163,36 @@ def test_dry_run_prefetch_matches_oracle(policy, S, E, k):
         pc = ref[layer].prefetch_counters()
         assert (got["prefetches"], got["prefetch_hits"]) == (pc["prefetches"], pc["prefetch_hits"])
     assert pool.counters()["prefetches"] > 0
+
+
+def test_prefetch_arguments_and_no_op():
+    pool = M.Pool(2, 8, 4, 256, 512, dry_run=True)
+    with pytest.raises(M.MoeError) as e:
+        pool.prefetch(2, 1)                       # layer out of range
+    assert e.value.status == M.MOE_ERR_INVALID
+    with pytest.raises(M.MoeError) as e:
+        pool.prefetch(0, -1)
+    assert e.value.status == M.MOE_ERR_INVALID
+    assert pool.prefetch(0, 3) == 0               # nothing routed yet: no candidates
+    c = np.zeros(8, np.int32)
+    c[[1, 2]] = 1
+    assert pool.stage(0, c) == M.MOE_OK
+    before = pool.slot_map(0).copy()
+    assert pool.prefetch(0, 0) == 0               # max_loads 0 changes nothing
+    assert np.array_equal(pool.slot_map(0), before)
+    assert pool.counters(0)["prefetches"] == 0
+
+
+def test_staged_prefill_window_of_one_loads_each_expert_once():
+    """Windows of one expert in a two-slot pool: every routed expert is its
+    own event, none is loaded twice, and the last two stay resident."""
+    pool = M.Pool(1, 8, 2, 256, 512, dry_run=True)
+    ref = oracle.PolicyPool(2, 8, "lru")
+    c = np.array([3, 0, 1, 2, 0, 0, 1, 1], np.int32)          # 5 routed experts, T*k = 8
+    pool.prefill_staged(0, c, 1, 2, T=4)
+    wins = ref.staged_prefill(c, 1)
+    assert [w for w, _ in wins] == [[0], [2], [3], [6], [7]]
+    got = pool.counters(0)
+    assert got["misses"] == 5 and got["events"] == 5
+    assert np.array_equal(pool.slot_map(0), ref.slot_map())
+    assert sorted(int(e) for e in np.nonzero(pool.slot_map(0) >= 0)[0]) == [6, 7]
