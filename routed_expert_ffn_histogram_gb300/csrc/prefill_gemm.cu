@@ -294,7 +294,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                     break;
                 }
                 for (int ks = 0; ks < n_kstages; ++ks) {
-                    if (!tc::mbar_wait(&sm.empty[stage], phase ^ 1u, err, 1u)) break;
+                    if (!tc::mbar_wait_hot(&sm.empty[stage], phase ^ 1u, err, 1u)) break;
                     tc::mbar_arrive_expect_tx(&sm.full[stage], kStageBytesA + kTxBytesB);
                     tc::tma_load_2d(sm.a[stage], &map_a, &sm.full[stage], ks * kBK, tl.m0);
                     tc::tma_load_3d(sm.b[stage], &map_b, &sm.full[stage], ks * kBK, tl.nt * kBN, slot);
@@ -308,12 +308,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
             int i = 0;
             for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x, ++i) {
                 // the epilogue has read tile i - 1 out of the accumulator
-                if (!tc::mbar_wait(&sm.acc_empty, (i & 1) ^ 1u, err, 2u)) break;
+                if (!tc::mbar_wait_hot(&sm.acc_empty, (i & 1) ^ 1u, err, 2u)) break;
                 tc::tc_fence_after();
                 bool ok = true;
                 for (int ks = 0; ks < n_kstages; ++ks) {
-                    if (!tc::mbar_wait(&sm.full[stage], phase, err, 2u) ||
-                        !tc::mbar_wait(&sm.sf_full[stage], phase, err, 2u)) {
+                    if (!tc::mbar_wait_hot(&sm.full[stage], phase, err, 2u) ||
+                        !tc::mbar_wait_hot(&sm.sf_full[stage], phase, err, 2u)) {
                         ok = false;
                         break;
                     }
@@ -382,7 +382,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     if (4 * g + w >= n_kstages) break;
-                    if (!tc::mbar_wait(&sm.empty[stage], phase ^ 1u, err, 64u)) {
+                    if (!tc::mbar_wait_hot(&sm.empty[stage], phase ^ 1u, err, 64u)) {
                         ok = false;
                         break;
                     }

@@ -66,6 +66,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
+// Wait for the phase of the given parity from a pipeline role that needs
+// to resume the moment it completes (TMA producer, MMA issuer, scale-factor
+// feeders): `mbarrier.try_wait` suspends the thread in hardware until the
+// phase completes or a short system-defined limit passes, so there is no
+// sleep between polls.  Bounded like mbar_wait (kHotWaitLimit tries).
+constexpr uint32_t kHotWaitLimit = 1u << 20;
+__device__ __forceinline__ bool mbar_wait_hot(uint64_t* bar, uint32_t parity, volatile uint32_t* err,
+                                              uint32_t code) {
+    for (uint32_t i = 0; i < kHotWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 63u) == 63u && *err) return false;
+    }
+    atomicOr(const_cast<uint32_t*>(err), code);
+    return false;
+}
+
 // ---- TMA ---------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
