@@ -44,7 +44,7 @@ NCU_TRAFFIC = {
     # depend on the number of layers)
     "decode_fused_kernel": 54_183_424 + 110_848,
     # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
-    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": None,
+    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_057_856 + 30_262_784) + (232_777_984 + 29_761_536),
 }
 
 def _peaks():
