@@ -30,11 +30,17 @@
 //   down     the 16 h values (f16 under one power-of-2 scale) times the
 //            block's codes, every consumer thread owning fixed output rows;
 //            partial sums stay in registers across an assignment's items.
-//   combine  w_a * y added to an fp32 accumulator in the workspace; the last
-//            CTA to finish (a ticket counter, no waiting) copies it to the
-//            output and clears it for the next call.
+//            E8M0 scales come from a 256-entry table in shared memory.
+//   combine  w_a * y added with float4 atomics (a lane quad's four rows) to
+//            `out` directly when the caller accumulates (out += result, a
+//            residual stream), else to an fp32 accumulator in the
+//            workspace that the last CTA to finish (a ticket counter, no
+//            waiting) copies to the output and clears for the next call.
 // No CTA waits for another: there is no grid barrier and no cooperative
-// launch.
+// launch.  The kernel is launched with programmatic stream serialisation:
+// each CTA runs its shared-memory-only prologue, lets the next kernel
+// launch, and waits for the previous one (griddepcontrol) before touching
+// global memory, so consecutive layers hand SMs over CTA by CTA.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

@@ -14,9 +14,14 @@
 //   2. gate/up GEMM: per expert e, rows [offsets[e], offsets[e+1]) of the
 //      grouped activations times the expert's interleaved gate/up matrix;
 //      epilogue h = bf16(silu(g) * u) -> MXFP8 (scale per 32 along I);
-//   3. down GEMM: grouped h times the expert's down matrix -> y (fp32, in
-//      grouped order);
-//   4. combine: out[t] = sum_j w[t][j] * y[inv[t*k+j]] in ascending j.
+//   3. down GEMM: grouped h times the expert's down matrix; its epilogue is
+//      the combine: out[token(row)] += w(row) * y(row) with float4 fp32
+//      atomics, so the k terms of a token land in completion order (out is
+//      zeroed first unless the caller accumulates into a residual stream).
+// The GEMM launches use programmatic stream serialisation (each waits for
+// its predecessor with griddepcontrol before touching global memory), and
+// the pipeline roles wait on their mbarriers with the hardware-suspending
+// try_wait, resuming the moment a phase completes.
 //
 // GEMM kernel (persistent, one CTA per SM, 16 warps in four warpgroups):
 //   warp 0     TMA producer: 128x128-byte A tile (E4M3) and 256x128-element
