@@ -432,6 +432,24 @@ MOE_API int moe_decode_layer_acc(const moe_pool_t* pool, int layer, const float*
                                  const int32_t* slot_of, void* workspace, size_t ws_bytes,
                                  float* out, moe_stream_t stream);
 
+/* Device-side status of the work done with `workspace` (path: the layout it
+ * was sized for, MOE_PATH_DECODE or MOE_PATH_PREFILL): every wait inside the
+ * kernels is bounded (about a second); one that runs out sets a bit here and
+ * the launch finishes with NaN where its data was missing, instead of
+ * hanging or faulting.  Waits for all work enqueued so far on `stream`,
+ * returns the bits in *bits (0: nothing ran out) and clears them.
+ * Decode bits: 4 copy producer, 8 consumers (data not landed).  Prefill
+ * bits: 1 TMA producer, 2 MMA issuer, 4 invalid slot, 8 epilogue, 16
+ * teardown, 32 misaligned output, 64 scale-factor feeders.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+MOE_API int moe_ffn_status(void* workspace, int path, moe_stream_t stream, uint32_t* bits);
+
+/* Test hook for the failure path above: the next n fused decode launches
+ * leave their first work item's copies unissued, so the waits on it run
+ * out and set status bits; nothing faults and the context stays usable.
+ * Errors: MOE_ERR_INVALID (n < 0). */
+MOE_API int moe_debug_stall_next_decode(int n);
+
 /* Weighted combine of per-assignment expert outputs held in grouped order:
  *   out[t][h] = sum_j w[t][j] * y_perm[inv[t*k+j]][h], j ascending, fp32.
  *   y_perm device fp32 [A][H]; w device fp32 [T][k]; inv device int32 [A];

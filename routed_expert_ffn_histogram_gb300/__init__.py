@@ -152,6 +152,19 @@ def moe_decode_layer(pool: "Pool", layer: int, logits, x_bf16, plan: RoutePlan, 
         workspace.numel() * workspace.element_size(), ptr(out), stream_handle(stream)))
 
 
+def moe_ffn_status(workspace, path: int, stream=None) -> int:
+    """Status bits of the kernels that used ``workspace`` (0: every bounded
+    wait completed); waits for ``stream`` and clears them (moe_ffn_status)."""
+    bits = C.c_uint32(0)
+    check("moe_ffn_status", lib().moe_ffn_status(ptr(workspace), path, stream_handle(stream), C.byref(bits)))
+    return bits.value
+
+
+def moe_debug_stall_next_decode(n: int = 1) -> None:
+    """Test hook: the next n fused decode launches time out on purpose."""
+    check("moe_debug_stall_next_decode", lib().moe_debug_stall_next_decode(n))
+
+
 def moe_combine(y_perm, w, inv, out, stream=None) -> None:
     T, k = w.shape
     H = out.shape[1]

@@ -275,6 +275,29 @@ extern "C" int moe_decode_layer_acc(const moe_pool_t* pool, int layer, const flo
                         ws_bytes, out, stream, true);
 }
 
+extern "C" int moe_ffn_status(void* workspace, int path, moe_stream_t stream, uint32_t* bits) {
+    if (!workspace || !bits || (path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL)) return MOE_ERR_INVALID;
+    if (!aligned(workspace, 256)) return MOE_ERR_INVALID;
+    // decode: word 2 of the 256-byte control block; prefill: the first word
+    uint32_t* dev = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + (path == MOE_PATH_DECODE ? 8 : 0));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t h = 0;
+    MOE_CUDA_TRY(cudaMemcpyAsync(&h, dev, sizeof h, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    if (h != 0) {
+        MOE_CUDA_TRY(cudaMemsetAsync(dev, 0, sizeof h, s));
+        MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    }
+    *bits = h;
+    return MOE_OK;
+}
+
+extern "C" int moe_debug_stall_next_decode(int n) {
+    if (n < 0) return MOE_ERR_INVALID;
+    moe::g_stall_decode.store(n);
+    return MOE_OK;
+}
+
 extern "C" int moe_combine(const float* y_perm, const float* w, const int32_t* inv, int T, int k, int H,
                            float* out, moe_stream_t stream) {
     if (T < 0 || k < 1 || k > MOE_MAX_TOPK || H < 1) return MOE_ERR_INVALID;

@@ -163,6 +163,7 @@ __device__ __forceinline__ void stage_block_f16(const uint16_t* __restrict__ src
 }
 
 struct FusedParams {
+    int stall;         // test hook: the first item's copies are not issued
     const uint8_t* slots;
     size_t expert_bytes;
     int S, E, H, I, k, T;
@@ -314,6 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 // the second item waits until the first has landed, so every
                 // CTA's first item is not queued behind the others' second
                 if (n == 1 && !tc::mbar_wait(&full[0], 0u, err, 4u)) break;
+                // test hook: leave the first item's barrier incomplete, so the
+                // bounded waits on it run out and set the status bits
+                if (n == 0 && p.stall) continue;
                 const int it = (g0 + n) * kGroup;
                 const int a = it / p.I, r = it - a * p.I;
                 const uint8_t* eb = tab.base[a];
@@ -530,6 +534,9 @@ size_t decode_fused_smem(int T, int k, int H, int I) {
     return need <= kFusedSmemBudget ? need : 0;
 }
 
+// Test hook (moe_debug_stall_next_decode): launches still to stall.
+std::atomic<int> g_stall_decode{0};
+
 int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const RouteOut* ro) {
     const Layout& L = *a.L;
     DeviceInfo di;
@@ -542,6 +549,12 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     if (slots < 2) return MOE_ERR_UNSUPPORTED;
     const size_t smem = st + size_t(slots) * ib;
     FusedParams p;
+    p.stall = 0;
+    for (int n = g_stall_decode.load(); n > 0; n = g_stall_decode.load())
+        if (g_stall_decode.compare_exchange_weak(n, n - 1)) {
+            p.stall = 1;
+            break;
+        }
     p.slots = a.slots;
     p.expert_bytes = a.expert_bytes;
     p.S = a.S;

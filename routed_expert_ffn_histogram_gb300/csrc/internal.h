@@ -118,6 +118,7 @@ size_t decode_workspace_bytes(int T, int k, int H, int I);
 size_t decode_acc_offset(int T, int k, int I);
 int launch_decode_layer(const FfnArgs& a, const RouteOut& ro, void* ws, cudaStream_t s);
 size_t decode_fused_smem(int T, int k, int H, int I);
+extern std::atomic<int> g_stall_decode;  // test hook: fused decode launches to stall
 int launch_decode_fused(const FfnArgs& a, void* ws, cudaStream_t s);
 int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 

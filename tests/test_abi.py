@@ -106,6 +106,11 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.moe_decode_layer_acc(None, 0, None, None, 1, 1, None, None, None, None, None, None, None, None, 0,
                                   None, None) == M.MOE_ERR_INVALID
     assert L.moe_pool_prefetch(None, 0, 1, None, None, None) == M.MOE_ERR_INVALID
+    bits = C.c_uint32(7)
+    assert L.moe_ffn_status(None, M.MOE_PATH_DECODE, None, C.byref(bits)) == M.MOE_ERR_INVALID
+    assert L.moe_ffn_status(None, 9, None, C.byref(bits)) == M.MOE_ERR_INVALID
+    assert L.moe_debug_stall_next_decode(-1) == M.MOE_ERR_INVALID
+    assert L.moe_debug_stall_next_decode(0) == M.MOE_OK
     d = _lib.MoePoolDesc(1, 8, 9, 256, 512, None, None, 0, 1)
     h = C.c_void_p()
     assert L.moe_pool_create(C.byref(d), C.byref(h)) == M.MOE_ERR_INVALID  # S > E

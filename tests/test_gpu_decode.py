@@ -227,3 +227,36 @@ def test_accumulate_into_residual(case):
             M.moe_expert_ffn(pool, 0, x, plan, slot_of, acc2, ws, path=path, accumulate=True)
         torch.cuda.synchronize()
         assert rel_l2(acc2.cpu().numpy().astype(np.float64) - r, ref) <= tol
+
+
+def test_wait_timeout_sets_status_and_context_stays_usable():
+    """Failure path without a fault: the test hook leaves one launch's first
+    work items unissued, so the bounded waits on them run out (about a
+    second); the launch finishes with NaN outputs and status bits that
+    moe_ffn_status reads and clears.  The next call on the same workspace is
+    correct and reports nothing."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[0]
+    pool, host, dev = make_pool(M, wl, layers=1)
+    T, E, k = 2, wl.experts, wl.top_k
+    lg = S.logits(wl, 0, 0, T)
+    xb = S.activations_bf16_bits(wl, 0, 0, T)
+    lgt = torch.from_numpy(lg).cuda()
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    slot_of = torch.from_numpy(pool_slot_map(pool, 0)).cuda()
+    plan = M.RoutePlan.allocate(T, E, k)
+    ws = M.alloc_ffn_workspace(T, k, wl.hidden, wl.inter, M.MOE_PATH_DECODE)
+    out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
+    assert M.moe_ffn_status(ws, M.MOE_PATH_DECODE) == 0
+    M.moe_debug_stall_next_decode(1)
+    M.moe_decode_layer(pool, 0, lgt, x, plan, slot_of, out, ws)
+    bits = M.moe_ffn_status(ws, M.MOE_PATH_DECODE)
+    assert bits & 8                               # a consumer's data wait ran out
+    assert np.isnan(out.cpu().numpy()).any()
+    assert M.moe_ffn_status(ws, M.MOE_PATH_DECODE) == 0   # read-and-clear
+    M.moe_decode_layer(pool, 0, lgt, x, plan, slot_of, out, ws)
+    assert M.moe_ffn_status(ws, M.MOE_PATH_DECODE) == 0
+    assert rel_l2(out.cpu().numpy(), _oracle_T(wl, lg, xb, prefill=False)) <= DECODE_REL_L2
