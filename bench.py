@@ -42,7 +42,7 @@ METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 roo
 NCU_TRAFFIC = {
     # one decode layer (2-layer decode capture; traffic per launch does not
     # depend on the number of layers)
-    "decode_fused_kernel": 54_183_424 + 110_848,
+    "decode_fused_kernel": 54_183_680 + 120_320,
     # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
     "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_057_856 + 30_262_784) + (232_777_984 + 29_761_536),
 }
