@@ -568,7 +568,7 @@ int get_encoder(EncodeTiledFn* out) {
 
 // Activation rows: [rows][K] bytes (E4M3), tile 128 x 128.
 int make_map_act(CUtensorMap* m, const void* base, int K, int rows) {
-    EncodeTiledFn enc;
+    EncodeTiledFn enc = nullptr;
     int rc = get_encoder(&enc);
     if (rc != MOE_OK) return rc;
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
@@ -588,7 +588,7 @@ int make_map_act(CUtensorMap* m, const void* base, int K, int rows) {
 // never multiplied (the MMA loop stops at K).
 int make_map_weights(CUtensorMap* m, const void* base, int K, int rows, int slots, size_t row_bytes,
                      size_t expert_bytes) {
-    EncodeTiledFn enc;
+    EncodeTiledFn enc = nullptr;
     int rc = get_encoder(&enc);
     if (rc != MOE_OK) return rc;
     const size_t k128 = round_up(size_t(K), 128);

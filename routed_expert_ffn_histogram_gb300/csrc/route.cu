@@ -27,7 +27,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileTokens = 256;
-constexpr int kMaxPerLane = MOE_MAX_EXPERTS / 32;
 
 struct Smem {
     int hist[MOE_MAX_EXPERTS];
