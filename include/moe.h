@@ -80,6 +80,12 @@ extern "C" {
 
 typedef void* moe_stream_t;
 
+/* Threads: the stateless calls (routing, expert FFN, combine, quantiser,
+ * packing) may be made from several host threads at once, each with its
+ * own workspace.  A pool keeps host state (slot maps, policy stamps,
+ * counters): calls on one pool must not overlap in time; different pools
+ * are independent. */
+
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
 #else
