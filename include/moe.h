@@ -82,7 +82,8 @@ typedef void* moe_stream_t;
 
 /* Threads: the stateless calls (routing, expert FFN, combine, quantiser,
  * packing) may be made from several host threads at once, each with its
- * own workspace.  A pool keeps host state (slot maps, policy stamps,
+ * own workspace (moe_route_plan_noalloc excepted: its calls share one
+ * device array).  A pool keeps host state (slot maps, policy stamps,
  * counters): calls on one pool must not overlap in time; different pools
  * are independent. */
 
