@@ -12,6 +12,9 @@ source.
 Parity status per function (what pins it, see ``tests/test_oracle_*.py``):
   * e2m1/e8m0/e4m3/bf16 codecs ........ pinned (OCP spec table, torch casts)
   * mxfp8_quant_row ................... pinned (torch e4m3 cast, frexp, closed form)
+  * e2m1_encode / mxfp4_quant_row ..... pinned (hand-worked OCP rounding cases,
+                                        brute-force nearest-with-ties-to-even,
+                                        scale closed form, dequantised bound)
   * route (top-k + softmax) ........... pinned (brute-force sort, closed forms)
   * hist_perm ......................... pinned (numpy stable argsort, invariants)
   * lru_step .......................... pinned (independent list simulator, hand cases)
@@ -84,6 +87,9 @@ def lib():
             L.oracle_f32_to_bf16.restype = C.c_uint16
             L.oracle_f32_to_bf16.argtypes = [C.c_float]
             L.oracle_mxfp8_quant_row.argtypes = [vp, i32, vp, vp]
+            L.oracle_e2m1_encode.restype = C.c_uint8
+            L.oracle_e2m1_encode.argtypes = [C.c_double]
+            L.oracle_mxfp4_quant_row.argtypes = [vp, i32, vp, vp]
             L.oracle_dequant_mxfp4.argtypes = [vp, vp, i32, i32, vp]
             L.oracle_route.argtypes = [vp, i32, i32, i32, vp, vp]
             L.oracle_hist_perm.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
@@ -135,6 +141,22 @@ def mxfp8_quant(x_bf16_bits: np.ndarray):
     s = np.zeros((rows, K // 32), np.uint8)
     for r in range(rows):
         lib().oracle_mxfp8_quant_row(_p(x[r]), K, _p(q[r]), _p(s[r]))
+    return q, s
+
+
+def e2m1_encode(v: float) -> int:
+    return lib().oracle_e2m1_encode(v)
+
+
+def mxfp4_quant(x_bf16_bits: np.ndarray):
+    """MXFP4 of each row of ``[rows, K]`` bf16 bits -> (packed codes u8
+    ``[rows, K/2]``, scales u8 ``[rows, K/32]``)."""
+    x = _c(x_bf16_bits, np.uint16)
+    rows, K = x.shape
+    q = np.zeros((rows, K // 2), np.uint8)
+    s = np.zeros((rows, K // 32), np.uint8)
+    for r in range(rows):
+        lib().oracle_mxfp4_quant_row(_p(x[r]), K, _p(q[r]), _p(s[r]))
     return q, s
 
 

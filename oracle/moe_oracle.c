@@ -164,6 +164,62 @@ void oracle_mxfp8_quant_row(const uint16_t* x_bf16, int K, uint8_t* codes, uint8
     }
 }
 
+/* E2M1 encoding (OCP MX v1.0, FP4 E2M1: bias 1, one mantissa bit, no
+ * infinities or NaN, largest 6, subnormal 0.5): round to nearest, ties to
+ * the even code, finite overflow saturated to +-6.  Sign kept for zero.    */
+uint8_t oracle_e2m1_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    if (isnan(v)) return 0x7;
+    double a = fabs(v);
+    if (a >= 6.0) return sign | 0x7;
+    if (a < 1.0) {
+        /* subnormal grid 0.5; n == 2 lands on 1.0, whose code is 2 as well */
+        double n = nearbyint(a / 0.5);
+        return sign | (uint8_t)n;
+    }
+    int ex;
+    frexp(a, &ex);                 /* a = f * 2^ex, f in [0.5, 1)          */
+    int e = ex - 1;                /* floor(log2 a), 0..2                  */
+    double n = nearbyint(a / ldexp(1.0, e - 1)); /* in [2, 4]              */
+    if (n == 4.0) { e += 1; n = 2.0; }
+    return sign | (uint8_t)(((e + 1) << 1) | ((int)n - 2));
+}
+
+/* MXFP4 quantisation of one row of K bf16 values, K a multiple of 32 (OCP
+ * MX v1.0, section 6.3 conversion with emax_elem = 2 for E2M1): per block
+ * of 32, scale byte = floor(log2(amax)) - 2 + 127 clamped to [0, 254] (0
+ * when amax = 0), element = E2M1_RNE_satfinite(x / 2^(byte-127)); codes
+ * packed two per byte, element 2i in the low nibble.                      */
+void oracle_mxfp4_quant_row(const uint16_t* x_bf16, int K, uint8_t* packed, uint8_t* scales)
+{
+    for (int b = 0; b < K / 32; ++b) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i) {
+            double v = fabs((double)oracle_bf16_to_f32(x_bf16[b * 32 + i]));
+            if (v > amax) amax = v;
+        }
+        int sb;
+        if (amax == 0.0) {
+            sb = 0;
+        } else {
+            int ex;
+            frexp(amax, &ex);
+            sb = (ex - 1) - 2 + 127;
+            if (sb < 0) sb = 0;
+            if (sb > 254) sb = 254;
+        }
+        scales[b] = (uint8_t)sb;
+        for (int i = 0; i < 16; ++i) {
+            double v0 = (double)oracle_bf16_to_f32(x_bf16[b * 32 + 2 * i]);
+            double v1 = (double)oracle_bf16_to_f32(x_bf16[b * 32 + 2 * i + 1]);
+            uint8_t c0 = oracle_e2m1_encode(ldexp(v0, 127 - sb));
+            uint8_t c1 = oracle_e2m1_encode(ldexp(v1, 127 - sb));
+            packed[b * 16 + i] = (uint8_t)(c0 | (c1 << 4));
+        }
+    }
+}
+
 /* One element of a canonical MXFP4 matrix [rows][K]: codes [rows][K/2] with
  * element 2i in the low nibble, scales [rows][K/32].  Exact in fp32.        */
 static float mxfp4_at(const uint8_t* codes, const uint8_t* scales, int K, int r, int c)

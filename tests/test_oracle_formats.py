@@ -138,3 +138,63 @@ def test_dequant_mxfp4_against_table():
     ref = el * np.exp2(np.repeat(scales.astype(np.float64) - 127, 32, axis=1))
     got = oracle.dequant_mxfp4(codes, scales)
     assert np.array_equal(got.astype(np.float64), ref)
+
+
+def _e2m1_nearest(v):
+    """Brute force: the E2M1 code whose value is nearest to v, ties to the
+    code with mantissa bit 0, sign kept (including for zero)."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    a = abs(v)
+    best = min(range(8), key=lambda i: (abs(a - mags[i]), i & 1))
+    return best | (8 if math.copysign(1.0, v) < 0 else 0)
+
+
+def test_e2m1_encode_hand_worked_cases():
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "e2m1_rounding.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        v, code = line.split()
+        assert oracle.e2m1_encode(float(v)) == int(code), v
+
+
+def test_e2m1_encode_matches_brute_force_nearest():
+    rng = np.random.default_rng(4)
+    vals = list(rng.standard_normal(20000) * 3) + list(rng.uniform(-8, 8, 20000))
+    vals += [m / 4 for m in range(-40, 41)]          # every quarter step: all ties
+    for v in vals:
+        assert oracle.e2m1_encode(float(v)) == _e2m1_nearest(float(v)), v
+    for c in range(16):                              # the grid maps to itself
+        assert oracle.e2m1_encode(oracle.e2m1_value(c)) == c
+
+
+def test_mxfp4_quant_scale_rule_and_bound():
+    """Scale byte = floor(log2 amax) - 2 + 127 (OCP MX v1.0 6.3, emax 2 for
+    E2M1); every element dequantises to within half the local grid step or
+    saturates to 6 * scale; zero blocks give scale 0 and zero codes."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((8, 256)) * np.exp(rng.uniform(-8, 8, (8, 1)))).astype(np.float32)
+    x[3, 64:96] = 0.0
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    q, s = oracle.mxfp4_quant(bits)
+    xf = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy().astype(np.float64)
+    for r in range(8):
+        for b in range(256 // 32):
+            blk = xf[r, 32 * b:32 * b + 32]
+            amax = np.abs(blk).max()
+            if amax == 0:
+                assert s[r, b] == 0 and not q[r, 16 * b:16 * b + 16].any()
+                continue
+            assert s[r, b] == math.frexp(amax)[1] - 1 - 2 + 127
+            scale = 2.0 ** (int(s[r, b]) - 127)
+            for i in range(32):
+                byte = q[r, 16 * b + i // 2]
+                code = (byte >> 4) if i & 1 else (byte & 15)
+                got = oracle.e2m1_value(code) * scale
+                ref = blk[i]
+                if abs(ref) / scale >= 6.0:
+                    assert got == math.copysign(6.0 * scale, ref)
+                else:
+                    a = abs(ref) / scale                      # grid steps 0.5 / 1 / 2 below 2 / 4 / 6
+                    half_step = 0.25 if a < 2 else (0.5 if a < 4 else 1.0)
+                    assert abs(got - ref) <= half_step * scale
