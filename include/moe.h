@@ -473,6 +473,18 @@ MOE_API int moe_combine(const float* y_perm, const float* w, const int32_t* inv,
 MOE_API int moe_quant_mxfp8(const void* x_bf16, int K, const int32_t* perm, int k, int rows,
                     uint8_t* q, uint8_t* scales, int scale_stride, moe_stream_t stream);
 
+/* MXFP4 quantisation of bf16 rows [MX] (OCP MX v1.0: E2M1 elements, shared
+ * exponent floor(log2(amax)) - 2 per block of 32, E8M0 byte clamped to
+ * [0, 254], 0 for an all-zero block; round to nearest even, finite overflow
+ * saturated to +-6), for MXFP4 activations:
+ *   x_bf16 device [rows][K] (16-byte aligned); q device uint8 [rows][K/2],
+ *   element 2i in the low nibble of byte i (16-byte aligned); scales device
+ *   uint8 [rows][scale_stride], the first K/32 of each row written;
+ *   K a multiple of 32.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+MOE_API int moe_quant_mxfp4(const void* x_bf16, int K, int rows, uint8_t* q, uint8_t* scales,
+                            int scale_stride, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -172,6 +172,14 @@ def moe_combine(y_perm, w, inv, out, stream=None) -> None:
                                            stream_handle(stream)))
 
 
+def moe_quant_mxfp4(x_bf16, q, scales, stream=None) -> None:
+    """MXFP4 of bf16 rows: q uint8 [rows][K/2] (two codes per byte), scales
+    uint8 [rows][>= K/32] (moe_quant_mxfp4)."""
+    rows, K = x_bf16.shape
+    check("moe_quant_mxfp4", lib().moe_quant_mxfp4(ptr(x_bf16), K, rows, ptr(q), ptr(scales), scales.shape[1],
+                                                   stream_handle(stream)))
+
+
 def moe_quant_mxfp8(x_bf16, q, scales, perm=None, k: int = 1, stream=None) -> None:
     rows, K = q.shape
     check("moe_quant_mxfp8", lib().moe_quant_mxfp8(ptr(x_bf16), K, ptr(perm), k, rows, ptr(q), ptr(scales),

@@ -85,6 +85,7 @@ SIGNATURES = {
     "moe_ffn_status": (_i32, [_vp, _i32, _vp, C.POINTER(C.c_uint32)]),
     "moe_debug_stall_next_decode": (_i32, [_i32]),
     "moe_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "moe_quant_mxfp4": (_i32, [_vp, _i32, _i32, _vp, _vp, _i32, _vp]),
     "moe_quant_mxfp8": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _vp]),
 }
 

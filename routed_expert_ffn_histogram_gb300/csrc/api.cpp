@@ -306,6 +306,15 @@ extern "C" int moe_combine(const float* y_perm, const float* w, const int32_t* i
     return moe::launch_combine(y_perm, w, inv, T, k, H, out, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int moe_quant_mxfp4(const void* x_bf16, int K, int rows, uint8_t* q, uint8_t* scales, int scale_stride,
+                               moe_stream_t stream) {
+    if (K <= 0 || K % 32 || rows < 0 || scale_stride < K / 32) return MOE_ERR_INVALID;
+    if (rows == 0) return MOE_OK;
+    if (!x_bf16 || !q || !scales || !aligned(x_bf16, 16) || !aligned(q, 16)) return MOE_ERR_INVALID;
+    return moe::launch_quant_mxfp4(static_cast<const uint16_t*>(x_bf16), K, rows, q, scales, scale_stride,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int moe_quant_mxfp8(const void* x_bf16, int K, const int32_t* perm, int k, int rows, uint8_t* q,
                                uint8_t* scales, int scale_stride, moe_stream_t stream) {
     if (K <= 0 || K % 32 || rows < 0 || k < 1 || scale_stride < K / 32) return MOE_ERR_INVALID;

@@ -135,6 +135,9 @@ int launch_combine(const float* y_perm, const float* w, const int32_t* inv, int 
                    float* out, cudaStream_t s);
 int launch_quant_mxfp8(const uint16_t* x, int K, const int32_t* perm, int k, int rows, uint8_t* q,
                        uint8_t* scales, int scale_stride, cudaStream_t s);
+// MXFP4 (E2M1 + E8M0 per 32) of bf16 rows, codes packed two per byte.
+int launch_quant_mxfp4(const uint16_t* x, int K, int rows, uint8_t* q, uint8_t* scales, int scale_stride,
+                       cudaStream_t s);
 // Prefill operand: token t's MXFP8 row written to grouped rows inv[t*k + j].
 int launch_quant_mxfp8_scatter(const uint16_t* x, int K, const int32_t* inv, int k, int T, uint8_t* q,
                                uint8_t* scales, int scale_stride, cudaStream_t s);

@@ -182,6 +182,73 @@ int grid_for(long work, int threads) {
 
 }  // namespace
 
+// MXFP4 quantisation of bf16 rows (OCP MX v1.0: E2M1 elements, shared
+// exponent floor(log2(amax)) - 2, E8M0 byte clamped to [0, 254], RNE with
+// finite overflow saturated to +-6), codes packed two per byte with element
+// 2i in the low nibble.  One thread per 32-element block: 64 bytes in, 16
+// code bytes and one scale byte out.
+__global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __restrict__ x, int K, long blocks,
+                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales,
+                                                          int scale_stride) {
+    const long g = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= blocks) return;
+    const int nb = K / 32;
+    const long row = g / nb;
+    const int b = int(g - row * nb);
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * K + (long)b * 32);
+    uint32_t w[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v = __ldg(src + c);
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+    const int ef = int((__float_as_uint(amax) >> 23) & 0xffu);
+    // floor(log2 amax) = ef - 127 for normal amax; bf16 subnormals land far
+    // below the clamp, which gives byte 0 as well
+    const int sb = (amax == 0.0f || ef == 0) ? 0 : min(max(ef - 127 - 2 + 127, 0), 254);
+    const float mul = ldexpf(1.0f, 127 - sb);
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t r;
+        // four bytes, each two E2M1 codes: element 2i in the low nibble
+        asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+            "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+            : "=r"(r)
+            : "f"(__uint_as_float(w[4 * j] << 16) * mul), "f"(__uint_as_float(w[4 * j] & 0xffff0000u) * mul),
+              "f"(__uint_as_float(w[4 * j + 1] << 16) * mul), "f"(__uint_as_float(w[4 * j + 1] & 0xffff0000u) * mul),
+              "f"(__uint_as_float(w[4 * j + 2] << 16) * mul), "f"(__uint_as_float(w[4 * j + 2] & 0xffff0000u) * mul),
+              "f"(__uint_as_float(w[4 * j + 3] << 16) * mul), "f"(__uint_as_float(w[4 * j + 3] & 0xffff0000u) * mul));
+        out[j] = r;
+    }
+    *reinterpret_cast<uint4*>(q + row * (K / 2) + (long)b * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+    scales[row * scale_stride + b] = uint8_t(sb);
+}
+
+int launch_quant_mxfp4(const uint16_t* x, int K, int rows, uint8_t* q, uint8_t* scales, int scale_stride,
+                       cudaStream_t s) {
+    const long blocks = (long)rows * (K / 32);
+    const long grid = (blocks + 255) / 256;
+    if (grid > 0x7fffffffL) return MOE_ERR_UNSUPPORTED;
+    if (grid == 0) return MOE_OK;
+    quant_mxfp4_kernel<<<(unsigned)grid, 256, 0, s>>>(x, K, blocks, q, scales, scale_stride);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
 int launch_quant_mxfp8(const uint16_t* x, int K, const int32_t* perm, int k, int rows, uint8_t* q,
                        uint8_t* scales, int scale_stride, cudaStream_t s) {
     // one warp per 32 blocks of a row: the gather (perm, then x) is a

@@ -74,3 +74,33 @@ def test_combine(T, k, H):
     M.moe_combine(torch.from_numpy(y_perm).cuda(), torch.from_numpy(w).cuda(), torch.from_numpy(inv).cuda(), out)
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), oracle.combine(y, w))
+
+
+def test_quant_mxfp4_bit_exact():
+    """MXFP4 activation quantisation (moe_quant_mxfp4, hardware E2M1
+    conversion) against the oracle: packed codes and E8M0 scales bit-exact
+    on rows spanning 2^-30..2^30 in magnitude, exact ties between E2M1 grid
+    points, all-zero blocks, bf16 subnormals and saturating values."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    rng = np.random.default_rng(12)
+    rows, K = 64, 512
+    x = (rng.standard_normal((rows, K)) * np.exp2(rng.integers(-30, 30, (rows, 1)))).astype(np.float32)
+    # exact ties: block max 4 (scale 1), the rest on quarter steps of the grid
+    x[1, :32] = 4.0
+    x[1, 1:32] = np.array([m / 4 for m in range(1, 32)], np.float32) % 6.0
+    x[2, 32:64] = 0.0                                  # all-zero block
+    x[3, 64:96] = np.float32(1e-40)                    # bf16 subnormals
+    x[4, 96:128] = np.linspace(-7.9, 7.9, 32, dtype=np.float32)   # saturates at +-6 after scaling by 1
+    x[4, 96] = 7.9
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    xb = xt.view(torch.int16).numpy().view(np.uint16)
+    q = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((rows, K // 32), dtype=torch.uint8, device="cuda")
+    M.moe_quant_mxfp4(xt.cuda(), q, s)
+    torch.cuda.synchronize()
+    qr, sr = oracle.mxfp4_quant(xb)
+    assert np.array_equal(s.cpu().numpy(), sr)
+    assert np.array_equal(q.cpu().numpy(), qr)
