@@ -26,8 +26,11 @@ Parity status per function (what pins it, see ``tests/test_oracle_*.py``):
                                         LFU victim, load-once and residency
                                         invariants)
   * expert_gateup / expert_down ....... pinned (integer-exact case, float64 numpy bound)
-  * layer (decode, prefill) ........... pinned piecewise; the end-to-end float
-                                        value has no printed worked example
+  * layer (decode, prefill, FP4 act) .. pinned piecewise and against a float64
+                                        numpy evaluation (brute-force E2M1
+                                        nearest for the FP4-activation mode);
+                                        the end-to-end float value has no
+                                        printed worked example
   * combine ........................... pinned (k=1 identity, float64 bound)
 """
 from __future__ import annotations
@@ -445,11 +448,25 @@ def expert_down(wt: dict, hf: np.ndarray) -> np.ndarray:
     return y
 
 
+_ACT_MODES = {"bf16": 0, "mxfp8": 1, "mxfp4": 2}
+
+
 def layer(x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray, weights: dict, prefill: bool,
-          threads: int = 1, want_intermediates: bool = False):
+          threads: int = 1, want_intermediates: bool = False, act: str | None = None):
     """The whole layer.  ``weights`` holds stacked ``[E, ...]`` canonical arrays
     indexed by ``ids``.  Returns ``out`` (fp32 ``[T, H]``), plus a dict of
-    intermediates when asked."""
+    intermediates when asked.
+
+    ``act`` picks the expert-input format at both quantisation points (x
+    before gate/up, h before down): ``"bf16"`` (the decode path),
+    ``"mxfp8"`` (the prefill path) or ``"mxfp4"`` (the FP4-activation
+    prefill variant); by default it follows ``prefill``.  With ``"mxfp4"``
+    the intermediates ``xq``/``hq`` are packed two codes per byte."""
+    if act is None:
+        act = "mxfp8" if prefill else "bf16"
+    if act not in _ACT_MODES:
+        raise ValueError(f"act must be one of {sorted(_ACT_MODES)}, got {act!r}")
+    mode = _ACT_MODES[act]
     x = _c(x_bf16, np.uint16)
     ids = _c(ids, np.int32)
     w = _c(w, np.float32)
@@ -459,12 +476,14 @@ def layer(x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray, weights: dict, pre
     out = np.zeros((T, H), np.float32)
     A = T * k
     h = np.zeros((A, I), np.uint16)
-    xq = np.zeros((T, H), np.uint8) if (prefill and want_intermediates) else None
-    xs = np.zeros((T, H // 32), np.uint8) if (prefill and want_intermediates) else None
-    hq = np.zeros((A, I), np.uint8) if (prefill and want_intermediates) else None
-    hs = np.zeros((A, I // 32), np.uint8) if (prefill and want_intermediates) else None
+    per = 2 if mode == 2 else 1           # elements per code byte
+    keep = bool(mode) and want_intermediates
+    xq = np.zeros((T, H // per), np.uint8) if keep else None
+    xs = np.zeros((T, H // 32), np.uint8) if keep else None
+    hq = np.zeros((A, I // per), np.uint8) if keep else None
+    hs = np.zeros((A, I // 32), np.uint8) if keep else None
     ws = {kk: _c(v, np.uint8) for kk, v in weights.items()}
-    rc = lib().oracle_layer(int(bool(prefill)), T, H, I, k, _p(x), _p(ids), _p(w),
+    rc = lib().oracle_layer(mode, T, H, I, k, _p(x), _p(ids), _p(w),
                             _p(ws["gate_codes"]), _p(ws["gate_scales"]), _p(ws["up_codes"]),
                             _p(ws["up_scales"]), _p(ws["down_codes"]), _p(ws["down_scales"]),
                             _p(out), _p(h), _p(xq), _p(xs), _p(hq), _p(hs), int(threads))

@@ -478,9 +478,14 @@ static void item_down_combine(void* p, long item)
  *   prefill = 1 (prefill path): the expert input is MXFP8(x) per token and
  *     the down projection reads MXFP8(bf16(h)) per assignment; both use the
  *     block-32 rule of oracle_mxfp8_quant_row.
+ *   prefill = 2 (FP4-activation variant of the prefill path): as 1, with
+ *     MXFP4 in place of MXFP8 for both quantisation points, by the block-32
+ *     rule of oracle_mxfp4_quant_row (E2M1 x E2M1 products, the all-FP4
+ *     block-scaled MMA of the Blackwell MX formats).
  * Weights are stacked canonical arrays indexed by the ids.  Optional outputs
  * (may be NULL): h_bf16 [T*k][I]; xq/xs [T][H], [T][H/32]; hq/hs [T*k][I],
- * [T*k][I/32] (prefill only).                                               */
+ * [T*k][I/32] (prefill only; with prefill = 2 the codes are packed two per
+ * byte, so xq is [T][H/2] and hq [T*k][I/2]).                               */
 int oracle_layer(int prefill, int T, int H, int I, int k,
                  const uint16_t* x_bf16, const int32_t* ids, const float* w,
                  const uint8_t* gate_codes, const uint8_t* gate_scales,
@@ -490,6 +495,7 @@ int oracle_layer(int prefill, int T, int H, int I, int k,
                  uint8_t* xq, uint8_t* xs, uint8_t* hq, uint8_t* hs, int threads)
 {
     if (T < 0 || H <= 0 || I <= 0 || k <= 0 || H % 32 || I % 32) return ORACLE_ERR_INVALID;
+    if (prefill < 0 || prefill > 2) return ORACLE_ERR_INVALID;
     size_t A = (size_t)T * k;
     float* xf = (float*)malloc(sizeof(float) * (size_t)T * H + 1);
     float* hf = (float*)malloc(sizeof(float) * A * I + 1);
@@ -502,6 +508,11 @@ int oracle_layer(int prefill, int T, int H, int I, int k,
         float* xo = xf + (size_t)t * H;
         if (!prefill) {
             for (int c = 0; c < H; ++c) xo[c] = oracle_bf16_to_f32(xr[c]);
+        } else if (prefill == 2) {
+            oracle_mxfp4_quant_row(xr, H, q, s);
+            for (int c = 0; c < H; ++c) xo[c] = mxfp4_at(q, s, H, 0, c);
+            if (xq) memcpy(xq + (size_t)t * (H / 2), q, (size_t)H / 2);
+            if (xs) memcpy(xs + (size_t)t * (H / 32), s, (size_t)H / 32);
         } else {
             oracle_mxfp8_quant_row(xr, H, q, s);
             for (int c = 0; c < H; ++c) xo[c] = (float)(oracle_e4m3_value(q[c]) * oracle_e8m0_value(s[c / 32]));
@@ -519,6 +530,11 @@ int oracle_layer(int prefill, int T, int H, int I, int k,
         float* ho = hf + a * I;
         if (!prefill) {
             for (int i = 0; i < I; ++i) ho[i] = oracle_bf16_to_f32(hr[i]);
+        } else if (prefill == 2) {
+            oracle_mxfp4_quant_row(hr, I, q, s);
+            for (int i = 0; i < I; ++i) ho[i] = mxfp4_at(q, s, I, 0, i);
+            if (hq) memcpy(hq + a * (I / 2), q, (size_t)I / 2);
+            if (hs) memcpy(hs + a * (I / 32), s, (size_t)I / 32);
         } else {
             oracle_mxfp8_quant_row(hr, I, q, s);
             for (int i = 0; i < I; ++i) ho[i] = (float)(oracle_e4m3_value(q[i]) * oracle_e8m0_value(s[i / 32]));

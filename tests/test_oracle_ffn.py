@@ -144,6 +144,92 @@ def test_layer_intermediates_consistent():
     assert np.array_equal(it["hq"], q2) and np.array_equal(it["hs"], s2)
 
 
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _mx4_64(bits_rows):
+    """MXFP4 quantise-dequantise in float64, written independently of the
+    oracle: scale 2^(floor(log2 amax) - 2) per 32 (OCP MX v1.0 conversion
+    with emax_elem = 2), each element the nearest E2M1 magnitude found by
+    brute force over the 8 grid points, ties to the even code, sign kept."""
+    x = _bits_f32(bits_rows).astype(np.float64)
+    R, K = x.shape
+    blk = x.reshape(R, K // 32, 32)
+    amax = np.abs(blk).max(-1)
+    _, ex = np.frexp(amax)
+    sb = np.where(amax == 0, 0, np.clip(ex - 1 - 2 + 127, 0, 254)).astype(np.float64)
+    sc = np.exp2(sb - 127)[..., None]
+    a = np.abs(blk / sc)
+    d = np.abs(a[..., None] - _E2M1_MAG)
+    tie = d == d.min(-1, keepdims=True)
+    even = tie & (np.arange(8) % 2 == 0)
+    code = np.where(even.any(-1), even.argmax(-1), tie.argmax(-1))
+    return (np.sign(blk) * _E2M1_MAG[code] * sc).reshape(R, K)
+
+
+def _deq4_act(packed, scales):
+    """Packed activation codes [R][K/2] + E8M0 [R][K/32] -> float64 [R][K]."""
+    return _deq64(packed, scales)
+
+
+def test_layer_mxfp4_activations_vs_float64():
+    """The FP4-activation variant: both quantisation points reproduce the
+    independent float64 MXFP4 quantiser exactly, h is the float64 SwiGLU to
+    within one bf16 ulp, and out is the float64 down + combine of the
+    quantised h within the fp32 summation bound."""
+    wl = S.WORKLOADS[0]
+    ids, w = oracle.route(S.logits(wl, 0), wl.top_k)
+    ws = S.stack_experts(S.layer_weights(wl, 0))
+    x = S.activations_bf16_bits(wl, 0)
+    out, it = oracle.layer(x, ids, w, ws, prefill=True, act="mxfp4", want_intermediates=True, threads=4)
+    T, H = x.shape
+    k = ids.shape[1]
+    I = ws["gate_codes"].shape[1]
+    assert it["xq"].shape == (T, H // 2) and it["hq"].shape == (T * k, I // 2)
+    xin = _mx4_64(x)
+    assert np.array_equal(_deq4_act(it["xq"], it["xs"]), xin)
+    # the same codes as the stand-alone quantiser
+    q, sc = oracle.mxfp4_quant(x)
+    assert np.array_equal(it["xq"], q) and np.array_equal(it["xs"], sc)
+    hin = _mx4_64(it["h"])
+    assert np.array_equal(_deq4_act(it["hq"], it["hs"]), hin)
+    ref = np.zeros((T, H))
+    bound = np.zeros((T, H))
+    ulp = []
+    for t in range(T):
+        for j in range(k):
+            e, a = ids[t, j], t * k + j
+            Wg = _deq64(ws["gate_codes"][e], ws["gate_scales"][e])
+            Wu = _deq64(ws["up_codes"][e], ws["up_scales"][e])
+            Wd = _deq64(ws["down_codes"][e], ws["down_scales"][e])
+            g, u = Wg @ xin[t], Wu @ xin[t]
+            hb = _bf16_bits((torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u).astype(np.float32))
+            ulp.append(np.abs(hb.astype(np.int32) - it["h"][a].astype(np.int32)))
+            y = Wd @ hin[a]
+            ref[t] += float(w[t, j]) * y
+            bound[t] += abs(float(w[t, j])) * (np.abs(Wd) @ np.abs(hin[a]))
+    ulp = np.concatenate(ulp)
+    assert np.all(ulp <= 1) and np.mean(ulp == 0) > 0.99
+    gamma = (I + k) * 2.0 ** -24 / (1 - (I + k) * 2.0 ** -24)
+    assert np.all(np.abs(out - ref) <= gamma * bound + 1e-30)
+    # threads change nothing; the FP8 mode is a different computation
+    assert np.array_equal(out, oracle.layer(x, ids, w, ws, prefill=True, act="mxfp4", threads=1))
+    assert not np.array_equal(out, oracle.layer(x, ids, w, ws, prefill=True, act="mxfp8"))
+
+
+def test_layer_act_argument():
+    wl = S.WORKLOADS[0]
+    ids, w = oracle.route(S.logits(wl, 0), wl.top_k)
+    ws = S.stack_experts(S.layer_weights(wl, 0))
+    x = S.activations_bf16_bits(wl, 0)
+    assert np.array_equal(oracle.layer(x, ids, w, ws, prefill=False),
+                          oracle.layer(x, ids, w, ws, prefill=True, act="bf16"))
+    assert np.array_equal(oracle.layer(x, ids, w, ws, prefill=True),
+                          oracle.layer(x, ids, w, ws, prefill=False, act="mxfp8"))
+    with pytest.raises(ValueError):
+        oracle.layer(x, ids, w, ws, prefill=True, act="fp4")
+
+
 def test_combine_pins():
     rng = np.random.default_rng(2)
     y = rng.standard_normal((5, 1, 64)).astype(np.float32)
