@@ -19,6 +19,10 @@ Canonical MXFP4 layout (one matrix of ``rows x K``):
   * codes  : uint8 ``[rows][K/2]``, element ``2i`` in the low nibble of byte ``i``;
   * scales : uint8 ``[rows][K/32]`` E8M0 bytes, one per 32-element block along K.
 Gate and up are ``[I][H]``; down is ``[H][I]``.
+
+GGUF weights (``gguf_matrix``) are rows of Q8_0 blocks (32 elements in 34
+bytes) or Q4_K super-blocks (256 elements in 144 bytes) along K, drawn as
+random bytes with their binary16 scales set to a bounded range.
 """
 from __future__ import annotations
 
@@ -36,6 +40,8 @@ TAG_X = 3
 TAG_GATE = 4
 TAG_UP = 5
 TAG_DOWN = 6
+
+TAG_GGUF = 16       # + 0 gate, 1 up, 2 down; GGUF block streams
 
 # E8M0 scale bytes are 127 + e with e uniform in {-6,...,-2}.
 SCALE_BYTE_LO = 121
@@ -125,6 +131,39 @@ def expert_weights(wl: Workload, layer: int, expert: int) -> dict:
     dc, ds = _matrix(wl, TAG_DOWN, layer, expert, H, I)
     return dict(gate_codes=gc, gate_scales=gs, up_codes=uc, up_scales=us,
                 down_codes=dc, down_scales=ds)
+
+
+GGUF_BLOCK = {"q8_0": (32, 34), "q4_k": (256, 144)}   # elements, bytes per block
+
+
+def gguf_matrix(wl: Workload, fmt: str, which: int, layer: int, expert: int, rows: int, K: int) -> np.ndarray:
+    """GGUF block bytes ``[rows, K/n * bytes]`` of one matrix (``which``: 0
+    gate, 1 up, 2 down), random in every byte except the binary16 scales:
+    Q8_0 ``d`` and Q4_K ``d``/``dmin`` are 2^u with u uniform in [-9, -6)
+    (Q8_0) or [-9, -7) (Q4_K), rounded to binary16, little-endian.  The
+    6-bit scales/mins and the values are uniform over their codes."""
+    n, nbytes = GGUF_BLOCK[fmt]
+    if K % n:
+        raise ValueError(f"K={K} is not a multiple of {n} ({fmt})")
+    rng = _rng(wl.weight_wid, TAG_GGUF + which, layer, expert, nbytes)
+    nb = K // n
+    blk = rng.integers(0, 256, size=(rows, nb, nbytes), dtype=np.uint8)
+    if fmt == "q8_0":
+        d = np.exp2(rng.uniform(-9, -6, size=(rows, nb))).astype("<f2")
+        blk[..., 0:2] = d.view(np.uint8).reshape(rows, nb, 2)
+    else:
+        d = np.exp2(rng.uniform(-9, -7, size=(rows, nb, 2))).astype("<f2")
+        blk[..., 0:4] = d.view(np.uint8).reshape(rows, nb, 4)
+    return blk.reshape(rows, nb * nbytes)
+
+
+def expert_weights_gguf(wl: Workload, fmt: str, layer: int, expert: int) -> dict:
+    """GGUF weights of one expert: ``gate``/``up`` ``[I][row bytes of H]``,
+    ``down`` ``[H][row bytes of I]``."""
+    H, I = wl.hidden, wl.inter
+    return dict(gate=gguf_matrix(wl, fmt, 0, layer, expert, I, H),
+                up=gguf_matrix(wl, fmt, 1, layer, expert, I, H),
+                down=gguf_matrix(wl, fmt, 2, layer, expert, H, I))
 
 
 def layer_weights(wl: Workload, layer: int, experts=None, threads: int | None = None) -> list:

@@ -32,6 +32,14 @@ Parity status per function (what pins it, see ``tests/test_oracle_*.py``):
                                         the end-to-end float value has no
                                         printed worked example
   * combine ........................... pinned (k=1 identity, float64 bound)
+  * f16 / GGUF Q8_0, Q4_K dequant ...... pinned (binary16 against torch over all
+                                        codes; hand-worked blocks; structural
+                                        special cases of the Q4_K scale/min
+                                        packing and nibble order)
+  * layer_gguf (decode) ............... pinned against a float64 numpy evaluation
+                                        within the fp32 summation bound, and
+                                        equal to the MXFP4 layer on weights
+                                        both formats represent exactly
 """
 from __future__ import annotations
 
@@ -102,6 +110,13 @@ def lib():
             L.oracle_layer.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                        vp, vp, vp, vp, vp, vp, i32]
             L.oracle_combine.argtypes = [vp, vp, i32, i32, i32, vp]
+            L.oracle_f16_value.restype = C.c_double
+            L.oracle_f16_value.argtypes = [C.c_uint16]
+            L.oracle_dequant_q8_0.argtypes = [vp, i32, i32, vp]
+            L.oracle_dequant_q4_k.argtypes = [vp, i32, i32, vp]
+            L.oracle_gguf_row_bytes.restype = C.c_long
+            L.oracle_gguf_row_bytes.argtypes = [i32, i32]
+            L.oracle_layer_gguf.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32]
             _lib = L
     return _lib
 
@@ -492,6 +507,58 @@ def layer(x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray, weights: dict, pre
     if want_intermediates:
         return out, dict(h=h, xq=xq, xs=xs, hq=hq, hs=hs)
     return out
+
+
+GGUF_FORMATS = {"q8_0": 0, "q4_k": 1}
+
+
+def f16_value(bits: int) -> float:
+    """IEEE binary16 bit pattern -> value (from the bit definition)."""
+    return lib().oracle_f16_value(int(bits))
+
+
+def gguf_row_bytes(fmt: str, K: int) -> int:
+    """Bytes of one row of ``K`` elements in GGUF ``fmt`` (0 if K does not fit)."""
+    return int(lib().oracle_gguf_row_bytes(GGUF_FORMATS[fmt], int(K)))
+
+
+def dequant_gguf(fmt: str, blocks: np.ndarray, K: int) -> np.ndarray:
+    """Rows of GGUF blocks ``[rows, row_bytes]`` (``"q8_0"`` or ``"q4_k"``)
+    -> fp32 ``[rows, K]``, by the format's rule (moe_oracle.c)."""
+    rb = gguf_row_bytes(fmt, K)
+    if not rb:
+        raise ValueError(f"K={K} does not fit {fmt}")
+    b = _c(blocks, np.uint8).reshape(-1, rb)
+    out = np.zeros((b.shape[0], K), np.float32)
+    fn = lib().oracle_dequant_q8_0 if fmt == "q8_0" else lib().oracle_dequant_q4_k
+    fn(_p(b), b.shape[0], int(K), _p(out))
+    return out
+
+
+def layer_gguf(fmt: str, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray, weights: dict,
+               threads: int = 1, want_h: bool = False):
+    """The decode layer on GGUF expert weights.  ``weights`` holds stacked
+    ``gate``/``up`` ``[E, I, row_bytes(H)]`` and ``down`` ``[E, H,
+    row_bytes(I)]`` block bytes.  Returns ``out`` (fp32 ``[T, H]``), and the
+    bf16 bits of h ``[T*k, I]`` when asked."""
+    x = _c(x_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    T, H = x.shape
+    k = ids.shape[1]
+    g = _c(weights["gate"], np.uint8)
+    u = _c(weights["up"], np.uint8)
+    d = _c(weights["down"], np.uint8)
+    E, I = g.shape[0], g.shape[1]
+    if g.shape[2] != gguf_row_bytes(fmt, H) or d.shape[1:] != (H, gguf_row_bytes(fmt, I)) or u.shape != g.shape:
+        raise ValueError("weight shapes do not match the format")
+    out = np.zeros((T, H), np.float32)
+    h = np.zeros((T * k, I), np.uint16)
+    rc = lib().oracle_layer_gguf(GGUF_FORMATS[fmt], T, H, I, k, _p(x), _p(ids), _p(w), _p(g), _p(u), _p(d),
+                                 E, _p(out), _p(h), int(threads))
+    if rc != OK:
+        raise ValueError(f"oracle_layer_gguf: {rc}")
+    return (out, h) if want_h else out
 
 
 def combine(y: np.ndarray, w: np.ndarray) -> np.ndarray:

@@ -28,7 +28,8 @@
  *     replay-semantics study: fused-event contract).
  *
  * Number formats follow the OCP Microscaling Formats (MX) v1.0 specification:
- * E2M1 elements, E8M0 block-32 scales, E4M3 elements for MXFP8.
+ * E2M1 elements, E8M0 block-32 scales, E4M3 elements for MXFP8.  The GGUF
+ * expert formats Q8_0 and Q4_K follow the published GGUF block layouts.
  *
  * Precision: the expert path is the one the method states -- bf16
  * activations times fp32-dequantised fp4, products and sums in fp32 taken in
@@ -235,6 +236,101 @@ void oracle_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int rows,
     for (int r = 0; r < rows; ++r)
         for (int c = 0; c < K; ++c)
             out[(size_t)r * K + c] = mxfp4_at(codes, scales, K, r, c);
+}
+
+/* ---- GGUF block formats Q8_0 and Q4_K ------------------------------------
+ * The tinyserve README ("How it works" item 2; "Supported models",
+ * Formats) runs GGUF experts in their native block formats (Q4_K, Q5_K,
+ * Q6_K, Q8_0).  The pages name the formats without defining them; the
+ * layouts below are the published GGUF / ggml block formats, restated.
+ * Blocks run along a row (the reduction dimension); a row of K elements is
+ * K/32 Q8_0 blocks or K/256 Q4_K super-blocks, stored back to back.         */
+
+/* IEEE 754 binary16: sign, 5 exponent bits with bias 15, 10 fraction bits;
+ * exponent field 0 is subnormal (fraction * 2^-24), 31 is infinity / NaN.  */
+double oracle_f16_value(uint16_t h)
+{
+    int sign = h >> 15;
+    int ef = (h >> 10) & 31;
+    int fr = h & 1023;
+    double mag;
+    if (ef == 31) mag = fr ? NAN : INFINITY;
+    else if (ef == 0) mag = ldexp((double)fr, -24);
+    else mag = ldexp(1024.0 + fr, ef - 25);
+    return sign ? -mag : mag;
+}
+
+static double f16_le(const uint8_t* p) { return oracle_f16_value((uint16_t)(p[0] | (p[1] << 8))); }
+
+#define Q8_0_BLOCK_BYTES 34
+#define Q4_K_BLOCK_BYTES 144
+
+/* Q8_0: per 32 elements, a little-endian binary16 scale d and 32 signed
+ * bytes q; element = d * q (exact in fp32: 11 by 8 significant bits).      */
+void oracle_dequant_q8_0(const uint8_t* blocks, int rows, int K, float* out)
+{
+    const size_t rb = (size_t)(K / 32) * Q8_0_BLOCK_BYTES;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < K / 32; ++b) {
+            const uint8_t* blk = blocks + r * rb + (size_t)b * Q8_0_BLOCK_BYTES;
+            double d = f16_le(blk);
+            for (int i = 0; i < 32; ++i)
+                out[(size_t)r * K + b * 32 + i] = (float)(d * (double)(int8_t)blk[2 + i]);
+        }
+}
+
+/* The 6-bit scale and min of sub-block j (0..7) from the 12 packed bytes
+ * p of a Q4_K super-block: sub-blocks 0-3 keep theirs in the low 6 bits of
+ * p[j] (scale) and p[j+4] (min); sub-blocks 4-7 keep their low 4 bits in
+ * the two nibbles of p[j+4] (scale low, min high) and their top 2 bits in
+ * the top 2 bits of p[j-4] (scale) and p[j] (min).                         */
+static void q4_k_scale_min(const uint8_t* p, int j, int* sc, int* m)
+{
+    if (j < 4) {
+        *sc = p[j] & 63;
+        *m = p[j + 4] & 63;
+    } else {
+        *sc = (p[j + 4] & 15) | ((p[j - 4] >> 6) << 4);
+        *m = (p[j + 4] >> 4) | ((p[j] >> 6) << 4);
+    }
+}
+
+/* Q4_K: per 256 elements (8 sub-blocks of 32), 144 bytes:
+ *   0-1 d, 2-3 dmin (little-endian binary16); 4-15 the packed 6-bit
+ *   scales and mins; 16-143 the 4-bit values: sub-blocks 2g and 2g+1 share
+ *   the 32 bytes 16+32g .. 16+32g+31, element l of sub-block 2g in the low
+ *   nibble of byte l, element l of sub-block 2g+1 in its high nibble.
+ * element = d*sc*q - dmin*m, rounded once to fp32.  d*sc and dmin*m are
+ * exact in fp32 (11 by 6 significant bits), so one fused multiply-add
+ * gives that single rounding.                                              */
+void oracle_dequant_q4_k(const uint8_t* blocks, int rows, int K, float* out)
+{
+    const size_t rb = (size_t)(K / 256) * Q4_K_BLOCK_BYTES;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < K / 256; ++b) {
+            const uint8_t* blk = blocks + r * rb + (size_t)b * Q4_K_BLOCK_BYTES;
+            double d = f16_le(blk), dmin = f16_le(blk + 2);
+            for (int j = 0; j < 8; ++j) {
+                int sc, m;
+                q4_k_scale_min(blk + 4, j, &sc, &m);
+                float dl = (float)(d * sc), ml = (float)(dmin * m);
+                const uint8_t* qs = blk + 16 + 32 * (j / 2);
+                for (int l = 0; l < 32; ++l) {
+                    int q = (j & 1) ? (qs[l] >> 4) : (qs[l] & 15);
+                    out[(size_t)r * K + b * 256 + j * 32 + l] = fmaf(dl, (float)q, -ml);
+                }
+            }
+        }
+}
+
+/* Bytes of one row of K elements in a GGUF format (0: Q8_0, 1: Q4_K), or 0
+ * when K does not fit the format's block.                                  */
+long oracle_gguf_row_bytes(int fmt, int K)
+{
+    if (K <= 0) return 0;
+    if (fmt == 0) return K % 32 ? 0 : (long)(K / 32) * Q8_0_BLOCK_BYTES;
+    if (fmt == 1) return K % 256 ? 0 : (long)(K / 256) * Q4_K_BLOCK_BYTES;
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -550,6 +646,110 @@ int oracle_layer(int prefill, int T, int H, int I, int k,
     if (!h_bf16) free(h);
     free(q);
     free(s);
+    return ORACLE_OK;
+}
+
+/* ---- whole decode layer on GGUF expert weights -------------------------- */
+
+typedef struct {
+    int H, I, n;           /* n assignments of the current expert            */
+    const int32_t* as;     /* their assignment indices a = t*k + j           */
+    int k;
+    const float *wg, *wu, *wd;  /* the expert's dequantised matrices         */
+    const float* xf;       /* [T][H] fp32 activations                        */
+    uint16_t* h;           /* [T*k][I]                                       */
+    float* hf;             /* [T*k][I]                                       */
+    float* y;              /* [T*k][H]                                       */
+} gguf_ctx;
+
+static void item_gguf_gateup(void* p, long item)
+{
+    gguf_ctx* c = (gguf_ctx*)p;
+    int a = c->as[item / c->I];
+    int r = (int)(item % c->I);
+    const float* x = c->xf + (size_t)(a / c->k) * c->H;
+    const float* gr = c->wg + (size_t)r * c->H;
+    const float* ur = c->wu + (size_t)r * c->H;
+    float g = 0.0f, u = 0.0f;
+    for (int i = 0; i < c->H; ++i) {
+        g = g + gr[i] * x[i];
+        u = u + ur[i] * x[i];
+    }
+    uint16_t hb = oracle_f32_to_bf16(silu_f32(g) * u);
+    c->h[(size_t)a * c->I + r] = hb;
+    c->hf[(size_t)a * c->I + r] = oracle_bf16_to_f32(hb);
+}
+
+static void item_gguf_down(void* p, long item)
+{
+    gguf_ctx* c = (gguf_ctx*)p;
+    int a = c->as[item / c->H];
+    int r = (int)(item % c->H);
+    const float* dr = c->wd + (size_t)r * c->I;
+    const float* hr = c->hf + (size_t)a * c->I;
+    float y = 0.0f;
+    for (int i = 0; i < c->I; ++i) y = y + dr[i] * hr[i];
+    c->y[(size_t)a * c->H + r] = y;
+}
+
+/* The decode path of oracle_layer on GGUF expert weights (fmt 0: Q8_0,
+ * 1: Q4_K): bf16 activations times the fp32-dequantised weights, products
+ * and sums in fp32 in ascending reduction index, h = bf16(silu(g)*u), and
+ * the combine in rank order.  Weights are stacked [E][rows][row bytes]:
+ * gate and up I rows of H elements, down H rows of I elements.  h_bf16
+ * [T*k][I] may be NULL.                                                    */
+int oracle_layer_gguf(int fmt, int T, int H, int I, int k, const uint16_t* x_bf16, const int32_t* ids,
+                      const float* w, const uint8_t* gate, const uint8_t* up, const uint8_t* down,
+                      int E, float* out, uint16_t* h_bf16, int threads)
+{
+    long rbh = oracle_gguf_row_bytes(fmt, H), rbi = oracle_gguf_row_bytes(fmt, I);
+    if (T < 0 || k <= 0 || E <= 0 || !rbh || !rbi) return ORACLE_ERR_INVALID;
+    size_t A = (size_t)T * k;
+    for (size_t a = 0; a < A; ++a)
+        if (ids[a] < 0 || ids[a] >= E) return ORACLE_ERR_INVALID;
+    void (*deq)(const uint8_t*, int, int, float*) = fmt == 0 ? oracle_dequant_q8_0 : oracle_dequant_q4_k;
+    float* xf = (float*)malloc(sizeof(float) * (size_t)T * H + 1);
+    float* wg = (float*)malloc(sizeof(float) * (size_t)I * H);
+    float* wu = (float*)malloc(sizeof(float) * (size_t)I * H);
+    float* wd = (float*)malloc(sizeof(float) * (size_t)H * I);
+    uint16_t* h = h_bf16 ? h_bf16 : (uint16_t*)malloc(sizeof(uint16_t) * A * I + 1);
+    float* hf = (float*)malloc(sizeof(float) * A * I + 1);
+    float* y = (float*)malloc(sizeof(float) * A * H + 1);
+    int32_t* as = (int32_t*)malloc(sizeof(int32_t) * A + 1);
+    for (size_t i = 0; i < (size_t)T * H; ++i) xf[i] = oracle_bf16_to_f32(x_bf16[i]);
+
+    for (int e = 0; e < E; ++e) {
+        int n = 0;
+        for (size_t a = 0; a < A; ++a)
+            if (ids[a] == e) as[n++] = (int32_t)a;
+        if (!n) continue;
+        const size_t eg = (size_t)I * rbh, ed = (size_t)H * rbi;
+        deq(gate + e * eg, I, H, wg);
+        deq(up + e * eg, I, H, wu);
+        deq(down + e * ed, H, I, wd);
+        gguf_ctx c = {H, I, n, as, k, wg, wu, wd, xf, h, hf, y};
+        parallel_for((long)n * I, threads, item_gguf_gateup, &c);
+        parallel_for((long)n * H, threads, item_gguf_down, &c);
+    }
+
+    for (int t = 0; t < T; ++t)
+        for (int r = 0; r < H; ++r) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                size_t a = (size_t)t * k + j;
+                acc = acc + w[a] * y[a * H + r];
+            }
+            out[(size_t)t * H + r] = acc;
+        }
+
+    free(xf);
+    free(wg);
+    free(wu);
+    free(wd);
+    if (!h_bf16) free(h);
+    free(hf);
+    free(y);
+    free(as);
     return ORACLE_OK;
 }
 
