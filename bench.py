@@ -319,6 +319,28 @@ def _pinned_link_peak(dev):
     return 3 * (1 << 30) / (a0.elapsed_time(b0) / 1e3) / 1e9
 
 
+def _store_link_rate(host, eb, dev, n=48):
+    """Copy rate from the expert store itself, GB/s: ``n`` whole experts
+    spread over the store, each one cudaMemcpyAsync into a device scratch
+    buffer, CUDA events.  Beside the fresh 1 GiB buffer of
+    ``_pinned_link_peak`` it shows whether the store's own pages copy
+    slower (a large pinned allocation need not get large pages)."""
+    import torch
+
+    count = host.numel() // eb
+    idx = np.linspace(0, count - 1, num=min(n, count)).astype(np.int64)
+    scratch = torch.empty(eb, dtype=torch.uint8, device=dev)
+    scratch.copy_(host[:eb], non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in idx:
+        scratch.copy_(host[int(i) * eb:(int(i) + 1) * eb], non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    return len(idx) * eb / (a.elapsed_time(b) / 1e3) / 1e9
+
+
 def staged_prefill_leg(args, wl):
     """Prefill of one layer through a pool of ``--prefill-slots`` slots (fewer
     than the routed experts), every expert in pinned host memory: per step,
@@ -342,6 +364,7 @@ def staged_prefill_leg(args, wl):
     slots = torch.empty(Sl * eb, dtype=torch.uint8, device=dev)
     pool = M.Pool(1, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy)
     link_peak = _pinned_link_peak(dev)
+    store_rate = _store_link_rate(host, eb, dev)
     G = 2  # two distinct input batches, alternated
     lg_pin = [torch.from_numpy(S.logits(wl, 0, g)).pin_memory() for g in range(G)]
     x_pin = [torch.from_numpy(S.activations_bf16_bits(wl, 0, g).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -396,6 +419,7 @@ def staged_prefill_leg(args, wl):
                                    "overlapping the previous window's grouped GEMMs",
                          "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
                          "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
+                         "store_copy_gbs": store_rate,
                          "traffic": None, "bytes_per_miss": h2d // max(1, misses)},
             "staging": {"unique_experts_per_step": uniq, "misses_per_step": misses / args.steps,
                         "hits": c1["hits"] - c0["hits"], "events_per_step": (c1["events"] - c0["events"]) / args.steps,
@@ -435,6 +459,7 @@ def offload_leg(args, wl):
                   stage_parts=args.stage_parts)
 
     link_peak = _pinned_link_peak(dev)
+    store_rate = _store_link_rate(host, eb, dev)
 
     G = args.warmup + args.steps
     lg_pin = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, g % wl.steps) for l in range(L)])
@@ -493,6 +518,7 @@ def offload_leg(args, wl):
             "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host",
                          "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
                          "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
+                         "store_copy_gbs": store_rate,
                          "traffic": None, "bytes_per_load": (c1["h2d_bytes"] - c0["h2d_bytes"]) //
                                                            max(1, c1["misses"] - c0["misses"] + c1["prefetches"] -
                                                                c0["prefetches"])},
