@@ -30,8 +30,9 @@ from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_FFN_ACCUMULATE, MOE_ERR_CAPACITY, 
 __all__ = [
     "moe_expert_bytes", "moe_pack_expert", "moe_route_workspace_bytes", "moe_route_plan", "moe_route_plan_noalloc",
     "moe_ffn_workspace_bytes", "alloc_ffn_workspace",
-    "moe_expert_ffn", "moe_decode_layer", "moe_combine", "moe_quant_mxfp8", "Pool", "RoutePlan", "MoeError", "lib", "status_str",
-    "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL",
+    "moe_expert_ffn", "moe_decode_layer", "moe_ffn_status", "moe_debug_stall_next_decode", "moe_combine",
+    "moe_quant_mxfp8", "moe_quant_mxfp4", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
+    "POLICIES", "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL", "MOE_FFN_ACCUMULATE",
 ]
 
 

@@ -31,6 +31,10 @@ def test_exports_every_declared_symbol():
     assert set(names) == set(_lib.SIGNATURES), set(names) ^ set(_lib.SIGNATURES)
 
 
+def test_python_names_exist():
+    assert all(hasattr(M, n) for n in M.__all__), [n for n in M.__all__ if not hasattr(M, n)]
+
+
 def test_status_strings_and_no_device_count():
     for s in [0, -1, -2, -3, -4, -5, -6]:
         assert M.status_str(s)
