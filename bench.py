@@ -1,18 +1,30 @@
 #!/usr/bin/env python
 """Benchmark of the routed-expert FFN layer on GB300.
 
-Default workload: GPT-OSS-20B-shaped decode with every expert resident --
+Headline (``value``): GPT-OSS-20B-shaped decode with every expert resident --
 24 stacked MoE layers (hidden 2880, expert intermediate 2880, 32 experts,
 top-4), one token per step, 768 distinct MXFP4 experts (10.2 GB) in the GPU
 slot pool.  One step = one token through all 24 layers: routing (top-k,
 softmax, histogram, permutation), the slot lookup, gate/up + SwiGLU, down,
 and the weighted combine.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
-the host cores on a bounded sample of the same workload instead.
+The same JSON line (one GPU) also carries the rest of the metric:
+  prefill  the 3072-token GPT-OSS-shaped and the 16384-token
+           Qwen-30B-A3B-shaped prefill layers (tcgen05 grouped GEMM), with
+           TFLOP/s against the measured rate of the MMA instruction they issue;
+  offload  the GPT-OSS-shaped decode through an 8-of-32-slot pool per layer
+           (LRU, skewed routing), end to end with the misses copied from
+           pinned host memory, against the pinned copy rate of this machine;
+  peaks    those measured denominators.
+Each part has its roofline, an end-to-end figure through the C ABI from
+pinned host buffers, and the CPU oracle timed on a bounded sample.
+
+``--impl reference`` times the CPU oracle on the host cores instead.
+``--workload 2|3|4`` prints the line of one of the other workloads alone.
 
 Multi-GPU: the layer does not shard in this form (one token's four experts);
-``--gpus N`` under torchrun runs N independent replicas and reports the sum.
+``--gpus N`` under torchrun runs N independent decode replicas and reports
+the sum (the prefill and offload parts are measured on one GPU only).
 """
 from __future__ import annotations
 
@@ -35,7 +47,6 @@ import moe_synth as S  # noqa: E402
 
 METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 roofline"
 
-
 # DRAM bytes per launch of the dominant kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum) from one ncu capture of the kernel as it is built
 # now; an entry goes back to None whenever that kernel changes.
@@ -47,6 +58,12 @@ NCU_TRAFFIC = {
     "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_057_856 + 30_262_784) + (232_777_984 + 29_761_536),
 }
 
+# Dense tensor-core rates of GB300 in the published ratios (bf16 : fp8 : fp4
+# = 2.25 : 4.5 : 13.5 PFLOP/s): the MXFP4 (kind::mxf4) rate is the measured
+# bf16 rate times 6.
+FP4_OVER_BF16 = 13.5 / 2.25
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -57,14 +74,15 @@ def _peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling (every ``interval_ms``) while a region runs."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, interval_ms: int = 50):
         self.idx = device_index
+        self.interval = interval_ms
         self.proc = None
         self.path = None
 
@@ -73,7 +91,7 @@ class Clocks:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -81,7 +99,7 @@ class Clocks:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -107,7 +125,7 @@ class Clocks:
                 if r[key].lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows),
+                "reasons": sorted(reasons), "samples": len(rows), "interval_ms": self.interval,
                 "power_w_max": max(r["power"] for r in rows)}
 
 
@@ -138,12 +156,33 @@ def _dist():
     return ws, rank, local
 
 
+def _events(n=2):
+    import torch
+
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _soak(fn, seconds: float):
+    """Run ``fn`` (enqueues GPU work) back to back for about ``seconds``."""
+    import torch
+
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds:
+        fn(n)
+        n += 1
+        if n % 8 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    return n, time.perf_counter() - t0
+
+
 # --------------------------------------------------------------------------
-# oracle leg (CPU baseline / reference arm)
+# oracle legs (CPU baseline / reference arm)
 # --------------------------------------------------------------------------
 
-def _oracle_token_sample(wl, step, layers, weights_cache, threads):
-    """Time the oracle on `layers` of one decode step; returns seconds."""
+def _oracle_decode_sample(wl, step, layers, weights_cache, threads):
+    """Time the oracle on ``layers`` of one decode step; returns seconds."""
     import oracle
 
     t0 = time.perf_counter()
@@ -156,19 +195,84 @@ def _oracle_token_sample(wl, step, layers, weights_cache, threads):
     return time.perf_counter() - t0
 
 
-def oracle_leg(wl, steps, layers_per_sample, threads):
-    layers = list(range(0, wl.layers, max(1, wl.layers // layers_per_sample)))[:layers_per_sample]
+def _sample_layers(wl, n):
+    return list(range(0, wl.layers, max(1, wl.layers // n)))[:n]
+
+
+def cpu_decode_baseline(wl, layers_per_sample, threads, steps=1):
+    """Oracle tokens/s on ``steps`` decode steps, ``layers_per_sample`` of
+    the 24 layers each, scaled to the whole stack."""
+    layers = _sample_layers(wl, layers_per_sample)
     cache = {l: S.stack_experts(S.layer_weights(wl, l)) for l in layers}
-    times = [_oracle_token_sample(wl, s, layers, cache, threads) for s in range(steps)]
+    times = [_oracle_decode_sample(wl, s, layers, cache, threads) for s in range(steps)]
     per_token = statistics.median(times) * wl.layers / len(layers)
-    return 1.0 / per_token, layers, times
+    return {"value": 1.0 / per_token, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{steps} decode step(s), {len(layers)} of {wl.layers} layers ({layers}), "
+                      f"scaled to {wl.layers} layers"}
+
+
+def cpu_offload_baseline(wl, layers_per_sample, threads):
+    """Oracle tokens/s of the offload workload: the layers of one step as in
+    the resident decode, plus the oracle's slot-pool simulation of every
+    layer's event of that step (the oracle keeps all experts in host memory,
+    so it has no copies)."""
+    import oracle
+
+    layers = _sample_layers(wl, layers_per_sample)
+    wsrc = S.WORKLOADS[wl.weight_wid]
+    cache = {l: S.stack_experts(S.layer_weights(wsrc, l)) for l in layers}
+    t0 = time.perf_counter()
+    pools = [oracle.LRUPool(wl.slots, wl.experts) for _ in range(wl.layers)]
+    for l in range(wl.layers):
+        ids, _ = oracle.route(S.logits(wl, l, 0), wl.top_k)
+        counts, _, _, _ = oracle.hist_perm(ids, wl.experts)
+        pools[l].step(counts)
+    t_pool = time.perf_counter() - t0
+    t_layers = _oracle_decode_sample(wl, 0, layers, cache, threads)
+    per_token = t_pool + t_layers * wl.layers / len(layers)
+    return {"value": 1.0 / per_token, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"1 step: the LRU simulation of all {wl.layers} layers' events and {len(layers)} of "
+                      f"{wl.layers} layers' expert FFN ({layers}), scaled to {wl.layers} layers"}
+
+
+def cpu_prefill_baseline(wl, tokens, threads):
+    """Oracle tokens/s of a prefill layer on the first ``tokens`` tokens
+    (routing of those tokens, then the layer on the MXFP8 path)."""
+    import oracle
+
+    ws = S.stack_experts(S.layer_weights(wl, 0))
+    lg = S.logits(wl, 0, 0)[:tokens]
+    x = S.activations_bf16_bits(wl, 0, 0)[:tokens]
+    t0 = time.perf_counter()
+    ids, w = oracle.route(lg, wl.top_k)
+    oracle.hist_perm(ids, wl.experts)
+    oracle.layer(x, ids, w, ws, prefill=True, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"the first {tokens} of {wl.tokens} tokens of the layer (routing + MXFP8 expert FFN)"}
 
 
 # --------------------------------------------------------------------------
-# GPU leg
+# GPU legs
 # --------------------------------------------------------------------------
 
-def gpu_leg(args, wl, rank, world):
+def build_host_store(M, wl, layers):
+    """Pinned host tensor [layers][E][expert_bytes] of packed experts."""
+    import torch
+
+    E, H, I = wl.experts, wl.hidden, wl.inter
+    eb = M.moe_expert_bytes(H, I)
+    host = torch.empty(layers * E * eb, dtype=torch.uint8).pin_memory()
+    src = S.WORKLOADS[wl.weight_wid]
+    for l in range(layers):
+        for e, w in enumerate(S.layer_weights(src, l)):
+            M.moe_pack_expert(w, H, I, host.data_ptr() + (l * E + e) * eb)
+    return host
+
+
+def gpu_decode_leg(args, wl, host, rank, world):
+    """The headline: per layer one moe_decode_layer(_acc) launch, each step's
+    24 launches captured in a CUDA graph of their own."""
     import torch
 
     import routed_expert_ffn_histogram_gb300 as M
@@ -176,12 +280,6 @@ def gpu_leg(args, wl, rank, world):
     dev = torch.device("cuda", torch.cuda.current_device())
     L, E, k, H, I = wl.layers, wl.experts, wl.top_k, wl.hidden, wl.inter
     eb = M.moe_expert_bytes(H, I)
-
-    # pinned host store of all experts (packed once), pool preloaded: resident
-    host = torch.empty(L * E * eb, dtype=torch.uint8).pin_memory()
-    for l in range(L):
-        for e, w in enumerate(S.layer_weights(wl, l)):
-            M.moe_pack_expert(w, H, I, host.data_ptr() + (l * E + e) * eb)
     slots = torch.empty(L * E * eb, dtype=torch.uint8, device=dev)
     pool = M.Pool(L, E, E, H, I, host_experts=host, dev_slots=slots, preload=True)
     slot_of = torch.arange(E, dtype=torch.int32, device=dev)
@@ -199,7 +297,6 @@ def gpu_leg(args, wl, rank, world):
     out_d = torch.zeros((G, 1 if residual else L, 1, H), dtype=torch.float32, device=dev)
     plan = M.RoutePlan.allocate(1, E, k, device=dev)
     ws = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
-
     stream = torch.cuda.Stream(device=dev)
 
     def step(g):
@@ -215,14 +312,12 @@ def gpu_leg(args, wl, rank, world):
     with torch.cuda.stream(stream):
         step(0)  # eager once before capture
     stream.synchronize()
-    out_d.zero_()  # every graph below runs once: a residual row starts at zero
     for g in range(G):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
             step(g)
         graphs.append(gr)
     torch.cuda.synchronize()
-
     for g in range(args.warmup):
         graphs[g].replay()
     torch.cuda.synchronize()
@@ -233,12 +328,20 @@ def gpu_leg(args, wl, rank, world):
         if world > 1:
             dist.barrier()
 
+    def replay(n):
+        with torch.cuda.stream(stream):
+            graphs[args.warmup + n % args.steps].replay()
+
+    # clocks are sampled over a soak of the same step graphs that encloses
+    # the timed region (about a second in all); the K timed steps start
+    # from outputs cleared after the first soak
     clocks = Clocks(torch.cuda.current_device())
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    soak_n, soak_s = _soak(replay, args.soak / 2)
+    out_d.zero_()
+    t_start, t_end = _events()
     barrier()
     torch.cuda.synchronize()
-    clocks.start()
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for g in range(args.warmup, G):
@@ -246,12 +349,10 @@ def gpu_leg(args, wl, rank, world):
         t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
+    graph_out = out_d.clone()
+    soak_n2, soak_s2 = _soak(replay, args.soak / 2)
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    # per-launch duration: the timed steps are back-to-back launches of the
-    # decode kernel on this stream, so step time / launches per step
-    ffn_ms = [elapsed_ms / args.steps / L]
-    route_ms = [0.0]
 
     # e2e through the public API, host buffers, copies inside the timed region
     lg_pin = lg_h.pin_memory()
@@ -278,8 +379,7 @@ def gpu_leg(args, wl, rank, world):
         for g in range(args.warmup):
             e2e_step(g)
         barrier()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+        a, b = _events()
         a.record(stream)
         for g in range(args.warmup, G):
             e2e_step(g)
@@ -289,15 +389,15 @@ def gpu_leg(args, wl, rank, world):
     e2e_ms = a.elapsed_time(b)
     # the graphed and eager runs produced the same outputs, up to the fp32
     # rounding order of the cross-CTA atomic sums
-    ref_o = out_d[args.warmup:].double()
+    ref_o = graph_out[args.warmup:].double()
     rel = float((out_pin[args.warmup:].to(dev).double() - ref_o).norm() / ref_o.norm().clamp_min(1e-30))
-    same = rel <= 1e-6
-
-    res = dict(elapsed_ms=elapsed_ms, ffn_ms=ffn_ms, route_ms=route_ms, clocks=clk, e2e_ms=e2e_ms,
+    res = dict(elapsed_ms=elapsed_ms, clocks=clk, e2e_ms=e2e_ms,
+               soak={"steps": soak_n + soak_n2, "seconds": soak_s + soak_s2},
                h2d=(lg_pin[0].numel() * 4 + x_pin[0].numel() * 2 + (res_in.numel() * 4 if residual else 0)),
-               d2h=out_pin[0].numel() * 4,
-               e2e_matches_graph=same, expert_bytes=eb)
+               d2h=out_pin[0].numel() * 4, e2e_matches_graph=rel <= 1e-6, expert_bytes=eb)
     pool.close()
+    del slots
+    torch.cuda.empty_cache()
     return res
 
 
@@ -310,7 +410,7 @@ def _pinned_link_peak(dev):
     probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
     probe_d.copy_(probe, non_blocking=True)
     torch.cuda.synchronize()
-    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0, b0 = _events()
     a0.record()
     for _ in range(3):
         probe_d.copy_(probe, non_blocking=True)
@@ -332,13 +432,330 @@ def _store_link_rate(host, eb, dev, n=48):
     scratch = torch.empty(eb, dtype=torch.uint8, device=dev)
     scratch.copy_(host[:eb], non_blocking=True)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a, b = _events()
     a.record()
     for i in idx:
         scratch.copy_(host[int(i) * eb:(int(i) + 1) * eb], non_blocking=True)
     b.record()
     torch.cuda.synchronize()
     return len(idx) * eb / (a.elapsed_time(b) / 1e3) / 1e9
+
+
+def measure_mma_peak(dev, seconds=1.0):
+    """Rate of tcgen05.mma.kind::mxf8f6f4 (M128 N256 K32, E4M3 x E2M1, E8M0
+    block scales), the instruction of the prefill GEMMs: the library's probe
+    (one CTA per SM issuing back-to-back MMAs on operands resident in shared
+    memory) timed with CUDA events.  Burst: best of five 4096-stage launches;
+    sustained: launches back to back for about ``seconds``."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stages = 4096
+    ctas = M.moe_probe_mxf8f6f4(stages, status)  # warm-up
+    torch.cuda.synchronize()
+    flops = ctas * stages * 4 * 2.0 * 128 * 256 * 32
+    best = 0.0
+    for _ in range(5):
+        a, b = _events()
+        a.record()
+        M.moe_probe_mxf8f6f4(stages, status)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, flops / (a.elapsed_time(b) / 1e3) / 1e12)
+    n = max(1, int(seconds / (flops / max(best, 1.0) / 1e12)))
+    a, b = _events()
+    a.record()
+    for _ in range(n):
+        M.moe_probe_mxf8f6f4(stages, status)
+    b.record()
+    torch.cuda.synchronize()
+    sustained = n * flops / (a.elapsed_time(b) / 1e3) / 1e12
+    if int(status.item()) != 0:
+        raise RuntimeError(f"tensor-core probe wait ran out (status {int(status.item())})")
+    return {"burst_tflops": best, "sustained_tflops": sustained, "ctas": ctas,
+            "how": "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale M128 N256 K32 back to back, operands in "
+                   "shared memory, one CTA per SM, CUDA events (moe_probe_mxf8f6f4)"}
+
+
+def offload_obj(args, wl, host, link_peak):
+    """The GPT-OSS-shaped decode with a small GPU pool (8 of 32 slots per
+    layer, skewed routing) and every expert in pinned host memory: per
+    layer, routing on the GPU, the routed experts' counts to the host, the
+    slot lookup and the copies of missed experts from pinned host memory on
+    a copy stream, then the decode FFN.  Timed end to end: each step's
+    logits and activations come from pinned host memory and its outputs go
+    back there."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L = wl.layers if args.layers is None else min(args.layers, wl.layers)
+    E, k, H, I, Sl = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.slots
+    eb = M.moe_expert_bytes(H, I)
+    slots = torch.empty(L * Sl * eb, dtype=torch.uint8, device=dev)
+    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy,
+                  stage_parts=args.stage_parts)
+    store_rate = _store_link_rate(host, eb, dev)
+    G = args.warmup + args.steps
+    lg_pin = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, g % wl.steps) for l in range(L)])
+                                        for g in range(G)])).pin_memory()
+    x_pin = torch.from_numpy(np.stack([np.stack([S.activations_bf16_bits(wl, l, g % wl.steps) for l in range(L)])
+                                       for g in range(G)]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_pin = torch.empty((G, L, 1, H), dtype=torch.float32).pin_memory()
+    lg_d = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
+    x_d = torch.empty((L, 1, H), dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty((L, 1, H), dtype=torch.float32, device=dev)
+    plan = M.RoutePlan.allocate(1, E, k, counts_host=True, device=dev)
+    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
+    ws = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
+    compute = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev)
+
+    def step(g):
+        lg_d.copy_(lg_pin[g], non_blocking=True)
+        x_d.copy_(x_pin[g], non_blocking=True)
+        for l in range(L):
+            M.moe_route_plan(lg_d[l], k, plan, stream=compute)
+            rc = pool.stage(l, plan.counts_host, slot_of, compute=compute, copy=copy)
+            if rc != M.MOE_OK:
+                raise RuntimeError(f"stage failed: {rc}")
+            if args.prefetch:
+                # the next layer's likely experts, copied while this layer computes
+                pool.prefetch((l + 1) % L, args.prefetch, compute=compute, copy=copy)
+            M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE, stream=compute)
+        out_pin[g].copy_(out_d, non_blocking=True)
+
+    with torch.cuda.stream(compute):
+        for g in range(args.warmup):
+            step(g)
+        compute.synchronize()
+        c0 = pool.counters()
+        clk = Clocks(torch.cuda.current_device())
+        clk.start()
+        a, b = _events()
+        t0 = time.perf_counter()
+        a.record(compute)
+        for g in range(args.warmup, G):
+            step(g)
+        b.record(compute)
+        compute.synchronize()
+        wall_ms = (time.perf_counter() - t0) / args.steps * 1e3
+        clocks = clk.stop()
+    c1 = pool.counters()
+    ms = a.elapsed_time(b) / args.steps
+    h2d = c1["h2d_bytes"] - c0["h2d_bytes"]
+    link = h2d / (ms * args.steps / 1e3) / 1e9
+    misses = c1["misses"] - c0["misses"]
+    obj = {"workload": wl.name, "value": 1e3 / ms, "unit": "tokens/s", "ms_per_step": ms,
+           "host_ms_per_step": wall_ms,
+           "config": {"layers": L, "hidden": H, "inter": I, "experts": E, "top_k": k, "slots_per_layer": Sl,
+                      "routing_bias": wl.bias_c, "policy": args.policy, "stage_parts": args.stage_parts,
+                      "prefetch": args.prefetch, "tokens_per_step": 1,
+                      "timing": "end to end through the C ABI: each step's logits and activations from pinned "
+                                "host memory, misses copied from the pinned expert store, outputs back to pinned "
+                                "host memory, CUDA events on the compute stream"},
+           "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host memory",
+                        "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
+                        "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
+                        "store_copy_gbs": store_rate, "traffic": None,
+                        "bytes_per_load": h2d // max(1, misses + c1["prefetches"] - c0["prefetches"])},
+           "staging": {"hits": c1["hits"] - c0["hits"], "misses": misses, "evictions": c1["evictions"] - c0["evictions"],
+                       "misses_per_step": misses / args.steps, "h2d_bytes": h2d,
+                       "prefetches": c1["prefetches"] - c0["prefetches"],
+                       "prefetch_hits": c1["prefetch_hits"] - c0["prefetch_hits"],
+                       "hit_rate": (c1["hits"] - c0["hits"]) / max(1, c1["hits"] - c0["hits"] + misses)},
+           "e2e": {"value": 1e3 / ms, "unit": "tokens/s",
+                   "h2d_bytes_per_step": (lg_pin[0].numel() * 4 + x_pin[0].numel() * 2) + h2d / args.steps,
+                   "d2h_bytes_per_step": out_pin[0].numel() * 4},
+           "gpu_launches": args.steps * L * 2,
+           "clocks": clocks}
+    pool.close()
+    del slots
+    torch.cuda.empty_cache()
+    return obj
+
+
+def _prefill_setup(M, wl, dev):
+    import torch
+
+    E, H, I = wl.experts, wl.hidden, wl.inter
+    eb = M.moe_expert_bytes(H, I)
+    host = torch.empty(E * eb, dtype=torch.uint8).pin_memory()
+    for e, w in enumerate(S.layer_weights(wl, 0)):
+        M.moe_pack_expert(w, H, I, host.data_ptr() + e * eb)
+    slots = torch.empty(E * eb, dtype=torch.uint8, device=dev)
+    pool = M.Pool(1, E, E, H, I, host_experts=host, dev_slots=slots, preload=True)
+    return host, slots, pool
+
+
+def prefill_timing(args, wl, soak_s=0.0):
+    """One prefill layer call per step: routing + grouped tcgen05 expert FFN
+    (the combine folded into the down GEMM's epilogue), graph-captured,
+    inputs resident in HBM, L2 flushed before every step.  Also the same
+    layer end to end through the C ABI from pinned host buffers (two
+    streams: step g + 1's inputs upload and step g - 1's output downloads
+    while step g computes)."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    E, k, H, I, T = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.tokens
+    host, slots, pool = _prefill_setup(M, wl, dev)
+    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
+    G = 2  # two distinct input batches, alternated
+    lg_h = [torch.from_numpy(S.logits(wl, 0, g)) for g in range(G)]
+    x_h = [torch.from_numpy(S.activations_bf16_bits(wl, 0, g).view(np.int16)).view(torch.bfloat16) for g in range(G)]
+    lg = [t.to(dev) for t in lg_h]
+    xb = [t.to(dev) for t in x_h]
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    plans = [M.RoutePlan.allocate(T, E, k, device=dev) for _ in range(G)]
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_PREFILL, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    ext = dict(enable_timing=True)
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext["external"] = True
+    except TypeError:
+        pass
+    ev = [(torch.cuda.Event(**ext), torch.cuda.Event(**ext), torch.cuda.Event(**ext)) for _ in range(G)]
+    residual = args.output == "residual"
+
+    def step(g):
+        e0, e1, e2 = ev[g]
+        flush.fill_(g)  # larger than L2: every step starts from a cold L2
+        e0.record(stream)
+        M.moe_route_plan(lg[g], k, plans[g], stream=stream, with_counts_host=False)
+        e1.record(stream)
+        M.moe_expert_ffn(pool, 0, xb[g], plans[g], slot_of, out, ws, path=M.MOE_PATH_PREFILL, stream=stream,
+                         accumulate=residual)
+        e2.record(stream)
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    graphs = []
+    for g in range(G):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(g)
+        graphs.append(gr)
+    for i in range(args.warmup):
+        graphs[i % G].replay()
+    torch.cuda.synchronize()
+    route_ms, ffn_ms = [], []
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    soak_n = 0
+    if soak_s > 0:
+        soak_n, _ = _soak(lambda n: graphs[n % G].replay(), soak_s)
+    total = 0.0
+    for i in range(args.steps):
+        graphs[i % G].replay()
+        torch.cuda.synchronize()
+        e0, e1, e2 = ev[i % G]
+        route_ms.append(e0.elapsed_time(e1))
+        ffn_ms.append(e1.elapsed_time(e2))
+        total += e0.elapsed_time(e2)
+    clk = clocks.stop()
+    res = dict(step_ms=total / args.steps, route_ms=route_ms, ffn_ms=ffn_ms, clocks=clk, soak_steps=soak_n)
+
+    # end to end through the C ABI
+    lg_pin = [t.pin_memory() for t in lg_h]
+    x_pin = [t.pin_memory() for t in x_h]
+    out_pin = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in range(2)]
+    lg_dev = [torch.empty((T, E), dtype=torch.float32, device=dev) for _ in range(2)]
+    x_dev = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    out_dev = [torch.empty((T, H), dtype=torch.float32, device=dev) for _ in range(2)]
+    compute = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev)
+    up_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
+    n_steps = args.warmup + args.steps
+
+    def upload(g):
+        b = g % 2
+        with torch.cuda.stream(copy):
+            copy.wait_event(comp_done[b]) if g >= 2 else None
+            lg_dev[b].copy_(lg_pin[g % G], non_blocking=True)
+            x_dev[b].copy_(x_pin[g % G], non_blocking=True)
+            up_done[b].record(copy)
+
+    def run(g):
+        b = g % 2
+        compute.wait_event(up_done[b])
+        if g >= 2:
+            compute.wait_event(down_done[b])  # out_dev[b] read back
+        M.moe_route_plan(lg_dev[b], k, plans[b], stream=compute, with_counts_host=False)
+        M.moe_expert_ffn(pool, 0, x_dev[b], plans[b], slot_of, out_dev[b], ws, path=M.MOE_PATH_PREFILL,
+                         stream=compute)
+        comp_done[b].record(compute)
+        with torch.cuda.stream(copy):
+            copy.wait_event(comp_done[b])
+            out_pin[b].copy_(out_dev[b], non_blocking=True)
+            down_done[b].record(copy)
+
+    def e2e_run(n):
+        upload(0)
+        for g in range(n):
+            if g + 1 < n:
+                upload(g + 1)
+            run(g)
+        torch.cuda.synchronize()
+
+    e2e_run(args.warmup)
+    t0 = time.perf_counter()
+    e2e_run(args.steps)
+    e2e_ms = (time.perf_counter() - t0) / args.steps * 1e3
+    res.update(e2e_ms=e2e_ms, h2d=lg_pin[0].numel() * 4 + x_pin[0].numel() * 2, d2h=out_pin[0].numel() * 4)
+    pool.close()
+    del slots, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_obj(args, wl, mma, threads, cpu=True):
+    res = prefill_timing(args, wl, soak_s=args.soak / 2)
+    flops = 6.0 * wl.hidden * wl.inter * wl.tokens * wl.top_k
+    ffn_s = statistics.median(res["ffn_ms"]) / 1e3
+    achieved = flops / ffn_s / 1e12
+    _, bf16_peak, peak_kind = _peaks()
+    fp4_peak = bf16_peak * FP4_OVER_BF16
+    obj = {"workload": wl.name, "value": wl.tokens / (res["step_ms"] / 1e3), "unit": "tokens/s",
+           "ms_per_step": res["step_ms"], "dtype": "mxf8f6f4->f32",
+           "config": {"hidden": wl.hidden, "inter": wl.inter, "experts": wl.experts, "top_k": wl.top_k,
+                      "tokens": wl.tokens, "l2": "256 MB flush before every step",
+                      "output": ("added into a residual stream (MOE_FFN_ACCUMULATE)" if args.output == "residual"
+                                 else "overwritten (out zeroed, then the combine adds into it)")},
+           "roofline": {"kernel": "prefill expert FFN (MXFP8 quant, gate/up GEMM, down GEMM with the combine in "
+                                  "its epilogue)",
+                        "bound": "tensor", "achieved": achieved, "peak": mma["burst_tflops"], "unit": "TFLOP/s",
+                        "frac": achieved / mma["burst_tflops"],
+                        "peak_kind": "measured rate of tcgen05.mma kind::mxf8f6f4 on this GPU (peaks.mxf8f6f4)",
+                        "frac_of_mxfp4_peak": achieved / fp4_peak,
+                        "mxfp4_peak": fp4_peak,
+                        "mxfp4_peak_kind": f"{peak_kind} bf16 x {FP4_OVER_BF16:g} (published dense ratio); the "
+                                           "kind::mxf4 MMA is not built, so it is not measured",
+                        "traffic": NCU_TRAFFIC.get("grouped_gemm_tc_kernel/" + wl.name),
+                        "traffic_scope": "DRAM bytes of the two GEMM launches of one layer",
+                        "algorithmic_flops_per_launch": flops, "avg_launch_us": ffn_s * 1e6},
+           "kernels_us": {"route_plan": statistics.median(res["route_ms"]) * 1e3, "expert_ffn": ffn_s * 1e6},
+           "e2e": {"value": wl.tokens / (res["e2e_ms"] / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
+                   "d2h_bytes_per_step": res["d2h"],
+                   "how": "moe_route_plan + moe_expert_ffn through the C ABI; logits and x from pinned host memory, "
+                          "out back to pinned host memory, uploads and read-backs on a second stream overlapping "
+                          "the neighbouring steps' compute; host clock over the steps"},
+           # per step: routing (top-k and scatter passes), quantisation, two GEMMs
+           "gpu_launches": args.steps * 5,
+           "clocks": res["clocks"]}
+    if cpu:
+        obj["cpu_baseline"] = cpu_prefill_baseline(wl, args.cpu_prefill_tokens.get(wl.wid, 32), threads)
+    return obj
 
 
 def staged_prefill_leg(args, wl):
@@ -348,8 +765,6 @@ def staged_prefill_leg(args, wl):
     staged on a copy stream while the previous window's grouped GEMMs run).
     Timed end to end on the host clock and by CUDA events on the compute
     stream: x and logits come from pinned host memory, out goes back there."""
-    import time
-
     import torch
 
     import routed_expert_ffn_histogram_gb300 as M
@@ -393,8 +808,7 @@ def staged_prefill_leg(args, wl):
         c0 = pool.counters()
         clk = Clocks(torch.cuda.current_device())
         clk.start()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+        a, b = _events()
         t0 = time.perf_counter()
         a.record(compute)
         for g in range(args.steps):
@@ -433,111 +847,6 @@ def staged_prefill_leg(args, wl):
     print(json.dumps(line))
 
 
-def offload_leg(args, wl):
-    """The GPT-OSS-shaped decode with a small GPU pool (8 of 32 slots per
-    layer, LRU, skewed routing) and every expert in pinned host memory: per
-    layer, routing on the GPU, the routed experts' counts to the host, the
-    slot lookup and the copies of missed experts from pinned host memory on
-    a copy stream, then the decode FFN.  Timed end to end: each step's
-    logits and activations come from pinned host memory and its outputs go
-    back there."""
-    import torch
-
-    import routed_expert_ffn_histogram_gb300 as M
-
-    dev = torch.device("cuda", torch.cuda.current_device())
-    L = wl.layers if args.layers is None else min(args.layers, wl.layers)
-    E, k, H, I, Sl = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.slots
-    eb = M.moe_expert_bytes(H, I)
-    wsrc = S.WORKLOADS[wl.weight_wid]
-    host = torch.empty(L * E * eb, dtype=torch.uint8).pin_memory()
-    for l in range(L):
-        for e, w in enumerate(S.layer_weights(wsrc, l)):
-            M.moe_pack_expert(w, H, I, host.data_ptr() + (l * E + e) * eb)
-    slots = torch.empty(L * Sl * eb, dtype=torch.uint8, device=dev)
-    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy,
-                  stage_parts=args.stage_parts)
-
-    link_peak = _pinned_link_peak(dev)
-    store_rate = _store_link_rate(host, eb, dev)
-
-    G = args.warmup + args.steps
-    lg_pin = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, g % wl.steps) for l in range(L)])
-                                        for g in range(G)])).pin_memory()
-    x_pin = torch.from_numpy(np.stack([np.stack([S.activations_bf16_bits(wl, l, g % wl.steps) for l in range(L)])
-                                       for g in range(G)]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    out_pin = torch.empty((G, L, 1, H), dtype=torch.float32).pin_memory()
-    lg_d = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
-    x_d = torch.empty((L, 1, H), dtype=torch.bfloat16, device=dev)
-    out_d = torch.empty((L, 1, H), dtype=torch.float32, device=dev)
-    plan = M.RoutePlan.allocate(1, E, k, counts_host=True, device=dev)
-    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
-    ws = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
-    compute = torch.cuda.Stream(device=dev)
-    copy = torch.cuda.Stream(device=dev)
-
-    def step(g):
-        lg_d.copy_(lg_pin[g], non_blocking=True)
-        x_d.copy_(x_pin[g], non_blocking=True)
-        for l in range(L):
-            M.moe_route_plan(lg_d[l], k, plan, stream=compute)
-            rc = pool.stage(l, plan.counts_host, slot_of, compute=compute, copy=copy)
-            if rc != M.MOE_OK:
-                raise RuntimeError(f"stage failed: {rc}")
-            if args.prefetch:
-                # the next layer's likely experts, copied while this layer computes
-                pool.prefetch((l + 1) % L, args.prefetch, compute=compute, copy=copy)
-            M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE, stream=compute)
-        out_pin[g].copy_(out_d, non_blocking=True)
-
-    with torch.cuda.stream(compute):
-        for g in range(args.warmup):
-            step(g)
-        compute.synchronize()
-        c0 = pool.counters()
-        clk = Clocks(torch.cuda.current_device())
-        clk.start()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(compute)
-        for g in range(args.warmup, G):
-            step(g)
-        b.record(compute)
-        compute.synchronize()
-        clocks = clk.stop()
-    c1 = pool.counters()
-    ms = a.elapsed_time(b) / args.steps
-    h2d = c1["h2d_bytes"] - c0["h2d_bytes"]
-    link = h2d / (ms * args.steps / 1e3) / 1e9
-    line = {"metric": METRIC, "value": 1e3 / ms, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "layers": L, "hidden": H, "inter": I, "experts": E, "top_k": k,
-                       "slots_per_layer": Sl, "routing_bias": wl.bias_c, "tokens_per_step": 1,
-                       "timing": "end to end: inputs from and outputs to pinned host memory every step"},
-            "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host",
-                         "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
-                         "frac": link / link_peak, "peak_kind": "pinned H2D copy measured in this run",
-                         "store_copy_gbs": store_rate,
-                         "traffic": None, "bytes_per_load": (c1["h2d_bytes"] - c0["h2d_bytes"]) //
-                                                           max(1, c1["misses"] - c0["misses"] + c1["prefetches"] -
-                                                               c0["prefetches"])},
-            "offload": {"policy": args.policy, "stage_parts": args.stage_parts, "prefetch": args.prefetch,
-                        "prefetches": c1["prefetches"] - c0["prefetches"],
-                        "prefetch_hits": c1["prefetch_hits"] - c0["prefetch_hits"],
-                        "hits": c1["hits"] - c0["hits"], "misses": c1["misses"] - c0["misses"],
-                        "evictions": c1["evictions"] - c0["evictions"], "h2d_bytes": h2d,
-                        "misses_per_step": (c1["misses"] - c0["misses"]) / args.steps},
-            "e2e": {"value": 1e3 / ms, "unit": "tokens/s",
-                    "h2d_bytes_per_step": (lg_pin[0].numel() * 4 + x_pin[0].numel() * 2) + h2d / args.steps,
-                    "d2h_bytes_per_step": out_pin[0].numel() * 4},
-            "gpu_launches": args.steps * L * 2,
-            "clocks": clocks}
-    if args.policy_sweep:
-        line["policy_sweep"] = policy_sweep(wl, L, dev)
-    print(json.dumps(line))
-
-
 def policy_sweep(wl, L, dev):
     """Every (step, layer) routing event of the offload workload, routed on
     the GPU once, replayed through a policy-only pool (no copies) for each
@@ -568,76 +877,55 @@ def policy_sweep(wl, L, dev):
     return {"events": len(events), "steps": wl.steps, "layers": L, "policies": out}
 
 
-def prefill_leg(args, wl):
-    """One prefill layer call per step: routing + grouped tcgen05 expert FFN
-    (the combine folded into the down GEMM's epilogue), graph-captured,
-    inputs resident in HBM."""
-    import torch
+def _standalone_line(obj, args):
+    """One workload's sub-object as a line of its own (``--workload N``)."""
+    line = {"metric": METRIC, "value": obj["value"], "unit": obj["unit"], "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": obj["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": obj.get("dtype", "f32"), "data": "synthetic",
+            "config": dict(workload=obj["workload"], **obj["config"])}
+    for key in ("roofline", "kernels_us", "staging", "e2e", "gpu_launches", "clocks", "cpu_baseline"):
+        if key in obj:
+            line[key] = obj[key]
+    return line
 
-    import routed_expert_ffn_histogram_gb300 as M
 
-    dev = torch.device("cuda", torch.cuda.current_device())
-    E, k, H, I, T = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.tokens
-    eb = M.moe_expert_bytes(H, I)
-    host = torch.empty(E * eb, dtype=torch.uint8).pin_memory()
-    for e, w in enumerate(S.layer_weights(wl, 0)):
-        M.moe_pack_expert(w, H, I, host.data_ptr() + e * eb)
-    slots = torch.empty(E * eb, dtype=torch.uint8, device=dev)
-    pool = M.Pool(1, E, E, H, I, host_experts=host, dev_slots=slots, preload=True)
-    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
-    G = 2  # two distinct input batches, alternated
-    lg = [torch.from_numpy(S.logits(wl, 0, g)).to(dev) for g in range(G)]
-    xb = [torch.from_numpy(S.activations_bf16_bits(wl, 0, g).view(np.int16)).to(dev).view(torch.bfloat16)
-          for g in range(G)]
-    out = torch.empty((T, H), dtype=torch.float32, device=dev)
-    plans = [M.RoutePlan.allocate(T, E, k, device=dev) for _ in range(G)]
-    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_PREFILL, device=dev)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-    ext = dict(enable_timing=True)
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        ext["external"] = True
-    except TypeError:
-        pass
-    ev = [(torch.cuda.Event(**ext), torch.cuda.Event(**ext), torch.cuda.Event(**ext)) for _ in range(G)]
+def reference_arm(args, wl, threads, rank):
+    """The CPU oracle as it stands, on the host cores: every step is one
+    decode token through a sample of ``--cpu-layers`` of the 24 layers (the
+    same layers each step, distinct tokens), timed on the host clock; the
+    value is tokens/s of that sample (a step is that fraction of a token)."""
+    if rank != 0:
+        return
+    import oracle
 
-    def step(g):
-        e0, e1, e2 = ev[g]
-        flush.fill_(g)  # larger than L2: every step starts from a cold L2
-        e0.record(stream)
-        M.moe_route_plan(lg[g], k, plans[g], stream=stream, with_counts_host=False)
-        e1.record(stream)
-        M.moe_expert_ffn(pool, 0, xb[g], plans[g], slot_of, out, ws, path=M.MOE_PATH_PREFILL, stream=stream,
-                         accumulate=args.output == "residual")
-        e2.record(stream)
+    oracle.build()
+    layers = _sample_layers(wl, args.cpu_layers)
+    cache = {l: S.stack_experts(S.layer_weights(wl, l)) for l in layers}
+    times = [_oracle_decode_sample(wl, s % wl.steps, layers, cache, threads)
+             for s in range(args.warmup + args.steps)]
+    timed = times[args.warmup:]
+    ms_step = statistics.mean(timed) * 1e3
+    frac = len(layers) / wl.layers
+    v = frac / (ms_step / 1e3)
+    sample = (f"each step: 1 decode token through {len(layers)} of {wl.layers} layers (layers {layers}), i.e. "
+              f"{frac:.4g} of a token; value = that fraction over the step time")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": _decode_config(wl, args, 1),
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
 
-    with torch.cuda.stream(stream):
-        step(0)
-    stream.synchronize()
-    graphs = []
-    for g in range(G):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=stream):
-            step(g)
-        graphs.append(gr)
-    for i in range(args.warmup):
-        graphs[i % G].replay()
-    torch.cuda.synchronize()
-    route_ms, ffn_ms = [], []
-    clocks = Clocks(torch.cuda.current_device())
-    clocks.start()
-    total = 0.0
-    for i in range(args.steps):
-        graphs[i % G].replay()
-        torch.cuda.synchronize()
-        e0, e1, e2 = ev[i % G]
-        route_ms.append(e0.elapsed_time(e1))
-        ffn_ms.append(e1.elapsed_time(e2))
-        total += e0.elapsed_time(e2)
-    clk = clocks.stop()
-    pool.close()
-    return dict(step_ms=total / args.steps, route_ms=route_ms, ffn_ms=ffn_ms, clocks=clk)
+
+def _decode_config(wl, args, world):
+    return {"workload": wl.name, "layers": wl.layers, "hidden": wl.hidden, "inter": wl.inter,
+            "experts": wl.experts, "top_k": wl.top_k, "tokens_per_step": 1,
+            "resident_experts": wl.layers * wl.experts,
+            "l2": "inputs larger than L2: each step reads 96 distinct experts (1.27 GB) of a 10.2 GB set",
+            "output": ("each layer adds into the step's residual row (moe_decode_layer_acc)"
+                       if args.output == "residual" else "each layer overwrites its own output (moe_decode_layer)"),
+            "parallelism": f"replicas{world}"}
 
 
 def main():
@@ -646,18 +934,22 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-layers", type=int, default=4, help="layers per oracle sample")
+    ap.add_argument("--cpu-layers", type=int, default=4, help="layers per oracle decode sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="default run: skip the prefill, offload and peak parts")
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of back-to-back steps around each timed region while clocks are sampled")
     ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3, 4],
-                    help="1: GPT-OSS decode (default); 2: the same with an 8-slot offload pool; "
-                         "3, 4: prefill layers (extra measurements)")
+                    help="1: the default line (decode headline + prefill/offload parts); 2, 3, 4: one line for "
+                         "that workload alone")
     ap.add_argument("--policy", default="lru", choices=["lru", "fifo", "lfu", "lfru", "slru"],
-                    help="eviction policy of the offload pool (--workload 2)")
+                    help="eviction policy of the offload pool (workload 2)")
     ap.add_argument("--stage-parts", default="whole", choices=["whole", "decode"],
-                    help="--workload 2: copy whole experts, or only what the decode kernel reads")
+                    help="workload 2: copy whole experts, or only what the decode kernel reads")
     ap.add_argument("--output", default="residual", choices=["residual", "overwrite"],
                     help="decode: each layer adds into the step's residual row (moe_decode_layer_acc) or "
-                         "overwrites its own output (moe_decode_layer)")
+                         "overwrites its own output (moe_decode_layer); prefill: out += or out =")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="workload 2: after each layer's staging, prefetch up to this many experts of the next layer")
     ap.add_argument("--prefill-slots", type=int, default=None,
@@ -670,85 +962,14 @@ def main():
                     help="run only the first N layers (smaller case for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    # oracle samples of the prefill workloads: tokens of the layer (about
+    # 10 s of CPU work each on 16 cores)
+    args.cpu_prefill_tokens = {3: 48, 4: 96}
     world, rank, local = _dist()
-    wl = S.WORKLOADS[args.workload]
-    if args.workload == 2:
-        import torch
-
-        torch.cuda.set_device(0)
-        from routed_expert_ffn_histogram_gb300 import build as B
-
-        B.build()
-        offload_leg(args, wl)
-        return
-    if args.workload in (3, 4):
-        import torch
-
-        torch.cuda.set_device(0)
-        from routed_expert_ffn_histogram_gb300 import build as B
-
-        B.build()
-        if args.prefill_slots:
-            staged_prefill_leg(args, wl)
-            return
-        res = prefill_leg(args, wl)
-        flops = 6.0 * wl.hidden * wl.inter * wl.tokens * wl.top_k
-        ffn_s = statistics.median(res["ffn_ms"]) / 1e3
-        _, bf16_peak, peak_kind = _peaks()
-        tc_peak = bf16_peak * 2.0  # kind::mxf8f6f4 issues at the FP8 rate: 2x the measured bf16 rate
-        achieved = flops / ffn_s / 1e12
-        line = {"metric": METRIC, "value": wl.tokens / (res["step_ms"] / 1e3), "unit": "tokens/s", "n_gpus": 1,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["step_ms"],
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxf8f6f4->f32",
-                "data": "synthetic",
-                "config": {"workload": wl.name, "hidden": wl.hidden, "inter": wl.inter, "experts": wl.experts,
-                           "top_k": wl.top_k, "tokens": wl.tokens, "l2": "256 MB flush before every step",
-                           "output": ("added into a residual stream (MOE_FFN_ACCUMULATE)" if args.output == "residual"
-                                      else "overwritten (out zeroed, then the combine adds into it)")},
-                "roofline": {"kernel": "prefill expert FFN (MXFP8 quant, gate/up GEMM, down GEMM with the combine in its epilogue)",
-                             "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                             "frac": achieved / tc_peak, "peak_kind": peak_kind + " bf16 x 2 (FP8-class rate)",
-                             "traffic": NCU_TRAFFIC.get("grouped_gemm_tc_kernel/" + wl.name),
-                             "traffic_scope": "DRAM bytes of the two GEMM launches of one layer",
-                             "algorithmic_flops_per_launch": flops,
-                             "avg_launch_us": ffn_s * 1e6},
-                "kernels_us": {"route_plan": statistics.median(res["route_ms"]) * 1e3,
-                               "expert_ffn": ffn_s * 1e6},
-                "clocks": res["clocks"]}
-        print(json.dumps(line))
-        return
-    if args.layers:
-        import dataclasses
-
-        wl = dataclasses.replace(wl, layers=min(args.layers, wl.layers))
-    hbm_peak, _, peak_kind = _peaks()
-    workload = {"workload": wl.name, "layers": wl.layers, "hidden": wl.hidden, "inter": wl.inter,
-                "experts": wl.experts, "top_k": wl.top_k, "tokens_per_step": 1,
-                "resident_experts": wl.layers * wl.experts,
-                "l2": "inputs larger than L2: each step reads 96 distinct experts (1.27 GB) of a 10.2 GB set",
-                "output": ("each layer adds into the step's residual row (moe_decode_layer_acc)"
-                           if args.output == "residual" else "each layer overwrites its own output (moe_decode_layer)"),
-                "parallelism": f"replicas{world}"}
     threads = os.cpu_count() or 1
+    wl = S.WORKLOADS[args.workload]
     if args.impl == "reference":
-        if rank != 0:
-            return
-        import oracle
-
-        oracle.build()
-        tps, layers, times = oracle_leg(wl, args.warmup + args.steps, args.cpu_layers, threads)
-        timed = times[args.warmup:]
-        per_token = statistics.median(timed) * wl.layers / len(layers)
-        v = 1.0 / per_token
-        sample = f"{len(layers)} of {wl.layers} layers per step (layers {layers}), scaled to {wl.layers} layers"
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_token * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-                "data": "synthetic", "config": workload,
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                 "sample": sample},
-                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        reference_arm(args, S.WORKLOADS[1], threads, rank)
         return
 
     import torch
@@ -763,19 +984,48 @@ def main():
     from routed_expert_ffn_histogram_gb300 import build as B
 
     B.build()
-    res = gpu_leg(args, wl, rank, world)
+    import routed_expert_ffn_histogram_gb300 as M
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if args.workload == 2:
+        host = build_host_store(M, wl, wl.layers if args.layers is None else min(args.layers, wl.layers))
+        obj = offload_obj(args, wl, host, _pinned_link_peak(dev))
+        line = _standalone_line(obj, args)
+        if args.policy_sweep:
+            line["policy_sweep"] = policy_sweep(wl, obj["config"]["layers"], dev)
+        print(json.dumps(line))
+        return
+    if args.workload in (3, 4):
+        if args.prefill_slots:
+            staged_prefill_leg(args, wl)
+            return
+        mma = measure_mma_peak(dev)
+        obj = prefill_obj(args, wl, mma, threads, cpu=not args.no_cpu_baseline)
+        line = _standalone_line(obj, args)
+        line["peaks"] = {"mxf8f6f4": mma}
+        print(json.dumps(line))
+        return
+
+    # ---- the default line: decode headline, then the other parts ----
+    if args.layers:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, layers=min(args.layers, wl.layers))
+    hbm_peak, _, peak_kind = _peaks()
+    host = build_host_store(M, wl, wl.layers)
+    res = gpu_decode_leg(args, wl, host, rank, world)
     ms = res["elapsed_ms"] / args.steps
     e2e_ms = res["e2e_ms"] / args.steps
     ms, e2e_ms = reduce_max_over_ranks([ms, e2e_ms], world, device="cuda")
-    if rank != 0:
-        return
-    value = world * 1e3 / ms
     layer_bytes = wl.top_k * 3 * (wl.hidden * wl.inter // 2 + wl.hidden * wl.inter // 32)
-    ffn_avg_s = statistics.mean(res["ffn_ms"]) / 1e3
-    achieved = layer_bytes / ffn_avg_s / 1e9
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    # per-launch duration: the timed steps are back-to-back launches of the
+    # decode kernel on this stream (one CUDA graph per step), so step time /
+    # launches per step
+    launch_s = ms / 1e3 / wl.layers
+    achieved = layer_bytes / launch_s / 1e9
+    line = {"metric": METRIC, "value": world * 1e3 / ms, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload,
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": _decode_config(wl, args, world),
             "formats": "weights MXFP4 (E2M1 + E8M0 per 32), activations bf16, fp32 accumulation",
             "roofline": {"kernel": "decode_fused_kernel: one launch per layer (routing, gate/up+SwiGLU, "
                                    "down+combine)",
@@ -783,21 +1033,38 @@ def main():
                          "frac": achieved / hbm_peak, "peak_kind": peak_kind,
                          "traffic": NCU_TRAFFIC["decode_fused_kernel"],
                          "algorithmic_bytes_per_launch": layer_bytes,
-                         "avg_launch_us": ffn_avg_s * 1e6},
-            "kernels_us": {"decode_layer": ffn_avg_s * 1e6},
+                         "avg_launch_us": launch_s * 1e6},
+            "kernels_us": {"decode_layer": launch_s * 1e6},
             "e2e": {"value": world * 1e3 / e2e_ms, "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"], "matches_graph_outputs": res["e2e_matches_graph"]},
             "gpu_launches": args.steps * wl.layers,
-            "clocks": res["clocks"]}
-    if not args.no_cpu_baseline:
+            "clocks": dict(res["clocks"] or {}, window="sampled over a soak of the same step graphs "
+                                                       f"({res['soak']['steps']} steps, "
+                                                       f"{res['soak']['seconds']:.2f} s) enclosing the timed region")
+            if res["clocks"] else None}
+    if not args.no_cpu_baseline and rank == 0:
         import oracle
 
         oracle.build()
-        tps, layers, times = oracle_leg(wl, 1, args.cpu_layers, threads)
-        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                "sample": f"1 decode step, {len(layers)} of {wl.layers} layers "
-                                          f"({layers}), scaled to {wl.layers} layers"}
-    print(json.dumps(line))
+        line["cpu_baseline"] = cpu_decode_baseline(wl, args.cpu_layers, threads, steps=2)
+    if world == 1 and not args.decode_only and args.layers is None:
+        mma = measure_mma_peak(dev)
+        link_peak = _pinned_link_peak(dev)
+        line["peaks"] = {"mxf8f6f4": mma, "pinned_h2d_gbs": link_peak,
+                         "hbm_gbs": hbm_peak, "hbm_kind": peak_kind,
+                         "mxfp4_tflops": _peaks()[1] * FP4_OVER_BF16,
+                         "mxfp4_kind": "measured bf16 x 6 (published dense ratio; kind::mxf4 not built)"}
+        line["prefill"] = {}
+        for wid in (3, 4):
+            pw = S.WORKLOADS[wid]
+            line["prefill"][pw.name] = prefill_obj(args, pw, mma, threads, cpu=not args.no_cpu_baseline)
+        ow = S.WORKLOADS[2]
+        off = offload_obj(args, ow, host, link_peak)
+        if not args.no_cpu_baseline:
+            off["cpu_baseline"] = cpu_offload_baseline(ow, args.cpu_layers, threads)
+        line["offload"] = {ow.name: off}
+    if rank == 0:
+        print(json.dumps(line))
 
 
 if __name__ == "__main__":

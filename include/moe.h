@@ -485,6 +485,28 @@ MOE_API int moe_quant_mxfp8(const void* x_bf16, int K, const int32_t* perm, int 
 MOE_API int moe_quant_mxfp4(const void* x_bf16, int K, int rows, uint8_t* q, uint8_t* scales,
                             int scale_stride, moe_stream_t stream);
 
+
+/* ------------------------------------------------------------------------ */
+/* Measurement                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Peak-rate probe of the tensor-core instruction the prefill GEMMs issue
+ * (tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X, M 128,
+ * N 256, K 32; E4M3 A and E2M1 B operands in shared memory, E8M0 scale
+ * factors in tensor memory).  The pages have no counterpart: it gives the
+ * roofline denominator of the prefill path.  One CTA per SM issues
+ * stages x 4 such MMAs back to back on operands that stay in shared memory
+ * (no global reads), so the launch's duration, timed by the caller with
+ * CUDA events on `stream`, gives the instruction's rate:
+ *   FLOPs per launch = ctas * stages * 4 * 2 * 128 * 256 * 32.
+ *   stages      1 .. 2^16 (a launch of 2^16 stages lasts some tens of
+ *               milliseconds, well inside the bounded wait)
+ *   status_dev  device uint32, bit 1 set if the bounded completion wait
+ *               ran out (caller zeroes it; read it after the launch)
+ *   ctas        host int, out: CTAs launched (one per SM); may be NULL
+ * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API int moe_probe_mxf8f6f4(int stages, uint32_t* status_dev, int* ctas, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ __all__ = [
     "moe_expert_bytes", "moe_pack_expert", "moe_route_workspace_bytes", "moe_route_plan", "moe_route_plan_noalloc",
     "moe_ffn_workspace_bytes", "alloc_ffn_workspace",
     "moe_expert_ffn", "moe_decode_layer", "moe_ffn_status", "moe_debug_stall_next_decode", "moe_combine",
-    "moe_quant_mxfp8", "moe_quant_mxfp4", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
+    "moe_quant_mxfp8", "moe_quant_mxfp4", "moe_probe_mxf8f6f4", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
     "POLICIES", "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL", "MOE_FFN_ACCUMULATE",
 ]
 
@@ -185,6 +185,15 @@ def moe_quant_mxfp8(x_bf16, q, scales, perm=None, k: int = 1, stream=None) -> No
     rows, K = q.shape
     check("moe_quant_mxfp8", lib().moe_quant_mxfp8(ptr(x_bf16), K, ptr(perm), k, rows, ptr(q), ptr(scales),
                                                    scales.shape[1], stream_handle(stream)))
+
+
+def moe_probe_mxf8f6f4(stages: int, status, stream=None) -> int:
+    """Launch the tensor-core rate probe; returns the CTAs launched.  FLOPs
+    per launch: ctas * stages * 4 * 2 * 128 * 256 * 32.  ``status``: a zeroed
+    device int32 tensor of one element (bit 1: the completion wait ran out)."""
+    n = C.c_int(0)
+    check("moe_probe_mxf8f6f4", lib().moe_probe_mxf8f6f4(stages, ptr(status), C.byref(n), stream_handle(stream)))
+    return n.value
 
 
 class Pool:

@@ -87,6 +87,7 @@ SIGNATURES = {
     "moe_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "moe_quant_mxfp4": (_i32, [_vp, _i32, _i32, _vp, _vp, _i32, _vp]),
     "moe_quant_mxfp8": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _vp]),
+    "moe_probe_mxf8f6f4": (_i32, [_i32, _vp, C.POINTER(C.c_int), _vp]),
 }
 
 _lock = threading.Lock()

@@ -131,6 +131,9 @@ int launch_prefill_prepare(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStre
 int launch_prefill_experts(const FfnArgs& a, void* ws, int e0, int e1, const int32_t* slot_tab, int max_mtiles,
                            cudaStream_t s);
 
+// Tensor-core rate probe (mma_probe.cu).
+int launch_mma_probe(int stages, uint32_t* err, int* ctas, cudaStream_t s);
+
 int launch_combine(const float* y_perm, const float* w, const int32_t* inv, int T, int k, int H,
                    float* out, cudaStream_t s);
 int launch_quant_mxfp8(const uint16_t* x, int K, const int32_t* perm, int k, int rows, uint8_t* q,
