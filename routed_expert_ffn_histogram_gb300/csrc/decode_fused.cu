@@ -45,19 +45,20 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cmath>
 
 #include "internal.h"
 #include "route_warp.cuh"
 #include "tc_ptx.cuh"
 
+
 namespace moe {
 namespace {
 
 constexpr int kGroup = 16;             // row pairs per ring slot (one bulk copy each for gate and up)
-constexpr int kThreads = 32 * (kGroup + 1);  // warp 0: copy producer; warps 1..16: one row pair each
+constexpr int kThreads = 32 * (kGroup + 2);  // warp 0: routing; warp 1: copy producer; warps 2..17: one row pair each
 static_assert(Layout::kChunk % kGroup == 0, "a group of gate rows stays inside one interleave chunk");
-constexpr int kMaxSlots = 16;
 
 // Value of an E8M0 scale byte: 2^(b - 127), byte 255 NaN (OCP MX v1.0).
 __device__ __forceinline__ float e8m0_value_f(int b) {
@@ -189,18 +190,12 @@ struct FusedParams {
 };
 
 constexpr int kMaxAssign = MOE_DECODE_MAX_ASSIGN;
-constexpr int kConsumers = kThreads - 32;   // threads of warps 1..kGroup
+constexpr int kConsumers = kThreads - 64;   // threads of warps 2..kGroup+1
+constexpr int kGuGroups = 4;                // arrival barriers per gate/up slot (4 consumer warps each)
+constexpr int kRowsPerGroup = kGroup / kGuGroups;
+constexpr int kMaxGuSlots = 3, kMaxDSlots = 2;
 
-__device__ __forceinline__ const uint8_t* expert_of(const FusedParams& p, int a) {
-    const int e = p.ids[a];
-    if (e < 0 || e >= p.E) return nullptr;
-    const int s = p.slot_of[e];
-    if (s < 0 || s >= p.S) return nullptr;
-    return p.slots + (size_t)s * p.expert_bytes;
-}
-
-// Per-CTA table of the routed assignments, filled once so the work loops
-// never wait on dependent loads of ids / slot_of / w.
+// Per-CTA table of the routed assignments.
 struct AssignTable {
     int slot_of[MOE_MAX_EXPERTS];
     const uint8_t* base[kMaxAssign];
@@ -217,27 +212,36 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
-// E8M0 byte -> fp32 value, one entry per byte, filled by each CTA at start:
-// a block's scale is then one shared-memory load and one multiply by the
-// power of two that staged its activations.
 __device__ __forceinline__ void named_bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
 }
 
+struct Ring {
+    uint64_t full_gu[kMaxGuSlots][kGuGroups];  // gate/up rows of a group of 4 row pairs landed
+    uint64_t empty_gu[kMaxGuSlots];            // 16 consumer warps done with the slot's rows
+    uint64_t full_d[kMaxDSlots];               // down block landed
+    uint64_t empty_d[kMaxDSlots];              // 16 consumer warps done with the block
+    uint64_t routed;                           // routing table (ids, weights, bases) written
+    uint64_t assigned[kMaxAssign];             // assignment a's expert and slot known
+};
+
 // Work item (a, c): gate/up rows 16c..16c+15 of assignment a, and block c of
-// the column-blocked down copy.  Warp j (1..16) computes h[16c + j - 1]; then
-// the 512 consumer threads apply the 16 h values to the block: thread q owns
-// output rows n = q + 512 m and accumulates y[n] += sum_i W[n][16c+i] h[16c+i]
-// in registers while the items of one assignment follow each other.  When the
-// assignment changes (and at the end) the thread adds w_a * y[n] into the fp32
-// accumulator of its token; the last CTA to finish copies the accumulator to
-// `out` and clears it.  No CTA ever waits for another one.
+// the column-blocked down copy.  The rows and the block travel in separate
+// rings: a gate/up slot is handed back as soon as the 16 h values exist, so
+// its next rows stream in while the down block is applied.  Warp j (1..16)
+// computes h[16c + j - 1], waiting only for the rows of its group of four;
+// then the 512 consumer threads apply the 16 h values to the block: thread
+// q owns output rows n = q + 512 m and accumulates y[n] in registers while
+// the items of one assignment follow each other.  When the assignment
+// changes (and at the end) the thread adds w_a * y[n] into out (residual
+// form) or into the fp32 accumulator of its token, which the last CTA to
+// finish copies to `out` and clears.  No CTA ever waits for another one.
 template <int NG, int NN>
-__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p, int slots, int ring_off) {
+__global__ void __launch_bounds__(kThreads, 1)
+decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ AssignTable tab;
-    __shared__ __align__(8) uint64_t full[kMaxSlots];
-    __shared__ __align__(8) uint64_t empty[kMaxSlots];
+    __shared__ __align__(8) Ring rb;
     __shared__ __align__(16) float hval[2][kGroup];
     __shared__ float e8m0_lut[256];
     __shared__ int last_cta;
@@ -251,111 +255,94 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
     // an input or writes an output before the previous kernel has finished.
     for (int i = threadIdx.x; i < 256; i += kThreads) e8m0_lut[i] = e8m0_value_f(i);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < slots; ++i) {
-            tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], kGroup);
+        for (int s = 0; s < n_gu; ++s) {
+            for (int q = 0; q < kGuGroups; ++q) tc::mbar_init(&rb.full_gu[s][q], 1);
+            tc::mbar_init(&rb.empty_gu[s], kGroup);
         }
+        for (int s = 0; s < n_d; ++s) {
+            tc::mbar_init(&rb.full_d[s], 1);
+            tc::mbar_init(&rb.empty_d[s], kGroup);
+        }
+        tc::mbar_init(&rb.routed, 1);
+        for (int a = 0; a < A; ++a) tc::mbar_init(&rb.assigned[a], 1);
         tc::fence_barrier_init();
     }
+    __syncthreads();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (p.logits != nullptr) {
-        // routing in every CTA: warp 0 ranks each token's logits while the
-        // other warps fetch the slot map
-        if (warp == 0) {
-            for (int t = 0; t < p.T; ++t) {
-                float sv;
-                int sid;
-                const float* row = p.logits + (size_t)t * p.E;
-                if (p.E <= 32) topk_warp<1>(row, p.E, p.k, sv, sid);
-                else if (p.E <= 64) topk_warp<2>(row, p.E, p.k, sv, sid);
-                else if (p.E <= 128) topk_warp<4>(row, p.E, p.k, sv, sid);
-                else topk_warp<8>(row, p.E, p.k, sv, sid);
-                if (lane < p.k) {
-                    tab.id[t * p.k + lane] = sid;
-                    tab.sel_v[t * p.k + lane] = sv;
-                }
-            }
-        } else {
-            for (int e = threadIdx.x - 32; e < p.E; e += kThreads - 32) tab.slot_of[e] = p.slot_of[e];
-        }
-        __syncthreads();
-        for (int a = threadIdx.x; a < A; a += kThreads) {
-            const int e = tab.id[a];
-            const int sl = (e >= 0 && e < p.E) ? tab.slot_of[e] : -1;
-            tab.base[a] = (sl >= 0 && sl < p.S) ? p.slots + (size_t)sl * p.expert_bytes : nullptr;
-        }
-    } else {
-        for (int a = threadIdx.x; a < A; a += kThreads) {
-            tab.base[a] = expert_of(p, a);
-            tab.w[a] = p.w[a];
-        }
-    }
-    __syncthreads();
 
     // This CTA's items: a contiguous range of the A * I / 16 items in
     // (assignment, column block) order.
     const int items = A * p.I / kGroup;
     const int per = (items + G - 1) / G;
     const int g0 = min(items, (int)blockIdx.x * per), g1 = min(items, g0 + per);
+    const int cnt = g1 - g0;
     const int nbx = p.H / 32;
     const size_t row_bytes = p.rs_gu;
     const uint32_t gu_bytes = uint32_t(2 * kGroup * row_bytes);       // gate rows, then up rows
     const uint32_t dt_bytes = uint32_t(p.H) * (kGroup / 2 + 1);          // codes, then scales
-    const size_t slot_bytes = (size_t(gu_bytes) + dt_bytes + 127) / 128 * 128;
-    uint8_t* ring = smem + ring_off;
+    const uint32_t dt_slot = (dt_bytes + 127u) / 128u * 128u;
+    uint8_t* ring_gu = smem + gu_off;
+    uint8_t* ring_d = smem + d_off;
 
     if (warp == 0) {
-        // ---- producer: the rows and the down block of each item, one ring slot per item ----
-        if (lane == 0) {
-            for (int n = 0; g0 + n < g1; ++n) {
-                const int slot = n % slots;
-                const uint32_t phase = uint32_t(n / slots) & 1u;
-                if (!tc::mbar_wait(&empty[slot], phase ^ 1u, err, 4u)) break;
-                // the second item waits until the first has landed, so every
-                // CTA's first item is not queued behind the others' second
-                if (n == 1 && !tc::mbar_wait(&full[0], 0u, err, 4u)) break;
-                // test hook: leave the first item's barrier incomplete, so the
-                // bounded waits on it run out and set the status bits
-                if (n == 0 && p.stall) continue;
-                const int it = (g0 + n) * kGroup;
-                const int a = it / p.I, r = it - a * p.I;
-                const uint8_t* eb = tab.base[a];
-                if (eb != nullptr) {
-                    uint8_t* dst = ring + (size_t)slot * slot_bytes;
-                    const uint8_t* g = eb + Layout::gate_row(r) * p.rs_gu;
-                    tc::mbar_arrive_expect_tx(&full[slot], gu_bytes + dt_bytes);
-                    bulk_copy_g2s(dst, g, uint32_t(kGroup * row_bytes), &full[slot]);
-                    bulk_copy_g2s(dst + kGroup * row_bytes, g + Layout::kChunk * p.rs_gu, uint32_t(kGroup * row_bytes),
-                                  &full[slot]);
-                    bulk_copy_g2s(dst + gu_bytes, eb + p.dt_off + (size_t)(r / kGroup) * p.dt_stride, dt_bytes,
-                                  &full[slot]);
-                } else {
-                    tc::mbar_arrive(&full[slot]);
-                }
+        // ---- routing (warp 0): each assignment's expert and slot are
+        // published (an mbarrier per assignment) as soon as its rank is
+        // decided, so the producer issues that assignment's copies while the
+        // remaining ranks are still being found ----
+        if (p.logits != nullptr) {
+        auto route_all = [&](auto epl_tag) {
+            constexpr int EPL = decltype(epl_tag)::value;
+            // the slot map and the first token's logits are fetched together
+            // (one memory round trip); lane l keeps slot_of[l + 32 i]
+            const int epl = (p.E + 31) / 32;
+            int sl[EPL];
+            float v[EPL];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                const bool in = i < epl && e < p.E;
+                v[i] = in ? __ldg(p.logits + e) : 0.0f;
+                sl[i] = in ? __ldg(p.slot_of + e) : -1;
             }
-        }
-    } else {
-        // ---- consumers (warps 1..16) ----
-        uint4* xs = reinterpret_cast<uint4*>(smem);
-        float* xe = reinterpret_cast<float*>(smem + (size_t)p.T * nbx * 64);
-        for (int c = threadIdx.x - 32; c < p.T * nbx; c += kConsumers) {
-            const int t = c / nbx, b = c - t * nbx;
-            stage_block_f16(p.x + (size_t)t * p.H, xs + (size_t)t * nbx * 4, b, xe + t * nbx);
-        }
-        named_bar_consumers();
-        if (p.logits != nullptr && warp == 1) {
-            // softmax weights, computed while the first copies are in flight;
-            // CTA 0 also writes the routing outputs
-            int my_id = MOE_MAX_EXPERTS;
             for (int t = 0; t < p.T; ++t) {
-                const int a0 = t * p.k;
-                const float sv = lane < p.k ? tab.sel_v[a0 + lane] : 0.0f;
-                const float wv = softmax_lane(sv, p.k);
-                if (lane < p.k) tab.w[a0 + lane] = wv;
+                const float* row = p.logits + (size_t)t * p.E;
+                uint32_t taken = 0, key[EPL];
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    const int e = lane + 32 * i;
+                    const bool in = i < epl && e < p.E;
+                    if (t > 0) v[i] = in ? __ldg(row + e) : 0.0f;
+                    key[i] = rank_key(v[i]);
+                    if (!in) taken |= 1u << i;
+                }
+                float sel_v = 0.0f;
+                for (int j = 0; j < p.k; ++j) {
+                    const int bid = topk_round<EPL>(key, taken);
+                    const int ws = from_winner<EPL>(sl, bid);   // the winner's slot
+                    const float bv = from_winner<EPL>(v, bid);
+                    if (lane == j) sel_v = bv;
+                    if (lane == 0) {
+                        const int a = t * p.k + j;
+                        const int slot = (bid >= 0 && bid < p.E) ? ws : -1;
+                        tab.id[a] = bid;
+                        tab.sel_v[a] = bv;
+                        tab.base[a] = (slot >= 0 && slot < p.S) ? p.slots + (size_t)slot * p.expert_bytes : nullptr;
+                        tc::mbar_arrive(&rb.assigned[a]);
+                    }
+                }
+                const float wv = softmax_lane(sel_v, p.k);
+                if (lane < p.k) tab.w[t * p.k + lane] = wv;
             }
+        };
+            if (p.E <= 32) route_all(std::integral_constant<int, 1>{});
+            else if (p.E <= 64) route_all(std::integral_constant<int, 2>{});
+            else if (p.E <= 128) route_all(std::integral_constant<int, 4>{});
+            else route_all(std::integral_constant<int, 8>{});
             __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&rb.routed);
             if (blockIdx.x == 0) {
+                int my_id = MOE_MAX_EXPERTS;
                 if (lane < A) {
                     my_id = tab.id[lane];
                     p.r_ids[lane] = my_id;
@@ -363,20 +350,101 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 }
                 plan_warp(my_id, A, p.E, p.r_counts, p.r_offsets, p.r_perm, p.r_inv);
             }
+        } else {
+            for (int a = lane; a < A; a += 32) {
+                const int e = p.ids[a];
+                const int s = (e >= 0 && e < p.E) ? p.slot_of[e] : -1;
+                tab.id[a] = e;
+                tab.base[a] = (s >= 0 && s < p.S) ? p.slots + (size_t)s * p.expert_bytes : nullptr;
+                tab.w[a] = p.w[a];
+            }
+            __syncwarp();
+            if (lane == 0) {
+                for (int a = 0; a < A; ++a) tc::mbar_arrive(&rb.assigned[a]);
+                tc::mbar_arrive(&rb.routed);
+            }
         }
-        named_bar_consumers();  // tab.w visible to every consumer
-        const int j = warp - 1;
-        const int ct = threadIdx.x - 32;
+    } else if (warp == 1) {
+        // ---- copy producer (lane 0): gate/up rows and down blocks of the
+        // CTA's items in the order the consumers take them, each as soon as
+        // its assignment is known and its ring slot is free ----
+        if (lane == 0) {
+        auto issue_gu = [&](int n) -> bool {
+            const int slot = n % n_gu;
+            if (!tc::mbar_wait_suspend(&rb.empty_gu[slot], (uint32_t(n / n_gu) & 1u) ^ 1u, err, 4u)) return false;
+            if (n == 0 && p.stall) return true;   // test hook: the first item never lands
+            const int it = (g0 + n) * kGroup;
+            const int a = it / p.I, r = it - a * p.I;
+            if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
+            const uint8_t* eb = tab.base[a];
+            uint8_t* dst = ring_gu + (size_t)slot * gu_bytes;
+            for (int q = 0; q < kGuGroups; ++q) {
+                if (eb != nullptr) {
+                    const uint8_t* g = eb + Layout::gate_row(r + kRowsPerGroup * q) * row_bytes;
+                    const uint32_t part = uint32_t(kRowsPerGroup * row_bytes);
+                    tc::mbar_arrive_expect_tx(&rb.full_gu[slot][q], 2 * part);
+                    bulk_copy_g2s(dst + (size_t)kRowsPerGroup * q * row_bytes, g, part, &rb.full_gu[slot][q]);
+                    bulk_copy_g2s(dst + (size_t)(kGroup + kRowsPerGroup * q) * row_bytes, g + Layout::kChunk * row_bytes,
+                                  part, &rb.full_gu[slot][q]);
+                } else {
+                    tc::mbar_arrive(&rb.full_gu[slot][q]);
+                }
+            }
+            return true;
+        };
+        auto issue_d = [&](int n) -> bool {
+            const int slot = n % n_d;
+            if (!tc::mbar_wait_suspend(&rb.empty_d[slot], (uint32_t(n / n_d) & 1u) ^ 1u, err, 4u)) return false;
+            if (n == 0 && p.stall) return true;
+            const int it = (g0 + n) * kGroup;
+            const int a = it / p.I, r = it - a * p.I;
+            if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
+            const uint8_t* eb = tab.base[a];
+            if (eb != nullptr) {
+                tc::mbar_arrive_expect_tx(&rb.full_d[slot], dt_bytes);
+                bulk_copy_g2s(ring_d + (size_t)slot * dt_slot, eb + p.dt_off + (size_t)(r / kGroup) * p.dt_stride,
+                              dt_bytes, &rb.full_d[slot]);
+            } else {
+                tc::mbar_arrive(&rb.full_d[slot]);
+            }
+            return true;
+        };
+            bool ok = true;
+            int next_gu = 0, next_d = 0;
+            while (ok && (next_gu < cnt || next_d < cnt)) {
+                if (next_gu < cnt && (next_gu <= next_d || next_d >= cnt)) {
+                    ok = issue_gu(next_gu);
+                    ++next_gu;
+                } else {
+                    ok = issue_d(next_d);
+                    ++next_d;
+                }
+            }
+        }
+    } else {
+        // ---- consumers (warps 2..17) ----
+        uint4* xs = reinterpret_cast<uint4*>(smem);
+        float* xe = reinterpret_cast<float*>(smem + (size_t)p.T * nbx * 64);
+        for (int c = threadIdx.x - 64; c < p.T * nbx; c += kConsumers) {
+            const int t = c / nbx, b = c - t * nbx;
+            stage_block_f16(p.x + (size_t)t * p.H, xs + (size_t)t * nbx * 4, b, xe + t * nbx);
+        }
+        named_bar_consumers();
+        const int j = warp - 2;
+        const int grp = j / kRowsPerGroup;
+        const int ct = threadIdx.x - 64;
         float y[NN];
 #pragma unroll
         for (int m = 0; m < NN; ++m) y[m] = 0.0f;
         int cur_a = -1;
+        bool routed = false;
         // Lanes 4i..4i+3 of a warp own four consecutive rows (H is a
         // multiple of 32, so a quad is all inside or all outside [0, H));
         // lane 4i adds the quad with one float4 atomic.
         auto flush = [&](int a) {
             if (a < 0) return;
-            const float wa = tab.w[a];
+            if (!routed) routed = tc::mbar_wait_suspend(&rb.routed, 0u, err, 8u);
+            const float wa = routed ? tab.w[a] : __int_as_float(0x7fc00000);
             float* dst = (p.accumulate ? p.out : p.acc) + (size_t)(a / p.k) * p.H;
 #pragma unroll
             for (int m = 0; m < NN; ++m) {
@@ -389,19 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 y[m] = 0.0f;
             }
         };
-        for (int n = 0; g0 + n < g1; ++n) {
-            const int slot = n % slots;
-            const uint32_t phase = uint32_t(n / slots) & 1u;
-            const bool got = tc::mbar_wait(&full[slot], phase, err, 8u);
+        for (int n = 0; n < cnt; ++n) {
             const int a = (g0 + n) * kGroup / p.I;
             if (a != cur_a) {
                 flush(cur_a);
                 cur_a = a;
             }
+            // (1) h for row r0 + j, once this warp's group of rows has landed
+            const int sg = n % n_gu;
+            const bool got = tc::mbar_wait_suspend(&rb.full_gu[sg][grp], uint32_t(n / n_gu) & 1u, err, 8u);
             const uint8_t* eb = tab.base[a];
             const bool have = got && eb != nullptr;
-            const uint8_t* sl = ring + (size_t)slot * slot_bytes;
-            // (1) h for row r0 + j
+            const uint8_t* sl = ring_gu + (size_t)sg * gu_bytes;
             float hj = __int_as_float(0x7fc00000);
             if (have) {
                 const uint8_t* g = sl + (size_t)j * row_bytes;
@@ -423,10 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                         au = fmaf(du, e8m0_lut[u[p.H / 2 + b]] * xf, au);
                     }
                 }
+                __syncwarp();
+                if (lane == 0 && got) tc::mbar_arrive(&rb.empty_gu[sg]);
                 ag = warp_sum(ag);
                 au = warp_sum(au);
                 const float silu = ag / (1.0f + expf(-ag));
                 hj = __bfloat162float(__float2bfloat16_rn(silu * au));
+            } else if (lane == 0 && got) {
+                tc::mbar_arrive(&rb.empty_gu[sg]);
             }
             if (lane == 0) {
                 hval[n & 1][j] = hj;
@@ -434,8 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 p.h[(size_t)(g0 + n) * kGroup + j] = *reinterpret_cast<const uint16_t*>(&hb);
             }
             named_bar_consumers();
-            // (2) y[n] += W[n][r0..r0+15] . h[r0..r0+15]
-            if (have) {
+            // (2) y[n] += W[n][r0..r0+15] . h[r0..r0+15], once the block has landed
+            const int sd = n % n_d;
+            const bool gotd = tc::mbar_wait_suspend(&rb.full_d[sd], uint32_t(n / n_d) & 1u, err, 8u);
+            if (have && gotd) {
                 // the 16 h values as f16 pairs under one power-of-2 scale (bf16 -> f16 is exact)
                 float hv[kGroup];
                 float amax = 0.0f;
@@ -459,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                     const __half2 hh = __floats2half2_rn(hv[2 * i] * mul, hv[2 * i + 1] * mul);
                     h2[i] = *reinterpret_cast<const uint32_t*>(&hh);
                 }
-                const uint8_t* codes = sl + gu_bytes;
+                const uint8_t* codes = ring_d + (size_t)sd * dt_slot;
                 const uint8_t* scales = codes + (size_t)p.H * (kGroup / 2);
 #pragma unroll
                 for (int m = 0; m < NN; ++m) {
@@ -486,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
                 for (int m = 0; m < NN; ++m) y[m] = __int_as_float(0x7fc00000);
             }
             __syncwarp();
-            if (lane == 0 && got) tc::mbar_arrive(&empty[slot]);
+            if (lane == 0 && gotd) tc::mbar_arrive(&rb.empty_d[sd]);
         }
         flush(cur_a);
     }
@@ -516,22 +589,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(FusedParams p
 }  // namespace
 
 // Shared memory of the fused kernel: the activation staging, then the ring
-// of work items (16 gate rows, 16 up rows, one column block of down).
+// of gate/up rows (16 gate + 16 up rows per slot), then the ring of down
+// blocks.
 static size_t staging_bytes(int T, int H) {
     return round_up(size_t(T) * H * 2 + size_t(T) * (H / 32) * 4, 128);
 }
-
-static size_t item_bytes(const Layout& L) {
-    return round_up(2 * size_t(kGroup) * L.rs_gu + size_t(L.H) * (kGroup / 2 + 1), 128);
-}
+static size_t gu_slot_bytes(const Layout& L) { return 2 * size_t(kGroup) * L.rs_gu; }
+static size_t d_slot_bytes(const Layout& L) { return round_up(size_t(L.H) * (kGroup / 2 + 1), 128); }
 
 constexpr size_t kFusedSmemBudget = 216 * 1024;
+
+// Ring depths that fit: three gate/up slots when they fit, else two.
+static bool fused_rings(int T, const Layout& L, int* n_gu, int* n_d, size_t* bytes) {
+    const size_t st = staging_bytes(T, L.H);
+    for (int g = kMaxGuSlots; g >= 2; --g) {
+        const size_t need = st + g * gu_slot_bytes(L) + kMaxDSlots * d_slot_bytes(L);
+        if (need <= kFusedSmemBudget) {
+            *n_gu = g;
+            *n_d = kMaxDSlots;
+            *bytes = need;
+            return true;
+        }
+    }
+    return false;
+}
 
 size_t decode_fused_smem(int T, int k, int H, int I) {
     Layout L;
     if (!Layout::make(H, I, &L) || T * k > kMaxAssign || I % kGroup || Layout::kDtCols != kGroup || H > 4096) return 0;
-    const size_t need = staging_bytes(T, H) + 2 * item_bytes(L);
-    return need <= kFusedSmemBudget ? need : 0;
+    int g, d;
+    size_t bytes;
+    return fused_rings(T, L, &g, &d, &bytes) ? bytes : 0;
 }
 
 // Test hook (moe_debug_stall_next_decode): launches still to stall.
@@ -543,11 +631,11 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     int rc = current_device_info(&di);
     if (rc != MOE_OK) return rc;
     if (decode_fused_smem(a.T, a.k, L.H, L.I) == 0) return MOE_ERR_UNSUPPORTED;
+    int n_gu = 0, n_d = 0;
+    size_t smem = 0;
+    if (!fused_rings(a.T, L, &n_gu, &n_d, &smem)) return MOE_ERR_UNSUPPORTED;
     const size_t st = staging_bytes(a.T, L.H);
-    const size_t ib = item_bytes(L);
-    const int slots = int(std::min<size_t>(kMaxSlots, (kFusedSmemBudget - st) / ib));
-    if (slots < 2) return MOE_ERR_UNSUPPORTED;
-    const size_t smem = st + size_t(slots) * ib;
+    const size_t d_off = st + size_t(n_gu) * gu_slot_bytes(L);
     FusedParams p;
     p.stall = 0;
     for (int n = g_stall_decode.load(); n > 0; n = g_stall_decode.load())
@@ -584,7 +672,7 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     p.r_inv = ro ? ro->inv : nullptr;
     if (ro && (a.T * a.k > 32 || a.E > MOE_MAX_EXPERTS)) return MOE_ERR_UNSUPPORTED;
     const int ng = (L.H / 32 + 31) / 32, nn = (L.H + kConsumers - 1) / kConsumers;
-    using Kern = void (*)(FusedParams, int, int);
+    using Kern = void (*)(FusedParams, int, int, int, int);
     struct Variant {
         int ng, nn;
         Kern kern;
@@ -621,7 +709,7 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p, slots, int(st)));
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p, n_gu, n_d, int(st), int(d_off)));
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }

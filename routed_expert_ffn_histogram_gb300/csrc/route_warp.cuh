@@ -1,6 +1,7 @@
 // Warp-level routing pieces shared by the routing kernels and the fused
 // decode kernel: top-k of one token's logits (larger logit first, equal
-// logits by lower id, NaN last) and the softmax over the k selected logits
+// logits by lower id, NaN last; one round = two redux.sync warp reductions
+// on an order-preserving key) and the softmax over the k selected logits
 // (float-float, about 48 bits, summed in rank order, rounded to fp32).
 #pragma once
 
@@ -10,46 +11,75 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ bool ranks_before(float la, int a, float lb, int b) {
-    const bool na = isnan(la), nb = isnan(lb);
-    if (na != nb) return nb;
-    if (!na && la != lb) return la > lb;
-    return a < b;
+// Order-preserving 32-bit key of a logit for the top-k: a larger logit has
+// a larger key, -0 and +0 share one key, and NaN has key 0, below every
+// number (the lowest non-NaN key, that of -inf, is 0x007fffff).
+__device__ __forceinline__ uint32_t rank_key(float f) {
+    if (isnan(f)) return 0u;
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One round of a warp top-k: candidate i of this lane is expert lane + 32 i
+// with key key[i]; bit i of `taken` marks a candidate already selected or
+// absent.  The round's winner (largest key, then lowest expert id) is found
+// with two warp reductions (redux.sync max over the lanes' best keys, then
+// min over the expert ids of the lanes holding that key), marked taken, and
+// returned to every lane.
+template <int EPL>
+__device__ __forceinline__ int topk_round(const uint32_t (&key)[EPL], uint32_t& taken) {
+    const int lane = threadIdx.x & 31;
+    uint32_t best = 0u;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        if (!((taken >> i) & 1u) && (bi < 0 || key[i] > best)) {
+            best = key[i];
+            bi = i;
+        }
+    const uint32_t top = __reduce_max_sync(0xffffffffu, bi >= 0 ? best : 0u);
+    const uint32_t cand = (bi >= 0 && best == top) ? uint32_t(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    if (int(win & 31u) == lane) taken |= 1u << (win >> 5);
+    return int(win);
+}
+
+// Value v[win >> 5] of the lane holding expert `win`, on every lane.
+template <int EPL, typename T>
+__device__ __forceinline__ T from_winner(const T (&v)[EPL], int win) {
+    T mine = v[0];
+#pragma unroll
+    for (int i = 1; i < EPL; ++i)
+        if ((win >> 5) == i) mine = v[i];
+    return __shfl_sync(0xffffffffu, mine, win & 31);
 }
 
 // Top-k of one token's logits by one warp: lane j < k ends with the j-th
-// ranked (logit, id).  EPL = candidates per lane (E <= 32 * EPL).
+// ranked (logit, id): larger logit first, equal logits by lower id, NaN
+// last.  EPL = candidates per lane (E <= 32 * EPL).
 template <int EPL>
 __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, int k, float& sel_v, int& sel_id) {
     const int lane = threadIdx.x & 31;
     float v[EPL];
+    uint32_t key[EPL];
     uint32_t taken = 0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         v[i] = (e < E) ? __ldg(row + e) : 0.0f;
+        key[i] = rank_key(v[i]);
         if (e >= E) taken |= 1u << i;
     }
     sel_v = 0.0f;
     sel_id = -1;
     for (int j = 0; j < k; ++j) {
-        float bv = 0.0f;
-        int bid = -1;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            if (taken & (1u << i)) continue;
-            const int e = lane + 32 * i;
-            if (bid < 0 || ranks_before(v[i], e, bv, bid)) { bv = v[i]; bid = e; }
+        const int win = topk_round<EPL>(key, taken);
+        const float wv = from_winner<EPL>(v, win);
+        if (lane == j) {
+            sel_v = wv;
+            sel_id = win;
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
-            if (oid >= 0 && (bid < 0 || ranks_before(ov, oid, bv, bid))) { bv = ov; bid = oid; }
-        }
-        // every lane now holds the same winner
-        if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-        if (lane == j) { sel_v = bv; sel_id = bid; }
     }
 }
 

@@ -90,6 +90,35 @@ __device__ __forceinline__ bool mbar_wait_hot(uint64_t* bar, uint32_t parity, vo
     return false;
 }
 
+
+// Wait for the phase of the given parity from a role that should neither
+// spin on the issue slots it shares with working warps nor sleep long:
+// `mbarrier.try_wait` with a suspend-time hint of kSuspendNs.  On GB300 a
+// suspended thread was measured to resume about when the hint runs out
+// rather than the moment the phase completes, so the hint is short; a
+// phase already complete returns at once.  At most kSuspendTries tries
+// (about a second in all); returns false after *err |= code on timeout, or
+// early when another role has already failed.
+constexpr uint32_t kSuspendNs = 128;
+constexpr uint32_t kSuspendTries = 1u << 23;
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, volatile uint32_t* err,
+                                                  uint32_t code) {
+    for (uint32_t i = 0; i < kSuspendTries; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+            : "memory");
+        if (ok) return true;
+        if ((i & 15u) == 15u && *err) return false;
+    }
+    atomicOr(const_cast<uint32_t*>(err), code);
+    return false;
+}
+
 // ---- TMA ---------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
