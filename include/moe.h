@@ -41,9 +41,13 @@
  *     memory (cudaHostAlloc / cudaHostRegister).  The library keeps host
  *     metadata only and allocates no device memory.
  *   - moe_stream_t is a cudaStream_t passed as an opaque pointer (NULL is
- *     the legacy default stream).  Work is enqueued asynchronously; no call
- *     synchronises the device except the bounded host wait in
- *     moe_pool_stage.
+ *     the legacy default stream).  Work is enqueued asynchronously.  The
+ *     calls that wait on the host are: moe_pool_stage and
+ *     moe_prefill_staged (for the work enqueued so far on their compute
+ *     stream, polling at most timeout_ms), moe_ffn_status (for the work
+ *     enqueued so far on its stream, polling at most 10 s) and
+ *     moe_pool_create with preload (synchronous copies of the preloaded
+ *     experts); no other call waits.
  *   - Tensors are dense row-major.  T tokens, E experts, k top_k,
  *     H hidden size, I expert intermediate size, A = T*k assignments,
  *     assignment a = t*k + j is the j-th ranked expert of token t.
@@ -166,18 +170,22 @@ MOE_API int moe_route_plan(const float* logits, int T, int E, int k,
 
 /* moe_route_plan without a workspace argument.  The pages have no
  * counterpart: this entry exists for callers that cannot allocate device
- * memory where they route -- code running while a CUDA graph is captured,
- * engines whose device memory is owned by their own fixed-budget allocator,
- * decode loops that must not call into the driver's allocator.  The
- * per-tile histograms use a 64 KB array that the library keeps in device
- * memory (every GPU that loads the library holds it until exit); nothing is
+ * memory where they route -- engines whose device memory is carved up in
+ * advance by their own allocator under a fixed budget (there is nothing left
+ * to hand out, and allocating behind that allocator breaks its accounting),
+ * and latency-bound decode loops that must never call into the driver's
+ * allocator, whose calls can block or synchronise the device.  The per-tile
+ * histograms use a 64 KB array that the library keeps in device memory
+ * (every GPU that loads the library holds it until exit); nothing is
  * allocated per call, and no cudaMalloc/cudaFree is ever made.
  *   Arguments, outputs and results are those of moe_route_plan.
  *   Limit: T <= 16384 tokens (64 tiles of 256); larger T returns
  *   MOE_ERR_INVALID before anything is enqueued.
  *   The first call on a device resolves the array's device address for that
- *   device (with it current); make that first call before any stream
- *   capture.  Each call clears the part of the array it uses with an
+ *   device (with it current) and keeps it for the life of the process; make
+ *   that first call before any stream capture, and do not call this entry
+ *   again after the device has been reset (cudaDeviceReset) in the same
+ *   process.  Each call clears the part of the array it uses with an
  *   asynchronous memset on `stream` (no allocation) before counting into
  *   it; all calls share the array, so calls that can overlap on the GPU
  *   race.
@@ -443,12 +451,14 @@ MOE_API int moe_decode_layer_acc(const moe_pool_t* pool, int layer, const float*
  * was sized for, MOE_PATH_DECODE or MOE_PATH_PREFILL): every wait inside the
  * kernels is bounded (about a second); one that runs out sets a bit here and
  * the launch finishes with NaN where its data was missing, instead of
- * hanging or faulting.  Waits for all work enqueued so far on `stream`,
- * returns the bits in *bits (0: nothing ran out) and clears them.
+ * hanging or faulting.  Waits (polling, at most 10 s) for all work enqueued
+ * so far on `stream`, returns the bits in *bits (0: nothing ran out) and
+ * clears them; MOE_ERR_TIMEOUT if the stream's work does not finish in time
+ * (the bits are then neither read nor cleared).
  * Decode bits: 4 copy producer, 8 consumers (data not landed).  Prefill
  * bits: 1 TMA producer, 2 MMA issuer, 4 invalid slot, 8 epilogue, 16
  * teardown, 32 misaligned output, 64 scale-factor feeders.
- * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+ * Errors: MOE_ERR_INVALID, MOE_ERR_TIMEOUT, MOE_ERR_CUDA. */
 MOE_API int moe_ffn_status(void* workspace, int path, moe_stream_t stream, uint32_t* bits);
 
 /* Test hook for the failure path above: the next n fused decode launches

@@ -1,7 +1,9 @@
 // C entry points: status text, validation, expert packing and dispatch to
 // the kernel launchers.  Every argument is checked before anything is
 // enqueued; nothing here allocates device memory.
+#include <chrono>
 #include <cstring>
+#include <thread>
 #include <mutex>
 
 #include "internal.h"
@@ -275,18 +277,39 @@ extern "C" int moe_decode_layer_acc(const moe_pool_t* pool, int layer, const flo
                         ws_bytes, out, stream, true);
 }
 
+namespace moe {
+// Wait, polling an event (at most timeout_ms), until the work enqueued so
+// far on `s` is done.  One event per host thread, created on first use.
+static int bounded_stream_wait(cudaStream_t s, int timeout_ms) {
+    thread_local cudaEvent_t ev = nullptr;
+    if (ev == nullptr) MOE_CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    MOE_CUDA_TRY(cudaEventRecord(ev, s));
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        const cudaError_t q = cudaEventQuery(ev);
+        if (q == cudaSuccess) return MOE_OK;
+        if (q != cudaErrorNotReady) return cuda_fail(q);
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms)) return MOE_ERR_TIMEOUT;
+        std::this_thread::yield();
+    }
+}
+}  // namespace moe
+
 extern "C" int moe_ffn_status(void* workspace, int path, moe_stream_t stream, uint32_t* bits) {
     if (!workspace || !bits || (path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL)) return MOE_ERR_INVALID;
     if (!aligned(workspace, 256)) return MOE_ERR_INVALID;
     // decode: word 2 of the 256-byte control block; prefill: the first word
     uint32_t* dev = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + (path == MOE_PATH_DECODE ? 8 : 0));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    constexpr int kStatusWaitMs = 10000;
+    int rc = moe::bounded_stream_wait(s, kStatusWaitMs);
+    if (rc != MOE_OK) return rc;
     uint32_t h = 0;
-    MOE_CUDA_TRY(cudaMemcpyAsync(&h, dev, sizeof h, cudaMemcpyDeviceToHost, s));
-    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    MOE_CUDA_TRY(cudaMemcpy(&h, dev, sizeof h, cudaMemcpyDeviceToHost));   // the stream's work is done
     if (h != 0) {
         MOE_CUDA_TRY(cudaMemsetAsync(dev, 0, sizeof h, s));
-        MOE_CUDA_TRY(cudaStreamSynchronize(s));
+        rc = moe::bounded_stream_wait(s, kStatusWaitMs);
+        if (rc != MOE_OK) return rc;
     }
     *bits = h;
     return MOE_OK;

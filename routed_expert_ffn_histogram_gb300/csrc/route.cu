@@ -263,12 +263,10 @@ int launch_route_plan(const float* logits, int T, int E, int k, int32_t* ids, fl
 // ---------------------------------------------------------------------------
 // Routing without caller-provided scratch (moe_route_plan_noalloc).
 //
-// Some callers cannot allocate device memory where they route: code running
-// while a CUDA graph is being captured (an allocation there would either be
-// refused or baked into the graph), engines whose device memory is carved
-// up in advance by their own allocator under a fixed budget, and real-time
-// decode loops that must never call into the driver's allocator, which can
-// block or synchronise.  For them the per-tile histograms live in this
+// Some callers cannot allocate device memory where they route: engines
+// whose device memory is carved up in advance by their own allocator under a
+// fixed budget, and real-time decode loops that must never call into the
+// driver's allocator, which can block or synchronise.  For them the per-tile histograms live in this
 // file-scope device array instead of a workspace.  It holds
 // kNoallocMaxTiles * MOE_MAX_EXPERTS int32 (64 KB), enough for up to
 // kNoallocMaxTiles * 256 = 16384 tokens; every GPU that loads the library
@@ -283,7 +281,9 @@ constexpr int kNoallocMaxTiles = 64;
 __device__ __align__(256) int32_t g_route_noalloc_scratch[kNoallocMaxTiles * MOE_MAX_EXPERTS];
 
 // Device address of the scratch array on the current device, resolved once
-// per device (with that device current) on the first call made there.
+// per device (with that device current) on the first call made there and
+// kept for the life of the process (the header asks callers not to use the
+// entry after a device reset, which could move the array).
 int noalloc_scratch(int32_t** out) {
     static std::mutex mu;
     static int32_t* addr[64] = {};

@@ -79,10 +79,14 @@ def test_injected_copy_failure_on_device_pool():
     assert torch.equal(dev[:eb].cpu(), host[3 * eb:4 * eb])
 
 
-def test_offload_decode_only_staging():
-    """A pool that stages only what the fused decode kernel reads gives the
-    same layer outputs as the oracle, copies fewer bytes than whole experts,
-    and refuses the prefill path (which needs the skipped matrix)."""
+@pytest.mark.parametrize("policy", ["lfru", "slru"])
+def test_offload_decode_only_staging(policy):
+    """A pool that stages only what the fused decode kernel reads, under a
+    non-LRU eviction policy: per (layer, step) event the load list and the
+    slot map equal the oracle's policy simulation bit for bit, and so do the
+    layer's hit/miss/eviction counters at the end; the layer outputs match
+    the oracle; fewer bytes than whole experts are copied; the prefill path
+    (which needs the skipped matrix) is refused."""
     import torch
 
     import routed_expert_ffn_histogram_gb300 as M
@@ -92,7 +96,8 @@ def test_offload_decode_only_staging():
     pool, host, dev = make_pool(M, wl, layers=L, preload=False)
     pool.close()
     pool = M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev,
-                  policy="lfru", stage_parts="decode")
+                  policy=policy, stage_parts="decode")
+    ref = [oracle.PolicyPool(wl.slots, wl.experts, policy) for _ in range(L)]
     T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
     plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
     slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
@@ -100,18 +105,27 @@ def test_offload_decode_only_staging():
     out = torch.empty((T, H), dtype=torch.float32, device="cuda")
     compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
     with torch.cuda.stream(compute):
-        for step in range(4):
+        for step in range(12):
             for layer in range(L):
                 lg = torch.from_numpy(S.logits(wl, layer, step)).cuda()
                 x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step).view(np.int16)).cuda().view(
                     torch.bfloat16)
                 M.moe_route_plan(lg, k, plan, stream=compute)
                 assert pool.stage(layer, plan.counts_host, slot_of, compute=compute, copy=copy) == M.MOE_OK
+                counts = plan.counts_host.numpy().copy()
+                assert pool.last_loads(layer) == ref[layer].step(counts)
+                assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
                 M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE, stream=compute)
-                compute.synchronize()
-                r, _ = _oracle_layer(wl, layer, step, prefill=False)
-                assert rel_l2(out.cpu().numpy(), r) <= DECODE_REL_L2
+                if step % 4 == 0 or step == 11:
+                    compute.synchronize()
+                    r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                    assert rel_l2(out.cpu().numpy(), r) <= DECODE_REL_L2
+        compute.synchronize()
+        for layer in range(L):
+            c, e = pool.counters(layer), ref[layer].counters()
+            assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
         c = pool.counters()
+        assert c["evictions"] > 0
         assert 0 < c["h2d_bytes"] < c["misses"] * M.moe_expert_bytes(H, I)
         pws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_PREFILL)
         with pytest.raises(M.MoeError):

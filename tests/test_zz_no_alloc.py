@@ -1,5 +1,5 @@
 """moe_route_plan_noalloc: routing for callers that cannot allocate device
-memory (graph capture in progress, engines with their own fixed-budget
+memory (engines whose device memory belongs to their own fixed-budget
 allocator, decode loops that must stay out of the driver's allocator).  It
 keeps its tile histograms in the library's own device array instead of a
 caller workspace, so its results must equal moe_route_plan's exactly --
