@@ -16,31 +16,47 @@
 // their rounding order (not their value beyond fp32 rounding) varies
 // between runs.
 //
-// Shape: one CTA per SM, 17 warps.  The work is cut into items of 16
-// consecutive rows of h for one assignment: the 16 gate rows and 16 up rows
-// (contiguous in the packed layout, two bulk copies) and the matching
-// 16-column block of the column-blocked down copy (one bulk copy), streamed
-// by warp 0 through a shared-memory ring.
-//   gate/up  warp j takes row pair j of the item: one 16-byte load = one MX
-//            block per lane; x is staged once per CTA in shared memory as
-//            f16 scaled per 32-block by a power of two (exact for every
-//            value within 2^-31 of the block maximum) in XOR-swizzled
-//            16-byte chunks; E2M1 pairs become f16x2 by hardware conversion
-//            and multiply-add into fp32 (products exact); h = bf16(silu(g)*u).
-//   down     the 16 h values (f16 under one power-of-2 scale) times the
-//            block's codes, every consumer thread owning fixed output rows;
-//            partial sums stay in registers across an assignment's items.
-//            E8M0 scales come from a 256-entry table in shared memory.
+// Shape: one CTA per SM, 18 warps in three roles.
+//   routing  warp 0 fetches the slot map and the token's logits in one
+//            memory round trip and ranks the logits (each top-k round two
+//            redux.sync warp reductions); each assignment's expert and slot
+//            are published through an mbarrier of their own as soon as its
+//            rank is decided, then the softmax weights.
+//   copies   warp 1 (one lane) streams the CTA's work items: items of 16
+//            consecutive rows of h for one assignment.  The 16 gate and 16
+//            up rows (contiguous in the packed layout) go into a 3-slot ring
+//            as eight bulk copies, one arrival barrier per group of four row
+//            pairs; the matching 16-column block of the column-blocked down
+//            copy goes into a 2-slot ring.  An item is issued as soon as its
+//            assignment is published and its slots are free.
+//   consumers warps 2..17 stage x (while warp 0 routes) and then, per item:
+//   gate/up  warp j takes row pair j of the item once its group of rows has
+//            landed: one 16-byte load = one MX block per lane; x is staged
+//            once per CTA in shared memory as f16 scaled per 32-block by a
+//            power of two (exact for every value within 2^-31 of the block
+//            maximum) in XOR-swizzled 16-byte chunks; E2M1 pairs become f16x2
+//            by hardware conversion and multiply-add into fp32 (products
+//            exact); h = bf16(silu(g)*u).  The gate/up slot is handed back
+//            before the per-item barrier, so its next rows stream in while
+//            the down block is applied.
+//   down     the 16 h values (f16 under one power-of-2 scale, taken from the
+//            item's largest |h|, which the gate/up warps record with a
+//            shared atomic max) times the block's codes, every consumer
+//            thread owning fixed output rows; partial sums stay in registers
+//            across an assignment's items.  E8M0 scales come from a
+//            256-entry table in shared memory.
 //   combine  w_a * y added with float4 atomics (a lane quad's four rows) to
 //            `out` directly when the caller accumulates (out += result, a
 //            residual stream), else to an fp32 accumulator in the
 //            workspace that the last CTA to finish (a ticket counter, no
 //            waiting) copies to the output and clears for the next call.
 // No CTA waits for another: there is no grid barrier and no cooperative
-// launch.  The kernel is launched with programmatic stream serialisation:
-// each CTA runs its shared-memory-only prologue, lets the next kernel
-// launch, and waits for the previous one (griddepcontrol) before touching
-// global memory, so consecutive layers hand SMs over CTA by CTA.
+// launch.  Waits inside the CTA are bounded mbarrier waits (about a second,
+// then an error bit and NaN output instead of a hang).  The kernel is
+// launched with programmatic stream serialisation: each CTA runs its
+// shared-memory-only prologue, lets the next kernel launch, and waits for the
+// previous one (griddepcontrol) before touching global memory, so
+// consecutive layers hand SMs over CTA by CTA.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -97,24 +113,24 @@ __device__ __forceinline__ void block_dot2_f16(const uint4 cg, const uint4 cu, c
                                                int b, float& dg, float& du) {
     const uint32_t wg[4] = {cg.x, cg.y, cg.z, cg.w};
     const uint32_t wu[4] = {cu.x, cu.y, cu.z, cu.w};
-    float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+    float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint4 xv = xs[hswz(b, q)];
         uint32_t fg[4], fu[4];
         e2m1x8_f16(wg[q], fg);
         e2m1x8_f16(wu[q], fu);
-        fma2_f16_f32(g[0], g[1], fg[0], xv.x);
-        fma2_f16_f32(u[0], u[1], fu[0], xv.x);
-        fma2_f16_f32(g[2], g[3], fg[1], xv.y);
-        fma2_f16_f32(u[2], u[3], fu[1], xv.y);
-        fma2_f16_f32(g[0], g[1], fg[2], xv.z);
-        fma2_f16_f32(u[0], u[1], fu[2], xv.z);
-        fma2_f16_f32(g[2], g[3], fg[3], xv.w);
-        fma2_f16_f32(u[2], u[3], fu[3], xv.w);
+        fma2_f16_f32(g0, g1, fg[0], xv.x);
+        fma2_f16_f32(u0, u1, fu[0], xv.x);
+        fma2_f16_f32(g0, g1, fg[1], xv.y);
+        fma2_f16_f32(u0, u1, fu[1], xv.y);
+        fma2_f16_f32(g0, g1, fg[2], xv.z);
+        fma2_f16_f32(u0, u1, fu[2], xv.z);
+        fma2_f16_f32(g0, g1, fg[3], xv.w);
+        fma2_f16_f32(u0, u1, fu[3], xv.w);
     }
-    dg = (g[0] + g[1]) + (g[2] + g[3]);
-    du = (u[0] + u[1]) + (u[2] + u[3]);
+    dg = g0 + g1;
+    du = u0 + u1;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -243,6 +259,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
     __shared__ AssignTable tab;
     __shared__ __align__(8) Ring rb;
     __shared__ __align__(16) float hval[2][kGroup];
+    __shared__ unsigned hmax_bits[3];
     __shared__ float e8m0_lut[256];
     __shared__ int last_cta;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -264,6 +281,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             tc::mbar_init(&rb.empty_d[s], kGroup);
         }
         tc::mbar_init(&rb.routed, 1);
+        hmax_bits[0] = hmax_bits[1] = hmax_bits[2] = 0u;
         for (int a = 0; a < A; ++a) tc::mbar_init(&rb.assigned[a], 1);
         tc::fence_barrier_init();
     }
@@ -501,17 +519,20 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             }
             if (lane == 0) {
                 hval[n & 1][j] = hj;
+                atomicMax(&hmax_bits[n % 3], __float_as_uint(fabsf(hj)));
                 const __nv_bfloat16 hb = __float2bfloat16_rn(hj);
                 p.h[(size_t)(g0 + n) * kGroup + j] = *reinterpret_cast<const uint16_t*>(&hb);
             }
             named_bar_consumers();
+            // the word of item n - 1 was last read before this barrier and is
+            // next written after the following one
+            if (ct == 0 && n >= 1) hmax_bits[(n - 1) % 3] = 0u;
             // (2) y[n] += W[n][r0..r0+15] . h[r0..r0+15], once the block has landed
             const int sd = n % n_d;
             const bool gotd = tc::mbar_wait_suspend(&rb.full_d[sd], uint32_t(n / n_d) & 1u, err, 8u);
             if (have && gotd) {
                 // the 16 h values as f16 pairs under one power-of-2 scale (bf16 -> f16 is exact)
                 float hv[kGroup];
-                float amax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < kGroup / 4; ++i) {
                     const float4 v4 = reinterpret_cast<const float4*>(hval[n & 1])[i];
@@ -520,12 +541,17 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                     hv[4 * i + 2] = v4.z;
                     hv[4 * i + 3] = v4.w;
                 }
-#pragma unroll
-                for (int i = 0; i < kGroup; ++i) amax = fmaxf(amax, fabsf(hv[i]));
-                const int ef = int((__float_as_uint(amax) >> 23) & 0xffu);
-                const int e = (amax == 0.f) ? 0 : (ef == 0 ? -126 - 14 : ef - 127 - 14);
-                const float mul = ldexpf(1.0f, -e);
-                const float hf = ldexpf(1.0f, e);
+                // scale 2^-e with e = exponent of the item's largest |h| minus 14
+                const int ef = int(hmax_bits[n % 3] >> 23);
+                float mul, hf;
+                if (ef >= 15 && ef <= 254) {
+                    mul = __uint_as_float(uint32_t(268 - ef) << 23);
+                    hf = __uint_as_float(uint32_t(ef - 14) << 23);
+                } else {
+                    const int e = (hmax_bits[n % 3] == 0u) ? 0 : (ef == 0 ? -126 - 14 : ef - 127 - 14);
+                    mul = ldexpf(1.0f, -e);
+                    hf = ldexpf(1.0f, e);
+                }
                 uint32_t h2[kGroup / 2];
 #pragma unroll
                 for (int i = 0; i < kGroup / 2; ++i) {
@@ -542,16 +568,16 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                         uint32_t w0[4], w1[4];
                         e2m1x8_f16(cw.x, w0);
                         e2m1x8_f16(cw.y, w1);
-                        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+                        float s0 = 0.0f, s1 = 0.0f;
                         fma2_f16_f32(s0, s1, w0[0], h2[0]);
-                        fma2_f16_f32(s2, s3, w0[1], h2[1]);
+                        fma2_f16_f32(s0, s1, w0[1], h2[1]);
                         fma2_f16_f32(s0, s1, w0[2], h2[2]);
-                        fma2_f16_f32(s2, s3, w0[3], h2[3]);
+                        fma2_f16_f32(s0, s1, w0[3], h2[3]);
                         fma2_f16_f32(s0, s1, w1[0], h2[4]);
-                        fma2_f16_f32(s2, s3, w1[1], h2[5]);
+                        fma2_f16_f32(s0, s1, w1[1], h2[5]);
                         fma2_f16_f32(s0, s1, w1[2], h2[6]);
-                        fma2_f16_f32(s2, s3, w1[3], h2[7]);
-                        y[m] = fmaf((s0 + s1) + (s2 + s3), e8m0_lut[scales[nn]] * hf, y[m]);
+                        fma2_f16_f32(s0, s1, w1[3], h2[7]);
+                        y[m] = fmaf(s0 + s1, e8m0_lut[scales[nn]] * hf, y[m]);
                     }
                 }
             } else {

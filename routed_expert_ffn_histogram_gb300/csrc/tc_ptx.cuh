@@ -12,13 +12,22 @@
 namespace moe {
 namespace tc {
 
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait gives up (~1 s)
+constexpr uint32_t kWaitLimit = 1u << 26;       // backstop on the polls of one wait
+constexpr uint64_t kWaitNs = 1000000000ull;      // a wait gives up after about a second
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 // ---- mbarrier ----------------------------------------------------------------
+
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -54,13 +63,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of the given parity.  Bounded: polls with a growing
-// sleep (about one second in total at most); on timeout, or when another
-// role has already failed, returns false after *err |= code.
+// sleep, for about kWaitNs of elapsed time on the global timer; on timeout,
+// or when another role has already failed, returns false after
+// *err |= code.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* err, uint32_t code) {
+    uint64_t t0 = 0;
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i >= 64) __nanosleep(i < 4096 ? 32 : 256);
-        if ((i & 255u) == 255u && *err) return false;
+        if ((i & 255u) == 255u) {
+            if (*err) return false;
+            const uint64_t t = global_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > kWaitNs) break;
+        }
     }
     atomicOr(const_cast<uint32_t*>(err), code);
     return false;
@@ -70,11 +86,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // to resume the moment it completes (TMA producer, MMA issuer, scale-factor
 // feeders): `mbarrier.try_wait` suspends the thread in hardware until the
 // phase completes or a short system-defined limit passes, so there is no
-// sleep between polls.  Bounded like mbar_wait (kHotWaitLimit tries).
-constexpr uint32_t kHotWaitLimit = 1u << 20;
+// sleep between polls.  Bounded like mbar_wait (about kWaitNs of elapsed
+// time, at most kWaitLimit tries).
 __device__ __forceinline__ bool mbar_wait_hot(uint64_t* bar, uint32_t parity, volatile uint32_t* err,
                                               uint32_t code) {
-    for (uint32_t i = 0; i < kHotWaitLimit; ++i) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -84,7 +101,12 @@ __device__ __forceinline__ bool mbar_wait_hot(uint64_t* bar, uint32_t parity, vo
             : "r"(smem_u32(bar)), "r"(parity)
             : "memory");
         if (ok) return true;
-        if ((i & 63u) == 63u && *err) return false;
+        if ((i & 63u) == 63u) {
+            if (*err) return false;
+            const uint64_t t = global_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > kWaitNs) break;
+        }
     }
     atomicOr(const_cast<uint32_t*>(err), code);
     return false;
@@ -93,17 +115,19 @@ __device__ __forceinline__ bool mbar_wait_hot(uint64_t* bar, uint32_t parity, vo
 
 // Wait for the phase of the given parity from a role that should neither
 // spin on the issue slots it shares with working warps nor sleep long:
-// `mbarrier.try_wait` with a suspend-time hint of kSuspendNs.  On GB300 a
-// suspended thread was measured to resume about when the hint runs out
-// rather than the moment the phase completes, so the hint is short; a
-// phase already complete returns at once.  At most kSuspendTries tries
-// (about a second in all); returns false after *err |= code on timeout, or
-// early when another role has already failed.
+// `mbarrier.try_wait` with a suspend-time hint of kSuspendNs.  A phase
+// already complete returns at once; a suspended thread resumes when the
+// phase completes or after a time the hardware chooses (measured on GB300
+// to be several microseconds when the phase never completes, whatever the
+// hint), so the wait is bounded by elapsed time on the global timer: about
+// kWaitNs, checked every 16 tries, with kWaitLimit tries as a backstop.
+// Returns false after *err |= code on timeout, or early when another role
+// has already failed.
 constexpr uint32_t kSuspendNs = 128;
-constexpr uint32_t kSuspendTries = 1u << 23;
 __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, volatile uint32_t* err,
                                                   uint32_t code) {
-    for (uint32_t i = 0; i < kSuspendTries; ++i) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -113,7 +137,12 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity
             : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (ok) return true;
-        if ((i & 15u) == 15u && *err) return false;
+        if ((i & 15u) == 15u) {
+            if (*err) return false;
+            const uint64_t t = global_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > kWaitNs) break;
+        }
     }
     atomicOr(const_cast<uint32_t*>(err), code);
     return false;
