@@ -162,6 +162,17 @@ def _events(n=2):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
+def _graph_event():
+    """A timing event that can be recorded inside a captured CUDA graph and
+    timed after a replay (an external event where torch offers it)."""
+    import torch
+
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
 def _soak(fn, seconds: float):
     """Run ``fn`` (enqueues GPU work) back to back for about ``seconds``."""
     import torch
@@ -624,13 +635,7 @@ def prefill_timing(args, wl, soak_s=0.0):
     ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_PREFILL, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    ext = dict(enable_timing=True)
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        ext["external"] = True
-    except TypeError:
-        pass
-    ev = [(torch.cuda.Event(**ext), torch.cuda.Event(**ext), torch.cuda.Event(**ext)) for _ in range(G)]
+    ev = [(_graph_event(), _graph_event(), _graph_event()) for _ in range(G)]
     residual = args.output == "residual"
 
     def step(g):
@@ -725,6 +730,80 @@ def prefill_timing(args, wl, soak_s=0.0):
     del slots, flush
     torch.cuda.empty_cache()
     return res
+
+
+def gguf_obj(args, fmt, wid=4):
+    """Decode on GGUF expert weights read in place (moe_expert_ffn_gguf): one
+    Qwen-30B-A3B-shaped layer (128 experts, top-8) resident in GGUF form, one
+    token per step (a different token each step), routing + the two GGUF
+    launches graph-captured, L2 flushed before every step.  HBM bytes per
+    step: the routed experts' GGUF rows (gate, up, down)."""
+    import torch
+
+    import oracle
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[wid]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    eb = M.moe_gguf_expert_bytes(fmt, H, I)
+    img = torch.empty(E * eb, dtype=torch.uint8).pin_memory()
+    for e in range(E):
+        M.pack_gguf_expert(S.expert_weights_gguf(wl, fmt, 0, e), fmt, H, I, img.data_ptr() + e * eb)
+    slots = img.to(dev)
+    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
+    G = args.warmup + args.steps
+    lg = torch.from_numpy(np.stack([S.logits(wl, 0, 0, G)[g:g + 1] for g in range(G)])).to(dev)
+    xb = torch.from_numpy(S.activations_bf16_bits(wl, 0, 0, G).view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.zeros((1, H), dtype=torch.float32, device=dev)
+    plan = M.RoutePlan.allocate(1, E, k, device=dev)
+    ws = M.alloc_gguf_workspace(1, k, H, I, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    ev = [(_graph_event(), _graph_event()) for _ in range(G)]
+
+    def step(g):
+        flush.fill_(g & 255)
+        ev[g][0].record(stream)
+        M.moe_route_plan(lg[g], k, plan, stream=stream, with_counts_host=False)
+        M.moe_expert_ffn_gguf(fmt, slots, E, H, I, xb[g:g + 1], plan, slot_of, E, out, ws, accumulate=True,
+                              stream=stream)
+        ev[g][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    graphs = []
+    for g in range(G):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(g)
+        graphs.append(gr)
+    for g in range(args.warmup):
+        graphs[g].replay()
+    torch.cuda.synchronize()
+    times = []
+    for g in range(args.warmup, G):
+        graphs[g].replay()
+        torch.cuda.synchronize()
+        times.append(ev[g][0].elapsed_time(ev[g][1]))
+    rbh, rbi = oracle.gguf_row_bytes(fmt, H), oracle.gguf_row_bytes(fmt, I)
+    step_bytes = k * (2 * I * rbh + H * rbi)
+    ms = statistics.median(times)
+    hbm_peak, _, peak_kind = _peaks()
+    achieved = step_bytes / (ms / 1e3) / 1e9
+    del slots, flush
+    torch.cuda.empty_cache()
+    return {"workload": f"{wl.name}_decode_gguf_{fmt}", "value": 1e3 / ms, "unit": "tokens/s (one layer)",
+            "ms_per_step": ms,
+            "config": {"hidden": H, "inter": I, "experts": E, "top_k": k, "tokens_per_step": 1, "format": fmt,
+                       "layers": 1, "l2": "256 MB flush before every step",
+                       "timing": "routing + moe_expert_ffn_gguf, graph per step, CUDA events"},
+            "roofline": {"kernel": "gguf_gateup_kernel + gguf_down_kernel + gguf_combine_kernel (routing included in the time)",
+                         "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": step_bytes},
+            "gpu_launches": args.steps * 5}
 
 
 def prefill_obj(args, wl, mma, threads, cpu=True):
@@ -1072,6 +1151,7 @@ def main():
         if not args.no_cpu_baseline:
             off["cpu_baseline"] = cpu_offload_baseline(ow, args.cpu_layers, threads)
         line["offload"] = {ow.name: off}
+        line["gguf_decode"] = {fmt: gguf_obj(args, fmt) for fmt in ("q4_k", "q8_0")}
     if rank == 0:
         print(json.dumps(line))
 

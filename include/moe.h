@@ -497,6 +497,59 @@ MOE_API int moe_quant_mxfp4(const void* x_bf16, int K, int rows, uint8_t* q, uin
 
 
 /* ------------------------------------------------------------------------ */
+/* Decode on GGUF expert weights [R3]                                        */
+/* ------------------------------------------------------------------------ */
+
+/* GGUF block formats of the experts (tinyserve README, "How it works" item
+ * 2 and "Supported models", Formats, run experts in their native GGUF
+ * quantisation; the block layouts are the published GGUF / ggml ones):
+ *   Q8_0  per 32 elements, 34 bytes: binary16 d (little-endian), 32 int8 q;
+ *         element = d * q.
+ *   Q4_K  per 256 elements, 144 bytes: binary16 d and dmin, 12 bytes packing
+ *         eight 6-bit scales sc and mins m (sub-blocks 0-3 in the low 6 bits
+ *         of bytes j and j+4; 4-7 split over the nibbles of byte j+4 and the
+ *         top 2 bits of bytes j-4 and j), 128 bytes of 4-bit values q
+ *         (sub-blocks 2g and 2g+1 in the low and high nibbles of the same 32
+ *         bytes); element = d*sc*q - dmin*m. */
+#define MOE_GGUF_Q8_0 0
+#define MOE_GGUF_Q4_K 1
+
+/* Bytes of one GGUF expert slot: [gate I rows][up I rows][down H rows],
+ * each row the format's blocks back to back (gate and up rows of H
+ * elements, down rows of I elements), the total rounded up to 256 bytes.
+ * Q8_0 needs hidden and inter multiples of 64, Q4_K multiples of 256.
+ * Errors: MOE_ERR_INVALID. */
+MOE_API int moe_gguf_expert_bytes(int fmt, int hidden, int inter, size_t* out_bytes);
+
+/* Scratch bytes moe_expert_ffn_gguf needs: bf16 h [T*k][inter], then fp32
+ * y [T*k][hidden] (each assignment's down output before the combine). */
+MOE_API int moe_gguf_workspace_bytes(int T, int k, int hidden, int inter, size_t* out_bytes);
+
+/* The routed experts of one layer on GGUF weights read in place, the
+ * decode path's arithmetic: out[t] = sum_j w[t][j] * down_e(h), h =
+ * bf16(silu(gate_e x_t) * up_e x_t), e = ids[t][j]; bf16 activations times
+ * the exactly dequantised weights, fp32 sums (each block summed in its own
+ * factors: d * sum(q x), or d*sc * sum(q x) - dmin*m * sum(x) per 32),
+ * the k terms summed in rank order.  Three launches (gate/up with SwiGLU;
+ * down per assignment; the combine), no atomics.
+ *   fmt       MOE_GGUF_Q8_0 or MOE_GGUF_Q4_K
+ *   slots     device [n_slots][moe_gguf_expert_bytes()] GGUF experts, 256-byte
+ *             aligned
+ *   x_bf16    device bf16 [T][hidden]
+ *   ids, w    device, from moe_route_plan ([T][k])
+ *   slot_of   device int32 [E]: slot of each expert; a routed expert without
+ *             a valid slot makes its token's output NaN
+ *   workspace device, >= moe_gguf_workspace_bytes(), 256-byte aligned
+ *   out       device fp32 [T][hidden]; accumulate != 0: out += result
+ * Limits: 1 <= E <= MOE_MAX_EXPERTS, 1 <= k <= MOE_MAX_TOPK, T >= 0, the
+ * shapes above, hidden and inter at most 11,000 (one fp32 staged copy per
+ * CTA).  Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API int moe_expert_ffn_gguf(int fmt, const void* slots, int n_slots, int hidden, int inter,
+                                const void* x_bf16, int T, int k, const int32_t* ids, const float* w,
+                                const int32_t* slot_of, int E, void* workspace, size_t ws_bytes, float* out,
+                                int accumulate, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Measurement                                                               */
 /* ------------------------------------------------------------------------ */
 

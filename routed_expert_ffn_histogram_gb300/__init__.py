@@ -23,7 +23,8 @@ from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_FFN_ACCUMULATE, MOE_ERR_CAPACITY, 
                    MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_OK,
                    MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_POLICY_FIFO, MOE_POLICY_LFRU,
                    MOE_POLICY_LFU, MOE_POLICY_LRU, MOE_POLICY_SLRU, MOE_STAGE_DECODE,
-                   MOE_STAGE_WHOLE, POLICIES, MoeCounters, MoeError, MoePoolDesc,
+                   MOE_STAGE_WHOLE, POLICIES, GGUF_FORMATS, MOE_GGUF_Q8_0, MOE_GGUF_Q4_K, MoeCounters, MoeError,
+                   MoePoolDesc,
                    check,
                    lib, ptr, status_str, stream_handle)
 
@@ -31,7 +32,8 @@ __all__ = [
     "moe_expert_bytes", "moe_pack_expert", "moe_route_workspace_bytes", "moe_route_plan", "moe_route_plan_noalloc",
     "moe_ffn_workspace_bytes", "alloc_ffn_workspace",
     "moe_expert_ffn", "moe_decode_layer", "moe_ffn_status", "moe_debug_stall_next_decode", "moe_combine",
-    "moe_quant_mxfp8", "moe_quant_mxfp4", "moe_probe_mxf8f6f4", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
+    "moe_quant_mxfp8", "moe_quant_mxfp4", "moe_probe_mxf8f6f4", "moe_gguf_expert_bytes", "pack_gguf_expert",
+    "moe_expert_ffn_gguf", "alloc_gguf_workspace", "GGUF_FORMATS", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
     "POLICIES", "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL", "MOE_FFN_ACCUMULATE",
 ]
 
@@ -185,6 +187,54 @@ def moe_quant_mxfp8(x_bf16, q, scales, perm=None, k: int = 1, stream=None) -> No
     rows, K = q.shape
     check("moe_quant_mxfp8", lib().moe_quant_mxfp8(ptr(x_bf16), K, ptr(perm), k, rows, ptr(q), ptr(scales),
                                                    scales.shape[1], stream_handle(stream)))
+
+
+def _fmt(fmt) -> int:
+    return GGUF_FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def moe_gguf_expert_bytes(fmt, hidden: int, inter: int) -> int:
+    out = C.c_size_t(0)
+    check("moe_gguf_expert_bytes", lib().moe_gguf_expert_bytes(_fmt(fmt), hidden, inter, C.byref(out)))
+    return out.value
+
+
+def pack_gguf_expert(w: dict, fmt, hidden: int, inter: int, dst) -> None:
+    """One GGUF expert's raw rows (host numpy ``gate``/``up`` [I][row bytes],
+    ``down`` [H][row bytes]) placed back to back into its slot image at the
+    host address / array ``dst`` (``moe_gguf_expert_bytes`` bytes)."""
+    import numpy as np
+
+    eb = moe_gguf_expert_bytes(fmt, hidden, inter)
+    parts = [np.ascontiguousarray(w[k], np.uint8).reshape(-1) for k in ("gate", "up", "down")]
+    img = np.zeros(eb, np.uint8)
+    o = 0
+    for part in parts:
+        img[o:o + part.size] = part
+        o += part.size
+    if o > eb:
+        raise ValueError("weight shapes do not match the format")
+    C.memmove(ptr(dst), img.ctypes.data, eb)
+
+
+def alloc_gguf_workspace(T: int, k: int, hidden: int, inter: int, device="cuda"):
+    import torch
+
+    out = C.c_size_t(0)
+    check("moe_gguf_workspace_bytes", lib().moe_gguf_workspace_bytes(T, k, hidden, inter, C.byref(out)))
+    return torch.empty(max(out.value, 256), dtype=torch.uint8, device=device)
+
+
+def moe_expert_ffn_gguf(fmt, slots, n_slots: int, hidden: int, inter: int, x_bf16, plan: "RoutePlan", slot_of,
+                        n_experts: int, out, workspace, accumulate: bool = False, stream=None) -> None:
+    """The routed experts on GGUF weights (``moe_expert_ffn_gguf``); ``plan``
+    holds ids and w from ``moe_route_plan``."""
+    T = x_bf16.shape[0]
+    k = plan.ids.shape[1]
+    check("moe_expert_ffn_gguf",
+          lib().moe_expert_ffn_gguf(_fmt(fmt), ptr(slots), n_slots, hidden, inter, ptr(x_bf16), T, k,
+                                    ptr(plan.ids), ptr(plan.w), ptr(slot_of), n_experts, ptr(workspace),
+                                    workspace.numel(), ptr(out), 1 if accumulate else 0, stream_handle(stream)))
 
 
 def moe_probe_mxf8f6f4(stages: int, status, stream=None) -> int:

@@ -31,6 +31,8 @@ MOE_FFN_ACCUMULATE = 0x100
 MOE_POLICY_LRU, MOE_POLICY_FIFO, MOE_POLICY_LFU, MOE_POLICY_LFRU, MOE_POLICY_SLRU = 0, 1, 2, 3, 4
 POLICIES = {"lru": 0, "fifo": 1, "lfu": 2, "lfru": 3, "slru": 4}
 MOE_STAGE_WHOLE, MOE_STAGE_DECODE = 0, 1
+MOE_GGUF_Q8_0, MOE_GGUF_Q4_K = 0, 1
+GGUF_FORMATS = {"q8_0": MOE_GGUF_Q8_0, "q4_k": MOE_GGUF_Q4_K}
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _i32, _sz = C.c_void_p, C.c_int, C.c_size_t
@@ -88,6 +90,10 @@ SIGNATURES = {
     "moe_quant_mxfp4": (_i32, [_vp, _i32, _i32, _vp, _vp, _i32, _vp]),
     "moe_quant_mxfp8": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _vp]),
     "moe_probe_mxf8f6f4": (_i32, [_i32, _vp, C.POINTER(C.c_int), _vp]),
+    "moe_gguf_expert_bytes": (_i32, [_i32, _i32, _i32, _szp]),
+    "moe_gguf_workspace_bytes": (_i32, [_i32, _i32, _i32, _i32, _szp]),
+    "moe_expert_ffn_gguf": (_i32, [_i32, _vp, _i32, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _sz,
+                                   _vp, _i32, _vp]),
 }
 
 _lock = threading.Lock()

@@ -346,3 +346,33 @@ extern "C" int moe_quant_mxfp8(const void* x_bf16, int K, const int32_t* perm, i
     return moe::launch_quant_mxfp8(static_cast<const uint16_t*>(x_bf16), K, perm, k, rows, q, scales,
                                    scale_stride, static_cast<cudaStream_t>(stream));
 }
+
+extern "C" int moe_gguf_expert_bytes(int fmt, int hidden, int inter, size_t* out) {
+    if (!out) return MOE_ERR_INVALID;
+    const size_t b = moe::gguf_expert_bytes(fmt, hidden, inter);
+    if (!b) return MOE_ERR_INVALID;
+    *out = b;
+    return MOE_OK;
+}
+
+extern "C" int moe_gguf_workspace_bytes(int T, int k, int hidden, int inter, size_t* out) {
+    if (!out || T < 0 || k < 1 || k > MOE_MAX_TOPK || hidden <= 0 || inter <= 0) return MOE_ERR_INVALID;
+    *out = moe::gguf_workspace_bytes(T, k, hidden, inter);
+    return MOE_OK;
+}
+
+extern "C" int moe_expert_ffn_gguf(int fmt, const void* slots, int n_slots, int hidden, int inter, const void* x_bf16,
+                                   int T, int k, const int32_t* ids, const float* w, const int32_t* slot_of, int E,
+                                   void* workspace, size_t ws_bytes, float* out, int accumulate,
+                                   moe_stream_t stream) {
+    if (fmt != MOE_GGUF_Q8_0 && fmt != MOE_GGUF_Q4_K) return MOE_ERR_INVALID;
+    if (!moe::gguf_expert_bytes(fmt, hidden, inter)) return MOE_ERR_INVALID;
+    if (T < 0 || k < 1 || k > MOE_MAX_TOPK || E < 1 || E > MOE_MAX_EXPERTS || n_slots < 1) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    if (!slots || !x_bf16 || !ids || !w || !slot_of || !out || !workspace) return MOE_ERR_INVALID;
+    if (!aligned(slots, 256) || !aligned(workspace, 256) || !aligned(x_bf16, 4)) return MOE_ERR_INVALID;
+    if (ws_bytes < moe::gguf_workspace_bytes(T, k, hidden, inter)) return MOE_ERR_INVALID;
+    return moe::launch_gguf_ffn(fmt, static_cast<const uint8_t*>(slots), n_slots, E, hidden, inter,
+                                static_cast<const uint16_t*>(x_bf16), T, k, ids, w, slot_of, workspace, out,
+                                accumulate != 0, static_cast<cudaStream_t>(stream));
+}
