@@ -806,6 +806,70 @@ def gguf_obj(args, fmt, wid=4):
             "gpu_launches": args.steps * 5}
 
 
+def tiny_obj(args, threads):
+    """Config 0 (hidden 256, inter 512, 8 experts, top-2, 16 tokens, all
+    resident): the layer on both GPU paths (routing + expert FFN, graph,
+    CUDA events) and the oracle on one thread and on every host core."""
+    import torch
+
+    import oracle
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[0]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    E, k, H, I, T = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.tokens
+    host, slots, pool = _prefill_setup(M, wl, dev)
+    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
+    lg = torch.from_numpy(S.logits(wl, 0)).to(dev)
+    x = torch.from_numpy(S.activations_bf16_bits(wl, 0).view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    plan = M.RoutePlan.allocate(T, E, k, device=dev)
+    res = {"workload": wl.name, "config": {"hidden": H, "inter": I, "experts": E, "top_k": k, "tokens": T}}
+    stream = torch.cuda.Stream(device=dev)
+    for name, path in (("decode_path", M.MOE_PATH_DECODE), ("prefill_path", M.MOE_PATH_PREFILL)):
+        ws = M.alloc_ffn_workspace(T, k, H, I, path, device=dev)
+
+        def step():
+            M.moe_route_plan(lg, k, plan, stream=stream, with_counts_host=False)
+            M.moe_expert_ffn(pool, 0, x, plan, slot_of, out, ws, path=path, stream=stream)
+
+        with torch.cuda.stream(stream):
+            step()
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step()
+        for _ in range(args.warmup):
+            gr.replay()
+        torch.cuda.synchronize()
+        a, b = _events()
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(args.steps):
+                gr.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / args.steps * 1e3
+        res[name] = {"us_per_layer_call": us, "tokens_per_s": T / (us / 1e6)}
+    ws_all = S.stack_experts(S.layer_weights(wl, 0))
+    lgh, xbh = S.logits(wl, 0), S.activations_bf16_bits(wl, 0)
+    cpu = {}
+    for n in (1, threads):
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 1.0:
+            ids, w = oracle.route(lgh, k)
+            oracle.hist_perm(ids, E)
+            oracle.layer(xbh, ids, w, ws_all, prefill=False, threads=n)
+            reps += 1
+        cpu[n] = reps * T / (time.perf_counter() - t0)
+    res["cpu_baseline"] = {"value": cpu[threads], "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                           "sample": "the whole layer (16 tokens, decode-path arithmetic), repeated for a second",
+                           "single_thread_value": cpu[1]}
+    pool.close()
+    return res
+
+
 def prefill_obj(args, wl, mma, threads, cpu=True):
     res = prefill_timing(args, wl, soak_s=args.soak / 2)
     flops = 6.0 * wl.hidden * wl.inter * wl.tokens * wl.top_k
@@ -1152,6 +1216,7 @@ def main():
             off["cpu_baseline"] = cpu_offload_baseline(ow, args.cpu_layers, threads)
         line["offload"] = {ow.name: off}
         line["gguf_decode"] = {fmt: gguf_obj(args, fmt) for fmt in ("q4_k", "q8_0")}
+        line["tiny"] = tiny_obj(args, threads)
     if rank == 0:
         print(json.dumps(line))
 
