@@ -387,12 +387,21 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
         // CTA's items in the order the consumers take them, each as soon as
         // its assignment is known and its ring slot is free ----
         if (lane == 0) {
+        // per ring: next slot, its phase, and the next item's (assignment, row)
+        const int it0 = g0 * kGroup;
+        const int a0 = it0 / p.I;
+        int gu_slot = 0, gu_a = a0, gu_r = it0 - a0 * p.I;
+        uint32_t gu_ph = 0;
+        int d_slot = 0, d_a = a0, d_r = gu_r;
+        uint32_t d_ph = 0;
         auto issue_gu = [&](int n) -> bool {
-            const int slot = n % n_gu;
-            if (!tc::mbar_wait_suspend(&rb.empty_gu[slot], (uint32_t(n / n_gu) & 1u) ^ 1u, err, 4u)) return false;
+            const int slot = gu_slot;
+            const uint32_t ph = gu_ph;
+            const int a = gu_a, r = gu_r;
+            if (++gu_slot == n_gu) { gu_slot = 0; gu_ph ^= 1u; }
+            if ((gu_r += kGroup) == p.I) { gu_r = 0; ++gu_a; }
+            if (!tc::mbar_wait_suspend(&rb.empty_gu[slot], ph ^ 1u, err, 4u)) return false;
             if (n == 0 && p.stall) return true;   // test hook: the first item never lands
-            const int it = (g0 + n) * kGroup;
-            const int a = it / p.I, r = it - a * p.I;
             if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
             const uint8_t* eb = tab.base[a];
             uint8_t* dst = ring_gu + (size_t)slot * gu_bytes;
@@ -411,11 +420,13 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             return true;
         };
         auto issue_d = [&](int n) -> bool {
-            const int slot = n % n_d;
-            if (!tc::mbar_wait_suspend(&rb.empty_d[slot], (uint32_t(n / n_d) & 1u) ^ 1u, err, 4u)) return false;
+            const int slot = d_slot;
+            const uint32_t ph = d_ph;
+            const int a = d_a, r = d_r;
+            if (++d_slot == n_d) { d_slot = 0; d_ph ^= 1u; }
+            if ((d_r += kGroup) == p.I) { d_r = 0; ++d_a; }
+            if (!tc::mbar_wait_suspend(&rb.empty_d[slot], ph ^ 1u, err, 4u)) return false;
             if (n == 0 && p.stall) return true;
-            const int it = (g0 + n) * kGroup;
-            const int a = it / p.I, r = it - a * p.I;
             if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
             const uint8_t* eb = tab.base[a];
             if (eb != nullptr) {
@@ -475,15 +486,24 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                 y[m] = 0.0f;
             }
         };
+        // item state carried from item to item: assignment and row, ring
+        // slots and phases, the token's staged x, the h-exponent word
+        const int it0 = g0 * kGroup;
+        int a = it0 / p.I, r = it0 - a * p.I;
+        int sg = 0, sd = 0, hm = 0;
+        uint32_t ph_gu = 0, ph_d = 0;
+        const uint4* xt = xs;
+        const float* et = xe;
         for (int n = 0; n < cnt; ++n) {
-            const int a = (g0 + n) * kGroup / p.I;
             if (a != cur_a) {
                 flush(cur_a);
                 cur_a = a;
+                const int t = a / p.k;
+                xt = xs + (size_t)t * nbx * 4;
+                et = xe + t * nbx;
             }
             // (1) h for row r0 + j, once this warp's group of rows has landed
-            const int sg = n % n_gu;
-            const bool got = tc::mbar_wait_suspend(&rb.full_gu[sg][grp], uint32_t(n / n_gu) & 1u, err, 8u);
+            const bool got = tc::mbar_wait_suspend(&rb.full_gu[sg][grp], ph_gu, err, 8u);
             const uint8_t* eb = tab.base[a];
             const bool have = got && eb != nullptr;
             const uint8_t* sl = ring_gu + (size_t)sg * gu_bytes;
@@ -491,14 +511,12 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             if (have) {
                 const uint8_t* g = sl + (size_t)j * row_bytes;
                 const uint8_t* u = g + kGroup * row_bytes;
-                const int t = a / p.k;
-                const uint4* xt = xs + (size_t)t * nbx * 4;
-                const float* et = xe + t * nbx;
                 float ag = 0.0f, au = 0.0f;
 #pragma unroll
                 for (int i = 0; i < NG; ++i) {
                     const int b = lane + 32 * i;
-                    if (b < nbx) {
+                    // NG = ceil(nbx / 32): only the last group has lanes past nbx
+                    if (i < NG - 1 || b < nbx) {
                         const uint4 cg = *reinterpret_cast<const uint4*>(g + 16 * b);
                         const uint4 cu = *reinterpret_cast<const uint4*>(u + 16 * b);
                         const float xf = et[b];
@@ -519,17 +537,16 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             }
             if (lane == 0) {
                 hval[n & 1][j] = hj;
-                atomicMax(&hmax_bits[n % 3], __float_as_uint(fabsf(hj)));
+                atomicMax(&hmax_bits[hm], __float_as_uint(fabsf(hj)));
                 const __nv_bfloat16 hb = __float2bfloat16_rn(hj);
                 p.h[(size_t)(g0 + n) * kGroup + j] = *reinterpret_cast<const uint16_t*>(&hb);
             }
             named_bar_consumers();
             // the word of item n - 1 was last read before this barrier and is
             // next written after the following one
-            if (ct == 0 && n >= 1) hmax_bits[(n - 1) % 3] = 0u;
+            if (ct == 0 && n >= 1) hmax_bits[hm == 0 ? 2 : hm - 1] = 0u;
             // (2) y[n] += W[n][r0..r0+15] . h[r0..r0+15], once the block has landed
-            const int sd = n % n_d;
-            const bool gotd = tc::mbar_wait_suspend(&rb.full_d[sd], uint32_t(n / n_d) & 1u, err, 8u);
+            const bool gotd = tc::mbar_wait_suspend(&rb.full_d[sd], ph_d, err, 8u);
             if (have && gotd) {
                 // the 16 h values as f16 pairs under one power-of-2 scale (bf16 -> f16 is exact)
                 float hv[kGroup];
@@ -542,13 +559,14 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                     hv[4 * i + 3] = v4.w;
                 }
                 // scale 2^-e with e = exponent of the item's largest |h| minus 14
-                const int ef = int(hmax_bits[n % 3] >> 23);
+                const uint32_t hbits = hmax_bits[hm];
+                const int ef = int(hbits >> 23);
                 float mul, hf;
                 if (ef >= 15 && ef <= 254) {
                     mul = __uint_as_float(uint32_t(268 - ef) << 23);
                     hf = __uint_as_float(uint32_t(ef - 14) << 23);
                 } else {
-                    const int e = (hmax_bits[n % 3] == 0u) ? 0 : (ef == 0 ? -126 - 14 : ef - 127 - 14);
+                    const int e = (hbits == 0u) ? 0 : (ef == 0 ? -126 - 14 : ef - 127 - 14);
                     mul = ldexpf(1.0f, -e);
                     hf = ldexpf(1.0f, e);
                 }
@@ -563,7 +581,8 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
 #pragma unroll
                 for (int m = 0; m < NN; ++m) {
                     const int nn = ct + kConsumers * m;
-                    if (nn < p.H) {
+                    // NN = ceil(H / 512): only the last row group reaches past H
+                    if (m < NN - 1 || nn < p.H) {
                         const uint2 cw = *reinterpret_cast<const uint2*>(codes + (size_t)nn * (kGroup / 2));
                         uint32_t w0[4], w1[4];
                         e2m1x8_f16(cw.x, w0);
@@ -586,6 +605,10 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             }
             __syncwarp();
             if (lane == 0 && gotd) tc::mbar_arrive(&rb.empty_d[sd]);
+            if ((r += kGroup) == p.I) { r = 0; ++a; }
+            if (++sg == n_gu) { sg = 0; ph_gu ^= 1u; }
+            if (++sd == n_d) { sd = 0; ph_d ^= 1u; }
+            hm = (hm == 2) ? 0 : hm + 1;
         }
         flush(cur_a);
     }
