@@ -745,12 +745,17 @@ def prefill_timing(args, wl, soak_s=0.0):
     return res
 
 
-def gguf_obj(args, fmt, wid=4):
-    """Decode on GGUF expert weights read in place (moe_expert_ffn_gguf): one
-    Qwen-30B-A3B-shaped layer (128 experts, top-8) resident in GGUF form, one
-    token per step (a different token each step), routing + the two GGUF
-    launches graph-captured, L2 flushed before every step.  HBM bytes per
-    step: the routed experts' GGUF rows (gate, up, down)."""
+def gguf_obj(args, fmt, wid=4, layers=24):
+    """Decode on GGUF expert weights read in place: Qwen-30B-A3B-shaped
+    layers (128 experts, top-8) resident in GGUF form, one token per step
+    through ``layers`` layers back to back (each layer its own copy of the
+    experts at its own addresses and its own logits and activations, so a
+    layer's rows were last read ``layers`` - 1 layers earlier: about 0.5 GB
+    in between, well over L2).  The timed step is ``layers`` calls of
+    moe_decode_layer_gguf (routing and the experts in one launch each),
+    graph-captured; moe_route_plan + moe_expert_ffn_gguf (two calls per
+    layer) is timed beside it.  HBM bytes per layer: the routed experts'
+    GGUF rows (gate, up, down)."""
     import torch
 
     import oracle
@@ -758,65 +763,84 @@ def gguf_obj(args, fmt, wid=4):
 
     wl = S.WORKLOADS[wid]
     dev = torch.device("cuda", torch.cuda.current_device())
-    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    E, k, H, I, L = wl.experts, wl.top_k, wl.hidden, wl.inter, layers
     eb = M.moe_gguf_expert_bytes(fmt, H, I)
     img = torch.empty(E * eb, dtype=torch.uint8).pin_memory()
     for e in range(E):
         M.pack_gguf_expert(S.expert_weights_gguf(wl, fmt, 0, e), fmt, H, I, img.data_ptr() + e * eb)
-    slots = img.to(dev)
+    slots = torch.empty((L, E * eb), dtype=torch.uint8, device=dev)
+    slots[0].copy_(img)
+    for l in range(1, L):
+        slots[l].copy_(slots[0])
     slot_of = torch.arange(E, dtype=torch.int32, device=dev)
     G = args.warmup + args.steps
-    lg = torch.from_numpy(np.stack([S.logits(wl, 0, 0, G)[g:g + 1] for g in range(G)])).to(dev)
-    xb = torch.from_numpy(S.activations_bf16_bits(wl, 0, 0, G).view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(S.logits(wl, 0, 0, G * L).reshape(G, L, 1, E)).to(dev)
+    xb = torch.from_numpy(S.activations_bf16_bits(wl, 0, 0, G * L).view(np.int16).reshape(G, L, 1, H)).to(dev)
+    xb = xb.view(torch.bfloat16)
     out = torch.zeros((1, H), dtype=torch.float32, device=dev)
     plan = M.RoutePlan.allocate(1, E, k, device=dev)
     ws = M.alloc_gguf_workspace(1, k, H, I, device=dev)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    ev = [(_graph_event(), _graph_event()) for _ in range(G)]
 
-    def step(g):
-        flush.fill_(g & 255)
-        ev[g][0].record(stream)
-        M.moe_route_plan(lg[g], k, plan, stream=stream, with_counts_host=False)
-        M.moe_expert_ffn_gguf(fmt, slots, E, H, I, xb[g:g + 1], plan, slot_of, E, out, ws, accumulate=True,
-                              stream=stream)
-        ev[g][1].record(stream)
+    def timed(call):
+        ev = [(_graph_event(), _graph_event()) for _ in range(G)]
 
-    with torch.cuda.stream(stream):
-        step(0)
-    stream.synchronize()
-    graphs = []
-    for g in range(G):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=stream):
-            step(g)
-        graphs.append(gr)
-    for g in range(args.warmup):
-        graphs[g].replay()
-    torch.cuda.synchronize()
-    times = []
-    for g in range(args.warmup, G):
-        graphs[g].replay()
+        def step(g):
+            ev[g][0].record(stream)
+            for l in range(L):
+                call(g, l)
+            ev[g][1].record(stream)
+
+        with torch.cuda.stream(stream):
+            step(0)
+        stream.synchronize()
+        graphs = []
+        for g in range(G):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                step(g)
+            graphs.append(gr)
+        for g in range(args.warmup):
+            graphs[g].replay()
         torch.cuda.synchronize()
-        times.append(ev[g][0].elapsed_time(ev[g][1]))
+        times = []
+        for g in range(args.warmup, G):
+            graphs[g].replay()
+            torch.cuda.synchronize()
+            times.append(ev[g][0].elapsed_time(ev[g][1]))
+        return statistics.median(times)
+
+    def fused(g, l):
+        M.moe_decode_layer_gguf(fmt, slots[l], E, H, I, lg[g, l], xb[g, l], plan, slot_of, E, out, ws,
+                                accumulate=True, stream=stream)
+
+    def two_calls(g, l):
+        M.moe_route_plan(lg[g, l], k, plan, stream=stream, with_counts_host=False)
+        M.moe_expert_ffn_gguf(fmt, slots[l], E, H, I, xb[g, l], plan, slot_of, E, out, ws, accumulate=True,
+                              stream=stream)
+
+    ms = timed(fused)
+    ms_two = timed(two_calls)
+    status = M.moe_ffn_status(ws, M.MOE_PATH_DECODE, stream=stream)
+    if status:
+        raise RuntimeError(f"GGUF decode: status bits {status:#x}")
     rbh, rbi = oracle.gguf_row_bytes(fmt, H), oracle.gguf_row_bytes(fmt, I)
-    step_bytes = k * (2 * I * rbh + H * rbi)
-    ms = statistics.median(times)
+    layer_bytes = k * (2 * I * rbh + H * rbi)
     hbm_peak, _, peak_kind = _peaks()
-    achieved = step_bytes / (ms / 1e3) / 1e9
-    del slots, flush
+    achieved = layer_bytes / (ms / L / 1e3) / 1e9
+    del slots
     torch.cuda.empty_cache()
-    return {"workload": f"{wl.name}_decode_gguf_{fmt}", "value": 1e3 / ms, "unit": "tokens/s (one layer)",
-            "ms_per_step": ms,
+    return {"workload": f"{wl.name}_decode_gguf_{fmt}", "value": 1e3 / ms, "unit": f"tokens/s ({L} layers)",
+            "ms_per_step": ms, "us_per_layer": ms / L * 1e3,
             "config": {"hidden": H, "inter": I, "experts": E, "top_k": k, "tokens_per_step": 1, "format": fmt,
-                       "layers": 1, "l2": "256 MB flush before every step",
-                       "timing": "routing + moe_expert_ffn_gguf, graph per step, CUDA events"},
-            "roofline": {"kernel": "gguf_gateup_kernel + gguf_down_kernel + gguf_combine_kernel (routing included in the time)",
+                       "layers": L, "l2": f"{L} layers, each its own copy of the experts (no layer's rows in L2)",
+                       "timing": f"{L} x moe_decode_layer_gguf (one launch each), graph per step, CUDA events"},
+            "route_plus_ffn_us_per_layer": ms_two / L * 1e3,
+            "roofline": {"kernel": "gguf_fused_kernel: one launch per layer (routing, gate/up+SwiGLU, down, combine)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "peak_kind": peak_kind, "traffic": None,
-                         "algorithmic_bytes_per_launch": step_bytes},
-            "gpu_launches": args.steps * 5}
+                         "algorithmic_bytes_per_launch": layer_bytes},
+            "gpu_launches": args.steps * L}
 
 
 def tiny_obj(args, threads):

@@ -521,8 +521,13 @@ MOE_API int moe_quant_mxfp4(const void* x_bf16, int K, int rows, uint8_t* q, uin
  * Errors: MOE_ERR_INVALID. */
 MOE_API int moe_gguf_expert_bytes(int fmt, int hidden, int inter, size_t* out_bytes);
 
-/* Scratch bytes moe_expert_ffn_gguf needs: bf16 h [T*k][inter], then fp32
- * y [T*k][hidden] (each assignment's down output before the combine). */
+/* Workspace bytes of moe_expert_ffn_gguf and moe_decode_layer_gguf: a
+ * 256-byte control block (word 2: the status bits moe_ffn_status reads
+ * with MOE_PATH_DECODE), bf16 h [T*k][inter] at byte 256, then fp32 y
+ * [T*k][hidden] at 256 + round_up(T*k*inter*2, 256) (each assignment's down
+ * output before the combine, on the three-launch path).  Allocate it
+ * zero-filled: the single-launch kernel keeps cross-CTA counters in the
+ * control block and leaves them zero after every call. */
 MOE_API int moe_gguf_workspace_bytes(int T, int k, int hidden, int inter, size_t* out_bytes);
 
 /* The routed experts of one layer on GGUF weights read in place, the
@@ -530,8 +535,15 @@ MOE_API int moe_gguf_workspace_bytes(int T, int k, int hidden, int inter, size_t
  * bf16(silu(gate_e x_t) * up_e x_t), e = ids[t][j]; bf16 activations times
  * the exactly dequantised weights, fp32 sums (each block summed in its own
  * factors: d * sum(q x), or d*sc * sum(q x) - dmin*m * sum(x) per 32),
- * the k terms summed in rank order.  Three launches (gate/up with SwiGLU;
- * down per assignment; the combine), no atomics.
+ * the k terms summed in rank order, no floating-point atomics.  Calls of
+ * at most 32 assignments whose GGUF rows are multiples of 16 bytes (and x
+ * 16-byte aligned) run as one cooperative launch: one CTA per SM streams
+ * its gate/up rows through shared memory with bulk copies and fetches the
+ * down rows of its output rows early; it forms its output rows for all k
+ * ranks of their token, once (a bounded wait: about a second, then status
+ * bit 16 and NaN output) the other CTAs have written all of h of those
+ * assignments.  Other calls take three launches (gate/up with SwiGLU;
+ * down per assignment; the combine).
  *   fmt       MOE_GGUF_Q8_0 or MOE_GGUF_Q4_K
  *   slots     device [n_slots][moe_gguf_expert_bytes()] GGUF experts, 256-byte
  *             aligned
@@ -548,6 +560,26 @@ MOE_API int moe_expert_ffn_gguf(int fmt, const void* slots, int n_slots, int hid
                                 const void* x_bf16, int T, int k, const int32_t* ids, const float* w,
                                 const int32_t* slot_of, int E, void* workspace, size_t ws_bytes, float* out,
                                 int accumulate, moe_stream_t stream);
+
+/* One decode step of one layer on GGUF experts in a single launch: the
+ * routing of moe_route_plan fused with moe_expert_ffn_gguf, the way
+ * moe_decode_layer fuses it for MXFP4 pools [R1][R3].  Every CTA ranks the
+ * logits itself (larger logit first, equal logits by lower id, NaN last;
+ * softmax over the k selected); CTA 0 writes the routing outputs (ids, w,
+ * counts, offsets, perm, inv, as moe_route_plan defines them).  Results
+ * equal moe_route_plan + moe_expert_ffn_gguf on the same inputs.
+ *   logits    device fp32 [T][E]
+ *   x_bf16    device bf16 [T][hidden], 16-byte aligned
+ *   other arguments as moe_expert_ffn_gguf and moe_route_plan
+ * Limits: T*k <= 32, k <= E; the shape must take the single-launch kernel
+ * (MOE_ERR_UNSUPPORTED otherwise: GGUF rows not multiples of 16 bytes, or
+ * more shared memory than the GPU has).  Errors: MOE_ERR_INVALID,
+ * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API int moe_decode_layer_gguf(int fmt, const void* slots, int n_slots, int hidden, int inter,
+                                  const float* logits, const void* x_bf16, int T, int k, int32_t* ids, float* w,
+                                  int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                  const int32_t* slot_of, int E, void* workspace, size_t ws_bytes, float* out,
+                                  int accumulate, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Measurement                                                               */

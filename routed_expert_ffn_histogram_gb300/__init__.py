@@ -33,7 +33,7 @@ __all__ = [
     "moe_ffn_workspace_bytes", "alloc_ffn_workspace",
     "moe_expert_ffn", "moe_decode_layer", "moe_ffn_status", "moe_debug_stall_next_decode", "moe_combine",
     "moe_quant_mxfp8", "moe_quant_mxfp4", "moe_probe_mxf8f6f4", "moe_gguf_expert_bytes", "pack_gguf_expert",
-    "moe_expert_ffn_gguf", "alloc_gguf_workspace", "GGUF_FORMATS", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
+    "moe_expert_ffn_gguf", "moe_decode_layer_gguf", "alloc_gguf_workspace", "gguf_workspace_h", "GGUF_FORMATS", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
     "POLICIES", "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL", "MOE_FFN_ACCUMULATE",
 ]
 
@@ -222,7 +222,16 @@ def alloc_gguf_workspace(T: int, k: int, hidden: int, inter: int, device="cuda")
 
     out = C.c_size_t(0)
     check("moe_gguf_workspace_bytes", lib().moe_gguf_workspace_bytes(T, k, hidden, inter, C.byref(out)))
-    return torch.empty(max(out.value, 256), dtype=torch.uint8, device=device)
+    # zero-filled: the single-launch kernel keeps its cross-CTA counters here
+    return torch.zeros(max(out.value, 256), dtype=torch.uint8, device=device)
+
+
+def gguf_workspace_h(workspace, T: int, k: int, inter: int):
+    """The bf16 h [T*k][inter] held in a GGUF workspace (from byte 256), as
+    uint16 bits."""
+    import torch
+
+    return workspace[256:256 + T * k * inter * 2].view(torch.int16).view(T * k, inter)
 
 
 def moe_expert_ffn_gguf(fmt, slots, n_slots: int, hidden: int, inter: int, x_bf16, plan: "RoutePlan", slot_of,
@@ -235,6 +244,17 @@ def moe_expert_ffn_gguf(fmt, slots, n_slots: int, hidden: int, inter: int, x_bf1
           lib().moe_expert_ffn_gguf(_fmt(fmt), ptr(slots), n_slots, hidden, inter, ptr(x_bf16), T, k,
                                     ptr(plan.ids), ptr(plan.w), ptr(slot_of), n_experts, ptr(workspace),
                                     workspace.numel(), ptr(out), 1 if accumulate else 0, stream_handle(stream)))
+
+
+def moe_decode_layer_gguf(fmt, slots, n_slots: int, hidden: int, inter: int, logits, x_bf16, plan: "RoutePlan",
+                          slot_of, n_experts: int, out, workspace, accumulate: bool = False, stream=None) -> None:
+    """Routing + routed GGUF experts of one decode step in one launch
+    (``moe_decode_layer_gguf``); fills ``plan`` like moe_route_plan."""
+    T = x_bf16.shape[0]
+    check("moe_decode_layer_gguf", lib().moe_decode_layer_gguf(
+        _fmt(fmt), ptr(slots), n_slots, hidden, inter, ptr(logits), ptr(x_bf16), T, plan.k, ptr(plan.ids),
+        ptr(plan.w), ptr(plan.counts), ptr(plan.offsets), ptr(plan.perm), ptr(plan.inv), ptr(slot_of), n_experts,
+        ptr(workspace), workspace.numel(), ptr(out), 1 if accumulate else 0, stream_handle(stream)))
 
 
 def moe_probe_mxf8f6f4(stages: int, status, stream=None) -> int:

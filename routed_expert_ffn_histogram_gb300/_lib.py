@@ -94,6 +94,8 @@ SIGNATURES = {
     "moe_gguf_workspace_bytes": (_i32, [_i32, _i32, _i32, _i32, _szp]),
     "moe_expert_ffn_gguf": (_i32, [_i32, _vp, _i32, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _sz,
                                    _vp, _i32, _vp]),
+    "moe_decode_layer_gguf": (_i32, [_i32, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _vp, _i32, _vp, _sz, _vp, _i32, _vp]),
 }
 
 _lock = threading.Lock()

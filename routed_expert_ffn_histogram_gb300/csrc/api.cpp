@@ -361,6 +361,34 @@ extern "C" int moe_gguf_workspace_bytes(int T, int k, int hidden, int inter, siz
     return MOE_OK;
 }
 
+extern "C" int moe_decode_layer_gguf(int fmt, const void* slots, int n_slots, int hidden, int inter,
+                                     const float* logits, const void* x_bf16, int T, int k, int32_t* ids, float* w,
+                                     int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                     const int32_t* slot_of, int E, void* workspace, size_t ws_bytes, float* out,
+                                     int accumulate, moe_stream_t stream) {
+    if (fmt != MOE_GGUF_Q8_0 && fmt != MOE_GGUF_Q4_K) return MOE_ERR_INVALID;
+    if (!moe::gguf_expert_bytes(fmt, hidden, inter)) return MOE_ERR_INVALID;
+    if (T < 1 || k < 1 || k > MOE_MAX_TOPK || k > E || E > MOE_MAX_EXPERTS || n_slots < 1 || T * k > 32)
+        return MOE_ERR_INVALID;
+    if (!slots || !logits || !x_bf16 || !ids || !w || !counts || !offsets || !perm || !inv || !slot_of || !out ||
+        !workspace)
+        return MOE_ERR_INVALID;
+    if (!aligned(slots, 256) || !aligned(workspace, 256) || !aligned(x_bf16, 16)) return MOE_ERR_INVALID;
+    if (ws_bytes < moe::gguf_workspace_bytes(T, k, hidden, inter)) return MOE_ERR_INVALID;
+    if (!moe::gguf_fused_supported(fmt, T, k, hidden, inter)) return MOE_ERR_UNSUPPORTED;
+    moe::RouteOut ro;
+    ro.logits = logits;
+    ro.ids = ids;
+    ro.w = w;
+    ro.counts = counts;
+    ro.offsets = offsets;
+    ro.perm = perm;
+    ro.inv = inv;
+    return moe::launch_gguf_fused(fmt, static_cast<const uint8_t*>(slots), n_slots, E, hidden, inter,
+                                  static_cast<const uint16_t*>(x_bf16), T, k, nullptr, nullptr, slot_of, &ro,
+                                  workspace, out, accumulate != 0, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int moe_expert_ffn_gguf(int fmt, const void* slots, int n_slots, int hidden, int inter, const void* x_bf16,
                                    int T, int k, const int32_t* ids, const float* w, const int32_t* slot_of, int E,
                                    void* workspace, size_t ws_bytes, float* out, int accumulate,

@@ -530,7 +530,9 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                 if (lane == 0 && got) tc::mbar_arrive(&rb.empty_gu[sg]);
                 ag = warp_sum(ag);
                 au = warp_sum(au);
-                const float silu = ag / (1.0f + expf(-ag));
+                // fast exponential and division: a few fp32 ulps, far below
+                // the bf16 rounding of h that follows
+                const float silu = __fdividef(ag, 1.0f + __expf(-ag));
                 hj = __bfloat162float(__float2bfloat16_rn(silu * au));
             } else if (lane == 0 && got) {
                 tc::mbar_arrive(&rb.empty_gu[sg]);

@@ -19,7 +19,8 @@
 //
 // One expert in a slot is [gate I rows][up I rows][down H rows], each row
 // the format's blocks back to back; the slot size is a multiple of 256 bytes.
-// Three launches per call:
+// Calls of at most 32 assignments whose rows are multiples of 16 bytes run
+// as one launch (gguf_fused.cu); the others as three launches:
 //   gguf_gateup_kernel  one warp per (assignment, row pair), the gate and up
 //                       rows read in one pass: h = bf16(silu(g) u) into the
 //                       workspace; x staged once per CTA as fp32.
@@ -329,10 +330,6 @@ size_t gguf_expert_bytes(int fmt, int H, int I) {
     return round_up(2 * size_t(I) * rh + size_t(H) * ri, 256);
 }
 
-size_t gguf_workspace_bytes(int T, int k, int H, int I) {
-    return round_up(size_t(T) * k * I * 2, 256) + size_t(T) * k * H * 4;
-}
-
 int launch_gguf_ffn(int fmt, const uint8_t* slots, int S, int E, int H, int I, const uint16_t* x, int T, int k,
                     const int32_t* ids, const float* w, const int32_t* slot_of, void* ws, float* out,
                     bool accumulate, cudaStream_t s) {
@@ -351,11 +348,14 @@ int launch_gguf_ffn(int fmt, const uint8_t* slots, int S, int E, int H, int I, c
     p.ids = ids;
     p.w = w;
     p.slot_of = slot_of;
-    p.h = static_cast<uint16_t*>(ws);
-    p.y = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + round_up(size_t(T) * k * I * 2, 256));
+    p.h = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + gguf_h_offset());
+    p.y = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gguf_y_offset(T, k, I));
     p.out = out;
     p.accumulate = accumulate ? 1 : 0;
     if (T == 0) return MOE_OK;
+    // decode-sized calls whose rows suit bulk copies take the single-launch kernel
+    if (T * k <= 32 && reinterpret_cast<uintptr_t>(x) % 16 == 0 && gguf_fused_supported(fmt, T, k, H, I))
+        return launch_gguf_fused(fmt, slots, S, E, H, I, x, T, k, ids, w, slot_of, nullptr, ws, out, accumulate, s);
     return fmt == MOE_GGUF_Q8_0 ? launch_gguf<MOE_GGUF_Q8_0>(p, s) : launch_gguf<MOE_GGUF_Q4_K>(p, s);
 }
 

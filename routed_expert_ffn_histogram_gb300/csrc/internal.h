@@ -131,13 +131,20 @@ int launch_prefill_prepare(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStre
 int launch_prefill_experts(const FfnArgs& a, void* ws, int e0, int e1, const int32_t* slot_tab, int max_mtiles,
                            cudaStream_t s);
 
-// Decode on GGUF expert weights (gguf_decode.cu).
+// Decode on GGUF expert weights (gguf_decode.cu: three launches;
+// gguf_fused.cu: one launch, its workspace layout and counters).
 size_t gguf_row_bytes(int fmt, int K);
 size_t gguf_expert_bytes(int fmt, int H, int I);
 size_t gguf_workspace_bytes(int T, int k, int H, int I);
+size_t gguf_h_offset();
+size_t gguf_y_offset(int T, int k, int I);
 int launch_gguf_ffn(int fmt, const uint8_t* slots, int S, int E, int H, int I, const uint16_t* x, int T, int k,
                     const int32_t* ids, const float* w, const int32_t* slot_of, void* ws, float* out,
                     bool accumulate, cudaStream_t s);
+bool gguf_fused_supported(int fmt, int T, int k, int H, int I);
+int launch_gguf_fused(int fmt, const uint8_t* slots, int S, int E, int H, int I, const uint16_t* x, int T, int k,
+                      const int32_t* ids, const float* w, const int32_t* slot_of, const RouteOut* ro, void* ws,
+                      float* out, bool accumulate, cudaStream_t s);
 
 // Tensor-core rate probe (mma_probe.cu).
 int launch_mma_probe(int stages, uint32_t* err, int* ctas, cudaStream_t s);

@@ -1,10 +1,13 @@
 """GPU parity of the decode layer on GGUF expert weights (Q8_0, Q4_K) read
-in place (moe_expert_ffn_gguf) against the oracle's GGUF layer
-(oracle.layer_gguf, reading r22): the SwiGLU output h within one bf16 ulp
-and the layer output within the decode path's rel-L2 bound, at the
-Qwen-30B-A3B shape (both formats), the GPT-OSS shape (Q8_0: 2880 is not a
-multiple of 256) and the tiny shape; accumulate mode, a routed expert
-without a slot, and the shape refusals."""
+in place (moe_expert_ffn_gguf, moe_decode_layer_gguf) against the oracle's
+GGUF layer (oracle.layer_gguf, reading r22): the SwiGLU output h within one
+bf16 ulp and the layer output within the decode path's rel-L2 bound, at the
+Qwen-30B-A3B shape (both formats, the single-launch kernel), the GPT-OSS
+shape (Q8_0: rows of 3060 bytes take the three-launch path) and the tiny
+shape (single launch up to 32 assignments, three launches beyond);
+accumulate mode, a routed expert without a slot, fused routing equal to
+moe_route_plan, bitwise-repeatable output, counters left zero, and the
+shape refusals."""
 import numpy as np
 import pytest
 
@@ -74,12 +77,14 @@ def _run(M, wl, fmt, c, accumulate=False, out=None):
     M.moe_expert_ffn_gguf(fmt, c["slots"], c["n_slots"], wl.hidden, wl.inter, c["x"], c["plan"], c["slot_of"],
                           wl.experts, out, ws, accumulate=accumulate)
     torch.cuda.synchronize()
-    h = ws[: T * wl.top_k * wl.inter * 2].view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, wl.inter)
+    h = M.gguf_workspace_h(ws, T, wl.top_k, wl.inter).cpu().numpy().view(np.uint16)
+    assert M.moe_ffn_status(ws, M.MOE_PATH_DECODE) == 0
     return out.cpu().numpy(), h
 
 
-@pytest.mark.parametrize("fmt,wid,T", [("q4_k", 4, 1), ("q8_0", 4, 1), ("q4_k", 4, 3), ("q8_0", 1, 1),
-                                       ("q8_0", 0, 16), ("q4_k", 0, 16)])
+@pytest.mark.parametrize("fmt,wid,T", [("q4_k", 4, 1), ("q8_0", 4, 1), ("q4_k", 4, 3), ("q8_0", 4, 4),
+                                       ("q8_0", 1, 1), ("q8_0", 0, 16), ("q4_k", 0, 16), ("q4_k", 0, 17),
+                                       ("q8_0", 0, 20)])
 def test_gguf_layer_matches_oracle(fmt, wid, T):
     import routed_expert_ffn_histogram_gb300 as M
 
@@ -127,3 +132,67 @@ def test_gguf_shape_refusals():
     assert n.value == 256 * ((2 * 2880 * 90 * 34 + 2880 * 90 * 34 + 255) // 256)
     assert L.moe_expert_ffn_gguf(M.MOE_GGUF_Q4_K, 256, 1, 2880, 2880, 256, 1, 4, 1, 1, 1, 32, 256, 1 << 20, 256,
                                  0, None) == M.MOE_ERR_INVALID
+
+
+def _counters_zero(M, ws, T, k, H, I):
+    """The control block of a GGUF workspace (ticket, status, per-assignment
+    counters of h rows) is all zero."""
+    import torch
+
+    return not ws[:256].view(torch.int32).cpu().numpy().any()
+
+
+@pytest.mark.parametrize("fmt,wid,T", [("q4_k", 4, 1), ("q8_0", 4, 1), ("q4_k", 4, 4), ("q8_0", 0, 16)])
+def test_gguf_decode_layer_fused_routing(fmt, wid, T):
+    """moe_decode_layer_gguf: routing outputs equal moe_route_plan's bit for
+    bit, the layer equals the oracle's, repeated calls give the same bits
+    (no floating-point atomics), and the counters are zero afterwards."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[wid]
+    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    c = _setup(M, wl, fmt, T)
+    lg = torch.from_numpy(S.logits(wl, 0, 0, T)).cuda()
+    plan = M.RoutePlan.allocate(T, E, k)
+    ws = M.alloc_gguf_workspace(T, k, H, I)
+    outs = []
+    for _ in range(3):
+        out = torch.full((T, H), 7.0, dtype=torch.float32, device="cuda")
+        M.moe_decode_layer_gguf(fmt, c["slots"], c["n_slots"], H, I, lg, c["x"], plan, c["slot_of"], E, out, ws)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+        assert _counters_zero(M, ws, T, k, H, I)
+    for name in ("ids", "w", "counts", "offsets", "perm", "inv"):
+        assert np.array_equal(getattr(plan, name).cpu().numpy(), getattr(c["plan"], name).cpu().numpy()), name
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    ref, href = oracle.layer_gguf(fmt, c["xb"], c["ids"], c["w"], c["stacked"], threads=16, want_h=True)
+    _check_h(M.gguf_workspace_h(ws, T, k, I).cpu().numpy().view(np.uint16), href)
+    assert rel_l2(outs[0], ref) <= DECODE_REL_L2
+    assert M.moe_ffn_status(ws, M.MOE_PATH_DECODE) == 0
+    # accumulate: out += layer
+    base = torch.full((T, H), 0.25, dtype=torch.float32, device="cuda")
+    M.moe_decode_layer_gguf(fmt, c["slots"], c["n_slots"], H, I, lg, c["x"], plan, c["slot_of"], E, base, ws,
+                            accumulate=True)
+    assert rel_l2(base.cpu().numpy() - 0.25, ref) <= DECODE_REL_L2
+
+
+def test_gguf_single_launch_matches_three_launch():
+    """The same layer through the single-launch kernel (8 tokens x top-2 =
+    16 assignments) and the three-launch path (24 tokens: 48 assignments):
+    the first 8 tokens' outputs agree to fp32 summation order."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl, fmt = S.WORKLOADS[0], "q4_k"
+    c = _setup(M, wl, fmt, 24)
+    big, _ = _run(M, wl, fmt, c)
+    small_plan = M.RoutePlan.allocate(8, wl.experts, wl.top_k)
+    M.moe_route_plan(torch.from_numpy(S.logits(wl, 0, 0, 24)[:8]).cuda(), wl.top_k, small_plan)
+    ws = M.alloc_gguf_workspace(8, wl.top_k, wl.hidden, wl.inter)
+    out = torch.empty((8, wl.hidden), dtype=torch.float32, device="cuda")
+    M.moe_expert_ffn_gguf(fmt, c["slots"], c["n_slots"], wl.hidden, wl.inter, c["x"][:8], small_plan, c["slot_of"],
+                          wl.experts, out, ws)
+    assert rel_l2(out.cpu().numpy(), big[:8]) <= 1e-5
