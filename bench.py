@@ -888,6 +888,31 @@ def tiny_obj(args, threads):
         torch.cuda.synchronize()
         us = a.elapsed_time(b) / args.steps * 1e3
         res[name] = {"us_per_layer_call": us, "tokens_per_s": T / (us / 1e6)}
+    # the decode step as one launch: routing inside the kernel (moe_decode_layer)
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE, device=dev)
+
+    def fused_step():
+        M.moe_decode_layer(pool, 0, lg, x, plan, slot_of, out, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        fused_step()
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        fused_step()
+    for _ in range(args.warmup):
+        gr.replay()
+    torch.cuda.synchronize()
+    a, b = _events()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(args.steps):
+            gr.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / args.steps * 1e3
+    res["decode_layer"] = {"us_per_layer_call": us, "tokens_per_s": T / (us / 1e6),
+                           "how": "moe_decode_layer: routing and the experts in one launch"}
     ws_all = S.stack_experts(S.layer_weights(wl, 0))
     lgh, xbh = S.logits(wl, 0), S.activations_bf16_bits(wl, 0)
     cpu = {}

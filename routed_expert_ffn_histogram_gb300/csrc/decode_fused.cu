@@ -17,11 +17,13 @@
 // between runs.
 //
 // Shape: one CTA per SM, 18 warps in three roles.
-//   routing  warp 0 fetches the slot map and the token's logits in one
-//            memory round trip and ranks the logits (each top-k round two
-//            redux.sync warp reductions); each assignment's expert and slot
-//            are published through an mbarrier of their own as soon as its
-//            rank is decided, then the softmax weights.
+//   routing  warp 0 fetches the slot map and the first token's logits in
+//            one memory round trip (the other tokens' logits are prefetched
+//            into L1 at the same time) and ranks each token's logits, each
+//            top-k round two redux.sync warp reductions; each assignment's
+//            expert and slot are published through an mbarrier of their own
+//            as soon as its rank is decided, then one softmax pass weighs
+//            every assignment.
 //   copies   warp 1 (one lane) streams the CTA's work items: items of 16
 //            consecutive rows of h for one assignment.  The 16 gate and 16
 //            up rows (contiguous in the packed layout) go into a 3-slot ring
@@ -209,7 +211,7 @@ constexpr int kMaxAssign = MOE_DECODE_MAX_ASSIGN;
 constexpr int kConsumers = kThreads - 64;   // threads of warps 2..kGroup+1
 constexpr int kGuGroups = 4;                // arrival barriers per gate/up slot (4 consumer warps each)
 constexpr int kRowsPerGroup = kGroup / kGuGroups;
-constexpr int kMaxGuSlots = 3, kMaxDSlots = 2;
+constexpr int kMaxGuSlots = 8, kMaxDSlots = 8;
 
 // Per-CTA table of the routed assignments.
 struct AssignTable {
@@ -314,6 +316,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             // the slot map and the first token's logits are fetched together
             // (one memory round trip); lane l keeps slot_of[l + 32 i]
             const int epl = (p.E + 31) / 32;
+            if (p.T > 1) prefetch_l1(p.logits, p.T * p.E);
             int sl[EPL];
             float v[EPL];
 #pragma unroll
@@ -334,12 +337,10 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                     key[i] = rank_key(v[i]);
                     if (!in) taken |= 1u << i;
                 }
-                float sel_v = 0.0f;
                 for (int j = 0; j < p.k; ++j) {
                     const int bid = topk_round<EPL>(key, taken);
                     const int ws = from_winner<EPL>(sl, bid);   // the winner's slot
                     const float bv = from_winner<EPL>(v, bid);
-                    if (lane == j) sel_v = bv;
                     if (lane == 0) {
                         const int a = t * p.k + j;
                         const int slot = (bid >= 0 && bid < p.E) ? ws : -1;
@@ -349,9 +350,11 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                         tc::mbar_arrive(&rb.assigned[a]);
                     }
                 }
-                const float wv = softmax_lane(sel_v, p.k);
-                if (lane < p.k) tab.w[t * p.k + lane] = wv;
             }
+            // every assignment's weight in one pass (lane a: assignment a)
+            __syncwarp();
+            const float wv = softmax_assign(lane < A ? tab.sel_v[lane] : 0.0f, p.k, A);
+            if (lane < A) tab.w[lane] = wv;
         };
             if (p.E <= 32) route_all(std::integral_constant<int, 1>{});
             else if (p.E <= 64) route_all(std::integral_constant<int, 2>{});
@@ -650,18 +653,22 @@ static size_t d_slot_bytes(const Layout& L) { return round_up(size_t(L.H) * (kGr
 
 constexpr size_t kFusedSmemBudget = 216 * 1024;
 
-// Ring depths that fit: three gate/up slots when they fit, else two.
+// Ring depths: the deepest gate/up ring that fits (at most 8 slots, at
+// least 2), then the deepest down ring beside it (2 up to as many slots).
+// At the GPT-OSS shape that is 3 and 2; small shapes get 8 and 8, so their
+// many small items keep enough bytes in flight.
 static bool fused_rings(int T, const Layout& L, int* n_gu, int* n_d, size_t* bytes) {
     const size_t st = staging_bytes(T, L.H);
-    for (int g = kMaxGuSlots; g >= 2; --g) {
-        const size_t need = st + g * gu_slot_bytes(L) + kMaxDSlots * d_slot_bytes(L);
-        if (need <= kFusedSmemBudget) {
-            *n_gu = g;
-            *n_d = kMaxDSlots;
-            *bytes = need;
-            return true;
+    for (int g = kMaxGuSlots; g >= 2; --g)
+        for (int d = g < kMaxDSlots ? g : kMaxDSlots; d >= 2; --d) {
+            const size_t need = st + g * gu_slot_bytes(L) + d * d_slot_bytes(L);
+            if (need <= kFusedSmemBudget) {
+                *n_gu = g;
+                *n_d = d;
+                *bytes = need;
+                return true;
+            }
         }
-    }
     return false;
 }
 

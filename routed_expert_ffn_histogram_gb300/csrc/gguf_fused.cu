@@ -20,10 +20,11 @@
 // Shape: one persistent CTA per SM, 18 warps, launched cooperatively (all
 // CTAs resident at once, which the waits between CTAs below rely on).
 //   warp 0   routing when logits are given (slot map and logits in one round
-//            trip, top-k by two warp reductions per rank, softmax), else the
-//            given ids and weights; each assignment's expert and slot are
-//            published through their own mbarrier.  CTA 0 writes the routing
-//            outputs.
+//            trip, the other tokens' logits prefetched into L1; top-k by two
+//            warp reductions per rank; one softmax pass for all assignments),
+//            else the given ids and weights; each assignment's expert and
+//            slot are published through their own mbarrier as soon as its
+//            rank is decided.  CTA 0 writes the routing outputs.
 //   warp 1   lane 0 copies: the CTA's gate/up work items (up to 8 rows of h of
 //            one assignment: 8 gate and 8 up rows, two bulk copies) into a ring
 //            of shared-memory slots, and, once the ring is first full, the down
@@ -95,6 +96,7 @@ struct GfParams {
 struct Table {
     const uint8_t* base[kMaxAssign];
     float w[kMaxAssign];
+    float sel_v[kMaxAssign];
     int id[kMaxAssign];
 };
 
@@ -395,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) gguf_fused_kernel(GfParams p, Car
             auto route_all = [&](auto epl_tag) {
                 constexpr int EPL = decltype(epl_tag)::value;
                 const int epl = (p.E + 31) / 32;
+                if (p.T > 1) prefetch_l1(p.logits, p.T * p.E);
                 int sl[EPL];
                 float v[EPL];
 #pragma unroll
@@ -415,23 +418,24 @@ __global__ void __launch_bounds__(kThreads, 1) gguf_fused_kernel(GfParams p, Car
                         key[i] = rank_key(v[i]);
                         if (!in) taken |= 1u << i;
                     }
-                    float sel_v = 0.0f;
                     for (int j = 0; j < p.k; ++j) {
                         const int bid = topk_round<EPL>(key, taken);
-                        const int ws = from_winner<EPL>(sl, bid);
+                        const int ws = from_winner<EPL>(sl, bid);   // the winner's slot
                         const float bv = from_winner<EPL>(v, bid);
-                        if (lane == j) sel_v = bv;
                         if (lane == 0) {
                             const int a = t * p.k + j;
                             const int slot = (bid >= 0 && bid < p.E) ? ws : -1;
                             tab.id[a] = bid;
+                            tab.sel_v[a] = bv;
                             tab.base[a] = (slot >= 0 && slot < p.S) ? p.slots + (size_t)slot * p.expert_bytes : nullptr;
                             tc::mbar_arrive(&bars.assigned[a]);
                         }
                     }
-                    const float wv = softmax_lane(sel_v, p.k);
-                    if (lane < p.k) tab.w[t * p.k + lane] = wv;
                 }
+                // every assignment's weight in one pass (lane a: assignment a)
+                __syncwarp();
+                const float wv = softmax_assign(lane < A ? tab.sel_v[lane] : 0.0f, p.k, A);
+                if (lane < A) tab.w[lane] = wv;
             };
             if (p.E <= 32) route_all(std::integral_constant<int, 1>{});
             else if (p.E <= 64) route_all(std::integral_constant<int, 2>{});

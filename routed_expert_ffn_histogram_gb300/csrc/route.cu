@@ -177,19 +177,38 @@ __global__ void __launch_bounds__(32) route_tiny_kernel(
     int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
     const int lane = threadIdx.x;
     const int A = T * k;
-    int my_id = MOE_MAX_EXPERTS;  // sorts after every real id
+    __shared__ int sel_id[32];
+    __shared__ float sel_v[32];
+    // every token's logits in flight at once, then each token ranked: the
+    // lane holding a winner records it for its assignment
+    if (T > 1) prefetch_l1(logits, T * E);
     for (int t = 0; t < T; ++t) {
-        float sel_v;
-        int sel_id;
-        topk_warp<EPL>(logits + (size_t)t * E, E, k, sel_v, sel_id);
-        const float wv = softmax_lane(sel_v, k);
-        if (lane < k) {
-            ids[(size_t)t * k + lane] = sel_id;
-            w[(size_t)t * k + lane] = wv;
+        const float* row = logits + (size_t)t * E;
+        float v[EPL];
+        uint32_t key[EPL], taken = 0;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? __ldg(row + e) : 0.0f;
+            key[i] = rank_key(v[i]);
+            if (e >= E) taken |= 1u << i;
         }
-        const int src = lane - t * k;
-        const int got = __shfl_sync(0xffffffffu, sel_id, src & 31);
-        if (src >= 0 && src < k) my_id = got;
+        for (int j = 0; j < k; ++j) {
+            const int bid = topk_round<EPL>(key, taken);
+            const float bv = from_winner<EPL>(v, bid);
+            if (lane == 0) {
+                sel_id[t * k + j] = bid;
+                sel_v[t * k + j] = bv;
+            }
+        }
+    }
+    __syncwarp();
+    // one softmax pass for every assignment (lane a: assignment a)
+    const int my_id = lane < A ? sel_id[lane] : MOE_MAX_EXPERTS;   // MOE_MAX_EXPERTS sorts after every real id
+    const float wv = softmax_assign(lane < A ? sel_v[lane] : 0.0f, k, A);
+    if (lane < A) {
+        ids[lane] = my_id;
+        w[lane] = wv;
     }
     plan_warp(my_id, A, E, counts, offsets, perm, inv);
 }

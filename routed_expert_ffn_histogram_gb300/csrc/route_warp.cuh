@@ -83,6 +83,15 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, 
     }
 }
 
+// Prefetch a contiguous array of n floats into L1, a 128-byte line per lane
+// at a time, so the rows a warp ranks one after another are all in flight at
+// once instead of costing a memory round trip each.
+__device__ __forceinline__ void prefetch_l1(const float* base, int n) {
+    const int lane = threadIdx.x & 31;
+    for (int c = lane; c * 32 < n; c += 32)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(base + c * 32) : "memory");
+}
+
 // ---- float-float ("double-single") arithmetic --------------------------
 // A value is an unevaluated sum hi + lo of two floats (about 48 bits).  The
 // error-free transforms are Knuth's two-sum and the fma-based two-product;
@@ -156,6 +165,29 @@ __device__ __forceinline__ float softmax_lane(float sel_v, int k) {
     FF s{0.0f, 0.0f};
     for (int j = 0; j < k; ++j) {
         const FF ej{__shfl_sync(0xffffffffu, e.hi, j), __shfl_sync(0xffffffffu, e.lo, j)};
+        s = ff_add(s, ej);
+    }
+    const float q1 = __fdiv_rn(e.hi, s.hi);
+    FF qs = ff_two_prod(s.hi, q1);
+    qs.lo = __fmaf_rn(s.lo, q1, qs.lo);
+    const FF r = ff_add(e, FF{-qs.hi, -qs.lo});
+    return __fadd_rn(q1, __fdiv_rn(r.hi, s.hi));
+}
+
+// Softmax over each token's k selected logits for all A = T * k <= 32
+// assignments at once: lane a < A holds the selected logit of assignment a
+// (token a / k, rank a % k) and gets its weight; the same arithmetic as
+// softmax_lane (float-float exponentials of l_j - l_0, summed in rank order,
+// rounded once), every token in parallel.
+__device__ __forceinline__ float softmax_assign(float sel_v, int k, int A) {
+    const int lane = threadIdx.x & 31;
+    const int t0 = (lane < A && A > k) ? (lane / k) * k : 0;   // first assignment of the lane's token
+    const float m = __shfl_sync(0xffffffffu, sel_v, t0);
+    FF e{0.0f, 0.0f};
+    if (lane < A) e = ff_exp_nonpos(ff_two_sum(sel_v, -m));
+    FF s{0.0f, 0.0f};
+    for (int j = 0; j < k; ++j) {
+        const FF ej{__shfl_sync(0xffffffffu, e.hi, t0 + j), __shfl_sync(0xffffffffu, e.lo, t0 + j)};
         s = ff_add(s, ej);
     }
     const float q1 = __fdiv_rn(e.hi, s.hi);

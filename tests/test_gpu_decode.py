@@ -167,6 +167,41 @@ def test_decode_layer_fused_equals_two_calls(wid, T):
     assert rel_l2(out_a.cpu().numpy(), ref) <= DECODE_REL_L2
 
 
+@pytest.mark.parametrize("E,k,T", [(8, 2, 16), (32, 4, 3), (100, 8, 2), (256, 4, 1)])
+def test_decode_layer_routing_ties_nan(E, k, T):
+    """Fused routing on logits with ties (equal values on several experts),
+    NaN and -inf: the kernel's ids, weights and grouping equal
+    moe_route_plan's bit for bit, for one to sixteen tokens and 8 to 256
+    experts."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.Workload(0, "routing_ties", 1, 256, 512, E, k, T, 1, E, 0.0, 0)
+    pool, host, dev = make_pool(M, wl, layers=1)
+    rng = np.random.default_rng(7 + E)
+    lg_np = rng.integers(-3, 4, size=(T, E)).astype(np.float32)   # many ties
+    lg_np[0, 1] = np.nan
+    lg_np[-1, E - 1] = -np.inf
+    lg_np[-1, 0] = np.nan
+    x_np = S.activations_bf16_bits(wl, 0, 0, T)
+    lg = torch.from_numpy(lg_np).cuda()
+    x = torch.from_numpy(x_np.view(np.int16)).cuda().view(torch.bfloat16)
+    slot_of = torch.arange(E, dtype=torch.int32, device="cuda")
+    a, b = M.RoutePlan.allocate(T, E, k), M.RoutePlan.allocate(T, E, k)
+    out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, wl.hidden, wl.inter, M.MOE_PATH_DECODE)
+    M.moe_decode_layer(pool, 0, lg, x, a, slot_of, out, ws)
+    M.moe_route_plan(lg, k, b, with_counts_host=False)
+    torch.cuda.synchronize()
+    n = T * k
+    for key in ("ids", "w", "counts", "offsets"):
+        assert torch.equal(getattr(a, key), getattr(b, key)), key
+    assert torch.equal(a.perm[:n], b.perm[:n]) and torch.equal(a.inv[:n], b.inv[:n])
+    ids, _ = oracle.route(lg_np, k)
+    assert np.array_equal(a.ids.cpu().numpy(), ids)
+
+
 def _oracle_T(wl, lg, xbits, prefill):
     ids, w = oracle.route(lg, wl.top_k)
     uniq = sorted(set(ids.reshape(-1).tolist()))
