@@ -17,13 +17,14 @@
 // between runs.
 //
 // Shape: one CTA per SM, 18 warps in three roles.
-//   routing  warp 0 fetches the slot map and the first token's logits in
-//            one memory round trip (the other tokens' logits are prefetched
-//            into L1 at the same time) and ranks each token's logits, each
-//            top-k round two redux.sync warp reductions; each assignment's
-//            expert and slot are published through an mbarrier of their own
-//            as soon as its rank is decided, then one softmax pass weighs
-//            every assignment.
+//   routing  warp 0, and for several tokens up to 16 consumer warps too,
+//            each rank their own tokens: the slot map and the first token's
+//            logits in one memory round trip (later tokens' logits
+//            prefetched into L1 at the same time), each top-k round two
+//            redux.sync warp reductions; each assignment's expert and slot
+//            are published through an mbarrier of their own as soon as its
+//            rank is decided.  Once every router has reported, warp 0 weighs
+//            every assignment in one softmax pass.
 //   copies   warp 1 (one lane) streams the CTA's work items: items of 16
 //            consecutive rows of h for one assignment.  The 16 gate and 16
 //            up rows (contiguous in the packed layout) go into a 3-slot ring
@@ -239,6 +240,7 @@ struct Ring {
     uint64_t empty_gu[kMaxGuSlots];            // 16 consumer warps done with the slot's rows
     uint64_t full_d[kMaxDSlots];               // down block landed
     uint64_t empty_d[kMaxDSlots];              // 16 consumer warps done with the block
+    uint64_t ranked;                           // every routing warp has published its tokens' ranks
     uint64_t routed;                           // routing table (ids, weights, bases) written
     uint64_t assigned[kMaxAssign];             // assignment a's expert and slot known
 };
@@ -283,6 +285,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             tc::mbar_init(&rb.empty_d[s], kGroup);
         }
         tc::mbar_init(&rb.routed, 1);
+        tc::mbar_init(&rb.ranked, p.logits != nullptr ? unsigned(min(p.T, 1 + kConsumers / 32)) : 1u);
         hmax_bits[0] = hmax_bits[1] = hmax_bits[2] = 0u;
         for (int a = 0; a < A; ++a) tc::mbar_init(&rb.assigned[a], 1);
         tc::fence_barrier_init();
@@ -305,35 +308,40 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
     uint8_t* ring_gu = smem + gu_off;
     uint8_t* ring_d = smem + d_off;
 
-    if (warp == 0) {
-        // ---- routing (warp 0): each assignment's expert and slot are
-        // published (an mbarrier per assignment) as soon as its rank is
-        // decided, so the producer issues that assignment's copies while the
-        // remaining ranks are still being found ----
-        if (p.logits != nullptr) {
-        auto route_all = [&](auto epl_tag) {
+    // ---- routing: with logits, warp 0 and up to 16 consumer warps each rank
+    // their own tokens (t = r, r + R, ...; warp 0 is router 0, warp w >= 2
+    // router w - 1), before the consumers stage x.  Each assignment's expert
+    // and slot are published (an mbarrier per assignment) as soon as its
+    // rank is decided, so the producer issues that assignment's copies while
+    // the remaining ranks are still being found; warp 0 weighs every
+    // assignment once all routers have reported ----
+    const int R = (p.logits != nullptr) ? min(p.T, 1 + kConsumers / 32) : 0;
+    const int rw = (warp == 0) ? 0 : warp - 1;
+    if (p.logits != nullptr && (warp == 0 || (warp >= 2 && rw < R))) {
+        auto route_tokens = [&](auto epl_tag) {
             constexpr int EPL = decltype(epl_tag)::value;
-            // the slot map and the first token's logits are fetched together
-            // (one memory round trip); lane l keeps slot_of[l + 32 i]
+            // the slot map and this router's first token's logits are fetched
+            // together (one memory round trip); its later tokens' logits are
+            // prefetched at the same time; lane l keeps slot_of[l + 32 i]
             const int epl = (p.E + 31) / 32;
-            if (p.T > 1) prefetch_l1(p.logits, p.T * p.E);
+            for (int t = rw + R; t < p.T; t += R) prefetch_l1(p.logits + (size_t)t * p.E, p.E);
             int sl[EPL];
             float v[EPL];
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
                 const int e = lane + 32 * i;
                 const bool in = i < epl && e < p.E;
-                v[i] = in ? __ldg(p.logits + e) : 0.0f;
+                v[i] = in ? __ldg(p.logits + (size_t)rw * p.E + e) : 0.0f;
                 sl[i] = in ? __ldg(p.slot_of + e) : -1;
             }
-            for (int t = 0; t < p.T; ++t) {
+            for (int t = rw; t < p.T; t += R) {
                 const float* row = p.logits + (size_t)t * p.E;
                 uint32_t taken = 0, key[EPL];
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
                     const int e = lane + 32 * i;
                     const bool in = i < epl && e < p.E;
-                    if (t > 0) v[i] = in ? __ldg(row + e) : 0.0f;
+                    if (t > rw) v[i] = in ? __ldg(row + e) : 0.0f;
                     key[i] = rank_key(v[i]);
                     if (!in) taken |= 1u << i;
                 }
@@ -351,21 +359,27 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
                     }
                 }
             }
-            // every assignment's weight in one pass (lane a: assignment a)
-            __syncwarp();
-            const float wv = softmax_assign(lane < A ? tab.sel_v[lane] : 0.0f, p.k, A);
-            if (lane < A) tab.w[lane] = wv;
         };
-            if (p.E <= 32) route_all(std::integral_constant<int, 1>{});
-            else if (p.E <= 64) route_all(std::integral_constant<int, 2>{});
-            else if (p.E <= 128) route_all(std::integral_constant<int, 4>{});
-            else route_all(std::integral_constant<int, 8>{});
+        if (p.E <= 32) route_tokens(std::integral_constant<int, 1>{});
+        else if (p.E <= 64) route_tokens(std::integral_constant<int, 2>{});
+        else if (p.E <= 128) route_tokens(std::integral_constant<int, 4>{});
+        else route_tokens(std::integral_constant<int, 8>{});
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&rb.ranked);
+    }
+    if (warp == 0) {
+        if (p.logits != nullptr) {
+            // every assignment's weight in one pass (lane a: assignment a)
+            const bool ranked = tc::mbar_wait_suspend(&rb.ranked, 0u, err, 8u);
+            const float sv = (ranked && lane < A) ? tab.sel_v[lane] : __int_as_float(0x7fc00000);
+            const float wv = softmax_assign(sv, p.k, A);
+            if (lane < A) tab.w[lane] = wv;
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&rb.routed);
             if (blockIdx.x == 0) {
                 int my_id = MOE_MAX_EXPERTS;
                 if (lane < A) {
-                    my_id = tab.id[lane];
+                    my_id = ranked ? tab.id[lane] : -1;
                     p.r_ids[lane] = my_id;
                     p.r_w[lane] = tab.w[lane];
                 }

@@ -19,12 +19,14 @@
 //
 // Shape: one persistent CTA per SM, 18 warps, launched cooperatively (all
 // CTAs resident at once, which the waits between CTAs below rely on).
-//   warp 0   routing when logits are given (slot map and logits in one round
-//            trip, the other tokens' logits prefetched into L1; top-k by two
-//            warp reductions per rank; one softmax pass for all assignments),
-//            else the given ids and weights; each assignment's expert and
-//            slot are published through their own mbarrier as soon as its
-//            rank is decided.  CTA 0 writes the routing outputs.
+//   warp 0   routing when logits are given, with up to 16 consumer warps
+//            ranking further tokens of a batch (slot map and logits in one
+//            round trip, later tokens' logits prefetched into L1; top-k by
+//            two warp reductions per rank; each assignment's expert and slot
+//            published through their own mbarrier as soon as its rank is
+//            decided; then one softmax pass for all assignments by warp 0),
+//            else the given ids and weights.  CTA 0 writes the routing
+//            outputs.
 //   warp 1   lane 0 copies: the CTA's gate/up work items (up to 8 rows of h of
 //            one assignment: 8 gate and 8 up rows, two bulk copies) into a ring
 //            of shared-memory slots, and, once the ring is first full, the down
@@ -104,6 +106,7 @@ struct Bars {
     uint64_t full[kMaxSlots];
     uint64_t empty[kMaxSlots];
     uint64_t down_full;
+    uint64_t ranked;        // every routing warp has published its tokens' ranks
     uint64_t routed;
     uint64_t assigned[kMaxAssign];
 };
@@ -377,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) gguf_fused_kernel(GfParams p, Car
         }
         tc::mbar_init(&bars.down_full, 1);
         tc::mbar_init(&bars.routed, 1);
+        tc::mbar_init(&bars.ranked, p.logits != nullptr ? unsigned(min(p.T, 1 + kConsumerWarps)) : 1u);
         for (int a = 0; a < A; ++a) tc::mbar_init(&bars.assigned[a], 1);
         tc::fence_barrier_init();
     }
@@ -391,62 +395,72 @@ __global__ void __launch_bounds__(kThreads, 1) gguf_fused_kernel(GfParams p, Car
     uint8_t* ring = smem + cv.ring_off;
     uint8_t* dbuf = smem + cv.down_off;
 
-    if (warp == 0) {
-        // ---- routing ----
-        if (p.logits != nullptr) {
-            auto route_all = [&](auto epl_tag) {
-                constexpr int EPL = decltype(epl_tag)::value;
-                const int epl = (p.E + 31) / 32;
-                if (p.T > 1) prefetch_l1(p.logits, p.T * p.E);
-                int sl[EPL];
-                float v[EPL];
+    // ---- routing: with logits, warp 0 and up to 16 consumer warps each rank
+    // their own tokens (t = r, r + R, ...; warp 0 is router 0, warp w >= 2
+    // router w - 1), publishing each assignment as soon as its rank is
+    // decided; warp 0 weighs every assignment once all routers reported ----
+    const int R = (p.logits != nullptr) ? min(p.T, 1 + kConsumerWarps) : 0;
+    const int rw = (warp == 0) ? 0 : warp - 1;
+    if (p.logits != nullptr && (warp == 0 || (warp >= 2 && rw < R))) {
+        auto route_tokens = [&](auto epl_tag) {
+            constexpr int EPL = decltype(epl_tag)::value;
+            const int epl = (p.E + 31) / 32;
+            for (int t = rw + R; t < p.T; t += R) prefetch_l1(p.logits + (size_t)t * p.E, p.E);
+            int sl[EPL];
+            float v[EPL];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                const bool in = i < epl && e < p.E;
+                v[i] = in ? __ldg(p.logits + (size_t)rw * p.E + e) : 0.0f;
+                sl[i] = in ? __ldg(p.slot_of + e) : -1;
+            }
+            for (int t = rw; t < p.T; t += R) {
+                const float* row = p.logits + (size_t)t * p.E;
+                uint32_t taken = 0, key[EPL];
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
                     const int e = lane + 32 * i;
                     const bool in = i < epl && e < p.E;
-                    v[i] = in ? __ldg(p.logits + e) : 0.0f;
-                    sl[i] = in ? __ldg(p.slot_of + e) : -1;
+                    if (t > rw) v[i] = in ? __ldg(row + e) : 0.0f;
+                    key[i] = rank_key(v[i]);
+                    if (!in) taken |= 1u << i;
                 }
-                for (int t = 0; t < p.T; ++t) {
-                    const float* row = p.logits + (size_t)t * p.E;
-                    uint32_t taken = 0, key[EPL];
-#pragma unroll
-                    for (int i = 0; i < EPL; ++i) {
-                        const int e = lane + 32 * i;
-                        const bool in = i < epl && e < p.E;
-                        if (t > 0) v[i] = in ? __ldg(row + e) : 0.0f;
-                        key[i] = rank_key(v[i]);
-                        if (!in) taken |= 1u << i;
-                    }
-                    for (int j = 0; j < p.k; ++j) {
-                        const int bid = topk_round<EPL>(key, taken);
-                        const int ws = from_winner<EPL>(sl, bid);   // the winner's slot
-                        const float bv = from_winner<EPL>(v, bid);
-                        if (lane == 0) {
-                            const int a = t * p.k + j;
-                            const int slot = (bid >= 0 && bid < p.E) ? ws : -1;
-                            tab.id[a] = bid;
-                            tab.sel_v[a] = bv;
-                            tab.base[a] = (slot >= 0 && slot < p.S) ? p.slots + (size_t)slot * p.expert_bytes : nullptr;
-                            tc::mbar_arrive(&bars.assigned[a]);
-                        }
+                for (int j = 0; j < p.k; ++j) {
+                    const int bid = topk_round<EPL>(key, taken);
+                    const int ws = from_winner<EPL>(sl, bid);   // the winner's slot
+                    const float bv = from_winner<EPL>(v, bid);
+                    if (lane == 0) {
+                        const int a = t * p.k + j;
+                        const int slot = (bid >= 0 && bid < p.E) ? ws : -1;
+                        tab.id[a] = bid;
+                        tab.sel_v[a] = bv;
+                        tab.base[a] = (slot >= 0 && slot < p.S) ? p.slots + (size_t)slot * p.expert_bytes : nullptr;
+                        tc::mbar_arrive(&bars.assigned[a]);
                     }
                 }
-                // every assignment's weight in one pass (lane a: assignment a)
-                __syncwarp();
-                const float wv = softmax_assign(lane < A ? tab.sel_v[lane] : 0.0f, p.k, A);
-                if (lane < A) tab.w[lane] = wv;
-            };
-            if (p.E <= 32) route_all(std::integral_constant<int, 1>{});
-            else if (p.E <= 64) route_all(std::integral_constant<int, 2>{});
-            else if (p.E <= 128) route_all(std::integral_constant<int, 4>{});
-            else route_all(std::integral_constant<int, 8>{});
+            }
+        };
+        if (p.E <= 32) route_tokens(std::integral_constant<int, 1>{});
+        else if (p.E <= 64) route_tokens(std::integral_constant<int, 2>{});
+        else if (p.E <= 128) route_tokens(std::integral_constant<int, 4>{});
+        else route_tokens(std::integral_constant<int, 8>{});
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars.ranked);
+    }
+    if (warp == 0) {
+        if (p.logits != nullptr) {
+            // every assignment's weight in one pass (lane a: assignment a)
+            const bool ranked = tc::mbar_wait_suspend(&bars.ranked, 0u, err, 8u);
+            const float sv = (ranked && lane < A) ? tab.sel_v[lane] : __int_as_float(0x7fc00000);
+            const float wv = softmax_assign(sv, p.k, A);
+            if (lane < A) tab.w[lane] = wv;
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars.routed);
             if (blockIdx.x == 0) {
                 int my_id = MOE_MAX_EXPERTS;
                 if (lane < A) {
-                    my_id = tab.id[lane];
+                    my_id = ranked ? tab.id[lane] : -1;
                     p.r_ids[lane] = my_id;
                     p.r_w[lane] = tab.w[lane];
                 }
