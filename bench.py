@@ -53,7 +53,10 @@ METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 roo
 NCU_TRAFFIC = {
     # one decode layer (2-layer decode capture; traffic per launch does not
     # depend on the number of layers)
-    "decode_fused_kernel": 54_225_408 + 15_360,
+    "decode_fused_kernel": 54_205_952 + 16_640,
+    # one layer of the 24-layer GGUF leg (a launch after 40 others)
+    "gguf_fused_kernel/q4_k": 21_341_184 + 0,
+    "gguf_fused_kernel/q8_0": 40_212_736 + 768,
     # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
     "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_057_856 + 30_262_784) + (232_777_984 + 29_761_536),
 }
@@ -838,7 +841,8 @@ def gguf_obj(args, fmt, wid=4, layers=24):
             "route_plus_ffn_us_per_layer": ms_two / L * 1e3,
             "roofline": {"kernel": "gguf_fused_kernel: one launch per layer (routing, gate/up+SwiGLU, down, combine)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "peak_kind": peak_kind, "traffic": None,
+                         "frac": achieved / hbm_peak, "peak_kind": peak_kind,
+                         "traffic": NCU_TRAFFIC.get(f"gguf_fused_kernel/{fmt}") if wid == 4 else None,
                          "algorithmic_bytes_per_launch": layer_bytes},
             "gpu_launches": args.steps * L}
 
@@ -1172,6 +1176,8 @@ def main():
                     help="with --prefill-slots: unique experts per staging window (default slots // 2)")
     ap.add_argument("--policy-sweep", action="store_true",
                     help="with --workload 2: also replay the whole routing stream under every policy")
+    ap.add_argument("--gguf-only", action="store_true",
+                    help="run only the GGUF decode legs (both formats) and print their JSON line")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (smaller case for profiler captures)")
     args = ap.parse_args()
@@ -1199,6 +1205,11 @@ def main():
 
     B.build()
     import routed_expert_ffn_histogram_gb300 as M
+
+    if args.gguf_only:
+        if rank == 0:
+            print(json.dumps({"gguf_decode": {fmt: gguf_obj(args, fmt) for fmt in ("q4_k", "q8_0")}}))
+        return
 
     dev = torch.device("cuda", torch.cuda.current_device())
     if args.workload == 2:
