@@ -14,8 +14,9 @@
 // (d * sum(q x); d*sc * sum(q x) - dmin*m * sum(x)), the k terms of a token
 // summed in rank order.  The activations are held as f16 scaled per block
 // of 32 by a power of two (exact for every value within 2^-31 of the
-// block's largest), the codes as exact f16 integers, so each product q * x
-// is exact in fp32 (mixed-precision FMA).
+// block's largest) and the codes as exact f16 values (Q8_0: the integer q;
+// Q4_K: 8 + q/2, its bias taken out with the min term through sum(x)), so
+// each product is exact in fp32 (mixed-precision FMA).
 //
 // Shape: one persistent CTA per SM, 18 warps, launched cooperatively (all
 // CTAs resident at once, which the waits between CTAs below rely on).
@@ -152,14 +153,16 @@ __device__ __forceinline__ void fma2(float& acc0, float& acc1, uint32_t w2, uint
         : "r"(w2), "r"(x2));
 }
 
-// The 4-bit fields at bits 0..3 and 16..19 of v as exact f16 integers: each
-// field placed in the low mantissa bits of 1024 (f16 0x6400), then 1024
-// subtracted.
-__device__ __forceinline__ uint32_t nib2_f16(uint32_t v) {
-    uint32_t r, o;
-    asm("lop3.b32 %0, %1, 0x000f000f, 0x64006400, 0xea;" : "=r"(r) : "r"(v));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o) : "r"(r), "r"(0x64006400u));
-    return o;
+// The 4-bit fields at bits 6..9 and 22..25 of v as the f16 pair 8 + q/2:
+// each field placed in mantissa bits 6..9 of f16 8.0 (0x4800), where a unit
+// of the field is worth 1/2.  Exact, and a product (8 + q/2) * x is exact in
+// fp32; the bias is taken out per sub-block through sum(q x) = 2 sum((8 +
+// q/2) x) - 16 sum(x), folded into the Q4_K min term, which holds sum(x)
+// already.
+__device__ __forceinline__ uint32_t nib2_b8_f16(uint32_t v) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, 0x03c003c0, 0x48004800, 0xea;" : "=r"(r) : "r"(v));
+    return r;
 }
 
 // Two bytes of v (sel: byte indices in nibbles 0 and 2, 4 in nibbles 1 and
@@ -289,14 +292,17 @@ __device__ __forceinline__ void unit_dots(const uint8_t* const (&rows)[NR], int 
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 const uint2 wv = *reinterpret_cast<const uint2*>(rows[r] + 144 * sb + 16 + 32 * g + 8 * c);
-                fma2(a0[r], a1[r], nib2_f16(wv.x), xl.x);
-                fma2(a0[r], a1[r], nib2_f16(wv.x >> 8), xl.y);
-                fma2(b0[r], b1[r], nib2_f16(wv.x >> 4), xh.x);
-                fma2(b0[r], b1[r], nib2_f16(wv.x >> 12), xh.y);
-                fma2(a0[r], a1[r], nib2_f16(wv.y), xl.z);
-                fma2(a0[r], a1[r], nib2_f16(wv.y >> 8), xl.w);
-                fma2(b0[r], b1[r], nib2_f16(wv.y >> 4), xh.z);
-                fma2(b0[r], b1[r], nib2_f16(wv.y >> 12), xh.w);
+                // low nibbles of bytes 0 and 2 (bits 0, 16), of bytes 1 and 3
+                // (bits 8, 24); high nibbles of bytes 0, 2 (4, 20) and 1, 3
+                // (12, 28): each shifted to bits 6 and 22
+                fma2(a0[r], a1[r], nib2_b8_f16(wv.x << 6), xl.x);
+                fma2(a0[r], a1[r], nib2_b8_f16(wv.x >> 2), xl.y);
+                fma2(b0[r], b1[r], nib2_b8_f16(wv.x << 2), xh.x);
+                fma2(b0[r], b1[r], nib2_b8_f16(wv.x >> 6), xh.y);
+                fma2(a0[r], a1[r], nib2_b8_f16(wv.y << 6), xl.z);
+                fma2(a0[r], a1[r], nib2_b8_f16(wv.y >> 2), xl.w);
+                fma2(b0[r], b1[r], nib2_b8_f16(wv.y << 2), xh.z);
+                fma2(b0[r], b1[r], nib2_b8_f16(wv.y >> 6), xh.w);
             }
         }
         const float x0 = xs.sum[2 * u], x1 = xs.sum[2 * u + 1];
@@ -307,8 +313,10 @@ __device__ __forceinline__ void unit_dots(const uint8_t* const (&rows)[NR], int 
             q4k_scale_min(hdr, 2 * g, sc0, m0);
             q4k_scale_min(hdr, 2 * g + 1, sc1, m1);
             const float d = f16lo(hdr.x), dmin = f16lo(hdr.x >> 16);
-            acc[r] += ((d * sc0) * (f0 * (a0[r] + a1[r])) - (dmin * m0) * x0) +
-                      ((d * sc1) * (f1 * (b0[r] + b1[r])) - (dmin * m1) * x1);
+            // sum(w x) = d sc sum(q x) - dmin m sum(x), sum(q x) = 2 f sum(b x') - 16 sum(x)
+            const float ds0 = d * sc0, ds1 = d * sc1;
+            acc[r] += ((2.0f * ds0) * (f0 * (a0[r] + a1[r])) - (16.0f * ds0 + dmin * m0) * x0) +
+                      ((2.0f * ds1) * (f1 * (b0[r] + b1[r])) - (16.0f * ds1 + dmin * m1) * x1);
         }
     } else {
         // blocks 2u and 2u + 1: 68 bytes at 68 u (4-byte aligned); block 2u's
