@@ -55,8 +55,8 @@ NCU_TRAFFIC = {
     # depend on the number of layers)
     "decode_fused_kernel": 54_205_952 + 16_640,
     # one layer of the 24-layer GGUF leg (a launch after 40 others)
-    "gguf_fused_kernel/q4_k": 21_341_184 + 0,
-    "gguf_fused_kernel/q8_0": 40_212_736 + 768,
+    "gguf_fused_kernel/q4_k": 21_341_440 + 0,
+    "gguf_fused_kernel/q8_0": 40_212_736 + 2_304,
     # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
     "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_057_856 + 30_262_784) + (232_777_984 + 29_761_536),
 }
