@@ -367,6 +367,16 @@ def gpu_decode_leg(args, wl, host, rank, world):
     soak_n2, soak_s2 = _soak(replay, args.soak / 2)
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
+    # the same K steps once more, each step between its own pair of events:
+    # median and coefficient of variation of the step time
+    step_ev = [_events() for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for n, g in enumerate(range(args.warmup, G)):
+            step_ev[n][0].record(stream)
+            graphs[g].replay()
+            step_ev[n][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
 
     # e2e through the public API, host buffers, copies inside the timed region:
     # every step's logits, activations and residual row go up from pinned
@@ -444,7 +454,7 @@ def gpu_decode_leg(args, wl, host, rank, world):
     # up to the fp32 rounding order of the cross-CTA atomic sums
     ref_o = graph_out[args.warmup:].double()
     rel = float((out_pin[args.warmup:].to(dev).double() - ref_o).norm() / ref_o.norm().clamp_min(1e-30))
-    res = dict(elapsed_ms=elapsed_ms, clocks=clk, e2e_ms=e2e_ms,
+    res = dict(elapsed_ms=elapsed_ms, clocks=clk, e2e_ms=e2e_ms, step_ms=step_ms,
                soak={"steps": soak_n + soak_n2, "seconds": soak_s + soak_s2},
                h2d=(lg_pin[0].numel() * 4 + x_pin[0].numel() * 2 + (res_in.numel() * 4 if residual else 0)),
                d2h=out_pin[0].numel() * 4, e2e_matches_graph=rel <= 1e-6, expert_bytes=eb)
@@ -988,6 +998,9 @@ def prefill_obj(args, wl, mma, threads, cpu=True):
                         "traffic_scope": "DRAM bytes of the two GEMM launches of one layer",
                         "algorithmic_flops_per_launch": flops, "avg_launch_us": ffn_s * 1e6},
            "kernels_us": {"route_plan": statistics.median(res["route_ms"]) * 1e3, "expert_ffn": ffn_s * 1e6},
+           "ffn_times": {"median_ms": statistics.median(res["ffn_ms"]),
+                         "cv": (statistics.pstdev(res["ffn_ms"]) / statistics.mean(res["ffn_ms"])
+                                if len(res["ffn_ms"]) > 1 else 0.0)},
            "e2e": {"value": wl.tokens / (res["e2e_ms"] / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                    "d2h_bytes_per_step": res["d2h"],
                    "how": "moe_route_plan + moe_expert_ffn through the C ABI; logits and x from pinned host memory, "
@@ -1126,7 +1139,7 @@ def _standalone_line(obj, args):
             "warmup": args.warmup, "ms_per_step": obj["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": obj.get("dtype", "f32"), "data": "synthetic",
             "config": dict(workload=obj["workload"], **obj["config"])}
-    for key in ("roofline", "kernels_us", "staging", "e2e", "gpu_launches", "clocks", "cpu_baseline"):
+    for key in ("roofline", "kernels_us", "ffn_times", "staging", "e2e", "gpu_launches", "clocks", "cpu_baseline"):
         if key in obj:
             line[key] = obj[key]
     return line
@@ -1286,6 +1299,10 @@ def main():
                          "algorithmic_bytes_per_launch": layer_bytes,
                          "avg_launch_us": launch_s * 1e6},
             "kernels_us": {"decode_layer": launch_s * 1e6},
+            "step_times": {"median_ms": statistics.median(res["step_ms"]),
+                           "cv": (statistics.pstdev(res["step_ms"]) / statistics.mean(res["step_ms"])
+                                  if len(res["step_ms"]) > 1 else 0.0),
+                           "how": "the K steps again, each between its own pair of CUDA events"},
             "e2e": {"value": world * 1e3 / e2e_ms, "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"], "matches_graph_outputs": res["e2e_matches_graph"],
                     "how": "moe_decode_layer_acc x 24 per step through the C ABI (one captured graph per staging "

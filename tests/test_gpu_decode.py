@@ -167,7 +167,7 @@ def test_decode_layer_fused_equals_two_calls(wid, T):
     assert rel_l2(out_a.cpu().numpy(), ref) <= DECODE_REL_L2
 
 
-@pytest.mark.parametrize("E,k,T", [(8, 2, 16), (32, 4, 3), (100, 8, 2), (256, 4, 1)])
+@pytest.mark.parametrize("E,k,T", [(8, 2, 16), (32, 4, 3), (100, 8, 2), (256, 4, 1), (256, 2, 8), (64, 1, 32)])
 def test_decode_layer_routing_ties_nan(E, k, T):
     """Fused routing on logits with ties (equal values on several experts),
     NaN and -inf: the kernel's ids, weights and grouping equal

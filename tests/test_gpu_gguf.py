@@ -178,6 +178,31 @@ def test_gguf_decode_layer_fused_routing(fmt, wid, T):
     assert rel_l2(base.cpu().numpy() - 0.25, ref) <= DECODE_REL_L2
 
 
+def test_gguf_decode_layer_many_experts_and_tokens():
+    """The fused GGUF kernel's routing with 256 experts (eight candidates a
+    lane) and several routing warps (4 tokens): routing outputs equal
+    moe_route_plan's bit for bit and the layer equals the oracle's."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    base = S.WORKLOADS[0]
+    wl = S.Workload(0, "gguf_e256", 1, base.hidden, base.inter, 256, 4, 4, 1, 256, 0.0, 0)
+    fmt, T, E, k, H, I = "q8_0", 4, 256, 4, base.hidden, base.inter
+    c = _setup(M, wl, fmt, T)
+    lg = torch.from_numpy(S.logits(wl, 0, 0, T)).cuda()
+    plan = M.RoutePlan.allocate(T, E, k)
+    ws = M.alloc_gguf_workspace(T, k, H, I)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    M.moe_decode_layer_gguf(fmt, c["slots"], c["n_slots"], H, I, lg, c["x"], plan, c["slot_of"], E, out, ws)
+    torch.cuda.synchronize()
+    for name in ("ids", "w", "counts", "offsets", "perm", "inv"):
+        assert np.array_equal(getattr(plan, name).cpu().numpy(), getattr(c["plan"], name).cpu().numpy()), name
+    ref = oracle.layer_gguf(fmt, c["xb"], c["ids"], c["w"], c["stacked"], threads=16)
+    assert rel_l2(out.cpu().numpy(), ref) <= DECODE_REL_L2
+    assert _counters_zero(M, ws, T, k, H, I)
+
+
 def test_gguf_single_launch_matches_three_launch():
     """The same layer through the single-launch kernel (8 tokens x top-2 =
     16 assignments) and the three-launch path (24 tokens: 48 assignments):
