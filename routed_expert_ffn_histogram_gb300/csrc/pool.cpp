@@ -15,16 +15,11 @@
 // ascending id; then each absent member, ascending, takes the lowest free
 // slot or evicts a resident expert that is not in U, chosen by the pool's
 // policy (tinyserve README, "Configuration": cache_policy lru, lfru, slru,
-// lfu, fifo; "How it works" item 3: frequency-recency eviction):
-//   lru   touch: fresh stamp.             victim: oldest stamp.
-//   fifo  touch: nothing (stamp = load).  victim: oldest load.
-//   lfu   touch: count + 1.               victim: fewest uses, then lowest id.
-//   lfru  touch: count + 1, fresh stamp.  victim: fewest uses, then oldest stamp.
-//   slru  touch: fresh stamp; a probationary expert moves to the protected
-//         segment (capacity S / 2, at least 1), whose least recent member,
-//         if it overflows, goes back to probation with a fresh stamp.
-//         victim: oldest probationary, else oldest protected.
-// A loaded expert gets a fresh stamp, count 1, probation.
+// lfu, fifo; "How it works" item 3: frequency-recency eviction).  The
+// planning itself (touch, victim choice, load) is pool_plan.h, shared with
+// the device planner of pool_dev.cu, which keeps the state in device memory
+// and plans each event on the GPU from the device counts (no host round
+// trip), copying the misses with the SMs out of the mapped host store.
 //
 // Prefill through a pool smaller than the routed set (moe_prefill_staged):
 // tinyserve README, "How it works" item 6 (batched prefill groups tokens by
@@ -51,6 +46,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "pool_plan.h"
 
 struct moe_pool {
     moe_pool_desc d;
@@ -80,69 +76,16 @@ namespace {
 
 constexpr uint32_t kStateMagic = 0x4d4f4551u;  // "MOEQ": with routing frequencies and prefetch flags
 
-struct Planned {
-    int32_t e, slot, victim;
-};
-
 // Per-layer policy state, planned on copies and committed on success.
 struct LayerState {
     std::vector<int32_t> se, es;  // slot -> expert, expert -> slot
     std::vector<int64_t> st, uses;
     std::vector<int8_t> seg;
     int64_t clk = 0;
+    moe::PlanView view(int S, int E, int policy) {
+        return moe::PlanView{se.data(), es.data(), st.data(), uses.data(), seg.data(), clk, S, E, policy};
+    }
 };
-
-void touch(LayerState& ls, int s, int policy, int S) {
-    switch (policy) {
-        case MOE_POLICY_FIFO: break;
-        case MOE_POLICY_LFU: ++ls.uses[s]; break;
-        case MOE_POLICY_LFRU: ++ls.uses[s]; ls.st[s] = ++ls.clk; break;
-        case MOE_POLICY_SLRU: {
-            ls.st[s] = ++ls.clk;
-            if (ls.seg[s] == 0) {
-                ls.seg[s] = 1;
-                const int cap = S / 2 > 0 ? S / 2 : 1;
-                int n = 0, oldest = -1;
-                for (int i = 0; i < S; ++i)
-                    if (ls.se[i] >= 0 && ls.seg[i] == 1) {
-                        ++n;
-                        if (oldest < 0 || ls.st[i] < ls.st[oldest]) oldest = i;
-                    }
-                if (n > cap) {
-                    ls.seg[oldest] = 0;
-                    ls.st[oldest] = ++ls.clk;
-                }
-            }
-            break;
-        }
-        default: ls.st[s] = ++ls.clk; break;  // lru
-    }
-}
-
-// Slot to evict for a miss: a resident expert with counts[e] == 0 (not
-// routed in this event) and, when keep is given, keep[e] == 0 (not read by
-// work still in flight).
-int victim_slot(const LayerState& ls, int policy, int S, const int32_t* counts, const uint8_t* keep) {
-    int best = -1;
-    auto better = [&](int i, int b) -> bool {
-        switch (policy) {
-            case MOE_POLICY_LFU:
-                return ls.uses[i] != ls.uses[b] ? ls.uses[i] < ls.uses[b] : ls.se[i] < ls.se[b];
-            case MOE_POLICY_LFRU:
-                return ls.uses[i] != ls.uses[b] ? ls.uses[i] < ls.uses[b] : ls.st[i] < ls.st[b];
-            case MOE_POLICY_SLRU:
-                return ls.seg[i] != ls.seg[b] ? ls.seg[i] < ls.seg[b] : ls.st[i] < ls.st[b];
-            default:
-                return ls.st[i] < ls.st[b];  // lru, fifo
-        }
-    };
-    for (int i = 0; i < S; ++i) {
-        const int e = ls.se[i];
-        if (e < 0 || counts[e] > 0 || (keep && keep[e])) continue;
-        if (best < 0 || better(i, best)) best = i;
-    }
-    return best;
-}
 
 // Copy expert e of `layer` from the host store into slot `slot`: the whole
 // packed expert, or (MOE_STAGE_DECODE) the gate/up rows and the
@@ -274,38 +217,20 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
     ls.uses.assign(us, us + S);
     ls.seg.assign(sg, sg + S);
     ls.clk = clk;
-    uint64_t hits = 0;
-    std::vector<int> hit_e;
-    for (int e = 0; e < E; ++e)
-        if (counts[e] > 0 && ls.es[e] >= 0) {
-            touch(ls, ls.es[e], policy, S);
-            ++hits;
-            hit_e.push_back(e);
-        }
-    std::vector<Planned> plan;
-    for (int e = 0; e < E; ++e) {
-        if (counts[e] <= 0 || ls.es[e] >= 0) continue;
-        int s = -1;
-        for (int i = 0; i < S; ++i)
-            if (ls.se[i] < 0) { s = i; break; }
-        int victim = -1;
-        if (s < 0) {
-            s = victim_slot(ls, policy, S, counts, keep);
-            if (s < 0) return MOE_ERR_CAPACITY;  // U and keep together fill the slots
-            victim = ls.se[s];
-            ls.es[victim] = -1;
-        }
-        ls.se[s] = e;
-        ls.es[e] = s;
-        ls.st[s] = ++ls.clk;
-        ls.uses[s] = 1;
-        ls.seg[s] = 0;
-        plan.push_back({e, s, victim});
-    }
+    std::vector<moe::PlanLoad> plan(size_t(S) + 1);
+    std::vector<int32_t> hit_e(size_t(S) + 1);
+    int n_hits = 0;
+    moe::PlanView v = ls.view(S, E, policy);
+    const int n_loads = moe::plan_event(v, counts, keep, plan.data(), hit_e.data(), &n_hits);
+    if (n_loads < 0) return MOE_ERR_CAPACITY;  // U and keep together fill the slots
+    ls.clk = v.clk;
+    plan.resize(size_t(n_loads));
+    hit_e.resize(size_t(n_hits));
+    const uint64_t hits = uint64_t(n_hits);
 
     size_t done = 0;
     int fail = MOE_OK;
-    for (const Planned& q : plan) {
+    for (const moe::PlanLoad& q : plan) {
         if (p->inject_fail > 0) {
             --p->inject_fail;
             fail = moe::cuda_fail(cudaErrorUnknown);
@@ -328,7 +253,7 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
         // Keep only the loads that were enqueued (their slots now hold the new
         // experts); everything else of the event is not applied.
         for (size_t i = 0; i < done; ++i) {
-            const Planned& q = plan[i];
+            const moe::PlanLoad& q = plan[i];
             fr[q.e] = 0;
             if (q.victim >= 0) {
                 es[q.victim] = -1;
@@ -354,13 +279,13 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
         clk = ls.clk;
         c.hits += hits;
         c.misses += plan.size();
-        for (const Planned& q : plan) c.evictions += q.victim >= 0;
+        for (const moe::PlanLoad& q : plan) c.evictions += q.victim >= 0;
         for (int e : hit_e)
             if (fr[e]) {
                 ++c.prefetch_hits;
                 fr[e] = 0;
             }
-        for (const Planned& q : plan) {
+        for (const moe::PlanLoad& q : plan) {
             fr[q.e] = 0;
             if (q.victim >= 0) fr[q.victim] = 0;
         }
@@ -542,7 +467,6 @@ extern "C" int moe_pool_prefetch(moe_pool_t* p, int layer, int max_loads, moe_st
     for (int e = 0; e < E; ++e)
         if (es[e] < 0 && fq[e] > 0) cand.push_back(e);
     std::stable_sort(cand.begin(), cand.end(), [&](int a, int b) { return fq[a] > fq[b]; });
-    const std::vector<int32_t> none(size_t(E), 0);
     std::vector<uint8_t> mine(size_t(E), 0);  // loaded by this call: never victims
     int n = 0;
     for (int e : cand) {
@@ -560,7 +484,8 @@ extern "C" int moe_pool_prefetch(moe_pool_t* p, int layer, int max_loads, moe_st
             if (ls.se[i] < 0) { s = i; break; }
         int victim = -1;
         if (s < 0) {
-            s = victim_slot(ls, p->d.policy, S, none.data(), mine.data());
+            const moe::PlanView v = ls.view(S, E, p->d.policy);
+            s = moe::plan_victim(v, nullptr, mine.data());
             if (s < 0) break;
             victim = ls.se[s];
             if (fq[victim] >= fq[e]) break;  // only displace experts routed less often
