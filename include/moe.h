@@ -45,9 +45,10 @@
  *     calls that wait on the host are: moe_pool_stage and
  *     moe_prefill_staged (for the work enqueued so far on their compute
  *     stream, polling at most timeout_ms), moe_ffn_status (for the work
- *     enqueued so far on its stream, polling at most 10 s) and
- *     moe_pool_create with preload (synchronous copies of the preloaded
- *     experts); no other call waits.
+ *     enqueued so far on its stream, polling at most 10 s),
+ *     moe_pool_device_attach and moe_pool_device_detach (for their state
+ *     copies, polling at most timeout_ms) and moe_pool_create with preload
+ *     (synchronous copies of the preloaded experts); no other call waits.
  *   - Tensors are dense row-major.  T tokens, E experts, k top_k,
  *     H hidden size, I expert intermediate size, A = T*k assignments,
  *     assignment a = t*k + j is the j-th ranked expert of token t.
@@ -344,6 +345,60 @@ MOE_API int moe_prefill_staged(moe_pool_t* pool, int layer, const void* x_bf16, 
  * were enqueued). */
 MOE_API int moe_pool_prefetch(moe_pool_t* pool, int layer, int max_loads, moe_stream_t compute,
                               moe_stream_t copy, int* loaded);
+
+/* Device-planned staging [R2][X1]: the same staging events as
+ * moe_pool_stage (the planning code is shared, so every hit, miss, victim,
+ * stamp and counter comes out the same under every policy), with the
+ * pool's state for all layers kept in a caller-provided device buffer while
+ * attached, each event planned on the GPU from the routing counts in
+ * device memory, and the missed experts copied by the SMs straight out of
+ * the pinned host store through its device address (Grace hosts: the same
+ * link rate as the copy engines).  A layer's routing, staging and FFN are
+ * then three enqueues on one stream with no host wait or round trip
+ * between them (tinyserve README, "How it works" items 3 and 4).
+ *
+ * moe_pool_device_state_bytes: size of the device buffer (L records).
+ *
+ * moe_pool_device_attach: uploads the pool's state into dev_state (device,
+ *   16-byte aligned, >= moe_pool_device_state_bytes; caller-owned, must stay
+ *   untouched while attached) on `stream`, orders `stream` after the pool's
+ *   prefetch copies still in flight, and waits (polling, at most timeout_ms;
+ *   <= 0 means 10 s) for the upload.  The host store must be mapped into the
+ *   device's address space (cudaHostAlloc, or cudaHostRegister with
+ *   cudaHostRegisterMapped): MOE_ERR_UNSUPPORTED otherwise.  Work the caller
+ *   enqueued on other streams that reads the slots must be ordered before
+ *   `stream` by the caller.  Dry-run pools and attached pools: MOE_ERR_STATE.
+ *
+ * moe_pool_stage_device: enqueues on `stream` one event of `layer`:
+ *   counts_dev  device int32 [E] (moe_route_plan's counts), read on the GPU
+ *   slot_of_dev device int32 [E], written: the layer's slot map after the
+ *               event (-1 = absent), for moe_expert_ffn on the same stream
+ *   Then the misses' bytes (the whole packed expert, or the decode parts
+ *   with MOE_STAGE_DECODE) are copied host -> slot by a kernel on `stream`.
+ *   An event with a negative count or more than S routed experts changes
+ *   nothing (no copies; slot_of_dev gets the current map) and is reported
+ *   by moe_pool_device_detach.  Nothing waits on the host; the call may be
+ *   captured in a CUDA graph.  Copy-failure injection does not apply.
+ *
+ * moe_pool_device_detach: downloads the state into the pool on `stream`
+ *   (polling, at most timeout_ms) after the work enqueued so far; the
+ *   counters, slot maps, last loads and checkpoints then read as after the
+ *   same events staged by moe_pool_stage.  Returns MOE_ERR_INVALID if an
+ *   event saw a negative count, MOE_ERR_CAPACITY if one routed more than S
+ *   experts (the state is detached either way), MOE_ERR_TIMEOUT if the wait
+ *   ran out (still attached).
+ *
+ * While attached, moe_pool_stage, moe_prefill_staged, moe_pool_prefetch,
+ * moe_pool_counters, moe_pool_slot_map, moe_pool_last_loads, moe_pool_save
+ * and moe_pool_load return MOE_ERR_STATE.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_STATE, MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT, MOE_ERR_CUDA. */
+MOE_API int moe_pool_device_state_bytes(const moe_pool_t* pool, size_t* out_bytes);
+MOE_API int moe_pool_device_attach(moe_pool_t* pool, void* dev_state, size_t bytes, moe_stream_t stream,
+                                   int timeout_ms);
+MOE_API int moe_pool_stage_device(moe_pool_t* pool, int layer, const int32_t* counts_dev,
+                                  int32_t* slot_of_dev, moe_stream_t stream);
+MOE_API int moe_pool_device_detach(moe_pool_t* pool, moe_stream_t stream, int timeout_ms);
 
 /* Counters of one layer, or summed over all layers with layer = -1. */
 MOE_API int moe_pool_counters(const moe_pool_t* pool, int layer, moe_counters* out);

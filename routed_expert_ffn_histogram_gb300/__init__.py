@@ -321,6 +321,37 @@ class Pool:
         check("moe_pool_prefetch", lib().moe_pool_prefetch(self.handle, layer, max_loads, comp, cop, C.byref(n)))
         return n.value
 
+    def device_state_bytes(self) -> int:
+        """Bytes of the device buffer that device-planned staging keeps the
+        pool's state in (moe_pool_device_state_bytes)."""
+        n = C.c_size_t(0)
+        check("moe_pool_device_state_bytes", lib().moe_pool_device_state_bytes(self.handle, C.byref(n)))
+        return n.value
+
+    def device_attach(self, dev_state, stream=None, timeout_ms=10000) -> None:
+        """Move the pool's state into ``dev_state`` (a device tensor of at
+        least device_state_bytes() bytes) for device-planned staging."""
+        nbytes = dev_state.numel() * dev_state.element_size()
+        check("moe_pool_device_attach", lib().moe_pool_device_attach(
+            self.handle, ptr(dev_state), nbytes, stream_handle(stream), timeout_ms))
+
+    def stage_device(self, layer, counts_dev, slot_of_dev, stream=None) -> None:
+        """Enqueue one staging event planned on the GPU from the device
+        counts: slot map into ``slot_of_dev``, misses copied by the SMs from
+        the mapped host store (moe_pool_stage_device)."""
+        check("moe_pool_stage_device", lib().moe_pool_stage_device(
+            self.handle, layer, ptr(counts_dev), ptr(slot_of_dev), stream_handle(stream)))
+
+    def device_detach(self, stream=None, timeout_ms=10000) -> int:
+        """Bring the state back from the device; returns the status
+        (MOE_ERR_CAPACITY or MOE_ERR_INVALID report an event that changed
+        nothing; other errors raise)."""
+        rc = lib().moe_pool_device_detach(self.handle, stream_handle(stream), timeout_ms)
+        if rc in (MOE_OK, MOE_ERR_CAPACITY, MOE_ERR_INVALID):
+            return rc
+        check("moe_pool_device_detach", rc)
+        return rc
+
     def counters(self, layer=-1) -> dict:
         c = MoeCounters()
         check("moe_pool_counters", lib().moe_pool_counters(self.handle, layer, C.byref(c)))

@@ -76,6 +76,10 @@ SIGNATURES = {
     "moe_pool_save": (_i32, [_vp, _vp, _sz]),
     "moe_pool_load": (_i32, [_vp, _vp, _sz]),
     "moe_pool_inject_copy_failures": (_i32, [_vp, _i32]),
+    "moe_pool_device_state_bytes": (_i32, [_vp, _szp]),
+    "moe_pool_device_attach": (_i32, [_vp, _vp, _sz, _vp, _i32]),
+    "moe_pool_stage_device": (_i32, [_vp, _i32, _vp, _vp, _vp]),
+    "moe_pool_device_detach": (_i32, [_vp, _vp, _i32]),
     "moe_pool_destroy": (None, [_vp]),
     "moe_ffn_workspace_bytes": (_i32, [_i32, _i32, _i32, _i32, _i32, _szp]),
     "moe_expert_ffn": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp,

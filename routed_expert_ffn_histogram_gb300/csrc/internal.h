@@ -146,6 +146,13 @@ int launch_gguf_fused(int fmt, const uint8_t* slots, int S, int E, int H, int I,
                       const int32_t* ids, const float* w, const int32_t* slot_of, const RouteOut* ro, void* ws,
                       float* out, bool accumulate, cudaStream_t s);
 
+// Device-planned pool staging (pool_dev.cu): `rec` is the layer's record in
+// the device state (pool_plan.h, dev_record).
+int launch_pool_plan(uint8_t* rec, int S, int E, int policy, const int32_t* counts, int32_t* slot_of,
+                     uint64_t bytes_per_load, cudaStream_t s);
+int launch_pool_gather(const uint8_t* rec, int S, int E, const uint8_t* host_layer, uint8_t* slots_layer,
+                       size_t eb, size_t len0, size_t off1, size_t len1, cudaStream_t s);
+
 // Tensor-core rate probe (mma_probe.cu).
 int launch_mma_probe(int stages, uint32_t* err, int* ctas, cudaStream_t s);
 

@@ -70,6 +70,8 @@ struct moe_pool {
     cudaEvent_t ev_win[2] = {nullptr, nullptr};  // staged prefill: window GEMMs finished
     std::vector<cudaEvent_t> ev_pf;     // [L] the layer's last prefetch copies finished
     int inject_fail = 0;
+    uint8_t* dev_state = nullptr;       // device-planned staging: the state lives here while attached
+    const uint8_t* host_dev = nullptr;  // device address of host_experts (mapped pinned memory)
 };
 
 namespace {
@@ -317,6 +319,7 @@ int order_after_prefetch(moe_pool_t* p, int layer, cudaStream_t cs, cudaStream_t
 extern "C" int moe_pool_stage(moe_pool_t* p, int layer, const int32_t* counts_host, int32_t* slot_of_dev,
                               moe_stream_t compute, moe_stream_t copy, int timeout_ms) {
     if (!p || !counts_host || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     const int E = p->d.experts;
     cudaStream_t cs = static_cast<cudaStream_t>(compute), ps = static_cast<cudaStream_t>(copy);
     if (!p->d.dry_run) {
@@ -349,6 +352,7 @@ extern "C" int moe_prefill_staged(moe_pool_t* p, int layer, const void* x_bf16, 
     if (!p || !counts_host || layer < 0 || layer >= p->d.layers || T < 0 || k < 1 || k > p->d.experts ||
         k > MOE_MAX_TOPK)
         return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     const int S = p->d.slots_per_layer, E = p->d.experts;
     if (window < 1 || 2 * window > S) return MOE_ERR_INVALID;
     if (p->d.stage_parts == MOE_STAGE_DECODE) return MOE_ERR_UNSUPPORTED;  // no row-major down matrix
@@ -446,6 +450,7 @@ extern "C" int moe_pool_prefetch(moe_pool_t* p, int layer, int max_loads, moe_st
                                  int* loaded) {
     if (loaded) *loaded = 0;
     if (!p || layer < 0 || layer >= p->d.layers || max_loads < 0) return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     const int S = p->d.slots_per_layer, E = p->d.experts;
     const bool dry = p->d.dry_run;
     cudaStream_t cs = static_cast<cudaStream_t>(compute), ps = static_cast<cudaStream_t>(copy);
@@ -532,6 +537,7 @@ extern "C" int moe_pool_prefetch(moe_pool_t* p, int layer, int max_loads, moe_st
 
 extern "C" int moe_pool_counters(const moe_pool_t* p, int layer, moe_counters* out) {
     if (!p || !out || layer < -1 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     if (layer >= 0) {
         *out = p->ctr[layer];
         return MOE_OK;
@@ -553,12 +559,14 @@ extern "C" int moe_pool_counters(const moe_pool_t* p, int layer, moe_counters* o
 
 extern "C" int moe_pool_slot_map(const moe_pool_t* p, int layer, int32_t* out) {
     if (!p || !out || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     std::memcpy(out, &p->expert_slot[size_t(layer) * p->d.experts], sizeof(int32_t) * p->d.experts);
     return MOE_OK;
 }
 
 extern "C" int moe_pool_last_loads(const moe_pool_t* p, int layer, int32_t* le, int32_t* ls, int* n) {
     if (!p || !le || !ls || !n || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     const int S = p->d.slots_per_layer;
     *n = p->last_n[layer];
     for (int i = 0; i < *n; ++i) {
@@ -588,6 +596,7 @@ extern "C" int moe_pool_state_bytes(const moe_pool_t* p, size_t* out) {
 
 extern "C" int moe_pool_save(const moe_pool_t* p, void* buf, size_t bytes) {
     if (!p || !buf || bytes < state_bytes(p)) return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     uint8_t* o = static_cast<uint8_t*>(buf);
     StateHeader h{kStateMagic, p->d.layers, p->d.experts, p->d.slots_per_layer, p->d.hidden, p->d.inter,
                   p->d.policy};
@@ -608,6 +617,7 @@ extern "C" int moe_pool_save(const moe_pool_t* p, void* buf, size_t bytes) {
 
 extern "C" int moe_pool_load(moe_pool_t* p, const void* buf, size_t bytes) {
     if (!p || !buf || bytes < state_bytes(p)) return MOE_ERR_INVALID;
+    if (p->dev_state) return MOE_ERR_STATE;
     const uint8_t* i = static_cast<const uint8_t*>(buf);
     StateHeader h;
     std::memcpy(&h, i, sizeof h);
@@ -641,6 +651,134 @@ extern "C" int moe_pool_load(moe_pool_t* p, const void* buf, size_t bytes) {
     get(p->ctr.data(), p->ctr.size() * sizeof(moe_counters));
     get(p->freq.data(), p->freq.size() * 8);
     get(p->fresh.data(), p->fresh.size());
+    return MOE_OK;
+}
+
+// ---- device-planned staging -------------------------------------------------
+
+namespace {
+// Host state of every layer <-> the device records (pool_plan.h, dev_record).
+void pack_device_state(const moe_pool_t* p, uint8_t* img) {
+    const int S = p->d.slots_per_layer, E = p->d.experts;
+    const moe::DevRecord dr = moe::dev_record(S, E);
+    for (int l = 0; l < p->d.layers; ++l) {
+        uint8_t* r = img + size_t(l) * dr.bytes;
+        std::memset(r, 0, dr.bytes);
+        std::memcpy(r + dr.ctr, &p->ctr[l], sizeof(moe_counters));
+        std::memcpy(r + dr.clk, &p->clock[l], 8);
+        const int32_t n = p->last_n[l];
+        std::memcpy(r + dr.n_loads, &n, 4);
+        std::memcpy(r + dr.st, &p->stamp[size_t(l) * S], 8 * size_t(S));
+        std::memcpy(r + dr.uses, &p->uses[size_t(l) * S], 8 * size_t(S));
+        std::memcpy(r + dr.freq, &p->freq[size_t(l) * E], 8 * size_t(E));
+        std::memcpy(r + dr.se, &p->slot_expert[size_t(l) * S], 4 * size_t(S));
+        std::memcpy(r + dr.es, &p->expert_slot[size_t(l) * E], 4 * size_t(E));
+        std::memcpy(r + dr.le, &p->last_e[size_t(l) * S], 4 * size_t(S));
+        std::memcpy(r + dr.ls, &p->last_s[size_t(l) * S], 4 * size_t(S));
+        std::memcpy(r + dr.seg, &p->seg[size_t(l) * S], size_t(S));
+        std::memcpy(r + dr.fresh, &p->fresh[size_t(l) * E], size_t(E));
+    }
+}
+
+// Returns the union of the records' status bits.
+uint32_t unpack_device_state(moe_pool_t* p, const uint8_t* img) {
+    const int S = p->d.slots_per_layer, E = p->d.experts;
+    const moe::DevRecord dr = moe::dev_record(S, E);
+    uint32_t status = 0;
+    for (int l = 0; l < p->d.layers; ++l) {
+        const uint8_t* r = img + size_t(l) * dr.bytes;
+        std::memcpy(&p->ctr[l], r + dr.ctr, sizeof(moe_counters));
+        std::memcpy(&p->clock[l], r + dr.clk, 8);
+        int32_t n = 0;
+        std::memcpy(&n, r + dr.n_loads, 4);
+        p->last_n[l] = n;
+        uint32_t st = 0;
+        std::memcpy(&st, r + dr.status, 4);
+        status |= st;
+        std::memcpy(&p->stamp[size_t(l) * S], r + dr.st, 8 * size_t(S));
+        std::memcpy(&p->uses[size_t(l) * S], r + dr.uses, 8 * size_t(S));
+        std::memcpy(&p->freq[size_t(l) * E], r + dr.freq, 8 * size_t(E));
+        std::memcpy(&p->slot_expert[size_t(l) * S], r + dr.se, 4 * size_t(S));
+        std::memcpy(&p->expert_slot[size_t(l) * E], r + dr.es, 4 * size_t(E));
+        std::memcpy(&p->last_e[size_t(l) * S], r + dr.le, 4 * size_t(S));
+        std::memcpy(&p->last_s[size_t(l) * S], r + dr.ls, 4 * size_t(S));
+        std::memcpy(&p->seg[size_t(l) * S], r + dr.seg, size_t(S));
+        std::memcpy(&p->fresh[size_t(l) * E], r + dr.fresh, size_t(E));
+    }
+    return status;
+}
+
+size_t device_state_bytes(const moe_pool_t* p) {
+    return size_t(p->d.layers) * moe::dev_record(p->d.slots_per_layer, p->d.experts).bytes;
+}
+}  // namespace
+
+extern "C" int moe_pool_device_state_bytes(const moe_pool_t* p, size_t* out) {
+    if (!p || !out) return MOE_ERR_INVALID;
+    *out = device_state_bytes(p);
+    return MOE_OK;
+}
+
+extern "C" int moe_pool_device_attach(moe_pool_t* p, void* dev_state, size_t bytes, moe_stream_t stream,
+                                      int timeout_ms) {
+    if (!p || !dev_state || (reinterpret_cast<uintptr_t>(dev_state) & 15) || bytes < device_state_bytes(p))
+        return MOE_ERR_INVALID;
+    if (p->d.dry_run || p->dev_state) return MOE_ERR_STATE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* hd = nullptr;
+    if (cudaHostGetDevicePointer(&hd, p->d.host_experts, 0) != cudaSuccess || !hd) {
+        (void)cudaGetLastError();
+        return MOE_ERR_UNSUPPORTED;  // the host store is not mapped into the device's address space
+    }
+    // prefetch copies still in flight write slots: the device planner's
+    // copies and the FFNs that follow on `stream` come after them
+    for (int l = 0; l < p->d.layers; ++l)
+        if (p->pending[l]) {
+            MOE_CUDA_TRY(cudaStreamWaitEvent(s, p->ev_pf[l], 0));
+            p->pending[l] = 0;
+        }
+    std::vector<uint8_t> img(device_state_bytes(p));
+    pack_device_state(p, img.data());
+    MOE_CUDA_TRY(cudaMemcpyAsync(dev_state, img.data(), img.size(), cudaMemcpyHostToDevice, s));
+    const int rc = wait_stream(p, s, timeout_ms);  // img must outlive the copy
+    if (rc != MOE_OK) return rc;
+    p->dev_state = static_cast<uint8_t*>(dev_state);
+    p->host_dev = static_cast<const uint8_t*>(hd);
+    return MOE_OK;
+}
+
+extern "C" int moe_pool_stage_device(moe_pool_t* p, int layer, const int32_t* counts_dev, int32_t* slot_of_dev,
+                                     moe_stream_t stream) {
+    if (!p || !counts_dev || !slot_of_dev || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    if (!p->dev_state) return MOE_ERR_STATE;
+    const int S = p->d.slots_per_layer, E = p->d.experts;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* rec = p->dev_state + size_t(layer) * moe::dev_record(S, E).bytes;
+    int rc = moe::launch_pool_plan(rec, S, E, p->d.policy, counts_dev, slot_of_dev, p->bytes_per_load, s);
+    if (rc != MOE_OK) return rc;
+    const size_t eb = p->eb;
+    const bool decode = p->d.stage_parts == MOE_STAGE_DECODE;
+    const size_t len0 = decode ? p->L.d_off : eb;
+    const size_t off1 = decode ? p->L.dt_off : eb;
+    const size_t len1 = decode ? eb - p->L.dt_off : 0;
+    const uint8_t* host_layer = p->host_dev + size_t(layer) * size_t(E) * eb;
+    uint8_t* slots_layer = static_cast<uint8_t*>(p->d.dev_slots) + size_t(layer) * size_t(S) * eb;
+    return moe::launch_pool_gather(rec, S, E, host_layer, slots_layer, eb, len0, off1, len1, s);
+}
+
+extern "C" int moe_pool_device_detach(moe_pool_t* p, moe_stream_t stream, int timeout_ms) {
+    if (!p) return MOE_ERR_INVALID;
+    if (!p->dev_state) return MOE_ERR_STATE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::vector<uint8_t> img(device_state_bytes(p));
+    MOE_CUDA_TRY(cudaMemcpyAsync(img.data(), p->dev_state, img.size(), cudaMemcpyDeviceToHost, s));
+    const int rc = wait_stream(p, s, timeout_ms);
+    if (rc != MOE_OK) return rc;  // still attached; the caller may retry
+    const uint32_t status = unpack_device_state(p, img.data());
+    p->dev_state = nullptr;
+    p->host_dev = nullptr;
+    if (status & 1u) return MOE_ERR_INVALID;
+    if (status & 2u) return MOE_ERR_CAPACITY;
     return MOE_OK;
 }
 

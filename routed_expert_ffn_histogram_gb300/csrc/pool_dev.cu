@@ -1,0 +1,195 @@
+// Device-planned staging of the expert-slot pool: the policy state of every
+// layer lives in a caller-provided device buffer (one record per layer, laid
+// out by pool_plan.h's dev_record), each staging event is planned on the GPU
+// from the device counts that routing wrote, and the SMs copy the missed
+// experts out of the pinned host store through its mapped device address.
+//
+// Sources: tinyserve README, "How it works" item 1 (experts kept as raw
+// quantised bytes in pinned CPU memory), item 3 (cache keyed by (layer,
+// expert_id) with a GPU slot map) and item 4 (host-to-device traffic
+// overlapped with compute); llama.cpp discussion "fixed GPU expert working
+// set", main post (routed ids split into resident hits and misses).  The
+// decisions are those of the host pool (the planning code is shared); what
+// differs is where they are taken: on a Grace host the GPU reads pinned host
+// memory at the link rate itself, so the route -> plan -> copy -> FFN chain
+// of a layer runs on one stream with no host round trip between routing and
+// the copies.
+//
+// Kernels:
+//   pool_plan_kernel    one CTA of 256 threads: the layer's record is loaded
+//                       into shared memory by all threads, thread 0 plans
+//                       the event (pool_plan.h) and updates the counters,
+//                       all threads write the record back and the slot map.
+//   pool_gather_kernel  2 CTAs per SM: 64 KB chunks of the planned loads
+//                       (both staged parts of each expert), 16-byte loads
+//                       from host memory, four in flight per thread.
+#include <cstdint>
+
+#include "internal.h"
+#include "pool_plan.h"
+
+namespace moe {
+namespace {
+
+constexpr int kPlanThreads = 256;
+static_assert(kPlanThreads >= MOE_MAX_EXPERTS, "one thread per expert in the planner");
+constexpr int kGatherThreads = 512;
+constexpr unsigned long long kChunk = 64ull << 10;
+
+__global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, DevRecord dr, int S, int E,
+                                                                 int policy, const int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ slot_of,
+                                                                 unsigned long long bytes_per_load) {
+    __shared__ int32_t se[MOE_MAX_EXPERTS], es[MOE_MAX_EXPERTS], cnt[MOE_MAX_EXPERTS], hit_e[MOE_MAX_EXPERTS];
+    __shared__ int64_t st[MOE_MAX_EXPERTS], uses[MOE_MAX_EXPERTS];
+    __shared__ int8_t seg[MOE_MAX_EXPERTS];
+    __shared__ PlanLoad loads[MOE_MAX_EXPERTS];
+    __shared__ int ok_s;
+    const int t = threadIdx.x;
+    int32_t* g_se = reinterpret_cast<int32_t*>(rec + dr.se);
+    int32_t* g_es = reinterpret_cast<int32_t*>(rec + dr.es);
+    int64_t* g_st = reinterpret_cast<int64_t*>(rec + dr.st);
+    int64_t* g_uses = reinterpret_cast<int64_t*>(rec + dr.uses);
+    int8_t* g_seg = reinterpret_cast<int8_t*>(rec + dr.seg);
+    int64_t* g_freq = reinterpret_cast<int64_t*>(rec + dr.freq);
+    uint8_t* g_fresh = rec + dr.fresh;
+    if (t < S) {
+        se[t] = g_se[t];
+        st[t] = g_st[t];
+        uses[t] = g_uses[t];
+        seg[t] = g_seg[t];
+    }
+    int c = 0;
+    if (t < E) {
+        es[t] = g_es[t];
+        c = counts[t];
+        cnt[t] = c;
+    }
+    const int any_negative = __syncthreads_or(c < 0);
+    const int uniq = __syncthreads_count(c > 0);
+    if (t == 0) {
+        uint64_t* ctr = reinterpret_cast<uint64_t*>(rec + dr.ctr);  // moe_counters, field order
+        int64_t* g_clk = reinterpret_cast<int64_t*>(rec + dr.clk);
+        int32_t* g_n = reinterpret_cast<int32_t*>(rec + dr.n_loads);
+        int ok = 0;
+        if (!any_negative && uniq <= S) {
+            PlanView v{se, es, st, uses, seg, *g_clk, S, E, policy};
+            int nh = 0;
+            const int n = plan_event(v, cnt, nullptr, loads, hit_e, &nh);
+            if (n >= 0) {  // always, without a keep set: U fits in the slots
+                ok = 1;
+                *g_clk = v.clk;
+                int32_t* le = reinterpret_cast<int32_t*>(rec + dr.le);
+                int32_t* ls = reinterpret_cast<int32_t*>(rec + dr.ls);
+                uint64_t ev = 0;
+                for (int i = 0; i < n; ++i) {
+                    le[i] = loads[i].e;
+                    ls[i] = loads[i].slot;
+                    ev += loads[i].victim >= 0;
+                }
+                ctr[0] += uint64_t(nh);                     // hits
+                ctr[1] += uint64_t(n);                      // misses
+                ctr[2] += ev;                               // evictions
+                ctr[3] += uint64_t(n) * bytes_per_load;     // h2d_bytes
+                ctr[5] += 1;                                // events
+                for (int i = 0; i < nh; ++i)
+                    if (g_fresh[hit_e[i]]) {
+                        ctr[7] += 1;                        // prefetch_hits
+                        g_fresh[hit_e[i]] = 0;
+                    }
+                for (int i = 0; i < n; ++i) {
+                    g_fresh[loads[i].e] = 0;
+                    if (loads[i].victim >= 0) g_fresh[loads[i].victim] = 0;
+                }
+                *g_n = n;
+            }
+        }
+        if (!ok) {
+            // nothing changes: the planned copies are none and the slot map
+            // stays the current one (routed experts that are absent stay -1)
+            *reinterpret_cast<int32_t*>(rec + dr.status) |= any_negative ? 1 : 2;
+            *g_n = 0;
+        }
+        ok_s = ok;
+    }
+    __syncthreads();
+    if (ok_s) {
+        if (t < S) {
+            g_se[t] = se[t];
+            g_st[t] = st[t];
+            g_uses[t] = uses[t];
+            g_seg[t] = seg[t];
+        }
+        if (t < E) {
+            g_es[t] = es[t];
+            g_freq[t] += cnt[t] > 0;
+        }
+    }
+    if (t < E) slot_of[t] = es[t];
+}
+
+__global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8_t* rec, DevRecord dr,
+                                                                     const uint8_t* host_layer, uint8_t* slots_layer,
+                                                                     unsigned long long eb, unsigned long long len0,
+                                                                     unsigned long long off1, unsigned long long len1) {
+    const int n = *reinterpret_cast<const int32_t*>(rec + dr.n_loads);
+    const int32_t* le = reinterpret_cast<const int32_t*>(rec + dr.le);
+    const int32_t* ls = reinterpret_cast<const int32_t*>(rec + dr.ls);
+    const unsigned long long c0 = (len0 + kChunk - 1) / kChunk, c1 = (len1 + kChunk - 1) / kChunk;
+    const unsigned long long cpl = c0 + c1;
+    for (unsigned long long c = blockIdx.x; c < (unsigned long long)n * cpl; c += gridDim.x) {
+        const unsigned long long i = c / cpl;
+        unsigned long long r = c - i * cpl, base, len;
+        if (r < c0) {
+            base = r * kChunk;
+            len = min(kChunk, len0 - base);
+        } else {
+            r -= c0;
+            base = off1 + r * kChunk;
+            len = min(kChunk, len1 - r * kChunk);
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(host_layer + (unsigned long long)le[i] * eb + base);
+        uint4* dst = reinterpret_cast<uint4*>(slots_layer + (unsigned long long)ls[i] * eb + base);
+        const unsigned long long n16 = len / 16;
+        for (unsigned long long j = threadIdx.x; j < n16; j += 4ull * kGatherThreads) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const unsigned long long jj = j + (unsigned long long)u * kGatherThreads;
+                if (jj < n16) v[u] = __ldg(src + jj);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const unsigned long long jj = j + (unsigned long long)u * kGatherThreads;
+                if (jj < n16) dst[jj] = v[u];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int launch_pool_plan(uint8_t* rec, int S, int E, int policy, const int32_t* counts, int32_t* slot_of,
+                     uint64_t bytes_per_load, cudaStream_t s) {
+    if (E > MOE_MAX_EXPERTS || S > E) return MOE_ERR_INVALID;
+    pool_plan_kernel<<<1, kPlanThreads, 0, s>>>(rec, dev_record(S, E), S, E, policy, counts, slot_of,
+                                                  (unsigned long long)bytes_per_load);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int launch_pool_gather(const uint8_t* rec, int S, int E, const uint8_t* host_layer, uint8_t* slots_layer,
+                       size_t eb, size_t len0, size_t off1, size_t len1, cudaStream_t s) {
+    if ((eb | len0 | off1 | len1) & 15) return MOE_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(host_layer) | reinterpret_cast<uintptr_t>(slots_layer)) & 15)
+        return MOE_ERR_INVALID;
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != MOE_OK) return rc;
+    pool_gather_kernel<<<2 * di.sms, kGatherThreads, 0, s>>>(rec, dev_record(S, E), host_layer, slots_layer, eb,
+                                                             len0, off1, len1);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -184,3 +184,125 @@ def test_offload_decode_with_prefetch():
     tot = pool.counters()
     assert tot["prefetch_hits"] > 0 and checked > 6
     pool.close()
+
+
+@pytest.mark.parametrize("policy,parts", [("lru", "decode"), ("fifo", "whole"), ("lfu", "decode"),
+                                          ("lfru", "decode"), ("slru", "decode")])
+def test_offload_device_planned_staging(policy, parts):
+    """Staging events planned on the GPU (moe_pool_stage_device) from the
+    device counts, with the misses copied by the SMs out of the mapped host
+    store: per (layer, step) event the slot map the planner writes equals
+    the oracle's policy simulation; staged slots hold the host store's
+    bytes; layer outputs match the oracle; after detaching, every layer's
+    counters, last loads and slot map equal the oracle's.  Host staging
+    before attaching and after detaching continues the same state."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    L = 3
+    pool, host, dev = make_pool(M, wl, layers=L, preload=False)
+    pool.close()
+    pool = M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev,
+                  policy=policy, stage_parts=parts)
+    ref = [oracle.PolicyPool(wl.slots, wl.experts, policy) for _ in range(L)]
+    T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
+    eb = M.moe_expert_bytes(H, I)
+    plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    last = [[] for _ in range(L)]
+    with torch.cuda.stream(stream):
+        for step in range(14):
+            device_side = 4 <= step < 12
+            if step == 4:
+                pool.device_attach(state, stream=stream)
+                with pytest.raises(M.MoeError):
+                    pool.counters(0)
+                counts_h = torch.zeros(E, dtype=torch.int32).pin_memory()
+                with pytest.raises(M.MoeError):
+                    pool.stage(0, counts_h, slot_of, compute=stream)
+            if step == 12:
+                assert pool.device_detach(stream=stream) == M.MOE_OK
+                for layer in range(L):
+                    c, e = pool.counters(layer), ref[layer].counters()
+                    assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+                    assert pool.last_loads(layer) == last[layer]
+                    assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
+            for layer in range(L):
+                lg = torch.from_numpy(S.logits(wl, layer, step)).cuda()
+                x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step).view(np.int16)).cuda().view(
+                    torch.bfloat16)
+                M.moe_route_plan(lg, k, plan, stream=stream)
+                if device_side:
+                    pool.stage_device(layer, plan.counts, slot_of, stream=stream)
+                    stream.synchronize()
+                    counts = plan.counts_host.numpy().copy()
+                    loads = ref[layer].step(counts)
+                    last[layer] = loads
+                    assert np.array_equal(slot_of.cpu().numpy(), ref[layer].slot_map())
+                    for e, s in loads:  # the staged parts, sampled at both ends of each
+                        got = dev[(layer * wl.slots + s) * eb:(layer * wl.slots + s + 1) * eb]
+                        want = host[((layer * E) + e) * eb:((layer * E) + e + 1) * eb]
+                        assert torch.equal(got[:4096].cpu(), want[:4096])
+                        assert torch.equal(got[-4096:].cpu(), want[-4096:])
+                else:
+                    assert pool.stage(layer, plan.counts_host, slot_of, compute=stream) == M.MOE_OK
+                    counts = plan.counts_host.numpy().copy()
+                    assert pool.last_loads(layer) == ref[layer].step(counts)
+                    assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
+                M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE, stream=stream)
+                if step in (4, 7, 11, 13):
+                    stream.synchronize()
+                    r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                    assert rel_l2(out.cpu().numpy(), r) <= DECODE_REL_L2
+        stream.synchronize()
+    bpl = eb if parts == "whole" else None
+    for layer in range(L):
+        c, e = pool.counters(layer), ref[layer].counters()
+        assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+        if bpl is not None:
+            assert c["h2d_bytes"] == e["misses"] * bpl
+    assert pool.counters()["evictions"] > 0
+    pool.close()
+
+
+def test_device_planned_capacity_and_negative_counts():
+    """An event routing more experts than slots, or with a negative count,
+    changes nothing on the device (no copies, the slot map stays) and is
+    reported when the state is detached."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[0]
+    pool, host, dev = make_pool(M, wl, slots=2, preload=False)
+    E = wl.experts
+    state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device="cuda")
+    slot_of = torch.full((E,), -7, dtype=torch.int32, device="cuda")
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    pool.device_attach(state)
+    counts[1] = 2
+    pool.stage_device(0, counts, slot_of)
+    torch.cuda.synchronize()
+    assert slot_of.cpu().tolist() == [-1, 0] + [-1] * (E - 2)
+    counts[2] = 1
+    counts[5] = 3
+    pool.stage_device(0, counts, slot_of)  # three routed, two slots
+    torch.cuda.synchronize()
+    assert slot_of.cpu().tolist() == [-1, 0] + [-1] * (E - 2)
+    assert pool.device_detach() == M.MOE_ERR_CAPACITY
+    assert pool.slot_map(0).tolist() == [-1, 0] + [-1] * (E - 2)
+    c = pool.counters(0)
+    assert (c["misses"], c["events"]) == (1, 1)
+    pool.device_attach(state)
+    counts.zero_()
+    counts[3] = -1
+    pool.stage_device(0, counts, slot_of)
+    assert pool.device_detach() == M.MOE_ERR_INVALID
+    assert pool.counters(0)["events"] == 1
+    pool.close()
