@@ -611,22 +611,35 @@ def offload_obj(args, wl, host):
         wall_ms = (time.perf_counter() - t0) / args.steps * 1e3
         clocks = clk.stop()
     c1 = pool.counters()
+    pool.close()
+    dv = _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L)
     rates.update(pinned_1gib_after=_pinned_link_peak(dev), store_after=_store_link_rate(host, eb, dev))
     link_peak = max(rates["pinned_1gib_before"], rates["pinned_1gib_after"])
     store_rate = min(rates["store_before"], rates["store_after"])
-    ms = a.elapsed_time(b) / args.steps
+    ms_host = a.elapsed_time(b) / args.steps
+    h2d_host = c1["h2d_bytes"] - c0["h2d_bytes"]
+    host_planned = {"value": 1e3 / ms_host, "unit": "tokens/s", "ms_per_step": ms_host, "host_ms_per_step": wall_ms,
+                    "link_gbs": h2d_host / (ms_host * args.steps / 1e3) / 1e9,
+                    "misses": c1["misses"] - c0["misses"], "hits": c1["hits"] - c0["hits"],
+                    "how": "per layer: routing, counts to pinned host memory, host waits for them, plans "
+                           "(moe_pool_stage), one cudaMemcpyAsync per staged part of each miss on a copy stream, "
+                           "the FFN after an event on it; eager calls"}
+    ms, c0, c1, clocks = dv["ms"], dv["c0"], dv["c1"], dv["clocks"]
     h2d = c1["h2d_bytes"] - c0["h2d_bytes"]
     link = h2d / (ms * args.steps / 1e3) / 1e9
     misses = c1["misses"] - c0["misses"]
     obj = {"workload": wl.name, "value": 1e3 / ms, "unit": "tokens/s", "ms_per_step": ms,
-           "host_ms_per_step": wall_ms,
+           "host_planned": host_planned, "same_events_as_host_planned": (misses, c1["hits"] - c0["hits"]) == (
+               host_planned["misses"], host_planned["hits"]),
            "config": {"layers": L, "hidden": H, "inter": I, "experts": E, "top_k": k, "slots_per_layer": Sl,
                       "routing_bias": wl.bias_c, "policy": args.policy, "stage_parts": args.stage_parts,
                       "prefetch": args.prefetch, "tokens_per_step": 1,
                       "timing": "end to end through the C ABI: each step's logits and activations from pinned "
-                                "host memory, misses copied from the pinned expert store, outputs back to pinned "
-                                "host memory, CUDA events on the compute stream"},
-           "roofline": {"kernel": "miss staging: cudaMemcpyAsync of packed experts from pinned host memory",
+                                "host memory, per layer routing, staging planned on the GPU from the device counts "
+                                "(moe_pool_stage_device), misses copied by the SMs from the mapped pinned expert "
+                                "store, the decode FFN, outputs back to pinned host memory; one CUDA graph per step "
+                                "(24 x (routing, plan, copy, FFN) plus the input and output copies), CUDA events"},
+           "roofline": {"kernel": "miss staging: SM copy of packed experts out of mapped pinned host memory",
                         "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
                         "frac": link / link_peak, "peak_kind": "pinned H2D copy of a fresh 1 GiB buffer, best of "
                                                                "the measurements just before and after",
@@ -641,12 +654,76 @@ def offload_obj(args, wl, host):
            "e2e": {"value": 1e3 / ms, "unit": "tokens/s",
                    "h2d_bytes_per_step": (lg_pin[0].numel() * 4 + x_pin[0].numel() * 2) + h2d / args.steps,
                    "d2h_bytes_per_step": out_pin[0].numel() * 4},
-           "gpu_launches": args.steps * L * 2,
+           "gpu_launches": args.steps * L * dv["launches_per_layer"],
            "clocks": clocks}
-    pool.close()
     del slots
     torch.cuda.empty_cache()
     return obj
+
+
+def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L):
+    """The offload decode with device-planned staging: the pool's state in
+    device memory, per layer routing -> plan -> SM copy of the misses -> FFN
+    on one stream, each step (with its input and output copies) one CUDA
+    graph.  Same events as the host-planned run (same routing stream, same
+    policy, a fresh pool)."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    E, k, H, I, Sl = wl.experts, wl.top_k, wl.hidden, wl.inter, wl.slots
+    G = args.warmup + args.steps
+    pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy,
+                  stage_parts=args.stage_parts)
+    stream = torch.cuda.Stream(device=dev)
+    state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device=dev)
+    lg_d = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
+    x_d = torch.empty((L, 1, H), dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty((L, 1, H), dtype=torch.float32, device=dev)
+    out_pin = torch.empty((G, L, 1, H), dtype=torch.float32).pin_memory()
+    plan = M.RoutePlan.allocate(1, E, k, device=dev)
+    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
+    ws = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
+    pool.device_attach(state, stream=stream)
+
+    def body(g):
+        lg_d.copy_(lg_pin[g], non_blocking=True)
+        x_d.copy_(x_pin[g], non_blocking=True)
+        for l in range(L):
+            M.moe_route_plan(lg_d[l], k, plan, stream=stream, with_counts_host=False)
+            pool.stage_device(l, plan.counts, slot_of, stream=stream)
+            M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE, stream=stream)
+        out_pin[g].copy_(out_d, non_blocking=True)
+
+    graphs = []
+    for g in range(G):
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            body(g)
+        graphs.append(cg)
+    with torch.cuda.stream(stream):
+        for g in range(args.warmup):
+            graphs[g].replay()
+    stream.synchronize()
+    assert pool.device_detach(stream=stream) == M.MOE_OK
+    c0 = pool.counters()
+    pool.device_attach(state, stream=stream)
+    clk = Clocks(torch.cuda.current_device())
+    clk.start()
+    a, b = _events()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for g in range(args.warmup, G):
+            graphs[g].replay()
+        b.record(stream)
+    stream.synchronize()
+    clocks = clk.stop()
+    assert pool.device_detach(stream=stream) == M.MOE_OK
+    c1 = pool.counters()
+    pool.close()
+    del graphs
+    return {"ms": a.elapsed_time(b) / args.steps, "c0": c0, "c1": c1, "clocks": clocks,
+            "launches_per_layer": 4}
 
 
 def _prefill_setup(M, wl, dev):
@@ -1139,7 +1216,8 @@ def _standalone_line(obj, args):
             "warmup": args.warmup, "ms_per_step": obj["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": obj.get("dtype", "f32"), "data": "synthetic",
             "config": dict(workload=obj["workload"], **obj["config"])}
-    for key in ("roofline", "kernels_us", "ffn_times", "staging", "e2e", "gpu_launches", "clocks", "cpu_baseline"):
+    for key in ("roofline", "kernels_us", "ffn_times", "staging", "host_planned", "same_events_as_host_planned", "e2e",
+                "gpu_launches", "clocks", "cpu_baseline"):
         if key in obj:
             line[key] = obj[key]
     return line
