@@ -637,8 +637,10 @@ def offload_obj(args, wl, host):
                       "timing": "end to end through the C ABI: each step's logits and activations from pinned "
                                 "host memory, per layer routing, staging planned on the GPU from the device counts "
                                 "(moe_pool_stage_device), misses copied by the SMs from the mapped pinned expert "
-                                "store, the decode FFN, outputs back to pinned host memory; one CUDA graph per step "
-                                "(24 x (routing, plan, copy, FFN) plus the input and output copies), CUDA events"},
+                                "store on a second stream while the FFN of the event's hits runs, then the FFN of "
+                                "the loaded experts added in, outputs back to pinned host memory; one CUDA graph "
+                                "per step (24 x (routing, plan, copy | hits' FFN, loads' FFN) plus the input and "
+                                "output copies), CUDA events"},
            "roofline": {"kernel": "miss staging: SM copy of packed experts out of mapped pinned host memory",
                         "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
                         "frac": link / link_peak, "peak_kind": "pinned H2D copy of a fresh 1 GiB buffer, best of "
@@ -661,12 +663,13 @@ def offload_obj(args, wl, host):
     return obj
 
 
-def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L):
+def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L, split=True):
     """The offload decode with device-planned staging: the pool's state in
-    device memory, per layer routing -> plan -> SM copy of the misses -> FFN
-    on one stream, each step (with its input and output copies) one CUDA
-    graph.  Same events as the host-planned run (same routing stream, same
-    policy, a fresh pool)."""
+    device memory; per layer routing -> plan, then the SM copy of the misses
+    on a second stream while the FFN of the event's hits runs, then (joined)
+    the FFN of the loaded experts added in; each step (with its input and
+    output copies) one CUDA graph.  Same events as the host-planned run
+    (same routing stream, same policy, a fresh pool)."""
     import torch
 
     import routed_expert_ffn_histogram_gb300 as M
@@ -676,6 +679,8 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L):
     pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy,
                   stage_parts=args.stage_parts)
     stream = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev)
+    maps = torch.empty((2, E), dtype=torch.int32, device=dev)
     state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device=dev)
     lg_d = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
     x_d = torch.empty((L, 1, H), dtype=torch.bfloat16, device=dev)
@@ -691,8 +696,17 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L):
         x_d.copy_(x_pin[g], non_blocking=True)
         for l in range(L):
             M.moe_route_plan(lg_d[l], k, plan, stream=stream, with_counts_host=False)
-            pool.stage_device(l, plan.counts, slot_of, stream=stream)
-            M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE, stream=stream)
+            if split:
+                pool.stage_device(l, plan.counts, slot_of, split_dev=maps, stream=stream, copy=copy)
+                M.moe_expert_ffn(pool, l, x_d[l], plan, maps[0], out_d[l], ws, path=M.MOE_PATH_DECODE,
+                                 stream=stream, skip_absent=True)
+                pool.device_join(l, stream=stream)
+                M.moe_expert_ffn(pool, l, x_d[l], plan, maps[1], out_d[l], ws, path=M.MOE_PATH_DECODE,
+                                 stream=stream, skip_absent=True, accumulate=True)
+            else:
+                pool.stage_device(l, plan.counts, slot_of, stream=stream)
+                M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE,
+                                 stream=stream)
         out_pin[g].copy_(out_d, non_blocking=True)
 
     graphs = []
@@ -723,7 +737,7 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L):
     pool.close()
     del graphs
     return {"ms": a.elapsed_time(b) / args.steps, "c0": c0, "c1": c1, "clocks": clocks,
-            "launches_per_layer": 4}
+            "launches_per_layer": 5 if split else 4}
 
 
 def _prefill_setup(M, wl, dev):

@@ -82,6 +82,13 @@ extern "C" {
 /* OR-ed into moe_expert_ffn's path: out is added to (out += the layer's
  * output, as a residual stream takes it) instead of overwritten. */
 #define MOE_FFN_ACCUMULATE 0x100
+/* OR-ed into moe_expert_ffn's path (decode only): assignments whose
+ * expert's slot_of entry is -1 (any negative value) are not served -- they
+ * add nothing and get no work -- instead of yielding NaN.  With two calls
+ * over complementary slot maps (the second with MOE_FFN_ACCUMULATE) a layer
+ * is computed in two parts, e.g. resident experts while missed ones are
+ * still being copied (moe_pool_stage_device). */
+#define MOE_FFN_SKIP_ABSENT 0x200
 
 typedef void* moe_stream_t;
 
@@ -369,16 +376,33 @@ MOE_API int moe_pool_prefetch(moe_pool_t* pool, int layer, int max_loads, moe_st
  *   enqueued on other streams that reads the slots must be ordered before
  *   `stream` by the caller.  Dry-run pools and attached pools: MOE_ERR_STATE.
  *
- * moe_pool_stage_device: enqueues on `stream` one event of `layer`:
+ * moe_pool_stage_device: enqueues one event of `layer`: the planner on
+ *   `compute`, then the copy of the misses' bytes (the whole packed expert,
+ *   or the decode parts with MOE_STAGE_DECODE) host -> slot by a kernel on
+ *   `copy` after the planner (on `compute` itself when copy is NULL or the
+ *   same stream).
  *   counts_dev  device int32 [E] (moe_route_plan's counts), read on the GPU
  *   slot_of_dev device int32 [E], written: the layer's slot map after the
- *               event (-1 = absent), for moe_expert_ffn on the same stream
- *   Then the misses' bytes (the whole packed expert, or the decode parts
- *   with MOE_STAGE_DECODE) are copied host -> slot by a kernel on `stream`.
+ *               event (-1 = absent)
+ *   split_dev   device int32 [2][E] or NULL, written: row 0 the slots of the
+ *               event's hits, row 1 the slots of its loads, -1 elsewhere --
+ *               the maps of two moe_expert_ffn calls with
+ *               MOE_FFN_SKIP_ABSENT: the hits' part on `compute` while the
+ *               copies run, then moe_pool_device_join, then the loads' part
+ *               with MOE_FFN_ACCUMULATE (tinyserve README, "How it works"
+ *               item 4: H2D overlapped with compute).
  *   An event with a negative count or more than S routed experts changes
- *   nothing (no copies; slot_of_dev gets the current map) and is reported
- *   by moe_pool_device_detach.  Nothing waits on the host; the call may be
- *   captured in a CUDA graph.  Copy-failure injection does not apply.
+ *   nothing (no copies; slot_of_dev gets the current map, row 0 of
+ *   split_dev slot S -- out of range, so NaN -- for routed experts without
+ *   a slot) and is reported by moe_pool_device_detach.  Nothing waits on
+ *   the host; the call may be captured in a CUDA graph (with `copy` forked
+ *   from and joined back to `compute` inside the capture).  Copy-failure
+ *   injection does not apply.
+ *
+ * moe_pool_device_join: makes `compute` wait for the copies of `layer`'s
+ *   last event enqueued on a separate copy stream (no-op otherwise).  The
+ *   layer's next moe_pool_stage_device and moe_pool_device_detach join by
+ *   themselves.
  *
  * moe_pool_device_detach: downloads the state into the pool on `stream`
  *   (polling, at most timeout_ms) after the work enqueued so far; the
@@ -397,7 +421,9 @@ MOE_API int moe_pool_device_state_bytes(const moe_pool_t* pool, size_t* out_byte
 MOE_API int moe_pool_device_attach(moe_pool_t* pool, void* dev_state, size_t bytes, moe_stream_t stream,
                                    int timeout_ms);
 MOE_API int moe_pool_stage_device(moe_pool_t* pool, int layer, const int32_t* counts_dev,
-                                  int32_t* slot_of_dev, moe_stream_t stream);
+                                  int32_t* slot_of_dev, int32_t* split_dev, moe_stream_t compute,
+                                  moe_stream_t copy);
+MOE_API int moe_pool_device_join(moe_pool_t* pool, int layer, moe_stream_t compute);
 MOE_API int moe_pool_device_detach(moe_pool_t* pool, moe_stream_t stream, int timeout_ms);
 
 /* Counters of one layer, or summed over all layers with layer = -1. */
@@ -446,7 +472,9 @@ MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int pat
  *   offsets, perm, inv  device, from moe_route_plan (prefill path only;
  *             may be NULL for the decode path)
  *   slot_of   device int32 [E]: slot of each expert in this layer; every
- *             routed expert must be resident (moe_pool_stage ensures it)
+ *             routed expert must be resident (moe_pool_stage ensures it),
+ *             except with MOE_FFN_SKIP_ABSENT: entries < 0 then mark the
+ *             assignments this call leaves out
  *   path      MOE_PATH_DECODE: bf16 activations times fp32-dequantised
  *             MXFP4 on CUDA cores, fp32 accumulation, SwiGLU output rounded
  *             to bf16.  MOE_PATH_PREFILL: activations and the SwiGLU output
@@ -456,7 +484,11 @@ MOE_API int moe_ffn_workspace_bytes(int T, int k, int hidden, int inter, int pat
  *             MOE_PATH_AUTO: decode when T*k <= MOE_DECODE_MAX_ASSIGN.
  *             With MOE_FFN_ACCUMULATE or-ed in, out += the result; the
  *             decode path then needs no completion pass and prefill no
- *             zeroing of out.
+ *             zeroing of out.  With MOE_FFN_SKIP_ABSENT or-ed in (decode
+ *             path with the one-launch kernel only, else
+ *             MOE_ERR_UNSUPPORTED) the result sums only the assignments
+ *             whose expert has slot_of >= 0, their work spread over all
+ *             CTAs (a token none of whose assignments is served gets 0).
  *   workspace device, >= moe_ffn_workspace_bytes(), 256-byte aligned.
  *             On the decode path it holds a completion counter and an fp32
  *             [T][H] accumulator that must be zero when the workspace is

@@ -19,7 +19,7 @@ import ctypes as C
 from dataclasses import dataclass
 
 from . import _lib
-from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_FFN_ACCUMULATE, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_INVALID, MOE_ERR_STATE,
+from ._lib import (MOE_DECODE_MAX_ASSIGN, MOE_FFN_ACCUMULATE, MOE_FFN_SKIP_ABSENT, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_INVALID, MOE_ERR_STATE,
                    MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_OK,
                    MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_POLICY_FIFO, MOE_POLICY_LFRU,
                    MOE_POLICY_LFU, MOE_POLICY_LRU, MOE_POLICY_SLRU, MOE_STAGE_DECODE,
@@ -34,7 +34,7 @@ __all__ = [
     "moe_expert_ffn", "moe_decode_layer", "moe_ffn_status", "moe_debug_stall_next_decode", "moe_combine",
     "moe_quant_mxfp8", "moe_quant_mxfp4", "moe_probe_mxf8f6f4", "moe_gguf_expert_bytes", "pack_gguf_expert",
     "moe_expert_ffn_gguf", "moe_decode_layer_gguf", "alloc_gguf_workspace", "gguf_workspace_h", "GGUF_FORMATS", "Pool", "RoutePlan", "MoeCounters", "MoeError", "lib", "status_str",
-    "POLICIES", "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL", "MOE_FFN_ACCUMULATE",
+    "POLICIES", "MOE_PATH_AUTO", "MOE_PATH_DECODE", "MOE_PATH_PREFILL", "MOE_FFN_ACCUMULATE", "MOE_FFN_SKIP_ABSENT",
 ]
 
 
@@ -128,13 +128,17 @@ def alloc_ffn_workspace(T: int, k: int, hidden: int, inter: int, path: int = MOE
 
 
 def moe_expert_ffn(pool: "Pool", layer: int, x_bf16, plan: RoutePlan, slot_of, out, workspace,
-                   path: int = MOE_PATH_AUTO, stream=None, accumulate: bool = False) -> None:
+                   path: int = MOE_PATH_AUTO, stream=None, accumulate: bool = False,
+                   skip_absent: bool = False) -> None:
     """Routed experts of one layer with the weighted combine (moe_expert_ffn);
     ``accumulate`` adds into ``out`` (a residual stream) instead of
-    overwriting it."""
+    overwriting it; ``skip_absent`` serves only the assignments whose
+    expert's ``slot_of`` entry is >= 0 (decode path)."""
     T = x_bf16.shape[0]
     if accumulate:
         path |= MOE_FFN_ACCUMULATE
+    if skip_absent:
+        path |= MOE_FFN_SKIP_ABSENT
     check("moe_expert_ffn", lib().moe_expert_ffn(
         pool.handle, layer, ptr(x_bf16), T, plan.k, ptr(plan.ids), ptr(plan.w), ptr(plan.offsets),
         ptr(plan.perm), ptr(plan.inv), ptr(slot_of), path, ptr(workspace),
@@ -335,12 +339,19 @@ class Pool:
         check("moe_pool_device_attach", lib().moe_pool_device_attach(
             self.handle, ptr(dev_state), nbytes, stream_handle(stream), timeout_ms))
 
-    def stage_device(self, layer, counts_dev, slot_of_dev, stream=None) -> None:
+    def stage_device(self, layer, counts_dev, slot_of_dev, split_dev=None, stream=None, copy=None) -> None:
         """Enqueue one staging event planned on the GPU from the device
-        counts: slot map into ``slot_of_dev``, misses copied by the SMs from
-        the mapped host store (moe_pool_stage_device)."""
+        counts: slot map into ``slot_of_dev`` (and, with ``split_dev``, the
+        hits' and the loads' maps), misses copied by the SMs from the mapped
+        host store on ``copy`` (or ``stream``) (moe_pool_stage_device)."""
         check("moe_pool_stage_device", lib().moe_pool_stage_device(
-            self.handle, layer, ptr(counts_dev), ptr(slot_of_dev), stream_handle(stream)))
+            self.handle, layer, ptr(counts_dev), ptr(slot_of_dev), ptr(split_dev), stream_handle(stream),
+            stream_handle(copy) if copy is not None else None))
+
+    def device_join(self, layer, stream=None) -> None:
+        """``stream`` waits for the layer's copies on the copy stream
+        (moe_pool_device_join)."""
+        check("moe_pool_device_join", lib().moe_pool_device_join(self.handle, layer, stream_handle(stream)))
 
     def device_detach(self, stream=None, timeout_ms=10000) -> int:
         """Bring the state back from the device; returns the status

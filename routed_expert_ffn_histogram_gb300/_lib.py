@@ -28,6 +28,7 @@ MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
 MOE_DECODE_MAX_ASSIGN = 64
 MOE_FFN_ACCUMULATE = 0x100
+MOE_FFN_SKIP_ABSENT = 0x200
 MOE_POLICY_LRU, MOE_POLICY_FIFO, MOE_POLICY_LFU, MOE_POLICY_LFRU, MOE_POLICY_SLRU = 0, 1, 2, 3, 4
 POLICIES = {"lru": 0, "fifo": 1, "lfu": 2, "lfru": 3, "slru": 4}
 MOE_STAGE_WHOLE, MOE_STAGE_DECODE = 0, 1
@@ -78,7 +79,8 @@ SIGNATURES = {
     "moe_pool_inject_copy_failures": (_i32, [_vp, _i32]),
     "moe_pool_device_state_bytes": (_i32, [_vp, _szp]),
     "moe_pool_device_attach": (_i32, [_vp, _vp, _sz, _vp, _i32]),
-    "moe_pool_stage_device": (_i32, [_vp, _i32, _vp, _vp, _vp]),
+    "moe_pool_stage_device": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_pool_device_join": (_i32, [_vp, _i32, _vp]),
     "moe_pool_device_detach": (_i32, [_vp, _vp, _i32]),
     "moe_pool_destroy": (None, [_vp]),
     "moe_ffn_workspace_bytes": (_i32, [_i32, _i32, _i32, _i32, _i32, _szp]),

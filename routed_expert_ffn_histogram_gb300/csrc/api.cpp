@@ -156,8 +156,8 @@ extern "C" int moe_route_plan_noalloc(const float* logits, int T, int E, int k, 
 }
 
 static int resolve_path(int path, int T, int k) {
-    if (path & ~(MOE_FFN_ACCUMULATE | 3)) return -1;
-    path &= ~MOE_FFN_ACCUMULATE;
+    if (path & ~(MOE_FFN_ACCUMULATE | MOE_FFN_SKIP_ABSENT | 3)) return -1;
+    path &= 3;
     if (path == MOE_PATH_AUTO) return size_t(T) * k <= MOE_DECODE_MAX_ASSIGN ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
     return path;
 }
@@ -183,8 +183,10 @@ extern "C" int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_b
     if (layer < 0 || layer >= d.layers || T < 0 || k < 1 || k > d.experts || k > MOE_MAX_TOPK)
         return MOE_ERR_INVALID;
     const bool accumulate = (path & MOE_FFN_ACCUMULATE) != 0;
+    const bool skip_absent = (path & MOE_FFN_SKIP_ABSENT) != 0;
     path = resolve_path(path, T, k);
     if (path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL) return MOE_ERR_INVALID;
+    if (skip_absent && path != MOE_PATH_DECODE) return MOE_ERR_UNSUPPORTED;
     size_t need = 0;
     moe_ffn_workspace_bytes(T, k, d.hidden, d.inter, path, &need);
     if (T > 0) {
@@ -210,6 +212,7 @@ extern "C" int moe_expert_ffn(const moe_pool_t* pool, int layer, const void* x_b
     a.slot_of = slot_of;
     a.out = out;
     a.accumulate = accumulate;
+    a.skip_absent = skip_absent;
     a.decode_parts_only = d.stage_parts == MOE_STAGE_DECODE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (path == MOE_PATH_DECODE) return moe::launch_decode_ffn(a, workspace, ws_bytes, s);

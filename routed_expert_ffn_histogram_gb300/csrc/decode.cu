@@ -340,7 +340,7 @@ int launch_decode_ffn(const FfnArgs& a, void* ws, size_t ws_bytes, cudaStream_t 
         const int rc = launch_decode_fused(a, ws, s);
         if (rc != MOE_ERR_UNSUPPORTED) return rc;
     }
-    if (a.decode_parts_only) return MOE_ERR_UNSUPPORTED;
+    if (a.decode_parts_only || a.skip_absent) return MOE_ERR_UNSUPPORTED;
     DecodeParams p;
     p.slots = a.slots;
     p.expert_bytes = a.expert_bytes;

@@ -136,6 +136,17 @@ __device__ __forceinline__ void block_dot2_f16(const uint4 cg, const uint4 cu, c
     du = u0 + u1;
 }
 
+// Served assignments as a bit mask: the n-th set bit (n counted from 0),
+// and the next set bit after a (64 when there is none).
+__device__ __forceinline__ int nth_active(uint64_t m, int n) {
+    for (int i = 0; i < n && m; ++i) m &= m - 1;
+    return m ? __ffsll((long long)m) - 1 : 64;
+}
+__device__ __forceinline__ int next_active(uint64_t m, int a) {
+    const uint64_t rest = (a >= 63) ? 0ull : (m >> (a + 1));
+    return rest ? a + __ffsll((long long)rest) : 64;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -197,6 +208,7 @@ struct FusedParams {
     float* out;        // fp32 [T][H]
     unsigned* ctl;     // [0] CTAs finished (zero between calls), [2] error bits
     int accumulate;    // out += result: partial sums go to out, no completion pass
+    int skip_absent;   // serve only the assignments whose expert's slot is >= 0
     // fused routing (logits != nullptr): the kernel selects the experts itself
     // and CTA 0 writes the routing outputs below
     const float* logits;
@@ -294,9 +306,26 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // This CTA's items: a contiguous range of the A * I / 16 items in
-    // (assignment, column block) order.
-    const int items = A * p.I / kGroup;
+    // The assignments this launch serves: all of them, or with skip_absent
+    // those whose expert has a slot (>= 0; a slot >= S still counts and
+    // yields NaN).  Every warp forms the same mask.
+    uint64_t act = (A >= 64) ? ~0ull : ((1ull << A) - 1ull);
+    if (p.skip_absent) {
+        uint64_t m = 0;
+        for (int base = 0; base < A; base += 32) {
+            const int a = base + lane;
+            bool on = false;
+            if (a < A) {
+                const int e = __ldg(p.ids + a);
+                on = e >= 0 && e < p.E && __ldg(p.slot_of + e) >= 0;
+            }
+            m |= uint64_t(__ballot_sync(0xffffffffu, on)) << base;
+        }
+        act = m;
+    }
+    // This CTA's items: a contiguous range of the n_act * I / 16 items in
+    // (served assignment, column block) order.
+    const int items = __popcll(act) * p.I / kGroup;
     const int per = (items + G - 1) / G;
     const int g0 = min(items, (int)blockIdx.x * per), g1 = min(items, g0 + per);
     const int cnt = g1 - g0;
@@ -406,8 +435,9 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
         if (lane == 0) {
         // per ring: next slot, its phase, and the next item's (assignment, row)
         const int it0 = g0 * kGroup;
-        const int a0 = it0 / p.I;
-        int gu_slot = 0, gu_a = a0, gu_r = it0 - a0 * p.I;
+        const int ai0 = it0 / p.I;
+        const int a0 = nth_active(act, ai0);
+        int gu_slot = 0, gu_a = a0, gu_r = it0 - ai0 * p.I;
         uint32_t gu_ph = 0;
         int d_slot = 0, d_a = a0, d_r = gu_r;
         uint32_t d_ph = 0;
@@ -416,7 +446,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             const uint32_t ph = gu_ph;
             const int a = gu_a, r = gu_r;
             if (++gu_slot == n_gu) { gu_slot = 0; gu_ph ^= 1u; }
-            if ((gu_r += kGroup) == p.I) { gu_r = 0; ++gu_a; }
+            if ((gu_r += kGroup) == p.I) { gu_r = 0; gu_a = next_active(act, gu_a); }
             if (!tc::mbar_wait_suspend(&rb.empty_gu[slot], ph ^ 1u, err, 4u)) return false;
             if (n == 0 && p.stall) return true;   // test hook: the first item never lands
             if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
@@ -441,7 +471,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             const uint32_t ph = d_ph;
             const int a = d_a, r = d_r;
             if (++d_slot == n_d) { d_slot = 0; d_ph ^= 1u; }
-            if ((d_r += kGroup) == p.I) { d_r = 0; ++d_a; }
+            if ((d_r += kGroup) == p.I) { d_r = 0; d_a = next_active(act, d_a); }
             if (!tc::mbar_wait_suspend(&rb.empty_d[slot], ph ^ 1u, err, 4u)) return false;
             if (n == 0 && p.stall) return true;
             if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
@@ -506,7 +536,8 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
         // item state carried from item to item: assignment and row, ring
         // slots and phases, the token's staged x, the h-exponent word
         const int it0 = g0 * kGroup;
-        int a = it0 / p.I, r = it0 - a * p.I;
+        const int ai0 = it0 / p.I;
+        int a = nth_active(act, ai0), r = it0 - ai0 * p.I;
         int sg = 0, sd = 0, hm = 0;
         uint32_t ph_gu = 0, ph_d = 0;
         const uint4* xt = xs;
@@ -624,7 +655,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             }
             __syncwarp();
             if (lane == 0 && gotd) tc::mbar_arrive(&rb.empty_d[sd]);
-            if ((r += kGroup) == p.I) { r = 0; ++a; }
+            if ((r += kGroup) == p.I) { r = 0; a = next_active(act, a); }
             if (++sg == n_gu) { sg = 0; ph_gu ^= 1u; }
             if (++sd == n_d) { sd = 0; ph_d ^= 1u; }
             hm = (hm == 2) ? 0 : hm + 1;
@@ -735,6 +766,7 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     p.acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_acc_offset(a.T, a.k, L.I));
     p.out = a.out;
     p.accumulate = a.accumulate ? 1 : 0;
+    p.skip_absent = a.skip_absent ? 1 : 0;
     p.logits = ro ? ro->logits : nullptr;
     p.r_ids = ro ? ro->ids : nullptr;
     p.r_w = ro ? ro->w : nullptr;

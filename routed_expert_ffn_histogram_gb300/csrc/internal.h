@@ -106,6 +106,7 @@ struct FfnArgs {
     const int32_t* slot_of;
     float* out;
     bool accumulate = false;   // out += result instead of out = result
+    bool skip_absent = false;  // decode: serve only assignments whose expert's slot is >= 0
 };
 
 struct RouteOut {
@@ -149,7 +150,7 @@ int launch_gguf_fused(int fmt, const uint8_t* slots, int S, int E, int H, int I,
 // Device-planned pool staging (pool_dev.cu): `rec` is the layer's record in
 // the device state (pool_plan.h, dev_record).
 int launch_pool_plan(uint8_t* rec, int S, int E, int policy, const int32_t* counts, int32_t* slot_of,
-                     uint64_t bytes_per_load, cudaStream_t s);
+                     int32_t* split, uint64_t bytes_per_load, cudaStream_t s);
 int launch_pool_gather(const uint8_t* rec, int S, int E, const uint8_t* host_layer, uint8_t* slots_layer,
                        size_t eb, size_t len0, size_t off1, size_t len1, cudaStream_t s);
 

@@ -72,6 +72,9 @@ struct moe_pool {
     int inject_fail = 0;
     uint8_t* dev_state = nullptr;       // device-planned staging: the state lives here while attached
     const uint8_t* host_dev = nullptr;  // device address of host_experts (mapped pinned memory)
+    cudaEvent_t ev_plan = nullptr;      // device planner done (the copy stream's copies follow it)
+    std::vector<cudaEvent_t> ev_gather; // [L] the layer's last copies on the copy stream done
+    std::vector<uint8_t> gather_pending;  // [L] copies on the copy stream not yet joined
 };
 
 namespace {
@@ -737,6 +740,12 @@ extern "C" int moe_pool_device_attach(moe_pool_t* p, void* dev_state, size_t byt
             MOE_CUDA_TRY(cudaStreamWaitEvent(s, p->ev_pf[l], 0));
             p->pending[l] = 0;
         }
+    if (!p->ev_plan) {
+        MOE_CUDA_TRY(cudaEventCreateWithFlags(&p->ev_plan, cudaEventDisableTiming));
+        p->ev_gather.assign(size_t(p->d.layers), nullptr);
+        for (auto& ev : p->ev_gather) MOE_CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+        p->gather_pending.assign(size_t(p->d.layers), 0);
+    }
     std::vector<uint8_t> img(device_state_bytes(p));
     pack_device_state(p, img.data());
     MOE_CUDA_TRY(cudaMemcpyAsync(dev_state, img.data(), img.size(), cudaMemcpyHostToDevice, s));
@@ -747,15 +756,33 @@ extern "C" int moe_pool_device_attach(moe_pool_t* p, void* dev_state, size_t byt
     return MOE_OK;
 }
 
+// The copy stream's copies of `layer` come before whatever is enqueued next
+// on `s`.
+static int join_gather(moe_pool_t* p, int layer, cudaStream_t s) {
+    if (!p->gather_pending.empty() && p->gather_pending[layer]) {
+        MOE_CUDA_TRY(cudaStreamWaitEvent(s, p->ev_gather[layer], 0));
+        p->gather_pending[layer] = 0;
+    }
+    return MOE_OK;
+}
+
 extern "C" int moe_pool_stage_device(moe_pool_t* p, int layer, const int32_t* counts_dev, int32_t* slot_of_dev,
-                                     moe_stream_t stream) {
+                                     int32_t* split_dev, moe_stream_t compute, moe_stream_t copy) {
     if (!p || !counts_dev || !slot_of_dev || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
     if (!p->dev_state) return MOE_ERR_STATE;
     const int S = p->d.slots_per_layer, E = p->d.experts;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint8_t* rec = p->dev_state + size_t(layer) * moe::dev_record(S, E).bytes;
-    int rc = moe::launch_pool_plan(rec, S, E, p->d.policy, counts_dev, slot_of_dev, p->bytes_per_load, s);
+    cudaStream_t s = static_cast<cudaStream_t>(compute), cp = static_cast<cudaStream_t>(copy);
+    // the planner rewrites the record the layer's previous copies read
+    int rc = join_gather(p, layer, s);
     if (rc != MOE_OK) return rc;
+    uint8_t* rec = p->dev_state + size_t(layer) * moe::dev_record(S, E).bytes;
+    rc = moe::launch_pool_plan(rec, S, E, p->d.policy, counts_dev, slot_of_dev, split_dev, p->bytes_per_load, s);
+    if (rc != MOE_OK) return rc;
+    const bool fork = copy != nullptr && cp != s;
+    if (fork) {
+        MOE_CUDA_TRY(cudaEventRecord(p->ev_plan, s));
+        MOE_CUDA_TRY(cudaStreamWaitEvent(cp, p->ev_plan, 0));
+    }
     const size_t eb = p->eb;
     const bool decode = p->d.stage_parts == MOE_STAGE_DECODE;
     const size_t len0 = decode ? p->L.d_off : eb;
@@ -763,13 +790,27 @@ extern "C" int moe_pool_stage_device(moe_pool_t* p, int layer, const int32_t* co
     const size_t len1 = decode ? eb - p->L.dt_off : 0;
     const uint8_t* host_layer = p->host_dev + size_t(layer) * size_t(E) * eb;
     uint8_t* slots_layer = static_cast<uint8_t*>(p->d.dev_slots) + size_t(layer) * size_t(S) * eb;
-    return moe::launch_pool_gather(rec, S, E, host_layer, slots_layer, eb, len0, off1, len1, s);
+    rc = moe::launch_pool_gather(rec, S, E, host_layer, slots_layer, eb, len0, off1, len1, fork ? cp : s);
+    if (rc != MOE_OK || !fork) return rc;
+    MOE_CUDA_TRY(cudaEventRecord(p->ev_gather[layer], cp));
+    p->gather_pending[layer] = 1;
+    return MOE_OK;
+}
+
+extern "C" int moe_pool_device_join(moe_pool_t* p, int layer, moe_stream_t compute) {
+    if (!p || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    if (!p->dev_state) return MOE_ERR_STATE;
+    return join_gather(p, layer, static_cast<cudaStream_t>(compute));
 }
 
 extern "C" int moe_pool_device_detach(moe_pool_t* p, moe_stream_t stream, int timeout_ms) {
     if (!p) return MOE_ERR_INVALID;
     if (!p->dev_state) return MOE_ERR_STATE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int l = 0; l < p->d.layers; ++l) {
+        const int rj = join_gather(p, l, s);
+        if (rj != MOE_OK) return rj;
+    }
     std::vector<uint8_t> img(device_state_bytes(p));
     MOE_CUDA_TRY(cudaMemcpyAsync(img.data(), p->dev_state, img.size(), cudaMemcpyDeviceToHost, s));
     const int rc = wait_stream(p, s, timeout_ms);
@@ -797,6 +838,9 @@ extern "C" void moe_pool_destroy(moe_pool_t* p) {
     for (cudaEvent_t ev : p->ev_pf)
         if (ev) cudaEventDestroy(ev);
     if (p->map_pinned) cudaFreeHost(p->map_pinned);
+    if (p->ev_plan) cudaEventDestroy(p->ev_plan);
+    for (cudaEvent_t ev : p->ev_gather)
+        if (ev) cudaEventDestroy(ev);
     delete p;
 }
 

@@ -20,9 +20,15 @@
 //                       into shared memory by all threads, thread 0 plans
 //                       the event (pool_plan.h) and updates the counters,
 //                       all threads write the record back and the slot map.
-//   pool_gather_kernel  2 CTAs per SM: 64 KB chunks of the planned loads
-//                       (both staged parts of each expert), 16-byte loads
-//                       from host memory, four in flight per thread.
+//   pool_gather_kernel  one CTA of 64 threads per SM: 64 KB chunks of the
+//                       planned loads (both staged parts of each expert),
+//                       16-byte loads from host memory, eight in flight per
+//                       thread (≈ 1.2 MB in flight: the link, ≈ 0.2 TB/s,
+//                       stays the limit).  Small in registers so that an SM
+//                       holding two of them (the CTA scheduler does not
+//                       spread them one per SM) still takes a decode FFN
+//                       CTA: the FFN of a layer's hits runs beside the copy
+//                       (with 128-thread CTAs it waited for the copy to end).
 #include <cstdint>
 
 #include "internal.h"
@@ -33,12 +39,14 @@ namespace {
 
 constexpr int kPlanThreads = 256;
 static_assert(kPlanThreads >= MOE_MAX_EXPERTS, "one thread per expert in the planner");
-constexpr int kGatherThreads = 512;
+constexpr int kGatherThreads = 64;
+constexpr int kGatherUnroll = 8;
 constexpr unsigned long long kChunk = 64ull << 10;
 
 __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, DevRecord dr, int S, int E,
                                                                  int policy, const int32_t* __restrict__ counts,
                                                                  int32_t* __restrict__ slot_of,
+                                                                 int32_t* __restrict__ split,
                                                                  unsigned long long bytes_per_load) {
     __shared__ int32_t se[MOE_MAX_EXPERTS], es[MOE_MAX_EXPERTS], cnt[MOE_MAX_EXPERTS], hit_e[MOE_MAX_EXPERTS];
     __shared__ int64_t st[MOE_MAX_EXPERTS], uses[MOE_MAX_EXPERTS];
@@ -59,9 +67,10 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
         uses[t] = g_uses[t];
         seg[t] = g_seg[t];
     }
-    int c = 0;
+    int c = 0, es0 = -1;
     if (t < E) {
-        es[t] = g_es[t];
+        es0 = g_es[t];
+        es[t] = es0;
         c = counts[t];
         cnt[t] = c;
     }
@@ -125,7 +134,23 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
             g_freq[t] += cnt[t] > 0;
         }
     }
-    if (t < E) slot_of[t] = es[t];
+    if (t < E) {
+        slot_of[t] = es[t];
+        if (split) {
+            // [0, E): the routed experts that were resident (the event's
+            // hits), [E, 2E): the ones this event loads; -1 elsewhere.  After
+            // an event that changed nothing, routed experts without a slot get
+            // slot S in the first map (out of range: a computation over it
+            // yields NaN instead of leaving them out).
+            if (ok_s) {
+                split[t] = (c > 0 && es0 >= 0) ? es[t] : -1;
+                split[E + t] = (c > 0 && es0 < 0) ? es[t] : -1;
+            } else {
+                split[t] = c > 0 ? (es0 >= 0 ? es0 : S) : -1;
+                split[E + t] = -1;
+            }
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8_t* rec, DevRecord dr,
@@ -151,15 +176,15 @@ __global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8
         const uint4* src = reinterpret_cast<const uint4*>(host_layer + (unsigned long long)le[i] * eb + base);
         uint4* dst = reinterpret_cast<uint4*>(slots_layer + (unsigned long long)ls[i] * eb + base);
         const unsigned long long n16 = len / 16;
-        for (unsigned long long j = threadIdx.x; j < n16; j += 4ull * kGatherThreads) {
-            uint4 v[4];
+        for (unsigned long long j = threadIdx.x; j < n16; j += (unsigned long long)kGatherUnroll * kGatherThreads) {
+            uint4 v[kGatherUnroll];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kGatherUnroll; ++u) {
                 const unsigned long long jj = j + (unsigned long long)u * kGatherThreads;
                 if (jj < n16) v[u] = __ldg(src + jj);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kGatherUnroll; ++u) {
                 const unsigned long long jj = j + (unsigned long long)u * kGatherThreads;
                 if (jj < n16) dst[jj] = v[u];
             }
@@ -170,9 +195,9 @@ __global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8
 }  // namespace
 
 int launch_pool_plan(uint8_t* rec, int S, int E, int policy, const int32_t* counts, int32_t* slot_of,
-                     uint64_t bytes_per_load, cudaStream_t s) {
+                     int32_t* split, uint64_t bytes_per_load, cudaStream_t s) {
     if (E > MOE_MAX_EXPERTS || S > E) return MOE_ERR_INVALID;
-    pool_plan_kernel<<<1, kPlanThreads, 0, s>>>(rec, dev_record(S, E), S, E, policy, counts, slot_of,
+    pool_plan_kernel<<<1, kPlanThreads, 0, s>>>(rec, dev_record(S, E), S, E, policy, counts, slot_of, split,
                                                   (unsigned long long)bytes_per_load);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
@@ -186,7 +211,18 @@ int launch_pool_gather(const uint8_t* rec, int S, int E, const uint8_t* host_lay
     DeviceInfo di;
     int rc = current_device_info(&di);
     if (rc != MOE_OK) return rc;
-    pool_gather_kernel<<<2 * di.sms, kGatherThreads, 0, s>>>(rec, dev_record(S, E), host_layer, slots_layer, eb,
+    if (di.device < 0 || di.device >= 64) return MOE_ERR_UNSUPPORTED;
+    static DeviceOnce carveout_set;
+    if (!carveout_set.done(di.device)) {
+        // An SM configured with a small shared-memory carve-out (what a
+        // kernel without shared memory would get) cannot take a decode FFN
+        // CTA (about 210 KB) until it drains: ask for the largest carve-out
+        // so the FFN of a layer's hits runs beside the copy.
+        MOE_CUDA_TRY(cudaFuncSetAttribute(pool_gather_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                          int(cudaSharedmemCarveoutMaxShared)));
+        carveout_set.mark(di.device);
+    }
+    pool_gather_kernel<<<di.sms, kGatherThreads, 0, s>>>(rec, dev_record(S, E), host_layer, slots_layer, eb,
                                                              len0, off1, len1);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;

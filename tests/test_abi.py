@@ -100,7 +100,7 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.moe_quant_mxfp8(None, 33, None, 1, 1, None, None, 2, None) == M.MOE_ERR_INVALID
     assert L.moe_ffn_workspace_bytes(4, 2, 250, 512, 0, C.byref(sz)) == M.MOE_ERR_INVALID
     # the accumulate flag is the only bit allowed beside the path; it does not change the size
-    assert L.moe_ffn_workspace_bytes(4, 2, 256, 512, 0x200, C.byref(sz)) == M.MOE_ERR_INVALID
+    assert L.moe_ffn_workspace_bytes(4, 2, 256, 512, 0x400, C.byref(sz)) == M.MOE_ERR_INVALID
     assert L.moe_ffn_workspace_bytes(4, 2, 256, 512, M.MOE_PATH_DECODE, C.byref(sz)) == M.MOE_OK
     plain = sz.value
     assert L.moe_ffn_workspace_bytes(4, 2, 256, 512, M.MOE_PATH_DECODE | M.MOE_FFN_ACCUMULATE, C.byref(sz)) == M.MOE_OK

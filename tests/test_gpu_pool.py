@@ -186,16 +186,21 @@ def test_offload_decode_with_prefetch():
     pool.close()
 
 
-@pytest.mark.parametrize("policy,parts", [("lru", "decode"), ("fifo", "whole"), ("lfu", "decode"),
-                                          ("lfru", "decode"), ("slru", "decode")])
-def test_offload_device_planned_staging(policy, parts):
+@pytest.mark.parametrize("policy,parts,split", [("lru", "decode", False), ("fifo", "whole", False),
+                                                ("lfu", "decode", False), ("lfru", "decode", False),
+                                                ("slru", "decode", False), ("lru", "decode", True),
+                                                ("slru", "whole", True)])
+def test_offload_device_planned_staging(policy, parts, split):
     """Staging events planned on the GPU (moe_pool_stage_device) from the
     device counts, with the misses copied by the SMs out of the mapped host
     store: per (layer, step) event the slot map the planner writes equals
     the oracle's policy simulation; staged slots hold the host store's
     bytes; layer outputs match the oracle; after detaching, every layer's
     counters, last loads and slot map equal the oracle's.  Host staging
-    before attaching and after detaching continues the same state."""
+    before attaching and after detaching continues the same state.  With
+    ``split`` the copies run on a second stream while the FFN of the event's
+    hits runs (MOE_FFN_SKIP_ABSENT over the planner's hits map), and the
+    loads' part is added after joining."""
     import torch
 
     import routed_expert_ffn_histogram_gb300 as M
@@ -215,6 +220,8 @@ def test_offload_device_planned_staging(policy, parts):
     out = torch.empty((T, H), dtype=torch.float32, device="cuda")
     state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
+    copy_stream = torch.cuda.Stream()
+    split_maps = torch.empty((2, E), dtype=torch.int32, device="cuda")
     last = [[] for _ in range(L)]
     with torch.cuda.stream(stream):
         for step in range(14):
@@ -239,12 +246,31 @@ def test_offload_device_planned_staging(policy, parts):
                     torch.bfloat16)
                 M.moe_route_plan(lg, k, plan, stream=stream)
                 if device_side:
-                    pool.stage_device(layer, plan.counts, slot_of, stream=stream)
+                    if split:
+                        pool.stage_device(layer, plan.counts, slot_of, split_dev=split_maps, stream=stream,
+                                          copy=copy_stream)
+                        M.moe_expert_ffn(pool, layer, x, plan, split_maps[0], out, ws, path=M.MOE_PATH_DECODE,
+                                         stream=stream, skip_absent=True)
+                        pool.device_join(layer, stream=stream)
+                        M.moe_expert_ffn(pool, layer, x, plan, split_maps[1], out, ws, path=M.MOE_PATH_DECODE,
+                                         stream=stream, skip_absent=True, accumulate=True)
+                    else:
+                        pool.stage_device(layer, plan.counts, slot_of, stream=stream)
+                        M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE,
+                                         stream=stream)
                     stream.synchronize()
                     counts = plan.counts_host.numpy().copy()
                     loads = ref[layer].step(counts)
                     last[layer] = loads
-                    assert np.array_equal(slot_of.cpu().numpy(), ref[layer].slot_map())
+                    smap = ref[layer].slot_map()
+                    assert np.array_equal(slot_of.cpu().numpy(), smap)
+                    if split:
+                        loaded = {e for e, _ in loads}
+                        routed = counts > 0
+                        want_hit = np.where(routed & ~np.isin(np.arange(E), list(loaded)), smap, -1)
+                        want_load = np.where(np.isin(np.arange(E), list(loaded)), smap, -1)
+                        got = split_maps.cpu().numpy()
+                        assert np.array_equal(got[0], want_hit) and np.array_equal(got[1], want_load)
                     for e, s in loads:  # the staged parts, sampled at both ends of each
                         got = dev[(layer * wl.slots + s) * eb:(layer * wl.slots + s + 1) * eb]
                         want = host[((layer * E) + e) * eb:((layer * E) + e + 1) * eb]
@@ -255,7 +281,8 @@ def test_offload_device_planned_staging(policy, parts):
                     counts = plan.counts_host.numpy().copy()
                     assert pool.last_loads(layer) == ref[layer].step(counts)
                     assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
-                M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE, stream=stream)
+                    M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE,
+                                     stream=stream)
                 if step in (4, 7, 11, 13):
                     stream.synchronize()
                     r, _ = _oracle_layer(wl, layer, step, prefill=False)
@@ -305,4 +332,51 @@ def test_device_planned_capacity_and_negative_counts():
     pool.stage_device(0, counts, slot_of)
     assert pool.device_detach() == M.MOE_ERR_INVALID
     assert pool.counters(0)["events"] == 1
+    pool.close()
+
+
+def test_decode_ffn_skip_absent_parts_sum_to_the_layer():
+    """MOE_FFN_SKIP_ABSENT: a layer's assignments served in two calls over
+    complementary slot maps (the second accumulating) sum to the one-call
+    result; a call that serves nothing leaves an accumulated out unchanged
+    and writes zeros otherwise."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[1]
+    pool, host, dev = make_pool(M, wl, layers=1, slots=wl.experts, preload=True)
+    T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
+    lg = torch.from_numpy(S.logits(wl, 0, 3)).cuda()
+    x = torch.from_numpy(S.activations_bf16_bits(wl, 0, 3).view(np.int16)).cuda().view(torch.bfloat16)
+    plan = M.RoutePlan.allocate(T, E, k)
+    M.moe_route_plan(lg, k, plan, with_counts_host=False)
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    full_map = torch.arange(E, dtype=torch.int32, device="cuda")
+    full = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    M.moe_expert_ffn(pool, 0, x, plan, full_map, full, ws, path=M.MOE_PATH_DECODE)
+    ids = plan.ids.cpu().numpy().ravel()
+    a_map = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    b_map = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    for j, e in enumerate(ids):
+        (a_map if j % 2 == 0 else b_map)[int(e)] = int(e)
+    part = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    M.moe_expert_ffn(pool, 0, x, plan, a_map, part, ws, path=M.MOE_PATH_DECODE, skip_absent=True)
+    M.moe_expert_ffn(pool, 0, x, plan, b_map, part, ws, path=M.MOE_PATH_DECODE, skip_absent=True,
+                     accumulate=True)
+    torch.cuda.synchronize()
+    assert rel_l2(part.cpu().numpy(), full.cpu().numpy()) <= 1e-6
+    r, _ = _oracle_layer(wl, 0, 3, prefill=False)
+    assert rel_l2(part.cpu().numpy(), r) <= DECODE_REL_L2
+    none = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    before = part.clone()
+    M.moe_expert_ffn(pool, 0, x, plan, none, part, ws, path=M.MOE_PATH_DECODE, skip_absent=True, accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.equal(part, before)
+    M.moe_expert_ffn(pool, 0, x, plan, none, part, ws, path=M.MOE_PATH_DECODE, skip_absent=True)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(part).item() == 0
+    pws = M.alloc_ffn_workspace(64, k, H, I, M.MOE_PATH_PREFILL)
+    with pytest.raises(M.MoeError):
+        M.moe_expert_ffn(pool, 0, x, plan, a_map, part, pws, path=M.MOE_PATH_PREFILL, skip_absent=True)
     pool.close()
