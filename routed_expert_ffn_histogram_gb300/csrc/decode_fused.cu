@@ -208,7 +208,6 @@ struct FusedParams {
     float* out;        // fp32 [T][H]
     unsigned* ctl;     // [0] CTAs finished (zero between calls), [2] error bits
     int accumulate;    // out += result: partial sums go to out, no completion pass
-    int skip_absent;   // serve only the assignments whose expert's slot is >= 0
     // fused routing (logits != nullptr): the kernel selects the experts itself
     // and CTA 0 writes the routing outputs below
     const float* logits;
@@ -268,7 +267,7 @@ struct Ring {
 // changes (and at the end) the thread adds w_a * y[n] into out (residual
 // form) or into the fp32 accumulator of its token, which the last CTA to
 // finish copies to `out` and clears.  No CTA ever waits for another one.
-template <int NG, int NN>
+template <int NG, int NN, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -306,11 +305,11 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // The assignments this launch serves: all of them, or with skip_absent
-    // those whose expert has a slot (>= 0; a slot >= S still counts and
-    // yields NaN).  Every warp forms the same mask.
+    // The assignments this launch serves: all of them, or (kSkip, the
+    // skip-absent launches) those whose expert has a slot (>= 0; a slot >= S
+    // still counts and yields NaN).  Every warp forms the same mask.
     uint64_t act = (A >= 64) ? ~0ull : ((1ull << A) - 1ull);
-    if (p.skip_absent) {
+    if (kSkip) {
         uint64_t m = 0;
         for (int base = 0; base < A; base += 32) {
             const int a = base + lane;
@@ -325,7 +324,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
     }
     // This CTA's items: a contiguous range of the n_act * I / 16 items in
     // (served assignment, column block) order.
-    const int items = __popcll(act) * p.I / kGroup;
+    const int items = (kSkip ? __popcll(act) : A) * p.I / kGroup;
     const int per = (items + G - 1) / G;
     const int g0 = min(items, (int)blockIdx.x * per), g1 = min(items, g0 + per);
     const int cnt = g1 - g0;
@@ -436,7 +435,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
         // per ring: next slot, its phase, and the next item's (assignment, row)
         const int it0 = g0 * kGroup;
         const int ai0 = it0 / p.I;
-        const int a0 = nth_active(act, ai0);
+        const int a0 = kSkip ? nth_active(act, ai0) : ai0;
         int gu_slot = 0, gu_a = a0, gu_r = it0 - ai0 * p.I;
         uint32_t gu_ph = 0;
         int d_slot = 0, d_a = a0, d_r = gu_r;
@@ -446,7 +445,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             const uint32_t ph = gu_ph;
             const int a = gu_a, r = gu_r;
             if (++gu_slot == n_gu) { gu_slot = 0; gu_ph ^= 1u; }
-            if ((gu_r += kGroup) == p.I) { gu_r = 0; gu_a = next_active(act, gu_a); }
+            if ((gu_r += kGroup) == p.I) { gu_r = 0; gu_a = kSkip ? next_active(act, gu_a) : gu_a + 1; }
             if (!tc::mbar_wait_suspend(&rb.empty_gu[slot], ph ^ 1u, err, 4u)) return false;
             if (n == 0 && p.stall) return true;   // test hook: the first item never lands
             if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
@@ -471,7 +470,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             const uint32_t ph = d_ph;
             const int a = d_a, r = d_r;
             if (++d_slot == n_d) { d_slot = 0; d_ph ^= 1u; }
-            if ((d_r += kGroup) == p.I) { d_r = 0; d_a = next_active(act, d_a); }
+            if ((d_r += kGroup) == p.I) { d_r = 0; d_a = kSkip ? next_active(act, d_a) : d_a + 1; }
             if (!tc::mbar_wait_suspend(&rb.empty_d[slot], ph ^ 1u, err, 4u)) return false;
             if (n == 0 && p.stall) return true;
             if (!tc::mbar_wait_suspend(&rb.assigned[a], 0u, err, 4u)) return false;
@@ -537,7 +536,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
         // slots and phases, the token's staged x, the h-exponent word
         const int it0 = g0 * kGroup;
         const int ai0 = it0 / p.I;
-        int a = nth_active(act, ai0), r = it0 - ai0 * p.I;
+        int a = kSkip ? nth_active(act, ai0) : ai0, r = it0 - ai0 * p.I;
         int sg = 0, sd = 0, hm = 0;
         uint32_t ph_gu = 0, ph_d = 0;
         const uint4* xt = xs;
@@ -655,7 +654,7 @@ decode_fused_kernel(FusedParams p, int n_gu, int n_d, int gu_off, int d_off) {
             }
             __syncwarp();
             if (lane == 0 && gotd) tc::mbar_arrive(&rb.empty_d[sd]);
-            if ((r += kGroup) == p.I) { r = 0; a = next_active(act, a); }
+            if ((r += kGroup) == p.I) { r = 0; a = kSkip ? next_active(act, a) : a + 1; }
             if (++sg == n_gu) { sg = 0; ph_gu ^= 1u; }
             if (++sd == n_d) { sd = 0; ph_d ^= 1u; }
             hm = (hm == 2) ? 0 : hm + 1;
@@ -766,7 +765,6 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     p.acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_acc_offset(a.T, a.k, L.I));
     p.out = a.out;
     p.accumulate = a.accumulate ? 1 : 0;
-    p.skip_absent = a.skip_absent ? 1 : 0;
     p.logits = ro ? ro->logits : nullptr;
     p.r_ids = ro ? ro->ids : nullptr;
     p.r_w = ro ? ro->w : nullptr;
@@ -779,20 +777,28 @@ int launch_decode_fused_impl(const FfnArgs& a, void* ws, cudaStream_t s, const R
     using Kern = void (*)(FusedParams, int, int, int, int);
     struct Variant {
         int ng, nn;
+        bool skip;
         Kern kern;
     };
     // ng = ceil(H / 1024) groups of 32 scale blocks per row, nn = ceil(H / 512)
-    // outputs per consumer thread; H <= 4096 gives exactly these pairs.
+    // outputs per consumer thread; H <= 4096 gives exactly these pairs.  The
+    // skip-absent launches have kernels of their own, so the others keep
+    // their code exactly.
     static const Variant variants[] = {
-        {1, 1, decode_fused_kernel<1, 1>}, {1, 2, decode_fused_kernel<1, 2>}, {2, 3, decode_fused_kernel<2, 3>},
-        {2, 4, decode_fused_kernel<2, 4>}, {3, 5, decode_fused_kernel<3, 5>}, {3, 6, decode_fused_kernel<3, 6>},
-        {4, 7, decode_fused_kernel<4, 7>}, {4, 8, decode_fused_kernel<4, 8>},
+        {1, 1, false, decode_fused_kernel<1, 1, false>}, {1, 2, false, decode_fused_kernel<1, 2, false>},
+        {2, 3, false, decode_fused_kernel<2, 3, false>}, {2, 4, false, decode_fused_kernel<2, 4, false>},
+        {3, 5, false, decode_fused_kernel<3, 5, false>}, {3, 6, false, decode_fused_kernel<3, 6, false>},
+        {4, 7, false, decode_fused_kernel<4, 7, false>}, {4, 8, false, decode_fused_kernel<4, 8, false>},
+        {1, 1, true, decode_fused_kernel<1, 1, true>},   {1, 2, true, decode_fused_kernel<1, 2, true>},
+        {2, 3, true, decode_fused_kernel<2, 3, true>},   {2, 4, true, decode_fused_kernel<2, 4, true>},
+        {3, 5, true, decode_fused_kernel<3, 5, true>},   {3, 6, true, decode_fused_kernel<3, 6, true>},
+        {4, 7, true, decode_fused_kernel<4, 7, true>},   {4, 8, true, decode_fused_kernel<4, 8, true>},
     };
     constexpr int kVariants = int(sizeof(variants) / sizeof(variants[0]));
     static DeviceOnce attr_set[kVariants];
     int vi = -1;
     for (int i = 0; i < kVariants; ++i)
-        if (variants[i].ng == ng && variants[i].nn == nn) vi = i;
+        if (variants[i].ng == ng && variants[i].nn == nn && variants[i].skip == a.skip_absent) vi = i;
     if (vi < 0) return MOE_ERR_UNSUPPORTED;
     const Kern kern = variants[vi].kern;
     if (di.device < 0 || di.device >= 64) return MOE_ERR_UNSUPPORTED;
