@@ -628,9 +628,12 @@ def offload_obj(args, wl, host):
     h2d = c1["h2d_bytes"] - c0["h2d_bytes"]
     link = h2d / (ms * args.steps / 1e3) / 1e9
     misses = c1["misses"] - c0["misses"]
+    ref_o = out_pin.double()
+    out_rel = float((dv["out"].double() - ref_o).norm() / ref_o.norm().clamp_min(1e-30))
     obj = {"workload": wl.name, "value": 1e3 / ms, "unit": "tokens/s", "ms_per_step": ms,
            "host_planned": host_planned, "same_events_as_host_planned": (misses, c1["hits"] - c0["hits"]) == (
                host_planned["misses"], host_planned["hits"]),
+           "outputs_vs_host_planned_rel_l2": out_rel,
            "config": {"layers": L, "hidden": H, "inter": I, "experts": E, "top_k": k, "slots_per_layer": Sl,
                       "routing_bias": wl.bias_c, "policy": args.policy, "stage_parts": args.stage_parts,
                       "prefetch": args.prefetch, "tokens_per_step": 1,
@@ -737,7 +740,7 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L, split=
     pool.close()
     del graphs
     return {"ms": a.elapsed_time(b) / args.steps, "c0": c0, "c1": c1, "clocks": clocks,
-            "launches_per_layer": 5 if split else 4}
+            "launches_per_layer": 5 if split else 4, "out": out_pin}
 
 
 def _prefill_setup(M, wl, dev):
@@ -1230,8 +1233,8 @@ def _standalone_line(obj, args):
             "warmup": args.warmup, "ms_per_step": obj["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": obj.get("dtype", "f32"), "data": "synthetic",
             "config": dict(workload=obj["workload"], **obj["config"])}
-    for key in ("roofline", "kernels_us", "ffn_times", "staging", "host_planned", "same_events_as_host_planned", "e2e",
-                "gpu_launches", "clocks", "cpu_baseline"):
+    for key in ("roofline", "kernels_us", "ffn_times", "staging", "host_planned", "same_events_as_host_planned",
+                "outputs_vs_host_planned_rel_l2", "e2e", "gpu_launches", "clocks", "cpu_baseline"):
         if key in obj:
             line[key] = obj[key]
     return line

@@ -380,3 +380,70 @@ def test_decode_ffn_skip_absent_parts_sum_to_the_layer():
     with pytest.raises(M.MoeError):
         M.moe_expert_ffn(pool, 0, x, plan, a_map, part, pws, path=M.MOE_PATH_PREFILL, skip_absent=True)
     pool.close()
+
+
+def test_device_planned_step_in_cuda_graphs():
+    """A decode step of device-planned staging (routing, planning, the copy
+    on a second stream beside the hits' FFN, the loads' FFN) captured in a
+    CUDA graph per step and replayed: counters, last loads and slot maps
+    after detaching equal the oracle's LRU over the same events, and the
+    replayed outputs match the oracle."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    L, steps = 3, 6
+    pool, host, dev = make_pool(M, wl, layers=L, preload=False)
+    pool.close()
+    pool = M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev, policy="lru",
+                  stage_parts="decode")
+    ref = [oracle.LRUPool(wl.slots, wl.experts) for _ in range(L)]
+    T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
+    lg = torch.stack([torch.stack([torch.from_numpy(S.logits(wl, l, g)) for l in range(L)])
+                      for g in range(steps)]).cuda()
+    xs = torch.stack([torch.stack([torch.from_numpy(S.activations_bf16_bits(wl, l, g).view(np.int16))
+                                   for l in range(L)]) for g in range(steps)]).cuda().view(torch.bfloat16)
+    outs = torch.zeros((steps, L, T, H), dtype=torch.float32, device="cuda")
+    counts = torch.zeros((steps, L, E), dtype=torch.int32, device="cuda")
+    plan = M.RoutePlan.allocate(T, E, k)
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    maps = torch.empty((2, E), dtype=torch.int32, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device="cuda")
+    stream, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    pool.device_attach(state, stream=stream)
+    graphs = []
+    for g in range(steps):
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            for l in range(L):
+                M.moe_route_plan(lg[g, l], k, plan, stream=stream, with_counts_host=False)
+                counts[g, l].copy_(plan.counts)
+                pool.stage_device(l, plan.counts, slot_of, split_dev=maps, stream=stream, copy=copy)
+                M.moe_expert_ffn(pool, l, xs[g, l], plan, maps[0], outs[g, l], ws,
+                                 path=M.MOE_PATH_DECODE, stream=stream, skip_absent=True)
+                pool.device_join(l, stream=stream)
+                M.moe_expert_ffn(pool, l, xs[g, l], plan, maps[1], outs[g, l], ws,
+                                 path=M.MOE_PATH_DECODE, stream=stream, skip_absent=True, accumulate=True)
+        graphs.append(cg)
+    with torch.cuda.stream(stream):
+        for cg in graphs:
+            cg.replay()
+    stream.synchronize()
+    assert pool.device_detach(stream=stream) == M.MOE_OK
+    c_host = counts.cpu().numpy()
+    last = [[] for _ in range(L)]
+    for g in range(steps):
+        for l in range(L):
+            last[l] = ref[l].step(c_host[g, l])
+    for l in range(L):
+        c, e = pool.counters(l), ref[l].counters()
+        assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+        assert pool.last_loads(l) == last[l]
+        assert np.array_equal(pool.slot_map(l), ref[l].slot_map())
+    for g, l in ((0, 0), (steps - 1, L - 1), (3, 1)):
+        r, _ = _oracle_layer(wl, l, g, prefill=False)
+        assert rel_l2(outs[g, l].cpu().numpy(), r) <= DECODE_REL_L2
+    assert pool.counters()["misses"] > 0
+    pool.close()
