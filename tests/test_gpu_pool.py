@@ -447,3 +447,66 @@ def test_device_planned_step_in_cuda_graphs():
         assert rel_l2(outs[g, l].cpu().numpy(), r) <= DECODE_REL_L2
     assert pool.counters()["misses"] > 0
     pool.close()
+
+
+def test_device_planned_events_after_host_prefetches():
+    """Host steps (staging plus next-layer prefetch) alternate with
+    device-planned steps: the experts a host prefetch copied in and an
+    event then routes count as prefetch hits on the device too, and every
+    counter (prefetches and prefetch hits included) and slot map equals the
+    oracle's policy simulation of the same sequence."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    L = 3
+    pool, host, dev = make_pool(M, wl, layers=L, preload=False)
+    pool.close()
+    pool = M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev, policy="lru")
+    ref = [oracle.PolicyPool(wl.slots, wl.experts, "lru") for _ in range(L)]
+    T, E, k, H, I = 1, wl.experts, wl.top_k, wl.hidden, wl.inter
+    plan = M.RoutePlan.allocate(T, E, k, counts_host=True)
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device="cuda")
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    device_hits = 0
+    with torch.cuda.stream(compute):
+        for step in range(12):
+            device_side = step % 2 == 1
+            if device_side:
+                before = pool.counters()["prefetch_hits"]
+                pool.device_attach(state, stream=compute)
+            for layer in range(L):
+                lg = torch.from_numpy(S.logits(wl, layer, step)).cuda()
+                x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step).view(np.int16)).cuda().view(
+                    torch.bfloat16)
+                M.moe_route_plan(lg, k, plan, stream=compute)
+                if device_side:
+                    pool.stage_device(layer, plan.counts, slot_of, stream=compute)
+                    compute.synchronize()
+                    ref[layer].step(plan.counts_host.numpy().copy())
+                    assert np.array_equal(slot_of.cpu().numpy(), ref[layer].slot_map())
+                else:
+                    assert pool.stage(layer, plan.counts_host, slot_of, compute=compute, copy=copy) == M.MOE_OK
+                    ref[layer].step(plan.counts_host.numpy().copy())
+                    nxt = (layer + 1) % L
+                    assert pool.prefetch(nxt, 2, compute=compute, copy=copy) == len(ref[nxt].prefetch(2))
+                M.moe_expert_ffn(pool, layer, x, plan, slot_of, out, ws, path=M.MOE_PATH_DECODE, stream=compute)
+                if step in (1, 11) and layer == 1:
+                    compute.synchronize()
+                    r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                    assert rel_l2(out.cpu().numpy(), r) <= DECODE_REL_L2
+            if device_side:
+                assert pool.device_detach(stream=compute) == M.MOE_OK
+                device_hits += pool.counters()["prefetch_hits"] - before
+    compute.synchronize()
+    for layer in range(L):
+        c, e, pc = pool.counters(layer), ref[layer].counters(), ref[layer].prefetch_counters()
+        assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+        assert (c["prefetches"], c["prefetch_hits"]) == (pc["prefetches"], pc["prefetch_hits"])
+        assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
+    assert device_hits > 0
+    pool.close()
