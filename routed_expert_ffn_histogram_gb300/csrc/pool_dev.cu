@@ -53,6 +53,10 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
     __shared__ int8_t seg[MOE_MAX_EXPERTS];
     __shared__ PlanLoad loads[MOE_MAX_EXPERTS];
     __shared__ int ok_s;
+    // launched with programmatic stream serialisation: the counts and the
+    // record are read only after the previous kernel has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int t = threadIdx.x;
     int32_t* g_se = reinterpret_cast<int32_t*>(rec + dr.se);
     int32_t* g_es = reinterpret_cast<int32_t*>(rec + dr.es);
@@ -197,8 +201,17 @@ __global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8
 int launch_pool_plan(uint8_t* rec, int S, int E, int policy, const int32_t* counts, int32_t* slot_of,
                      int32_t* split, uint64_t bytes_per_load, cudaStream_t s) {
     if (E > MOE_MAX_EXPERTS || S > E) return MOE_ERR_INVALID;
-    pool_plan_kernel<<<1, kPlanThreads, 0, s>>>(rec, dev_record(S, E), S, E, policy, counts, slot_of, split,
-                                                  (unsigned long long)bytes_per_load);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, pool_plan_kernel, rec, dev_record(S, E), S, E, policy, counts, slot_of,
+                                    split, (unsigned long long)bytes_per_load));
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }

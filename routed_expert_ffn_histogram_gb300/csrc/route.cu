@@ -175,6 +175,10 @@ __global__ void __launch_bounds__(32) route_tiny_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    // launched with programmatic stream serialisation: nothing is read
+    // before the previous kernel in the stream has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x;
     const int A = T * k;
     __shared__ int sel_id[32];
@@ -256,7 +260,17 @@ int launch_route_epl(const float* logits, int T, int E, int k, int32_t* ids, flo
                      int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* tile_hist, int n_tiles,
                      cudaStream_t s) {
     if (T * k <= 32) {
-        route_tiny_kernel<EPL><<<1, 32, 0, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, inv);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(32);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, route_tiny_kernel<EPL>, logits, T, E, k, ids, w, counts, offsets,
+                                        perm, inv));
     } else if (n_tiles <= 1) {
         route_single_kernel<EPL><<<1, kThreads, 0, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, inv);
     } else {
