@@ -482,6 +482,20 @@ def _pinned_link_peak(dev):
     return 3 * (1 << 30) / (a0.elapsed_time(b0) / 1e3) / 1e9
 
 
+def _store_warm_pass(host, eb, dev):
+    """Every expert of the store copied once into a device scratch buffer;
+    returns the pass's rate, GB/s (host clock)."""
+    import torch
+
+    scratch = torch.empty(eb, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(host.numel() // eb):
+        scratch.copy_(host[i * eb:(i + 1) * eb], non_blocking=True)
+    torch.cuda.synchronize()
+    return host.numel() / (time.perf_counter() - t0) / 1e9
+
+
 def _store_link_rate(host, eb, dev, n=48):
     """Copy rate from the expert store itself, GB/s: ``n`` whole experts
     spread over the store, each one cudaMemcpyAsync into a device scratch
@@ -561,10 +575,16 @@ def offload_obj(args, wl, host):
     slots = torch.empty(L * Sl * eb, dtype=torch.uint8, device=dev)
     pool = M.Pool(L, E, Sl, H, I, host_experts=host, dev_slots=slots, preload=False, policy=args.policy,
                   stage_parts=args.stage_parts)
+    # One pass over the whole store first (every expert copied once): the
+    # first device reads of a store the CPU has just packed run at a
+    # fraction of the link rate, a one-time cost of loading that a server
+    # pays before it serves, not a per-token cost.
+    warm_gbs = _store_warm_pass(host, eb, dev)
     # the host copy rates right before and after the timed region: a fresh
     # 1 GiB pinned buffer and whole experts out of the store itself (the
     # store's rate has been seen to vary between boxes and runs)
-    rates = {"pinned_1gib_before": _pinned_link_peak(dev), "store_before": _store_link_rate(host, eb, dev)}
+    rates = {"pinned_1gib_before": _pinned_link_peak(dev), "store_before": _store_link_rate(host, eb, dev),
+             "store_warm_pass": warm_gbs}
     G = args.warmup + args.steps
     lg_pin = torch.from_numpy(np.stack([np.stack([S.logits(wl, l, g % wl.steps) for l in range(L)])
                                         for g in range(G)])).pin_memory()
