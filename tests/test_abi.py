@@ -199,3 +199,38 @@ def test_injected_copy_failure_rolls_back():
     assert pool.stage(0, c2) == M.MOE_OK
     assert pool.last_loads(0) == ref.step(c2)
     assert np.array_equal(pool.slot_map(0), ref.slot_map())
+
+
+def test_device_planned_staging_arguments_checked_on_the_host():
+    """The device-planned staging calls validate on the host before any CUDA
+    call: a dry-run pool cannot attach, an unattached pool cannot stage on
+    the device, join or detach, bad pointers and layers are refused, and the
+    state size is one record per layer (16-byte multiples)."""
+    import ctypes as C
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    L = M._lib.lib()
+    pool = M.Pool(3, 32, 8, 2880, 2880, dry_run=True)
+    n = pool.device_state_bytes()
+    assert n > 0 and n % (3 * 16) == 0
+    buf = C.create_string_buffer(n + 16)
+    aligned = (C.addressof(buf) + 15) & ~15
+    assert L.moe_pool_device_attach(pool.handle, aligned, n, None, 100) == M.MOE_ERR_STATE
+    assert L.moe_pool_device_attach(pool.handle, None, n, None, 100) == M.MOE_ERR_INVALID
+    assert L.moe_pool_device_attach(pool.handle, aligned + 4, n, None, 100) == M.MOE_ERR_INVALID
+    assert L.moe_pool_device_attach(pool.handle, aligned, n - 16, None, 100) == M.MOE_ERR_INVALID
+    assert L.moe_pool_device_attach(None, aligned, n, None, 100) == M.MOE_ERR_INVALID
+    counts = (C.c_int32 * 32)()
+    slots = (C.c_int32 * 32)()
+    assert L.moe_pool_stage_device(pool.handle, 0, counts, slots, None, None, None) == M.MOE_ERR_STATE
+    assert L.moe_pool_stage_device(pool.handle, 3, counts, slots, None, None, None) == M.MOE_ERR_INVALID
+    assert L.moe_pool_stage_device(pool.handle, 0, None, slots, None, None, None) == M.MOE_ERR_INVALID
+    assert L.moe_pool_stage_device(pool.handle, 0, counts, None, None, None, None) == M.MOE_ERR_INVALID
+    assert L.moe_pool_device_join(pool.handle, 0, None) == M.MOE_ERR_STATE
+    assert L.moe_pool_device_join(pool.handle, -1, None) == M.MOE_ERR_INVALID
+    assert L.moe_pool_device_detach(pool.handle, None, 100) == M.MOE_ERR_STATE
+    assert L.moe_pool_device_detach(None, None, 100) == M.MOE_ERR_INVALID
+    # the host-side calls still work on the (never attached) pool
+    assert pool.counters()["events"] == 0
+    pool.close()
