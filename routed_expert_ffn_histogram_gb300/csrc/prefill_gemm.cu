@@ -30,9 +30,11 @@
 //   warp 1     MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale 1X,
 //              M=128 N=256 K=32, four per stage, into a tensor-memory
 //              accumulator;
-//   warps 4-7  scale-factor feeders: per stage, the E8M0 bytes of the
-//              tile's 128 activation rows and 256 weight rows go into a
-//              tensor-memory ring slot tied to the shared-memory stage;
+//   warps 4-7  scale-factor feeders: per group of four stages, the E8M0
+//              bytes of the tile's 128 activation rows and 256 weight rows
+//              go into one of two tensor-memory slots, freed by an MMA
+//              commit once the group that used the slot two groups back
+//              has finished;
 //   warps 8-15 epilogue: copy the finished accumulator into registers
 //              (a half row per thread), hand it back to the MMA for the
 //              next tile, and finish the tile from registers.
@@ -64,19 +66,22 @@ constexpr uint32_t kStageBytesA = kBM * kBK;   // E4M3: one byte per element
 constexpr uint32_t kStageBytesB = kBN * kBK;   // E2M1 unpacked: 16 bytes per 16 elements in smem
 constexpr uint32_t kTxBytesB = kBN * kBK / 2;  // ...of which TMA writes the 8 packed bytes per 16
 constexpr uint32_t kTmemCols = 512;
-// Tensor-memory columns: the fp32 accumulator at [0, kBN); the scale-factor
-// ring after it, 16 columns per shared-memory stage: A at +0 (4 columns), B
-// at +8 (kBN / 32 columns).  Row m of an operand keeps its stage's four E8M0
-// bytes in lane m % 32 of every lane quarter, column base + m / 32 (each
-// quarter of the tensor core reads its own copy); byte j of that word
-// belongs to the stage's j-th block of 32 and is picked by the MMA's
-// scale-factor id.
+// Tensor-memory columns: the fp32 accumulator at [0, kBN); then two
+// scale-factor slots of 64 columns, each holding the factors of a group of
+// four K stages (the feeders write a whole group at once, which the MMA
+// waits for once per group: fresh factors before every stage cost the
+// tensor pipe about 200 cycles a stage), 16 columns per stage: A at +0 (4
+// columns), B at +8 (kBN / 32 columns).  Row m of an operand keeps its
+// stage's four E8M0 bytes in lane m % 32 of every lane quarter, column
+// base + m / 32 (each quarter of the tensor core reads its own copy); byte
+// j of that word belongs to the stage's j-th block of 32 and is picked by
+// the MMA's scale-factor id.
 constexpr uint32_t kColSf = kBN;
-__host__ __device__ constexpr uint32_t sf_col(int s) { return kColSf + 16 * s; }
+__host__ __device__ constexpr uint32_t sf_col_g(int gs, int s) { return kColSf + 64 * gs + 16 * s; }
 constexpr int kMaxExperts = MOE_MAX_EXPERTS;
 constexpr int kYPad = 20;          // padded row of the epilogue's y staging tile (words)
 static_assert(kBN % 64 == 0 && kBN / 32 <= 8, "tile width: whole chunk pairs, B scales in 8 columns");
-static_assert(sf_col(kStages) <= kTmemCols, "tensor-memory columns");
+static_assert(sf_col_g(2, 0) <= kTmemCols, "tensor-memory columns");
 // Register split between the warpgroups (setmaxnreg): launched with
 // kLaunchRegs per thread, warpgroup 0 (TMA, MMA) gives registers up to the
 // scale-factor feeders (warpgroup 1) and the epilogue (warpgroups 2, 3),
@@ -117,7 +122,8 @@ struct __align__(1024) Smem {
     uint8_t a[kStages][kStageBytesA];
     uint8_t b[kStages][kStageBytesB];
     uint64_t full[kStages];      // TMA bytes landed
-    uint64_t sf_full[kStages];   // scale factors of the stage written to tensor memory
+    uint64_t sf_full[2];         // scale factors of a group slot written to tensor memory
+    uint64_t sf_empty[2];        // the MMAs of the group that used a slot have finished
     uint64_t empty[kStages];     // MMAs of the stage finished (smem and scale slot free)
     uint64_t acc_full;           // accumulator holds a finished tile
     uint64_t acc_empty;          // epilogue has read the accumulator into registers
@@ -264,7 +270,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
             sm.n_tiles = uint32_t(carry) * uint32_t(NT);
             for (int s = 0; s < kStages; ++s) {
                 tc::mbar_init(&sm.full[s], 1);
-                tc::mbar_init(&sm.sf_full[s], 128);
+                if (s < 2) {
+                    tc::mbar_init(&sm.sf_full[s], 128);
+                    tc::mbar_init(&sm.sf_empty[s], 1);
+                }
                 tc::mbar_init(&sm.empty[s], 1);
             }
             tc::mbar_init(&sm.acc_full, 1);
@@ -311,21 +320,23 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
             int stage = 0;
             uint32_t phase = 0;
             int i = 0;
+            int gr = 0;   // scale-factor groups consumed so far
             for (int t = blockIdx.x; t < n_tiles && !*err; t += gridDim.x, ++i) {
                 // the epilogue has read tile i - 1 out of the accumulator
                 if (!tc::mbar_wait_hot(&sm.acc_empty, (i & 1) ^ 1u, err, 2u)) break;
                 tc::tc_fence_after();
                 bool ok = true;
                 for (int ks = 0; ks < n_kstages; ++ks) {
-                    if (!tc::mbar_wait_hot(&sm.full[stage], phase, err, 2u) ||
-                        !tc::mbar_wait_hot(&sm.sf_full[stage], phase, err, 2u)) {
+                    const int sg = ks & 3;
+                    if ((sg == 0 && !tc::mbar_wait_hot(&sm.sf_full[gr & 1], uint32_t(gr >> 1) & 1u, err, 2u)) ||
+                        !tc::mbar_wait_hot(&sm.full[stage], phase, err, 2u)) {
                         ok = false;
                         break;
                     }
                     tc::tc_fence_after();
                     const uint32_t a0 = tc::smem_u32(sm.a[stage]);
                     const uint32_t b0 = tc::smem_u32(sm.b[stage]);
-                    const uint32_t sfa = tmem + sf_col(stage);
+                    const uint32_t sfa = tmem + sf_col_g(gr & 1, sg);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk) {
                         const int kb = ks * (kBK / 32) + kk;
@@ -337,6 +348,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                         }
                     }
                     tc::mma_commit(&sm.empty[stage]);
+                    if (sg == 3 || ks == n_kstages - 1) {
+                        tc::mma_commit(&sm.sf_empty[gr & 1]);
+                        ++gr;
+                    }
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -349,17 +364,17 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
     } else if (wg == 1) {
         setmaxnreg_inc<kRegsSf>();
         // ---------------- scale-factor feeders (warps 4..7 = lane quarters 0..3) ----------------
-        // Thread (quarter q, lane l) writes lane 32q + l of the ring slot:
-        // column c of the A part gets the stage's four scale bytes of
-        // activation row 32c + l (c < 4), column c of the B part those of
-        // weight row 32c + l (c < kBN / 32).  Each row's bytes are read 16 at
-        // a time (a group of four stages), one group ahead -- across tile
-        // boundaries too, so a new tile's first stages never wait for loads.
+        // Thread (quarter q, lane l) writes lane 32q + l of a group slot:
+        // for each stage of the group, column c of the A part gets the
+        // stage's four scale bytes of activation row 32c + l (c < 4), column
+        // c of the B part those of weight row 32c + l (c < kBN / 32).  Each
+        // row's bytes are read 16 at a time (a group of four stages), one
+        // group ahead -- across tile boundaries too, so a new tile's first
+        // stages never wait for loads.
         const int q = warp & 3;
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
         const int ngroups = (n_kstages + 3) / 4;
-        int stage = 0;
-        uint32_t phase = 0;
+        int gr = 0;   // scale-factor groups written so far
         int t = blockIdx.x;
         Tile tl{};
         uint4 xa[4], xb[kRb];
@@ -384,25 +399,26 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                     next_ok = nx.slot >= 0 && nx.slot < p.S;
                     if (next_ok) sf_load_group(p, nx, lane, 0, na, nb);
                 }
+                // the group slot is free once the MMAs of the group two back have finished
+                if (gr >= 2 && !tc::mbar_wait_hot(&sm.sf_empty[gr & 1], uint32_t((gr >> 1) + 1) & 1u, err, 64u)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     if (4 * g + w >= n_kstages) break;
-                    if (!tc::mbar_wait_hot(&sm.empty[stage], phase ^ 1u, err, 64u)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    const uint32_t col = lane_base + sf_col(stage);
+                    const uint32_t col = lane_base + sf_col_g(gr & 1, w);
                     tc::tmem_st_x4(col, word_of(xa[0], w), word_of(xa[1], w), word_of(xa[2], w), word_of(xa[3], w));
                     uint32_t bw[8];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) bw[c] = c < kRb ? word_of(xb[c < kRb ? c : 0], w) : 0u;
                     tc::tmem_st_x8(col + 8, bw);
-                    tc::tmem_st_wait();
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(&sm.sf_full[stage]);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sm.sf_full[gr & 1]);
+                ++gr;
                 if (g + 1 < ngroups || next_ok) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) xa[c] = na[c];
