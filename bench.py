@@ -58,7 +58,7 @@ NCU_TRAFFIC = {
     "gguf_fused_kernel/q4_k": 21_341_440 + 0,
     "gguf_fused_kernel/q8_0": 40_212_736 + 2_304,
     # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
-    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_076_544 + 30_997_760) + (234_813_952 + 32_667_392),
+    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_092_928 + 30_377_216) + (233_449_216 + 30_491_392),
 }
 
 # Dense tensor-core rates of GB300 in the published ratios (bf16 : fp8 : fp4

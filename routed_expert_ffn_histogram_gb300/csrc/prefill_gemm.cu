@@ -30,7 +30,7 @@
 //   warp 1     MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale 1X,
 //              M=128 N=256 K=32, four per stage, into a tensor-memory
 //              accumulator;
-//   warps 4-7  scale-factor feeders: per group of four stages, the E8M0
+//   warps 4-7  scale-factor feeders: per group of eight stages, the E8M0
 //              bytes of the tile's 128 activation rows and 256 weight rows
 //              go into one of two tensor-memory slots, freed by an MMA
 //              commit once the group that used the slot two groups back
@@ -67,8 +67,8 @@ constexpr uint32_t kStageBytesB = kBN * kBK;   // E2M1 unpacked: 16 bytes per 16
 constexpr uint32_t kTxBytesB = kBN * kBK / 2;  // ...of which TMA writes the 8 packed bytes per 16
 constexpr uint32_t kTmemCols = 512;
 // Tensor-memory columns: the fp32 accumulator at [0, kBN); then two
-// scale-factor slots of 64 columns, each holding the factors of a group of
-// four K stages (the feeders write a whole group at once, which the MMA
+// scale-factor slots of 128 columns, each holding the factors of a group of
+// eight K stages (the feeders write a whole group at once, which the MMA
 // waits for once per group: fresh factors before every stage cost the
 // tensor pipe about 200 cycles a stage), 16 columns per stage: A at +0 (4
 // columns), B at +8 (kBN / 32 columns).  Row m of an operand keeps its
@@ -77,7 +77,8 @@ constexpr uint32_t kTmemCols = 512;
 // j of that word belongs to the stage's j-th block of 32 and is picked by
 // the MMA's scale-factor id.
 constexpr uint32_t kColSf = kBN;
-__host__ __device__ constexpr uint32_t sf_col_g(int gs, int s) { return kColSf + 64 * gs + 16 * s; }
+constexpr int kSfGroup = 8;   // K stages per scale-factor group
+__host__ __device__ constexpr uint32_t sf_col_g(int gs, int s) { return kColSf + 16 * kSfGroup * gs + 16 * s; }
 constexpr int kMaxExperts = MOE_MAX_EXPERTS;
 constexpr int kYPad = 20;          // padded row of the epilogue's y staging tile (words)
 static_assert(kBN % 64 == 0 && kBN / 32 <= 8, "tile width: whole chunk pairs, B scales in 8 columns");
@@ -165,21 +166,29 @@ __device__ __forceinline__ Tile decode_tile(const Smem& sm, const GemmParams& p,
 
 constexpr int kRb = kBN / 32;  // 32-row groups of a B tile
 
-// Scale bytes of group g (stages 4g..4g+3) of a tile's rows for feeder lane
-// `lane`: A rows m0 + 32c + lane, B rows nt * kBN + 32c + lane (clamped to
-// the last row; the clamped rows' factors only meet padding).
-__device__ __forceinline__ void sf_load_group(const GemmParams& p, const Tile& tl, int lane, int g, uint4 (&xa)[4],
-                                              uint4 (&xb)[kRb]) {
+// Scale bytes of group g (stages 8g..8g+7, 32 bytes a row) of a tile's
+// rows for feeder lane `lane`: A rows m0 + 32c + lane, B rows
+// nt * kBN + 32c + lane (clamped to the last row; the clamped rows' factors
+// only meet padding), xa[2c + h] / xb[2c + h] the row's h-th 16 bytes;
+// zero past the row's scale bytes (a last group of four stages or fewer).
+__device__ __forceinline__ void sf_load_group8(const GemmParams& p, const Tile& tl, int lane, int g, uint4 (&xa)[8],
+                                               uint4 (&xb)[2 * kRb]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int arow = min(tl.m0 + 32 * c + lane, p.A - 1);
-        xa[c] = __ldg(reinterpret_cast<const uint4*>(p.a_scales + (size_t)arow * p.a_sf_stride) + g);
+        const uint4* r = reinterpret_cast<const uint4*>(p.a_scales + (size_t)arow * p.a_sf_stride);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            xa[2 * c + h] = (2 * g + h) * 16 < p.a_sf_stride ? __ldg(r + 2 * g + h) : make_uint4(0u, 0u, 0u, 0u);
     }
     const uint8_t* bb = p.b_base + (size_t)tl.slot * p.expert_bytes + p.b_code_bytes;
 #pragma unroll
     for (int c = 0; c < kRb; ++c) {
         const int brow = min(tl.nt * kBN + 32 * c + lane, p.N - 1);
-        xb[c] = __ldg(reinterpret_cast<const uint4*>(bb + (size_t)brow * p.b_rs) + g);
+        const uint4* r = reinterpret_cast<const uint4*>(bb + (size_t)brow * p.b_rs);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            xb[2 * c + h] = (2 * g + h) * 16 < p.b_sf_bytes ? __ldg(r + 2 * g + h) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -327,7 +336,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                 tc::tc_fence_after();
                 bool ok = true;
                 for (int ks = 0; ks < n_kstages; ++ks) {
-                    const int sg = ks & 3;
+                    const int sg = ks & (kSfGroup - 1);
                     if ((sg == 0 && !tc::mbar_wait_hot(&sm.sf_full[gr & 1], uint32_t(gr >> 1) & 1u, err, 2u)) ||
                         !tc::mbar_wait_hot(&sm.full[stage], phase, err, 2u)) {
                         ok = false;
@@ -348,7 +357,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                         }
                     }
                     tc::mma_commit(&sm.empty[stage]);
-                    if (sg == 3 || ks == n_kstages - 1) {
+                    if (sg == kSfGroup - 1 || ks == n_kstages - 1) {
                         tc::mma_commit(&sm.sf_empty[gr & 1]);
                         ++gr;
                     }
@@ -368,21 +377,22 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
         // for each stage of the group, column c of the A part gets the
         // stage's four scale bytes of activation row 32c + l (c < 4), column
         // c of the B part those of weight row 32c + l (c < kBN / 32).  Each
-        // row's bytes are read 16 at a time (a group of four stages), one
-        // group ahead -- across tile boundaries too, so a new tile's first
-        // stages never wait for loads.
+        // row's bytes are read 32 at a time (a group of eight stages) right
+        // after the previous group is written, a group ahead of their use --
+        // across tile boundaries too, so a new tile's first stages never
+        // wait for loads; one register set suffices.
         const int q = warp & 3;
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
-        const int ngroups = (n_kstages + 3) / 4;
+        const int ngroups = (n_kstages + kSfGroup - 1) / kSfGroup;
         int gr = 0;   // scale-factor groups written so far
         int t = blockIdx.x;
         Tile tl{};
-        uint4 xa[4], xb[kRb];
+        uint4 xa[8], xb[2 * kRb];
         bool have = false;
         if (t < n_tiles) {
             tl = decode_tile(sm, p, t, NT);
             if (tl.slot >= 0 && tl.slot < p.S) {
-                sf_load_group(p, tl, lane, 0, xa, xb);
+                sf_load_group8(p, tl, lane, 0, xa, xb);
                 have = true;
             }
         }
@@ -391,14 +401,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
             Tile nx{};
             bool next_ok = false, ok = true;
             for (int g = 0; g < ngroups && ok; ++g) {
-                uint4 na[4], nb[kRb];
-                if (g + 1 < ngroups) {
-                    sf_load_group(p, tl, lane, g + 1, na, nb);
-                } else if (tn < n_tiles) {
-                    nx = decode_tile(sm, p, tn, NT);
-                    next_ok = nx.slot >= 0 && nx.slot < p.S;
-                    if (next_ok) sf_load_group(p, nx, lane, 0, na, nb);
-                }
                 // the group slot is free once the MMAs of the group two back have finished
                 if (gr >= 2 && !tc::mbar_wait_hot(&sm.sf_empty[gr & 1], uint32_t((gr >> 1) + 1) & 1u, err, 64u)) {
                     ok = false;
@@ -406,24 +408,28 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                 }
                 tc::tc_fence_after();
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    if (4 * g + w >= n_kstages) break;
+                for (int w = 0; w < kSfGroup; ++w) {
+                    if (kSfGroup * g + w >= n_kstages) break;
                     const uint32_t col = lane_base + sf_col_g(gr & 1, w);
-                    tc::tmem_st_x4(col, word_of(xa[0], w), word_of(xa[1], w), word_of(xa[2], w), word_of(xa[3], w));
+                    const int h = w >> 2, wi = w & 3;
+                    tc::tmem_st_x4(col, word_of(xa[h], wi), word_of(xa[2 + h], wi), word_of(xa[4 + h], wi),
+                                   word_of(xa[6 + h], wi));
                     uint32_t bw[8];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) bw[c] = c < kRb ? word_of(xb[c < kRb ? c : 0], w) : 0u;
+                    for (int c = 0; c < 8; ++c) bw[c] = c < kRb ? word_of(xb[2 * (c < kRb ? c : 0) + h], wi) : 0u;
                     tc::tmem_st_x8(col + 8, bw);
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 tc::mbar_arrive(&sm.sf_full[gr & 1]);
                 ++gr;
-                if (g + 1 < ngroups || next_ok) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) xa[c] = na[c];
-#pragma unroll
-                    for (int c = 0; c < kRb; ++c) xb[c] = nb[c];
+                // the next group's bytes, loaded while this group is consumed
+                if (g + 1 < ngroups) {
+                    sf_load_group8(p, tl, lane, g + 1, xa, xb);
+                } else if (tn < n_tiles) {
+                    nx = decode_tile(sm, p, tn, NT);
+                    next_ok = nx.slot >= 0 && nx.slot < p.S;
+                    if (next_ok) sf_load_group8(p, nx, lane, 0, xa, xb);
                 }
             }
             if (!ok || !next_ok) break;
