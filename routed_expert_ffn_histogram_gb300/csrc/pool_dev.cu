@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
         uint64_t* ctr = reinterpret_cast<uint64_t*>(rec + dr.ctr);  // moe_counters, field order
         int64_t* g_clk = reinterpret_cast<int64_t*>(rec + dr.clk);
         int32_t* g_n = reinterpret_cast<int32_t*>(rec + dr.n_loads);
+        int32_t* g_copy = reinterpret_cast<int32_t*>(rec + dr.n_copy);
         int ok = 0;
         if (!any_negative && uniq <= S) {
             PlanView v{se, es, st, uses, seg, *g_clk, S, E, policy};
@@ -115,13 +116,15 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
                     if (loads[i].victim >= 0) g_fresh[loads[i].victim] = 0;
                 }
                 *g_n = n;
+                *g_copy = n;
             }
         }
         if (!ok) {
-            // nothing changes: the planned copies are none and the slot map
-            // stays the current one (routed experts that are absent stay -1)
+            // nothing changes: no copies, the slot map stays the current one
+            // (routed experts that are absent stay -1), and the last loads
+            // stay those of the last successful event
             *reinterpret_cast<int32_t*>(rec + dr.status) |= any_negative ? 1 : 2;
-            *g_n = 0;
+            *g_copy = 0;
         }
         ok_s = ok;
     }
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8
                                                                      const uint8_t* host_layer, uint8_t* slots_layer,
                                                                      unsigned long long eb, unsigned long long len0,
                                                                      unsigned long long off1, unsigned long long len1) {
-    const int n = *reinterpret_cast<const int32_t*>(rec + dr.n_loads);
+    const int n = *reinterpret_cast<const int32_t*>(rec + dr.n_copy);
     const int32_t* le = reinterpret_cast<const int32_t*>(rec + dr.le);
     const int32_t* ls = reinterpret_cast<const int32_t*>(rec + dr.ls);
     const unsigned long long c0 = (len0 + kChunk - 1) / kChunk, c1 = (len1 + kChunk - 1) / kChunk;

@@ -155,7 +155,7 @@ MOE_HD int plan_event(PlanView& v, const int32_t* counts, const uint8_t* keep, P
 // at these byte offsets (16-byte aligned record).
 struct DevRecord {
     size_t bytes;
-    size_t ctr, clk, n_loads, status, st, uses, freq, se, es, le, ls, seg, fresh;
+    size_t ctr, clk, n_loads, status, n_copy, st, uses, freq, se, es, le, ls, seg, fresh;
 };
 
 MOE_HD size_t dev_align16(size_t n) { return (n + 15) & ~size_t(15); }
@@ -165,8 +165,9 @@ MOE_HD DevRecord dev_record(int S, int E) {
     size_t o = 0;
     r.ctr = o;     o += 8 * 8;               // moe_counters: eight uint64
     r.clk = o;     o += 8;
-    r.n_loads = o; o += 4;                   // loads of the last event
+    r.n_loads = o; o += 4;                   // loads of the last successful event
     r.status = o;  o += 4;                   // bit 0: negative count, bit 1: more than S routed
+    r.n_copy = o;  o += 8;                   // loads the current event's copy kernel makes (0 after a failed event)
     r.st = o;      o += 8 * size_t(S);
     r.uses = o;    o += 8 * size_t(S);
     r.freq = o;    o += 8 * size_t(E);       // events that routed each expert

@@ -326,6 +326,7 @@ def test_device_planned_capacity_and_negative_counts():
     assert pool.slot_map(0).tolist() == [-1, 0] + [-1] * (E - 2)
     c = pool.counters(0)
     assert (c["misses"], c["events"]) == (1, 1)
+    assert pool.last_loads(0) == [(1, 0)]   # the last successful event's, as moe_pool_stage keeps them
     pool.device_attach(state)
     counts.zero_()
     counts[3] = -1
@@ -510,3 +511,52 @@ def test_device_planned_events_after_host_prefetches():
         assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
     assert device_hits > 0
     pool.close()
+
+
+
+@pytest.mark.parametrize("policy", ["lru", "fifo", "lfu", "lfru", "slru"])
+def test_device_planned_random_events_match_host_planning(policy):
+    """Random routing counts (including events that route more experts than
+    slots) staged on the GPU and, for the same sequence, by a dry-run host
+    pool: counters, slot maps and last loads of every layer agree after
+    detaching, and the copied slots hold the host store's bytes."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[0]
+    L, Sl, E = 2, 3, wl.experts
+    pool, host, dev = make_pool(M, wl, layers=L, slots=Sl, preload=False)
+    pool.close()
+    pool = M.Pool(L, E, Sl, wl.hidden, wl.inter, host_experts=host, dev_slots=dev, policy=policy)
+    ref = M.Pool(L, E, Sl, wl.hidden, wl.inter, dry_run=True, policy=policy)
+    state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device="cuda")
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    counts_d = torch.empty(E, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(1234 + ["lru", "fifo", "lfu", "lfru", "slru"].index(policy))
+    pool.device_attach(state)
+    capacity_events = 0
+    for i in range(80):
+        layer = int(rng.integers(0, L))
+        routed = rng.choice(E, size=int(rng.integers(0, Sl + 2)), replace=False)
+        counts = np.zeros(E, np.int32)
+        counts[routed] = rng.integers(1, 4, size=len(routed))
+        counts_d.copy_(torch.from_numpy(counts))
+        pool.stage_device(layer, counts_d, slot_of)
+        rc = ref.stage(layer, torch.from_numpy(counts))
+        capacity_events += rc == M.MOE_ERR_CAPACITY
+    torch.cuda.synchronize()
+    assert pool.device_detach() == (M.MOE_ERR_CAPACITY if capacity_events else M.MOE_OK)
+    assert capacity_events > 0
+    eb = M.moe_expert_bytes(wl.hidden, wl.inter)
+    for layer in range(L):
+        assert pool.counters(layer) == {**ref.counters(layer), "errors": pool.counters(layer)["errors"]}
+        assert np.array_equal(pool.slot_map(layer), ref.slot_map(layer))
+        assert pool.last_loads(layer) == ref.last_loads(layer)
+        for e, s in enumerate(pool.slot_map(layer).tolist()):
+            if s >= 0:
+                got = dev[(layer * Sl + s) * eb:(layer * Sl + s + 1) * eb]
+                want = host[(layer * E + e) * eb:(layer * E + e + 1) * eb]
+                assert torch.equal(got.cpu(), want)
+    pool.close()
+    ref.close()
