@@ -295,3 +295,38 @@ def test_wait_timeout_sets_status_and_context_stays_usable():
     M.moe_decode_layer(pool, 0, lgt, x, plan, slot_of, out, ws)
     assert M.moe_ffn_status(ws, M.MOE_PATH_DECODE) == 0
     assert rel_l2(out.cpu().numpy(), _oracle_T(wl, lg, xb, prefill=False)) <= DECODE_REL_L2
+
+
+@pytest.mark.parametrize("H", [768, 1536, 2560, 3584, 4096])
+def test_decode_hidden_sizes_of_every_kernel_instance(H):
+    """Hidden sizes that select the decode kernel's other instances (groups
+    of 32 scale blocks per row and output rows per thread: 768 -> (1, 2),
+    1536 -> (2, 3), 2560 -> (3, 5), 3584 -> (4, 7), 4096 -> (4, 8), the
+    largest; the last may not fit the one-launch kernel's shared memory and
+    then runs on the two-kernel path): the expert FFN and the fused layer
+    call both match the oracle."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.Workload(200 + H // 256, "hidden_sweep", 1, H, 512, 8, 2, 2, 1, 8, 0.0, 200 + H // 256)
+    pool, host, dev = make_pool(M, wl)
+    lgn, xb = S.logits(wl, 0), S.activations_bf16_bits(wl, 0)
+    ref, _ = _oracle_layer(wl, 0, 0, prefill=False)
+    out = _gpu_layer(M, pool, 0, lgn, xb, wl.top_k, M.MOE_PATH_DECODE)
+    assert rel_l2(out, ref) <= 1e-4
+    lg = torch.from_numpy(lgn).cuda()
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    plan = M.RoutePlan.allocate(wl.tokens, wl.experts, wl.top_k)
+    ws = M.alloc_ffn_workspace(wl.tokens, wl.top_k, H, wl.inter, M.MOE_PATH_DECODE)
+    out2 = torch.empty((wl.tokens, H), dtype=torch.float32, device="cuda")
+    slot_of = torch.arange(wl.experts, dtype=torch.int32, device="cuda")
+    try:
+        M.moe_decode_layer(pool, 0, lg, x, plan, slot_of, out2, ws)
+    except M.MoeError:
+        # the fused layer call needs the one-launch kernel; at the largest
+        # size it may not fit, which the call reports instead of running
+        assert H == 4096
+        return
+    torch.cuda.synchronize()
+    assert rel_l2(out2.cpu().numpy(), ref) <= 1e-4
