@@ -170,3 +170,19 @@ def test_prefill_staged_small_pool(wid, slots, window, T):
     assert rel_l2(out.cpu().numpy(), out2.cpu().numpy()) <= 1e-6
     pool.close()
     resident.close()
+
+
+@pytest.mark.parametrize("H,I", [(4096, 1024), (1024, 4096), (3584, 640)])
+def test_prefill_reduction_lengths(H, I):
+    """Prefill at the largest hidden and intermediate sizes the GEMM takes and
+    at a reduction length whose last group of scale factors is partial
+    (K = 640: five 128-K stages, one group of five; K = 3584: 28 stages,
+    three groups of eight and one of four), against the oracle."""
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.Workload(300 + H // 256 + I // 64, "prefill_k_sweep", 1, H, I, 8, 2, 260, 1, 8, 0.0,
+                    300 + H // 256 + I // 64)
+    pool, host, dev = make_pool(M, wl)
+    out, lg, x, plan, ws = _run_prefill(M, pool, wl)
+    ref, _ = _oracle_tokens(wl, lg, x, np.arange(wl.tokens))
+    _check_prefill(out, ref)
