@@ -53,6 +53,12 @@
 //            residual stream), else to an fp32 accumulator in the
 //            workspace that the last CTA to finish (a ticket counter, no
 //            waiting) copies to the output and clears for the next call.
+// Skip-absent launches (MOE_FFN_SKIP_ABSENT; kernel instances of their own)
+// serve only the assignments whose expert has a slot: every warp forms the
+// same bit mask of them, and the work items run over those assignments
+// alone, spread over all CTAs -- a layer then computes in two launches over
+// complementary slot maps (the event's hits beside the copy of its misses,
+// then the loaded experts).
 // No CTA waits for another: there is no grid barrier and no cooperative
 // launch.  Waits inside the CTA are bounded mbarrier waits (about a second,
 // then an error bit and NaN output instead of a hang).  The kernel is
