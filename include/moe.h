@@ -190,10 +190,9 @@ MOE_API int moe_route_plan(const float* logits, int T, int E, int k,
  *   Limit: T <= 16384 tokens (64 tiles of 256); larger T returns
  *   MOE_ERR_INVALID before anything is enqueued.
  *   The first call on a device resolves the array's device address for that
- *   device (with it current) and keeps it for the life of the process; make
- *   that first call before any stream capture, and do not call this entry
- *   again after the device has been reset (cudaDeviceReset) in the same
- *   process.  Each call clears the part of the array it uses with an
+ *   device (a runtime symbol lookup, made with that device current) and keeps
+ *   it for the life of the process; do not call this entry again after the
+ *   device has been reset (cudaDeviceReset) in the same process.  Each call clears the part of the array it uses with an
  *   asynchronous memset on `stream` (no allocation) before counting into
  *   it; all calls share the array, so calls that can overlap on the GPU
  *   race.
