@@ -44,10 +44,14 @@
 // memory, and the quick register copy stands in for a second accumulator.
 // Tiles (expert, 128-row block, 256-column block) are enumerated on the
 // device from the offsets; columns vary fastest so the CTAs working at the
-// same time share an expert's activation rows and weight rows through L2.
+// same time share an expert's activation rows and weight rows through L2
+// (for a down launch whose output exceeds half of L2, within groups of a
+// few column blocks, so that the output rows its combine adds into stay
+// in L2 while they are being hit).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstddef>
 #include <mutex>
 
@@ -116,6 +120,8 @@ struct GemmParams {
     const float* w;             // mode 1: [A] routing weight of each assignment
     int k;                      // mode 1: assignments per token
     float* out;                 // mode 1: [A / k][N], zero before the launch; w * y added atomically
+    int n_group;                // 256-column blocks per tile group (1..NT): the tiles run group by
+                                // group, 128-row blocks within a group, columns innermost
     uint32_t* err;              // error bits (device word)
 };
 
@@ -148,8 +154,20 @@ struct Tile {
 
 __device__ __forceinline__ Tile decode_tile(const Smem& sm, const GemmParams& p, int t, int NT) {
     Tile tl;
-    const int mt = t / NT;
-    tl.nt = t - mt * NT;
+    int mt;
+    const int G = p.n_group;
+    if (G >= NT) {
+        mt = t / NT;
+        tl.nt = t - mt * NT;
+    } else {
+        // groups of G column blocks (the last one may be narrower)
+        const int per = int(sm.n_tiles / uint32_t(NT)) * G;
+        const int g = t / per;
+        const int r = t - g * per;
+        const int Gg = min(G, NT - g * G);
+        mt = r / Gg;
+        tl.nt = g * G + (r - mt * Gg);
+    }
     int lo = 0, hi = p.E;  // largest e with mt_prefix[e] <= mt
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -758,6 +776,7 @@ int launch_prefill_experts(const FfnArgs& a, void* ws, int e0, int e1, const int
     g.hq = hq;
     g.hs = hs;
     g.hs_stride = w.hs_stride;
+    g.n_group = (g.N + kBN - 1) / kBN;
     rc = launch_gemm(map_x, map_gu, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
     if (rc != MOE_OK) return rc;
     // down: K = I, N = H, epilogue w * y added into out[token]
@@ -775,6 +794,18 @@ int launch_prefill_experts(const FfnArgs& a, void* ws, int e0, int e1, const int
     g.w = a.w;
     g.k = a.k;
     g.out = a.out;
+    // The down tiles of one column block add into that block of every
+    // routed token's row of out: when out is larger than half of L2, the
+    // tiles run a few column blocks at a time so that the out rows they
+    // read-modify-write stay in L2.
+    {
+        const int NT = (g.N + kBN - 1) / kBN;
+        const size_t per_block = size_t(a.T) * kBN * sizeof(float);
+        const size_t budget = size_t(64) << 20;
+        g.n_group = size_t(a.T) * size_t(g.N) * sizeof(float) <= budget
+                        ? NT
+                        : int(std::max<size_t>(1, std::min<size_t>(size_t(NT), budget / per_block)));
+    }
     return launch_gemm(map_h, map_d, g, max_mtiles * ((g.N + kBN - 1) / kBN), s);
 }
 
