@@ -53,12 +53,12 @@ METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 roo
 NCU_TRAFFIC = {
     # one decode layer (2-layer decode capture; traffic per launch does not
     # depend on the number of layers)
-    "decode_fused_kernel": 54_205_952 + 16_640,
+    "decode_fused_kernel": 54_206_208 + 7_936,
     # one layer of the 24-layer GGUF leg (a launch after 40 others)
     "gguf_fused_kernel/q4_k": 21_341_440 + 0,
     "gguf_fused_kernel/q8_0": 40_212_736 + 2_304,
     # gate/up launch + down launch of one 3072-token GPT-OSS-shaped layer
-    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_092_928 + 30_377_216) + (233_449_216 + 30_491_392),
+    "grouped_gemm_tc_kernel/gptoss20b_prefill_t3072": (320_126_976 + 31_258_624) + (234_308_096 + 31_640_832),
 }
 
 # Dense tensor-core rates of GB300 in the published ratios (bf16 : fp8 : fp4
