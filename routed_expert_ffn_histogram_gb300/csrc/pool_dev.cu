@@ -12,8 +12,9 @@
 // decisions are those of the host pool (the planning code is shared); what
 // differs is where they are taken: on a Grace host the GPU reads pinned host
 // memory at the link rate itself, so the route -> plan -> copy -> FFN chain
-// of a layer runs on one stream with no host round trip between routing and
-// the copies.
+// of a layer is enqueued once and runs with no host round trip between
+// routing and the copies (the copy on a second stream, beside the FFN of the
+// event's hits, when the caller asks for it).
 //
 // Kernels:
 //   pool_plan_kernel    one CTA of 256 threads: the layer's record is loaded
