@@ -223,10 +223,10 @@ int stage_event(moe_pool_t* p, int layer, const int32_t* counts, const uint8_t* 
     ls.seg.assign(sg, sg + S);
     ls.clk = clk;
     std::vector<moe::PlanLoad> plan(size_t(S) + 1);
-    std::vector<int32_t> hit_e(size_t(S) + 1);
+    std::vector<int32_t> hit_e(size_t(S) + 1), miss_e(size_t(S) + 1);
     int n_hits = 0;
     moe::PlanView v = ls.view(S, E, policy);
-    const int n_loads = moe::plan_event(v, counts, keep, plan.data(), hit_e.data(), &n_hits);
+    const int n_loads = moe::plan_event(v, counts, keep, plan.data(), hit_e.data(), &n_hits, miss_e.data());
     if (n_loads < 0) return MOE_ERR_CAPACITY;  // U and keep together fill the slots
     ls.clk = v.clk;
     plan.resize(size_t(n_loads));

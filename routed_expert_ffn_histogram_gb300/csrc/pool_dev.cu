@@ -49,7 +49,9 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
                                                                  int32_t* __restrict__ slot_of,
                                                                  int32_t* __restrict__ split,
                                                                  unsigned long long bytes_per_load) {
-    __shared__ int32_t se[MOE_MAX_EXPERTS], es[MOE_MAX_EXPERTS], cnt[MOE_MAX_EXPERTS], hit_e[MOE_MAX_EXPERTS];
+    __shared__ int32_t se[MOE_MAX_EXPERTS], es[MOE_MAX_EXPERTS], cnt[MOE_MAX_EXPERTS], hit_e[MOE_MAX_EXPERTS],
+        miss_e[MOE_MAX_EXPERTS];
+    __shared__ int warp_hits[kPlanThreads / 32], warp_misses[kPlanThreads / 32];
     __shared__ int64_t st[MOE_MAX_EXPERTS], uses[MOE_MAX_EXPERTS];
     __shared__ int8_t seg[MOE_MAX_EXPERTS];
     __shared__ PlanLoad loads[MOE_MAX_EXPERTS];
@@ -79,8 +81,31 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
         c = counts[t];
         cnt[t] = c;
     }
+    // the event's routed experts, split into resident (hits) and absent
+    // (misses), each list in ascending expert id, built by all threads so
+    // that the planning thread walks only the routed experts
+    const int lane = t & 31, wid = t >> 5;
+    const bool is_hit = c > 0 && es0 >= 0, is_miss = c > 0 && es0 < 0;
+    const unsigned bh = __ballot_sync(0xffffffffu, is_hit), bm = __ballot_sync(0xffffffffu, is_miss);
+    if (lane == 0) {
+        warp_hits[wid] = __popc(bh);
+        warp_misses[wid] = __popc(bm);
+    }
     const int any_negative = __syncthreads_or(c < 0);
     const int uniq = __syncthreads_count(c > 0);
+    int nh_all = 0, nm_all = 0, oh = 0, om = 0;
+    for (int i = 0; i < kPlanThreads / 32; ++i) {
+        if (i == wid) {
+            oh = nh_all;
+            om = nm_all;
+        }
+        nh_all += warp_hits[i];
+        nm_all += warp_misses[i];
+    }
+    const unsigned below = (1u << lane) - 1u;
+    if (is_hit) hit_e[oh + __popc(bh & below)] = t;
+    if (is_miss) miss_e[om + __popc(bm & below)] = t;
+    __syncthreads();
     if (t == 0) {
         uint64_t* ctr = reinterpret_cast<uint64_t*>(rec + dr.ctr);  // moe_counters, field order
         int64_t* g_clk = reinterpret_cast<int64_t*>(rec + dr.clk);
@@ -89,8 +114,8 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
         int ok = 0;
         if (!any_negative && uniq <= S) {
             PlanView v{se, es, st, uses, seg, *g_clk, S, E, policy};
-            int nh = 0;
-            const int n = plan_event(v, cnt, nullptr, loads, hit_e, &nh);
+            const int nh = nh_all;
+            const int n = plan_event_lists(v, cnt, nullptr, hit_e, nh_all, miss_e, nm_all, loads);
             if (n >= 0) {  // always, without a keep set: U fits in the slots
                 ok = 1;
                 *g_clk = v.clk;

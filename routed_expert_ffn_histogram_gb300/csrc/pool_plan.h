@@ -120,24 +120,20 @@ MOE_HD void plan_load(PlanView& v, int e, int s) {
     v.seg[s] = 0;
 }
 
-// Plans one event in place.  counts: [E], every entry >= 0 and at most S of
-// them nonzero (the caller checks).  Writes the hits' expert ids to hit_e
-// (ascending, *n_hits of them) and the loads to `loads` in issue order
-// (ascending expert id).  Returns the number of loads, or -1 if a miss
-// found neither a free slot nor a victim (only possible with `keep`); the
-// view is then partly modified, so callers plan on copies.
-MOE_HD int plan_event(PlanView& v, const int32_t* counts, const uint8_t* keep, PlanLoad* loads, int32_t* hit_e,
-                      int* n_hits) {
-    int nh = 0;
-    for (int e = 0; e < v.E; ++e)
-        if (counts[e] > 0 && v.es[e] >= 0) {
-            plan_touch(v, v.es[e]);
-            hit_e[nh++] = e;
-        }
-    *n_hits = nh;
+// Plans one event in place from its routed experts already split into the
+// resident ones (hits, ascending expert id) and the absent ones (misses,
+// ascending): the hits are touched in that order, then each miss takes the
+// lowest free slot or the policy's victim.  A routed expert is never a
+// victim, so the misses are exactly the routed experts absent before the
+// event.  Writes the loads to `loads` in issue order; returns their number,
+// or -1 if a miss found neither a free slot nor a victim (only possible
+// with `keep`); the view is then partly modified, so callers plan on copies.
+MOE_HD int plan_event_lists(PlanView& v, const int32_t* counts, const uint8_t* keep, const int32_t* hits, int nh,
+                            const int32_t* misses, int nm, PlanLoad* loads) {
+    for (int i = 0; i < nh; ++i) plan_touch(v, v.es[hits[i]]);
     int n = 0;
-    for (int e = 0; e < v.E; ++e) {
-        if (counts[e] <= 0 || v.es[e] >= 0) continue;
+    for (int i = 0; i < nm; ++i) {
+        const int e = misses[i];
         int s = plan_free_slot(v);
         int victim = -1;
         if (s < 0) {
@@ -149,6 +145,23 @@ MOE_HD int plan_event(PlanView& v, const int32_t* counts, const uint8_t* keep, P
         loads[n++] = PlanLoad{int32_t(e), int32_t(s), int32_t(victim)};
     }
     return n;
+}
+
+// Plans one event in place.  counts: [E], every entry >= 0 and at most S of
+// them nonzero (the caller checks).  Writes the hits' expert ids to hit_e
+// (ascending, *n_hits of them) and the loads to `loads` in issue order
+// (ascending expert id); `misses` is scratch for up to S expert ids.
+// Returns what plan_event_lists returns.
+MOE_HD int plan_event(PlanView& v, const int32_t* counts, const uint8_t* keep, PlanLoad* loads, int32_t* hit_e,
+                      int* n_hits, int32_t* misses) {
+    int nh = 0, nm = 0;
+    for (int e = 0; e < v.E; ++e) {
+        if (counts[e] <= 0) continue;
+        if (v.es[e] >= 0) hit_e[nh++] = e;
+        else misses[nm++] = e;
+    }
+    *n_hits = nh;
+    return plan_event_lists(v, counts, keep, hit_e, nh, misses, nm, loads);
 }
 
 // Device copy of the pool's per-layer state: one record per layer, fields
