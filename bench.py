@@ -658,11 +658,12 @@ def offload_obj(args, wl, host):
                       "routing_bias": wl.bias_c, "policy": args.policy, "stage_parts": args.stage_parts,
                       "prefetch": args.prefetch, "tokens_per_step": 1,
                       "timing": "end to end through the C ABI: each step's logits and activations from pinned "
-                                "host memory, per layer routing, staging planned on the GPU from the device counts "
-                                "(moe_pool_stage_device), misses copied by the SMs from the mapped pinned expert "
+                                "host memory, per layer routing and the staging event planned on the GPU in one "
+                                "launch (moe_pool_route_stage_device), misses copied by the SMs from the mapped "
+                                "pinned expert "
                                 "store on a second stream while the FFN of the event's hits runs, then the FFN of "
                                 "the loaded experts added in, outputs back to pinned host memory; one CUDA graph "
-                                "per step (24 x (routing, plan, copy | hits' FFN, loads' FFN) plus the input and "
+                                "per step (24 x (routing + plan, copy | hits' FFN, loads' FFN) plus the input and "
                                 "output copies), CUDA events"},
            "roofline": {"kernel": "miss staging: SM copy of packed experts out of mapped pinned host memory",
                         "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
@@ -688,7 +689,8 @@ def offload_obj(args, wl, host):
 
 def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L, split=True):
     """The offload decode with device-planned staging: the pool's state in
-    device memory; per layer routing -> plan, then the SM copy of the misses
+    device memory; per layer routing + planning (one launch,
+    moe_pool_route_stage_device), then the SM copy of the misses
     on a second stream while the FFN of the event's hits runs, then (joined)
     the FFN of the loaded experts added in; each step (with its input and
     output copies) one CUDA graph.  Same events as the host-planned run
@@ -718,16 +720,16 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L, split=
         lg_d.copy_(lg_pin[g], non_blocking=True)
         x_d.copy_(x_pin[g], non_blocking=True)
         for l in range(L):
-            M.moe_route_plan(lg_d[l], k, plan, stream=stream, with_counts_host=False)
+            # routing and the staging event's planning in one launch
             if split:
-                pool.stage_device(l, plan.counts, slot_of, split_dev=maps, stream=stream, copy=copy)
+                pool.route_stage_device(l, lg_d[l], k, plan, slot_of, split_dev=maps, stream=stream, copy=copy)
                 M.moe_expert_ffn(pool, l, x_d[l], plan, maps[0], out_d[l], ws, path=M.MOE_PATH_DECODE,
                                  stream=stream, skip_absent=True)
                 pool.device_join(l, stream=stream)
                 M.moe_expert_ffn(pool, l, x_d[l], plan, maps[1], out_d[l], ws, path=M.MOE_PATH_DECODE,
                                  stream=stream, skip_absent=True, accumulate=True)
             else:
-                pool.stage_device(l, plan.counts, slot_of, stream=stream)
+                pool.route_stage_device(l, lg_d[l], k, plan, slot_of, stream=stream)
                 M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE,
                                  stream=stream)
         out_pin[g].copy_(out_d, non_blocking=True)
@@ -760,7 +762,7 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L, split=
     pool.close()
     del graphs
     return {"ms": a.elapsed_time(b) / args.steps, "c0": c0, "c1": c1, "clocks": clocks,
-            "launches_per_layer": 5 if split else 4, "out": out_pin}
+            "launches_per_layer": 4 if split else 3, "out": out_pin}
 
 
 def _prefill_setup(M, wl, dev):

@@ -398,10 +398,21 @@ MOE_API int moe_pool_prefetch(moe_pool_t* pool, int layer, int max_loads, moe_st
  *   from and joined back to `compute` inside the capture).  Copy-failure
  *   injection does not apply.
  *
+ * moe_pool_route_stage_device: moe_route_plan of T tokens (T * k <= 32, the
+ *   decode shapes; MOE_ERR_UNSUPPORTED above) followed by
+ *   moe_pool_stage_device on its counts, with the routing and the planning
+ *   in one launch on `compute` (the routing warp ranks the tokens while the
+ *   other warps load the layer's record; the counts reach the planner in
+ *   shared memory).  logits, ids, w, counts, offsets, perm and inv are
+ *   moe_route_plan's (device, same layouts; E = the pool's experts) and get
+ *   the same values; slot_of_dev, split_dev, compute and copy are
+ *   moe_pool_stage_device's.  Validation happens before anything is
+ *   enqueued.
+ *
  * moe_pool_device_join: makes `compute` wait for the copies of `layer`'s
  *   last event enqueued on a separate copy stream (no-op otherwise).  The
- *   layer's next moe_pool_stage_device and moe_pool_device_detach join by
- *   themselves.
+ *   layer's next moe_pool_stage_device / moe_pool_route_stage_device and
+ *   moe_pool_device_detach join by themselves.
  *
  * moe_pool_device_detach: downloads the state into the pool on `stream`
  *   (polling, at most timeout_ms) after the work enqueued so far; the
@@ -422,6 +433,10 @@ MOE_API int moe_pool_device_attach(moe_pool_t* pool, void* dev_state, size_t byt
 MOE_API int moe_pool_stage_device(moe_pool_t* pool, int layer, const int32_t* counts_dev,
                                   int32_t* slot_of_dev, int32_t* split_dev, moe_stream_t compute,
                                   moe_stream_t copy);
+MOE_API int moe_pool_route_stage_device(moe_pool_t* pool, int layer, const float* logits, int T, int k,
+                                        int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                        int32_t* inv, int32_t* slot_of_dev, int32_t* split_dev,
+                                        moe_stream_t compute, moe_stream_t copy);
 MOE_API int moe_pool_device_join(moe_pool_t* pool, int layer, moe_stream_t compute);
 MOE_API int moe_pool_device_detach(moe_pool_t* pool, moe_stream_t stream, int timeout_ms);
 

@@ -348,6 +348,17 @@ class Pool:
             self.handle, layer, ptr(counts_dev), ptr(slot_of_dev), ptr(split_dev), stream_handle(stream),
             stream_handle(copy) if copy is not None else None))
 
+    def route_stage_device(self, layer, logits, k, plan, slot_of_dev, split_dev=None, stream=None,
+                           copy=None) -> None:
+        """Route ``logits`` (device fp32 [T, E], T * k <= 32) into ``plan``
+        and plan the layer's staging event from the routing in the same
+        launch; maps and copies as stage_device (moe_pool_route_stage_device)."""
+        T = int(logits.shape[0])
+        check("moe_pool_route_stage_device", lib().moe_pool_route_stage_device(
+            self.handle, layer, ptr(logits), T, k, ptr(plan.ids), ptr(plan.w), ptr(plan.counts), ptr(plan.offsets),
+            ptr(plan.perm), ptr(plan.inv), ptr(slot_of_dev), ptr(split_dev), stream_handle(stream),
+            stream_handle(copy) if copy is not None else None))
+
     def device_join(self, layer, stream=None) -> None:
         """``stream`` waits for the layer's copies on the copy stream
         (moe_pool_device_join)."""

@@ -80,6 +80,8 @@ SIGNATURES = {
     "moe_pool_device_state_bytes": (_i32, [_vp, _szp]),
     "moe_pool_device_attach": (_i32, [_vp, _vp, _sz, _vp, _i32]),
     "moe_pool_stage_device": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_pool_route_stage_device": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                           _vp]),
     "moe_pool_device_join": (_i32, [_vp, _i32, _vp]),
     "moe_pool_device_detach": (_i32, [_vp, _vp, _i32]),
     "moe_pool_destroy": (None, [_vp]),

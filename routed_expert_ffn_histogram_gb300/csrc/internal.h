@@ -151,6 +151,11 @@ int launch_gguf_fused(int fmt, const uint8_t* slots, int S, int E, int H, int I,
 // the device state (pool_plan.h, dev_record).
 int launch_pool_plan(uint8_t* rec, int S, int E, int policy, const int32_t* counts, int32_t* slot_of,
                      int32_t* split, uint64_t bytes_per_load, cudaStream_t s);
+// Routing of T tokens (T * k <= 32; the one-warp plan of launch_route_plan)
+// and the planning of the layer's event in one launch.
+int launch_pool_route_plan(const float* logits, int T, int k, int32_t* ids, float* w, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, uint8_t* rec, int S, int E, int policy,
+                           int32_t* slot_of, int32_t* split, uint64_t bytes_per_load, cudaStream_t s);
 int launch_pool_gather(const uint8_t* rec, int S, int E, const uint8_t* host_layer, uint8_t* slots_layer,
                        size_t eb, size_t len0, size_t off1, size_t len1, cudaStream_t s);
 

@@ -766,6 +766,33 @@ static int join_gather(moe_pool_t* p, int layer, cudaStream_t s) {
     return MOE_OK;
 }
 
+namespace {
+// After the planner: the staged parts of the event's loads copied by the SMs
+// out of the mapped store, on `copy` (forked from `compute` after the
+// planner) or on `compute`.
+int enqueue_gather(moe_pool_t* p, int layer, cudaStream_t s, cudaStream_t cp) {
+    const int S = p->d.slots_per_layer, E = p->d.experts;
+    uint8_t* rec = p->dev_state + size_t(layer) * moe::dev_record(S, E).bytes;
+    const bool fork = cp != nullptr && cp != s;
+    if (fork) {
+        MOE_CUDA_TRY(cudaEventRecord(p->ev_plan, s));
+        MOE_CUDA_TRY(cudaStreamWaitEvent(cp, p->ev_plan, 0));
+    }
+    const size_t eb = p->eb;
+    const bool decode = p->d.stage_parts == MOE_STAGE_DECODE;
+    const size_t len0 = decode ? p->L.d_off : eb;
+    const size_t off1 = decode ? p->L.dt_off : eb;
+    const size_t len1 = decode ? eb - p->L.dt_off : 0;
+    const uint8_t* host_layer = p->host_dev + size_t(layer) * size_t(E) * eb;
+    uint8_t* slots_layer = static_cast<uint8_t*>(p->d.dev_slots) + size_t(layer) * size_t(S) * eb;
+    const int rc = moe::launch_pool_gather(rec, S, E, host_layer, slots_layer, eb, len0, off1, len1, fork ? cp : s);
+    if (rc != MOE_OK || !fork) return rc;
+    MOE_CUDA_TRY(cudaEventRecord(p->ev_gather[layer], cp));
+    p->gather_pending[layer] = 1;
+    return MOE_OK;
+}
+}  // namespace
+
 extern "C" int moe_pool_stage_device(moe_pool_t* p, int layer, const int32_t* counts_dev, int32_t* slot_of_dev,
                                      int32_t* split_dev, moe_stream_t compute, moe_stream_t copy) {
     if (!p || !counts_dev || !slot_of_dev || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
@@ -778,23 +805,27 @@ extern "C" int moe_pool_stage_device(moe_pool_t* p, int layer, const int32_t* co
     uint8_t* rec = p->dev_state + size_t(layer) * moe::dev_record(S, E).bytes;
     rc = moe::launch_pool_plan(rec, S, E, p->d.policy, counts_dev, slot_of_dev, split_dev, p->bytes_per_load, s);
     if (rc != MOE_OK) return rc;
-    const bool fork = copy != nullptr && cp != s;
-    if (fork) {
-        MOE_CUDA_TRY(cudaEventRecord(p->ev_plan, s));
-        MOE_CUDA_TRY(cudaStreamWaitEvent(cp, p->ev_plan, 0));
-    }
-    const size_t eb = p->eb;
-    const bool decode = p->d.stage_parts == MOE_STAGE_DECODE;
-    const size_t len0 = decode ? p->L.d_off : eb;
-    const size_t off1 = decode ? p->L.dt_off : eb;
-    const size_t len1 = decode ? eb - p->L.dt_off : 0;
-    const uint8_t* host_layer = p->host_dev + size_t(layer) * size_t(E) * eb;
-    uint8_t* slots_layer = static_cast<uint8_t*>(p->d.dev_slots) + size_t(layer) * size_t(S) * eb;
-    rc = moe::launch_pool_gather(rec, S, E, host_layer, slots_layer, eb, len0, off1, len1, fork ? cp : s);
-    if (rc != MOE_OK || !fork) return rc;
-    MOE_CUDA_TRY(cudaEventRecord(p->ev_gather[layer], cp));
-    p->gather_pending[layer] = 1;
-    return MOE_OK;
+    return enqueue_gather(p, layer, s, cp);
+}
+
+extern "C" int moe_pool_route_stage_device(moe_pool_t* p, int layer, const float* logits, int T, int k,
+                                           int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                           int32_t* inv, int32_t* slot_of_dev, int32_t* split_dev,
+                                           moe_stream_t compute, moe_stream_t copy) {
+    if (!p || layer < 0 || layer >= p->d.layers) return MOE_ERR_INVALID;
+    if (!logits || !ids || !w || !counts || !offsets || !perm || !inv || !slot_of_dev) return MOE_ERR_INVALID;
+    const int S = p->d.slots_per_layer, E = p->d.experts;
+    if (T < 1 || k < 1 || k > E) return MOE_ERR_INVALID;
+    if (T * k > 32) return MOE_ERR_UNSUPPORTED;
+    if (!p->dev_state) return MOE_ERR_STATE;
+    cudaStream_t s = static_cast<cudaStream_t>(compute), cp = static_cast<cudaStream_t>(copy);
+    int rc = join_gather(p, layer, s);
+    if (rc != MOE_OK) return rc;
+    uint8_t* rec = p->dev_state + size_t(layer) * moe::dev_record(S, E).bytes;
+    rc = moe::launch_pool_route_plan(logits, T, k, ids, w, counts, offsets, perm, inv, rec, S, E, p->d.policy,
+                                     slot_of_dev, split_dev, p->bytes_per_load, s);
+    if (rc != MOE_OK) return rc;
+    return enqueue_gather(p, layer, s, cp);
 }
 
 extern "C" int moe_pool_device_join(moe_pool_t* p, int layer, moe_stream_t compute) {

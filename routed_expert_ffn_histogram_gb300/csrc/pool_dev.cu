@@ -21,6 +21,9 @@
 //                       into shared memory by all threads, thread 0 plans
 //                       the event (pool_plan.h) and updates the counters,
 //                       all threads write the record back and the slot map.
+//   pool_route_plan_kernel  the same planning, with the routing of the event's
+//                       tokens (T * k <= 32) done by warp 0 in the same launch
+//                       while the other warps load the record.
 //   pool_gather_kernel  one CTA of 64 threads per SM: 64 KB chunks of the
 //                       planned loads (both staged parts of each expert),
 //                       16-byte loads from host memory, eight in flight per
@@ -34,6 +37,7 @@
 
 #include "internal.h"
 #include "pool_plan.h"
+#include "route_warp.cuh"
 
 namespace moe {
 namespace {
@@ -44,22 +48,39 @@ constexpr int kGatherThreads = 64;
 constexpr int kGatherUnroll = 8;
 constexpr unsigned long long kChunk = 64ull << 10;
 
-__global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, DevRecord dr, int S, int E,
-                                                                 int policy, const int32_t* __restrict__ counts,
-                                                                 int32_t* __restrict__ slot_of,
-                                                                 int32_t* __restrict__ split,
-                                                                 unsigned long long bytes_per_load) {
-    __shared__ int32_t se[MOE_MAX_EXPERTS], es[MOE_MAX_EXPERTS], cnt[MOE_MAX_EXPERTS], hit_e[MOE_MAX_EXPERTS],
+// The planner's shared-memory copy of a layer's record and the event.
+struct PlanSmem {
+    int32_t se[MOE_MAX_EXPERTS], es[MOE_MAX_EXPERTS], cnt[MOE_MAX_EXPERTS], hit_e[MOE_MAX_EXPERTS],
         miss_e[MOE_MAX_EXPERTS];
-    __shared__ int warp_hits[kPlanThreads / 32], warp_misses[kPlanThreads / 32];
-    __shared__ int64_t st[MOE_MAX_EXPERTS], uses[MOE_MAX_EXPERTS];
-    __shared__ int8_t seg[MOE_MAX_EXPERTS];
-    __shared__ PlanLoad loads[MOE_MAX_EXPERTS];
-    __shared__ int ok_s;
-    // launched with programmatic stream serialisation: the counts and the
-    // record are read only after the previous kernel has finished
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    int warp_hits[kPlanThreads / 32], warp_misses[kPlanThreads / 32];
+    int64_t st[MOE_MAX_EXPERTS], uses[MOE_MAX_EXPERTS];
+    int8_t seg[MOE_MAX_EXPERTS];
+    PlanLoad loads[MOE_MAX_EXPERTS];
+    int ok_s;
+};
+
+// Slot-indexed fields of the record into shared memory (threads t0, t0 +
+// nt, ...); the expert-indexed ones are loaded by the callers.
+__device__ __forceinline__ void load_slots(PlanSmem& sm, const uint8_t* rec, const DevRecord& dr, int S, int t0,
+                                           int nt) {
+    const int32_t* g_se = reinterpret_cast<const int32_t*>(rec + dr.se);
+    const int64_t* g_st = reinterpret_cast<const int64_t*>(rec + dr.st);
+    const int64_t* g_uses = reinterpret_cast<const int64_t*>(rec + dr.uses);
+    const int8_t* g_seg = reinterpret_cast<const int8_t*>(rec + dr.seg);
+    for (int i = t0; i < S; i += nt) {
+        sm.se[i] = g_se[i];
+        sm.st[i] = g_st[i];
+        sm.uses[i] = g_uses[i];
+        sm.seg[i] = g_seg[i];
+    }
+}
+
+// One event planned by the whole CTA once the record and the counts are in
+// shared memory; c and es0: this thread's expert's count and slot before the
+// event (0 and -1 past E).
+__device__ void plan_block(PlanSmem& sm, int c, int es0, uint8_t* rec, const DevRecord& dr, int S, int E,
+                           int policy, int32_t* __restrict__ slot_of, int32_t* __restrict__ split,
+                           unsigned long long bytes_per_load) {
     const int t = threadIdx.x;
     int32_t* g_se = reinterpret_cast<int32_t*>(rec + dr.se);
     int32_t* g_es = reinterpret_cast<int32_t*>(rec + dr.es);
@@ -68,19 +89,18 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
     int8_t* g_seg = reinterpret_cast<int8_t*>(rec + dr.seg);
     int64_t* g_freq = reinterpret_cast<int64_t*>(rec + dr.freq);
     uint8_t* g_fresh = rec + dr.fresh;
-    if (t < S) {
-        se[t] = g_se[t];
-        st[t] = g_st[t];
-        uses[t] = g_uses[t];
-        seg[t] = g_seg[t];
-    }
-    int c = 0, es0 = -1;
-    if (t < E) {
-        es0 = g_es[t];
-        es[t] = es0;
-        c = counts[t];
-        cnt[t] = c;
-    }
+    int32_t* se = sm.se;
+    int32_t* es = sm.es;
+    int32_t* cnt = sm.cnt;
+    int32_t* hit_e = sm.hit_e;
+    int32_t* miss_e = sm.miss_e;
+    int64_t* st = sm.st;
+    int64_t* uses = sm.uses;
+    int8_t* seg = sm.seg;
+    PlanLoad* loads = sm.loads;
+    int* warp_hits = sm.warp_hits;
+    int* warp_misses = sm.warp_misses;
+    int& ok_s = sm.ok_s;
     // the event's routed experts, split into resident (hits) and absent
     // (misses), each list in ascending expert id, built by all threads so
     // that the planning thread walks only the routed experts
@@ -186,6 +206,64 @@ __global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, D
     }
 }
 
+__global__ void __launch_bounds__(kPlanThreads) pool_plan_kernel(uint8_t* rec, DevRecord dr, int S, int E,
+                                                                 int policy, const int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ slot_of,
+                                                                 int32_t* __restrict__ split,
+                                                                 unsigned long long bytes_per_load) {
+    __shared__ PlanSmem sm;
+    // launched with programmatic stream serialisation: the counts and the
+    // record are read only after the previous kernel has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int t = threadIdx.x;
+    load_slots(sm, rec, dr, S, t, kPlanThreads);
+    int c = 0, es0 = -1;
+    if (t < E) {
+        es0 = reinterpret_cast<const int32_t*>(rec + dr.es)[t];
+        sm.es[t] = es0;
+        c = counts[t];
+        sm.cnt[t] = c;
+    }
+    plan_block(sm, c, es0, rec, dr, S, E, policy, slot_of, split, bytes_per_load);
+}
+
+// Routing (T * k <= 32 assignments, warp 0, the code of the one-warp
+// routing kernel) and the event's planning in one launch: the other warps
+// load the layer's record while warp 0 ranks the tokens, and the counts
+// reach the planner through shared memory.
+template <int EPL>
+__global__ void __launch_bounds__(kPlanThreads) pool_route_plan_kernel(
+    const float* __restrict__ logits, int T, int k, int32_t* __restrict__ ids, float* __restrict__ w,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, uint8_t* rec, DevRecord dr, int S, int E, int policy, int32_t* __restrict__ slot_of,
+    int32_t* __restrict__ split, unsigned long long bytes_per_load) {
+    __shared__ PlanSmem sm;
+    __shared__ int sel_id[32];
+    __shared__ float sel_v[32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int t = threadIdx.x;
+    if (t < 32) {
+        const int my_id = route_tiny_warp<EPL>(logits, T, E, k, ids, w, counts, offsets, perm, inv, sel_id, sel_v);
+        const int A = T * k;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + t;
+            int eq = 0;
+            for (int b = 0; b < A; ++b) eq += __shfl_sync(0xffffffffu, my_id, b) == e;
+            if (e < E) sm.cnt[e] = eq;
+        }
+    } else {
+        load_slots(sm, rec, dr, S, t - 32, kPlanThreads - 32);
+        const int32_t* g_es = reinterpret_cast<const int32_t*>(rec + dr.es);
+        for (int i = t - 32; i < E; i += kPlanThreads - 32) sm.es[i] = g_es[i];
+    }
+    __syncthreads();
+    const int c = t < E ? sm.cnt[t] : 0;
+    const int es0 = t < E ? sm.es[t] : -1;
+    plan_block(sm, c, es0, rec, dr, S, E, policy, slot_of, split, bytes_per_load);
+}
+
 __global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8_t* rec, DevRecord dr,
                                                                      const uint8_t* host_layer, uint8_t* slots_layer,
                                                                      unsigned long long eb, unsigned long long len0,
@@ -243,6 +321,45 @@ int launch_pool_plan(uint8_t* rec, int S, int E, int policy, const int32_t* coun
                                     split, (unsigned long long)bytes_per_load));
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
+}
+
+namespace {
+template <int EPL>
+int launch_route_plan_epl(const float* logits, int T, int k, int32_t* ids, float* w, int32_t* counts,
+                          int32_t* offsets, int32_t* perm, int32_t* inv, uint8_t* rec, int S, int E, int policy,
+                          int32_t* slot_of, int32_t* split, uint64_t bytes_per_load, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, pool_route_plan_kernel<EPL>, logits, T, k, ids, w, counts, offsets, perm,
+                                    inv, rec, dev_record(S, E), S, E, policy, slot_of, split,
+                                    (unsigned long long)bytes_per_load));
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+}  // namespace
+
+int launch_pool_route_plan(const float* logits, int T, int k, int32_t* ids, float* w, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, uint8_t* rec, int S, int E, int policy,
+                           int32_t* slot_of, int32_t* split, uint64_t bytes_per_load, cudaStream_t s) {
+    if (E > MOE_MAX_EXPERTS || S > E || T < 1 || k < 1 || k > E || T * k > 32) return MOE_ERR_INVALID;
+    if (E <= 32)
+        return launch_route_plan_epl<1>(logits, T, k, ids, w, counts, offsets, perm, inv, rec, S, E, policy, slot_of,
+                                        split, bytes_per_load, s);
+    if (E <= 64)
+        return launch_route_plan_epl<2>(logits, T, k, ids, w, counts, offsets, perm, inv, rec, S, E, policy, slot_of,
+                                        split, bytes_per_load, s);
+    if (E <= 128)
+        return launch_route_plan_epl<4>(logits, T, k, ids, w, counts, offsets, perm, inv, rec, S, E, policy, slot_of,
+                                        split, bytes_per_load, s);
+    return launch_route_plan_epl<8>(logits, T, k, ids, w, counts, offsets, perm, inv, rec, S, E, policy, slot_of,
+                                    split, bytes_per_load, s);
 }
 
 int launch_pool_gather(const uint8_t* rec, int S, int E, const uint8_t* host_layer, uint8_t* slots_layer,

@@ -166,10 +166,8 @@ __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(
     }
 }
 
-// Whole plan in one warp when T * k <= 32 (the decode shapes): no shared
-// memory and no block barriers.  Lane a owns assignment a = t*k + j; its
-// grouped position is (# assignments with a smaller expert id) + (# earlier
-// assignments with the same id).
+// Whole plan in one warp when T * k <= 32 (the decode shapes): no block
+// barriers (route_tiny_warp).
 template <int EPL>
 __global__ void __launch_bounds__(32) route_tiny_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
@@ -179,42 +177,9 @@ __global__ void __launch_bounds__(32) route_tiny_kernel(
     // before the previous kernel in the stream has finished
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int lane = threadIdx.x;
-    const int A = T * k;
     __shared__ int sel_id[32];
     __shared__ float sel_v[32];
-    // every token's logits in flight at once, then each token ranked: the
-    // lane holding a winner records it for its assignment
-    if (T > 1) prefetch_l1(logits, T * E);
-    for (int t = 0; t < T; ++t) {
-        const float* row = logits + (size_t)t * E;
-        float v[EPL];
-        uint32_t key[EPL], taken = 0;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = e < E ? __ldg(row + e) : 0.0f;
-            key[i] = rank_key(v[i]);
-            if (e >= E) taken |= 1u << i;
-        }
-        for (int j = 0; j < k; ++j) {
-            const int bid = topk_round<EPL>(key, taken);
-            const float bv = from_winner<EPL>(v, bid);
-            if (lane == 0) {
-                sel_id[t * k + j] = bid;
-                sel_v[t * k + j] = bv;
-            }
-        }
-    }
-    __syncwarp();
-    // one softmax pass for every assignment (lane a: assignment a)
-    const int my_id = lane < A ? sel_id[lane] : MOE_MAX_EXPERTS;   // MOE_MAX_EXPERTS sorts after every real id
-    const float wv = softmax_assign(lane < A ? sel_v[lane] : 0.0f, k, A);
-    if (lane < A) {
-        ids[lane] = my_id;
-        w[lane] = wv;
-    }
-    plan_warp(my_id, A, E, counts, offsets, perm, inv);
+    route_tiny_warp<EPL>(logits, T, E, k, ids, w, counts, offsets, perm, inv, sel_id, sel_v);
 }
 
 // Multi-tile, pass 2: global offsets from all tile histograms, then the

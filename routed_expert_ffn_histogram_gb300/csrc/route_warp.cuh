@@ -228,5 +228,52 @@ __device__ __forceinline__ void plan_warp(int my_id, int A, int E, int32_t* __re
     }
 }
 
+// The whole routing plan of T tokens (T * k <= 32) in one warp: lane a
+// owns assignment a = t*k + j; its grouped position is (# assignments with a
+// smaller expert id) + (# earlier assignments with the same id).  Every
+// token's logits are put in flight at once, then each token is ranked (the
+// lane holding a winner records it for its assignment in sel_id / sel_v,
+// 32 entries of shared memory), then one softmax pass serves every
+// assignment.  Returns the lane's expert id (MOE_MAX_EXPERTS past A).
+template <int EPL>
+__device__ __forceinline__ int route_tiny_warp(const float* __restrict__ logits, int T, int E, int k,
+                                               int32_t* __restrict__ ids, float* __restrict__ w,
+                                               int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                               int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                                               int* sel_id, float* sel_v) {
+    const int lane = threadIdx.x & 31;
+    const int A = T * k;
+    if (T > 1) prefetch_l1(logits, T * E);
+    for (int t = 0; t < T; ++t) {
+        const float* row = logits + (size_t)t * E;
+        float v[EPL];
+        uint32_t key[EPL], taken = 0;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? __ldg(row + e) : 0.0f;
+            key[i] = rank_key(v[i]);
+            if (e >= E) taken |= 1u << i;
+        }
+        for (int j = 0; j < k; ++j) {
+            const int bid = topk_round<EPL>(key, taken);
+            const float bv = from_winner<EPL>(v, bid);
+            if (lane == 0) {
+                sel_id[t * k + j] = bid;
+                sel_v[t * k + j] = bv;
+            }
+        }
+    }
+    __syncwarp();
+    const int my_id = lane < A ? sel_id[lane] : MOE_MAX_EXPERTS;   // MOE_MAX_EXPERTS sorts after every real id
+    const float wv = softmax_assign(lane < A ? sel_v[lane] : 0.0f, k, A);
+    if (lane < A) {
+        ids[lane] = my_id;
+        w[lane] = wv;
+    }
+    plan_warp(my_id, A, E, counts, offsets, perm, inv);
+    return my_id;
+}
+
 }  // namespace
 }  // namespace moe

@@ -227,6 +227,26 @@ def test_device_planned_staging_arguments_checked_on_the_host():
     assert L.moe_pool_stage_device(pool.handle, 3, counts, slots, None, None, None) == M.MOE_ERR_INVALID
     assert L.moe_pool_stage_device(pool.handle, 0, None, slots, None, None, None) == M.MOE_ERR_INVALID
     assert L.moe_pool_stage_device(pool.handle, 0, counts, None, None, None, None) == M.MOE_ERR_INVALID
+    # routing + planning in one launch: the same checks, plus the routing's
+    # (logits and outputs present, 1 <= k <= E, T >= 1, T * k <= 32)
+    lg = (C.c_float * 64)()
+    o32 = [(C.c_int32 * 64)() for _ in range(5)]
+    wt = (C.c_float * 64)()
+
+    def rsd(layer, logits, T, k, slot_map):
+        return L.moe_pool_route_stage_device(pool.handle, layer, logits, T, k, o32[0], wt, o32[1], o32[2], o32[3],
+                                             o32[4], slot_map, None, None, None)
+
+    assert rsd(0, lg, 1, 4, slots) == M.MOE_ERR_STATE
+    assert rsd(3, lg, 1, 4, slots) == M.MOE_ERR_INVALID
+    assert rsd(0, None, 1, 4, slots) == M.MOE_ERR_INVALID
+    assert rsd(0, lg, 1, 4, None) == M.MOE_ERR_INVALID
+    assert rsd(0, lg, 0, 4, slots) == M.MOE_ERR_INVALID
+    assert rsd(0, lg, 1, 0, slots) == M.MOE_ERR_INVALID
+    assert rsd(0, lg, 1, 33, slots) == M.MOE_ERR_INVALID
+    assert rsd(0, lg, 9, 4, slots) == M.MOE_ERR_UNSUPPORTED
+    assert L.moe_pool_route_stage_device(None, 0, lg, 1, 4, o32[0], wt, o32[1], o32[2], o32[3], o32[4], slots,
+                                         None, None, None) == M.MOE_ERR_INVALID
     assert L.moe_pool_device_join(pool.handle, 0, None) == M.MOE_ERR_STATE
     assert L.moe_pool_device_join(pool.handle, -1, None) == M.MOE_ERR_INVALID
     assert L.moe_pool_device_detach(pool.handle, None, 100) == M.MOE_ERR_STATE

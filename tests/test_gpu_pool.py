@@ -560,3 +560,105 @@ def test_device_planned_random_events_match_host_planning(policy):
                 assert torch.equal(got.cpu(), want)
     pool.close()
     ref.close()
+
+
+@pytest.mark.parametrize("policy,split", [("lru", True), ("slru", False)])
+def test_route_stage_device_matches_route_then_stage(policy, split):
+    """moe_pool_route_stage_device (routing and planning in one launch)
+    against moe_route_plan followed by moe_pool_stage_device on a second
+    pool over the same host store: per event the routing outputs (ids, w,
+    counts, offsets, perm, inv), the slot map and the split maps are
+    bit-exact; the staged slots and the layer outputs agree; after
+    detaching, counters, last loads and slot maps are equal and equal to
+    the oracle's policy simulation.  One step routes 8 tokens (32
+    assignments, the most one launch takes), whose event overflows the 8
+    slots in some layers: both pools then change nothing alike."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    L = 3
+    pool_a, host, dev_a = make_pool(M, wl, layers=L, preload=False)
+    pool_a.close()
+    dev_b = torch.empty_like(dev_a)
+    mk = lambda dev: M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev,
+                            policy=policy, stage_parts="decode")
+    pool_a, pool_b = mk(dev_a), mk(dev_b)
+    ref = [oracle.PolicyPool(wl.slots, wl.experts, policy) for _ in range(L)]
+    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    state_a = torch.zeros(pool_a.device_state_bytes(), dtype=torch.uint8, device="cuda")
+    state_b = torch.zeros_like(state_a)
+    with torch.cuda.stream(stream):
+        pool_a.device_attach(state_a, stream=stream)
+        pool_b.device_attach(state_b, stream=stream)
+        for step in range(6):
+            T = 8 if step == 3 else 1
+            plan_a = M.RoutePlan.allocate(T, E, k, counts_host=True)
+            plan_b = M.RoutePlan.allocate(T, E, k)
+            ws = M.alloc_ffn_workspace(T, k, H, I, M.MOE_PATH_DECODE)
+            slot_a = torch.empty(E, dtype=torch.int32, device="cuda")
+            slot_b = torch.empty_like(slot_a)
+            maps_a = torch.full((2, E), -7, dtype=torch.int32, device="cuda")
+            maps_b = torch.full((2, E), -7, dtype=torch.int32, device="cuda")
+            out_a = torch.empty((T, H), dtype=torch.float32, device="cuda")
+            out_b = torch.empty_like(out_a)
+            for layer in range(L):
+                lg = torch.from_numpy(S.logits(wl, layer, step, tokens=T)).cuda()
+                x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step, tokens=T).view(np.int16)).cuda().view(
+                    torch.bfloat16)
+                M.moe_route_plan(lg, k, plan_a, stream=stream)
+                cp = copy_stream if split else None
+                pool_a.stage_device(layer, plan_a.counts, slot_a, split_dev=maps_a if split else None,
+                                    stream=stream, copy=cp)
+                pool_b.route_stage_device(layer, lg, k, plan_b, slot_b, split_dev=maps_b if split else None,
+                                          stream=stream, copy=cp)
+                stream.synchronize()
+                copy_stream.synchronize()
+                for f in ("ids", "w", "counts", "offsets", "perm", "inv"):
+                    assert torch.equal(getattr(plan_a, f), getattr(plan_b, f)), f
+                assert torch.equal(slot_a, slot_b)
+                if split:
+                    assert torch.equal(maps_a, maps_b)
+                counts = plan_a.counts_host.numpy().copy()
+                ok = counts.astype(bool).sum() <= wl.slots
+                if ok:
+                    ref[layer].step(counts)
+                assert np.array_equal(slot_b.cpu().numpy(), ref[layer].slot_map())
+                if T == 1:
+                    for pool, dev, smap, out in ((pool_a, dev_a, slot_a, out_a), (pool_b, dev_b, slot_b, out_b)):
+                        if split:
+                            m = maps_a if pool is pool_a else maps_b
+                            M.moe_expert_ffn(pool, layer, x, plan_a, m[0], out, ws, path=M.MOE_PATH_DECODE,
+                                             stream=stream, skip_absent=True)
+                            pool.device_join(layer, stream=stream)
+                            M.moe_expert_ffn(pool, layer, x, plan_a, m[1], out, ws, path=M.MOE_PATH_DECODE,
+                                             stream=stream, skip_absent=True, accumulate=True)
+                        else:
+                            M.moe_expert_ffn(pool, layer, x, plan_a, smap, out, ws, path=M.MOE_PATH_DECODE,
+                                             stream=stream)
+                        stream.synchronize()
+                    r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                    assert rel_l2(out_a.cpu().numpy(), r) <= DECODE_REL_L2
+                    assert rel_l2(out_b.cpu().numpy(), out_a.cpu().numpy()) <= 1e-6
+        pool_a.device_join(L - 1, stream=stream)
+        ra = pool_a.device_detach(stream=stream)
+        rb = pool_b.device_detach(stream=stream)
+    assert ra == rb
+    eb = M.moe_expert_bytes(H, I)
+    for layer in range(L):
+        for s_ in pool_b.slot_map(layer):
+            if s_ >= 0:  # the staged parts of each resident expert, sampled at both ends
+                a0 = (layer * wl.slots + s_) * eb
+                assert torch.equal(dev_a[a0:a0 + 4096], dev_b[a0:a0 + 4096])
+                assert torch.equal(dev_a[a0 + eb - 4096:a0 + eb], dev_b[a0 + eb - 4096:a0 + eb])
+    for layer in range(L):
+        ca, cb, e = pool_a.counters(layer), pool_b.counters(layer), ref[layer].counters()
+        assert ca == cb
+        assert (ca["hits"], ca["misses"], ca["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+        assert pool_a.last_loads(layer) == pool_b.last_loads(layer)
+        assert np.array_equal(pool_a.slot_map(layer), pool_b.slot_map(layer))
+        assert np.array_equal(pool_b.slot_map(layer), ref[layer].slot_map())
+    pool_a.close()
+    pool_b.close()
