@@ -26,13 +26,14 @@
 //                       while the other warps load the record.
 //   pool_gather_kernel  one CTA of 64 threads per SM: 64 KB chunks of the
 //                       planned loads (both staged parts of each expert),
-//                       16-byte loads from host memory, eight in flight per
-//                       thread (≈ 1.2 MB in flight: the link, ≈ 0.2 TB/s,
-//                       stays the limit).  Small in registers so that an SM
-//                       holding two of them (the CTA scheduler does not
-//                       spread them one per SM) still takes a decode FFN
-//                       CTA: the FFN of a layer's hits runs beside the copy
-//                       (with 128-thread CTAs it waited for the copy to end).
+//                       16-byte loads from host memory, sixteen in flight
+//                       per thread (≈ 2.5 MB in flight: the link, ≈ 0.2
+//                       TB/s, stays the limit; eight gave 1 % less).  Small
+//                       CTAs so that the FFN of a layer's hits runs beside
+//                       the copy: an SM holding one of them (93 registers a
+//                       thread) still takes a decode FFN CTA (with 128-thread
+//                       CTAs the FFN waited for the copy to end; the CTA
+//                       scheduler does not spread them one per SM).
 #include <cstdint>
 
 #include "internal.h"
@@ -45,7 +46,7 @@ namespace {
 constexpr int kPlanThreads = 256;
 static_assert(kPlanThreads >= MOE_MAX_EXPERTS, "one thread per expert in the planner");
 constexpr int kGatherThreads = 64;
-constexpr int kGatherUnroll = 8;
+constexpr int kGatherUnroll = 16;
 constexpr unsigned long long kChunk = 64ull << 10;
 
 // The planner's shared-memory copy of a layer's record and the event.
