@@ -661,9 +661,10 @@ def offload_obj(args, wl, host):
                                 "host memory, per layer routing and the staging event planned on the GPU in one "
                                 "launch (moe_pool_route_stage_device), misses copied by the SMs from the mapped "
                                 "pinned expert "
-                                "store on a second stream while the FFN of the event's hits runs, then the FFN of "
-                                "the loaded experts added in, outputs back to pinned host memory; one CUDA graph "
-                                "per step (24 x (routing + plan, copy | hits' FFN, loads' FFN) plus the input and "
+                                "store on a second stream while the FFN of the event's hits runs, the FFN of the "
+                                "loaded experts on that stream right behind the copy, outputs back to pinned host "
+                                "memory; one CUDA graph "
+                                "per step (24 x (routing + plan, (copy, loads' FFN) | hits' FFN) plus the input and "
                                 "output copies), CUDA events"},
            "roofline": {"kernel": "miss staging: SM copy of packed experts out of mapped pinned host memory",
                         "bound": "host_link", "achieved": link, "peak": link_peak, "unit": "GB/s",
@@ -691,10 +692,11 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L, split=
     """The offload decode with device-planned staging: the pool's state in
     device memory; per layer routing + planning (one launch,
     moe_pool_route_stage_device), then the SM copy of the misses
-    on a second stream while the FFN of the event's hits runs, then (joined)
-    the FFN of the loaded experts added in; each step (with its input and
-    output copies) one CUDA graph.  Same events as the host-planned run
-    (same routing stream, same policy, a fresh pool)."""
+    on a second stream while the FFN of the event's hits runs, the FFN of
+    the loaded experts on that stream right behind the copy (both adding
+    into the zeroed output), and the compute stream joined to it; each step
+    (with its input and output copies) one CUDA graph.  Same events as the
+    host-planned run (same routing stream, same policy, a fresh pool)."""
     import torch
 
     import routed_expert_ffn_histogram_gb300 as M
@@ -714,20 +716,28 @@ def _offload_device_planned(args, wl, host, slots, lg_pin, x_pin, dev, L, split=
     plan = M.RoutePlan.allocate(1, E, k, device=dev)
     slot_of = torch.empty(E, dtype=torch.int32, device=dev)
     ws = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
+    ws_loads = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE, device=dev)
+    joined = [torch.cuda.Event() for _ in range(L)]
     pool.device_attach(state, stream=stream)
 
     def body(g):
         lg_d.copy_(lg_pin[g], non_blocking=True)
         x_d.copy_(x_pin[g], non_blocking=True)
+        if split:
+            out_d.zero_()
         for l in range(L):
             # routing and the staging event's planning in one launch
             if split:
                 pool.route_stage_device(l, lg_d[l], k, plan, slot_of, split_dev=maps, stream=stream, copy=copy)
+                # the hits' part beside the copy; the loads' part on the copy
+                # stream right behind it; both add into the zeroed output
                 M.moe_expert_ffn(pool, l, x_d[l], plan, maps[0], out_d[l], ws, path=M.MOE_PATH_DECODE,
-                                 stream=stream, skip_absent=True)
-                pool.device_join(l, stream=stream)
-                M.moe_expert_ffn(pool, l, x_d[l], plan, maps[1], out_d[l], ws, path=M.MOE_PATH_DECODE,
                                  stream=stream, skip_absent=True, accumulate=True)
+                M.moe_expert_ffn(pool, l, x_d[l], plan, maps[1], out_d[l], ws_loads, path=M.MOE_PATH_DECODE,
+                                 stream=copy, skip_absent=True, accumulate=True)
+                joined[l].record(copy)
+                stream.wait_event(joined[l])
+                pool.device_join(l, stream=stream)
             else:
                 pool.route_stage_device(l, lg_d[l], k, plan, slot_of, stream=stream)
                 M.moe_expert_ffn(pool, l, x_d[l], plan, slot_of, out_d[l], ws, path=M.MOE_PATH_DECODE,

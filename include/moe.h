@@ -389,7 +389,13 @@ MOE_API int moe_pool_prefetch(moe_pool_t* pool, int layer, int max_loads, moe_st
  *               MOE_FFN_SKIP_ABSENT: the hits' part on `compute` while the
  *               copies run, then moe_pool_device_join, then the loads' part
  *               with MOE_FFN_ACCUMULATE (tinyserve README, "How it works"
- *               item 4: H2D overlapped with compute).
+ *               item 4: H2D overlapped with compute).  Or the loads' part
+ *               on `copy` right behind the copy kernel (which is launched
+ *               with programmatic stream serialisation, so the FFN launches
+ *               while it runs and waits for it), both parts with
+ *               MOE_FFN_ACCUMULATE into a zeroed or residual `out` and with
+ *               workspaces of their own, and `compute` made to wait for
+ *               `copy` (an event) before `out` is read.
  *   An event with a negative count or more than S routed experts changes
  *   nothing (no copies; slot_of_dev gets the current map, row 0 of
  *   split_dev slot S -- out of range, so NaN -- for routed experts without

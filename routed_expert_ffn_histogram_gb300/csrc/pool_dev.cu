@@ -269,6 +269,12 @@ __global__ void __launch_bounds__(kGatherThreads) pool_gather_kernel(const uint8
                                                                      const uint8_t* host_layer, uint8_t* slots_layer,
                                                                      unsigned long long eb, unsigned long long len0,
                                                                      unsigned long long off1, unsigned long long len1) {
+    // launched with programmatic stream serialisation: the planned loads are
+    // read after the previous kernel in the stream has finished, and the
+    // next one (the loaded experts' FFN, when the caller puts it behind the
+    // copy) may launch and wait for this grid
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int n = *reinterpret_cast<const int32_t*>(rec + dr.n_copy);
     const int32_t* le = reinterpret_cast<const int32_t*>(rec + dr.le);
     const int32_t* ls = reinterpret_cast<const int32_t*>(rec + dr.ls);
@@ -382,8 +388,18 @@ int launch_pool_gather(const uint8_t* rec, int S, int E, const uint8_t* host_lay
                                           int(cudaSharedmemCarveoutMaxShared)));
         carveout_set.mark(di.device);
     }
-    pool_gather_kernel<<<di.sms, kGatherThreads, 0, s>>>(rec, dev_record(S, E), host_layer, slots_layer, eb,
-                                                             len0, off1, len1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(di.sms));
+    cfg.blockDim = dim3(unsigned(kGatherThreads));
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, pool_gather_kernel, rec, dev_record(S, E), host_layer, slots_layer,
+                                    (unsigned long long)eb, (unsigned long long)len0, (unsigned long long)off1,
+                                    (unsigned long long)len1));
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }

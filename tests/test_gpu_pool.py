@@ -662,3 +662,63 @@ def test_route_stage_device_matches_route_then_stage(policy, split):
         assert np.array_equal(pool_b.slot_map(layer), ref[layer].slot_map())
     pool_a.close()
     pool_b.close()
+
+
+def test_offload_loads_ffn_behind_the_copy():
+    """The loaded experts' FFN on the copy stream right behind the copy
+    kernel (launched programmatically after it), the hits' FFN beside the
+    copy on the compute stream, both adding into a zeroed output with
+    workspaces of their own, the compute stream joined to the copy stream
+    by an event: layer outputs match the oracle and the counters and slot
+    maps after detaching match the oracle's LRU."""
+    import torch
+
+    import routed_expert_ffn_histogram_gb300 as M
+
+    wl = S.WORKLOADS[2]
+    L = 3
+    pool, host, dev = make_pool(M, wl, layers=L, preload=False)
+    pool.close()
+    pool = M.Pool(L, wl.experts, wl.slots, wl.hidden, wl.inter, host_experts=host, dev_slots=dev,
+                  policy="lru", stage_parts="decode")
+    ref = [oracle.PolicyPool(wl.slots, wl.experts, "lru") for _ in range(L)]
+    E, k, H, I = wl.experts, wl.top_k, wl.hidden, wl.inter
+    plan = M.RoutePlan.allocate(1, E, k, counts_host=True)
+    slot_of = torch.empty(E, dtype=torch.int32, device="cuda")
+    maps = torch.empty((2, E), dtype=torch.int32, device="cuda")
+    ws_hits = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE)
+    ws_loads = M.alloc_ffn_workspace(1, k, H, I, M.MOE_PATH_DECODE)
+    out = torch.empty((1, H), dtype=torch.float32, device="cuda")
+    state = torch.zeros(pool.device_state_bytes(), dtype=torch.uint8, device="cuda")
+    stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    joined = torch.cuda.Event()
+    with torch.cuda.stream(stream):
+        pool.device_attach(state, stream=stream)
+        for step in range(8):
+            for layer in range(L):
+                lg = torch.from_numpy(S.logits(wl, layer, step)).cuda()
+                x = torch.from_numpy(S.activations_bf16_bits(wl, layer, step).view(np.int16)).cuda().view(
+                    torch.bfloat16)
+                out.zero_()
+                pool.route_stage_device(layer, lg, k, plan, slot_of, split_dev=maps, stream=stream,
+                                        copy=copy_stream)
+                M.moe_expert_ffn(pool, layer, x, plan, maps[0], out, ws_hits, path=M.MOE_PATH_DECODE,
+                                 stream=stream, skip_absent=True, accumulate=True)
+                M.moe_expert_ffn(pool, layer, x, plan, maps[1], out, ws_loads, path=M.MOE_PATH_DECODE,
+                                 stream=copy_stream, skip_absent=True, accumulate=True)
+                joined.record(copy_stream)
+                stream.wait_event(joined)
+                stream.synchronize()
+                counts = np.bincount(plan.ids.cpu().numpy().ravel(), minlength=E).astype(np.int32)
+                ref[layer].step(counts)
+                assert np.array_equal(slot_of.cpu().numpy(), ref[layer].slot_map())
+                if step in (0, 3, 7):
+                    r, _ = _oracle_layer(wl, layer, step, prefill=False)
+                    assert rel_l2(out.cpu().numpy(), r) <= DECODE_REL_L2
+        assert pool.device_detach(stream=stream) == M.MOE_OK
+    for layer in range(L):
+        c, e = pool.counters(layer), ref[layer].counters()
+        assert (c["hits"], c["misses"], c["evictions"]) == (e["hits"], e["misses"], e["evictions"])
+        assert np.array_equal(pool.slot_map(layer), ref[layer].slot_map())
+    assert pool.counters()["misses"] > 0
+    pool.close()
